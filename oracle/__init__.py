@@ -1,0 +1,139 @@
+"""fp64 CPU oracle for the Simple GLA mixer -- TEST INFRASTRUCTURE ONLY.
+
+The plain, slow, obviously-correct reference that the CUDA path is checked
+against.  Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU
+baseline leg may import it; the product package never does, and it shares no
+code with the CUDA library.
+
+The arithmetic lives in ``gla_oracle.c`` (token-by-token recurrence, hand-derived
+backward, decode step, decay schedule); this module only compiles it with gcc,
+loads it with ctypes and converts numpy arrays to contiguous float64.
+
+Source: "Beyond the KV cache: Training and serving i14's Laplace 3B linear
+attention model on AWS Trainium2 with native PyTorch", section "i14 and the
+Laplace 3B architecture" ("GLA mixer", "Decay schedule", "Decay schedule's
+reach") and section "Challenge 3" (backward through the sequential updates).
+
+Pins (tests/test_oracle_*.py): brute-force closed form, central finite
+differences, the printed decay values, the a=0 half-strength skip, the lambda=1
+reduction to causal linear attention, state-carry and init-zero invariants,
+decode/forward consistency and an independent chunked restatement.  Every
+function here is pinned; none is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gla_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_D = ctypes.POINTER(ctypes.c_double)
+_L = ctypes.c_long
+
+
+def build(force: bool = False, src: str = _SRC, out: str = _LIB_PATH) -> str:
+    """Compile the oracle into a shared library with gcc (IEEE fp64, no fast-math)."""
+    if force or not os.path.exists(out) or os.path.getmtime(out) < os.path.getmtime(src):
+        os.makedirs(os.path.dirname(out), exist_ok=True)
+        tmp = out + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+                               "-fno-fast-math", src, "-o", tmp, "-lm"])
+        os.replace(tmp, out)
+    return out
+
+
+def load(path: str | None = None):
+    """Load (building if needed) the oracle library; ``path`` selects another build."""
+    global _lib
+    if path is not None:
+        return _bind(ctypes.CDLL(path))
+    with _lock:
+        if _lib is None:
+            _lib = _bind(ctypes.CDLL(build()))
+    return _lib
+
+
+def _bind(lib):
+    lib.oracle_decay_schedule.argtypes = [ctypes.c_int, ctypes.c_double, ctypes.c_double, _D]
+    lib.oracle_decay_schedule.restype = None
+    lib.oracle_fwd.argtypes = [_D] * 8 + [_L] * 5 + [ctypes.c_int]
+    lib.oracle_fwd.restype = ctypes.c_int
+    lib.oracle_bwd.argtypes = [_D] * 13 + [_L] * 5 + [ctypes.c_int]
+    lib.oracle_bwd.restype = ctypes.c_int
+    lib.oracle_decode_step.argtypes = [_D] * 7 + [_L] * 5 + [ctypes.c_int]
+    lib.oracle_decode_step.restype = ctypes.c_int
+    return lib
+
+
+def _c(x):
+    return np.ascontiguousarray(x, dtype=np.float64)
+
+
+def _p(x):
+    return None if x is None else x.ctypes.data_as(_D)
+
+
+def decay_schedule(H: int, t_min: float = 1.0, t_max: float = 2048.0, lib=None) -> np.ndarray:
+    """gamma_h = ln(lambda_h), half-lives geometric from t_min to t_max (float64 [H])."""
+    lib = lib or load()
+    g = np.empty(H, np.float64)
+    lib.oracle_decay_schedule(int(H), float(t_min), float(t_max), _p(g))
+    return g
+
+
+def fwd(q, k, v, gamma, a, init_state=None, nthreads: int = 0, lib=None):
+    """Token-by-token forward.  q,k [B,T,H,dk]; v [B,T,H,dv]; returns (o, final_state)."""
+    lib = lib or load()
+    q, k, v, gamma, a = map(_c, (q, k, v, gamma, a))
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    init = None if init_state is None else _c(init_state)
+    o = np.empty((B, T, H, dv), np.float64)
+    fin = np.empty((B, H, dk, dv), np.float64)
+    rc = lib.oracle_fwd(_p(q), _p(k), _p(v), _p(gamma), _p(a), _p(init), _p(o), _p(fin),
+                        B, T, H, dk, dv, int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_fwd: bad sizes")
+    return o, fin
+
+
+def bwd(q, k, v, gamma, a, dO, init_state=None, d_final_state=None, nthreads: int = 0, lib=None):
+    """Hand-derived backward.  Returns dict dq, dk, dv, d_a [H,dk], d_init_state [B,H,dk,dv]."""
+    lib = lib or load()
+    q, k, v, gamma, a, dO = map(_c, (q, k, v, gamma, a, dO))
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    init = None if init_state is None else _c(init_state)
+    dfin = None if d_final_state is None else _c(d_final_state)
+    out = dict(dq=np.empty_like(q), dk=np.empty_like(k), dv=np.empty_like(v),
+               d_a=np.empty((H, dk), np.float64), d_init_state=np.empty((B, H, dk, dv), np.float64))
+    rc = lib.oracle_bwd(_p(q), _p(k), _p(v), _p(gamma), _p(a), _p(init), _p(dO), _p(dfin),
+                        _p(out["dq"]), _p(out["dk"]), _p(out["dv"]), _p(out["d_a"]),
+                        _p(out["d_init_state"]), B, T, H, dk, dv, int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_bwd: bad sizes")
+    return out
+
+
+def decode_step(state, q, k, v, gamma, a, nthreads: int = 0, lib=None):
+    """One decode token.  state [N,L,H,dk,dv]; q,k [N,L,H,dk]; v [N,L,H,dv]; a [L,H,dk].
+    Returns (o [N,L,H,dv], new_state); the input array is not modified."""
+    lib = lib or load()
+    st = np.array(state, dtype=np.float64, order="C", copy=True)
+    q, k, v, gamma, a = map(_c, (q, k, v, gamma, a))
+    N, L, H, dk, dv = st.shape
+    o = np.empty((N, L, H, dv), np.float64)
+    rc = lib.oracle_decode_step(_p(st), _p(q), _p(k), _p(v), _p(gamma), _p(a), _p(o),
+                                N, L, H, dk, dv, int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_decode_step: bad sizes")
+    return o, st
