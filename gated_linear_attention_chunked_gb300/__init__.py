@@ -1,0 +1,219 @@
+"""GB300 (sm_103a) Simple GLA mixer: Python binding of libgla.
+
+Argument marshalling only: every step of the method runs in the CUDA kernels behind the
+C ABI in include/gla.h.  PyTorch supplies device memory and the current CUDA stream.
+There is no CPU fallback: if libgla.so is missing or the tensors are not on a CUDA device,
+the calls raise.
+
+Functions (same names as the C ABI, without the ``gla_`` prefix):
+  decay_schedule(H, t_min, t_max)                     -> float32 [H] (host) log-decays
+  chunk_fwd(q, k, v, log_decay, aug_balance, ...)     -> (o, final_state)
+  chunk_bwd(q, k, v, log_decay, aug_balance, dO, ...) -> (dq, dk, dv, d_aug, d_init_state)
+  decode_step(state, q, k, v, log_decay, aug_balance) -> o  (state updated in place)
+  get_device_error(), set_wait_timeout_ns(ns), status_string(code)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import _build
+
+GLA_BF16, GLA_FP32, GLA_FP16 = 0, 1, 2
+STATUS = {0: "GLA_OK", 1: "GLA_ERR_INVALID_ARG", 2: "GLA_ERR_UNSUPPORTED",
+          3: "GLA_ERR_ALIGNMENT", 4: "GLA_ERR_CUDA", 5: "GLA_ERR_TIMEOUT", 6: "GLA_ERR_RANGE",
+          7: "GLA_ERR_WORKSPACE", 8: "GLA_ERR_LAYOUT"}
+DK, DV, CHUNK = 96, 192, 128
+
+_lib = None
+_lock = threading.Lock()
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_S = ctypes.c_size_t
+
+
+class GlaError(RuntimeError):
+    def __init__(self, call: str, code: int):
+        self.code = code
+        super().__init__(f"{call}: {STATUS.get(code, code)} ({status_string(code)})")
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load(path: str | None = None):
+    """Load libgla.so (built by ``_build.build()`` / ``__graft_entry__.build()``)."""
+    global _lib
+    with _lock:
+        if _lib is None or path is not None:
+            p = path or lib_path()
+            if not os.path.exists(p):
+                raise RuntimeError(f"libgla.so not built ({p}); run __graft_entry__.build()")
+            lib = ctypes.CDLL(p)
+            lib.gla_status_string.argtypes = [_I]
+            lib.gla_status_string.restype = ctypes.c_char_p
+            lib.gla_get_device_error.argtypes = []
+            lib.gla_get_device_error.restype = _I
+            lib.gla_set_wait_timeout_ns.argtypes = [ctypes.c_ulonglong]
+            lib.gla_set_wait_timeout_ns.restype = _I
+            lib.gla_decay_schedule.argtypes = [_I, ctypes.c_double, ctypes.c_double, _P]
+            lib.gla_decay_schedule.restype = _I
+            lib.gla_chunk_fwd_workspace_size.argtypes = [_I] * 6
+            lib.gla_chunk_fwd_workspace_size.restype = _S
+            lib.gla_chunk_fwd.argtypes = [_P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _S] + [_I] * 5 + [_P]
+            lib.gla_chunk_fwd.restype = _I
+            lib.gla_chunk_bwd_workspace_size.argtypes = [_I] * 6
+            lib.gla_chunk_bwd_workspace_size.restype = _S
+            lib.gla_chunk_bwd.argtypes = [_P] * 3 + [_I] + [_P] * 11 + [_S] + [_I] * 5 + [_P]
+            lib.gla_chunk_bwd.restype = _I
+            lib.gla_decode_step.argtypes = [_P] * 7 + [_I] * 5 + [_P]
+            lib.gla_decode_step.restype = _I
+            if path is not None:
+                return lib
+            _lib = lib
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return load().gla_status_string(int(code)).decode()
+
+
+def _check(call: str, rc: int):
+    if rc != 0:
+        raise GlaError(call, rc)
+
+
+# --------------------------------------------------------------------------- marshalling
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    m = {torch.bfloat16: GLA_BF16, torch.float32: GLA_FP32, torch.float16: GLA_FP16}
+    if t.dtype not in m:
+        raise TypeError(f"unsupported input dtype {t.dtype}")
+    return m[t.dtype]
+
+
+def _dev(t, name, dtype=None):
+    """Pointer of a contiguous CUDA tensor (None -> NULL)."""
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def decay_schedule(H: int, t_min: float = 1.0, t_max: float = 2048.0):
+    """Host float32 tensor [H] of log-decays gamma_h = -ln2 / T_h (gla_decay_schedule)."""
+    torch = _torch()
+    out = torch.empty(H, dtype=torch.float32)
+    _check("gla_decay_schedule", load().gla_decay_schedule(H, t_min, t_max, out.data_ptr()))
+    return out
+
+
+def chunk_fwd_workspace_size(B, T, H, in_dtype) -> int:
+    return load().gla_chunk_fwd_workspace_size(B, T, H, DK, DV, in_dtype)
+
+
+def chunk_bwd_workspace_size(B, T, H, in_dtype) -> int:
+    return load().gla_chunk_bwd_workspace_size(B, T, H, DK, DV, in_dtype)
+
+
+def _workspace(nbytes, device, workspace):
+    torch = _torch()
+    if nbytes == 0:
+        return None
+    if workspace is not None:
+        if workspace.numel() * workspace.element_size() < nbytes:
+            raise ValueError("workspace too small")
+        return workspace
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def chunk_fwd(q, k, v, log_decay, aug_balance, init_state=None, *, want_final_state=True,
+              out=None, final_state=None, workspace=None, stream=None):
+    """Chunked forward (gla_chunk_fwd).  q,k [B,T,H,96], v [B,T,H,192] (bf16/fp16/fp32);
+    log_decay [H], aug_balance [H,96], init_state [B,H,96,192] fp32 (optional).
+    Returns (o fp32 [B,T,H,192], final_state fp32 [B,H,96,192] or None)."""
+    torch = _torch()
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    code = _dtype_code(q)
+    if out is None:
+        out = torch.empty((B, T, H, dv), dtype=torch.float32, device=q.device)
+    if final_state is None and want_final_state:
+        final_state = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
+    ws = _workspace(load().gla_chunk_fwd_workspace_size(B, T, H, dk, dv, code), q.device, workspace)
+    rc = load().gla_chunk_fwd(
+        _dev(q, "q"), _dev(k, "k", q.dtype), _dev(v, "v", q.dtype), code,
+        _dev(log_decay, "log_decay", torch.float32), _dev(aug_balance, "aug_balance", torch.float32),
+        _dev(init_state, "init_state", torch.float32), _dev(out, "o", torch.float32),
+        _dev(final_state, "final_state", torch.float32), _dev(ws, "workspace"),
+        0 if ws is None else ws.numel() * ws.element_size(), B, T, H, dk, dv, _stream(stream))
+    _check("gla_chunk_fwd", rc)
+    return out, final_state
+
+
+def chunk_bwd(q, k, v, log_decay, aug_balance, dO, init_state=None, d_final_state=None, *,
+              want_d_init_state=True, workspace=None, stream=None):
+    """Chunked backward (gla_chunk_bwd).  Returns (dq, dk, dv, d_aug, d_init_state), fp32."""
+    torch = _torch()
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    code = _dtype_code(q)
+    f32 = dict(dtype=torch.float32, device=q.device)
+    dq = torch.empty((B, T, H, dk), **f32)
+    dk_ = torch.empty((B, T, H, dk), **f32)
+    dv_ = torch.empty((B, T, H, dv), **f32)
+    d_aug = torch.empty((H, dk), **f32)
+    dinit = torch.empty((B, H, dk, dv), **f32) if want_d_init_state else None
+    ws = _workspace(load().gla_chunk_bwd_workspace_size(B, T, H, dk, dv, code), q.device, workspace)
+    rc = load().gla_chunk_bwd(
+        _dev(q, "q"), _dev(k, "k", q.dtype), _dev(v, "v", q.dtype), code,
+        _dev(log_decay, "log_decay", torch.float32), _dev(aug_balance, "aug_balance", torch.float32),
+        _dev(init_state, "init_state", torch.float32), _dev(dO, "dO", q.dtype),
+        _dev(d_final_state, "d_final_state", torch.float32), _dev(dq, "dq"), _dev(dk_, "dk"),
+        _dev(dv_, "dv"), _dev(d_aug, "d_aug"), _dev(dinit, "d_init_state"), _dev(ws, "workspace"),
+        0 if ws is None else ws.numel() * ws.element_size(), B, T, H, dk, dv, _stream(stream))
+    _check("gla_chunk_bwd", rc)
+    return dq, dk_, dv_, d_aug, dinit
+
+
+def decode_step(state, q, k, v, log_decay, aug_balance, *, out=None, stream=None):
+    """One decode token (gla_decode_step).  state [N,L,H,96,192] fp32 is updated in place;
+    q,k [N,L,H,96], v [N,L,H,192] fp32; aug_balance [L,H,96].  Returns o [N,L,H,192]."""
+    torch = _torch()
+    N, L, H, dk, dv = state.shape
+    if out is None:
+        out = torch.empty((N, L, H, dv), dtype=torch.float32, device=state.device)
+    f = torch.float32
+    rc = load().gla_decode_step(
+        _dev(state, "state", f), _dev(q, "q", f), _dev(k, "k", f), _dev(v, "v", f),
+        _dev(log_decay, "log_decay", f), _dev(aug_balance, "aug_balance", f), _dev(out, "o", f),
+        N, L, H, dk, dv, _stream(stream))
+    _check("gla_decode_step", rc)
+    return out
+
+
+def get_device_error() -> int:
+    """Read and clear the device error word (synchronises the device).  0 = none."""
+    return load().gla_get_device_error()
+
+
+def set_wait_timeout_ns(ns: int) -> None:
+    _check("gla_set_wait_timeout_ns", load().gla_set_wait_timeout_ns(int(ns)))

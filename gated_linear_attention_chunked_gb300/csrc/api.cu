@@ -1,0 +1,206 @@
+// api.cu -- the C ABI declared in include/gla.h: argument checks, workspace layout, device
+// error word, and the launches on the caller's stream.  No device memory is allocated here.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+
+#include "gla.h"
+#include "kernels.h"
+
+namespace {
+
+__device__ int g_device_error = 0;
+std::atomic<unsigned long long> g_wait_ns{2000000000ull};
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
+size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+gla_status ctl_for_current_device(gla::DevCtl* ctl) {
+  if (cudaGetSymbolAddress(reinterpret_cast<void**>(&ctl->err), g_device_error) != cudaSuccess)
+    return GLA_ERR_CUDA;
+  ctl->wait_ns = g_wait_ns.load();
+  return GLA_OK;
+}
+
+bool valid_dtype(gla_dtype t) { return t == GLA_BF16 || t == GLA_FP16 || t == GLA_FP32; }
+
+// Common checks of the chunked calls.
+gla_status check_chunk_sizes(int B, int T, int H, int dk, int dv, gla_dtype t) {
+  if (B <= 0 || T <= 0 || H <= 0) return GLA_ERR_INVALID_ARG;
+  if (dk != gla::kDK || dv != gla::kDV || T % gla::kChunk != 0 || !valid_dtype(t))
+    return GLA_ERR_UNSUPPORTED;
+  if ((long long)B * T > (1ll << 31) - 1 || (long long)B * H > (1ll << 31) - 1)
+    return GLA_ERR_UNSUPPORTED;
+  return GLA_OK;
+}
+
+// fp32 inputs are narrowed to fp16 in the workspace: q, k [B,T,H,96], v (and dO) [B,T,H,192].
+size_t half_copy_bytes(int B, int T, int H, bool with_dO) {
+  const size_t tok = (size_t)B * T * H;
+  size_t s = 2 * round256(tok * gla::kDK * 2) + round256(tok * gla::kDV * 2);
+  if (with_dO) s += round256(tok * gla::kDV * 2);
+  return s;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* gla_status_string(gla_status s) {
+  switch (s) {
+    case GLA_OK: return "ok";
+    case GLA_ERR_INVALID_ARG: return "invalid argument";
+    case GLA_ERR_UNSUPPORTED: return "unsupported size or dtype";
+    case GLA_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+    case GLA_ERR_CUDA: return "CUDA error";
+    case GLA_ERR_TIMEOUT: return "device wait timed out";
+    case GLA_ERR_RANGE: return "operand outside the fp16 range";
+    case GLA_ERR_WORKSPACE: return "workspace missing or too small";
+    case GLA_ERR_LAYOUT: return "shared memory layout error";
+  }
+  return "unknown status";
+}
+
+gla_status gla_get_device_error(void) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return GLA_ERR_CUDA;
+  int v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof(int)) != cudaSuccess) return GLA_ERR_CUDA;
+  if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int)) != cudaSuccess) return GLA_ERR_CUDA;
+  switch (v) {
+    case gla::DEV_OK: return GLA_OK;
+    case gla::DEV_TIMEOUT: return GLA_ERR_TIMEOUT;
+    case gla::DEV_RANGE: return GLA_ERR_RANGE;
+    case gla::DEV_LAYOUT: return GLA_ERR_LAYOUT;
+  }
+  return GLA_ERR_CUDA;
+}
+
+gla_status gla_set_wait_timeout_ns(unsigned long long ns) {
+  g_wait_ns.store(ns ? ns : 2000000000ull);
+  return GLA_OK;
+}
+
+gla_status gla_decay_schedule(int H, double t_min, double t_max, float* log_decay) {
+  if (H <= 0 || !(t_min > 0) || !(t_max > 0) || !log_decay) return GLA_ERR_INVALID_ARG;
+  for (int h = 0; h < H; ++h) {
+    const double frac = H > 1 ? (double)h / (double)(H - 1) : 0.0;
+    const double half_life = t_min * std::pow(t_max / t_min, frac);
+    log_decay[h] = (float)(-std::log(2.0) / half_life);
+  }
+  return GLA_OK;
+}
+
+size_t gla_chunk_fwd_workspace_size(int B, int T, int H, int dk, int dv, gla_dtype in_dtype) {
+  if (check_chunk_sizes(B, T, H, dk, dv, in_dtype) != GLA_OK) return 0;
+  return in_dtype == GLA_FP32 ? half_copy_bytes(B, T, H, false) : 0;
+}
+
+gla_status gla_chunk_fwd(const void* q, const void* k, const void* v, gla_dtype in_dtype,
+                         const float* log_decay, const float* aug_balance,
+                         const float* init_state, float* o, float* final_state, void* workspace,
+                         size_t workspace_bytes, int B, int T, int H, int dk, int dv,
+                         cudaStream_t stream) {
+  gla_status st = check_chunk_sizes(B, T, H, dk, dv, in_dtype);
+  if (st != GLA_OK) return st;
+  if (!q || !k || !v || !log_decay || !aug_balance || !o) return GLA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(log_decay) ||
+      !aligned16(aug_balance) || !aligned16(init_state) || !aligned16(o) ||
+      !aligned16(final_state))
+    return GLA_ERR_ALIGNMENT;
+  const size_t need = gla_chunk_fwd_workspace_size(B, T, H, dk, dv, in_dtype);
+  if (need && (!workspace || workspace_bytes < need)) return GLA_ERR_WORKSPACE;
+  if (need && !aligned256(workspace)) return GLA_ERR_ALIGNMENT;
+  gla::DevCtl ctl;
+  if ((st = ctl_for_current_device(&ctl)) != GLA_OK) return st;
+
+  gla::FwdArgs a;
+  a.q = q; a.k = k; a.v = v; a.bf16 = in_dtype == GLA_BF16;
+  a.log_decay = log_decay; a.aug = aug_balance; a.init = init_state;
+  a.o = o; a.fin = final_state; a.B = B; a.T = T; a.H = H;
+  if (in_dtype == GLA_FP32) {
+    const size_t tok = (size_t)B * T * H;
+    uint8_t* w = static_cast<uint8_t*>(workspace);
+    void* hq = w;
+    void* hk = w + round256(tok * dk * 2);
+    void* hv = w + 2 * round256(tok * dk * 2);
+    if (gla::launch_to_half((const float*)q, hq, (long long)(tok * dk), ctl, stream) != cudaSuccess ||
+        gla::launch_to_half((const float*)k, hk, (long long)(tok * dk), ctl, stream) != cudaSuccess ||
+        gla::launch_to_half((const float*)v, hv, (long long)(tok * dv), ctl, stream) != cudaSuccess)
+      return GLA_ERR_CUDA;
+    a.q = hq; a.k = hk; a.v = hv; a.bf16 = false;
+  }
+  return gla::launch_chunk_fwd(a, ctl, stream) == cudaSuccess ? GLA_OK : GLA_ERR_CUDA;
+}
+
+size_t gla_chunk_bwd_workspace_size(int B, int T, int H, int dk, int dv, gla_dtype in_dtype) {
+  if (check_chunk_sizes(B, T, H, dk, dv, in_dtype) != GLA_OK) return 0;
+  size_t s = gla::chunk_bwd_workspace_bytes(B, T, H);
+  if (in_dtype == GLA_FP32) s += half_copy_bytes(B, T, H, true);
+  return s;
+}
+
+gla_status gla_chunk_bwd(const void* q, const void* k, const void* v, gla_dtype in_dtype,
+                         const float* log_decay, const float* aug_balance,
+                         const float* init_state, const void* dO, const float* d_final_state,
+                         float* dq, float* dk, float* dv, float* d_aug, float* d_init_state,
+                         void* workspace, size_t workspace_bytes, int B, int T, int H, int dk_,
+                         int dv_, cudaStream_t stream) {
+  gla_status st = check_chunk_sizes(B, T, H, dk_, dv_, in_dtype);
+  if (st != GLA_OK) return st;
+  if (!q || !k || !v || !log_decay || !aug_balance || !dO || !dq || !dk || !dv || !d_aug)
+    return GLA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(log_decay) ||
+      !aligned16(aug_balance) || !aligned16(init_state) || !aligned16(dO) ||
+      !aligned16(d_final_state) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
+      !aligned16(d_aug) || !aligned16(d_init_state))
+    return GLA_ERR_ALIGNMENT;
+  const size_t need = gla_chunk_bwd_workspace_size(B, T, H, dk_, dv_, in_dtype);
+  if (need && (!workspace || workspace_bytes < need)) return GLA_ERR_WORKSPACE;
+  if (need && !aligned256(workspace)) return GLA_ERR_ALIGNMENT;
+  gla::DevCtl ctl;
+  if ((st = ctl_for_current_device(&ctl)) != GLA_OK) return st;
+
+  gla::BwdArgs a;
+  a.q = q; a.k = k; a.v = v; a.dO = dO; a.bf16 = in_dtype == GLA_BF16;
+  a.log_decay = log_decay; a.aug = aug_balance; a.init = init_state; a.dfin = d_final_state;
+  a.dq = dq; a.dk = dk; a.dv = dv; a.d_aug = d_aug; a.dinit = d_init_state;
+  a.workspace = workspace; a.workspace_bytes = gla::chunk_bwd_workspace_bytes(B, T, H);
+  a.B = B; a.T = T; a.H = H;
+  if (in_dtype == GLA_FP32) {
+    const size_t tok = (size_t)B * T * H;
+    uint8_t* w = static_cast<uint8_t*>(workspace) + a.workspace_bytes;
+    void* hq = w;
+    void* hk = w + round256(tok * dk_ * 2);
+    void* hv = w + 2 * round256(tok * dk_ * 2);
+    void* hd = w + 2 * round256(tok * dk_ * 2) + round256(tok * dv_ * 2);
+    if (gla::launch_to_half((const float*)q, hq, (long long)(tok * dk_), ctl, stream) != cudaSuccess ||
+        gla::launch_to_half((const float*)k, hk, (long long)(tok * dk_), ctl, stream) != cudaSuccess ||
+        gla::launch_to_half((const float*)v, hv, (long long)(tok * dv_), ctl, stream) != cudaSuccess ||
+        gla::launch_to_half((const float*)dO, hd, (long long)(tok * dv_), ctl, stream) != cudaSuccess)
+      return GLA_ERR_CUDA;
+    a.q = hq; a.k = hk; a.v = hv; a.dO = hd; a.bf16 = false;
+  }
+  return gla::launch_chunk_bwd(a, ctl, stream) == cudaSuccess ? GLA_OK : GLA_ERR_CUDA;
+}
+
+gla_status gla_decode_step(float* state, const float* q, const float* k, const float* v,
+                           const float* log_decay, const float* aug_balance, float* o, int N,
+                           int L, int H, int dk, int dv, cudaStream_t stream) {
+  if (N <= 0 || L <= 0 || H <= 0) return GLA_ERR_INVALID_ARG;
+  if (dk != gla::kDK || dv != gla::kDV) return GLA_ERR_UNSUPPORTED;
+  if (!state || !q || !k || !v || !log_decay || !aug_balance || !o) return GLA_ERR_INVALID_ARG;
+  if (!aligned16(state) || !aligned16(q) || !aligned16(k) || !aligned16(v) ||
+      !aligned16(log_decay) || !aligned16(aug_balance) || !aligned16(o))
+    return GLA_ERR_ALIGNMENT;
+  const long long n = (long long)N * L * H;
+  if (n > (1ll << 31) - 1) return GLA_ERR_UNSUPPORTED;
+  return gla::launch_decode(state, q, k, v, log_decay, aug_balance, o, n, L, H, stream) ==
+                 cudaSuccess
+             ? GLA_OK
+             : GLA_ERR_CUDA;
+}
+
+}  // extern "C"

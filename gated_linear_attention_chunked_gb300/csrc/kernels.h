@@ -1,0 +1,58 @@
+// kernels.h -- internal launch interface between the C ABI (api.cu) and the kernels.
+#pragma once
+#include <cuda_runtime_api.h>
+
+#include <cstddef>
+
+#include "ptx.cuh"
+
+namespace gla {
+
+constexpr int kDK = 96, kDV = 192, kChunk = 128;
+
+cudaError_t launch_decode(float* state, const float* q, const float* k, const float* v,
+                          const float* log_decay, const float* aug, float* o, long long n_states,
+                          int L, int H, cudaStream_t stream);
+
+// fp32 -> fp16 copy (for GLA_FP32 inputs); values with |x| >= 65504 record DEV_RANGE.
+cudaError_t launch_to_half(const float* src, void* dst, long long n, DevCtl ctl,
+                           cudaStream_t stream);
+
+struct FwdArgs {
+  const void* q;  // [B,T,H,96] 16-bit
+  const void* k;
+  const void* v;  // [B,T,H,192] 16-bit
+  bool bf16;      // element type of q,k,v: bf16 (true) or fp16 (false)
+  const float* log_decay;  // [H]
+  const float* aug;        // [H,96]
+  const float* init;       // [B,H,96,192] or null
+  float* o;                // [B,T,H,192]
+  float* fin;              // [B,H,96,192] or null
+  int B, T, H;
+};
+// Returns cudaErrorInvalidValue if a tensor map cannot be encoded.
+cudaError_t launch_chunk_fwd(const FwdArgs& a, DevCtl ctl, cudaStream_t stream);
+
+struct BwdArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* dO;  // [B,T,H,192] 16-bit
+  bool bf16;
+  const float* log_decay;
+  const float* aug;
+  const float* init;
+  const float* dfin;
+  float* dq;
+  float* dk;
+  float* dv;
+  float* d_aug;
+  float* dinit;
+  void* workspace;
+  size_t workspace_bytes;
+  int B, T, H;
+};
+size_t chunk_bwd_workspace_bytes(int B, int T, int H);
+cudaError_t launch_chunk_bwd(const BwdArgs& a, DevCtl ctl, cudaStream_t stream);
+
+}  // namespace gla

@@ -1,0 +1,171 @@
+/*
+ * gla.h -- C ABI of libgla, the GB300 (sm_103a) Simple GLA mixer library.
+ *
+ * The method is the "Simple GLA" token mixer of the Laplace 3B linear-attention
+ * model, as described in "Beyond the KV cache: Training and serving i14's
+ * Laplace 3B linear attention model on AWS Trainium2 with native PyTorch":
+ *   section "i14 and the Laplace 3B architecture", paragraph "GLA mixer":
+ *     S_t = lambda_h S_{t-1} + k_t v_t^T     (per-head 96x192 matrix state)
+ *     o_t = S_t^T q_t + sigmoid(sum_c a_{h,c} q_{t,c} k_{t,c}) v_t
+ *   paragraph "Decay schedule": lambda_h fixed, half-lives geometric from
+ *     T_min to T_max (lambda_0 = 0.5, lambda_15 ~ 0.9997 for 1..2048);
+ *   section "Challenge 1": the chunked parallel form (intra-chunk masked
+ *     attention, inter-chunk running state, state advanced by the decay
+ *     compounded over the chunk), chunk C = 128;
+ *   section "Challenge 3": the backward through the sequential updates;
+ *   section "Inference optimization on Trainium2": one fixed recurrent state
+ *     per sequence, updated one token at a time while serving.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Ownership: the caller owns every buffer.  Tensor arguments are DEVICE
+ *    pointers unless a comment says "host".  The library allocates no device
+ *    memory; scratch comes from the caller's `workspace`.
+ *  - Streams: calls enqueue work on `stream` (NULL = legacy default stream)
+ *    and return without synchronising.
+ *  - Errors: argument errors are returned before anything is launched, as
+ *    GLA_ERR_INVALID_ARG / GLA_ERR_UNSUPPORTED / GLA_ERR_ALIGNMENT /
+ *    GLA_ERR_WORKSPACE.  A failed launch returns GLA_ERR_CUDA.  Errors found
+ *    on the device while a kernel runs (a bounded wait that gave up, an fp16
+ *    operand out of range) are recorded in a device error word that
+ *    gla_get_device_error() reads and clears.
+ *  - Layout: token-major and contiguous.  q, k: [B, T, H, dk]; v, o, dO:
+ *    [B, T, H, dv]; states: [B, H, dk, dv] (row i = key channel, column n =
+ *    value channel); aug_balance: [H, dk]; log_decay: [H].
+ *  - Supported sizes: dk = 96, dv = 192 (the model's head sizes); T a
+ *    multiple of the chunk size 128 for the chunked calls; B, T, H > 0.
+ *  - Alignment: every tensor pointer must be 16-byte aligned.
+ *  - Decay: log_decay[h] = gamma_h = ln(lambda_h) (natural log, < 0 for a
+ *    decaying head).  The decay is fixed, so there is no gradient for it.
+ *  - No internal scaling: q is used as given (callers pre-scale it).
+ */
+#ifndef GLA_H
+#define GLA_H
+
+#include <stddef.h>
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define GLA_API __attribute__((visibility("default")))
+#else
+#define GLA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  GLA_OK = 0,
+  GLA_ERR_INVALID_ARG = 1, /* null pointer where one is required, size <= 0 */
+  GLA_ERR_UNSUPPORTED = 2, /* dk != 96, dv != 192, T % 128 != 0, unknown dtype */
+  GLA_ERR_ALIGNMENT = 3,   /* a tensor pointer is not 16-byte aligned */
+  GLA_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed */
+  GLA_ERR_TIMEOUT = 5,     /* device: a bounded wait inside a kernel gave up */
+  GLA_ERR_RANGE = 6,       /* device: an operand or state left the fp16 range */
+  GLA_ERR_WORKSPACE = 7,   /* workspace missing or smaller than required */
+  GLA_ERR_LAYOUT = 8       /* device: shared memory not aligned as required */
+} gla_status;
+
+/* Element type of the q, k, v, dO inputs.  Outputs and states are fp32. */
+typedef enum {
+  GLA_BF16 = 0, /* bfloat16 */
+  GLA_FP32 = 1, /* float32: converted to fp16 on the device (|x| < 65504) */
+  GLA_FP16 = 2  /* IEEE half */
+} gla_dtype;
+
+/* Human-readable name of a status code (static string). */
+GLA_API const char* gla_status_string(gla_status s);
+
+/* Reads the device error word of the current device and clears it.  Blocks
+ * until all work on the device has finished (it synchronises the device).
+ * Returns GLA_OK, GLA_ERR_TIMEOUT, GLA_ERR_RANGE or GLA_ERR_LAYOUT, or
+ * GLA_ERR_CUDA if the device cannot be queried. */
+GLA_API gla_status gla_get_device_error(void);
+
+/* Wall-clock limit, in nanoseconds, of every bounded wait inside the chunk
+ * kernels (default 2e9).  A wait that runs out records GLA_ERR_TIMEOUT and
+ * the kernel finishes early without touching memory outside its tensors.
+ * Applies to calls made after it returns.  ns == 0 restores the default. */
+GLA_API gla_status gla_set_wait_timeout_ns(unsigned long long ns);
+
+/* Decay schedule ("Decay schedule" paragraph): half-lives
+ *   T_h = t_min * (t_max / t_min)^(h / (H - 1))   (T_0 = t_min if H == 1)
+ * and log_decay[h] = ln(2^(-1/T_h)) = -ln(2) / T_h, computed in double and
+ * stored as float.  log_decay is a HOST array of H floats.
+ * Errors: GLA_ERR_INVALID_ARG if H <= 0, t_min <= 0, t_max <= 0 or
+ * log_decay is NULL. */
+GLA_API gla_status gla_decay_schedule(int H, double t_min, double t_max, float* log_decay);
+
+/* ---------------------------------------------------------------------------
+ * Chunked forward ("Challenge 1" chunked form of the "GLA mixer" recurrence).
+ *
+ *   o[b,t,h,:]          = S_t^T q_t + sigmoid(q_t . (a_h * k_t)) v_t
+ *   final_state[b,h]    = S_T
+ * with S_0 = init_state[b,h] (zeros if init_state is NULL).
+ *
+ *   q, k         [B,T,H,96]  in_dtype        v [B,T,H,192] in_dtype
+ *   log_decay    [H] fp32 (device)           aug_balance [H,96] fp32 (device)
+ *   init_state   [B,H,96,192] fp32 or NULL   (read only)
+ *   o            [B,T,H,192] fp32 (written)
+ *   final_state  [B,H,96,192] fp32 or NULL   (written)
+ *   workspace    device scratch of at least gla_chunk_fwd_workspace_size()
+ *                bytes (may be NULL when that size is 0), 256-byte aligned.
+ * Arithmetic: the tensor cores take fp16 operands with fp32 accumulation; the
+ * state is carried in fp32 across chunks.  Inputs must satisfy |x| < 65504.
+ */
+GLA_API size_t gla_chunk_fwd_workspace_size(int B, int T, int H, int dk, int dv, gla_dtype in_dtype);
+GLA_API gla_status gla_chunk_fwd(const void* q, const void* k, const void* v, gla_dtype in_dtype,
+                         const float* log_decay, const float* aug_balance,
+                         const float* init_state, float* o, float* final_state, void* workspace,
+                         size_t workspace_bytes, int B, int T, int H, int dk, int dv,
+                         cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Chunked backward ("Challenge 3": the gradient through every sequential
+ * state update), for the scalar loss  L = sum o.dO + <d_final_state, S_T>:
+ *
+ *   dq_t = S_t dO_t + r_t (a*k_t)        dk_t = G_t v_t + r_t (a*q_t)
+ *   dv_t = G_t^T k_t + sigmoid(z_t) dO_t
+ *   d_aug[h] = sum_{b,t} r_t (q_t * k_t)  d_init_state = lambda G_1
+ * where G_t = q_t dO_t^T + lambda G_{t+1}, G_T = q_T dO_T^T + d_final_state,
+ * z_t = q_t.(a*k_t), r_t = sigmoid'(z_t) (dO_t . v_t).
+ *
+ *   q, k, v, in_dtype, log_decay, aug_balance, init_state: as in the forward
+ *   dO            [B,T,H,192] in_dtype
+ *   d_final_state [B,H,96,192] fp32 or NULL (= zeros)
+ *   dq, dk        [B,T,H,96]  fp32 (written)    dv [B,T,H,192] fp32 (written)
+ *   d_aug         [H,96] fp32 (written, summed over B and T)
+ *   d_init_state  [B,H,96,192] fp32 or NULL (written)
+ *   workspace     at least gla_chunk_bwd_workspace_size() bytes, 256-aligned
+ */
+GLA_API size_t gla_chunk_bwd_workspace_size(int B, int T, int H, int dk, int dv, gla_dtype in_dtype);
+GLA_API gla_status gla_chunk_bwd(const void* q, const void* k, const void* v, gla_dtype in_dtype,
+                         const float* log_decay, const float* aug_balance,
+                         const float* init_state, const void* dO, const float* d_final_state,
+                         float* dq, float* dk, float* dv, float* d_aug, float* d_init_state,
+                         void* workspace, size_t workspace_bytes, int B, int T, int H,
+                         int dk_, int dv_, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * One recurrent decode step for a pool of N sequences x L layers x H heads
+ * ("Inference optimization on Trainium2": a fixed state per sequence, read
+ * and written in the serving pool, O(1) per token).  In place, fp32:
+ *
+ *   S'  = lambda_h S + k v^T
+ *   o   = S'^T q + sigmoid(q . (a_{l,h} * k)) v
+ *
+ *   state        [N,L,H,96,192] fp32, read and overwritten with S'
+ *   q, k         [N,L,H,96] fp32     v [N,L,H,192] fp32
+ *   log_decay    [H] fp32            aug_balance [L,H,96] fp32
+ *   o            [N,L,H,192] fp32 (written)
+ * N*L*H may be any positive count; nothing is allocated.
+ */
+GLA_API gla_status gla_decode_step(float* state, const float* q, const float* k, const float* v,
+                           const float* log_decay, const float* aug_balance, float* o, int N,
+                           int L, int H, int dk, int dv, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GLA_H */

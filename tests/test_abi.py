@@ -1,0 +1,116 @@
+"""The C ABI without a GPU: the library loads, exports every declared symbol, and rejects
+bad arguments with its documented status codes before touching the device."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import gated_linear_attention_chunked_gb300 as gla
+from gated_linear_attention_chunked_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return gla.load()
+
+
+def declared_symbols():
+    txt = open(os.path.join(ROOT, "include", "gla.h")).read()
+    return sorted(set(re.findall(r"GLA_API\s+[\w\s\*]+?\b(gla_\w+)\s*\(", txt)))
+
+
+def test_header_declares_the_calls():
+    names = declared_symbols()
+    for n in ("gla_chunk_fwd", "gla_chunk_bwd", "gla_decode_step", "gla_decay_schedule",
+              "gla_get_device_error", "gla_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    raw = ctypes.CDLL(gla.lib_path())
+    for n in declared_symbols():
+        assert hasattr(raw, n), f"{n} not exported"
+
+
+def test_status_strings(lib):
+    for code in gla.STATUS:
+        assert gla.status_string(code)
+    assert gla.status_string(0) == "ok"
+
+
+def test_decay_schedule_matches_oracle(lib):
+    import oracle
+    for H, tmin, tmax in [(16, 1.0, 2048.0), (2, 1.0, 2048.0), (1, 4.0, 4.0), (7, 2.0, 300.0)]:
+        g = gla.decay_schedule(H, tmin, tmax).numpy()
+        ref = oracle.decay_schedule(H, tmin, tmax)
+        # same fp64 formula on both sides, rounded once to fp32
+        assert np.array_equal(g, ref.astype(np.float32))
+    g = gla.decay_schedule(16).numpy().astype(np.float64)
+    assert np.exp(g[0]) == pytest.approx(0.5, rel=1e-7)
+    assert np.exp(g[15]) == pytest.approx(2 ** (-1 / 2048), rel=1e-7)
+
+
+def test_decay_schedule_rejects(lib):
+    out = (ctypes.c_float * 4)()
+    assert lib.gla_decay_schedule(0, 1.0, 2.0, ctypes.addressof(out)) == 1
+    assert lib.gla_decay_schedule(4, 0.0, 2.0, ctypes.addressof(out)) == 1
+    assert lib.gla_decay_schedule(4, 1.0, 2.0, None) == 1
+
+
+A16 = 0x1000  # a 16-byte aligned fake address; never dereferenced by the checks below
+
+
+def fwd(lib, q=A16, k=A16, v=A16, dt=0, ld=A16, a=A16, init=None, o=A16, fin=None, ws=None,
+        wsb=0, B=1, T=128, H=1, dk=96, dv=192):
+    return lib.gla_chunk_fwd(q, k, v, dt, ld, a, init, o, fin, ws, wsb, B, T, H, dk, dv, None)
+
+
+def test_chunk_fwd_argument_checks(lib):
+    assert fwd(lib, dk=64) == 2                      # unsupported head size
+    assert fwd(lib, dv=128) == 2
+    assert fwd(lib, T=200) == 2                      # not a multiple of the chunk
+    assert fwd(lib, dt=7) == 2                       # unknown dtype
+    assert fwd(lib, B=0) == 1 and fwd(lib, T=0) == 1 and fwd(lib, H=-1) == 1
+    assert fwd(lib, q=None) == 1 and fwd(lib, o=None) == 1 and fwd(lib, a=None) == 1
+    assert fwd(lib, q=A16 + 8) == 3                  # misaligned
+    assert fwd(lib, init=A16 + 4) == 3
+    # fp32 inputs need a workspace for their fp16 copies
+    assert gla.chunk_fwd_workspace_size(1, 128, 1, gla.GLA_FP32) > 0
+    assert gla.chunk_fwd_workspace_size(1, 128, 1, gla.GLA_BF16) == 0
+    assert fwd(lib, dt=1) == 7
+    need = gla.chunk_fwd_workspace_size(1, 128, 1, gla.GLA_FP32)
+    assert fwd(lib, dt=1, ws=A16, wsb=need - 1) == 7
+    assert fwd(lib, dt=1, ws=A16 + 16, wsb=need) == 3  # workspace must be 256-aligned
+
+
+def test_chunk_bwd_argument_checks(lib):
+    def bwd(dO=A16, dq=A16, dk_=64, T=128, d_aug=A16):
+        return lib.gla_chunk_bwd(A16, A16, A16, 0, A16, A16, None, dO, None, dq, A16, A16, d_aug,
+                                 None, None, 0, 1, T, 1, dk_, 192, None)
+    assert bwd() == 2
+    assert bwd(dk_=96, T=100) == 2
+    assert bwd(dk_=96, dO=None) == 1
+    assert bwd(dk_=96, d_aug=None) == 1
+    assert bwd(dk_=96, dq=A16 + 2) == 3
+
+
+def test_decode_argument_checks(lib):
+    def dec(st=A16, N=1, L=1, H=1, dk=96, dv=192, o=A16):
+        return lib.gla_decode_step(st, A16, A16, A16, A16, A16, o, N, L, H, dk, dv, None)
+    assert dec(N=0) == 1 and dec(L=0) == 1
+    assert dec(dk=64) == 2 and dec(dv=96) == 2
+    assert dec(st=None) == 1 and dec(o=None) == 1
+    assert dec(st=A16 + 4) == 3
+
+
+def test_binding_refuses_host_tensors(lib):
+    torch = pytest.importorskip("torch")
+    q = torch.zeros(1, 128, 1, 96, dtype=torch.bfloat16)
+    v = torch.zeros(1, 128, 1, 192, dtype=torch.bfloat16)
+    with pytest.raises((ValueError, RuntimeError, AssertionError)):
+        gla.chunk_fwd(q, q, v, torch.zeros(1), torch.zeros(1, 96))

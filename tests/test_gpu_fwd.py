@@ -1,0 +1,125 @@
+"""GPU parity of gla_chunk_fwd against the fp64 oracle (bar: 2e-2 of the output RMS)."""
+import numpy as np
+import pytest
+
+import synth
+from _util import TOL_CHUNK, as_dtype_values, rel_err, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def env():
+    import torch
+    assert torch.cuda.is_available(), "GPU test without a CUDA device"
+    import gated_linear_attention_chunked_gb300 as gla
+    from gated_linear_attention_chunked_gb300 import _build
+    _build.build()
+    gla.load()
+    return gla, torch
+
+
+TDT = {"bf16": "bfloat16", "fp16": "float16", "fp32": "float32"}
+
+
+def run_fwd(env, q, k, v, a, init, H, dtype):
+    import oracle
+    gla, torch = env
+    td = getattr(torch, TDT[dtype])
+    q, k, v = (as_dtype_values(x, dtype) for x in (q, k, v))
+    gam = gla.decay_schedule(H)
+    gam64 = oracle.decay_schedule(H).astype(np.float32).astype(np.float64)
+    init_d = None if init is None else to_dev(init, torch.float32)
+    o, fin = gla.chunk_fwd(to_dev(q, td), to_dev(k, td), to_dev(v, td), gam.cuda(),
+                           to_dev(a, torch.float32), init_d)
+    torch.cuda.synchronize()
+    assert gla.get_device_error() == 0
+    return o.cpu().numpy(), fin.cpu().numpy(), (q, k, v, gam64)
+
+
+CASES = [
+    # B, T, H, dtype, init std, a std, seed
+    (1, 128, 1, "bf16", 0.0, 0.1, 11),     # one chunk, one head
+    (2, 384, 5, "bf16", 0.05, 0.1, 12),    # odd head count, 3 chunks, initial state
+    (1, 256, 2, "fp16", 0.05, 0.1, 13),
+    (1, 256, 2, "fp32", 0.0, 0.1, 0),      # the tiny fp32 workload shape
+    (3, 640, 16, "bf16", 0.02, 0.02, 14),  # all 16 decay tiers, 5 chunks
+]
+
+
+@pytest.mark.parametrize("B,T,H,dtype,init_std,a_std,seed", CASES)
+def test_fwd_small(env, B, T, H, dtype, init_std, a_std, seed):
+    import oracle
+    q, k, v = synth.qkv(seed, B, T, H, bf16=False)
+    a = synth.aug_balance(seed, (H, 96), a_std)
+    init = synth.init_state(seed, B, H, init_std) if init_std > 0 else None
+    o, fin, (q, k, v, gam64) = run_fwd(env, q, k, v, a, init, H, dtype)
+    o_ref, fin_ref = oracle.fwd(q, k, v, gam64, a, init)
+    eo, ef = rel_err(o, o_ref), rel_err(fin, fin_ref)
+    print(f"fwd B={B} T={T} H={H} {dtype}: o {eo:.2e} final {ef:.2e}")
+    assert eo <= TOL_CHUNK and ef <= TOL_CHUNK
+
+
+def test_fwd_tiny_fp32_workload(env):
+    import oracle
+    x = synth.chunk_inputs("tiny_fp32")
+    c = x["cfg"]
+    o, fin, (q, k, v, gam64) = run_fwd(env, x["q"], x["k"], x["v"], x["a"], None, c["H"], "fp32")
+    o_ref, fin_ref = oracle.fwd(q, k, v, gam64, x["a"])
+    eo, ef = rel_err(o, o_ref), rel_err(fin, fin_ref)
+    print(f"fwd tiny fp32: o {eo:.2e} final {ef:.2e}")
+    assert eo <= TOL_CHUNK and ef <= TOL_CHUNK
+
+
+@pytest.mark.parametrize("name", ["layer_fwd", "layer_fwd_aug"])
+def test_fwd_layer_workload(env, name):
+    """One training-shape layer, B=8, T=2048, H=16, bf16; a = 0 and a ~ N(0, 0.02)."""
+    import oracle
+    x = synth.chunk_inputs(name)
+    c = x["cfg"]
+    o, fin, (q, k, v, gam64) = run_fwd(env, x["q"], x["k"], x["v"], x["a"], None, c["H"], "bf16")
+    o_ref, fin_ref = oracle.fwd(q, k, v, gam64, x["a"])
+    eo, ef = rel_err(o, o_ref), rel_err(fin, fin_ref)
+    print(f"fwd {name}: o {eo:.2e} final {ef:.2e}")
+    assert eo <= TOL_CHUNK and ef <= TOL_CHUNK
+
+
+def test_fwd_zero_init_equals_no_init(env):
+    gla, torch = env
+    B, T, H = 2, 256, 3
+    q, k, v = synth.qkv(21, B, T, H)
+    a = synth.aug_balance(21, (H, 96), 0.1)
+    o1, f1, _ = run_fwd(env, q, k, v, a, None, H, "bf16")
+    o2, f2, _ = run_fwd(env, q, k, v, a, np.zeros((B, H, 96, 192), np.float32), H, "bf16")
+    assert np.array_equal(o1, o2) and np.array_equal(f1, f2)
+
+
+def test_fwd_state_carry(env):
+    """fwd over T tokens equals fwd over the second part started from the first part's
+    final state (the chunk boundary is a multiple of 128)."""
+    B, T, H, T1 = 2, 512, 4, 256
+    q, k, v = synth.qkv(22, B, T, H)
+    a = synth.aug_balance(22, (H, 96), 0.1)
+    o, fin, _ = run_fwd(env, q, k, v, a, None, H, "bf16")
+    o1, f1, _ = run_fwd(env, q[:, :T1], k[:, :T1], v[:, :T1], a, None, H, "bf16")
+    o2, f2, _ = run_fwd(env, q[:, T1:], k[:, T1:], v[:, T1:], a, f1, H, "bf16")
+    assert rel_err(np.concatenate([o1, o2], 1), o) <= 1e-6
+    assert rel_err(f2, fin) <= 1e-6
+
+
+def test_fwd_long_prefill_workload(env):
+    """Long-context prefill: B=2, T=131072, H=16, bf16, initial state ~ N(0, 0.01).
+    Checked on the first and last 4,096 outputs and on the full final state."""
+    import oracle
+    x = synth.chunk_inputs("long_prefill")
+    c = x["cfg"]
+    o, fin, (q, k, v, gam64) = run_fwd(env, x["q"], x["k"], x["v"], x["a"], x["init_state"],
+                                       c["H"], "bf16")
+    o_ref, fin_ref = oracle.fwd(q, k, v, gam64, x["a"], x["init_state"])
+    n = 4096
+    e_first = rel_err(o[:, :n], o_ref[:, :n])
+    e_last = rel_err(o[:, -n:], o_ref[:, -n:])
+    ef = rel_err(fin, fin_ref)
+    print(f"fwd long: first {e_first:.2e} last {e_last:.2e} final {ef:.2e}")
+    assert e_first <= TOL_CHUNK and e_last <= TOL_CHUNK and ef <= TOL_CHUNK
+    assert np.all(np.isfinite(o))
