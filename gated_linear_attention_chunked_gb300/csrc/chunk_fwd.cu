@@ -3,23 +3,26 @@
 // Method ("Beyond the KV cache ... Laplace 3B ...", section "Challenge 1", the chunked form
 // of the "GLA mixer" recurrence).  Per (b, h) and chunk c of C = 128 tokens, with
 // D_ij = lambda^(i-j) (i >= j, else 0), Lq = diag(lambda^(i+1)), Lk = diag(lambda^(C-1-j)):
-//   O_c     = (Q K^T o D) V + Lq Q S_c  + sigmoid(z) v      (intra + inter + self-augmentation)
-//   S_{c+1} = lambda^C S_c + K^T Lk V                         (the only serial step)
+//   O_c     = (Q K^T o D) V + Lq Q S_c + sigmoid(z) v       (intra + inter + self-augmentation)
+//   S_{c+1} = lambda^C S_c + K^T Lk V                        (the only serial step)
 //
 // One CTA owns one (b, h) and walks its chunks in order; the fp32 state never leaves the chip.
-//   warp 4      TMA producer: q, k tiles (3 boxes of 32 channels, 64-byte swizzle) and v tiles
-//               (3 boxes of 64 channels, 128-byte swizzle) into a 2-stage ring.
-//   warp 5      tcgen05 issuer (one thread) and TMEM owner (512 columns):
-//                 D_P [cols 384,512)  P = Q K^T                  (bf16/fp16 inputs as given)
-//                 D_O [cols   0,192)  O = Q'' S_c + P'' V          (fp16 operands)
-//                 D_S [cols 192,384)  S = lambda^C S + K'^T V      (fp16 operands, fp32 state;
-//                                    rows 96..127 are padding and never read)
-//   warps 0..3  epilogue, thread = token row (= TMEM lane):
-//                 (a) z = q.(a*k); Q'' = fp16(lambda^(i+1) q), K' = fp16(lambda^(127-i) k),
-//                     V -> fp16 in place; P'' = fp16(mask(P) * 2^-e) into shared memory;
-//                 (b) o = 2^e D_O + sigmoid(z) v, stored as fp32;
-//                 (c) S -> fp16(S * 2^-e') into the drained q/k slot (B operand of the next
-//                     Q'' S), and D_S <- lambda^C D_S ready for the next accumulation.
+//   warp 12     TMA producer: q, k tiles (3 boxes of 32 channels, 64-byte swizzle) and v tiles
+//               (3 boxes of 64 channels, 128-byte swizzle) into a 2-stage ring, plus L2
+//               prefetch of the chunk after next.
+//   warp 13     tcgen05 issuer (one thread) and TMEM owner (512 columns):
+//                 D_P [384,512)  P = Q K^T                   (bf16/fp16 inputs as given)
+//                 D_O [  0,192)  O = Q'' S_c + P'' V           (fp16 operands)
+//                 D_S [192,384)  S = lambda^C S + K'^T V       (fp16 operands, fp32 state;
+//                                rows 96..127 are padding and never read)
+//   warps 0..3  convert group, thread = token row i (= TMEM lane), one chunk ahead of the
+//               emit group: V -> fp16 in place; z = q.(a*k); Q'' = fp16(lambda^(i+1) q) and
+//               K' = fp16(lambda^(127-i) k) in place; P'' = fp16(mask(P) * 2^-e).
+//   warps 4..11 emit group, same rows, two warps per row quadrant splitting the value
+//               columns: (1) the serial step -- S -> fp16(S * 2^-e') into the drained q/k
+//               slot (B operand of the next Q'' S) and D_S <- lambda^C D_S; (2) o = 2^e D_O +
+//               sigmoid(z) v as fp32, TMA-stored from staging in the chunk's v tile (no
+//               longer read by then).
 // fp16 operands (11-bit significand) keep the long-memory heads accurate; the state copy is
 // scaled by a power of two e' chosen from max|S| so it never overflows fp16.
 #include <cuda_bf16.h>
@@ -27,29 +30,38 @@
 #include <cuda_runtime.h>
 
 #include "kernels.h"
+#include "scan_common.cuh"
 #include "tmap.h"
 
 namespace gla {
 namespace {
 
-constexpr int C = kChunk, DK = kDK, DV = kDV;
+using namespace scan;
+
 constexpr uint32_t Q_BOX = 8192;    // 128 rows x 64 B (32 channels), SW64
 constexpr uint32_t V_BOX = 16384;   // 128 rows x 128 B (64 channels), SW128
 constexpr uint32_t OFF_Q = 0, OFF_K = 3 * Q_BOX, OFF_V = 6 * Q_BOX;
 constexpr uint32_t STAGE = OFF_V + 3 * V_BOX;  // 98304
-constexpr uint32_t OFF_P = 2 * STAGE;          // 196608: P'' 2 atoms x 16 KB (K-major SW128)
+constexpr uint32_t OFF_P = 2 * STAGE;          // P'' 2 atoms x 16 KB (K-major SW128)
 constexpr uint32_t P_ATOM = 16384;
-constexpr uint32_t S_ATOM = 12288;             // S copy: 3 atoms of 96 rows x 128 B (MN-major)
-constexpr uint32_t OFF_BAR = OFF_P + 2 * P_ATOM;  // 229376
-constexpr uint32_t OFF_TMEM = OFF_BAR + 16 * 8;
+constexpr uint32_t S_ATOM = 12288;             // state copy: 3 atoms of 96 rows x 128 B
+constexpr uint32_t OFF_BAR = OFF_P + 2 * P_ATOM;
+constexpr uint32_t NBAR = 24;
+constexpr uint32_t OFF_TMEM = OFF_BAR + NBAR * 8;
 constexpr uint32_t OFF_ABORT = OFF_TMEM + 4;
-constexpr uint32_t OFF_RED = OFF_TMEM + 16;     // float red[2][4]
-constexpr uint32_t OFF_PW = OFF_BAR + 256;      // float pw[128]
-constexpr uint32_t OFF_A = OFF_PW + 512;        // float a[96]
-constexpr uint32_t SMEM_USED = OFF_A + 384;
-constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // + alignment slack
-static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-static_assert(3 * S_ATOM <= 2 * 3 * Q_BOX, "state copy fits in a drained q/k slot");
+constexpr uint32_t OFF_RED = OFF_TMEM + 16;     // float red[3][8]: per-warp max|S|
+constexpr uint32_t OFF_ES = OFF_RED + 96;       // int es[2]: state-copy exponent per chunk parity
+constexpr uint32_t OFF_KV = OFF_ES + 16;        // float kvmax[2][8]: per-warp max|K'|, max|V|
+constexpr uint32_t OFF_ZS = OFF_KV + 64;        // float zs[2][128]: gate dot products
+constexpr uint32_t OFF_A = OFF_ZS + 1024;       // float a[96]: aug_balance of the head
+constexpr uint32_t OFF_PW = OFF_A + 384;        // float pw[128] = lambda^d
+constexpr uint32_t SMEM_USED = OFF_PW + 512;
+// The whole opt-in maximum is requested; the kernel aligns its base to 1024 bytes and
+// refuses to run (GLA_ERR_LAYOUT, before touching shared memory) if the padding that
+// takes would not fit.  The dynamic shared window normally starts 1024-aligned.
+constexpr uint32_t SMEM_BYTES = 232448;
+static_assert(SMEM_USED <= SMEM_BYTES, "shared memory budget");
+static_assert(3 * S_ATOM <= 6 * Q_BOX, "state copy fits in a drained q/k slot");
 
 constexpr uint32_t QK_BYTES = 6 * Q_BOX, V_BYTES = 3 * V_BOX;
 constexpr uint32_t TM_O = 0, TM_S = 192, TM_P = 384;
@@ -66,130 +78,115 @@ enum Bar : uint32_t {
   EP_O = 12,
   EP_S = 13,
   DRAIN = 14,
-  RED = 15,      // exchange of the per-warp max|S| (bounded wait, unlike bar.sync)
+  RED = 15,  // exchange of the per-warp max|S| inside the emit group
 };
 
-constexpr int THREADS = 192;
-constexpr uint64_t DRAIN_NS = 4000000000ull;
-
-struct Smem {
-  uint8_t* base;
-  uint32_t sb;
-  __device__ uint32_t bar(uint32_t i) const { return sb + OFF_BAR + 8 * i; }
-  __device__ volatile int* abort_flag() const { return (volatile int*)(base + OFF_ABORT); }
-};
-
-// Bounded wait that also gives up as soon as another role has aborted.
-__device__ __forceinline__ bool wait_or_abort(const Smem& sm, uint32_t bar, uint32_t parity,
-                                              const DevCtl& ctl) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 31u) == 0) {
-      if (*sm.abort_flag()) return false;
-      if (globaltimer() - t0 > ctl.wait_ns) {
-        record_error(ctl, DEV_TIMEOUT);
-        *sm.abort_flag() = 1;
-        return false;
-      }
-    }
-  }
-}
-
-template <bool BF16>
-__device__ __forceinline__ float ld16(uint16_t bits) {
-  if constexpr (BF16) return __uint_as_float((uint32_t)bits << 16);
-  else return __half2float(__ushort_as_half(bits));
-}
-__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
-  __half2 h = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&h);
-}
-__device__ __forceinline__ float h2lo(uint32_t u) { return __half2float(__ushort_as_half((uint16_t)(u & 0xFFFF))); }
-__device__ __forceinline__ float h2hi(uint32_t u) { return __half2float(__ushort_as_half((uint16_t)(u >> 16))); }
-__device__ __forceinline__ float pow2i(int e) { return __int_as_float((127 + e) << 23); }  // |e| < 127
+constexpr int THREADS = 448;
+constexpr int PRODUCER_WARP = 12, MMA_WARP = 13;
+constexpr int EMIT_THREADS = 256;  // warps 4..11
 
 template <bool BF16>
 __global__ void __launch_bounds__(THREADS, 1)
 fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
-           const __grid_constant__ CUtensorMap map_v, const float* __restrict__ log_decay,
+           const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o,
+           const __grid_constant__ CUtensorMap map_fin, const float* __restrict__ log_decay,
            const float* __restrict__ aug, const float* __restrict__ init, float* __restrict__ out,
            float* __restrict__ fin, int T, int H, DevCtl ctl) {
-  extern __shared__ uint8_t smem_raw[];
-  Smem sm;
-  sm.base = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  sm.sb = smem_u32(sm.base);
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  Cta cta;
+  cta.base = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  if ((uint32_t)(cta.base - smem_raw) + SMEM_USED > SMEM_BYTES) {
+    if (threadIdx.x == 0) record_error(ctl, DEV_LAYOUT);
+    return;
+  }
+  cta.sb = smem_u32(cta.base);
+  cta.bar_off = OFF_BAR;
+  cta.abort_off = OFF_ABORT;
+  uint8_t* const base = cta.base;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int bh = blockIdx.x, b = bh / H, h = bh % H;
   const int nc = T / C;
   const float gamma = __ldg(log_decay + h);
-  float* pw = (float*)(sm.base + OFF_PW);
-  float* sa = (float*)(sm.base + OFF_A);
-  float* red = (float*)(sm.base + OFF_RED);
-  uint32_t* tmem_slot = (uint32_t*)(sm.base + OFF_TMEM);
+  float* pw = (float*)(base + OFF_PW);
+  float* red = (float*)(base + OFF_RED);
+  int* es = (int*)(base + OFF_ES);
+  float* kvmax = (float*)(base + OFF_KV);
+  float* zs = (float*)(base + OFF_ZS);
+  float* sa = (float*)(base + OFF_A);
+  uint32_t* tmem_slot = (uint32_t*)(base + OFF_TMEM);
 
-  if (warp == 5) {
+  if (warp == MMA_WARP) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
-  if (tid == 128) {
+  if (tid == PRODUCER_WARP * 32) {
     for (uint32_t s = 0; s < 2; ++s) {
-      mbar_init(sm.bar(QK_FULL + s), 1);
-      mbar_init(sm.bar(V_FULL + s), 1);
-      mbar_init(sm.bar(QK_EMPTY + s), 1);
-      mbar_init(sm.bar(V_EMPTY + s), 1 + 128);
+      mbar_init(cta.bar(QK_FULL + s), 1);
+      mbar_init(cta.bar(V_FULL + s), 1);
+      mbar_init(cta.bar(QK_EMPTY + s), 1);
+      mbar_init(cta.bar(V_EMPTY + s), 1 + EMIT_THREADS);
     }
-    mbar_init(sm.bar(P_DONE), 1);
-    mbar_init(sm.bar(O_DONE), 1);
-    mbar_init(sm.bar(S_DONE), 1);
-    mbar_init(sm.bar(DRAIN), 1);
-    mbar_init(sm.bar(EP_CONV), 128);
-    mbar_init(sm.bar(EP_O), 128);
-    mbar_init(sm.bar(EP_S), 128);
-    mbar_init(sm.bar(RED), 128);
-    *sm.abort_flag() = 0;
+    mbar_init(cta.bar(P_DONE), 1);
+    mbar_init(cta.bar(O_DONE), 1);
+    mbar_init(cta.bar(S_DONE), 1);
+    mbar_init(cta.bar(DRAIN), 1);
+    mbar_init(cta.bar(EP_CONV), 128);           // convert group
+    mbar_init(cta.bar(EP_O), EMIT_THREADS);     // emit group
+    mbar_init(cta.bar(EP_S), EMIT_THREADS);     // emit group
+    mbar_init(cta.bar(RED), EMIT_THREADS);      // emit group
+    *cta.abort_flag() = 0;
     fence_barrier_init();
   }
   if (tid < C) pw[tid] = expf((float)tid * gamma);  // lambda^d, d = 0..127
   if (tid < DK) sa[tid] = __ldg(aug + h * DK + tid);
-  if ((sm.sb & 1023u) != 0) record_error(ctl, DEV_LAYOUT);  // cannot happen: base aligned above
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 4) {
+  if (warp == PRODUCER_WARP) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
       prefetch_tensormap(&map_q);
       prefetch_tensormap(&map_k);
       prefetch_tensormap(&map_v);
+      prefetch_tensormap(&map_o);
       const int row0 = b * T;
+      auto prefetch_chunk = [&](int c) {
+        if (c >= nc) return;
+        const int row = row0 + c * C;
+        for (int j = 0; j < 3; ++j) {
+          tma_prefetch_3d(&map_v, 64 * j, h, row);
+          tma_prefetch_3d(&map_q, 32 * j, h, row);
+          tma_prefetch_3d(&map_k, 32 * j, h, row);
+        }
+      };
+      prefetch_chunk(1);
       int armed_qk[2] = {0, 0}, armed_v[2] = {0, 0};
       for (int c = 0; c < nc; ++c) {
-        const uint32_t s = c & 1, st = sm.sb + s * STAGE;
+        const uint32_t s = c & 1, st = cta.sb + s * STAGE;
         const int row = row0 + c * C;
-        if (c >= 2 && !wait_or_abort(sm, sm.bar(V_EMPTY + s), ((c >> 1) - 1) & 1, ctl)) break;
-        mbar_arrive_expect_tx(sm.bar(V_FULL + s), V_BYTES);
+        if (c >= 2 && !wait(cta, cta.bar(V_EMPTY + s), ((c >> 1) - 1) & 1, ctl)) break;
+        mbar_arrive_expect_tx(cta.bar(V_FULL + s), V_BYTES);
         for (int j = 0; j < 3; ++j)
-          tma_load_3d(st + OFF_V + j * V_BOX, &map_v, sm.bar(V_FULL + s), 64 * j, h, row);
+          tma_load_3d(st + OFF_V + j * V_BOX, &map_v, cta.bar(V_FULL + s), 64 * j, h, row);
         ++armed_v[s];
-        if (c >= 1 && !wait_or_abort(sm, sm.bar(QK_EMPTY + s), ((c - 1) >> 1) & 1, ctl)) break;
-        mbar_arrive_expect_tx(sm.bar(QK_FULL + s), QK_BYTES);
+        prefetch_chunk(c + 2);
+        if (c >= 1 && !wait(cta, cta.bar(QK_EMPTY + s), ((c - 1) >> 1) & 1, ctl)) break;
+        mbar_arrive_expect_tx(cta.bar(QK_FULL + s), QK_BYTES);
         for (int j = 0; j < 3; ++j) {
-          tma_load_3d(st + OFF_Q + j * Q_BOX, &map_q, sm.bar(QK_FULL + s), 32 * j, h, row);
-          tma_load_3d(st + OFF_K + j * Q_BOX, &map_k, sm.bar(QK_FULL + s), 32 * j, h, row);
+          tma_load_3d(st + OFF_Q + j * Q_BOX, &map_q, cta.bar(QK_FULL + s), 32 * j, h, row);
+          tma_load_3d(st + OFF_K + j * Q_BOX, &map_k, cta.bar(QK_FULL + s), 32 * j, h, row);
         }
         ++armed_qk[s];
       }
       // drain: every armed load has landed before the CTA may exit
       for (int s = 0; s < 2; ++s) {
-        if (armed_v[s]) mbar_wait(sm.bar(V_FULL + s), (armed_v[s] - 1) & 1, ctl, DRAIN_NS);
-        if (armed_qk[s]) mbar_wait(sm.bar(QK_FULL + s), (armed_qk[s] - 1) & 1, ctl, DRAIN_NS);
+        if (armed_v[s]) mbar_wait(cta.bar(V_FULL + s), (armed_v[s] - 1) & 1, ctl, DRAIN_NS);
+        if (armed_qk[s]) mbar_wait(cta.bar(QK_FULL + s), (armed_qk[s] - 1) & 1, ctl, DRAIN_NS);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == MMA_WARP) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t ID_QK = idesc_f16(128, 128, BF16, BF16, false, false);
@@ -197,20 +194,20 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
       constexpr uint32_t ID_PV = idesc_f16(128, 192, false, false, false, true);
       constexpr uint32_t ID_KV = idesc_f16(128, 192, false, false, true, true);
       for (int c = 0; c < nc; ++c) {
-        const uint32_t s = c & 1, st = sm.sb + s * STAGE;
-        const uint32_t slot = sm.sb + (s ^ 1) * STAGE;  // state copy for this chunk
-        if (!wait_or_abort(sm, sm.bar(QK_FULL + s), (c >> 1) & 1, ctl)) break;
+        const uint32_t s = c & 1, st = cta.sb + s * STAGE;
+        const uint32_t slot = cta.sb + (s ^ 1) * STAGE;  // state copy for this chunk
+        if (!wait(cta, cta.bar(QK_FULL + s), (c >> 1) & 1, ctl)) break;
         tc_fence_after();
 #pragma unroll
-        for (int ks = 0; ks < 6; ++ks) {
+        for (int ks = 0; ks < 6; ++ks) {  // P = Q K^T
           const uint32_t off = (ks >> 1) * Q_BOX + (ks & 1) * 32;
           mma_f16_ss(tmem + TM_P, smem_desc(st + OFF_Q + off, 16, 512, SW_64),
                      smem_desc(st + OFF_K + off, 16, 512, SW_64), ID_QK, ks > 0);
         }
-        mma_commit(sm.bar(P_DONE));
-        if (!wait_or_abort(sm, sm.bar(EP_CONV), c & 1, ctl)) break;
-        if (!wait_or_abort(sm, sm.bar(EP_S), c & 1, ctl)) break;
-        if (c >= 1 && !wait_or_abort(sm, sm.bar(EP_O), (c - 1) & 1, ctl)) break;
+        mma_commit(cta.bar(P_DONE));
+        if (!wait(cta, cta.bar(EP_CONV), c & 1, ctl)) break;
+        if (!wait(cta, cta.bar(EP_S), c & 1, ctl)) break;
+        if (c >= 1 && !wait(cta, cta.bar(EP_O), (c - 1) & 1, ctl)) break;
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 6; ++ks) {  // O = Q'' S
@@ -221,252 +218,313 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {  // O += P'' V
           mma_f16_ss(tmem + TM_O,
-                     smem_desc(sm.sb + OFF_P + (ks >> 2) * P_ATOM + (ks & 3) * 32, 16, 1024, SW_128),
+                     smem_desc(cta.sb + OFF_P + (ks >> 2) * P_ATOM + (ks & 3) * 32, 16, 1024, SW_128),
                      smem_desc(st + OFF_V + ks * 2048, V_BOX, 1024, SW_128), ID_PV, 1);
         }
-        mma_commit(sm.bar(O_DONE));
-        mma_commit(sm.bar(QK_EMPTY + (s ^ 1)));
+        mma_commit(cta.bar(O_DONE));
+        mma_commit(cta.bar(QK_EMPTY + (s ^ 1)));
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {  // S += K'^T V
           mma_f16_ss(tmem + TM_S, smem_desc(st + OFF_K + ks * 1024, Q_BOX, 512, SW_64),
                      smem_desc(st + OFF_V + ks * 2048, V_BOX, 1024, SW_128), ID_KV, 1);
         }
-        mma_commit(sm.bar(S_DONE));
-        mma_commit(sm.bar(V_EMPTY + s));
+        mma_commit(cta.bar(S_DONE));
+        mma_commit(cta.bar(V_EMPTY + s));
       }
-      mma_commit(sm.bar(DRAIN));
-      mbar_wait(sm.bar(DRAIN), 0, ctl, DRAIN_NS);
+      mma_commit(cta.bar(DRAIN));
+      mbar_wait(cta.bar(DRAIN), 0, ctl, DRAIN_NS);
     }
-  } else {
-    // ------------------------------------------------------------------ epilogue, row i
-    const int i = tid;
-    const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
-    const float lamC = expf((float)C * gamma);
+  } else if (warp < 4) {
+    // ------------------------------------------------------------------ convert group
+    // Row i of chunk c: gate dot product, in-place fp16 operands, masked scores.
+    const int i = tid;  // token row == TMEM lane (warp w serves lanes 32w..32w+31)
+    const uint32_t trow = tmem + ((uint32_t)(32 * warp) << 16);
+    const float lam = pw[1], lamC = expf((float)C * gamma);
     const float lq = (i + 1 < C) ? pw[i + 1] : lamC;  // lambda^(i+1)
     const float lk = pw[C - 1 - i];                   // lambda^(C-1-i)
-    bool range_bad = false;
-    int e_cur = 0;
-
-    // Make a scaled fp16 copy of the state rows in the q/k slot at `slot_off`, and set
-    // D_S <- lambda^C S.  Row i of S (fp32) comes from TMEM or from init_state (`g_row`,
-    // null = zeros).  `use` counts the calls (parity of the RED exchange).  Returns the
-    // power-of-two exponent e of the copy (copy = S * 2^-e), or -1 if it gave up waiting.
-    auto publish_state = [&](uint32_t slot_off, int use, const float* g_row, bool from_tmem) {
-      const int par = use & 1;
-      float m = 0.f;
-      uint32_t r[32];
-      if (warp < 3) {
-        for (int nb = 0; nb < 6; ++nb) {
-          if (from_tmem) {
-            tmem_ld32(trow + TM_S + nb * 32, r);
-            tmem_wait_ld();
-          } else {
-            for (int j = 0; j < 32; ++j)
-              r[j] = __float_as_uint(g_row ? __ldg(g_row + nb * 32 + j) : 0.f);
-          }
-          for (int j = 0; j < 32; ++j) m = fmaxf(m, fabsf(__uint_as_float(r[j])));
+    float range_max = 0.f;
+    for (int c = 0; c < nc; ++c) {
+      const uint32_t s = c & 1, par = c & 1;
+      uint8_t* stg = base + s * STAGE;
+      float vmax = 0.f, kmax = 0.f, qmax = 0.f;
+      if (!wait(cta, cta.bar(V_FULL + s), (c >> 1) & 1, ctl)) break;
+      if constexpr (BF16) {  // v -> fp16 in place (exact for |v| in the fp16 normal range)
+#pragma unroll 4
+        for (int cc = 0; cc < 24; ++cc)
+          scale_chunk_to_half<true>(
+              (uint4*)(stg + OFF_V + (cc >> 3) * V_BOX + swz_off(i, cc & 7, 128)), 1.f, vmax);
+      } else {
+#pragma unroll 4
+        for (int cc = 0; cc < 24; ++cc) {
+          const uint4 x = *(const uint4*)(stg + OFF_V + (cc >> 3) * V_BOX + swz_off(i, cc & 7, 128));
+          const uint32_t* w = (const uint32_t*)&x;
+#pragma unroll
+          for (int e2 = 0; e2 < 4; ++e2) vmax = fmaxf(vmax, fmaxf(fabsf(h_lo(w[e2])), fabsf(h_hi(w[e2]))));
         }
       }
+      if (!wait(cta, cta.bar(P_DONE), par, ctl)) break;
+      if (!wait(cta, cta.bar(QK_FULL + s), (c >> 1) & 1, ctl)) break;
+      tc_fence_after();
+      float z = 0.f;
+#pragma unroll 2
+      for (int cc = 0; cc < 12; ++cc) {  // channels 8cc..8cc+7
+        const uint32_t off = (cc >> 2) * Q_BOX + swz_off(i, cc & 3, 64);
+        uint4 qv = *(uint4*)(stg + OFF_Q + off);
+        uint4 kv = *(uint4*)(stg + OFF_K + off);
+        uint32_t* qw = (uint32_t*)&qv;
+        uint32_t* kw = (uint32_t*)&kv;
+        const float4 a0 = *reinterpret_cast<const float4*>(sa + 8 * cc);
+        const float4 a1 = *reinterpret_cast<const float4*>(sa + 8 * cc + 4);
+        const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-      if (lane == 0) red[par * 4 + warp] = m;
-      mbar_arrive(sm.bar(RED));
-      if (!wait_or_abort(sm, sm.bar(RED), par, ctl)) return -1;
-      m = fmaxf(fmaxf(red[par * 4 + 0], red[par * 4 + 1]), fmaxf(red[par * 4 + 2], red[par * 4 + 3]));
-      int e = 0;
-      if (!(m <= 3.0e38f)) {  // inf or nan in the state
-        range_bad = true;
-      } else if (m > 0.f) {
-        int ex;
-        frexpf(m, &ex);
-        e = ex > 14 ? ex - 14 : 0;
+        for (int e2 = 0; e2 < 4; ++e2) {
+          const float q0 = ld16<BF16>(qw[e2] & 0xFFFFu), q1 = ld16<BF16>(qw[e2] >> 16);
+          const float k0 = ld16<BF16>(kw[e2] & 0xFFFFu), k1 = ld16<BF16>(kw[e2] >> 16);
+          z = fmaf(av[2 * e2] * q0, k0, z);
+          z = fmaf(av[2 * e2 + 1] * q1, k1, z);
+          const float x0 = q0 * lq, x1 = q1 * lq, y0 = k0 * lk, y1 = k1 * lk;
+          qmax = fmaxf(qmax, fmaxf(fabsf(x0), fabsf(x1)));
+          kmax = fmaxf(kmax, fmaxf(fabsf(y0), fabsf(y1)));
+          qw[e2] = pack_h2(x0, x1);
+          kw[e2] = pack_h2(y0, y1);
+        }
+        *(uint4*)(stg + OFF_Q + off) = qv;
+        *(uint4*)(stg + OFF_K + off) = kv;
       }
-      if (warp < 3) {
+      zs[par * 128 + i] = z;
+      // chunk maxima of |K'| and |V| (for the emit group's bound on the next state)
+      {
+        float km = kmax, vm = vmax;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+          km = fmaxf(km, __shfl_xor_sync(0xffffffffu, km, off));
+          vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, off));
+        }
+        if (lane == 0) {
+          kvmax[par * 8 + warp] = km;
+          kvmax[par * 8 + 4 + warp] = vm;
+        }
+      }
+      // the state exponent of this chunk (and P'' of the previous chunk consumed)
+      if (!wait(cta, cta.bar(EP_S), par, ctl)) break;
+      const float psc = pow2i(-es[par]);
+      float pmax = 0.f;
+      {
+        uint32_t r[32];
+#pragma unroll 1
+        for (int jb = 0; jb < 4; ++jb) {
+          const int j0 = 32 * jb;
+          float p[32];
+          if (jb <= warp) {  // block touches columns j <= i for this warp's rows
+            tmem_ld32(trow + TM_P + j0, r);
+            tmem_wait_ld();
+            // lambda^(i-j) by repeated multiplication going left from j = min(i, j0+31)
+            float f = pw[max(i - (j0 + 31), 0)] * psc;
+#pragma unroll
+            for (int u = 31; u >= 0; --u) {
+              const bool in = j0 + u <= i;
+              p[u] = in ? __uint_as_float(r[u]) * f : 0.f;
+              f = in ? f * lam : f;
+              pmax = fmaxf(pmax, fabsf(p[u]));
+            }
+          } else {
+#pragma unroll
+            for (int u = 0; u < 32; ++u) p[u] = 0.f;
+          }
+#pragma unroll
+          for (int q8 = 0; q8 < 4; ++q8) {
+            uint4 pk;
+            pk.x = pack_h2(p[8 * q8 + 0], p[8 * q8 + 1]);
+            pk.y = pack_h2(p[8 * q8 + 2], p[8 * q8 + 3]);
+            pk.z = pack_h2(p[8 * q8 + 4], p[8 * q8 + 5]);
+            pk.w = pack_h2(p[8 * q8 + 6], p[8 * q8 + 7]);
+            *(uint4*)(base + OFF_P + (jb >> 1) * P_ATOM + swz_off(i, 4 * (jb & 1) + q8, 128)) = pk;
+          }
+        }
+      }
+      range_max = fmaxf(range_max, fmaxf(fmaxf(vmax, kmax), fmaxf(qmax, pmax)));
+      fence_proxy_async();
+      tc_fence_before();
+      mbar_arrive(cta.bar(EP_CONV));
+    }
+    if (range_max >= 65504.f) record_error(ctl, DEV_RANGE);
+  } else if (warp < PRODUCER_WARP) {
+    // ------------------------------------------------------------------ emit group
+    // Warp w serves rows 32(w&3)..+31 and value columns [96hf, 96hf+96), hf = (w-4)>>2.
+    // State copy for the next chunk (the serial chain, first), then the output rows.
+    const int q4 = warp & 3, hf = (warp - 4) >> 2, ew = warp - 4;
+    const int i = 32 * q4 + lane;
+    const uint32_t trow = tmem + ((uint32_t)(32 * q4) << 16);
+    const float lamC = expf((float)C * gamma);
+    bool bad = false;
+
+    // fp16 copy S * 2^-e of this warp's state rows / column half into the q/k slot at
+    // `slot_off`, D_S <- lambda^C S, and the warp's max|S| into red[use & 1].  Row i comes
+    // from TMEM (the state after the chunk's update) or from init_state (`g_row`).
+    auto publish_state = [&](uint32_t slot_off, int use, int e, const float* g_row,
+                             bool from_tmem) {
+      float m = 0.f;
+      if (q4 < 3) {
         const float sc = pow2i(-e);
-        for (int nb = 0; nb < 6; ++nb) {
+        float r[32];
+#pragma unroll 1
+        for (int nb = 0; nb < 3; ++nb) {
+          const int col = 96 * hf + 32 * nb;
           if (from_tmem) {
-            tmem_ld32(trow + TM_S + nb * 32, r);
+            tmem_ld32(trow + TM_S + col, *reinterpret_cast<uint32_t(*)[32]>(r));
             tmem_wait_ld();
           } else {
-            for (int j = 0; j < 32; ++j)
-              r[j] = __float_as_uint(g_row ? __ldg(g_row + nb * 32 + j) : 0.f);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) r[j] = g_row ? __ldg(g_row + col + j) : 0.f;
           }
 #pragma unroll
-          for (int q8 = 0; q8 < 4; ++q8) {  // 4 chunks of 8 value channels
-            const int n = nb * 32 + q8 * 8;
+          for (int q8 = 0; q8 < 4; ++q8) {
+            const int n = col + 8 * q8;
             uint4 pk;
-            pk.x = pack_h2(__uint_as_float(r[q8 * 8 + 0]) * sc, __uint_as_float(r[q8 * 8 + 1]) * sc);
-            pk.y = pack_h2(__uint_as_float(r[q8 * 8 + 2]) * sc, __uint_as_float(r[q8 * 8 + 3]) * sc);
-            pk.z = pack_h2(__uint_as_float(r[q8 * 8 + 4]) * sc, __uint_as_float(r[q8 * 8 + 5]) * sc);
-            pk.w = pack_h2(__uint_as_float(r[q8 * 8 + 6]) * sc, __uint_as_float(r[q8 * 8 + 7]) * sc);
-            *(uint4*)(sm.base + slot_off + (n >> 6) * S_ATOM + swz_off(i, (n & 63) >> 3, 128)) = pk;
+            pk.x = pack_h2(r[8 * q8 + 0] * sc, r[8 * q8 + 1] * sc);
+            pk.y = pack_h2(r[8 * q8 + 2] * sc, r[8 * q8 + 3] * sc);
+            pk.z = pack_h2(r[8 * q8 + 4] * sc, r[8 * q8 + 5] * sc);
+            pk.w = pack_h2(r[8 * q8 + 6] * sc, r[8 * q8 + 7] * sc);
+            *(uint4*)(base + slot_off + (n >> 6) * S_ATOM + swz_off(i, (n & 63) >> 3, 128)) = pk;
           }
-          for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * lamC);
-          tmem_st32(trow + TM_S + nb * 32, r);
+          uint32_t u[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            m = fmaxf(m, fabsf(r[j]));
+            u[j] = __float_as_uint(r[j] * lamC);
+          }
+          tmem_st32(trow + TM_S + col, u);
         }
         tmem_wait_st();
       }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+      if (lane == 0) red[(use & 1) * 8 + ew] = m;
+      if (tid == 128) es[use & 1] = e;
       fence_proxy_async();
       tc_fence_before();
-      mbar_arrive(sm.bar(EP_S));
-      return e;
+      mbar_arrive(cta.bar(EP_S));
+    };
+    auto red_max = [&](int slot) {
+      float m = red[slot * 8];
+#pragma unroll
+      for (int w = 1; w < 8; ++w) m = fmaxf(m, red[slot * 8 + w]);
+      return m;
     };
 
-    // initial state -> copy in stage 1's q/k slot, D_S = lambda^C S_0
+    // initial state: its exponent needs its exact max first (one exchange in the group)
+    const float* g_row0 = (init && i < DK) ? init + ((size_t)bh * DK + i) * DV : nullptr;
+    int e_cur = 0;
     {
-      const float* g_row = (init && i < DK) ? init + ((size_t)bh * DK + i) * DV : nullptr;
-      e_cur = publish_state(1 * STAGE + OFF_Q, 0, g_row, false);
+      float m = 0.f;
+      if (g_row0)
+        for (int j = 96 * hf; j < 96 * hf + 96; ++j) m = fmaxf(m, fabsf(__ldg(g_row0 + j)));
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+      if (lane == 0) red[16 + ew] = m;
+      mbar_arrive(cta.bar(RED));
+    }
+    bool ok = wait(cta, cta.bar(RED), 0, ctl);
+    if (ok) {
+      e_cur = state_exponent(red_max(2));
+      if (e_cur < 0) {
+        bad = true;
+        e_cur = 0;
+      }
+      publish_state(1 * STAGE + OFF_Q, 0, e_cur, g_row0, false);
     }
 
-    bool ok = e_cur >= 0;
     for (int c = 0; c < nc && ok; ++c) {
-      const uint32_t s = c & 1;
-      uint8_t* stg = sm.base + s * STAGE;
-      // ---- (a) gate, in-place operand conversion, masked scores
-      if (!(ok = wait_or_abort(sm, sm.bar(P_DONE), c & 1, ctl))) break;
-      if (!(ok = wait_or_abort(sm, sm.bar(QK_FULL + s), (c >> 1) & 1, ctl))) break;
-      if (!(ok = wait_or_abort(sm, sm.bar(V_FULL + s), (c >> 1) & 1, ctl))) break;
+      const uint32_t s = c & 1, par = c & 1;
+      uint8_t* stg = base + s * STAGE;
+      if (!(ok = wait(cta, cta.bar(O_DONE), par, ctl))) break;
+      if (!(ok = wait(cta, cta.bar(S_DONE), par, ctl))) break;
+      if (!(ok = wait(cta, cta.bar(EP_CONV), par, ctl))) break;
       tc_fence_after();
-      float z = 0.f;
-#pragma unroll
-      for (int j = 0; j < 3; ++j) {
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          const uint32_t off = j * Q_BOX + swz_off(i, ch, 64);
-          uint4 qv = *(uint4*)(stg + OFF_Q + off);
-          uint4 kv = *(uint4*)(stg + OFF_K + off);
-          const uint32_t* qw = (const uint32_t*)&qv;
-          const uint32_t* kw = (const uint32_t*)&kv;
-          uint4 qo, ko;
-          uint32_t* qow = (uint32_t*)&qo;
-          uint32_t* kow = (uint32_t*)&ko;
-#pragma unroll
-          for (int e2 = 0; e2 < 4; ++e2) {
-            const int d = j * 32 + ch * 8 + e2 * 2;
-            const float q0 = ld16<BF16>((uint16_t)(qw[e2] & 0xFFFF)), q1 = ld16<BF16>((uint16_t)(qw[e2] >> 16));
-            const float k0 = ld16<BF16>((uint16_t)(kw[e2] & 0xFFFF)), k1 = ld16<BF16>((uint16_t)(kw[e2] >> 16));
-            z = fmaf(sa[d] * q0, k0, z);
-            z = fmaf(sa[d + 1] * q1, k1, z);
-            const float a0 = q0 * lq, a1 = q1 * lq, b0 = k0 * lk, b1 = k1 * lk;
-            range_bad |= fmaxf(fmaxf(fabsf(a0), fabsf(a1)), fmaxf(fabsf(b0), fabsf(b1))) >= 65504.f;
-            qow[e2] = pack_h2(a0, a1);
-            kow[e2] = pack_h2(b0, b1);
-          }
-          *(uint4*)(stg + OFF_Q + off) = qo;
-          *(uint4*)(stg + OFF_K + off) = ko;
+      // ---- next chunk's state copy first: it is on the serial chain.  Its exponent comes
+      // from a bound, |S_{c+1}| <= lambda^C max|S_c| + 128 max|K'_c| max|V_c|, so the copy
+      // needs a single pass over the state.
+      int e_next = e_cur;
+      if (c < nc - 1) {
+        // every emit thread has stored its part of max|S_c| (EP_S phase c is complete)
+        if (!(ok = wait(cta, cta.bar(EP_S), par, ctl))) break;
+        const float ms = red_max(par);
+        const float km = fmaxf(fmaxf(kvmax[par * 8 + 0], kvmax[par * 8 + 1]),
+                               fmaxf(kvmax[par * 8 + 2], kvmax[par * 8 + 3]));
+        const float vm = fmaxf(fmaxf(kvmax[par * 8 + 4], kvmax[par * 8 + 5]),
+                               fmaxf(kvmax[par * 8 + 6], kvmax[par * 8 + 7]));
+        e_next = state_exponent(lamC * ms + (float)C * km * vm);
+        if (e_next < 0) {
+          bad = true;
+          e_next = 0;
         }
+        publish_state(s * STAGE + OFF_Q, c + 1, e_next, nullptr, true);
       }
-      if constexpr (BF16) {  // v -> fp16 in place (exact for |v| < 65504 normal range)
-#pragma unroll
-        for (int j = 0; j < 3; ++j) {
-#pragma unroll
-          for (int ch = 0; ch < 8; ++ch) {
-            const uint32_t off = OFF_V + j * V_BOX + swz_off(i, ch, 128);
-            uint4 vv = *(uint4*)(stg + off);
-            uint32_t* vw = (uint32_t*)&vv;
-#pragma unroll
-            for (int e2 = 0; e2 < 4; ++e2) {
-              const float v0 = ld16<true>((uint16_t)(vw[e2] & 0xFFFF)), v1 = ld16<true>((uint16_t)(vw[e2] >> 16));
-              range_bad |= fmaxf(fabsf(v0), fabsf(v1)) >= 65504.f;
-              vw[e2] = pack_h2(v0, v1);
-            }
-            *(uint4*)(stg + off) = vv;
-          }
-        }
-      }
+      // ---- output rows: o = 2^e D_O + sigmoid(z) v for columns [96hf, 96hf+96), TMA-stored
+      // from this warp's rows of v box (hf ? 2 : 0), which no one reads any more once the
+      // values below are in registers
+      uint8_t* const stage_o = stg + OFF_V + (hf ? 2 : 0) * V_BOX + q4 * 4096;
       {
-        const float psc = pow2i(-e_cur);
-        uint32_t r[32];
-#pragma unroll
-        for (int jb = 0; jb < 4; ++jb) {
-          tmem_ld32(trow + TM_P + jb * 32, r);
-          tmem_wait_ld();
-#pragma unroll
-          for (int q8 = 0; q8 < 4; ++q8) {
-            float p[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const int jj = jb * 32 + q8 * 8 + u;
-              const float x = __uint_as_float(r[q8 * 8 + u]);
-              p[u] = (jj <= i) ? x * pw[i - jj] * psc : 0.f;
-              range_bad |= fabsf(p[u]) >= 65504.f;
-            }
-            uint4 pk;
-            pk.x = pack_h2(p[0], p[1]);
-            pk.y = pack_h2(p[2], p[3]);
-            pk.z = pack_h2(p[4], p[5]);
-            pk.w = pack_h2(p[6], p[7]);
-            const int j0 = jb * 32 + q8 * 8;
-            *(uint4*)(sm.base + OFF_P + (j0 >> 6) * P_ATOM + swz_off(i, (j0 & 63) >> 3, 128)) = pk;
-          }
-        }
-      }
-      fence_proxy_async();
-      tc_fence_before();
-      mbar_arrive(sm.bar(EP_CONV));
-
-      // ---- (b) output row: o = 2^e D_O + sigmoid(z) v
-      if (!(ok = wait_or_abort(sm, sm.bar(O_DONE), c & 1, ctl))) break;
-      tc_fence_after();
-      {
-        const float sg = 1.f / (1.f + expf(-z));
+        const float sg = sigmoid(zs[par * 128 + i]);
         const float osc = pow2i(e_cur);
-        float* orow = out + (((size_t)b * T + (size_t)c * C + i) * H + h) * DV;
-        uint32_t r[32];
-#pragma unroll 1
-        for (int nb = 0; nb < 6; ++nb) {
-          tmem_ld32(trow + TM_O + nb * 32, r);
-          tmem_wait_ld();
+        const int row = b * T + c * C + 32 * q4;
+        uint4 vv[12];  // value channels 96hf .. 96hf+95 of row i (fp16)
 #pragma unroll
-          for (int q8 = 0; q8 < 4; ++q8) {
-            const int n = nb * 32 + q8 * 8;
-            const uint4 vv = *(const uint4*)(stg + OFF_V + (n >> 6) * V_BOX + swz_off(i, (n & 63) >> 3, 128));
-            const uint32_t* vw = (const uint32_t*)&vv;
-            float4 o0, o1;
-            o0.x = fmaf(__uint_as_float(r[q8 * 8 + 0]), osc, sg * h2lo(vw[0]));
-            o0.y = fmaf(__uint_as_float(r[q8 * 8 + 1]), osc, sg * h2hi(vw[0]));
-            o0.z = fmaf(__uint_as_float(r[q8 * 8 + 2]), osc, sg * h2lo(vw[1]));
-            o0.w = fmaf(__uint_as_float(r[q8 * 8 + 3]), osc, sg * h2hi(vw[1]));
-            o1.x = fmaf(__uint_as_float(r[q8 * 8 + 4]), osc, sg * h2lo(vw[2]));
-            o1.y = fmaf(__uint_as_float(r[q8 * 8 + 5]), osc, sg * h2hi(vw[2]));
-            o1.z = fmaf(__uint_as_float(r[q8 * 8 + 6]), osc, sg * h2lo(vw[3]));
-            o1.w = fmaf(__uint_as_float(r[q8 * 8 + 7]), osc, sg * h2hi(vw[3]));
-            __stcs(reinterpret_cast<float4*>(orow + n), o0);
-            __stcs(reinterpret_cast<float4*>(orow + n + 4), o1);
-          }
+        for (int ch = 0; ch < 12; ++ch) {
+          const int n = 96 * hf + 8 * ch;
+          vv[ch] = *(const uint4*)(stg + OFF_V + (n >> 6) * V_BOX + swz_off(i, (n & 63) >> 3, 128));
         }
+        __syncwarp();
+        emit_rows_tma<6>(
+            stage_o, lane,
+            [&](int k, float (&o)[16]) {
+              uint32_t r[16];
+              tmem_ld16(trow + TM_O + 96 * hf + 16 * k, r);
+              tmem_wait_ld();
+#pragma unroll
+              for (int ch = 0; ch < 2; ++ch) {
+                const uint4 v4 = vv[2 * k + ch];
+                const uint32_t* vw = (const uint32_t*)&v4;
+#pragma unroll
+                for (int e2 = 0; e2 < 4; ++e2) {
+                  o[8 * ch + 2 * e2] = fmaf(__uint_as_float(r[8 * ch + 2 * e2]), osc, sg * h_lo(vw[e2]));
+                  o[8 * ch + 2 * e2 + 1] =
+                      fmaf(__uint_as_float(r[8 * ch + 2 * e2 + 1]), osc, sg * h_hi(vw[e2]));
+                }
+              }
+            },
+            [&](int k, uint32_t src) { tma_store_3d(&map_o, src, 96 * hf + 16 * k, h, row); });
       }
       tc_fence_before();
-      mbar_arrive(sm.bar(EP_O));
-      mbar_arrive(sm.bar(V_EMPTY + s));
-
-      // ---- (c) state: publish the next chunk's state copy, or write the final state
-      if (!(ok = wait_or_abort(sm, sm.bar(S_DONE), c & 1, ctl))) break;
-      tc_fence_after();
-      if (c == nc - 1) {
-        if (fin && warp < 3) {
-          float* frow = fin + ((size_t)bh * DK + i) * DV;
-          uint32_t r[32];
-          for (int nb = 0; nb < 6; ++nb) {
-            tmem_ld32(trow + TM_S + nb * 32, r);
-            tmem_wait_ld();
-            for (int j = 0; j < 32; j += 4)
-              *reinterpret_cast<float4*>(frow + nb * 32 + j) =
-                  make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
-                              __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
-          }
-        }
-      } else {
-        e_cur = publish_state(s * STAGE + OFF_Q, c + 1, nullptr, true);
-        if (!(ok = e_cur >= 0)) break;
+      mbar_arrive(cta.bar(EP_O));
+      // ---- final state (after the last chunk), staged through the same rows
+      if (c == nc - 1 && fin && q4 < 3) {
+        if (lane == 0) bulk_wait_read<0>();
+        __syncwarp();
+        emit_rows_tma<6>(
+            stage_o, lane,
+            [&](int k, float (&f)[16]) {
+              uint32_t r[16];
+              tmem_ld16(trow + TM_S + 96 * hf + 16 * k, r);
+              tmem_wait_ld();
+#pragma unroll
+              for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(r[j]);
+            },
+            [&](int k, uint32_t src) { tma_store_3d(&map_fin, src, 96 * hf + 16 * k, 32 * q4, bh); });
       }
+      if (lane == 0) bulk_wait_read<0>();  // the v tile is free for the next load
+      __syncwarp();
+      mbar_arrive(cta.bar(V_EMPTY + s));
+      e_cur = e_next;
     }
-    if (range_bad) record_error(ctl, DEV_RANGE);
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
+    if (bad) record_error(ctl, DEV_RANGE);
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == MMA_WARP) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -475,16 +533,18 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
 }  // namespace
 
 cudaError_t launch_chunk_fwd(const FwdArgs& a, DevCtl ctl, cudaStream_t stream) {
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo, mfin;
   const long long rows = (long long)a.B * a.T;
   if (!make_tmap_3d_16bit(&mq, a.q, DK, a.H, rows, 32, C, CU_TENSOR_MAP_SWIZZLE_64B, a.bf16) ||
       !make_tmap_3d_16bit(&mk, a.k, DK, a.H, rows, 32, C, CU_TENSOR_MAP_SWIZZLE_64B, a.bf16) ||
-      !make_tmap_3d_16bit(&mv, a.v, DV, a.H, rows, 64, C, CU_TENSOR_MAP_SWIZZLE_128B, a.bf16))
+      !make_tmap_3d_16bit(&mv, a.v, DV, a.H, rows, 64, C, CU_TENSOR_MAP_SWIZZLE_128B, a.bf16) ||
+      !make_tmap_out_f32(&mo, a.o, DV, a.H, rows) ||
+      !make_tmap_state_f32(&mfin, a.fin ? (const void*)a.fin : (const void*)a.o, (long long)a.B * a.H))
     return cudaErrorInvalidValue;
   auto kern = a.bf16 ? fwd_kernel<true> : fwd_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  kern<<<a.B * a.H, THREADS, SMEM_BYTES, stream>>>(mq, mk, mv, a.log_decay, a.aug, a.init, a.o,
+  kern<<<a.B * a.H, THREADS, SMEM_BYTES, stream>>>(mq, mk, mv, mo, mfin, a.log_decay, a.aug, a.init, a.o,
                                                    a.fin, a.T, a.H, ctl);
   return cudaGetLastError();
 }

@@ -42,4 +42,39 @@ inline bool make_tmap_3d_16bit(CUtensorMap* map, const void* base, int d, int H,
   return r == CUDA_SUCCESS;
 }
 
+// A generic 3-D tensor map: dims / box innermost first, strides in bytes of dims 1 and 2.
+inline bool make_tmap_3d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype,
+                         const unsigned long long (&dims)[3], const unsigned long long (&strides)[2],
+                         const unsigned (&box)[3], CUtensorMapSwizzle sw) {
+  auto fn = encode_tiled_fn();
+  if (!fn) return false;
+  cuuint64_t d[3] = {dims[0], dims[1], dims[2]};
+  cuuint64_t st[2] = {strides[0], strides[1]};
+  cuuint32_t bx[3] = {box[0], box[1], box[2]};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, dtype, 3, const_cast<void*>(base), d, st, bx, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
+// fp32 token-major output [rows, H, d] stored from shared memory in boxes of 16 channels x
+// 32 consecutive tokens of one head (64-byte rows, 64-byte swizzle).
+inline bool make_tmap_out_f32(CUtensorMap* map, const void* base, int d, int H, long long rows) {
+  const unsigned long long dims[3] = {(unsigned long long)d, (unsigned long long)H,
+                                      (unsigned long long)rows};
+  const unsigned long long strides[2] = {(unsigned long long)d * 4, (unsigned long long)d * 4 * H};
+  const unsigned box[3] = {16, 1, 32};
+  return make_tmap_3d(map, base, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dims, strides, box,
+                      CU_TENSOR_MAP_SWIZZLE_64B);
+}
+
+// fp32 states [BH, 96, 192] stored in boxes of 16 value channels x 32 key channels.
+inline bool make_tmap_state_f32(CUtensorMap* map, const void* base, long long bh) {
+  const unsigned long long dims[3] = {192, 96, (unsigned long long)bh};
+  const unsigned long long strides[2] = {192 * 4, 192 * 96 * 4};
+  const unsigned box[3] = {16, 32, 1};
+  return make_tmap_3d(map, base, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dims, strides, box,
+                      CU_TENSOR_MAP_SWIZZLE_64B);
+}
+
 }  // namespace gla
