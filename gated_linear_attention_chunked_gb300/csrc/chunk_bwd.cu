@@ -1,14 +1,676 @@
-// chunk_bwd.cu -- chunked backward (placeholder until the tcgen05 kernels land).
+// chunk_bwd.cu -- chunked backward of the Simple GLA mixer on tcgen05 tensor cores.
+//
+// Method: the gradient through every sequential state update ("Beyond the KV cache ...
+// Laplace 3B ...", section "Challenge 3"), in the chunked form of section "Challenge 1".
+// Per (b, h) and chunk c, with S_c the state entering the chunk, dS_{c+1} the adjoint of the
+// state leaving it, D_ij = lambda^(i-j) (i >= j), Lq = diag(lambda^(i+1)),
+// Lk = diag(lambda^(C-1-j)), z = q.(a*k), r = sigmoid'(z) (dO.v):
+//   dQ  = (dO V^T o D) K + Lq dO S_c^T + r (a*k)           (needs the forward state scan)
+//   dK  = (dO V^T o D)^T Q + Lk V dS_{c+1}^T + r (a*q)      (needs the reverse adjoint scan)
+//   dV  = (Q K^T o D)^T dO + Lk K dS_{c+1} + sigmoid(z) dO   (needs the reverse adjoint scan)
+//   dS_c = lambda^C dS_{c+1} + Q^T Lq dO,  d_init = dS_0,  d_a = sum r (q*k)
+//
+// One launch runs three independent CTA roles per (b, h), each a chunk scan with its state
+// (or adjoint) kept on chip, so no role waits for another:
+//   role DQ  forward order : score dP = dO V^T, out dq = dP'' K + dO'' S^T, state S += K^T V'
+//   role DV  reverse order : score P^T = K Q^T, out dv = P''^T dO + K' dS,  adjoint dS += Q''^T dO
+//   role DK  reverse order : score dP^T = V dO^T, out dk = dP''^T Q + V' dS^T, adjoint dS += Q^T dO''
+// (X'' denotes an fp16 copy of X scaled by its decay factors; scores are masked with D and
+// scaled by 2^-e in fp32 before their fp16 copy.)  Warp layout as in the forward:
+//   warp 12 TMA producer (single stage: q, k, v, dO tiles of one chunk, L2 prefetch of the next),
+//   warp 13 tcgen05 issuer + TMEM owner (D_X [0,192) output, D_S [192,384) state,
+//           D_P [384,512) score),
+//   warps 0..3 convert group (row = token = TMEM lane): gate scalars, in-place fp16 operands,
+//           masked score copy;
+//   warps 4..11 emit group (two warps per row quadrant, split columns): the next state copy
+//           (the serial step, first), then the output rows, TMA-stored from staging.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "kernels.h"
+#include "scan_common.cuh"
+#include "tmap.h"
 
 namespace gla {
+namespace {
 
-size_t chunk_bwd_workspace_bytes(int B, int T, int H) { return 0; }
+using namespace scan;
+
+enum Role : int { R_DQ = 0, R_DV = 1, R_DK = 2 };
+
+constexpr uint32_t Q_BOX = 8192, V_BOX = 16384;
+constexpr uint32_t OFF_Q = 0, OFF_K = 3 * Q_BOX, OFF_V = 6 * Q_BOX, OFF_G = OFF_V + 3 * V_BOX;
+constexpr uint32_t OFF_SC = OFF_G + 3 * V_BOX;  // masked score copy, 2 atoms x 16 KB
+constexpr uint32_t SC_ATOM = 16384;
+constexpr uint32_t OFF_CP = OFF_SC + 2 * SC_ATOM;  // state copy, 3 atoms x 12 KB
+constexpr uint32_t S_ATOM = 12288;
+constexpr uint32_t OFF_BAR = OFF_CP + 3 * S_ATOM;
+constexpr uint32_t NBAR = 16;
+constexpr uint32_t OFF_TMEM = OFF_BAR + NBAR * 8;
+constexpr uint32_t OFF_ABORT = OFF_TMEM + 4;
+constexpr uint32_t OFF_RED = OFF_TMEM + 16;  // float red[3][8]
+constexpr uint32_t OFF_ES = OFF_RED + 96;    // int es[2]
+constexpr uint32_t OFF_AB = OFF_ES + 16;     // float abmax[2][8]: state-MMA operand maxima
+constexpr uint32_t OFF_RS = OFF_AB + 64;     // float rs[2][128]: r (DQ, DK) or sigmoid (DV)
+constexpr uint32_t OFF_A = OFF_RS + 1024;    // float a[96]
+constexpr uint32_t OFF_PW = OFF_A + 384;     // float pw[128]
+constexpr uint32_t SMEM_USED = OFF_PW + 512;
+constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+
+constexpr uint32_t TM_X = 0, TM_S = 192, TM_P = 384;
+
+enum Bar : uint32_t {
+  FULL = 0,
+  EMPTY = 1,  // tiles free: state MMA done + emit group done with them
+  P_DONE = 2,
+  X_DONE = 3,
+  S_DONE = 4,
+  EP_CONV = 5,
+  EP_X = 6,
+  EP_S = 7,
+  RED = 8,
+  DRAIN = 9,
+};
+
+constexpr int THREADS = 448;
+constexpr int PRODUCER_WARP = 12, MMA_WARP = 13;
+constexpr int EMIT_THREADS = 256;
+
+struct BwdParams {
+  const float* log_decay;
+  const float* aug;
+  const float* init;
+  const float* dfin;
+  float* da_part;  // [B*H, 96]
+  int T, H;
+  bool want_dinit;
+};
+
+template <int ROLE>
+__device__ __forceinline__ constexpr uint32_t tile_bytes() {
+  return ROLE == R_DV ? 6 * Q_BOX + 3 * V_BOX : 6 * Q_BOX + 6 * V_BOX;
+}
+
+// Chunk handled at step t of the role's scan.
+template <int ROLE>
+__device__ __forceinline__ int chunk_at(int t, int nc) {
+  return ROLE == R_DQ ? t : nc - 1 - t;
+}
+
+// 16-byte chunk `cc` of row `i` of a 16-bit tile: q/k tiles have 3 boxes of 32 channels
+// (64-byte rows), v/dO tiles 3 boxes of 64 channels (128-byte rows).
+__device__ __forceinline__ uint32_t qk_chunk(uint32_t i, int cc) {
+  return (cc >> 2) * Q_BOX + swz_off(i, cc & 3, 64);
+}
+__device__ __forceinline__ uint32_t vg_chunk(uint32_t i, int cc) {
+  return (cc >> 3) * V_BOX + swz_off(i, cc & 7, 128);
+}
+
+template <bool SRC_BF16>
+__device__ __forceinline__ void unpack8(const uint4& x, float (&f)[8]) {
+  const uint32_t* w = (const uint32_t*)&x;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    f[2 * e] = ld16<SRC_BF16>(w[e] & 0xFFFFu);
+    f[2 * e + 1] = ld16<SRC_BF16>(w[e] >> 16);
+  }
+}
+
+template <int ROLE, bool BF16>
+__device__ __forceinline__ void run_role(
+    uint8_t* base, const Cta& cta, int bh, const BwdParams& p, const CUtensorMap& map_q,
+    const CUtensorMap& map_k, const CUtensorMap& map_v, const CUtensorMap& map_g,
+    const CUtensorMap& map_out, const CUtensorMap& map_dinit, const DevCtl& ctl) {
+  constexpr int NX = ROLE == R_DV ? 192 : 96;  // output columns
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int H = p.H, T = p.T, b = bh / H, h = bh % H;
+  const int nc = T / C;
+  const float gamma = __ldg(p.log_decay + h);
+  float* pw = (float*)(base + OFF_PW);
+  float* red = (float*)(base + OFF_RED);
+  int* es = (int*)(base + OFF_ES);
+  float* abmax = (float*)(base + OFF_AB);
+  float* rs = (float*)(base + OFF_RS);
+  float* sa = (float*)(base + OFF_A);
+  uint32_t* tmem_slot = (uint32_t*)(base + OFF_TMEM);
+
+  if (warp == MMA_WARP) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  if (tid == PRODUCER_WARP * 32) {
+    mbar_init(cta.bar(FULL), 1);
+    mbar_init(cta.bar(EMPTY), 1 + EMIT_THREADS);
+    mbar_init(cta.bar(P_DONE), 1);
+    mbar_init(cta.bar(X_DONE), 1);
+    mbar_init(cta.bar(S_DONE), 1);
+    mbar_init(cta.bar(DRAIN), 1);
+    mbar_init(cta.bar(EP_CONV), 128);
+    mbar_init(cta.bar(EP_X), EMIT_THREADS);
+    mbar_init(cta.bar(EP_S), EMIT_THREADS);
+    mbar_init(cta.bar(RED), EMIT_THREADS);
+    *cta.abort_flag() = 0;
+    fence_barrier_init();
+  }
+  if (tid < C) pw[tid] = expf((float)tid * gamma);
+  if (tid < DK) sa[tid] = __ldg(p.aug + h * DK + tid);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t sb = cta.sb;
+
+  if (warp == PRODUCER_WARP) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const int row0 = b * T;
+      auto load = [&](int c, bool prefetch_only) {
+        const int row = row0 + c * C;
+        for (int j = 0; j < 3; ++j) {
+          if (prefetch_only) {
+            tma_prefetch_3d(&map_q, 32 * j, h, row);
+            tma_prefetch_3d(&map_k, 32 * j, h, row);
+            if (ROLE != R_DV) tma_prefetch_3d(&map_v, 64 * j, h, row);
+            tma_prefetch_3d(&map_g, 64 * j, h, row);
+          } else {
+            tma_load_3d(sb + OFF_Q + j * Q_BOX, &map_q, cta.bar(FULL), 32 * j, h, row);
+            tma_load_3d(sb + OFF_K + j * Q_BOX, &map_k, cta.bar(FULL), 32 * j, h, row);
+            if (ROLE != R_DV)
+              tma_load_3d(sb + OFF_V + j * V_BOX, &map_v, cta.bar(FULL), 64 * j, h, row);
+            tma_load_3d(sb + OFF_G + j * V_BOX, &map_g, cta.bar(FULL), 64 * j, h, row);
+          }
+        }
+      };
+      int armed = 0;
+      for (int t = 0; t < nc; ++t) {
+        if (t >= 1 && !wait(cta, cta.bar(EMPTY), (t - 1) & 1, ctl)) break;
+        mbar_arrive_expect_tx(cta.bar(FULL), tile_bytes<ROLE>());
+        load(chunk_at<ROLE>(t, nc), false);
+        ++armed;
+        if (t + 1 < nc) load(chunk_at<ROLE>(t + 1, nc), true);
+      }
+      if (armed) mbar_wait(cta.bar(FULL), (armed - 1) & 1, ctl, DRAIN_NS);
+    }
+  } else if (warp == MMA_WARP) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      for (int t = 0; t < nc; ++t) {
+        const uint32_t par = t & 1;
+        if (!wait(cta, cta.bar(FULL), par, ctl)) break;
+        tc_fence_after();
+        // score (inputs as given, bf16 or fp16)
+        if constexpr (ROLE == R_DQ || ROLE == R_DK) {
+          // DQ: dP = dO V^T (A = dO, B = V);  DK: dP^T = V dO^T (A = V, B = dO); K = 192
+          constexpr uint32_t ID = idesc_f16(128, 128, BF16, BF16, false, false);
+          const uint32_t A = sb + (ROLE == R_DQ ? OFF_G : OFF_V), B = sb + (ROLE == R_DQ ? OFF_V : OFF_G);
+#pragma unroll
+          for (int ks = 0; ks < 12; ++ks) {
+            const uint32_t off = (ks >> 2) * V_BOX + (ks & 3) * 32;
+            mma_f16_ss(tmem + TM_P, smem_desc(A + off, 16, 1024, SW_128),
+                       smem_desc(B + off, 16, 1024, SW_128), ID, ks > 0);
+          }
+        } else {  // DV: P^T = K Q^T, K = 96
+          constexpr uint32_t ID = idesc_f16(128, 128, BF16, BF16, false, false);
+#pragma unroll
+          for (int ks = 0; ks < 6; ++ks) {
+            const uint32_t off = (ks >> 1) * Q_BOX + (ks & 1) * 32;
+            mma_f16_ss(tmem + TM_P, smem_desc(sb + OFF_K + off, 16, 512, SW_64),
+                       smem_desc(sb + OFF_Q + off, 16, 512, SW_64), ID, ks > 0);
+          }
+        }
+        mma_commit(cta.bar(P_DONE));
+        if (!wait(cta, cta.bar(EP_CONV), par, ctl)) break;
+        if (!wait(cta, cta.bar(EP_S), par, ctl)) break;
+        if (t >= 1 && !wait(cta, cta.bar(EP_X), (t - 1) & 1, ctl)) break;
+        tc_fence_after();
+        const uint32_t SC = sb + OFF_SC, CP = sb + OFF_CP;
+        if constexpr (ROLE == R_DQ) {
+          // dq = dO'' S^T  (A = dO'' K-major, K = dv; B = state copy as [dk rows][dv], K-major)
+          constexpr uint32_t ID1 = idesc_f16(128, 96, false, false, false, false);
+#pragma unroll
+          for (int ks = 0; ks < 12; ++ks)
+            mma_f16_ss(tmem + TM_X,
+                       smem_desc(sb + OFF_G + (ks >> 2) * V_BOX + (ks & 3) * 32, 16, 1024, SW_128),
+                       smem_desc(CP + (ks >> 2) * S_ATOM + (ks & 3) * 32, 16, 1024, SW_128), ID1,
+                       ks > 0);
+          //    + dP'' K  (A = dP'' K-major, K = j; B = K as [j][dk], MN-major)
+          constexpr uint32_t ID2 = idesc_f16(128, 96, false, false, false, true);
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            mma_f16_ss(tmem + TM_X, smem_desc(SC + (ks >> 2) * SC_ATOM + (ks & 3) * 32, 16, 1024, SW_128),
+                       smem_desc(sb + OFF_K + ks * 1024, Q_BOX, 512, SW_64), ID2, 1);
+        } else if constexpr (ROLE == R_DV) {
+          // dv = P''^T dO  (A = P''^T K-major, K = i; B = dO as [i][dv], MN-major)
+          constexpr uint32_t ID1 = idesc_f16(128, 192, false, false, false, true);
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            mma_f16_ss(tmem + TM_X, smem_desc(SC + (ks >> 2) * SC_ATOM + (ks & 3) * 32, 16, 1024, SW_128),
+                       smem_desc(sb + OFF_G + ks * 2048, V_BOX, 1024, SW_128), ID1, ks > 0);
+          //    + K' dS  (A = K' K-major, K = dk; B = adjoint copy [dk][dv], MN-major)
+#pragma unroll
+          for (int ks = 0; ks < 6; ++ks)
+            mma_f16_ss(tmem + TM_X,
+                       smem_desc(sb + OFF_K + (ks >> 1) * Q_BOX + (ks & 1) * 32, 16, 512, SW_64),
+                       smem_desc(CP + ks * 2048, S_ATOM, 1024, SW_128), ID1, 1);
+        } else {
+          // dk = dP''^T Q  (A = dP''^T K-major, K = i; B = Q as [i][dk], MN-major)
+          constexpr uint32_t ID1 = idesc_f16(128, 96, false, false, false, true);
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            mma_f16_ss(tmem + TM_X, smem_desc(SC + (ks >> 2) * SC_ATOM + (ks & 3) * 32, 16, 1024, SW_128),
+                       smem_desc(sb + OFF_Q + ks * 1024, Q_BOX, 512, SW_64), ID1, ks > 0);
+          //    + V' dS^T  (A = V' K-major, K = dv; B = adjoint copy [dk][dv], K-major)
+          constexpr uint32_t ID2 = idesc_f16(128, 96, false, false, false, false);
+#pragma unroll
+          for (int ks = 0; ks < 12; ++ks)
+            mma_f16_ss(tmem + TM_X,
+                       smem_desc(sb + OFF_V + (ks >> 2) * V_BOX + (ks & 3) * 32, 16, 1024, SW_128),
+                       smem_desc(CP + (ks >> 2) * S_ATOM + (ks & 3) * 32, 16, 1024, SW_128), ID2, 1);
+        }
+        mma_commit(cta.bar(X_DONE));
+        // state / adjoint update, M = 128 (96 key channels + padding rows never read)
+        {
+          constexpr uint32_t ID = idesc_f16(128, 192, false, false, true, true);
+          const uint32_t A = sb + (ROLE == R_DQ ? OFF_K : OFF_Q);  // K^T (DQ) or Q''^T / Q^T
+          const uint32_t B = sb + (ROLE == R_DQ ? OFF_V : OFF_G);  // V' (DQ) or dO / dO''
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            mma_f16_ss(tmem + TM_S, smem_desc(A + ks * 1024, Q_BOX, 512, SW_64),
+                       smem_desc(B + ks * 2048, V_BOX, 1024, SW_128), ID, 1);
+        }
+        mma_commit(cta.bar(S_DONE));
+        mma_commit(cta.bar(EMPTY));
+      }
+      mma_commit(cta.bar(DRAIN));
+      mbar_wait(cta.bar(DRAIN), 0, ctl, DRAIN_NS);
+    }
+  } else if (warp < 4) {
+    // ------------------------------------------------------------------ convert group
+    const int i = tid;  // tile row (token) == TMEM lane
+    const uint32_t trow = tmem + ((uint32_t)(32 * warp) << 16);
+    const float lam = pw[1], lamC = expf((float)C * gamma);
+    const float lq = (i + 1 < C) ? pw[i + 1] : lamC;  // lambda^(row+1)
+    const float lk = pw[C - 1 - i];                   // lambda^(C-1-row)
+    float range_max = 0.f;
+    for (int t = 0; t < nc; ++t) {
+      const uint32_t par = t & 1;
+      if (!wait(cta, cta.bar(FULL), par, ctl)) break;
+      // gate scalars from the 16-bit inputs (read before any in-place conversion)
+      float z = 0.f, dov = 0.f;
+#pragma unroll 2
+      for (int cc = 0; cc < 12; ++cc) {
+        float q8[8], k8[8];
+        unpack8<BF16>(*(const uint4*)(base + OFF_Q + qk_chunk(i, cc)), q8);
+        unpack8<BF16>(*(const uint4*)(base + OFF_K + qk_chunk(i, cc)), k8);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) z = fmaf(sa[8 * cc + e] * q8[e], k8[e], z);
+      }
+      if constexpr (ROLE != R_DV) {
+#pragma unroll 2
+        for (int cc = 0; cc < 24; ++cc) {
+          float g8[8], v8[8];
+          unpack8<BF16>(*(const uint4*)(base + OFF_G + vg_chunk(i, cc)), g8);
+          unpack8<BF16>(*(const uint4*)(base + OFF_V + vg_chunk(i, cc)), v8);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) dov = fmaf(g8[e], v8[e], dov);
+        }
+      }
+      const float sg = sigmoid(z);
+      rs[par * 128 + i] = ROLE == R_DV ? sg : sg * (1.f - sg) * dov;
+      // the score MMA has read the 16-bit tiles: convert in place
+      if (!wait(cta, cta.bar(P_DONE), par, ctl)) break;
+      tc_fence_after();
+      float amax = 0.f, bmax = 0.f;  // operands of the state MMA
+      if constexpr (ROLE == R_DQ) {
+        for (int cc = 0; cc < 12; ++cc)  // K -> fp16 (A of the state MMA, B of dP'' K)
+          scale_chunk_to_half<BF16>((uint4*)(base + OFF_K + qk_chunk(i, cc)), 1.f, amax);
+        for (int cc = 0; cc < 24; ++cc)  // V' = lambda^(C-1-j) v (B of the state MMA)
+          scale_chunk_to_half<BF16>((uint4*)(base + OFF_V + vg_chunk(i, cc)), lk, bmax);
+        for (int cc = 0; cc < 24; ++cc)  // dO'' = lambda^(i+1) dO (A of dO'' S^T)
+          scale_chunk_to_half<BF16>((uint4*)(base + OFF_G + vg_chunk(i, cc)), lq, range_max);
+      } else if constexpr (ROLE == R_DV) {
+        for (int cc = 0; cc < 12; ++cc)  // Q'' = lambda^(j+1) q (A of the adjoint MMA)
+          scale_chunk_to_half<BF16>((uint4*)(base + OFF_Q + qk_chunk(i, cc)), lq, amax);
+        for (int cc = 0; cc < 12; ++cc)  // K' = lambda^(C-1-j) k (A of K' dS)
+          scale_chunk_to_half<BF16>((uint4*)(base + OFF_K + qk_chunk(i, cc)), lk, range_max);
+        for (int cc = 0; cc < 24; ++cc)  // dO -> fp16 (B of P''^T dO and of the adjoint MMA)
+          scale_chunk_to_half<BF16>((uint4*)(base + OFF_G + vg_chunk(i, cc)), 1.f, bmax);
+      } else {
+        for (int cc = 0; cc < 12; ++cc)  // Q -> fp16 (B of dP''^T Q, A of the adjoint MMA)
+          scale_chunk_to_half<BF16>((uint4*)(base + OFF_Q + qk_chunk(i, cc)), 1.f, amax);
+        for (int cc = 0; cc < 24; ++cc)  // V' = lambda^(C-1-j) v (A of V' dS^T)
+          scale_chunk_to_half<BF16>((uint4*)(base + OFF_V + vg_chunk(i, cc)), lk, range_max);
+        for (int cc = 0; cc < 24; ++cc)  // dO'' = lambda^(j+1) dO (B of the adjoint MMA)
+          scale_chunk_to_half<BF16>((uint4*)(base + OFF_G + vg_chunk(i, cc)), lq, bmax);
+      }
+      {
+        float am = amax, bm = bmax;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+          am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, off));
+          bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, off));
+        }
+        if (lane == 0) {
+          abmax[par * 8 + warp] = am;
+          abmax[par * 8 + 4 + warp] = bm;
+        }
+      }
+      range_max = fmaxf(range_max, fmaxf(amax, bmax));
+      // masked score copy, scaled by 2^-e of this step's state copy
+      if (!wait(cta, cta.bar(EP_S), par, ctl)) break;
+      const float psc = pow2i(-es[par]);
+      float pmax = 0.f;
+      {
+        uint32_t r[32];
+#pragma unroll 1
+        for (int jb = 0; jb < 4; ++jb) {
+          const int c0 = 32 * jb;
+          float sc[32];
+          // DQ (rows = queries i, columns j <= i) or DV/DK (rows = keys j, columns i >= j)
+          const bool live = ROLE == R_DQ ? jb <= warp : jb >= warp;
+          if (live) {
+            tmem_ld32(trow + TM_P + c0, r);
+            tmem_wait_ld();
+            if constexpr (ROLE == R_DQ) {
+              float f = pw[max(i - (c0 + 31), 0)] * psc;  // going left from min(i, c0+31)
+#pragma unroll
+              for (int u = 31; u >= 0; --u) {
+                const bool in = c0 + u <= i;
+                sc[u] = in ? __uint_as_float(r[u]) * f : 0.f;
+                f = in ? f * lam : f;
+                pmax = fmaxf(pmax, fabsf(sc[u]));
+              }
+            } else {
+              float f = pw[max(c0 - i, 0)] * psc;  // going right from max(j, c0)
+#pragma unroll
+              for (int u = 0; u < 32; ++u) {
+                const bool in = c0 + u >= i;
+                sc[u] = in ? __uint_as_float(r[u]) * f : 0.f;
+                f = in ? f * lam : f;
+                pmax = fmaxf(pmax, fabsf(sc[u]));
+              }
+            }
+          } else {
+#pragma unroll
+            for (int u = 0; u < 32; ++u) sc[u] = 0.f;
+          }
+#pragma unroll
+          for (int q8 = 0; q8 < 4; ++q8) {
+            uint4 pk;
+            pk.x = pack_h2(sc[8 * q8 + 0], sc[8 * q8 + 1]);
+            pk.y = pack_h2(sc[8 * q8 + 2], sc[8 * q8 + 3]);
+            pk.z = pack_h2(sc[8 * q8 + 4], sc[8 * q8 + 5]);
+            pk.w = pack_h2(sc[8 * q8 + 6], sc[8 * q8 + 7]);
+            *(uint4*)(base + OFF_SC + (jb >> 1) * SC_ATOM + swz_off(i, 4 * (jb & 1) + q8, 128)) = pk;
+          }
+        }
+      }
+      range_max = fmaxf(range_max, pmax);
+      fence_proxy_async();
+      tc_fence_before();
+      mbar_arrive(cta.bar(EP_CONV));
+    }
+    if (range_max >= 65504.f) record_error(ctl, DEV_RANGE);
+  } else if (warp < PRODUCER_WARP) {
+    // ------------------------------------------------------------------ emit group
+    const int q4 = warp & 3, hf = (warp - 4) >> 2, ew = warp - 4;
+    const int i = 32 * q4 + lane;
+    const uint32_t trow = tmem + ((uint32_t)(32 * q4) << 16);
+    const float lamC = expf((float)C * gamma);
+    uint8_t* const stage = base + OFF_V + ew * 4096;  // v region: free in every role by then
+    bool bad = false;
+    float da_acc = 0.f;  // DQ: d_a of channel (tid - 128) < 96, summed over this CTA's rows
+
+    auto publish_state = [&](int use, int e, const float* g_row, bool from_tmem) {
+      float m = 0.f;
+      if (q4 < 3) {
+        const float sc = pow2i(-e);
+        float r[32];
+#pragma unroll 1
+        for (int nb = 0; nb < 3; ++nb) {
+          const int col = 96 * hf + 32 * nb;
+          if (from_tmem) {
+            tmem_ld32(trow + TM_S + col, *reinterpret_cast<uint32_t(*)[32]>(r));
+            tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) r[j] = g_row ? __ldg(g_row + col + j) : 0.f;
+          }
+#pragma unroll
+          for (int q8 = 0; q8 < 4; ++q8) {
+            const int n = col + 8 * q8;
+            uint4 pk;
+            pk.x = pack_h2(r[8 * q8 + 0] * sc, r[8 * q8 + 1] * sc);
+            pk.y = pack_h2(r[8 * q8 + 2] * sc, r[8 * q8 + 3] * sc);
+            pk.z = pack_h2(r[8 * q8 + 4] * sc, r[8 * q8 + 5] * sc);
+            pk.w = pack_h2(r[8 * q8 + 6] * sc, r[8 * q8 + 7] * sc);
+            *(uint4*)(base + OFF_CP + (n >> 6) * S_ATOM + swz_off(i, (n & 63) >> 3, 128)) = pk;
+          }
+          uint32_t u[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            m = fmaxf(m, fabsf(r[j]));
+            u[j] = __float_as_uint(r[j] * lamC);
+          }
+          tmem_st32(trow + TM_S + col, u);
+        }
+        tmem_wait_st();
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+      if (lane == 0) red[(use & 1) * 8 + ew] = m;
+      if (tid == 128) es[use & 1] = e;
+      fence_proxy_async();
+      tc_fence_before();
+      mbar_arrive(cta.bar(EP_S));
+    };
+    auto red_max = [&](int slot) {
+      float m = red[slot * 8];
+#pragma unroll
+      for (int w = 1; w < 8; ++w) m = fmaxf(m, red[slot * 8 + w]);
+      return m;
+    };
+
+    // initial state (DQ) or adjoint of the final state (DV, DK)
+    const float* src0 = ROLE == R_DQ ? p.init : p.dfin;
+    const float* g_row0 = (src0 && i < DK) ? src0 + ((size_t)bh * DK + i) * DV : nullptr;
+    int e_cur = 0;
+    {
+      float m = 0.f;
+      if (g_row0)
+        for (int j = 96 * hf; j < 96 * hf + 96; ++j) m = fmaxf(m, fabsf(__ldg(g_row0 + j)));
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+      if (lane == 0) red[16 + ew] = m;
+      mbar_arrive(cta.bar(RED));
+    }
+    bool ok = wait(cta, cta.bar(RED), 0, ctl);
+    if (ok) {
+      e_cur = state_exponent(red_max(2));
+      if (e_cur < 0) {
+        bad = true;
+        e_cur = 0;
+      }
+      publish_state(0, e_cur, g_row0, false);
+    }
+
+    for (int t = 0; t < nc && ok; ++t) {
+      const uint32_t par = t & 1;
+      const int c = chunk_at<ROLE>(t, nc);
+      if (!(ok = wait(cta, cta.bar(X_DONE), par, ctl))) break;
+      if (!(ok = wait(cta, cta.bar(S_DONE), par, ctl))) break;
+      if (!(ok = wait(cta, cta.bar(EP_CONV), par, ctl))) break;
+      tc_fence_after();
+      int e_next = e_cur;
+      if (t < nc - 1) {
+        if (!(ok = wait(cta, cta.bar(EP_S), par, ctl))) break;
+        const float ms = red_max(par);
+        const float am = fmaxf(fmaxf(abmax[par * 8 + 0], abmax[par * 8 + 1]),
+                               fmaxf(abmax[par * 8 + 2], abmax[par * 8 + 3]));
+        const float bm = fmaxf(fmaxf(abmax[par * 8 + 4], abmax[par * 8 + 5]),
+                               fmaxf(abmax[par * 8 + 6], abmax[par * 8 + 7]));
+        e_next = state_exponent(lamC * ms + (float)C * am * bm);
+        if (e_next < 0) {
+          bad = true;
+          e_next = 0;
+        }
+        publish_state(t + 1, e_next, nullptr, true);
+      }
+      // ---- d_a (DQ): channel d of the emit thread, summed over this chunk's rows
+      if constexpr (ROLE == R_DQ) {
+        const int d = tid - 128;
+        if (d < DK) {
+          const uint32_t off = (d >> 5) * Q_BOX + 2 * (d & 7);
+          float acc = 0.f;
+#pragma unroll 4
+          for (int rr = 0; rr < C; ++rr) {
+            const uint32_t o = off + swz_off(rr, (d & 31) >> 3, 64);
+            const float qv = ld16<BF16>(*(const uint16_t*)(base + OFF_Q + o));
+            const float kv = __half2float(*(const __half*)(base + OFF_K + o));
+            acc = fmaf(rs[par * 128 + rr] * qv, kv, acc);
+          }
+          da_acc += acc;
+        }
+      }
+      // ---- output rows: x = 2^e D_X + (self-augmentation term), TMA-stored
+      {
+        const float g = rs[par * 128 + i];  // r (DQ, DK) or sigmoid(z) (DV)
+        const float osc = pow2i(e_cur);
+        const int row = b * T + c * C + 32 * q4;
+        constexpr int NB = NX / 32;  // 16-column blocks of this warp's half
+        emit_rows_tma<NB>(
+            stage, lane,
+            [&](int k, float (&x)[16]) {
+              const int col = (NX / 2) * hf + 16 * k;
+              uint32_t r[16];
+              tmem_ld16(trow + TM_X + col, r);
+              tmem_wait_ld();
+              // self-augmentation operand of row i, columns col..col+15 (fp16 tiles)
+              float f8[2][8];
+              if constexpr (ROLE == R_DV) {  // sigmoid(z) dO
+                unpack8<false>(*(const uint4*)(base + OFF_G + vg_chunk(i, col / 8)), f8[0]);
+                unpack8<false>(*(const uint4*)(base + OFF_G + vg_chunk(i, col / 8 + 1)), f8[1]);
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                  x[j] = fmaf(__uint_as_float(r[j]), osc, g * f8[j >> 3][j & 7]);
+              } else {  // r (a * k) (DQ) or r (a * q) (DK)
+                constexpr uint32_t SRC = ROLE == R_DQ ? OFF_K : OFF_Q;
+                unpack8<false>(*(const uint4*)(base + SRC + qk_chunk(i, col / 8)), f8[0]);
+                unpack8<false>(*(const uint4*)(base + SRC + qk_chunk(i, col / 8 + 1)), f8[1]);
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                  x[j] = fmaf(__uint_as_float(r[j]), osc, g * sa[col + j] * f8[j >> 3][j & 7]);
+              }
+            },
+            [&](int k, uint32_t src) { tma_store_3d(&map_out, src, (NX / 2) * hf + 16 * k, h, row); });
+      }
+      tc_fence_before();
+      mbar_arrive(cta.bar(EP_X));
+      // ---- adjoint of the initial state (DV, after the last step = chunk 0)
+      if (ROLE == R_DV && t == nc - 1 && p.want_dinit && q4 < 3) {
+        if (lane == 0) bulk_wait_read<0>();
+        __syncwarp();
+        emit_rows_tma<6>(
+            stage, lane,
+            [&](int k, float (&f)[16]) {
+              uint32_t r[16];
+              tmem_ld16(trow + TM_S + 96 * hf + 16 * k, r);
+              tmem_wait_ld();
+#pragma unroll
+              for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(r[j]);
+            },
+            [&](int k, uint32_t src) { tma_store_3d(&map_dinit, src, 96 * hf + 16 * k, 32 * q4, bh); });
+      }
+      if (lane == 0) bulk_wait_read<0>();
+      __syncwarp();
+      mbar_arrive(cta.bar(EMPTY));
+      e_cur = e_next;
+    }
+    if (ROLE == R_DQ && tid - 128 < DK) p.da_part[(size_t)bh * DK + (tid - 128)] = da_acc;
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
+    if (bad) record_error(ctl, DEV_RANGE);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == MMA_WARP) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(THREADS, 1)
+bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+           const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_g,
+           const __grid_constant__ CUtensorMap map_dq, const __grid_constant__ CUtensorMap map_dk,
+           const __grid_constant__ CUtensorMap map_dv, const __grid_constant__ CUtensorMap map_dinit,
+           BwdParams p, DevCtl ctl) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  Cta cta;
+  cta.base = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  cta.sb = smem_u32(cta.base);
+  cta.bar_off = OFF_BAR;
+  cta.abort_off = OFF_ABORT;
+  const int role = blockIdx.x % 3, bh = blockIdx.x / 3;
+  if (role == R_DQ)
+    run_role<R_DQ, BF16>(cta.base, cta, bh, p, map_q, map_k, map_v, map_g, map_dq, map_dinit, ctl);
+  else if (role == R_DV)
+    run_role<R_DV, BF16>(cta.base, cta, bh, p, map_q, map_k, map_v, map_g, map_dv, map_dinit, ctl);
+  else
+    run_role<R_DK, BF16>(cta.base, cta, bh, p, map_q, map_k, map_v, map_g, map_dk, map_dinit, ctl);
+}
+
+// d_aug[h, d] = sum over b of the per-(b, h) partial sums, in order of b (deterministic).
+__global__ void reduce_daug_kernel(const float* __restrict__ part, float* __restrict__ d_aug,
+                                   int B, int H) {
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= H * DK) return;
+  const int h = idx / DK, d = idx % DK;
+  float s = 0.f;
+  for (int b = 0; b < B; ++b) s += part[((size_t)b * H + h) * DK + d];
+  d_aug[idx] = s;
+}
+
+}  // namespace
+
+size_t chunk_bwd_workspace_bytes(int B, int T, int H) {
+  (void)T;
+  return (((size_t)B * H * DK * sizeof(float)) + 255) & ~(size_t)255;
+}
 
 cudaError_t launch_chunk_bwd(const BwdArgs& a, DevCtl ctl, cudaStream_t stream) {
-  return cudaErrorNotSupported;
+  CUtensorMap mq, mk, mv, mg, mdq, mdk, mdv, mdi;
+  const long long rows = (long long)a.B * a.T;
+  if (!make_tmap_3d_16bit(&mq, a.q, DK, a.H, rows, 32, C, CU_TENSOR_MAP_SWIZZLE_64B, a.bf16) ||
+      !make_tmap_3d_16bit(&mk, a.k, DK, a.H, rows, 32, C, CU_TENSOR_MAP_SWIZZLE_64B, a.bf16) ||
+      !make_tmap_3d_16bit(&mv, a.v, DV, a.H, rows, 64, C, CU_TENSOR_MAP_SWIZZLE_128B, a.bf16) ||
+      !make_tmap_3d_16bit(&mg, a.dO, DV, a.H, rows, 64, C, CU_TENSOR_MAP_SWIZZLE_128B, a.bf16) ||
+      !make_tmap_out_f32(&mdq, a.dq, DK, a.H, rows) || !make_tmap_out_f32(&mdk, a.dk, DK, a.H, rows) ||
+      !make_tmap_out_f32(&mdv, a.dv, DV, a.H, rows) ||
+      !make_tmap_state_f32(&mdi, a.dinit ? (const void*)a.dinit : (const void*)a.dv,
+                           (long long)a.B * a.H))
+    return cudaErrorInvalidValue;
+  BwdParams p;
+  p.log_decay = a.log_decay;
+  p.aug = a.aug;
+  p.init = a.init;
+  p.dfin = a.dfin;
+  p.da_part = static_cast<float*>(a.workspace);
+  p.T = a.T;
+  p.H = a.H;
+  p.want_dinit = a.dinit != nullptr;
+  auto kern = a.bf16 ? bwd_kernel<true> : bwd_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  kern<<<3 * a.B * a.H, THREADS, SMEM_BYTES, stream>>>(mq, mk, mv, mg, mdq, mdk, mdv, mdi, p, ctl);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const int n = a.H * DK;
+  reduce_daug_kernel<<<(n + 255) / 256, 256, 0, stream>>>(p.da_part, a.d_aug, a.B, a.H);
+  return cudaGetLastError();
 }
 
 }  // namespace gla
