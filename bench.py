@@ -1,0 +1,419 @@
+"""Benchmark of the Simple GLA mixer hot path on GB300.
+
+One step = the whole hot path on its two workloads:
+  * chunked forward + backward at the training shape B=32, T=2048, H=16, dk=96, dv=192
+    (bf16 inputs, fp32 outputs) -- `value` is its throughput in tokens/s;
+  * one recurrent decode step over the serving pool of 1,280 sequences x 24 layers x 16
+    heads of 96x192 fp32 states (36.2 GB resident in HBM) -- reported in `decode` as GB/s.
+
+Prints one JSON line (rank 0).  `--impl reference` times the fp64 CPU oracle instead (the
+reference arm: the plain definition, on the host cores, one bounded sample per step).
+
+Inputs are synthetic (seeded Gaussians with the workloads' shapes and scales) and larger
+than L2, so no flush is needed between timed iterations.  Kernel times come from CUDA
+events on the launching stream; SM clocks are sampled with nvidia-smi during the timed
+region.  Multi-GPU (torchrun): every rank runs the same per-GPU workload (independent
+replicas, no collective on the data path); times are maxed over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GLA fwd+bwd tokens/s (H=16,T=2048) and decode-step GB/s vs HBM roofline"
+B, T, H, DK, DV = 32, 2048, 16, 96, 192
+N_SEQ, N_LAYERS = 1280, 24
+WORKLOAD = ("GLA chunked fwd+bwd B=32 T=2048 H=16 dk=96 dv=192 chunk=128 bf16-in/fp32-out, "
+            "plus one decode step over 1280 seqs x 24 layers x 16 heads of 96x192 fp32 states")
+# Algorithmic work per unit (what the calls must move / compute at minimum)
+FWD_BYTES_TH = (96 + 96 + 192) * 2 + 192 * 4             # bf16 q,k,v in, fp32 o out = 1536
+BWD_BYTES_TH = (96 + 96 + 192 + 192) * 2 + (96 + 96 + 192) * 4  # + dO in, fp32 dq,dk,dv = 2688
+FWD_FLOPS_TH = 2 * (128 * 96 + 128 * 192 + 96 * 192 + 96 * 192)  # QK^T, PV, QS, K^T V = 147456
+BWD_FLOPS_TH = 319488                                     # 9 dense chunk matmuls per token-head
+DEC_BYTES_STATE = 2 * 96 * 192 * 4 + (96 + 96 + 192 + 192) * 4  # state r+w, q,k,v,o = 149760
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sus=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                    src="of measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="of fallback")
+
+
+def traffic_record(kernel: str):
+    """dram bytes per unit from an ncu capture (profiles/traffic.json), if the kernel
+    source it was taken on is unchanged; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    rec = json.load(open(p)).get(kernel)
+    if not rec:
+        return None
+    m = hashlib.sha256()
+    for f in rec["source"]:
+        src = os.path.join(ROOT, "gated_linear_attention_chunked_gb300", "csrc", f)
+        if not os.path.exists(src):
+            return None
+        m.update(open(src, "rb").read())
+    return rec if m.hexdigest()[:16] == rec.get("source_sha256_16") else None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms while running."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.out = None
+
+    def __enter__(self):
+        try:
+            self.out = open(os.devnull, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                txt, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                txt, _ = self.proc.communicate()
+            self.lines = [l for l in txt.splitlines() if l.strip()]
+        if self.out:
+            self.out.close()
+
+    def mark(self, which: str):
+        setattr(self, which, time.time())
+
+    def summary(self):
+        import datetime
+        import statistics
+        mhz, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        t0, t1 = getattr(self, "t_start", None), getattr(self, "t_end", None)
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                if t0 is not None and not (t0 <= ts <= t1):
+                    continue  # outside the timed region
+                mhz.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not mhz:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(mhz)}
+
+
+# --------------------------------------------------------------------------- CPU oracle
+def oracle_sample(n_seq: int, seed: int = 2):
+    """Time the fp64 oracle's fwd+bwd over `n_seq` sequences of the training workload."""
+    import numpy as np
+
+    import oracle
+    import synth
+    x = synth.chunk_inputs("train_fwd_bwd", B=n_seq)
+    g = oracle.decay_schedule(H).astype(np.float32).astype(np.float64)
+    t0 = time.perf_counter()
+    oracle.fwd(x["q"], x["k"], x["v"], g, x["a"])
+    oracle.bwd(x["q"], x["k"], x["v"], g, x["a"], x["dO"])
+    dt = time.perf_counter() - t0
+    return n_seq * T / dt, dt
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    cores = os.cpu_count() or 1
+    import numpy as np
+    for _ in range(args.warmup):
+        oracle_sample(1)
+    rates, times = [], []
+    for _ in range(args.steps):
+        r, dt = oracle_sample(1)
+        rates.append(r)
+        times.append(dt)
+    tot_tok = args.steps * T
+    value = tot_tok / sum(times)
+    line = dict(
+        impl="reference", metric=METRIC, value=value, unit="tokens/s", n_gpus=args.gpus,
+        steps=args.steps, warmup=args.warmup, ms_per_step=1e3 * float(np.mean(times)),
+        higher_is_better=True, scaling="weak", vs_baseline=None, dtype="f64",
+        data="synthetic (seeded Gaussians, training-shape recipe)",
+        config=dict(workload=WORKLOAD, B=B, T=T, H=H, dk=DK, dv=DV, chunk=128,
+                    step_sample="oracle fwd+bwd over 1 of the 32 sequences (T=2048, H=16)"),
+        cpu_baseline=dict(value=value, unit="tokens/s", cores=cores, kind="oracle",
+                          sample="fp64 token-by-token fwd + hand-derived bwd, 1 sequence x "
+                                 "T=2048 x H=16 per step, threaded over heads"),
+        e2e=dict(value=value, unit="tokens/s", h2d_bytes_per_step=0, d2h_bytes_per_step=0),
+    )
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------------------- GPU arm
+def run_gpu(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+
+    Bn, Ns = args.batch, args.n_seq
+    do_fwd = args.part in ("all", "fwd")
+    do_bwd = args.part in ("all", "bwd")
+    do_dec = args.part in ("all", "decode")
+
+    import gated_linear_attention_chunked_gb300 as gla
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    gla.load()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    pk = peaks()
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1234 + rank)
+
+    def randn(*shape, std=1.0, dtype=torch.float32):
+        return (torch.randn(*shape, generator=gen, device=dev) * std).to(dtype)
+
+    # ---- training-shape tensors (bf16 inputs, fp32 outputs), resident in HBM
+    gam = gla.decay_schedule(H).to(dev)
+    a = randn(H, DK, std=0.02)
+    if do_fwd or do_bwd:
+        q = randn(Bn, T, H, DK, std=DK ** -0.5, dtype=torch.bfloat16)
+        k = randn(Bn, T, H, DK, dtype=torch.bfloat16)
+        v = randn(Bn, T, H, DV, dtype=torch.bfloat16)
+        dO = randn(Bn, T, H, DV, dtype=torch.bfloat16)
+        o = torch.empty(Bn, T, H, DV, device=dev)
+        fin = torch.empty(Bn, H, DK, DV, device=dev)
+        ws = torch.empty(max(1, gla.chunk_bwd_workspace_size(Bn, T, H, gla.GLA_BF16)),
+                         dtype=torch.uint8, device=dev)
+
+    # ---- serving pool: 1280 x 24 x 16 states, warmed by 64 recurrent steps from zero
+    if do_dec:
+        st = torch.zeros(Ns, N_LAYERS, H, DK, DV, device=dev)
+        ad = randn(N_LAYERS, H, DK, std=0.02)
+        dq_ = randn(Ns, N_LAYERS, H, DK, std=DK ** -0.5)
+        dk_ = randn(Ns, N_LAYERS, H, DK)
+        dv_ = randn(Ns, N_LAYERS, H, DV)
+        od = torch.empty(Ns, N_LAYERS, H, DV, device=dev)
+        for _ in range(64):
+            dq_.normal_(0.0, DK ** -0.5, generator=gen)
+            dk_.normal_(generator=gen)
+            dv_.normal_(generator=gen)
+            gla.decode_step(st, dq_, dk_, dv_, gam, ad, out=od)
+        dq_.normal_(0.0, DK ** -0.5, generator=gen)
+        dk_.normal_(generator=gen)
+        dv_.normal_(generator=gen)
+    torch.cuda.synchronize()
+    if gla.get_device_error() != 0:
+        raise RuntimeError("device error during setup")
+
+    stream = torch.cuda.current_stream()
+    n_states = Ns * N_LAYERS * H
+
+    def step(evs=None):
+        if evs:
+            evs[0].record(stream)
+        if do_fwd:
+            gla.chunk_fwd(q, k, v, gam, a, out=o, final_state=fin)
+        if evs:
+            evs[1].record(stream)
+        if do_bwd:
+            gla.chunk_bwd(q, k, v, gam, a, dO, workspace=ws)
+        if evs:
+            evs[2].record(stream)
+        if do_dec:
+            gla.decode_step(st, dq_, dk_, dv_, gam, ad, out=od)
+        if evs:
+            evs[3].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        time.sleep(0.5)  # let the sampler come up
+        clk.mark("t_start")
+        t_wall = time.perf_counter()
+        for s in range(args.steps):
+            step(evs[s])
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+        clk.mark("t_end")
+    if dist:
+        dist.barrier()
+    fwd_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    bwd_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    dec_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    tot_ms = [e[0].elapsed_time(e[3]) for e in evs]
+    if gla.get_device_error() != 0:
+        raise RuntimeError("device error in the timed region")
+    sums = torch.tensor([sum(fwd_ms), sum(bwd_ms), sum(dec_ms), sum(tot_ms)], device=dev,
+                        dtype=torch.float64)
+    if dist:
+        dist.all_reduce(sums, op=dist.ReduceOp.MAX)
+    fwd_t, bwd_t, dec_t, tot_t = (float(x) / args.steps for x in sums.cpu())  # ms per step
+    if args.part != "all":
+        part_ms = dict(fwd=fwd_t, bwd=bwd_t, decode=dec_t)[args.part]
+        if rank == 0:
+            print(json.dumps(dict(part=args.part, ms=part_ms, batch=Bn, n_seq=Ns, steps=args.steps,
+                                  warmup=args.warmup, clocks=clk.summary())), flush=True)
+        if dist:
+            dist.destroy_process_group()
+        return 0
+    tokens = B * T
+    value = world * tokens / ((fwd_t + bwd_t) * 1e-3)
+    dec_bytes = n_states * DEC_BYTES_STATE
+    dec_gbs = dec_bytes / (dec_t * 1e-3) / 1e9
+    th = B * T * H
+    gpu_launches_per_step = 4  # chunk fwd, chunk bwd, d_aug reduction, decode
+
+    def roof(bound, achieved, peak, unit, traffic):
+        return dict(bound=bound, achieved=achieved, peak=peak, unit=unit, frac=achieved / peak,
+                    traffic=traffic, peak_source=pk["src"])
+
+    tr_dec = traffic_record("decode")
+    tr_fwd = traffic_record("chunk_fwd")
+    tr_bwd = traffic_record("chunk_bwd")
+    roofline = roof("hbm", dec_gbs, pk["hbm"], "GB/s",
+                    None if tr_dec is None else tr_dec["bytes_per_unit"] * n_states)
+    roofline["kernel"] = "decode_kernel (dominant: largest share of the step time)"
+    fwd_gbs = th * FWD_BYTES_TH / (fwd_t * 1e-3) / 1e9
+    bwd_gbs = th * BWD_BYTES_TH / (bwd_t * 1e-3) / 1e9
+    roof_fwd = roof("hbm", fwd_gbs, pk["hbm"], "GB/s",
+                    None if tr_fwd is None else tr_fwd["bytes_per_unit"] * th)
+    roof_fwd["tensor"] = dict(achieved=th * FWD_FLOPS_TH / (fwd_t * 1e-3) / 1e12, peak=pk["bf16"],
+                              unit="TFLOP/s", frac=th * FWD_FLOPS_TH / (fwd_t * 1e-3) / 1e12 / pk["bf16"])
+    roof_bwd = roof("hbm", bwd_gbs, pk["hbm"], "GB/s",
+                    None if tr_bwd is None else tr_bwd["bytes_per_unit"] * th)
+    roof_bwd["tensor"] = dict(achieved=th * BWD_FLOPS_TH / (bwd_t * 1e-3) / 1e12, peak=pk["bf16"],
+                              unit="TFLOP/s", frac=th * BWD_FLOPS_TH / (bwd_t * 1e-3) / 1e12 / pk["bf16"])
+
+    # ---- end to end through the public API: pinned host inputs -> HBM -> fwd+bwd -> d_aug
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv, hdO = (x.cpu().pin_memory() for x in (q, k, v, dO))
+        h_daug = torch.empty(H, DK).pin_memory()
+        h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hdO))
+        d2h = h_daug.numel() * 4
+        e2e_steps = max(3, min(args.steps, 10))
+        times = []
+        for s in range(e2e_steps + 2):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            dq2, dk2, dv2, dO2 = (x.to(dev, non_blocking=True) for x in (hq, hk, hv, hdO))
+            gla.chunk_fwd(dq2, dk2, dv2, gam, a, out=o, final_state=fin)
+            _, _, _, daug, _ = gla.chunk_bwd(dq2, dk2, dv2, gam, a, dO2, workspace=ws,
+                                             want_d_init_state=False)
+            h_daug.copy_(daug, non_blocking=True)
+            torch.cuda.synchronize()
+            if s >= 2:
+                times.append(time.perf_counter() - t0)
+            del dq2, dk2, dv2, dO2
+        tt = torch.tensor([sum(times)], device=dev, dtype=torch.float64)
+        if dist:
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e = dict(value=world * tokens * len(times) / float(tt.item()), unit="tokens/s",
+                   h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h,
+                   path="pinned host q,k,v,dO -> gla chunk_fwd + chunk_bwd -> host d_aug")
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, dt = oracle_sample(args.cpu_seqs)
+        cpu = dict(value=rate, unit="tokens/s", cores=os.cpu_count() or 1, kind="oracle",
+                   sample=f"fp64 oracle fwd+bwd over {args.cpu_seqs} of the 32 sequences "
+                          f"(T=2048, H=16) = {args.cpu_seqs * T} tokens, {dt:.1f} s")
+
+    clocks = clk.summary()
+    line = dict(
+        metric=METRIC, value=value, unit="tokens/s", n_gpus=world, steps=args.steps,
+        warmup=args.warmup, ms_per_step=tot_t, higher_is_better=True, scaling="weak",
+        vs_baseline=None, dtype="f16-mma/f32-acc (bf16 in, fp32 out); decode f32",
+        data="synthetic (seeded Gaussians with the workloads' shapes and scales)",
+        config=dict(workload=WORKLOAD, B=B, T=T, H=H, dk=DK, dv=DV, chunk=128,
+                    decode_pool=[N_SEQ, N_LAYERS, H, DK, DV], parallelism=f"replicas x{world}",
+                    l2="inputs larger than L2 (1.2 GB chunk inputs, 36 GB state pool); no flush"),
+        roofline=roofline,
+        decode=dict(value=dec_gbs, unit="GB/s", ms_per_step=dec_t, states=n_states,
+                    frac_of_hbm=dec_gbs / pk["hbm"], peak_source=pk["src"]),
+        parts_ms=dict(chunk_fwd=fwd_t, chunk_bwd=bwd_t, decode=dec_t),
+        roofline_chunk_fwd=roof_fwd, roofline_chunk_bwd=roof_bwd,
+        cpu_baseline=cpu, e2e=e2e, gpu_launches=gpu_launches_per_step * args.steps,
+        gpu_launches_detail="per step: chunk fwd, chunk bwd, d_aug reduction, decode",
+        clocks=clocks, wall_s_timed=t_wall,
+    )
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seqs", type=int, default=8)
+    ap.add_argument("--part", choices=["all", "fwd", "bwd", "decode"], default="all",
+                    help="time one call alone (smaller profiling cases); the default is the "
+                         "whole hot path")
+    ap.add_argument("--batch", type=int, default=B, help="sequences of the training shape")
+    ap.add_argument("--n-seq", type=int, default=N_SEQ, help="sequences of the serving pool")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.part != "all" or args.batch != B or args.n_seq != N_SEQ:
+        args.no_e2e = True
+        args.no_cpu_baseline = True
+    if args.gpus > 1 and world == 1:
+        print("bench.py: for --gpus N > 1 launch with torch.distributed.run (one rank per GPU)",
+              file=sys.stderr)
+        return 2
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    return run_gpu(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
