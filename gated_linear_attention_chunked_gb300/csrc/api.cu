@@ -47,6 +47,14 @@ size_t half_copy_bytes(int B, int T, int H, bool with_dO) {
 
 }  // namespace
 
+namespace gla {
+cudaError_t current_device_ctl(DevCtl* ctl) {
+  cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void**>(&ctl->err), g_device_error);
+  ctl->wait_ns = g_wait_ns.load();
+  return e;
+}
+}  // namespace gla
+
 extern "C" {
 
 const char* gla_status_string(gla_status s) {

@@ -53,6 +53,9 @@ struct BwdArgs {
   int B, T, H;
 };
 size_t chunk_bwd_workspace_bytes(int B, int T, int H);
+
+// The device error word and wait limit of the current device (defined in api.cu).
+cudaError_t current_device_ctl(DevCtl* ctl);
 cudaError_t launch_chunk_bwd(const BwdArgs& a, DevCtl ctl, cudaStream_t stream);
 
 }  // namespace gla

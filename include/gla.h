@@ -148,6 +148,37 @@ GLA_API gla_status gla_chunk_bwd(const void* q, const void* k, const void* v, gl
                          int dk_, int dv_, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Chunked backward that allocates nothing and takes no workspace.
+ *
+ * The article has no counterpart to this call; it exists for callers that cannot give the
+ * library a device buffer: code running inside an engine's or plugin's execution callback
+ * where device allocation is not allowed, processes whose device memory is reserved in full
+ * up front, and latency-critical loops that must avoid cudaMalloc / cudaFree (which can
+ * synchronise the whole device).  It computes exactly what gla_chunk_bwd computes, with the
+ * same arguments minus the workspace, by running the same kernels; its only scratch -- the
+ * per-(b, h) partial sums of d_aug -- is a fixed array of GLA_NOALLOC_MAX_BH x 96 floats
+ * (768 KiB) inside the library, held by every GPU that loads the library until exit.
+ *  - Sizes: B * H must be <= GLA_NOALLOC_MAX_BH, else GLA_ERR_WORKSPACE (nothing launched).
+ *    Inputs must be GLA_BF16 or GLA_FP16 (fp32 inputs need a workspace for their fp16
+ *    copies): GLA_ERR_UNSUPPORTED otherwise.  Other checks and errors as gla_chunk_bwd;
+ *    device errors go to the same error word (gla_get_device_error()).
+ *  - The first call on each device looks up the array's device address (cudaGetSymbolAddress,
+ *    which may load the module); make that first call before any stream capture.
+ *  - Every call on a device shares the one array, and a call leaves its partial sums in it.
+ *    Each call overwrites every entry it later reads, so nothing needs clearing, but calls
+ *    that overlap on the GPU (in flight at once, e.g. on two streams) race on the array:
+ *    order them on one stream or with events.
+ */
+#define GLA_NOALLOC_MAX_BH 2048
+GLA_API gla_status gla_chunk_bwd_noalloc(const void* q, const void* k, const void* v,
+                                         gla_dtype in_dtype, const float* log_decay,
+                                         const float* aug_balance, const float* init_state,
+                                         const void* dO, const float* d_final_state, float* dq,
+                                         float* dk, float* dv, float* d_aug,
+                                         float* d_init_state, int B, int T, int H, int dk_,
+                                         int dv_, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
  * One recurrent decode step for a pool of N sequences x L layers x H heads
  * ("Inference optimization on Trainium2": a fixed state per sequence, read
  * and written in the serving pool, O(1) per token).  In place, fp32:
