@@ -14,16 +14,18 @@
 // (or adjoint) kept on chip, so no role waits for another:
 //   role DQ  forward order : score dP = dO V^T, out dq = dP'' K + dO'' S^T, state S += K^T V'
 //   role DV  reverse order : score P^T = K Q^T, out dv = P''^T dO + K' dS,  adjoint dS += Q''^T dO
+//                            (sigmoid(z) dO enters through the diagonal of P''^T)
 //   role DK  reverse order : score dP^T = V dO^T, out dk = dP''^T Q + V' dS^T, adjoint dS += Q^T dO''
 // (X'' denotes an fp16 copy of X scaled by its decay factors; scores are masked with D and
 // scaled by 2^-e in fp32 before their fp16 copy.)  Warp layout as in the forward:
 //   warp 12 TMA producer (single stage: q, k, v, dO tiles of one chunk, L2 prefetch of the next),
 //   warp 13 tcgen05 issuer + TMEM owner (D_X [0,192) output, D_S [192,384) state,
 //           D_P [384,512) score),
-//   warps 0..3 convert group (row = token = TMEM lane): gate scalars, in-place fp16 operands,
-//           masked score copy;
-//   warps 4..11 emit group (two warps per row quadrant, split columns): the next state copy
-//           (the serial step, first), then the output rows, TMA-stored from staging.
+//   warps 0..11 epilogue, three warps per row quadrant (row = token = TMEM lane), each with a
+//           third of the row: gate dot products, in-place fp16 operands, then (part 0) the
+//           masked score copy written back into TMEM as an MMA operand; after the MMAs, the
+//           release of the tiles, the next state copy (the serial step) and the output rows,
+//           TMA-stored from per-warp staging.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -41,25 +43,24 @@ enum Role : int { R_DQ = 0, R_DV = 1, R_DK = 2 };
 
 constexpr uint32_t Q_BOX = 8192, V_BOX = 16384;
 constexpr uint32_t OFF_Q = 0, OFF_K = 3 * Q_BOX, OFF_V = 6 * Q_BOX, OFF_G = OFF_V + 3 * V_BOX;
-constexpr uint32_t OFF_SC = OFF_G + 3 * V_BOX;  // masked score copy, 2 atoms x 16 KB
-constexpr uint32_t SC_ATOM = 16384;
-constexpr uint32_t OFF_CP = OFF_SC + 2 * SC_ATOM;  // state copy, 3 atoms x 12 KB
+constexpr uint32_t OFF_STG = OFF_G + 3 * V_BOX;  // output staging, 12 warps x 2 KB
+constexpr uint32_t OFF_CP = OFF_STG + 12 * 2048;  // state copy, 3 atoms x 12 KB
 constexpr uint32_t S_ATOM = 12288;
 constexpr uint32_t OFF_BAR = OFF_CP + 3 * S_ATOM;
 constexpr uint32_t NBAR = 16;
 constexpr uint32_t OFF_TMEM = OFF_BAR + NBAR * 8;
 constexpr uint32_t OFF_ABORT = OFF_TMEM + 4;
-constexpr uint32_t OFF_RED = OFF_TMEM + 16;  // float red[3][8]
-constexpr uint32_t OFF_ES = OFF_RED + 96;    // int es[2]
-constexpr uint32_t OFF_AB = OFF_ES + 16;     // float abmax[2][8]: state-MMA operand maxima
-constexpr uint32_t OFF_RS = OFF_AB + 64;     // float rs[2][128]: r (DQ, DK) or sigmoid (DV)
-constexpr uint32_t OFF_A = OFF_RS + 1024;    // float a[96]
+constexpr uint32_t OFF_RED = OFF_TMEM + 16;  // float red[3][12]: per-warp max|S|
+constexpr uint32_t OFF_ES = OFF_RED + 144;   // int es[2]
+constexpr uint32_t OFF_AB = OFF_ES + 16;     // float abmax[2][24]: state-MMA operand maxima
+constexpr uint32_t OFF_GP = OFF_AB + 192;    // float gate_part[3][2][128]: gate partial sums
+constexpr uint32_t OFF_A = OFF_GP + 3072;    // float a[96]
 constexpr uint32_t OFF_PW = OFF_A + 384;     // float pw[128]
 constexpr uint32_t SMEM_USED = OFF_PW + 512;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
-constexpr uint32_t TM_X = 0, TM_S = 192, TM_P = 384;
+constexpr uint32_t TM_X = 0, TM_A = 96, TM_S = 192, TM_P = 384;  // TM_A: d_a (DQ role)
 
 enum Bar : uint32_t {
   FULL = 0,
@@ -72,11 +73,12 @@ enum Bar : uint32_t {
   EP_S = 7,
   RED = 8,
   DRAIN = 9,
+  GX = 10,  // the gate partial sums of every part are in shared memory
 };
 
 constexpr int THREADS = 448;
 constexpr int PRODUCER_WARP = 12, MMA_WARP = 13;
-constexpr int EMIT_THREADS = 256;
+constexpr int EPI_THREADS = 384;  // warps 0..11
 
 struct BwdParams {
   const float* log_decay;
@@ -132,7 +134,7 @@ __device__ __forceinline__ void run_role(
   float* red = (float*)(base + OFF_RED);
   int* es = (int*)(base + OFF_ES);
   float* abmax = (float*)(base + OFF_AB);
-  float* rs = (float*)(base + OFF_RS);
+  float* gate_part = (float*)(base + OFF_GP);
   float* sa = (float*)(base + OFF_A);
   uint32_t* tmem_slot = (uint32_t*)(base + OFF_TMEM);
 
@@ -142,15 +144,16 @@ __device__ __forceinline__ void run_role(
   }
   if (tid == PRODUCER_WARP * 32) {
     mbar_init(cta.bar(FULL), 1);
-    mbar_init(cta.bar(EMPTY), 1 + EMIT_THREADS);
+    mbar_init(cta.bar(EMPTY), 1 + EPI_THREADS);
     mbar_init(cta.bar(P_DONE), 1);
     mbar_init(cta.bar(X_DONE), 1);
     mbar_init(cta.bar(S_DONE), 1);
     mbar_init(cta.bar(DRAIN), 1);
-    mbar_init(cta.bar(EP_CONV), 128);
-    mbar_init(cta.bar(EP_X), EMIT_THREADS);
-    mbar_init(cta.bar(EP_S), EMIT_THREADS);
-    mbar_init(cta.bar(RED), EMIT_THREADS);
+    mbar_init(cta.bar(EP_CONV), EPI_THREADS);
+    mbar_init(cta.bar(EP_X), EPI_THREADS);
+    mbar_init(cta.bar(EP_S), EPI_THREADS);
+    mbar_init(cta.bar(RED), EPI_THREADS);
+    mbar_init(cta.bar(GX), EPI_THREADS);
     *cta.abort_flag() = 0;
     fence_barrier_init();
   }
@@ -225,7 +228,7 @@ __device__ __forceinline__ void run_role(
         if (!wait(cta, cta.bar(EP_S), par, ctl)) break;
         if (t >= 1 && !wait(cta, cta.bar(EP_X), (t - 1) & 1, ctl)) break;
         tc_fence_after();
-        const uint32_t SC = sb + OFF_SC, CP = sb + OFF_CP;
+        const uint32_t CP = sb + OFF_CP;
         if constexpr (ROLE == R_DQ) {
           // dq = dO'' S^T  (A = dO'' K-major, K = dv; B = state copy as [dk rows][dv], K-major)
           constexpr uint32_t ID1 = idesc_f16(128, 96, false, false, false, false);
@@ -235,18 +238,18 @@ __device__ __forceinline__ void run_role(
                        smem_desc(sb + OFF_G + (ks >> 2) * V_BOX + (ks & 3) * 32, 16, 1024, SW_128),
                        smem_desc(CP + (ks >> 2) * S_ATOM + (ks & 3) * 32, 16, 1024, SW_128), ID1,
                        ks > 0);
-          //    + dP'' K  (A = dP'' K-major, K = j; B = K as [j][dk], MN-major)
+          //    + dP'' K  (A = dP'' from TMEM, K = j; B = K as [j][dk], MN-major)
           constexpr uint32_t ID2 = idesc_f16(128, 96, false, false, false, true);
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
-            mma_f16_ss(tmem + TM_X, smem_desc(SC + (ks >> 2) * SC_ATOM + (ks & 3) * 32, 16, 1024, SW_128),
+            mma_f16_ts(tmem + TM_X, tmem + TM_P + 8 * ks,
                        smem_desc(sb + OFF_K + ks * 1024, Q_BOX, 512, SW_64), ID2, 1);
         } else if constexpr (ROLE == R_DV) {
-          // dv = P''^T dO  (A = P''^T K-major, K = i; B = dO as [i][dv], MN-major)
+          // dv = P''^T dO  (A = P''^T from TMEM, K = i; B = dO as [i][dv], MN-major)
           constexpr uint32_t ID1 = idesc_f16(128, 192, false, false, false, true);
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
-            mma_f16_ss(tmem + TM_X, smem_desc(SC + (ks >> 2) * SC_ATOM + (ks & 3) * 32, 16, 1024, SW_128),
+            mma_f16_ts(tmem + TM_X, tmem + TM_P + 8 * ks,
                        smem_desc(sb + OFF_G + ks * 2048, V_BOX, 1024, SW_128), ID1, ks > 0);
           //    + K' dS  (A = K' K-major, K = dk; B = adjoint copy [dk][dv], MN-major)
 #pragma unroll
@@ -255,11 +258,11 @@ __device__ __forceinline__ void run_role(
                        smem_desc(sb + OFF_K + (ks >> 1) * Q_BOX + (ks & 1) * 32, 16, 512, SW_64),
                        smem_desc(CP + ks * 2048, S_ATOM, 1024, SW_128), ID1, 1);
         } else {
-          // dk = dP''^T Q  (A = dP''^T K-major, K = i; B = Q as [i][dk], MN-major)
+          // dk = dP''^T Q  (A = dP''^T from TMEM, K = i; B = Q as [i][dk], MN-major)
           constexpr uint32_t ID1 = idesc_f16(128, 96, false, false, false, true);
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
-            mma_f16_ss(tmem + TM_X, smem_desc(SC + (ks >> 2) * SC_ATOM + (ks & 3) * 32, 16, 1024, SW_128),
+            mma_f16_ts(tmem + TM_X, tmem + TM_P + 8 * ks,
                        smem_desc(sb + OFF_Q + ks * 1024, Q_BOX, 512, SW_64), ID1, ks > 0);
           //    + V' dS^T  (A = V' K-major, K = dv; B = adjoint copy [dk][dv], K-major)
           constexpr uint32_t ID2 = idesc_f16(128, 96, false, false, false, false);
@@ -280,157 +283,49 @@ __device__ __forceinline__ void run_role(
             mma_f16_ss(tmem + TM_S, smem_desc(A + ks * 1024, Q_BOX, 512, SW_64),
                        smem_desc(B + ks * 2048, V_BOX, 1024, SW_128), ID, 1);
         }
+        if constexpr (ROLE == R_DQ) {
+          // d_a: diag((r q)^T k) accumulated over every chunk (A = r q as [i][dk] MN-major,
+          // B = K as [i][dk] MN-major); rows 96..127 are padding
+          constexpr uint32_t ID = idesc_f16(128, 96, false, false, true, true);
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            mma_f16_ss(tmem + TM_A, smem_desc(sb + OFF_Q + ks * 1024, Q_BOX, 512, SW_64),
+                       smem_desc(sb + OFF_K + ks * 1024, Q_BOX, 512, SW_64), ID, (t > 0 || ks > 0));
+        }
         mma_commit(cta.bar(S_DONE));
         mma_commit(cta.bar(EMPTY));
       }
       mma_commit(cta.bar(DRAIN));
       mbar_wait(cta.bar(DRAIN), 0, ctl, DRAIN_NS);
     }
-  } else if (warp < 4) {
-    // ------------------------------------------------------------------ convert group
-    const int i = tid;  // tile row (token) == TMEM lane
-    const uint32_t trow = tmem + ((uint32_t)(32 * warp) << 16);
+  } else {
+    // ------------------------------------------------------------------ epilogue warps 0..11
+    // Warp w serves rows 32q..32q+31 (q = w & 3, one row per thread = TMEM lane) and part
+    // sub = w >> 2 (0..2) of the work on each row: a third of the channels for the gate dot
+    // products and the in-place conversions, a third of the columns of the state copy and of
+    // the output rows.  The masked score copy (TMEM, in place) is done by part 0.
+    const int q4 = warp & 3, sub = warp >> 2;
+    const int i = 32 * q4 + lane;
+    const uint32_t trow = tmem + ((uint32_t)(32 * q4) << 16);
     const float lam = pw[1], lamC = expf((float)C * gamma);
     const float lq = (i + 1 < C) ? pw[i + 1] : lamC;  // lambda^(row+1)
     const float lk = pw[C - 1 - i];                   // lambda^(C-1-row)
+    uint8_t* const stage = base + OFF_STG + warp * 2048;  // this warp's output staging
+    auto qk = [&](int cc) { return qk_chunk(i, 4 * sub + cc); };  // this part's q/k chunks
+    auto vg = [&](int cc) { return vg_chunk(i, 8 * sub + cc); };  // this part's v/dO chunks
     float range_max = 0.f;
-    for (int t = 0; t < nc; ++t) {
-      const uint32_t par = t & 1;
-      if (!wait(cta, cta.bar(FULL), par, ctl)) break;
-      // gate scalars from the 16-bit inputs (read before any in-place conversion)
-      float z = 0.f, dov = 0.f;
-#pragma unroll 2
-      for (int cc = 0; cc < 12; ++cc) {
-        float q8[8], k8[8];
-        unpack8<BF16>(*(const uint4*)(base + OFF_Q + qk_chunk(i, cc)), q8);
-        unpack8<BF16>(*(const uint4*)(base + OFF_K + qk_chunk(i, cc)), k8);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) z = fmaf(sa[8 * cc + e] * q8[e], k8[e], z);
-      }
-      if constexpr (ROLE != R_DV) {
-#pragma unroll 2
-        for (int cc = 0; cc < 24; ++cc) {
-          float g8[8], v8[8];
-          unpack8<BF16>(*(const uint4*)(base + OFF_G + vg_chunk(i, cc)), g8);
-          unpack8<BF16>(*(const uint4*)(base + OFF_V + vg_chunk(i, cc)), v8);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) dov = fmaf(g8[e], v8[e], dov);
-        }
-      }
-      const float sg = sigmoid(z);
-      rs[par * 128 + i] = ROLE == R_DV ? sg : sg * (1.f - sg) * dov;
-      // the score MMA has read the 16-bit tiles: convert in place
-      if (!wait(cta, cta.bar(P_DONE), par, ctl)) break;
-      tc_fence_after();
-      float amax = 0.f, bmax = 0.f;  // operands of the state MMA
-      if constexpr (ROLE == R_DQ) {
-        for (int cc = 0; cc < 12; ++cc)  // K -> fp16 (A of the state MMA, B of dP'' K)
-          scale_chunk_to_half<BF16>((uint4*)(base + OFF_K + qk_chunk(i, cc)), 1.f, amax);
-        for (int cc = 0; cc < 24; ++cc)  // V' = lambda^(C-1-j) v (B of the state MMA)
-          scale_chunk_to_half<BF16>((uint4*)(base + OFF_V + vg_chunk(i, cc)), lk, bmax);
-        for (int cc = 0; cc < 24; ++cc)  // dO'' = lambda^(i+1) dO (A of dO'' S^T)
-          scale_chunk_to_half<BF16>((uint4*)(base + OFF_G + vg_chunk(i, cc)), lq, range_max);
-      } else if constexpr (ROLE == R_DV) {
-        for (int cc = 0; cc < 12; ++cc)  // Q'' = lambda^(j+1) q (A of the adjoint MMA)
-          scale_chunk_to_half<BF16>((uint4*)(base + OFF_Q + qk_chunk(i, cc)), lq, amax);
-        for (int cc = 0; cc < 12; ++cc)  // K' = lambda^(C-1-j) k (A of K' dS)
-          scale_chunk_to_half<BF16>((uint4*)(base + OFF_K + qk_chunk(i, cc)), lk, range_max);
-        for (int cc = 0; cc < 24; ++cc)  // dO -> fp16 (B of P''^T dO and of the adjoint MMA)
-          scale_chunk_to_half<BF16>((uint4*)(base + OFF_G + vg_chunk(i, cc)), 1.f, bmax);
-      } else {
-        for (int cc = 0; cc < 12; ++cc)  // Q -> fp16 (B of dP''^T Q, A of the adjoint MMA)
-          scale_chunk_to_half<BF16>((uint4*)(base + OFF_Q + qk_chunk(i, cc)), 1.f, amax);
-        for (int cc = 0; cc < 24; ++cc)  // V' = lambda^(C-1-j) v (A of V' dS^T)
-          scale_chunk_to_half<BF16>((uint4*)(base + OFF_V + vg_chunk(i, cc)), lk, range_max);
-        for (int cc = 0; cc < 24; ++cc)  // dO'' = lambda^(j+1) dO (B of the adjoint MMA)
-          scale_chunk_to_half<BF16>((uint4*)(base + OFF_G + vg_chunk(i, cc)), lq, bmax);
-      }
-      {
-        float am = amax, bm = bmax;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-          am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, off));
-          bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, off));
-        }
-        if (lane == 0) {
-          abmax[par * 8 + warp] = am;
-          abmax[par * 8 + 4 + warp] = bm;
-        }
-      }
-      range_max = fmaxf(range_max, fmaxf(amax, bmax));
-      // masked score copy, scaled by 2^-e of this step's state copy
-      if (!wait(cta, cta.bar(EP_S), par, ctl)) break;
-      const float psc = pow2i(-es[par]);
-      float pmax = 0.f;
-      {
-        uint32_t r[32];
-#pragma unroll 1
-        for (int jb = 0; jb < 4; ++jb) {
-          const int c0 = 32 * jb;
-          float sc[32];
-          // DQ (rows = queries i, columns j <= i) or DV/DK (rows = keys j, columns i >= j)
-          const bool live = ROLE == R_DQ ? jb <= warp : jb >= warp;
-          if (live) {
-            tmem_ld32(trow + TM_P + c0, r);
-            tmem_wait_ld();
-            if constexpr (ROLE == R_DQ) {
-              float f = pw[max(i - (c0 + 31), 0)] * psc;  // going left from min(i, c0+31)
-#pragma unroll
-              for (int u = 31; u >= 0; --u) {
-                const bool in = c0 + u <= i;
-                sc[u] = in ? __uint_as_float(r[u]) * f : 0.f;
-                f = in ? f * lam : f;
-                pmax = fmaxf(pmax, fabsf(sc[u]));
-              }
-            } else {
-              float f = pw[max(c0 - i, 0)] * psc;  // going right from max(j, c0)
-#pragma unroll
-              for (int u = 0; u < 32; ++u) {
-                const bool in = c0 + u >= i;
-                sc[u] = in ? __uint_as_float(r[u]) * f : 0.f;
-                f = in ? f * lam : f;
-                pmax = fmaxf(pmax, fabsf(sc[u]));
-              }
-            }
-          } else {
-#pragma unroll
-            for (int u = 0; u < 32; ++u) sc[u] = 0.f;
-          }
-#pragma unroll
-          for (int q8 = 0; q8 < 4; ++q8) {
-            uint4 pk;
-            pk.x = pack_h2(sc[8 * q8 + 0], sc[8 * q8 + 1]);
-            pk.y = pack_h2(sc[8 * q8 + 2], sc[8 * q8 + 3]);
-            pk.z = pack_h2(sc[8 * q8 + 4], sc[8 * q8 + 5]);
-            pk.w = pack_h2(sc[8 * q8 + 6], sc[8 * q8 + 7]);
-            *(uint4*)(base + OFF_SC + (jb >> 1) * SC_ATOM + swz_off(i, 4 * (jb & 1) + q8, 128)) = pk;
-          }
-        }
-      }
-      range_max = fmaxf(range_max, pmax);
-      fence_proxy_async();
-      tc_fence_before();
-      mbar_arrive(cta.bar(EP_CONV));
-    }
-    if (range_max >= 65504.f) record_error(ctl, DEV_RANGE);
-  } else if (warp < PRODUCER_WARP) {
-    // ------------------------------------------------------------------ emit group
-    const int q4 = warp & 3, hf = (warp - 4) >> 2, ew = warp - 4;
-    const int i = 32 * q4 + lane;
-    const uint32_t trow = tmem + ((uint32_t)(32 * q4) << 16);
-    const float lamC = expf((float)C * gamma);
-    uint8_t* const stage = base + OFF_V + ew * 4096;  // v region: free in every role by then
     bool bad = false;
-    float da_acc = 0.f;  // DQ: d_a of channel (tid - 128) < 96, summed over this CTA's rows
 
+    // state copy S * 2^-e (rows < 96, this part's 64 columns) into the copy buffer,
+    // D_S <- lambda^C S, and this warp's max|S| into red[use & 1]
     auto publish_state = [&](int use, int e, const float* g_row, bool from_tmem) {
       float m = 0.f;
       if (q4 < 3) {
         const float sc = pow2i(-e);
         float r[32];
 #pragma unroll 1
-        for (int nb = 0; nb < 3; ++nb) {
-          const int col = 96 * hf + 32 * nb;
+        for (int nb = 0; nb < 2; ++nb) {
+          const int col = 64 * sub + 32 * nb;
           if (from_tmem) {
             tmem_ld32(trow + TM_S + col, *reinterpret_cast<uint32_t(*)[32]>(r));
             tmem_wait_ld();
@@ -460,35 +355,35 @@ __device__ __forceinline__ void run_role(
       }
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-      if (lane == 0) red[(use & 1) * 8 + ew] = m;
-      if (tid == 128) es[use & 1] = e;
+      if (lane == 0) red[(use & 1) * 12 + warp] = m;
+      if (tid == 0) es[use & 1] = e;
       fence_proxy_async();
       tc_fence_before();
       mbar_arrive(cta.bar(EP_S));
     };
-    auto red_max = [&](int slot) {
-      float m = red[slot * 8];
+    auto max12 = [&](const float* v) {
+      float m = v[0];
 #pragma unroll
-      for (int w = 1; w < 8; ++w) m = fmaxf(m, red[slot * 8 + w]);
+      for (int w = 1; w < 12; ++w) m = fmaxf(m, v[w]);
       return m;
     };
 
-    // initial state (DQ) or adjoint of the final state (DV, DK)
+    // initial state (DQ) or adjoint of the final state (DV, DK): its exact max first
     const float* src0 = ROLE == R_DQ ? p.init : p.dfin;
     const float* g_row0 = (src0 && i < DK) ? src0 + ((size_t)bh * DK + i) * DV : nullptr;
     int e_cur = 0;
     {
       float m = 0.f;
       if (g_row0)
-        for (int j = 96 * hf; j < 96 * hf + 96; ++j) m = fmaxf(m, fabsf(__ldg(g_row0 + j)));
+        for (int j = 64 * sub; j < 64 * sub + 64; ++j) m = fmaxf(m, fabsf(__ldg(g_row0 + j)));
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-      if (lane == 0) red[16 + ew] = m;
+      if (lane == 0) red[24 + warp] = m;
       mbar_arrive(cta.bar(RED));
     }
     bool ok = wait(cta, cta.bar(RED), 0, ctl);
     if (ok) {
-      e_cur = state_exponent(red_max(2));
+      e_cur = state_exponent(max12(red + 24));
       if (e_cur < 0) {
         bad = true;
         e_cur = 0;
@@ -499,72 +394,159 @@ __device__ __forceinline__ void run_role(
     for (int t = 0; t < nc && ok; ++t) {
       const uint32_t par = t & 1;
       const int c = chunk_at<ROLE>(t, nc);
+      if (!(ok = wait(cta, cta.bar(FULL), par, ctl))) break;
+      // ---- gate scalars from the 16-bit inputs, in three parts per row
+      {
+        const float zp = dot_rows<BF16, 4, true>(base + OFF_Q, qk, base + OFF_K, qk, sa + 32 * sub);
+        float dp = 0.f;
+        if constexpr (ROLE != R_DV) dp = dot_rows<BF16, 8, false>(base + OFF_G, vg, base + OFF_V, vg, nullptr);
+        gate_part[sub * 256 + i] = zp;
+        gate_part[sub * 256 + 128 + i] = dp;
+        mbar_arrive(cta.bar(GX));
+      }
+      if (!(ok = wait(cta, cta.bar(GX), par, ctl))) break;
+      const float z = gate_part[i] + gate_part[256 + i] + gate_part[512 + i];
+      const float dov = gate_part[128 + i] + gate_part[384 + i] + gate_part[640 + i];
+      const float sg = sigmoid(z);
+      const float rr = sg * (1.f - sg) * dov;  // r (DQ, DK)
+      // ---- in-place fp16 operands, once the score MMA has read the 16-bit tiles
+      if (!(ok = wait(cta, cta.bar(P_DONE), par, ctl))) break;
+      tc_fence_after();
+      float amax = 0.f, bmax = 0.f;  // A and B operands of the state MMA
+      if constexpr (ROLE == R_DQ) {
+        convert_row<BF16, 4>(base + OFF_K, qk, 1.f, amax);      // K -> fp16 (state A, dP''K B)
+        convert_row<BF16, 8>(base + OFF_V, vg, lk, bmax);       // V' (state B)
+        convert_row<BF16, 8>(base + OFF_G, vg, lq, range_max);  // dO'' (A of dO'' S^T)
+      } else if constexpr (ROLE == R_DV) {
+        convert_row<BF16, 4>(base + OFF_Q, qk, lq, amax);       // Q'' (adjoint A)
+        convert_row<BF16, 4>(base + OFF_K, qk, lk, range_max);  // K' (A of K' dS)
+        convert_row<BF16, 8>(base + OFF_G, vg, 1.f, bmax);      // dO (adjoint B, P''^T dO B)
+      } else {
+        convert_row<BF16, 4>(base + OFF_Q, qk, 1.f, amax);      // Q (adjoint A, dP''^T Q B)
+        convert_row<BF16, 8>(base + OFF_V, vg, lk, range_max);  // V' (A of V' dS^T)
+        convert_row<BF16, 8>(base + OFF_G, vg, lq, bmax);       // dO'' (adjoint B)
+      }
+      range_max = fmaxf(range_max, fmaxf(amax, bmax));
+      {
+        float am = amax, bm = bmax;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+          am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, off));
+          bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, off));
+        }
+        if (lane == 0) {
+          abmax[par * 24 + warp] = am;
+          abmax[par * 24 + 12 + warp] = bm;
+        }
+      }
+      // ---- masked score copy (part 0), scaled by 2^-e of this step's state copy
+      if (sub == 0) {
+        if (!(ok = wait(cta, cta.bar(EP_S), par, ctl))) break;
+        const float psc = pow2i(-es[par]);
+        float pmax = 0.f;
+        uint32_t r[32];
+#pragma unroll 1
+        for (int jb = 0; jb < 4; ++jb) {
+          const int c0 = 32 * jb;
+          float sc[32];
+          // DQ (rows = queries i, columns j <= i) or DV/DK (rows = keys j, columns i >= j)
+          const bool live = ROLE == R_DQ ? jb <= q4 : jb >= q4;
+          if (live) {
+            tmem_ld32(trow + TM_P + c0, r);
+            tmem_wait_ld();
+            if constexpr (ROLE == R_DQ) {
+              float f = pw[max(i - (c0 + 31), 0)] * psc;  // going left from min(i, c0+31)
+#pragma unroll
+              for (int u = 31; u >= 0; --u) {
+                const bool in = c0 + u <= i;
+                sc[u] = in ? __uint_as_float(r[u]) * f : 0.f;
+                f = in ? f * lam : f;
+                pmax = fmaxf(pmax, fabsf(sc[u]));
+              }
+            } else {
+              float f = pw[max(c0 - i, 0)] * psc;  // going right from max(j, c0)
+#pragma unroll
+              for (int u = 0; u < 32; ++u) {
+                const bool in = c0 + u >= i;
+                sc[u] = in ? __uint_as_float(r[u]) * f : 0.f;
+                f = in ? f * lam : f;
+                // DV: the self-augmentation sigmoid(z_j) dO_j rides on the diagonal, so that
+                // P''^T dO includes it: (P^T + diag(sigmoid(z))) 2^-e
+                if (ROLE == R_DV && jb == q4 && u == lane) sc[u] += sg * psc;
+                pmax = fmaxf(pmax, fabsf(sc[u]));
+              }
+            }
+          } else {
+#pragma unroll
+            for (int u = 0; u < 32; ++u) sc[u] = 0.f;
+          }
+          // fp16 pairs, in place over the fp32 scores: this block's 16 packed columns land on
+          // fp32 columns 16jb..16jb+15, which blocks <= jb have already read
+          uint32_t pk[16];
+#pragma unroll
+          for (int u = 0; u < 16; ++u) pk[u] = pack_h2(sc[2 * u], sc[2 * u + 1]);
+          tmem_st16(trow + TM_P + 16 * jb, pk);
+        }
+        tmem_wait_st();
+        range_max = fmaxf(range_max, pmax);
+      }
+      if constexpr (ROLE == R_DQ) {  // r q for the d_a MMA (after the gate: it read q)
+        convert_row<BF16, 4>(base + OFF_Q, qk, rr, range_max);
+      }
+      fence_proxy_async();
+      tc_fence_before();
+      mbar_arrive(cta.bar(EP_CONV));
+
+      // ---- the MMAs of this step ran: take the self-augmentation operand (DQ: k, DK: q,
+      // this part's 32 channels) and release the tiles -- the next chunk's loads overlap the
+      // rest of this step.  DV's self-augmentation is inside D_X already.
       if (!(ok = wait(cta, cta.bar(X_DONE), par, ctl))) break;
       if (!(ok = wait(cta, cta.bar(S_DONE), par, ctl))) break;
-      if (!(ok = wait(cta, cta.bar(EP_CONV), par, ctl))) break;
       tc_fence_after();
+      uint4 vv[4];
+      if constexpr (ROLE != R_DV) {
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) vv[ch] = *(const uint4*)(base + (ROLE == R_DQ ? OFF_K : OFF_Q) + qk(ch));
+      }
+      mbar_arrive(cta.bar(EMPTY));
       int e_next = e_cur;
       if (t < nc - 1) {
+        // bound on the next state: all parts' operand maxima and max|S| of this step's copy
+        if (!(ok = wait(cta, cta.bar(EP_CONV), par, ctl))) break;
         if (!(ok = wait(cta, cta.bar(EP_S), par, ctl))) break;
-        const float ms = red_max(par);
-        const float am = fmaxf(fmaxf(abmax[par * 8 + 0], abmax[par * 8 + 1]),
-                               fmaxf(abmax[par * 8 + 2], abmax[par * 8 + 3]));
-        const float bm = fmaxf(fmaxf(abmax[par * 8 + 4], abmax[par * 8 + 5]),
-                               fmaxf(abmax[par * 8 + 6], abmax[par * 8 + 7]));
-        e_next = state_exponent(lamC * ms + (float)C * am * bm);
+        e_next = state_exponent(lamC * max12(red + par * 12) +
+                                (float)C * max12(abmax + par * 24) * max12(abmax + par * 24 + 12));
         if (e_next < 0) {
           bad = true;
           e_next = 0;
         }
         publish_state(t + 1, e_next, nullptr, true);
       }
-      // ---- d_a (DQ): channel d of the emit thread, summed over this chunk's rows
-      if constexpr (ROLE == R_DQ) {
-        const int d = tid - 128;
-        if (d < DK) {
-          const uint32_t off = (d >> 5) * Q_BOX + 2 * (d & 7);
-          float acc = 0.f;
-#pragma unroll 4
-          for (int rr = 0; rr < C; ++rr) {
-            const uint32_t o = off + swz_off(rr, (d & 31) >> 3, 64);
-            const float qv = ld16<BF16>(*(const uint16_t*)(base + OFF_Q + o));
-            const float kv = __half2float(*(const __half*)(base + OFF_K + o));
-            acc = fmaf(rs[par * 128 + rr] * qv, kv, acc);
-          }
-          da_acc += acc;
-        }
-      }
-      // ---- output rows: x = 2^e D_X + (self-augmentation term), TMA-stored
+      // ---- output rows, this part's columns: x = 2^e D_X (+ r (a * k|q) for DQ, DK)
       {
-        const float g = rs[par * 128 + i];  // r (DQ, DK) or sigmoid(z) (DV)
         const float osc = pow2i(e_cur);
         const int row = b * T + c * C + 32 * q4;
-        constexpr int NB = NX / 32;  // 16-column blocks of this warp's half
-        emit_rows_tma<NB>(
+        constexpr int NCOL = NX / 3;  // 32 (DQ, DK) or 64 (DV)
+        emit_rows_tma1<NCOL / 16>(
             stage, lane,
             [&](int k, float (&x)[16]) {
-              const int col = (NX / 2) * hf + 16 * k;
+              const int col = NCOL * sub + 16 * k;
               uint32_t r[16];
               tmem_ld16(trow + TM_X + col, r);
               tmem_wait_ld();
-              // self-augmentation operand of row i, columns col..col+15 (fp16 tiles)
-              float f8[2][8];
-              if constexpr (ROLE == R_DV) {  // sigmoid(z) dO
-                unpack8<false>(*(const uint4*)(base + OFF_G + vg_chunk(i, col / 8)), f8[0]);
-                unpack8<false>(*(const uint4*)(base + OFF_G + vg_chunk(i, col / 8 + 1)), f8[1]);
+              if constexpr (ROLE == R_DV) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) x[j] = __uint_as_float(r[j]) * osc;
+              } else {
+                float f8[2][8];
+                unpack8<false>(vv[2 * k], f8[0]);
+                unpack8<false>(vv[2 * k + 1], f8[1]);
 #pragma unroll
                 for (int j = 0; j < 16; ++j)
-                  x[j] = fmaf(__uint_as_float(r[j]), osc, g * f8[j >> 3][j & 7]);
-              } else {  // r (a * k) (DQ) or r (a * q) (DK)
-                constexpr uint32_t SRC = ROLE == R_DQ ? OFF_K : OFF_Q;
-                unpack8<false>(*(const uint4*)(base + SRC + qk_chunk(i, col / 8)), f8[0]);
-                unpack8<false>(*(const uint4*)(base + SRC + qk_chunk(i, col / 8 + 1)), f8[1]);
-#pragma unroll
-                for (int j = 0; j < 16; ++j)
-                  x[j] = fmaf(__uint_as_float(r[j]), osc, g * sa[col + j] * f8[j >> 3][j & 7]);
+                  x[j] = fmaf(__uint_as_float(r[j]), osc, rr * sa[col + j] * f8[j >> 3][j & 7]);
               }
             },
-            [&](int k, uint32_t src) { tma_store_3d(&map_out, src, (NX / 2) * hf + 16 * k, h, row); });
+            [&](int k, uint32_t src) { tma_store_3d(&map_out, src, NCOL * sub + 16 * k, h, row); });
       }
       tc_fence_before();
       mbar_arrive(cta.bar(EP_X));
@@ -572,26 +554,36 @@ __device__ __forceinline__ void run_role(
       if (ROLE == R_DV && t == nc - 1 && p.want_dinit && q4 < 3) {
         if (lane == 0) bulk_wait_read<0>();
         __syncwarp();
-        emit_rows_tma<6>(
+        emit_rows_tma1<4>(
             stage, lane,
             [&](int k, float (&f)[16]) {
               uint32_t r[16];
-              tmem_ld16(trow + TM_S + 96 * hf + 16 * k, r);
+              tmem_ld16(trow + TM_S + 64 * sub + 16 * k, r);
               tmem_wait_ld();
 #pragma unroll
               for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(r[j]);
             },
-            [&](int k, uint32_t src) { tma_store_3d(&map_dinit, src, 96 * hf + 16 * k, 32 * q4, bh); });
+            [&](int k, uint32_t src) { tma_store_3d(&map_dinit, src, 64 * sub + 16 * k, 32 * q4, bh); });
       }
-      if (lane == 0) bulk_wait_read<0>();
+      if (lane == 0) bulk_wait_read<0>();  // the staging buffer is free for the next step
       __syncwarp();
-      mbar_arrive(cta.bar(EMPTY));
       e_cur = e_next;
     }
-    if (ROLE == R_DQ && tid - 128 < DK) p.da_part[(size_t)bh * DK + (tid - 128)] = da_acc;
+    // DQ: d_a of this (b, h) is the diagonal of the accumulated (r q)^T k; row d (lane of
+    // quadrant d / 32) takes column d
+    if (ROLE == R_DQ && ok && sub == 0 && q4 < 3) {
+      tc_fence_after();
+      uint32_t r[32];
+      tmem_ld32(trow + TM_A + 32 * q4, r);
+      tmem_wait_ld();
+      float dd = 0.f;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) dd = (j == lane) ? __uint_as_float(r[j]) : dd;
+      p.da_part[(size_t)bh * DK + 32 * q4 + lane] = dd;
+    }
     if (lane == 0) bulk_wait_all();
     __syncwarp();
-    if (bad) record_error(ctl, DEV_RANGE);
+    if (bad || range_max >= 65504.f) record_error(ctl, DEV_RANGE);
   }
 
   tc_fence_before();

@@ -3,7 +3,7 @@
 // Method ("Beyond the KV cache ... Laplace 3B ...", section "Challenge 1", the chunked form
 // of the "GLA mixer" recurrence).  Per (b, h) and chunk c of C = 128 tokens, with
 // D_ij = lambda^(i-j) (i >= j, else 0), Lq = diag(lambda^(i+1)), Lk = diag(lambda^(C-1-j)):
-//   O_c     = (Q K^T o D) V + Lq Q S_c + sigmoid(z) v       (intra + inter + self-augmentation)
+//   O_c     = (Q K^T o D + diag(sigmoid(z))) V + Lq Q S_c   (intra + self-augmentation + inter)
 //   S_{c+1} = lambda^C S_c + K^T Lk V                        (the only serial step)
 //
 // One CTA owns one (b, h) and walks its chunks in order; the fp32 state never leaves the chip.
@@ -11,20 +11,22 @@
 //               (3 boxes of 64 channels, 128-byte swizzle) into a 2-stage ring, plus L2
 //               prefetch of the chunk after next.
 //   warp 13     tcgen05 issuer (one thread) and TMEM owner (512 columns):
-//                 D_P [384,512)  P = Q K^T                   (bf16/fp16 inputs as given)
+//                 D_P [384,512)  P = Q K^T (bf16/fp16 inputs as given); the masked fp16
+//                                copy P'' is written back in place (64 columns) and read
+//                                from TMEM as the A operand of P'' V
 //                 D_O [  0,192)  O = Q'' S_c + P'' V           (fp16 operands)
 //                 D_S [192,384)  S = lambda^C S + K'^T V       (fp16 operands, fp32 state;
 //                                rows 96..127 are padding and never read)
 //   warps 0..3  convert group, thread = token row i (= TMEM lane), one chunk ahead of the
 //               emit group: V -> fp16 in place; z = q.(a*k); Q'' = fp16(lambda^(i+1) q) and
-//               K' = fp16(lambda^(127-i) k) in place; P'' = fp16(mask(P) * 2^-e).
+//               K' = fp16(lambda^(127-i) k) in place; P'' = fp16((mask(P) + diag(sigmoid(z)))
+//               * 2^-e) into TMEM -- the self-augmentation rides on the diagonal of P''.
 //   warps 4..11 emit group, same rows, two warps per row quadrant splitting the value
 //               columns: (1) the serial step -- S -> fp16(S * 2^-e') into the drained q/k
-//               slot (B operand of the next Q'' S) and D_S <- lambda^C D_S; (2) o = 2^e D_O +
-//               sigmoid(z) v as fp32, TMA-stored from staging in the chunk's v tile (no
-//               longer read by then).
+//               slot (B operand of the next Q'' S) and D_S <- lambda^C D_S; (2) the output rows
+//               o = 2^e D_O as fp32, TMA-stored from per-warp staging.
 // fp16 operands (11-bit significand) keep the long-memory heads accurate; the state copy is
-// scaled by a power of two e' chosen from max|S| so it never overflows fp16.
+// scaled by a power of two e' chosen from a bound on max|S| so it never overflows fp16.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -42,18 +44,16 @@ constexpr uint32_t Q_BOX = 8192;    // 128 rows x 64 B (32 channels), SW64
 constexpr uint32_t V_BOX = 16384;   // 128 rows x 128 B (64 channels), SW128
 constexpr uint32_t OFF_Q = 0, OFF_K = 3 * Q_BOX, OFF_V = 6 * Q_BOX;
 constexpr uint32_t STAGE = OFF_V + 3 * V_BOX;  // 98304
-constexpr uint32_t OFF_P = 2 * STAGE;          // P'' 2 atoms x 16 KB (K-major SW128)
-constexpr uint32_t P_ATOM = 16384;
+constexpr uint32_t OFF_STG = 2 * STAGE;        // output staging, 8 emit warps x 4 KB
 constexpr uint32_t S_ATOM = 12288;             // state copy: 3 atoms of 96 rows x 128 B
-constexpr uint32_t OFF_BAR = OFF_P + 2 * P_ATOM;
+constexpr uint32_t OFF_BAR = OFF_STG + 8 * 4096;
 constexpr uint32_t NBAR = 24;
 constexpr uint32_t OFF_TMEM = OFF_BAR + NBAR * 8;
 constexpr uint32_t OFF_ABORT = OFF_TMEM + 4;
 constexpr uint32_t OFF_RED = OFF_TMEM + 16;     // float red[3][8]: per-warp max|S|
 constexpr uint32_t OFF_ES = OFF_RED + 96;       // int es[2]: state-copy exponent per chunk parity
 constexpr uint32_t OFF_KV = OFF_ES + 16;        // float kvmax[2][8]: per-warp max|K'|, max|V|
-constexpr uint32_t OFF_ZS = OFF_KV + 64;        // float zs[2][128]: gate dot products
-constexpr uint32_t OFF_A = OFF_ZS + 1024;       // float a[96]: aug_balance of the head
+constexpr uint32_t OFF_A = OFF_KV + 64;         // float a[96]: aug_balance of the head
 constexpr uint32_t OFF_PW = OFF_A + 384;        // float pw[128] = lambda^d
 constexpr uint32_t SMEM_USED = OFF_PW + 512;
 // The whole opt-in maximum is requested; the kernel aligns its base to 1024 bytes and
@@ -111,7 +111,6 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
   float* red = (float*)(base + OFF_RED);
   int* es = (int*)(base + OFF_ES);
   float* kvmax = (float*)(base + OFF_KV);
-  float* zs = (float*)(base + OFF_ZS);
   float* sa = (float*)(base + OFF_A);
   uint32_t* tmem_slot = (uint32_t*)(base + OFF_TMEM);
 
@@ -124,7 +123,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
       mbar_init(cta.bar(QK_FULL + s), 1);
       mbar_init(cta.bar(V_FULL + s), 1);
       mbar_init(cta.bar(QK_EMPTY + s), 1);
-      mbar_init(cta.bar(V_EMPTY + s), 1 + EMIT_THREADS);
+      mbar_init(cta.bar(V_EMPTY + s), 1);  // the MMAs are the only readers of v
     }
     mbar_init(cta.bar(P_DONE), 1);
     mbar_init(cta.bar(O_DONE), 1);
@@ -197,6 +196,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
         const uint32_t s = c & 1, st = cta.sb + s * STAGE;
         const uint32_t slot = cta.sb + (s ^ 1) * STAGE;  // state copy for this chunk
         if (!wait(cta, cta.bar(QK_FULL + s), (c >> 1) & 1, ctl)) break;
+        // P'' of the previous chunk lives in D_P's columns: P'' V must be done before Q K^T
+        // overwrites them
+        if (c >= 1 && !wait(cta, cta.bar(O_DONE), (c - 1) & 1, ctl)) break;
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 6; ++ks) {  // P = Q K^T
@@ -216,9 +218,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                      smem_desc(slot + ks * 2048, S_ATOM, 1024, SW_128), ID_QS, ks > 0);
         }
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {  // O += P'' V
-          mma_f16_ss(tmem + TM_O,
-                     smem_desc(cta.sb + OFF_P + (ks >> 2) * P_ATOM + (ks & 3) * 32, 16, 1024, SW_128),
+        for (int ks = 0; ks < 8; ++ks) {  // O += P'' V  (P'' from TMEM)
+          mma_f16_ts(tmem + TM_O, tmem + TM_P + 8 * ks,
                      smem_desc(st + OFF_V + ks * 2048, V_BOX, 1024, SW_128), ID_PV, 1);
         }
         mma_commit(cta.bar(O_DONE));
@@ -291,7 +292,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
         *(uint4*)(stg + OFF_Q + off) = qv;
         *(uint4*)(stg + OFF_K + off) = kv;
       }
-      zs[par * 128 + i] = z;
+      const float sg = sigmoid(z);
       // chunk maxima of |K'| and |V| (for the emit group's bound on the next state)
       {
         float km = kmax, vm = vmax;
@@ -325,24 +326,25 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
               const bool in = j0 + u <= i;
               p[u] = in ? __uint_as_float(r[u]) * f : 0.f;
               f = in ? f * lam : f;
+              // the self-augmentation sigmoid(z_i) v_i rides on the diagonal, so P'' V
+              // includes it: (P o D + diag(sigmoid(z))) 2^-e
+              if (jb == warp && u == lane) p[u] += sg * psc;
               pmax = fmaxf(pmax, fabsf(p[u]));
             }
           } else {
 #pragma unroll
             for (int u = 0; u < 32; ++u) p[u] = 0.f;
           }
+          // fp16 pairs, in place over the fp32 scores: this block's 16 packed columns land on
+          // fp32 columns 16jb..16jb+15, which blocks <= jb have already read
+          uint32_t pk[16];
 #pragma unroll
-          for (int q8 = 0; q8 < 4; ++q8) {
-            uint4 pk;
-            pk.x = pack_h2(p[8 * q8 + 0], p[8 * q8 + 1]);
-            pk.y = pack_h2(p[8 * q8 + 2], p[8 * q8 + 3]);
-            pk.z = pack_h2(p[8 * q8 + 4], p[8 * q8 + 5]);
-            pk.w = pack_h2(p[8 * q8 + 6], p[8 * q8 + 7]);
-            *(uint4*)(base + OFF_P + (jb >> 1) * P_ATOM + swz_off(i, 4 * (jb & 1) + q8, 128)) = pk;
-          }
+          for (int u = 0; u < 16; ++u) pk[u] = pack_h2(p[2 * u], p[2 * u + 1]);
+          tmem_st16(trow + TM_P + 16 * jb, pk);
         }
       }
       range_max = fmaxf(range_max, fmaxf(fmaxf(vmax, kmax), fmaxf(qmax, pmax)));
+      tmem_wait_st();
       fence_proxy_async();
       tc_fence_before();
       mbar_arrive(cta.bar(EP_CONV));
@@ -460,21 +462,12 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
         }
         publish_state(s * STAGE + OFF_Q, c + 1, e_next, nullptr, true);
       }
-      // ---- output rows: o = 2^e D_O + sigmoid(z) v for columns [96hf, 96hf+96), TMA-stored
-      // from this warp's rows of v box (hf ? 2 : 0), which no one reads any more once the
-      // values below are in registers
-      uint8_t* const stage_o = stg + OFF_V + (hf ? 2 : 0) * V_BOX + q4 * 4096;
+      // ---- output rows: o = 2^e D_O for columns [96hf, 96hf+96) (the self-augmentation
+      // sigmoid(z) v is already in D_O through the diagonal of P''), TMA-stored
+      uint8_t* const stage_o = base + OFF_STG + ew * 4096;
       {
-        const float sg = sigmoid(zs[par * 128 + i]);
         const float osc = pow2i(e_cur);
         const int row = b * T + c * C + 32 * q4;
-        uint4 vv[12];  // value channels 96hf .. 96hf+95 of row i (fp16)
-#pragma unroll
-        for (int ch = 0; ch < 12; ++ch) {
-          const int n = 96 * hf + 8 * ch;
-          vv[ch] = *(const uint4*)(stg + OFF_V + (n >> 6) * V_BOX + swz_off(i, (n & 63) >> 3, 128));
-        }
-        __syncwarp();
         emit_rows_tma<6>(
             stage_o, lane,
             [&](int k, float (&o)[16]) {
@@ -482,16 +475,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
               tmem_ld16(trow + TM_O + 96 * hf + 16 * k, r);
               tmem_wait_ld();
 #pragma unroll
-              for (int ch = 0; ch < 2; ++ch) {
-                const uint4 v4 = vv[2 * k + ch];
-                const uint32_t* vw = (const uint32_t*)&v4;
-#pragma unroll
-                for (int e2 = 0; e2 < 4; ++e2) {
-                  o[8 * ch + 2 * e2] = fmaf(__uint_as_float(r[8 * ch + 2 * e2]), osc, sg * h_lo(vw[e2]));
-                  o[8 * ch + 2 * e2 + 1] =
-                      fmaf(__uint_as_float(r[8 * ch + 2 * e2 + 1]), osc, sg * h_hi(vw[e2]));
-                }
-              }
+              for (int j = 0; j < 16; ++j) o[j] = __uint_as_float(r[j]) * osc;
             },
             [&](int k, uint32_t src) { tma_store_3d(&map_o, src, 96 * hf + 16 * k, h, row); });
       }
@@ -512,9 +496,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
             },
             [&](int k, uint32_t src) { tma_store_3d(&map_fin, src, 96 * hf + 16 * k, 32 * q4, bh); });
       }
-      if (lane == 0) bulk_wait_read<0>();  // the v tile is free for the next load
+      if (lane == 0) bulk_wait_read<0>();  // the staging buffers are free for the next chunk
       __syncwarp();
-      mbar_arrive(cta.bar(V_EMPTY + s));
       e_cur = e_next;
     }
     if (lane == 0) bulk_wait_all();

@@ -76,6 +76,68 @@ __device__ __forceinline__ void scale_chunk_to_half(uint4* p, float s, float& vm
   *p = x;
 }
 
+// Convert NCH 16-byte chunks of one tile row in place (scale s, to fp16), four chunks at a
+// time with their loads issued together so that the shared-memory latency overlaps.
+// `off(c)` is the byte offset of chunk c.
+template <bool SRC_BF16, int NCH, typename Off>
+__device__ __forceinline__ void convert_row(uint8_t* tile, Off off, float s, float& vmax) {
+  static_assert(NCH % 4 == 0, "chunks in groups of four");
+#pragma unroll
+  for (int c0 = 0; c0 < NCH; c0 += 4) {
+    uint4 x[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) x[u] = *(const uint4*)(tile + off(c0 + u));
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      uint32_t* w = reinterpret_cast<uint32_t*>(&x[u]);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float a = ld16<SRC_BF16>(w[e] & 0xFFFFu) * s, b = ld16<SRC_BF16>(w[e] >> 16) * s;
+        vmax = fmaxf(vmax, fmaxf(fabsf(a), fabsf(b)));
+        w[e] = pack_h2(a, b);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) *(uint4*)(tile + off(c0 + u)) = x[u];
+  }
+}
+
+// sum_e w_e x_e y_e over NCH 16-byte chunks of two rows of 16-bit data (w_e = wt[8c + e], or
+// 1 without weights), loading four chunks at a time and keeping four partial sums so that
+// neither the loads nor the multiply-adds form one long dependent chain.
+template <bool SRC_BF16, int NCH, bool WEIGHTED, typename OffX, typename OffY>
+__device__ __forceinline__ float dot_rows(const uint8_t* tx, OffX offx, const uint8_t* ty, OffY offy,
+                                          const float* wt) {
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int c0 = 0; c0 < NCH; c0 += 4) {
+    uint4 x[4], y[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      x[u] = *(const uint4*)(tx + offx(c0 + u));
+      y[u] = *(const uint4*)(ty + offy(c0 + u));
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const uint32_t* xw = reinterpret_cast<const uint32_t*>(&x[u]);
+      const uint32_t* yw = reinterpret_cast<const uint32_t*>(&y[u]);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int d = 8 * (c0 + u) + 2 * e;
+        float x0 = ld16<SRC_BF16>(xw[e] & 0xFFFFu), x1 = ld16<SRC_BF16>(xw[e] >> 16);
+        const float y0 = ld16<SRC_BF16>(yw[e] & 0xFFFFu), y1 = ld16<SRC_BF16>(yw[e] >> 16);
+        if constexpr (WEIGHTED) {
+          x0 *= wt[d];
+          x1 *= wt[d + 1];
+        }
+        acc[u] = fmaf(x0, y0, acc[u]);
+        acc[u] = fmaf(x1, y1, acc[u]);
+      }
+    }
+  }
+  return (acc[0] + acc[1]) + (acc[2] + acc[3]);
+}
+
 // Power-of-two exponent e >= 0 such that m * 2^-e < 2^14 (fp16 copy with headroom).
 // Returns -1 for a non-finite m.
 __device__ __forceinline__ int state_exponent(float m) {
@@ -137,6 +199,29 @@ __device__ __forceinline__ void emit_rows_tma(uint8_t* buf0, int lane, Produce p
     produce(k, r);
     if (k >= 2) {  // the store that last read this buffer must have finished reading it
       if (lane == 0) bulk_wait_read<1>();
+      __syncwarp();
+    }
+    stage_rows16_sw64(buf, r, lane);
+    fence_proxy_async();
+    __syncwarp();
+    if (lane == 0) {
+      store(k, smem_u32(buf));
+      bulk_commit();
+    }
+  }
+}
+
+// As emit_rows_tma, with a single 2 KB staging buffer (for callers short of shared memory):
+// before a block reuses the buffer, the previous block's TMA store must have read it.
+template <int NBLK16, typename Produce, typename Store>
+__device__ __forceinline__ void emit_rows_tma1(uint8_t* buf, int lane, Produce produce,
+                                               Store store) {
+#pragma unroll
+  for (int k = 0; k < NBLK16; ++k) {
+    float r[16];
+    produce(k, r);
+    if (k >= 1) {
+      if (lane == 0) bulk_wait_read<0>();
       __syncwarp();
     }
     stage_rows16_sw64(buf, r, lane);
