@@ -47,14 +47,15 @@ constexpr uint32_t OFF_STG = OFF_G + 3 * V_BOX;  // output staging, 12 warps x 2
 constexpr uint32_t OFF_CP = OFF_STG + 12 * 2048;  // state copy, 3 atoms x 12 KB
 constexpr uint32_t S_ATOM = 12288;
 constexpr uint32_t OFF_BAR = OFF_CP + 3 * S_ATOM;
-constexpr uint32_t NBAR = 16;
+constexpr uint32_t NBAR = 18;
 constexpr uint32_t OFF_TMEM = OFF_BAR + NBAR * 8;
 constexpr uint32_t OFF_ABORT = OFF_TMEM + 4;
 constexpr uint32_t OFF_RED = OFF_TMEM + 16;  // float red[3][12]: per-warp max|S|
 constexpr uint32_t OFF_ES = OFF_RED + 144;   // int es[2]
 constexpr uint32_t OFF_AB = OFF_ES + 16;     // float abmax[2][24]: state-MMA operand maxima
-constexpr uint32_t OFF_GP = OFF_AB + 192;    // float gate_part[3][2][128]: gate partial sums
-constexpr uint32_t OFF_A = OFF_GP + 3072;    // float a[96]
+constexpr uint32_t OFF_GP = OFF_AB + 192;    // float gate_part[3][128]: gate partial sums
+constexpr uint32_t OFF_DP = OFF_GP + 1536;   // float dpv[128]: dO.v per row (DQ, DK)
+constexpr uint32_t OFF_A = OFF_DP + 512;     // float a[96]
 constexpr uint32_t OFF_PW = OFF_A + 384;     // float pw[128]
 constexpr uint32_t SMEM_USED = OFF_PW + 512;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;
@@ -73,7 +74,8 @@ enum Bar : uint32_t {
   EP_S = 7,
   RED = 8,
   DRAIN = 9,
-  GX = 10,  // the gate partial sums of every part are in shared memory
+  QG0 = 10,  // 10..13: quadrant q's three gate partial sums are in shared memory
+  QS0 = 14,  // 14..17: quadrant q's three parts have read their score blocks
 };
 
 constexpr int THREADS = 448;
@@ -135,6 +137,7 @@ __device__ __forceinline__ void run_role(
   int* es = (int*)(base + OFF_ES);
   float* abmax = (float*)(base + OFF_AB);
   float* gate_part = (float*)(base + OFF_GP);
+  float* dpv = (float*)(base + OFF_DP);
   float* sa = (float*)(base + OFF_A);
   uint32_t* tmem_slot = (uint32_t*)(base + OFF_TMEM);
 
@@ -153,7 +156,10 @@ __device__ __forceinline__ void run_role(
     mbar_init(cta.bar(EP_X), EPI_THREADS);
     mbar_init(cta.bar(EP_S), EPI_THREADS);
     mbar_init(cta.bar(RED), EPI_THREADS);
-    mbar_init(cta.bar(GX), EPI_THREADS);
+    for (int q = 0; q < 4; ++q) {
+      mbar_init(cta.bar(QG0 + q), 96);
+      mbar_init(cta.bar(QS0 + q), 96);
+    }
     *cta.abort_flag() = 0;
     fence_barrier_init();
   }
@@ -391,38 +397,65 @@ __device__ __forceinline__ void run_role(
       publish_state(0, e_cur, g_row0, false);
     }
 
+    // in-register fp16 copy of four q/k chunks of this part (x: 16-bit input words), scaled
+    // by s and stored back in place
+    auto cvt4 = [&](uint4 (&x)[4], uint32_t tile_off, float s, float& vmax) {
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t* w = reinterpret_cast<uint32_t*>(&x[cc]);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float a0 = ld16<BF16>(w[e] & 0xFFFFu) * s, a1 = ld16<BF16>(w[e] >> 16) * s;
+          vmax = fmaxf(vmax, fmaxf(fabsf(a0), fabsf(a1)));
+          w[e] = pack_h2(a0, a1);
+        }
+        *(uint4*)(base + tile_off + qk(cc)) = x[cc];
+      }
+    };
+
     for (int t = 0; t < nc && ok; ++t) {
       const uint32_t par = t & 1;
       const int c = chunk_at<ROLE>(t, nc);
       if (!(ok = wait(cta, cta.bar(FULL), par, ctl))) break;
-      // ---- gate scalars from the 16-bit inputs, in three parts per row
+      // ---- gate partial sum z = q.(a*k) over this part's 32 channels, fused with the fp16
+      // copy of whichever of q, k the score MMA does not read (DQ: k, DK: q, both scale 1);
+      // DV's score reads both, so DV converts them once the score MMA is done
+      float amax = 0.f, bmax = 0.f;  // A and B operands of the state MMA
+      uint4 xq[4], xk[4];
       {
-        const float zp = dot_rows<BF16, 4, true>(base + OFF_Q, qk, base + OFF_K, qk, sa + 32 * sub);
-        float dp = 0.f;
-        if constexpr (ROLE != R_DV) dp = dot_rows<BF16, 8, false>(base + OFF_G, vg, base + OFF_V, vg, nullptr);
-        gate_part[sub * 256 + i] = zp;
-        gate_part[sub * 256 + 128 + i] = dp;
-        mbar_arrive(cta.bar(GX));
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          xq[cc] = *(const uint4*)(base + OFF_Q + qk(cc));
+          xk[cc] = *(const uint4*)(base + OFF_K + qk(cc));
+        }
+        float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          const uint32_t* xw = reinterpret_cast<const uint32_t*>(&xq[cc]);
+          const uint32_t* yw = reinterpret_cast<const uint32_t*>(&xk[cc]);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int d = 32 * sub + 8 * cc + 2 * e;
+            acc0 = fmaf(ld16<BF16>(xw[e] & 0xFFFFu) * sa[d], ld16<BF16>(yw[e] & 0xFFFFu), acc0);
+            acc1 = fmaf(ld16<BF16>(xw[e] >> 16) * sa[d + 1], ld16<BF16>(yw[e] >> 16), acc1);
+          }
+        }
+        gate_part[sub * 128 + i] = acc0 + acc1;
+        mbar_arrive(cta.bar(QG0 + q4));
       }
-      if (!(ok = wait(cta, cta.bar(GX), par, ctl))) break;
-      const float z = gate_part[i] + gate_part[256 + i] + gate_part[512 + i];
-      const float dov = gate_part[128 + i] + gate_part[384 + i] + gate_part[640 + i];
-      const float sg = sigmoid(z);
-      const float rr = sg * (1.f - sg) * dov;  // r (DQ, DK)
-      // ---- in-place fp16 operands, once the score MMA has read the 16-bit tiles
+      if constexpr (ROLE == R_DQ) cvt4(xk, OFF_K, 1.f, amax);  // K (state A, dP''K B)
+      if constexpr (ROLE == R_DK) cvt4(xq, OFF_Q, 1.f, amax);  // Q (adjoint A, dP''^T Q B)
+      if constexpr (ROLE == R_DV) convert_row<BF16, 8>(base + OFF_G, vg, 1.f, bmax);  // dO
+      // ---- once the score MMA has read its 16-bit tiles: their fp16 copies
       if (!(ok = wait(cta, cta.bar(P_DONE), par, ctl))) break;
       tc_fence_after();
-      float amax = 0.f, bmax = 0.f;  // A and B operands of the state MMA
       if constexpr (ROLE == R_DQ) {
-        convert_row<BF16, 4>(base + OFF_K, qk, 1.f, amax);      // K -> fp16 (state A, dP''K B)
         convert_row<BF16, 8>(base + OFF_V, vg, lk, bmax);       // V' (state B)
         convert_row<BF16, 8>(base + OFF_G, vg, lq, range_max);  // dO'' (A of dO'' S^T)
       } else if constexpr (ROLE == R_DV) {
         convert_row<BF16, 4>(base + OFF_Q, qk, lq, amax);       // Q'' (adjoint A)
         convert_row<BF16, 4>(base + OFF_K, qk, lk, range_max);  // K' (A of K' dS)
-        convert_row<BF16, 8>(base + OFF_G, vg, 1.f, bmax);      // dO (adjoint B, P''^T dO B)
       } else {
-        convert_row<BF16, 4>(base + OFF_Q, qk, 1.f, amax);      // Q (adjoint A, dP''^T Q B)
         convert_row<BF16, 8>(base + OFF_V, vg, lk, range_max);  // V' (A of V' dS^T)
         convert_row<BF16, 8>(base + OFF_G, vg, lq, bmax);       // dO'' (adjoint B)
       }
@@ -439,69 +472,85 @@ __device__ __forceinline__ void run_role(
           abmax[par * 24 + 12 + warp] = bm;
         }
       }
-      // ---- masked score copy (part 0), scaled by 2^-e of this step's state copy
-      if (sub == 0) {
-        if (!(ok = wait(cta, cta.bar(EP_S), par, ctl))) break;
+      // ---- the row's gate: the three partial sums
+      if (!(ok = wait(cta, cta.bar(QG0 + q4), par, ctl))) break;
+      const float sg = sigmoid(gate_part[i] + gate_part[128 + i] + gate_part[256 + i]);
+      // ---- masked score copy, scaled by 2^-e of this step's state copy: this part's 16-column
+      // blocks hb = sub, sub+3, sub+6 of the quadrant's rows, packed to fp16 pairs in registers.
+      // Block hb's pairs go to 32-bit columns 8hb..8hb+7, inside block hb/2's fp32 columns, so
+      // the three parts of a quadrant finish reading before any of them writes.
+      if (!(ok = wait(cta, cta.bar(EP_S), par, ctl))) break;
+      {
         const float psc = pow2i(-es[par]);
         float pmax = 0.f;
-        uint32_t r[32];
-#pragma unroll 1
-        for (int jb = 0; jb < 4; ++jb) {
-          const int c0 = 32 * jb;
-          float sc[32];
-          // DQ (rows = queries i, columns j <= i) or DV/DK (rows = keys j, columns i >= j)
-          const bool live = ROLE == R_DQ ? jb <= q4 : jb >= q4;
-          if (live) {
-            tmem_ld32(trow + TM_P + c0, r);
-            tmem_wait_ld();
-            if constexpr (ROLE == R_DQ) {
-              float f = pw[max(i - (c0 + 31), 0)] * psc;  // going left from min(i, c0+31)
+        uint32_t pk[3][8];
 #pragma unroll
-              for (int u = 31; u >= 0; --u) {
+        for (int m = 0; m < 3; ++m) {
+          const int hb = sub + 3 * m;
+          const int c0 = 16 * hb;
+          // DQ keeps columns j <= i (rows = queries i), DV and DK columns i >= j (rows = keys j)
+          const bool live = hb < 8 && (ROLE == R_DQ ? hb <= 2 * q4 + 1 : hb >= 2 * q4);
+          float sc[16];
+          if (live) {
+            uint32_t r[16];
+            tmem_ld16(trow + TM_P + c0, r);
+            tmem_wait_ld();
+            float dg = 0.f;
+            if constexpr (ROLE == R_DQ) {
+              float f = pw[max(i - (c0 + 15), 0)] * psc;  // going left from min(i, c0+15)
+#pragma unroll
+              for (int u = 15; u >= 0; --u) {
                 const bool in = c0 + u <= i;
                 sc[u] = in ? __uint_as_float(r[u]) * f : 0.f;
                 f = in ? f * lam : f;
-                pmax = fmaxf(pmax, fabsf(sc[u]));
+                dg = (c0 + u == i) ? __uint_as_float(r[u]) : dg;
               }
             } else {
               float f = pw[max(c0 - i, 0)] * psc;  // going right from max(j, c0)
 #pragma unroll
-              for (int u = 0; u < 32; ++u) {
+              for (int u = 0; u < 16; ++u) {
                 const bool in = c0 + u >= i;
                 sc[u] = in ? __uint_as_float(r[u]) * f : 0.f;
                 f = in ? f * lam : f;
+                dg = (c0 + u == i) ? __uint_as_float(r[u]) : dg;
                 // DV: the self-augmentation sigmoid(z_j) dO_j rides on the diagonal, so that
                 // P''^T dO includes it: (P^T + diag(sigmoid(z))) 2^-e
-                if (ROLE == R_DV && jb == q4 && u == lane) sc[u] += sg * psc;
-                pmax = fmaxf(pmax, fabsf(sc[u]));
+                if (ROLE == R_DV && c0 + u == i) sc[u] += sg * psc;
               }
             }
+            // DQ, DK: the score's diagonal is dO_i . v_i, the gate's other factor
+            if (ROLE != R_DV && (i >> 4) == hb) dpv[i] = dg;
           } else {
 #pragma unroll
-            for (int u = 0; u < 32; ++u) sc[u] = 0.f;
+            for (int u = 0; u < 16; ++u) sc[u] = 0.f;
           }
-          // fp16 pairs, in place over the fp32 scores: this block's 16 packed columns land on
-          // fp32 columns 16jb..16jb+15, which blocks <= jb have already read
-          uint32_t pk[16];
 #pragma unroll
-          for (int u = 0; u < 16; ++u) pk[u] = pack_h2(sc[2 * u], sc[2 * u + 1]);
-          tmem_st16(trow + TM_P + 16 * jb, pk);
+          for (int u = 0; u < 8; ++u) {
+            pmax = fmaxf(pmax, fmaxf(fabsf(sc[2 * u]), fabsf(sc[2 * u + 1])));
+            pk[m][u] = pack_h2(sc[2 * u], sc[2 * u + 1]);
+          }
         }
-        tmem_wait_st();
         range_max = fmaxf(range_max, pmax);
+        tc_fence_before();
+        mbar_arrive(cta.bar(QS0 + q4));
+        if (!(ok = wait(cta, cta.bar(QS0 + q4), par, ctl))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int m = 0; m < 3; ++m)
+          if (sub + 3 * m < 8) tmem_st8(trow + TM_P + 8 * (sub + 3 * m), pk[m]);
+        tmem_wait_st();
       }
-      if constexpr (ROLE == R_DQ) {  // r q for the d_a MMA (after the gate: it read q)
-        convert_row<BF16, 4>(base + OFF_Q, qk, rr, range_max);
-      }
+      float rr = 0.f;  // r = sigmoid'(z) (dO.v) (DQ, DK)
+      if constexpr (ROLE != R_DV) rr = sg * (1.f - sg) * dpv[i];
+      if constexpr (ROLE == R_DQ) convert_row<BF16, 4>(base + OFF_Q, qk, rr, range_max);  // r q
       fence_proxy_async();
       tc_fence_before();
       mbar_arrive(cta.bar(EP_CONV));
 
-      // ---- the MMAs of this step ran: take the self-augmentation operand (DQ: k, DK: q,
-      // this part's 32 channels) and release the tiles -- the next chunk's loads overlap the
-      // rest of this step.  DV's self-augmentation is inside D_X already.
+      // ---- output MMAs done: take the self-augmentation operand (DQ: k, DK: q, this part's 32
+      // channels) and release the tiles (the state MMA's commit completes the release), so the
+      // next chunk's loads overlap the rest of this step.  DV's term is inside D_X already.
       if (!(ok = wait(cta, cta.bar(X_DONE), par, ctl))) break;
-      if (!(ok = wait(cta, cta.bar(S_DONE), par, ctl))) break;
       tc_fence_after();
       uint4 vv[4];
       if constexpr (ROLE != R_DV) {
@@ -509,20 +558,10 @@ __device__ __forceinline__ void run_role(
         for (int ch = 0; ch < 4; ++ch) vv[ch] = *(const uint4*)(base + (ROLE == R_DQ ? OFF_K : OFF_Q) + qk(ch));
       }
       mbar_arrive(cta.bar(EMPTY));
-      int e_next = e_cur;
-      if (t < nc - 1) {
-        // bound on the next state: all parts' operand maxima and max|S| of this step's copy
-        if (!(ok = wait(cta, cta.bar(EP_CONV), par, ctl))) break;
-        if (!(ok = wait(cta, cta.bar(EP_S), par, ctl))) break;
-        e_next = state_exponent(lamC * max12(red + par * 12) +
-                                (float)C * max12(abmax + par * 24) * max12(abmax + par * 24 + 12));
-        if (e_next < 0) {
-          bad = true;
-          e_next = 0;
-        }
-        publish_state(t + 1, e_next, nullptr, true);
-      }
-      // ---- output rows, this part's columns: x = 2^e D_X (+ r (a * k|q) for DQ, DK)
+      // ---- output rows, this part's columns: x = 2^e D_X (+ r (a * k|q) for DQ, DK), while
+      // the state MMA runs
+      if (lane == 0) bulk_wait_read<0>();  // the staging buffer is free again
+      __syncwarp();
       {
         const float osc = pow2i(e_cur);
         const int row = b * T + c * C + 32 * q4;
@@ -550,6 +589,21 @@ __device__ __forceinline__ void run_role(
       }
       tc_fence_before();
       mbar_arrive(cta.bar(EP_X));
+      // ---- the state MMA ran: next state copy (the serial step)
+      if (!(ok = wait(cta, cta.bar(S_DONE), par, ctl))) break;
+      tc_fence_after();
+      int e_next = e_cur;
+      if (t < nc - 1) {
+        // bound on the next state: all parts' operand maxima and max|S| of this step's copy
+        if (!(ok = wait(cta, cta.bar(EP_CONV), par, ctl))) break;
+        e_next = state_exponent(lamC * max12(red + par * 12) +
+                                (float)C * max12(abmax + par * 24) * max12(abmax + par * 24 + 12));
+        if (e_next < 0) {
+          bad = true;
+          e_next = 0;
+        }
+        publish_state(t + 1, e_next, nullptr, true);
+      }
       // ---- adjoint of the initial state (DV, after the last step = chunk 0)
       if (ROLE == R_DV && t == nc - 1 && p.want_dinit && q4 < 3) {
         if (lane == 0) bulk_wait_read<0>();
@@ -565,8 +619,6 @@ __device__ __forceinline__ void run_role(
             },
             [&](int k, uint32_t src) { tma_store_3d(&map_dinit, src, 64 * sub + 16 * k, 32 * q4, bh); });
       }
-      if (lane == 0) bulk_wait_read<0>();  // the staging buffer is free for the next step
-      __syncwarp();
       e_cur = e_next;
     }
     // DQ: d_a of this (b, h) is the diagonal of the accumulated (r q)^T k; row d (lane of

@@ -160,16 +160,18 @@ __device__ __forceinline__ void store_rows_coalesced(uint8_t* stage, const float
   constexpr int CH = NC / 4;            // 16-byte chunks per row
   constexpr int RB = NC * 4;            // row bytes
   constexpr int RPI = 32 / CH;          // rows per store instruction
+  // chunk swizzle by row: 8 consecutive rows cover all 32 banks in both phases
+  auto key = [](int row) { return CH == 4 ? (row >> 1) & 3 : row & 7; };
 #pragma unroll
   for (int c = 0; c < CH; ++c)
-    *reinterpret_cast<float4*>(stage + lane * RB + ((c ^ (lane & (CH - 1))) << 4)) =
+    *reinterpret_cast<float4*>(stage + lane * RB + ((c ^ key(lane)) << 4)) =
         make_float4(r[4 * c], r[4 * c + 1], r[4 * c + 2], r[4 * c + 3]);
   __syncwarp();
 #pragma unroll
   for (int k = 0; k < CH; ++k) {
     const int rr = RPI * k + lane / CH, c = lane % CH;
     const float4 x =
-        *reinterpret_cast<const float4*>(stage + rr * RB + ((c ^ (rr & (CH - 1))) << 4));
+        *reinterpret_cast<const float4*>(stage + rr * RB + ((c ^ key(rr)) << 4));
     *reinterpret_cast<float4*>(row_ptr(rr) + 4 * c) = x;
   }
   __syncwarp();
