@@ -214,7 +214,7 @@ __device__ __forceinline__ void run_role(
           // DQ: dP = dO V^T (A = dO, B = V);  DK: dP^T = V dO^T (A = V, B = dO); K = 192
           constexpr uint32_t ID = idesc_f16(128, 128, BF16, BF16, false, false);
           const uint32_t A = sb + (ROLE == R_DQ ? OFF_G : OFF_V), B = sb + (ROLE == R_DQ ? OFF_V : OFF_G);
-#pragma unroll
+#pragma unroll 1
           for (int ks = 0; ks < 12; ++ks) {
             const uint32_t off = (ks >> 2) * V_BOX + (ks & 3) * 32;
             mma_f16_ss(tmem + TM_P, smem_desc(A + off, 16, 1024, SW_128),
@@ -222,7 +222,7 @@ __device__ __forceinline__ void run_role(
           }
         } else {  // DV: P^T = K Q^T, K = 96
           constexpr uint32_t ID = idesc_f16(128, 128, BF16, BF16, false, false);
-#pragma unroll
+#pragma unroll 1
           for (int ks = 0; ks < 6; ++ks) {
             const uint32_t off = (ks >> 1) * Q_BOX + (ks & 1) * 32;
             mma_f16_ss(tmem + TM_P, smem_desc(sb + OFF_K + off, 16, 512, SW_64),
@@ -238,7 +238,7 @@ __device__ __forceinline__ void run_role(
         if constexpr (ROLE == R_DQ) {
           // dq = dO'' S^T  (A = dO'' K-major, K = dv; B = state copy as [dk rows][dv], K-major)
           constexpr uint32_t ID1 = idesc_f16(128, 96, false, false, false, false);
-#pragma unroll
+#pragma unroll 1
           for (int ks = 0; ks < 12; ++ks)
             mma_f16_ss(tmem + TM_X,
                        smem_desc(sb + OFF_G + (ks >> 2) * V_BOX + (ks & 3) * 32, 16, 1024, SW_128),
@@ -246,19 +246,19 @@ __device__ __forceinline__ void run_role(
                        ks > 0);
           //    + dP'' K  (A = dP'' from TMEM, K = j; B = K as [j][dk], MN-major)
           constexpr uint32_t ID2 = idesc_f16(128, 96, false, false, false, true);
-#pragma unroll
+#pragma unroll 1
           for (int ks = 0; ks < 8; ++ks)
             mma_f16_ts(tmem + TM_X, tmem + TM_P + 8 * ks,
                        smem_desc(sb + OFF_K + ks * 1024, Q_BOX, 512, SW_64), ID2, 1);
         } else if constexpr (ROLE == R_DV) {
           // dv = P''^T dO  (A = P''^T from TMEM, K = i; B = dO as [i][dv], MN-major)
           constexpr uint32_t ID1 = idesc_f16(128, 192, false, false, false, true);
-#pragma unroll
+#pragma unroll 1
           for (int ks = 0; ks < 8; ++ks)
             mma_f16_ts(tmem + TM_X, tmem + TM_P + 8 * ks,
                        smem_desc(sb + OFF_G + ks * 2048, V_BOX, 1024, SW_128), ID1, ks > 0);
           //    + K' dS  (A = K' K-major, K = dk; B = adjoint copy [dk][dv], MN-major)
-#pragma unroll
+#pragma unroll 1
           for (int ks = 0; ks < 6; ++ks)
             mma_f16_ss(tmem + TM_X,
                        smem_desc(sb + OFF_K + (ks >> 1) * Q_BOX + (ks & 1) * 32, 16, 512, SW_64),
@@ -266,13 +266,13 @@ __device__ __forceinline__ void run_role(
         } else {
           // dk = dP''^T Q  (A = dP''^T from TMEM, K = i; B = Q as [i][dk], MN-major)
           constexpr uint32_t ID1 = idesc_f16(128, 96, false, false, false, true);
-#pragma unroll
+#pragma unroll 1
           for (int ks = 0; ks < 8; ++ks)
             mma_f16_ts(tmem + TM_X, tmem + TM_P + 8 * ks,
                        smem_desc(sb + OFF_Q + ks * 1024, Q_BOX, 512, SW_64), ID1, ks > 0);
           //    + V' dS^T  (A = V' K-major, K = dv; B = adjoint copy [dk][dv], K-major)
           constexpr uint32_t ID2 = idesc_f16(128, 96, false, false, false, false);
-#pragma unroll
+#pragma unroll 1
           for (int ks = 0; ks < 12; ++ks)
             mma_f16_ss(tmem + TM_X,
                        smem_desc(sb + OFF_V + (ks >> 2) * V_BOX + (ks & 3) * 32, 16, 1024, SW_128),
@@ -284,7 +284,7 @@ __device__ __forceinline__ void run_role(
           constexpr uint32_t ID = idesc_f16(128, 192, false, false, true, true);
           const uint32_t A = sb + (ROLE == R_DQ ? OFF_K : OFF_Q);  // K^T (DQ) or Q''^T / Q^T
           const uint32_t B = sb + (ROLE == R_DQ ? OFF_V : OFF_G);  // V' (DQ) or dO / dO''
-#pragma unroll
+#pragma unroll 1
           for (int ks = 0; ks < 8; ++ks)
             mma_f16_ss(tmem + TM_S, smem_desc(A + ks * 1024, Q_BOX, 512, SW_64),
                        smem_desc(B + ks * 2048, V_BOX, 1024, SW_128), ID, 1);
@@ -293,7 +293,7 @@ __device__ __forceinline__ void run_role(
           // d_a: diag((r q)^T k) accumulated over every chunk (A = r q as [i][dk] MN-major,
           // B = K as [i][dk] MN-major); rows 96..127 are padding
           constexpr uint32_t ID = idesc_f16(128, 96, false, false, true, true);
-#pragma unroll
+#pragma unroll 1
           for (int ks = 0; ks < 8; ++ks)
             mma_f16_ss(tmem + TM_A, smem_desc(sb + OFF_Q + ks * 1024, Q_BOX, 512, SW_64),
                        smem_desc(sb + OFF_K + ks * 1024, Q_BOX, 512, SW_64), ID, (t > 0 || ks > 0));

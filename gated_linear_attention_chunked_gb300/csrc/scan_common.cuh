@@ -25,22 +25,32 @@ struct Cta {
   __device__ volatile int* abort_flag() const { return (volatile int*)(base + abort_off); }
 };
 
-// Bounded wait that also returns false as soon as another role of the CTA has given up.
-__device__ __forceinline__ bool wait(const Cta& cta, uint32_t bar, uint32_t parity,
-                                     const DevCtl& ctl) {
-  if (mbar_try_wait(bar, parity)) return true;
+// The polling part of a bounded wait, kept out of line: every wait site then costs one
+// try_wait and a call, which keeps the unrolled chunk loops small enough for the
+// instruction cache.
+static __device__ __noinline__ bool wait_slow(volatile int* abort, uint32_t bar, uint32_t parity,
+                                              int* err, unsigned long long wait_ns) {
   const uint64_t t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 31u) == 0) {
-      if (*cta.abort_flag()) return false;
-      if (globaltimer() - t0 > ctl.wait_ns) {
-        record_error(ctl, DEV_TIMEOUT);
-        *cta.abort_flag() = 1;
+      if (*abort) return false;
+      if (globaltimer() - t0 > wait_ns) {
+        DevCtl c;
+        c.err = err;
+        c.wait_ns = wait_ns;
+        record_error(c, DEV_TIMEOUT);
+        *abort = 1;
         return false;
       }
     }
   }
+}
+// Bounded wait that also returns false as soon as another role of the CTA has given up.
+__device__ __forceinline__ bool wait(const Cta& cta, uint32_t bar, uint32_t parity,
+                                     const DevCtl& ctl) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait_slow(cta.abort_flag(), bar, parity, ctl.err, ctl.wait_ns);
 }
 
 template <bool BF16>
@@ -82,7 +92,7 @@ __device__ __forceinline__ void scale_chunk_to_half(uint4* p, float s, float& vm
 template <bool SRC_BF16, int NCH, typename Off>
 __device__ __forceinline__ void convert_row(uint8_t* tile, Off off, float s, float& vmax) {
   static_assert(NCH % 4 == 0, "chunks in groups of four");
-#pragma unroll
+#pragma unroll 1  // batches of four chunks; a rolled loop keeps the code small
   for (int c0 = 0; c0 < NCH; c0 += 4) {
     uint4 x[4];
 #pragma unroll
