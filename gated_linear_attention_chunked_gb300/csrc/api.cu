@@ -45,6 +45,20 @@ size_t half_copy_bytes(int B, int T, int H, bool with_dO) {
   return s;
 }
 
+// SMs of the current device (0 if there is none).
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+// Bytes the forward must have (fp16 copies of fp32 inputs) and the segment-parallel path's
+// share on top, at the offset round256(must).
+size_t fwd_min_workspace(int B, int T, int H, gla_dtype in_dtype) {
+  return in_dtype == GLA_FP32 ? half_copy_bytes(B, T, H, false) : 0;
+}
+
 }  // namespace
 
 namespace gla {
@@ -103,7 +117,9 @@ gla_status gla_decay_schedule(int H, double t_min, double t_max, float* log_deca
 
 size_t gla_chunk_fwd_workspace_size(int B, int T, int H, int dk, int dv, gla_dtype in_dtype) {
   if (check_chunk_sizes(B, T, H, dk, dv, in_dtype) != GLA_OK) return 0;
-  return in_dtype == GLA_FP32 ? half_copy_bytes(B, T, H, false) : 0;
+  const size_t must = fwd_min_workspace(B, T, H, in_dtype);
+  const int G = gla::fwd_segments(B, T, H, sm_count());
+  return G > 1 ? round256(must) + gla::fwd_segment_workspace_bytes(B, H, G) : must;
 }
 
 gla_status gla_chunk_fwd(const void* q, const void* k, const void* v, gla_dtype in_dtype,
@@ -118,9 +134,14 @@ gla_status gla_chunk_fwd(const void* q, const void* k, const void* v, gla_dtype 
       !aligned16(aug_balance) || !aligned16(init_state) || !aligned16(o) ||
       !aligned16(final_state))
     return GLA_ERR_ALIGNMENT;
-  const size_t need = gla_chunk_fwd_workspace_size(B, T, H, dk, dv, in_dtype);
-  if (need && (!workspace || workspace_bytes < need)) return GLA_ERR_WORKSPACE;
-  if (need && !aligned256(workspace)) return GLA_ERR_ALIGNMENT;
+  const size_t must = fwd_min_workspace(B, T, H, in_dtype);
+  if (must && (!workspace || workspace_bytes < must)) return GLA_ERR_WORKSPACE;
+  if (must && !aligned256(workspace)) return GLA_ERR_ALIGNMENT;
+  // few long sequences: segment-parallel when the workspace has room for it
+  int G = gla::fwd_segments(B, T, H, sm_count());
+  if (G > 1 && !(workspace && aligned256(workspace) &&
+                 workspace_bytes >= round256(must) + gla::fwd_segment_workspace_bytes(B, H, G)))
+    G = 1;
   gla::DevCtl ctl;
   if ((st = ctl_for_current_device(&ctl)) != GLA_OK) return st;
 
@@ -140,7 +161,11 @@ gla_status gla_chunk_fwd(const void* q, const void* k, const void* v, gla_dtype 
       return GLA_ERR_CUDA;
     a.q = hq; a.k = hk; a.v = hv; a.bf16 = false;
   }
-  return gla::launch_chunk_fwd(a, ctl, stream) == cudaSuccess ? GLA_OK : GLA_ERR_CUDA;
+  const cudaError_t e =
+      G > 1 ? gla::launch_chunk_fwd_segmented(a, G, static_cast<uint8_t*>(workspace) + round256(must),
+                                              ctl, stream)
+            : gla::launch_chunk_fwd(a, ctl, stream);
+  return e == cudaSuccess ? GLA_OK : GLA_ERR_CUDA;
 }
 
 size_t gla_chunk_bwd_workspace_size(int B, int T, int H, int dk, int dv, gla_dtype in_dtype) {

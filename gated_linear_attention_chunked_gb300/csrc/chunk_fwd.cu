@@ -91,7 +91,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
            const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o,
            const __grid_constant__ CUtensorMap map_fin, const float* __restrict__ log_decay,
            const float* __restrict__ aug, const float* __restrict__ init, float* __restrict__ out,
-           float* __restrict__ fin, int T, int H, DevCtl ctl) {
+           float* __restrict__ fin, int T, int H, int seg, DevCtl ctl) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   Cta cta;
   cta.base = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -438,7 +438,6 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
 
     for (int c = 0; c < nc && ok; ++c) {
       const uint32_t s = c & 1, par = c & 1;
-      uint8_t* stg = base + s * STAGE;
       if (!(ok = wait(cta, cta.bar(O_DONE), par, ctl))) break;
       if (!(ok = wait(cta, cta.bar(S_DONE), par, ctl))) break;
       if (!(ok = wait(cta, cta.bar(EP_CONV), par, ctl))) break;
@@ -482,7 +481,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
       tc_fence_before();
       mbar_arrive(cta.bar(EP_O));
       // ---- final state (after the last chunk), staged through the same rows
-      if (c == nc - 1 && fin && q4 < 3) {
+      // (with seg > 1 the CTAs are segments of longer sequences: only the last one's counts)
+      if (c == nc - 1 && fin && q4 < 3 && b % seg == seg - 1) {
         if (lane == 0) bulk_wait_read<0>();
         __syncwarp();
         emit_rows_tma<6>(
@@ -494,7 +494,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
 #pragma unroll
               for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(r[j]);
             },
-            [&](int k, uint32_t src) { tma_store_3d(&map_fin, src, 96 * hf + 16 * k, 32 * q4, bh); });
+            [&](int k, uint32_t src) {
+              tma_store_3d(&map_fin, src, 96 * hf + 16 * k, 32 * q4, (b / seg) * H + h);
+            });
       }
       if (lane == 0) bulk_wait_read<0>();  // the staging buffers are free for the next chunk
       __syncwarp();
@@ -522,13 +524,14 @@ cudaError_t launch_chunk_fwd(const FwdArgs& a, DevCtl ctl, cudaStream_t stream) 
       !make_tmap_3d_16bit(&mk, a.k, DK, a.H, rows, 32, C, CU_TENSOR_MAP_SWIZZLE_64B, a.bf16) ||
       !make_tmap_3d_16bit(&mv, a.v, DV, a.H, rows, 64, C, CU_TENSOR_MAP_SWIZZLE_128B, a.bf16) ||
       !make_tmap_out_f32(&mo, a.o, DV, a.H, rows) ||
-      !make_tmap_state_f32(&mfin, a.fin ? (const void*)a.fin : (const void*)a.o, (long long)a.B * a.H))
+      !make_tmap_state_f32(&mfin, a.fin ? (const void*)a.fin : (const void*)a.o,
+                           (long long)(a.B / a.seg) * a.H))
     return cudaErrorInvalidValue;
   auto kern = a.bf16 ? fwd_kernel<true> : fwd_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
   kern<<<a.B * a.H, THREADS, SMEM_BYTES, stream>>>(mq, mk, mv, mo, mfin, a.log_decay, a.aug, a.init, a.o,
-                                                   a.fin, a.T, a.H, ctl);
+                                                   a.fin, a.T, a.H, a.seg, ctl);
   return cudaGetLastError();
 }
 

@@ -27,8 +27,11 @@ struct FwdArgs {
   const float* aug;        // [H,96]
   const float* init;       // [B,H,96,192] or null
   float* o;                // [B,T,H,192]
-  float* fin;              // [B,H,96,192] or null
+  float* fin;              // [B/seg,H,96,192] or null
   int B, T, H;
+  // seg > 1: the B "sequences" are seg consecutive segments of each of B/seg longer ones;
+  // only the last segment of each writes its final state, to fin[b / seg].
+  int seg = 1;
 };
 // Returns cudaErrorInvalidValue if a tensor map cannot be encoded.
 cudaError_t launch_chunk_fwd(const FwdArgs& a, DevCtl ctl, cudaStream_t stream);
@@ -53,6 +56,13 @@ struct BwdArgs {
   int B, T, H;
 };
 size_t chunk_bwd_workspace_bytes(int B, int T, int H);
+
+// Segment-parallel forward for few, long sequences: the number of segments G (1 = not
+// worth it) for this shape on a device with n_sm SMs, the workspace it needs, and the call.
+int fwd_segments(int B, int T, int H, int n_sm);
+size_t fwd_segment_workspace_bytes(int B, int H, int G);
+cudaError_t launch_chunk_fwd_segmented(const FwdArgs& a, int G, void* workspace, DevCtl ctl,
+                                       cudaStream_t stream);
 
 // The device error word and wait limit of the current device (defined in api.cu).
 cudaError_t current_device_ctl(DevCtl* ctl);

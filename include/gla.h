@@ -109,8 +109,15 @@ GLA_API gla_status gla_decay_schedule(int H, double t_min, double t_max, float* 
  *   init_state   [B,H,96,192] fp32 or NULL   (read only)
  *   o            [B,T,H,192] fp32 (written)
  *   final_state  [B,H,96,192] fp32 or NULL   (written)
- *   workspace    device scratch of at least gla_chunk_fwd_workspace_size()
- *                bytes (may be NULL when that size is 0), 256-byte aligned.
+ *   workspace    device scratch, 256-byte aligned, of gla_chunk_fwd_workspace_size()
+ *                bytes.  fp32 inputs need their fp16 copies there (GLA_ERR_WORKSPACE
+ *                if it is smaller).  With few long sequences (2*B*H <= the current
+ *                device's SM count and T >= 4096) the size also covers the
+ *                segment-parallel path: every segment's state sum in parallel, their
+ *                recurrence, then the segments as independent sequences (the state
+ *                recurrence is linear).  Given less (or NULL for 16-bit inputs), the
+ *                call runs the serial chunk scan instead: same results up to rounding,
+ *                fewer SMs busy.  The size depends on the device current at the call.
  * Arithmetic: the tensor cores take fp16 operands with fp32 accumulation; the
  * state is carried in fp32 across chunks.  Inputs must satisfy |x| < 65504.
  */

@@ -123,3 +123,39 @@ def test_fwd_long_prefill_workload(env):
     print(f"fwd long: first {e_first:.2e} last {e_last:.2e} final {ef:.2e}")
     assert e_first <= TOL_CHUNK and e_last <= TOL_CHUNK and ef <= TOL_CHUNK
     assert np.all(np.isfinite(o))
+
+
+@pytest.mark.parametrize("B,T,H,seed", [(1, 4096, 2, 31), (1, 8192, 3, 32)])
+def test_fwd_segmented_path(env, B, T, H, seed):
+    """Few long sequences take the segment-parallel path (the state sum of every segment but
+    the last in parallel, their recurrence, then the segments as independent sequences).  It
+    must match the oracle, initial and final state included, and the serial path, which the
+    same call takes when it is given no workspace."""
+    import oracle
+    gla, torch = env
+    assert gla.chunk_fwd_workspace_size(B, T, H, gla.GLA_BF16) > 0, "shape not segmented"
+    q, k, v = synth.qkv(seed, B, T, H)
+    a = synth.aug_balance(seed, (H, 96), 0.1)
+    init = synth.init_state(seed, B, H, 0.05)
+    o, fin, (q, k, v, gam64) = run_fwd(env, q, k, v, a, init, H, "bf16")
+    o_ref, fin_ref = oracle.fwd(q, k, v, gam64, a, init)
+    eo, ef = rel_err(o, o_ref), rel_err(fin, fin_ref)
+    # the serial path: same call through the C ABI without a workspace
+    lib = gla.load()
+    qd, kd, vd = (to_dev(x, torch.bfloat16) for x in (q, k, v))
+    gam = gla.decay_schedule(H).cuda()
+    ad, idd = to_dev(a, torch.float32), to_dev(init, torch.float32)
+    o2 = torch.empty((B, T, H, 192), dtype=torch.float32, device="cuda")
+    f2 = torch.empty((B, H, 96, 192), dtype=torch.float32, device="cuda")
+    rc = lib.gla_chunk_fwd(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), gla.GLA_BF16,
+                           gam.data_ptr(), ad.data_ptr(), idd.data_ptr(), o2.data_ptr(),
+                           f2.data_ptr(), None, 0, B, T, H, 96, 192,
+                           torch.cuda.current_stream().cuda_stream)
+    assert rc == 0, gla.status_string(rc)
+    torch.cuda.synchronize()
+    assert gla.get_device_error() == 0
+    es = rel_err(o, o2.cpu().numpy())
+    print(f"fwd segmented B={B} T={T} H={H}: o {eo:.2e} final {ef:.2e} vs serial {es:.2e}")
+    assert eo <= TOL_CHUNK and ef <= TOL_CHUNK
+    assert rel_err(o2.cpu().numpy(), o_ref) <= TOL_CHUNK
+    assert rel_err(f2.cpu().numpy(), fin_ref) <= TOL_CHUNK
