@@ -323,33 +323,57 @@ def run_gpu(args, rank, world, local_rank):
     roof_bwd["tensor"] = dict(achieved=th * BWD_FLOPS_TH / (bwd_t * 1e-3) / 1e12, peak=pk["bf16"],
                               unit="TFLOP/s", frac=th * BWD_FLOPS_TH / (bwd_t * 1e-3) / 1e12 / pk["bf16"])
 
-    # ---- end to end through the public API: pinned host inputs -> HBM -> fwd+bwd -> d_aug
+    # ---- end to end through the public API: pinned host inputs -> HBM -> fwd+bwd -> d_aug.
+    # Every step copies its own inputs from pinned host memory and reads its d_aug back; as
+    # in a training loop's prefetch, the copy of step s+1 runs on a second stream into the
+    # other of two device buffers while step s computes (host->device is ~5.8 ms per step
+    # here, the kernels ~2 ms).  The clock starts before the first copy and stops after the
+    # last read-back has landed.
     e2e = None
     if not args.no_e2e:
         hq, hk, hv, hdO = (x.cpu().pin_memory() for x in (q, k, v, dO))
-        h_daug = torch.empty(H, DK).pin_memory()
-        h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hdO))
-        d2h = h_daug.numel() * 4
         e2e_steps = max(3, min(args.steps, 10))
-        times = []
-        for s in range(e2e_steps + 2):
+        h_daug = torch.empty(e2e_steps, H, DK).pin_memory()
+        h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hdO))
+        d2h = H * DK * 4
+        bufs = [tuple(torch.empty_like(x) for x in (q, k, v, dO)) for _ in range(2)]
+        copy_stream = torch.cuda.Stream(device=dev)
+        copied = [torch.cuda.Event() for _ in range(2)]
+        consumed = [torch.cuda.Event() for _ in range(2)]
+
+        def e2e_run(nsteps):
+            for s_ in range(nsteps):
+                i = s_ % 2
+                with torch.cuda.stream(copy_stream):
+                    if s_ >= 2:
+                        copy_stream.wait_event(consumed[i])  # step s-2 is done with buffer i
+                    for d, hsrc in zip(bufs[i], (hq, hk, hv, hdO)):
+                        d.copy_(hsrc, non_blocking=True)
+                    copied[i].record(copy_stream)
+                stream.wait_event(copied[i])
+                bq, bk, bv, bdO = bufs[i]
+                gla.chunk_fwd(bq, bk, bv, gam, a, out=o, final_state=fin)
+                _, _, _, daug, _ = gla.chunk_bwd(bq, bk, bv, gam, a, bdO, workspace=ws,
+                                                 want_d_init_state=False)
+                consumed[i].record(stream)
+                h_daug[s_].copy_(daug, non_blocking=True)
             torch.cuda.synchronize()
-            t0 = time.perf_counter()
-            dq2, dk2, dv2, dO2 = (x.to(dev, non_blocking=True) for x in (hq, hk, hv, hdO))
-            gla.chunk_fwd(dq2, dk2, dv2, gam, a, out=o, final_state=fin)
-            _, _, _, daug, _ = gla.chunk_bwd(dq2, dk2, dv2, gam, a, dO2, workspace=ws,
-                                             want_d_init_state=False)
-            h_daug.copy_(daug, non_blocking=True)
-            torch.cuda.synchronize()
-            if s >= 2:
-                times.append(time.perf_counter() - t0)
-            del dq2, dk2, dv2, dO2
-        tt = torch.tensor([sum(times)], device=dev, dtype=torch.float64)
+
+        e2e_run(2)  # warm-up
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        e2e_run(e2e_steps)
+        tt = torch.tensor([time.perf_counter() - t0], device=dev, dtype=torch.float64)
         if dist:
             dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e = dict(value=world * tokens * len(times) / float(tt.item()), unit="tokens/s",
+        e2e = dict(value=world * tokens * e2e_steps / float(tt.item()), unit="tokens/s",
                    h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h,
-                   path="pinned host q,k,v,dO -> gla chunk_fwd + chunk_bwd -> host d_aug")
+                   path="pinned host q,k,v,dO -> gla chunk_fwd + chunk_bwd -> host d_aug; "
+                        "next step's inputs copied on a second stream during this step's "
+                        "kernels (two device buffers)")
+        del bufs
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -383,6 +407,63 @@ def run_gpu(args, rank, world, local_rank):
     return 0
 
 
+def run_long_prefill(args):
+    """--part long: the long-context prefill forward (B=2, T=131072, H=16, bf16, initial state
+    ~ N(0, 0.01)), through the public API with its workspace (segment-parallel path) and,
+    for comparison, without one (serial chunk scan)."""
+    import torch
+    import gated_linear_attention_chunked_gb300 as gla
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    lib = gla.load()
+    Bl, Tl = 2, 131072
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(4321)
+    rn = lambda *sh, std=1.0: torch.randn(*sh, generator=gen, device=dev) * std
+    q = rn(Bl, Tl, H, DK, std=DK ** -0.5).bfloat16()
+    k = rn(Bl, Tl, H, DK).bfloat16()
+    v = rn(Bl, Tl, H, DV).bfloat16()
+    init = rn(Bl, H, DK, DV, std=0.01)
+    a = rn(H, DK, std=0.02)
+    gam = gla.decay_schedule(H).to(dev)
+    o = torch.empty(Bl, Tl, H, DV, device=dev)
+    fin = torch.empty(Bl, H, DK, DV, device=dev)
+    nws = gla.chunk_fwd_workspace_size(Bl, Tl, H, gla.GLA_BF16)
+    ws = torch.empty(max(nws, 256), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def call(w, nb):
+        rc = lib.gla_chunk_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), gla.GLA_BF16,
+                               gam.data_ptr(), a.data_ptr(), init.data_ptr(), o.data_ptr(),
+                               fin.data_ptr(), w, nb, Bl, Tl, H, DK, DV, stream.cuda_stream)
+        if rc != 0:
+            raise RuntimeError(gla.status_string(rc))
+
+    def timed(w, nb, n):
+        for _ in range(args.warmup):
+            call(w, nb)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(n):
+            call(w, nb)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n
+
+    seg_ms = timed(ws.data_ptr(), nws, max(args.steps, 5))
+    ser_ms = timed(None, 0, 3)
+    if gla.get_device_error() != 0:
+        raise RuntimeError("device error")
+    byts = Bl * Tl * H * FWD_BYTES_TH
+    pk = peaks()
+    print(json.dumps(dict(part="long", workload="long prefill fwd B=2 T=131072 H=16 bf16 in, fp32 out",
+                          ms=seg_ms, tokens_per_s=Bl * Tl / (seg_ms * 1e-3),
+                          gbs=byts / (seg_ms * 1e-3) / 1e9, frac_hbm=byts / (seg_ms * 1e-3) / 1e9 / pk["hbm"],
+                          peak_source=pk["src"], workspace_bytes=nws, serial_ms=ser_ms)), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -392,7 +473,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seqs", type=int, default=8)
-    ap.add_argument("--part", choices=["all", "fwd", "bwd", "decode"], default="all",
+    ap.add_argument("--part", choices=["all", "fwd", "bwd", "decode", "long"], default="all",
                     help="time one call alone (smaller profiling cases); the default is the "
                          "whole hot path")
     ap.add_argument("--batch", type=int, default=B, help="sequences of the training shape")
@@ -412,6 +493,8 @@ def main():
         return 2
     if args.impl == "reference":
         return run_reference(args, rank, world)
+    if args.part == "long":
+        return run_long_prefill(args) if rank == 0 else 0
     return run_gpu(args, rank, world, local_rank)
 
 
