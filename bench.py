@@ -407,6 +407,49 @@ def run_gpu(args, rank, world, local_rank):
     return 0
 
 
+def run_paged_decode(args):
+    """--part paged: one decode step over the serving pool (1280 pages x 24 layers x 16 heads
+    of 96x192 fp32 states) for an active set of 1024 sequences in shuffled page order, through
+    gla_decode_step_paged."""
+    import torch
+    import gated_linear_attention_chunked_gb300 as gla
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    gla.load()
+    n_act = 1024
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(777)
+    pool = torch.randn(N_SEQ, N_LAYERS, H, DK, DV, generator=gen, device=dev) * 0.05
+    page = torch.randperm(N_SEQ, generator=gen, device=dev)[:n_act].to(torch.int32)
+    q = torch.randn(n_act, N_LAYERS, H, DK, generator=gen, device=dev) * DK ** -0.5
+    k = torch.randn(n_act, N_LAYERS, H, DK, generator=gen, device=dev)
+    v = torch.randn(n_act, N_LAYERS, H, DV, generator=gen, device=dev)
+    a = torch.randn(N_LAYERS, H, DK, generator=gen, device=dev) * 0.02
+    gam = gla.decay_schedule(H).to(dev)
+    o = torch.empty(n_act, N_LAYERS, H, DV, device=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        gla.decode_step_paged(pool, page, q, k, v, gam, a, out=o)
+    n = max(args.steps, 5)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(n):
+        gla.decode_step_paged(pool, page, q, k, v, gam, a, out=o)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if gla.get_device_error() != 0:
+        raise RuntimeError("device error")
+    ms = e0.elapsed_time(e1) / n
+    byts = n_act * N_LAYERS * H * DEC_BYTES_STATE
+    pk = peaks()
+    print(json.dumps(dict(part="paged", workload="paged decode, 1024 active of 1280 pages x 24 x 16 "
+                          "fp32 states, shuffled page order", ms=ms, gbs=byts / (ms * 1e-3) / 1e9,
+                          frac_hbm=byts / (ms * 1e-3) / 1e9 / pk["hbm"], peak_source=pk["src"])),
+          flush=True)
+    return 0
+
+
 def run_long_prefill(args):
     """--part long: the long-context prefill forward (B=2, T=131072, H=16, bf16, initial state
     ~ N(0, 0.01)), through the public API with its workspace (segment-parallel path) and,
@@ -473,7 +516,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seqs", type=int, default=8)
-    ap.add_argument("--part", choices=["all", "fwd", "bwd", "decode", "long"], default="all",
+    ap.add_argument("--part", choices=["all", "fwd", "bwd", "decode", "long", "paged"], default="all",
                     help="time one call alone (smaller profiling cases); the default is the "
                          "whole hot path")
     ap.add_argument("--batch", type=int, default=B, help="sequences of the training shape")
@@ -495,6 +538,8 @@ def main():
         return run_reference(args, rank, world)
     if args.part == "long":
         return run_long_prefill(args) if rank == 0 else 0
+    if args.part == "paged":
+        return run_paged_decode(args) if rank == 0 else 0
     return run_gpu(args, rank, world, local_rank)
 
 

@@ -69,6 +69,11 @@ def load(path: str | None = None):
             lib.gla_chunk_bwd.argtypes = [_P] * 3 + [_I] + [_P] * 11 + [_S] + [_I] * 5 + [_P]
             lib.gla_chunk_bwd.restype = _I
             lib.gla_decode_step.argtypes = [_P] * 7 + [_I] * 5 + [_P]
+            lib.gla_decode_step_paged.argtypes = [_P, _P] + [_I] * 4 + [_P] * 6 + [_I] * 4 + [_P]
+            lib.gla_decode_step_paged.restype = _I
+            lib.gla_chunk_fwd_paged.argtypes = ([_P] * 3 + [_I] + [_P] * 4 + [_I] * 4 + [_P] * 2 +
+                                                [_S] + [_I] * 5 + [_P])
+            lib.gla_chunk_fwd_paged.restype = _I
             lib.gla_decode_step.restype = _I
             if path is not None:
                 return lib
@@ -207,6 +212,55 @@ def decode_step(state, q, k, v, log_decay, aug_balance, *, out=None, stream=None
         _dev(log_decay, "log_decay", f), _dev(aug_balance, "aug_balance", f), _dev(out, "o", f),
         N, L, H, dk, dv, _stream(stream))
     _check("gla_decode_step", rc)
+    return out
+
+
+def _pages(page, n):
+    torch = _torch()
+    if page.dtype != torch.int32 or page.dim() != 1 or page.numel() != n:
+        raise ValueError(f"page must be a 1-D int32 tensor of {n} entries")
+    return _dev(page, "page")
+
+
+def decode_step_paged(pool, page, q, k, v, log_decay, aug_balance, *, layer0=0, out=None,
+                      stream=None):
+    """Decode step over a state pool (gla_decode_step_paged).  pool [P, pool_layers, H, 96, 192]
+    fp32 is updated in place for pages page[n] (int32 [n_active]) and layers layer0..layer0+L-1;
+    q,k [n_active,L,H,96], v [n_active,L,H,192]; aug_balance [L,H,96].  Returns o."""
+    torch = _torch()
+    P, PL, H, dk, dv = pool.shape
+    n, L = q.shape[0], q.shape[1]
+    if out is None:
+        out = torch.empty((n, L, H, dv), dtype=torch.float32, device=pool.device)
+    f = torch.float32
+    rc = load().gla_decode_step_paged(
+        _dev(pool, "pool", f), _pages(page, n), n, P, PL, layer0, _dev(q, "q", f),
+        _dev(k, "k", f), _dev(v, "v", f), _dev(log_decay, "log_decay", f),
+        _dev(aug_balance, "aug_balance", f), _dev(out, "o", f), L, H, dk, dv, _stream(stream))
+    _check("gla_decode_step_paged", rc)
+    return out
+
+
+def chunk_fwd_paged(q, k, v, log_decay, aug_balance, pool, page, layer, *, init_from_pool=True,
+                    out=None, workspace=None, stream=None):
+    """Chunked prefill into a state pool (gla_chunk_fwd_paged): sequence b starts from layer
+    `layer` of page[b] (or zero) and its final state is written back there.  Returns o."""
+    torch = _torch()
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    P, PL = pool.shape[0], pool.shape[1]
+    code = _dtype_code(q)
+    if out is None:
+        out = torch.empty((B, T, H, dv), dtype=torch.float32, device=q.device)
+    ws = _workspace(load().gla_chunk_fwd_workspace_size(B, T, H, dk, dv, code), q.device, workspace)
+    f = torch.float32
+    rc = load().gla_chunk_fwd_paged(
+        _dev(q, "q"), _dev(k, "k", q.dtype), _dev(v, "v", q.dtype), code,
+        _dev(log_decay, "log_decay", f), _dev(aug_balance, "aug_balance", f),
+        _dev(pool, "pool", f), _pages(page, B), P, PL, layer, 1 if init_from_pool else 0,
+        _dev(out, "o", f), _dev(ws, "workspace"), 0 if ws is None else ws.numel() * ws.element_size(),
+        B, T, H, dk, dv, _stream(stream))
+    _check("gla_chunk_fwd_paged", rc)
     return out
 
 

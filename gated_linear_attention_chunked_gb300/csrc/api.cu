@@ -59,6 +59,53 @@ size_t fwd_min_workspace(int B, int T, int H, gla_dtype in_dtype) {
   return in_dtype == GLA_FP32 ? half_copy_bytes(B, T, H, false) : 0;
 }
 
+
+gla_status chunk_fwd_impl(const void* q, const void* k, const void* v, gla_dtype in_dtype,
+                          const float* log_decay, const float* aug_balance,
+                          const float* init_state, float* o, float* final_state, void* workspace,
+                          size_t workspace_bytes, int B, int T, int H, int dk, int dv,
+                          const gla::StatePages& sp, cudaStream_t stream) {
+  gla_status st = check_chunk_sizes(B, T, H, dk, dv, in_dtype);
+  if (st != GLA_OK) return st;
+  if (!q || !k || !v || !log_decay || !aug_balance || !o) return GLA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(log_decay) ||
+      !aligned16(aug_balance) || !aligned16(init_state) || !aligned16(o) ||
+      !aligned16(final_state))
+    return GLA_ERR_ALIGNMENT;
+  const size_t must = fwd_min_workspace(B, T, H, in_dtype);
+  if (must && (!workspace || workspace_bytes < must)) return GLA_ERR_WORKSPACE;
+  if (must && !aligned256(workspace)) return GLA_ERR_ALIGNMENT;
+  // few long sequences: segment-parallel when the workspace has room for it
+  int G = gla::fwd_segments(B, T, H, sm_count());
+  if (G > 1 && !(workspace && aligned256(workspace) &&
+                 workspace_bytes >= round256(must) + gla::fwd_segment_workspace_bytes(B, H, G)))
+    G = 1;
+  gla::DevCtl ctl;
+  if ((st = ctl_for_current_device(&ctl)) != GLA_OK) return st;
+
+  gla::FwdArgs a;
+  a.q = q; a.k = k; a.v = v; a.bf16 = in_dtype == GLA_BF16;
+  a.log_decay = log_decay; a.aug = aug_balance; a.init = init_state;
+  a.o = o; a.fin = final_state; a.B = B; a.T = T; a.H = H; a.sp = sp;
+  if (in_dtype == GLA_FP32) {
+    const size_t tok = (size_t)B * T * H;
+    uint8_t* w = static_cast<uint8_t*>(workspace);
+    void* hq = w;
+    void* hk = w + round256(tok * dk * 2);
+    void* hv = w + 2 * round256(tok * dk * 2);
+    if (gla::launch_to_half((const float*)q, hq, (long long)(tok * dk), ctl, stream) != cudaSuccess ||
+        gla::launch_to_half((const float*)k, hk, (long long)(tok * dk), ctl, stream) != cudaSuccess ||
+        gla::launch_to_half((const float*)v, hv, (long long)(tok * dv), ctl, stream) != cudaSuccess)
+      return GLA_ERR_CUDA;
+    a.q = hq; a.k = hk; a.v = hv; a.bf16 = false;
+  }
+  const cudaError_t e =
+      G > 1 ? gla::launch_chunk_fwd_segmented(a, G, static_cast<uint8_t*>(workspace) + round256(must),
+                                              ctl, stream)
+            : gla::launch_chunk_fwd(a, ctl, stream);
+  return e == cudaSuccess ? GLA_OK : GLA_ERR_CUDA;
+}
+
 }  // namespace
 
 namespace gla {
@@ -127,45 +174,29 @@ gla_status gla_chunk_fwd(const void* q, const void* k, const void* v, gla_dtype 
                          const float* init_state, float* o, float* final_state, void* workspace,
                          size_t workspace_bytes, int B, int T, int H, int dk, int dv,
                          cudaStream_t stream) {
-  gla_status st = check_chunk_sizes(B, T, H, dk, dv, in_dtype);
-  if (st != GLA_OK) return st;
-  if (!q || !k || !v || !log_decay || !aug_balance || !o) return GLA_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(log_decay) ||
-      !aligned16(aug_balance) || !aligned16(init_state) || !aligned16(o) ||
-      !aligned16(final_state))
-    return GLA_ERR_ALIGNMENT;
-  const size_t must = fwd_min_workspace(B, T, H, in_dtype);
-  if (must && (!workspace || workspace_bytes < must)) return GLA_ERR_WORKSPACE;
-  if (must && !aligned256(workspace)) return GLA_ERR_ALIGNMENT;
-  // few long sequences: segment-parallel when the workspace has room for it
-  int G = gla::fwd_segments(B, T, H, sm_count());
-  if (G > 1 && !(workspace && aligned256(workspace) &&
-                 workspace_bytes >= round256(must) + gla::fwd_segment_workspace_bytes(B, H, G)))
-    G = 1;
-  gla::DevCtl ctl;
-  if ((st = ctl_for_current_device(&ctl)) != GLA_OK) return st;
+  return chunk_fwd_impl(q, k, v, in_dtype, log_decay, aug_balance, init_state, o, final_state,
+                        workspace, workspace_bytes, B, T, H, dk, dv, gla::StatePages{}, stream);
+}
 
-  gla::FwdArgs a;
-  a.q = q; a.k = k; a.v = v; a.bf16 = in_dtype == GLA_BF16;
-  a.log_decay = log_decay; a.aug = aug_balance; a.init = init_state;
-  a.o = o; a.fin = final_state; a.B = B; a.T = T; a.H = H;
-  if (in_dtype == GLA_FP32) {
-    const size_t tok = (size_t)B * T * H;
-    uint8_t* w = static_cast<uint8_t*>(workspace);
-    void* hq = w;
-    void* hk = w + round256(tok * dk * 2);
-    void* hv = w + 2 * round256(tok * dk * 2);
-    if (gla::launch_to_half((const float*)q, hq, (long long)(tok * dk), ctl, stream) != cudaSuccess ||
-        gla::launch_to_half((const float*)k, hk, (long long)(tok * dk), ctl, stream) != cudaSuccess ||
-        gla::launch_to_half((const float*)v, hv, (long long)(tok * dv), ctl, stream) != cudaSuccess)
-      return GLA_ERR_CUDA;
-    a.q = hq; a.k = hk; a.v = hv; a.bf16 = false;
-  }
-  const cudaError_t e =
-      G > 1 ? gla::launch_chunk_fwd_segmented(a, G, static_cast<uint8_t*>(workspace) + round256(must),
-                                              ctl, stream)
-            : gla::launch_chunk_fwd(a, ctl, stream);
-  return e == cudaSuccess ? GLA_OK : GLA_ERR_CUDA;
+gla_status gla_chunk_fwd_paged(const void* q, const void* k, const void* v, gla_dtype in_dtype,
+                               const float* log_decay, const float* aug_balance, float* pool,
+                               const int* page, int n_pages, int pool_layers, int layer,
+                               int init_from_pool, float* o, void* workspace,
+                               size_t workspace_bytes, int B, int T, int H, int dk, int dv,
+                               cudaStream_t stream) {
+  if (!pool || !page) return GLA_ERR_INVALID_ARG;
+  if (n_pages <= 0 || pool_layers <= 0 || layer < 0 || layer >= pool_layers || H <= 0)
+    return GLA_ERR_INVALID_ARG;
+  if ((long long)n_pages * pool_layers * H > (1ll << 31) - 1) return GLA_ERR_UNSUPPORTED;
+  if (!aligned16(page)) return GLA_ERR_ALIGNMENT;
+  gla::StatePages sp;
+  sp.page = page;
+  sp.n_pages = n_pages;
+  sp.pool_layers = pool_layers;
+  sp.layer = layer;
+  sp.init_paged = init_from_pool != 0;
+  return chunk_fwd_impl(q, k, v, in_dtype, log_decay, aug_balance, sp.init_paged ? pool : nullptr,
+                        o, pool, workspace, workspace_bytes, B, T, H, dk, dv, sp, stream);
 }
 
 size_t gla_chunk_bwd_workspace_size(int B, int T, int H, int dk, int dv, gla_dtype in_dtype) {
@@ -232,6 +263,32 @@ gla_status gla_decode_step(float* state, const float* q, const float* k, const f
   if (n > (1ll << 31) - 1) return GLA_ERR_UNSUPPORTED;
   return gla::launch_decode(state, q, k, v, log_decay, aug_balance, o, n, L, H, stream) ==
                  cudaSuccess
+             ? GLA_OK
+             : GLA_ERR_CUDA;
+}
+
+gla_status gla_decode_step_paged(float* pool, const int* page, int n_active, int n_pages,
+                                 int pool_layers, int layer0, const float* q, const float* k,
+                                 const float* v, const float* log_decay, const float* aug_balance,
+                                 float* o, int L, int H, int dk, int dv, cudaStream_t stream) {
+  if (n_active < 0 || n_pages <= 0 || pool_layers <= 0 || L <= 0 || H <= 0 || layer0 < 0 ||
+      layer0 + L > pool_layers)
+    return GLA_ERR_INVALID_ARG;
+  if (dk != gla::kDK || dv != gla::kDV) return GLA_ERR_UNSUPPORTED;
+  if (n_active == 0) return GLA_OK;
+  if (!pool || !page || !q || !k || !v || !log_decay || !aug_balance || !o)
+    return GLA_ERR_INVALID_ARG;
+  if (!aligned16(pool) || !aligned16(q) || !aligned16(k) || !aligned16(v) ||
+      !aligned16(log_decay) || !aligned16(aug_balance) || !aligned16(o))
+    return GLA_ERR_ALIGNMENT;
+  if ((long long)n_active * L * H > (1ll << 31) - 1 ||
+      (long long)n_pages * pool_layers * H > (1ll << 40))
+    return GLA_ERR_UNSUPPORTED;
+  gla::DevCtl ctl;
+  gla_status st = ctl_for_current_device(&ctl);
+  if (st != GLA_OK) return st;
+  return gla::launch_decode_paged(pool, page, n_pages, pool_layers, layer0, q, k, v, log_decay,
+                                  aug_balance, o, n_active, L, H, ctl, stream) == cudaSuccess
              ? GLA_OK
              : GLA_ERR_CUDA;
 }

@@ -91,7 +91,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
            const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o,
            const __grid_constant__ CUtensorMap map_fin, const float* __restrict__ log_decay,
            const float* __restrict__ aug, const float* __restrict__ init, float* __restrict__ out,
-           float* __restrict__ fin, int T, int H, int seg, DevCtl ctl) {
+           float* __restrict__ fin, int T, int H, int seg, StatePages sp, DevCtl ctl) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   Cta cta;
   cta.base = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -414,8 +414,21 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
       return m;
     };
 
+    // slot of this sequence's initial/final state: [b / seg][h] of the caller's arrays, or
+    // its page of a state pool
+    const int breal = b / seg;
+    long long zst = (long long)breal * H + h;
+    bool page_ok = true;
+    if (sp.page) {
+      const int pg = __ldg(sp.page + breal);
+      page_ok = pg >= 0 && pg < sp.n_pages;
+      zst = ((long long)pg * sp.pool_layers + sp.layer) * H + h;
+      if (!page_ok && tid == 128) record_error(ctl, DEV_RANGE);
+    }
+    const long long zinit = sp.init_paged ? zst : bh;
     // initial state: its exponent needs its exact max first (one exchange in the group)
-    const float* g_row0 = (init && i < DK) ? init + ((size_t)bh * DK + i) * DV : nullptr;
+    const float* g_row0 =
+        (init && page_ok && i < DK) ? init + ((size_t)zinit * DK + i) * DV : nullptr;
     int e_cur = 0;
     {
       float m = 0.f;
@@ -482,7 +495,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
       mbar_arrive(cta.bar(EP_O));
       // ---- final state (after the last chunk), staged through the same rows
       // (with seg > 1 the CTAs are segments of longer sequences: only the last one's counts)
-      if (c == nc - 1 && fin && q4 < 3 && b % seg == seg - 1) {
+      if (c == nc - 1 && fin && q4 < 3 && b % seg == seg - 1 && page_ok) {
         if (lane == 0) bulk_wait_read<0>();
         __syncwarp();
         emit_rows_tma<6>(
@@ -495,7 +508,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
               for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(r[j]);
             },
             [&](int k, uint32_t src) {
-              tma_store_3d(&map_fin, src, 96 * hf + 16 * k, 32 * q4, (b / seg) * H + h);
+              tma_store_3d(&map_fin, src, 96 * hf + 16 * k, 32 * q4, (int)zst);
             });
       }
       if (lane == 0) bulk_wait_read<0>();  // the staging buffers are free for the next chunk
@@ -525,13 +538,14 @@ cudaError_t launch_chunk_fwd(const FwdArgs& a, DevCtl ctl, cudaStream_t stream) 
       !make_tmap_3d_16bit(&mv, a.v, DV, a.H, rows, 64, C, CU_TENSOR_MAP_SWIZZLE_128B, a.bf16) ||
       !make_tmap_out_f32(&mo, a.o, DV, a.H, rows) ||
       !make_tmap_state_f32(&mfin, a.fin ? (const void*)a.fin : (const void*)a.o,
-                           (long long)(a.B / a.seg) * a.H))
+                           a.sp.page ? (long long)a.sp.n_pages * a.sp.pool_layers * a.H
+                                     : (long long)(a.B / a.seg) * a.H))
     return cudaErrorInvalidValue;
   auto kern = a.bf16 ? fwd_kernel<true> : fwd_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
   kern<<<a.B * a.H, THREADS, SMEM_BYTES, stream>>>(mq, mk, mv, mo, mfin, a.log_decay, a.aug, a.init, a.o,
-                                                   a.fin, a.T, a.H, a.seg, ctl);
+                                                   a.fin, a.T, a.H, a.seg, a.sp, ctl);
   return cudaGetLastError();
 }
 

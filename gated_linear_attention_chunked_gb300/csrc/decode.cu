@@ -11,6 +11,12 @@
 // 4c..4c+3) and rows 12g..12g+11 (key channels).  All 12 float4 loads of a thread are issued
 // before any use (streaming, evict-first), the update and the partial readout are done in
 // registers, and the 8 row-group partials of S'^T q are summed through shared memory.
+//
+// Paged variant (a state pool with one fixed page per sequence, as the vLLM wrapper of the
+// same section keeps it): the CTA of active sequence n, layer l, head h updates the state of
+// page[n] -- pool[(page[n] * pool_layers + layer0 + l) * H + h] -- so the active set is any
+// list of pages, in any order, with no padding.  A page outside [0, n_pages) records
+// DEV_RANGE and its CTA touches nothing.
 #include <cuda_runtime.h>
 
 #include "kernels.h"
@@ -21,19 +27,37 @@ namespace {
 constexpr int DK = 96, DV = 192, DV4 = DV / 4, RG = 8, ROWS = DK / RG, THREADS = DV4 * RG;
 static_assert(ROWS * RG == DK && THREADS == 384, "decode tiling");
 
+struct Pages {
+  const int* page;  // null: state s is state[s]
+  int n_pages, pool_layers, layer0;
+  DevCtl ctl;
+};
+
+template <bool PAGED>
 __global__ void __launch_bounds__(THREADS, 2)
 decode_kernel(float* __restrict__ state, const float* __restrict__ q,
               const float* __restrict__ k, const float* __restrict__ v,
               const float* __restrict__ log_decay, const float* __restrict__ aug,
-              float* __restrict__ o, int L, int H) {
+              float* __restrict__ o, int L, int H, Pages pg) {
   __shared__ float sq[DK], sk[DK];
   __shared__ float4 sv[DV4];
   __shared__ float4 part[RG][DV4];
   __shared__ float sgate;
 
-  const long long s = blockIdx.x;  // state index ((seq * L + l) * H + h)
+  const long long s = blockIdx.x;  // index of q, k, v, o: ((seq * L + l) * H + h)
   const int t = threadIdx.x, c4 = t % DV4, g = t / DV4;
-  float4* S = reinterpret_cast<float4*>(state + s * (long long)(DK * DV)) + g * ROWS * DV4 + c4;
+  long long ss = s;  // index of the state
+  if constexpr (PAGED) {
+    const long long n = s / ((long long)L * H);
+    const int lh = (int)(s % ((long long)L * H));
+    const int p = __ldg(pg.page + n);
+    if (p < 0 || p >= pg.n_pages) {  // the same page for every thread of the CTA
+      if (t == 0) record_error(pg.ctl, DEV_RANGE);
+      return;
+    }
+    ss = ((long long)p * pg.pool_layers + pg.layer0 + lh / H) * H + lh % H;
+  }
+  float4* S = reinterpret_cast<float4*>(state + ss * (long long)(DK * DV)) + g * ROWS * DV4 + c4;
 
   float4 x[ROWS];
 #pragma unroll
@@ -99,8 +123,20 @@ cudaError_t launch_decode(float* state, const float* q, const float* k, const fl
                           const float* log_decay, const float* aug, float* o, long long n_states,
                           int L, int H, cudaStream_t stream) {
   if (n_states <= 0) return cudaSuccess;
-  decode_kernel<<<(unsigned)n_states, THREADS, 0, stream>>>(state, q, k, v, log_decay, aug, o,
-                                                             L, H);
+  decode_kernel<false><<<(unsigned)n_states, THREADS, 0, stream>>>(state, q, k, v, log_decay, aug,
+                                                                    o, L, H, Pages{});
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_paged(float* pool, const int* page, int n_pages, int pool_layers,
+                                int layer0, const float* q, const float* k, const float* v,
+                                const float* log_decay, const float* aug, float* o, int n_active,
+                                int L, int H, DevCtl ctl, cudaStream_t stream) {
+  const long long n_states = (long long)n_active * L * H;
+  if (n_states <= 0) return cudaSuccess;
+  Pages pg{page, n_pages, pool_layers, layer0, ctl};
+  decode_kernel<true><<<(unsigned)n_states, THREADS, 0, stream>>>(pool, q, k, v, log_decay, aug, o,
+                                                                   L, H, pg);
   return cudaGetLastError();
 }
 

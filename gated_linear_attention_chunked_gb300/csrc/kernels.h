@@ -14,9 +14,25 @@ cudaError_t launch_decode(float* state, const float* q, const float* k, const fl
                           const float* log_decay, const float* aug, float* o, long long n_states,
                           int L, int H, cudaStream_t stream);
 
+// The same step over a pool of pages: active sequence n uses the states of page[n], layers
+// layer0 .. layer0+L-1 of the pool's pool_layers; pages outside [0, n_pages) record DEV_RANGE.
+cudaError_t launch_decode_paged(float* pool, const int* page, int n_pages, int pool_layers,
+                                int layer0, const float* q, const float* k, const float* v,
+                                const float* log_decay, const float* aug, float* o, int n_active,
+                                int L, int H, DevCtl ctl, cudaStream_t stream);
+
 // fp32 -> fp16 copy (for GLA_FP32 inputs); values with |x| >= 65504 record DEV_RANGE.
 cudaError_t launch_to_half(const float* src, void* dst, long long n, DevCtl ctl,
                            cudaStream_t stream);
+
+// Initial/final states in a pool with one page per sequence: sequence b's slot is
+// pool[(page[b] * pool_layers + layer) * H + h]; init_paged: the initial state is read from
+// that slot too (else from init as [b][h]).  page == null: the caller's [B][H] arrays.
+struct StatePages {
+  const int* page = nullptr;
+  int n_pages = 0, pool_layers = 1, layer = 0;
+  bool init_paged = false;
+};
 
 struct FwdArgs {
   const void* q;  // [B,T,H,96] 16-bit
@@ -32,6 +48,7 @@ struct FwdArgs {
   // seg > 1: the B "sequences" are seg consecutive segments of each of B/seg longer ones;
   // only the last segment of each writes its final state, to fin[b / seg].
   int seg = 1;
+  StatePages sp;  // with sp.page: init and fin are the pool (see StatePages)
 };
 // Returns cudaErrorInvalidValue if a tensor map cannot be encoded.
 cudaError_t launch_chunk_fwd(const FwdArgs& a, DevCtl ctl, cudaStream_t stream);

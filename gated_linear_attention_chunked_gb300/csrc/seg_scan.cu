@@ -204,14 +204,19 @@ seg_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constan
 // g on exit; vinit[b*G][h] receives the caller's initial state (or zeros).  One thread per
 // 4 consecutive state elements, walking the segments in order.
 __global__ void seg_combine_kernel(const float* __restrict__ init, const float* __restrict__ log_decay,
-                                   float* __restrict__ vinit, int H, int G, int L) {
+                                   float* __restrict__ vinit, int H, int G, int L, StatePages sp) {
   constexpr int N4 = DK * DV / 4;
   const int bh = blockIdx.y, b = bh / H, h = bh % H;
   const int e = blockIdx.x * blockDim.x + threadIdx.x;
   if (e >= N4) return;
   const float lamL = expf(__ldg(log_decay + h) * (float)L);  // lambda^L
-  float4 s = init ? __ldg(reinterpret_cast<const float4*>(init) + (size_t)bh * N4 + e)
-                  : make_float4(0.f, 0.f, 0.f, 0.f);
+  long long zi = bh;  // slot of the caller's initial state: [b][h] or a pool page
+  if (sp.init_paged) {
+    const int pg = __ldg(sp.page + b);
+    zi = (pg >= 0 && pg < sp.n_pages) ? ((long long)pg * sp.pool_layers + sp.layer) * H + h : -1;
+  }
+  float4 s = (init && zi >= 0) ? __ldg(reinterpret_cast<const float4*>(init) + (size_t)zi * N4 + e)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
   float4* out = reinterpret_cast<float4*>(vinit);
   out[((size_t)b * G * H + h) * N4 + e] = s;
   for (int g = 1; g < G; ++g) {
@@ -254,13 +259,14 @@ cudaError_t launch_chunk_fwd_segmented(const FwdArgs& a, int G, void* workspace,
                                                              G, ctl);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   seg_combine_kernel<<<dim3((DK * DV / 4 + 255) / 256, a.B * a.H), 256, 0, stream>>>(
-      a.init, a.log_decay, vinit, a.H, G, a.T / G);
+      a.init, a.log_decay, vinit, a.H, G, a.T / G, a.sp);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   FwdArgs c = a;
   c.B = a.B * G;
   c.T = a.T / G;
   c.init = vinit;
   c.seg = G;
+  c.sp.init_paged = false;  // the segments' initial states are in the workspace
   return launch_chunk_fwd(c, ctl, stream);
 }
 

@@ -62,7 +62,7 @@ typedef enum {
   GLA_ERR_ALIGNMENT = 3,   /* a tensor pointer is not 16-byte aligned */
   GLA_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed */
   GLA_ERR_TIMEOUT = 5,     /* device: a bounded wait inside a kernel gave up */
-  GLA_ERR_RANGE = 6,       /* device: an operand or state left the fp16 range */
+  GLA_ERR_RANGE = 6,       /* device: an operand or state left the fp16 range, or a pool page index was out of range */
   GLA_ERR_WORKSPACE = 7,   /* workspace missing or smaller than required */
   GLA_ERR_LAYOUT = 8       /* device: shared memory not aligned as required */
 } gla_status;
@@ -202,6 +202,49 @@ GLA_API gla_status gla_chunk_bwd_noalloc(const void* q, const void* k, const voi
 GLA_API gla_status gla_decode_step(float* state, const float* q, const float* k, const float* v,
                            const float* log_decay, const float* aug_balance, float* o, int N,
                            int L, int H, int dk, int dv, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * State pool with one fixed page per sequence ("Inference optimization on
+ * Trainium2": the model declares itself attention-free, so the serving engine
+ * gives every sequence one fixed page of recurrent state).  A page holds
+ * pool_layers x H states of 96x192 fp32:
+ *
+ *   pool  [n_pages, pool_layers, H, 96, 192] fp32
+ *   state of (page p, layer l, head h) = pool[(p * pool_layers + l) * H + h]
+ *
+ * gla_decode_step_paged: the decode step above for a variable active set, no
+ * padding: active sequence n (0 <= n < n_active) uses page[n] and layers
+ * layer0 .. layer0+L-1 of its page.
+ *   page         [n_active] int32 (device); distinct pages -- two active
+ *                sequences on one page race.  A page outside [0, n_pages)
+ *                leaves that sequence untouched (o not written) and sets the
+ *                device error word to GLA_ERR_RANGE (gla_get_device_error).
+ *   q, k         [n_active,L,H,96] fp32   v, o [n_active,L,H,192] fp32
+ *   log_decay    [H]     aug_balance [L,H,96] (the layers of this call)
+ * n_active == 0 returns GLA_OK without launching.
+ */
+GLA_API gla_status gla_decode_step_paged(float* pool, const int* page, int n_active, int n_pages,
+                                         int pool_layers, int layer0, const float* q,
+                                         const float* k, const float* v, const float* log_decay,
+                                         const float* aug_balance, float* o, int L, int H, int dk,
+                                         int dv, cudaStream_t stream);
+
+/* gla_chunk_fwd_paged: chunked prefill straight into the pool.  Sequence b of
+ * the call (q, k, v, o as in gla_chunk_fwd) starts from the state in layer
+ * `layer` of page[b] (init_from_pool != 0) or from zero (init_from_pool == 0:
+ * the page need not be cleared), and its final state is written back to that
+ * slot.  page [B] int32 (device), distinct pages; a page outside [0, n_pages)
+ * leaves its slot untouched and sets the device error word to GLA_ERR_RANGE.
+ * Workspace: gla_chunk_fwd_workspace_size(B, T, H, ...) as for gla_chunk_fwd
+ * (the segment-parallel path applies here too).
+ */
+GLA_API gla_status gla_chunk_fwd_paged(const void* q, const void* k, const void* v,
+                                       gla_dtype in_dtype, const float* log_decay,
+                                       const float* aug_balance, float* pool, const int* page,
+                                       int n_pages, int pool_layers, int layer,
+                                       int init_from_pool, float* o, void* workspace,
+                                       size_t workspace_bytes, int B, int T, int H, int dk,
+                                       int dv, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

@@ -137,3 +137,19 @@ def decode_step(state, q, k, v, gamma, a, nthreads: int = 0, lib=None):
     if rc != 0:
         raise ValueError("oracle_decode_step: bad sizes")
     return o, st
+
+
+def decode_step_paged(pool, page, layer0, q, k, v, gamma, a, nthreads: int = 0, lib=None):
+    """Decode step over a state pool with one page per sequence (the serving pool of section
+    "Inference optimization on Trainium2").  pool [P, pool_layers, H, dk, dv]; active sequence
+    n updates the states of page[n], layers layer0 .. layer0+L-1, and every other state is
+    left as it is.  It is decode_step on the gathered states, scattered back.
+    Returns (o [n_active, L, H, dv], new_pool); the input array is not modified."""
+    page = np.asarray(page, dtype=np.int64)
+    L = np.asarray(q).shape[1]
+    if len(set(page.tolist())) != len(page):
+        raise ValueError("pages of one call must be distinct")
+    new = np.array(pool, dtype=np.float64, order="C", copy=True)
+    o, st = decode_step(new[page, layer0:layer0 + L], q, k, v, gamma, a, nthreads, lib)
+    new[page, layer0:layer0 + L] = st
+    return o, new

@@ -27,7 +27,8 @@ def declared_symbols():
 def test_header_declares_the_calls():
     names = declared_symbols()
     for n in ("gla_chunk_fwd", "gla_chunk_bwd", "gla_decode_step", "gla_decay_schedule",
-              "gla_get_device_error", "gla_status_string"):
+              "gla_get_device_error", "gla_status_string", "gla_decode_step_paged",
+              "gla_chunk_fwd_paged"):
         assert n in names
 
 
@@ -114,3 +115,23 @@ def test_binding_refuses_host_tensors(lib):
     v = torch.zeros(1, 128, 1, 192, dtype=torch.bfloat16)
     with pytest.raises((ValueError, RuntimeError, AssertionError)):
         gla.chunk_fwd(q, q, v, torch.zeros(1), torch.zeros(1, 96))
+
+
+def test_paged_argument_checks(lib):
+    def dec(n=2, P=4, PL=3, l0=0, L=2, H=2, dk=96, pool=A16, page=A16, q=A16):
+        return lib.gla_decode_step_paged(pool, page, n, P, PL, l0, q, A16, A16, A16, A16, A16,
+                                         L, H, dk, 192, None)
+    assert dec(n=0) == 0                   # empty active set: nothing to do
+    assert dec(l0=2, L=2) == 1             # layers beyond the page
+    assert dec(P=0) == 1 and dec(PL=0) == 1 and dec(n=-1) == 1 and dec(H=0) == 1
+    assert dec(dk=64) == 2
+    assert dec(page=None) == 1 and dec(pool=None) == 1
+    assert dec(q=A16 + 4) == 3
+
+    def fwdp(layer=0, PL=2, P=3, page=A16, pool=A16, T=128):
+        return lib.gla_chunk_fwd_paged(A16, A16, A16, 0, A16, A16, pool, page, P, PL, layer, 1,
+                                       A16, None, 0, 1, T, 1, 96, 192, None)
+    assert fwdp(layer=2) == 1 and fwdp(layer=-1) == 1 and fwdp(P=0) == 1
+    assert fwdp(page=None) == 1 and fwdp(pool=None) == 1
+    assert fwdp(page=A16 + 4) == 3
+    assert fwdp(T=100) == 2
