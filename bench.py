@@ -407,6 +407,55 @@ def run_gpu(args, rank, world, local_rank):
     return 0
 
 
+def run_head_norm(args):
+    """--part norm: the output epilogue (Head RMSNorm per decay tier, SiLU(g) gate) and its
+    gradient at the training shape B=32, T=2048, H=16, 4 tiers; o, dy fp32, g bf16."""
+    import torch
+    import gated_linear_attention_chunked_gb300 as gla
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    gla.load()
+    n_tok, tiers = B * T, 4
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(99)
+    o = torch.randn(n_tok, H, DV, generator=gen, device=dev)
+    g = torch.randn(n_tok, H, DV, generator=gen, device=dev).bfloat16()
+    dy = torch.randn(n_tok, H, DV, generator=gen, device=dev)
+    w = 1.0 + 0.2 * torch.randn(tiers, DV, generator=gen, device=dev)
+    y = torch.empty_like(o)
+    ws = torch.empty(gla.head_norm_gate_bwd_workspace_size(n_tok, H), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def timed(fn, n):
+        for _ in range(args.warmup):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n
+
+    n = max(args.steps, 5)
+    f_ms = timed(lambda: gla.head_norm_gate(o, g, w, tiers, out=y), n)
+    b_ms = timed(lambda: gla.head_norm_gate_bwd(dy, o, g, w, tiers, workspace=ws), n)
+    if gla.get_device_error() != 0:
+        raise RuntimeError("device error")
+    rows = n_tok * H
+    fb = rows * (DV * 4 + DV * 2 + DV * 4)               # o, g in; y out
+    bb = rows * (DV * 4 + DV * 4 + DV * 2 + 2 * DV * 4)  # dy, o, g in; d_o, dg out
+    pk = peaks()
+    print(json.dumps(dict(part="norm", workload="head RMSNorm (4 tiers) + SiLU gate, B=32 T=2048 "
+                          "H=16: o, dy fp32, g bf16", fwd_ms=f_ms, fwd_gbs=fb / (f_ms * 1e-3) / 1e9,
+                          fwd_frac_hbm=fb / (f_ms * 1e-3) / 1e9 / pk["hbm"], bwd_ms=b_ms,
+                          bwd_gbs=bb / (b_ms * 1e-3) / 1e9,
+                          bwd_frac_hbm=bb / (b_ms * 1e-3) / 1e9 / pk["hbm"],
+                          peak_source=pk["src"])), flush=True)
+    return 0
+
+
 def run_paged_decode(args):
     """--part paged: one decode step over the serving pool (1280 pages x 24 layers x 16 heads
     of 96x192 fp32 states) for an active set of 1024 sequences in shuffled page order, through
@@ -516,7 +565,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seqs", type=int, default=8)
-    ap.add_argument("--part", choices=["all", "fwd", "bwd", "decode", "long", "paged"], default="all",
+    ap.add_argument("--part", choices=["all", "fwd", "bwd", "decode", "long", "paged", "norm"], default="all",
                     help="time one call alone (smaller profiling cases); the default is the "
                          "whole hot path")
     ap.add_argument("--batch", type=int, default=B, help="sequences of the training shape")
@@ -540,6 +589,8 @@ def main():
         return run_long_prefill(args) if rank == 0 else 0
     if args.part == "paged":
         return run_paged_decode(args) if rank == 0 else 0
+    if args.part == "norm":
+        return run_head_norm(args) if rank == 0 else 0
     return run_gpu(args, rank, world, local_rank)
 
 

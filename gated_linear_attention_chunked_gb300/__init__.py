@@ -74,6 +74,15 @@ def load(path: str | None = None):
             lib.gla_chunk_fwd_paged.argtypes = ([_P] * 3 + [_I] + [_P] * 4 + [_I] * 4 + [_P] * 2 +
                                                 [_S] + [_I] * 5 + [_P])
             lib.gla_chunk_fwd_paged.restype = _I
+            _L = ctypes.c_longlong
+            _F = ctypes.c_float
+            lib.gla_head_norm_gate_fwd.argtypes = [_P, _P, _I, _P, _I, _F, _P, _P, _L, _I, _I, _P]
+            lib.gla_head_norm_gate_fwd.restype = _I
+            lib.gla_head_norm_gate_bwd_workspace_size.argtypes = [_L, _I, _I]
+            lib.gla_head_norm_gate_bwd_workspace_size.restype = _S
+            lib.gla_head_norm_gate_bwd.argtypes = ([_P] * 3 + [_I, _P, _I, _F] + [_P] * 4 + [_S] +
+                                                   [_L, _I, _I, _P])
+            lib.gla_head_norm_gate_bwd.restype = _I
             lib.gla_decode_step.restype = _I
             if path is not None:
                 return lib
@@ -262,6 +271,59 @@ def chunk_fwd_paged(q, k, v, log_decay, aug_balance, pool, page, layer, *, init_
         B, T, H, dk, dv, _stream(stream))
     _check("gla_chunk_fwd_paged", rc)
     return out
+
+
+def _gate_code(g):
+    torch = _torch()
+    m = {torch.bfloat16: GLA_BF16, torch.float32: GLA_FP32}
+    if g.dtype not in m:
+        raise TypeError(f"g must be bf16 or fp32, got {g.dtype}")
+    return m[g.dtype]
+
+
+def head_norm_gate_bwd_workspace_size(n_tokens, H) -> int:
+    return load().gla_head_norm_gate_bwd_workspace_size(n_tokens, H, DV)
+
+
+def head_norm_gate(o, g, weight, n_tiers, eps=1e-6, *, want_rstd=False, out=None, stream=None):
+    """Head RMSNorm per decay tier, then the SiLU(g) gate (gla_head_norm_gate_fwd).
+    o [..., H, 192] fp32, g the same shape (bf16 or fp32), weight [n_tiers, 192] fp32.
+    Returns (y fp32, rstd fp32 [..., H] or None)."""
+    torch = _torch()
+    H, dv = o.shape[-2], o.shape[-1]
+    n_tok = o.numel() // (H * dv)
+    if g.shape != o.shape:
+        raise ValueError("g must have the shape of o")
+    if out is None:
+        out = torch.empty_like(o)
+    rstd = torch.empty(o.shape[:-1], dtype=torch.float32, device=o.device) if want_rstd else None
+    f = torch.float32
+    rc = load().gla_head_norm_gate_fwd(
+        _dev(o, "o", f), _dev(g, "g"), _gate_code(g), _dev(weight, "weight", f), n_tiers, eps,
+        _dev(out, "y", f), _dev(rstd, "rstd", f), n_tok, H, dv, _stream(stream))
+    _check("gla_head_norm_gate_fwd", rc)
+    return out, rstd
+
+
+def head_norm_gate_bwd(dy, o, g, weight, n_tiers, eps=1e-6, *, workspace=None, stream=None):
+    """Gradient of the output epilogue (gla_head_norm_gate_bwd): returns (d_o, dg, d_weight),
+    fp32."""
+    torch = _torch()
+    H, dv = o.shape[-2], o.shape[-1]
+    n_tok = o.numel() // (H * dv)
+    d_o = torch.empty_like(o)
+    dg = torch.empty(o.shape, dtype=torch.float32, device=o.device)
+    d_w = torch.empty((n_tiers, dv), dtype=torch.float32, device=o.device)
+    ws = _workspace(load().gla_head_norm_gate_bwd_workspace_size(n_tok, H, dv), o.device,
+                    workspace)
+    f = torch.float32
+    rc = load().gla_head_norm_gate_bwd(
+        _dev(dy, "dy", f), _dev(o, "o", f), _dev(g, "g"), _gate_code(g), _dev(weight, "weight", f),
+        n_tiers, eps, _dev(d_o, "d_o", f), _dev(dg, "dg", f), _dev(d_w, "d_weight", f),
+        _dev(ws, "workspace"), 0 if ws is None else ws.numel() * ws.element_size(), n_tok, H, dv,
+        _stream(stream))
+    _check("gla_head_norm_gate_bwd", rc)
+    return d_o, dg, d_w
 
 
 def get_device_error() -> int:

@@ -293,4 +293,55 @@ gla_status gla_decode_step_paged(float* pool, const int* page, int n_active, int
              : GLA_ERR_CUDA;
 }
 
+static gla_status check_head_norm(const float* o, const void* g, gla_dtype g_dtype,
+                                  const float* weight, int n_tiers, float eps, long long n_tokens,
+                                  int H, int dv) {
+  if (n_tokens < 0 || H <= 0 || n_tiers <= 0 || H % n_tiers != 0 || !(eps >= 0.f) ||
+      !(eps < 1e30f))
+    return GLA_ERR_INVALID_ARG;
+  if (dv != gla::kDV || (g_dtype != GLA_BF16 && g_dtype != GLA_FP32)) return GLA_ERR_UNSUPPORTED;
+  if (n_tokens > 0 && (!o || !g || !weight)) return GLA_ERR_INVALID_ARG;
+  if (!aligned16(o) || !aligned16(g) || !aligned16(weight)) return GLA_ERR_ALIGNMENT;
+  return GLA_OK;
+}
+
+gla_status gla_head_norm_gate_fwd(const float* o, const void* g, gla_dtype g_dtype,
+                                  const float* weight, int n_tiers, float eps, float* y,
+                                  float* rstd, long long n_tokens, int H, int dv,
+                                  cudaStream_t stream) {
+  gla_status st = check_head_norm(o, g, g_dtype, weight, n_tiers, eps, n_tokens, H, dv);
+  if (st != GLA_OK) return st;
+  if (n_tokens > 0 && !y) return GLA_ERR_INVALID_ARG;
+  if (!aligned16(y) || !aligned16(rstd)) return GLA_ERR_ALIGNMENT;
+  return gla::launch_head_norm_fwd(o, g, g_dtype == GLA_BF16, weight, y, rstd, n_tokens * H, H,
+                                   n_tiers, eps, sm_count(), stream) == cudaSuccess
+             ? GLA_OK
+             : GLA_ERR_CUDA;
+}
+
+size_t gla_head_norm_gate_bwd_workspace_size(long long n_tokens, int H, int dv) {
+  if (n_tokens <= 0 || H <= 0 || dv != gla::kDV) return 0;
+  return gla::head_norm_bwd_workspace_bytes(n_tokens * H, H, sm_count());
+}
+
+gla_status gla_head_norm_gate_bwd(const float* dy, const float* o, const void* g,
+                                  gla_dtype g_dtype, const float* weight, int n_tiers, float eps,
+                                  float* d_o, float* dg, float* d_weight, void* workspace,
+                                  size_t workspace_bytes, long long n_tokens, int H, int dv,
+                                  cudaStream_t stream) {
+  gla_status st = check_head_norm(o, g, g_dtype, weight, n_tiers, eps, n_tokens, H, dv);
+  if (st != GLA_OK) return st;
+  if (!d_weight || (n_tokens > 0 && (!dy || !d_o || !dg))) return GLA_ERR_INVALID_ARG;
+  if (!aligned16(dy) || !aligned16(d_o) || !aligned16(dg) || !aligned16(d_weight))
+    return GLA_ERR_ALIGNMENT;
+  const size_t need = gla_head_norm_gate_bwd_workspace_size(n_tokens, H, dv);
+  if (need && (!workspace || workspace_bytes < need)) return GLA_ERR_WORKSPACE;
+  if (need && !aligned256(workspace)) return GLA_ERR_ALIGNMENT;
+  return gla::launch_head_norm_bwd(dy, o, g, g_dtype == GLA_BF16, weight, d_o, dg, d_weight,
+                                   static_cast<float*>(workspace), n_tokens * H, H, n_tiers, eps,
+                                   sm_count(), stream) == cudaSuccess
+             ? GLA_OK
+             : GLA_ERR_CUDA;
+}
+
 }  // extern "C"

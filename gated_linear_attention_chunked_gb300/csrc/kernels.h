@@ -85,4 +85,16 @@ cudaError_t launch_chunk_fwd_segmented(const FwdArgs& a, int G, void* workspace,
 cudaError_t current_device_ctl(DevCtl* ctl);
 cudaError_t launch_chunk_bwd(const BwdArgs& a, DevCtl ctl, cudaStream_t stream);
 
+// Head RMSNorm per decay tier + SiLU(g) gate (head_norm.cu).  rows = tokens * H rows of 192;
+// n_tiers divides H; g bf16 or fp32.  rstd [rows] may be null.  The backward's partial sums
+// of dw need head_norm_bwd_workspace_bytes(rows, H, n_sm) bytes at `part`.
+size_t head_norm_bwd_workspace_bytes(long long rows, int H, int n_sm);
+cudaError_t launch_head_norm_fwd(const float* o, const void* g, bool g_bf16, const float* w,
+                                 float* y, float* rstd, long long rows, int H, int n_tiers,
+                                 float eps, int n_sm, cudaStream_t stream);
+cudaError_t launch_head_norm_bwd(const float* dy, const float* o, const void* g, bool g_bf16,
+                                 const float* w, float* d_o, float* dg, float* dw, float* part,
+                                 long long rows, int H, int n_tiers, float eps, int n_sm,
+                                 cudaStream_t stream);
+
 }  // namespace gla

@@ -246,6 +246,42 @@ GLA_API gla_status gla_chunk_fwd_paged(const void* q, const void* k, const void*
                                        size_t workspace_bytes, int B, int T, int H, int dk,
                                        int dv, cudaStream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * The mixer's output epilogue ("i14 and the Laplace 3B architecture", "GLA
+ * mixer" and "Decay schedule's reach": a Head RMSNorm shared within each decay
+ * tier, then the SiLU(g_t) gate).  Per token t and head h, tier(h) =
+ * h / (H / n_tiers) (consecutive heads, i.e. neighbouring half-lives):
+ *
+ *   r_th   = 1 / sqrt(mean_c o_thc^2 + eps)
+ *   y_thc  = o_thc r_th weight[tier(h), c] SiLU(g_thc),   SiLU(x) = x sigmoid(x)
+ *
+ *   o, y         [n_tokens, H, 192] fp32 (tokens = B*T, any order)
+ *   g            [n_tokens, H, 192] g_dtype (GLA_BF16 or GLA_FP32)
+ *   weight       [n_tiers, 192] fp32, n_tiers divides H
+ *   rstd         [n_tokens, H] fp32 or NULL (written: r_th)
+ * All fp32 arithmetic, nothing allocated.
+ */
+GLA_API gla_status gla_head_norm_gate_fwd(const float* o, const void* g, gla_dtype g_dtype,
+                                          const float* weight, int n_tiers, float eps, float* y,
+                                          float* rstd, long long n_tokens, int H, int dv,
+                                          cudaStream_t stream);
+
+/* Its gradient for the scalar loss sum(y . dy): with n = o r, s = SiLU(g),
+ *   dg        = dy n weight sigmoid(g) (1 + g (1 - sigmoid(g)))
+ *   d_o       = r (dn - n mean_c(dn n)),   dn = dy s weight
+ *   d_weight  [n_tiers, 192] = sum over tokens and each tier's heads of dy s n
+ * (written, summed in a fixed order: deterministic).  dy, d_o, dg [n_tokens,
+ * H, 192] fp32.  workspace: gla_head_norm_gate_bwd_workspace_size() bytes,
+ * 256-byte aligned (per-row-slot partial sums of d_weight).
+ */
+GLA_API size_t gla_head_norm_gate_bwd_workspace_size(long long n_tokens, int H, int dv);
+GLA_API gla_status gla_head_norm_gate_bwd(const float* dy, const float* o, const void* g,
+                                          gla_dtype g_dtype, const float* weight, int n_tiers,
+                                          float eps, float* d_o, float* dg, float* d_weight,
+                                          void* workspace, size_t workspace_bytes,
+                                          long long n_tokens, int H, int dv,
+                                          cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

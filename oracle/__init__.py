@@ -5,9 +5,11 @@ against.  Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU
 baseline leg may import it; the product package never does, and it shares no
 code with the CUDA library.
 
-The arithmetic lives in ``gla_oracle.c`` (token-by-token recurrence, hand-derived
-backward, decode step, decay schedule); this module only compiles it with gcc,
-loads it with ctypes and converts numpy arrays to contiguous float64.
+The mixer's arithmetic lives in ``gla_oracle.c`` (token-by-token recurrence,
+hand-derived backward, decode step, decay schedule); this module compiles it with
+gcc, loads it with ctypes and converts numpy arrays to contiguous float64.  The
+state-pool decode is that decode step on gathered pages, and the output epilogue
+(Head RMSNorm per decay tier, SiLU gate) is written out below in fp64 numpy.
 
 Source: "Beyond the KV cache: Training and serving i14's Laplace 3B linear
 attention model on AWS Trainium2 with native PyTorch", section "i14 and the
@@ -153,3 +155,44 @@ def decode_step_paged(pool, page, layer0, q, k, v, gamma, a, nthreads: int = 0, 
     o, st = decode_step(new[page, layer0:layer0 + L], q, k, v, gamma, a, nthreads, lib)
     new[page, layer0:layer0 + L] = st
     return o, new
+
+
+# --------------------------------------------------------------------------- output epilogue
+# Head RMSNorm shared within each decay tier, then the SiLU(g) gate (section "i14 and the
+# Laplace 3B architecture", "GLA mixer" and "Decay schedule's reach").  Plain fp64 numpy, the
+# definition written out: tier(h) = h // (H // n_tiers).
+
+def _tiers(H, n_tiers):
+    if n_tiers <= 0 or H % n_tiers:
+        raise ValueError("n_tiers must divide H")
+    return np.arange(H) // (H // n_tiers)
+
+
+def head_norm_gate(o, g, weight, n_tiers, eps):
+    """y[t,h,c] = o[t,h,c] r[t,h] weight[tier(h),c] SiLU(g[t,h,c]) with
+    r = 1/sqrt(mean_c o^2 + eps).  o, g [N,H,C]; weight [n_tiers,C].  Returns (y, r)."""
+    o, g, w = (np.asarray(x, np.float64) for x in (o, g, weight))
+    tier = _tiers(o.shape[1], n_tiers)
+    r = 1.0 / np.sqrt(np.mean(o * o, axis=-1) + eps)
+    silu = g / (1.0 + np.exp(-g))
+    return o * r[..., None] * w[tier][None] * silu, r
+
+
+def head_norm_gate_bwd(dy, o, g, weight, n_tiers, eps):
+    """Gradient of sum(y * dy) (hand-derived): returns (d_o, dg, d_weight)."""
+    dy, o, g, w = (np.asarray(x, np.float64) for x in (dy, o, g, weight))
+    H, C = o.shape[1], o.shape[2]
+    tier = _tiers(H, n_tiers)
+    r = (1.0 / np.sqrt(np.mean(o * o, axis=-1) + eps))[..., None]
+    n = o * r
+    sg = 1.0 / (1.0 + np.exp(-g))
+    s = g * sg
+    wt = w[tier][None]
+    dg = dy * n * wt * sg * (1.0 + g * (1.0 - sg))
+    dn = dy * s * wt
+    d_o = r * (dn - n * np.mean(dn * n, axis=-1, keepdims=True))
+    per_head = np.sum(dy * s * n, axis=0)  # [H, C]
+    d_w = np.zeros((n_tiers, C))
+    for h in range(H):
+        d_w[tier[h]] += per_head[h]
+    return d_o, dg, d_w

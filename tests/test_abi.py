@@ -135,3 +135,17 @@ def test_paged_argument_checks(lib):
     assert fwdp(page=None) == 1 and fwdp(pool=None) == 1
     assert fwdp(page=A16 + 4) == 3
     assert fwdp(T=100) == 2
+
+
+def test_head_norm_argument_checks(lib):
+    def fwdn(n_tiers=4, H=16, dv=192, eps=1e-6, gdt=0, o=A16, y=A16, N=3):
+        return lib.gla_head_norm_gate_fwd(o, A16, gdt, A16, n_tiers, eps, y, None, N, H, dv, None)
+    assert fwdn(n_tiers=3) == 1          # tiers must divide the heads
+    assert fwdn(n_tiers=0) == 1 and fwdn(H=0) == 1 and fwdn(N=-1) == 1
+    assert fwdn(eps=-1.0) == 1
+    assert fwdn(dv=96) == 2 and fwdn(gdt=2) == 2   # fp16 gate not offered
+    assert fwdn(o=None) == 1 and fwdn(y=None) == 1
+    assert fwdn(o=A16 + 8) == 3
+    assert lib.gla_head_norm_gate_bwd_workspace_size(0, 16, 192) == 0
+    assert lib.gla_head_norm_gate_bwd(A16, A16, A16, 0, A16, 4, 1e-6, A16, A16, A16, None, 0,
+                                      3, 16, 192, None) in (7, 4)  # needs a workspace
