@@ -407,6 +407,64 @@ def run_gpu(args, rank, world, local_rank):
     return 0
 
 
+def run_conv(args):
+    """--part conv: the causal depth-wise conv + SiLU at the training shape (B=32, T=2048,
+    D=3072, x bf16), forward and gradient, and one decode step over 1280 sequences x 24 layers
+    of 3-input states."""
+    import torch
+    import gated_linear_attention_chunked_gb300 as gla
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    gla.load()
+    Dm = 3072
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(55)
+    x = torch.randn(B, T, Dm, generator=gen, device=dev).bfloat16()
+    dy = torch.randn(B, T, Dm, generator=gen, device=dev)
+    w = 0.5 * torch.randn(Dm, 4, generator=gen, device=dev)
+    b = 0.1 * torch.randn(Dm, generator=gen, device=dev)
+    init = torch.randn(B, 3, Dm, generator=gen, device=dev)
+    y = torch.empty(B, T, Dm, device=dev)
+    ws = torch.empty(gla.load().gla_conv_bwd_workspace_size(B, T, Dm), dtype=torch.uint8, device=dev)
+    n_dec = N_SEQ * N_LAYERS
+    st = torch.randn(n_dec, 3, Dm, generator=gen, device=dev)
+    xd = torch.randn(n_dec, Dm, generator=gen, device=dev)
+    yd = torch.empty_like(xd)
+    stream = torch.cuda.current_stream()
+
+    def timed(fn, n):
+        for _ in range(args.warmup):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n
+
+    n = max(args.steps, 5)
+    f_ms = timed(lambda: gla.conv_fwd(x, w, b, init, out=y), n)
+    b_ms = timed(lambda: gla.conv_bwd(x, w, dy, b, init, workspace=ws), n)
+    d_ms = timed(lambda: gla.conv_decode_step(st, xd, w, b, out=yd), n)
+    if gla.get_device_error() != 0:
+        raise RuntimeError("device error")
+    el = B * T * Dm
+    fb, bb = el * (2 + 4), el * (2 + 4 + 4)          # x bf16 + y | x + dy + dx
+    db_ = n_dec * Dm * (3 * 4 * 2 + 4 + 4)            # state r+w, x, y
+    pk = peaks()
+    gbs = lambda byts, ms: byts / (ms * 1e-3) / 1e9
+    print(json.dumps(dict(part="conv", workload="causal depth-wise conv k=4 + SiLU, B=32 T=2048 "
+                          "D=3072 (x bf16), decode over 1280 x 24 states", fwd_ms=f_ms,
+                          fwd_gbs=gbs(fb, f_ms), fwd_frac_hbm=gbs(fb, f_ms) / pk["hbm"], bwd_ms=b_ms,
+                          bwd_gbs=gbs(bb, b_ms), bwd_frac_hbm=gbs(bb, b_ms) / pk["hbm"],
+                          decode_ms=d_ms, decode_gbs=gbs(db_, d_ms),
+                          decode_frac_hbm=gbs(db_, d_ms) / pk["hbm"], peak_source=pk["src"])),
+          flush=True)
+    return 0
+
+
 def run_head_norm(args):
     """--part norm: the output epilogue (Head RMSNorm per decay tier, SiLU(g) gate) and its
     gradient at the training shape B=32, T=2048, H=16, 4 tiers; o, dy fp32, g bf16."""
@@ -565,7 +623,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seqs", type=int, default=8)
-    ap.add_argument("--part", choices=["all", "fwd", "bwd", "decode", "long", "paged", "norm"], default="all",
+    ap.add_argument("--part", choices=["all", "fwd", "bwd", "decode", "long", "paged", "norm", "conv"], default="all",
                     help="time one call alone (smaller profiling cases); the default is the "
                          "whole hot path")
     ap.add_argument("--batch", type=int, default=B, help="sequences of the training shape")
@@ -591,6 +649,8 @@ def main():
         return run_paged_decode(args) if rank == 0 else 0
     if args.part == "norm":
         return run_head_norm(args) if rank == 0 else 0
+    if args.part == "conv":
+        return run_conv(args) if rank == 0 else 0
     return run_gpu(args, rank, world, local_rank)
 
 

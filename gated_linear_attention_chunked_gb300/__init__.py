@@ -83,6 +83,14 @@ def load(path: str | None = None):
             lib.gla_head_norm_gate_bwd.argtypes = ([_P] * 3 + [_I, _P, _I, _F] + [_P] * 4 + [_S] +
                                                    [_L, _I, _I, _P])
             lib.gla_head_norm_gate_bwd.restype = _I
+            lib.gla_conv_fwd.argtypes = [_P, _I] + [_P] * 5 + [_I] * 3 + [_P]
+            lib.gla_conv_fwd.restype = _I
+            lib.gla_conv_bwd_workspace_size.argtypes = [_I] * 3
+            lib.gla_conv_bwd_workspace_size.restype = _S
+            lib.gla_conv_bwd.argtypes = [_P, _I] + [_P] * 9 + [_S] + [_I] * 3 + [_P]
+            lib.gla_conv_bwd.restype = _I
+            lib.gla_conv_decode_step.argtypes = [_P] * 5 + [_L, _I, _P]
+            lib.gla_conv_decode_step.restype = _I
             lib.gla_decode_step.restype = _I
             if path is not None:
                 return lib
@@ -324,6 +332,66 @@ def head_norm_gate_bwd(dy, o, g, weight, n_tiers, eps=1e-6, *, workspace=None, s
         _stream(stream))
     _check("gla_head_norm_gate_bwd", rc)
     return d_o, dg, d_w
+
+
+def _x_code(x):
+    torch = _torch()
+    m = {torch.bfloat16: GLA_BF16, torch.float32: GLA_FP32}
+    if x.dtype not in m:
+        raise TypeError(f"x must be bf16 or fp32, got {x.dtype}")
+    return m[x.dtype]
+
+
+def conv_fwd(x, weight, bias=None, init_state=None, *, want_final_state=True, out=None,
+             stream=None):
+    """Causal depth-wise Conv1d (width 4) + SiLU (gla_conv_fwd).  x [B,T,D] bf16/fp32,
+    weight [D,4], bias [D], init_state [B,3,D].  Returns (y fp32, final_state or None)."""
+    torch = _torch()
+    B, T, D = x.shape
+    f = torch.float32
+    y = out if out is not None else torch.empty((B, T, D), dtype=f, device=x.device)
+    fin = torch.empty((B, 3, D), dtype=f, device=x.device) if want_final_state else None
+    rc = load().gla_conv_fwd(_dev(x, "x"), _x_code(x), _dev(weight, "weight", f),
+                             _dev(bias, "bias", f), _dev(init_state, "init_state", f),
+                             _dev(y, "y", f), _dev(fin, "final_state", f), B, T, D, _stream(stream))
+    _check("gla_conv_fwd", rc)
+    return y, fin
+
+
+def conv_bwd(x, weight, dy, bias=None, init_state=None, *, want_d_init_state=True,
+             workspace=None, stream=None):
+    """Gradient of conv_fwd (gla_conv_bwd): returns (dx, d_init_state or None, d_weight,
+    d_bias), fp32."""
+    torch = _torch()
+    B, T, D = x.shape
+    f = torch.float32
+    dx = torch.empty((B, T, D), dtype=f, device=x.device)
+    dinit = torch.empty((B, 3, D), dtype=f, device=x.device) if want_d_init_state else None
+    dw = torch.empty((D, 4), dtype=f, device=x.device)
+    db = torch.empty((D,), dtype=f, device=x.device)
+    ws = _workspace(load().gla_conv_bwd_workspace_size(B, T, D), x.device, workspace)
+    rc = load().gla_conv_bwd(_dev(x, "x"), _x_code(x), _dev(weight, "weight", f),
+                             _dev(bias, "bias", f), _dev(init_state, "init_state", f),
+                             _dev(dy, "dy", f), _dev(dx, "dx", f), _dev(dinit, "d_init_state", f),
+                             _dev(dw, "d_weight", f), _dev(db, "d_bias", f), _dev(ws, "workspace"),
+                             ws.numel() * ws.element_size(), B, T, D, _stream(stream))
+    _check("gla_conv_bwd", rc)
+    return dx, dinit, dw, db
+
+
+def conv_decode_step(state, x, weight, bias=None, *, out=None, stream=None):
+    """One decode token of the conv (gla_conv_decode_step): state [..., 3, D] fp32 updated in
+    place, x [..., D] fp32.  Returns y [..., D]."""
+    torch = _torch()
+    D = x.shape[-1]
+    n = x.numel() // D
+    f = torch.float32
+    y = out if out is not None else torch.empty_like(x)
+    rc = load().gla_conv_decode_step(_dev(state, "state", f), _dev(x, "x", f),
+                                     _dev(weight, "weight", f), _dev(bias, "bias", f),
+                                     _dev(y, "y", f), n, D, _stream(stream))
+    _check("gla_conv_decode_step", rc)
+    return y
 
 
 def get_device_error() -> int:

@@ -20,7 +20,7 @@ OUT_DIR = os.path.join(PKG, "_lib")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libgla.so")
 
-SOURCES = ["api.cu", "decode.cu", "convert.cu", "chunk_fwd.cu", "chunk_bwd.cu", "noalloc.cu", "seg_scan.cu", "head_norm.cu"]
+SOURCES = ["api.cu", "decode.cu", "convert.cu", "chunk_fwd.cu", "chunk_bwd.cu", "noalloc.cu", "seg_scan.cu", "head_norm.cu", "conv.cu"]
 HEADERS = ["ptx.cuh", "tmap.h", "kernels.h", "scan_common.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",

@@ -344,4 +344,70 @@ gla_status gla_head_norm_gate_bwd(const float* dy, const float* o, const void* g
              : GLA_ERR_CUDA;
 }
 
+static gla_status check_conv(const void* x, gla_dtype x_dtype, const float* weight,
+                             const float* bias, const float* init, int B, int T, int D) {
+  if (B <= 0 || T <= 0 || D <= 0) return GLA_ERR_INVALID_ARG;
+  if (D % 4 != 0 || (x_dtype != GLA_BF16 && x_dtype != GLA_FP32)) return GLA_ERR_UNSUPPORTED;
+  if ((long long)B * ((T + 63) / 64) > (1ll << 31) - 1 || (long long)B * T * D > (1ll << 40))
+    return GLA_ERR_UNSUPPORTED;
+  if (!x || !weight) return GLA_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(weight) || !aligned16(bias) || !aligned16(init))
+    return GLA_ERR_ALIGNMENT;
+  return GLA_OK;
+}
+
+gla_status gla_conv_fwd(const void* x, gla_dtype x_dtype, const float* weight, const float* bias,
+                        const float* init_state, float* y, float* final_state, int B, int T,
+                        int D, cudaStream_t stream) {
+  gla_status st = check_conv(x, x_dtype, weight, bias, init_state, B, T, D);
+  if (st != GLA_OK) return st;
+  if (!y) return GLA_ERR_INVALID_ARG;
+  if (!aligned16(y) || !aligned16(final_state)) return GLA_ERR_ALIGNMENT;
+  return gla::launch_conv_fwd(x, x_dtype == GLA_BF16, weight, bias, init_state, y, final_state,
+                              B, T, D, stream) == cudaSuccess
+             ? GLA_OK
+             : GLA_ERR_CUDA;
+}
+
+size_t gla_conv_bwd_workspace_size(int B, int T, int D) {
+  if (B <= 0 || T <= 0 || D <= 0 || D % 4 != 0) return 0;
+  return gla::conv_bwd_workspace_bytes(B, T, D);
+}
+
+gla_status gla_conv_bwd(const void* x, gla_dtype x_dtype, const float* weight, const float* bias,
+                        const float* init_state, const float* dy, float* dx,
+                        float* d_init_state, float* d_weight, float* d_bias, void* workspace,
+                        size_t workspace_bytes, int B, int T, int D, cudaStream_t stream) {
+  gla_status st = check_conv(x, x_dtype, weight, bias, init_state, B, T, D);
+  if (st != GLA_OK) return st;
+  if (!dy || !dx || !d_weight) return GLA_ERR_INVALID_ARG;
+  if (!aligned16(dy) || !aligned16(dx) || !aligned16(d_init_state) || !aligned16(d_weight) ||
+      !aligned16(d_bias))
+    return GLA_ERR_ALIGNMENT;
+  const size_t need = gla_conv_bwd_workspace_size(B, T, D);
+  if (!workspace || workspace_bytes < need) return GLA_ERR_WORKSPACE;
+  if (!aligned256(workspace)) return GLA_ERR_ALIGNMENT;
+  return gla::launch_conv_bwd(x, x_dtype == GLA_BF16, weight, bias, init_state, dy, dx,
+                              d_init_state, d_weight, d_bias, static_cast<float*>(workspace), B,
+                              T, D, stream) == cudaSuccess
+             ? GLA_OK
+             : GLA_ERR_CUDA;
+}
+
+gla_status gla_conv_decode_step(float* state, const float* x, const float* weight,
+                                const float* bias, float* y, long long N, int D,
+                                cudaStream_t stream) {
+  if (N < 0 || D <= 0) return GLA_ERR_INVALID_ARG;
+  if (D % 4 != 0) return GLA_ERR_UNSUPPORTED;
+  if (N == 0) return GLA_OK;
+  if (!state || !x || !weight || !y) return GLA_ERR_INVALID_ARG;
+  if (!aligned16(state) || !aligned16(x) || !aligned16(weight) || !aligned16(bias) ||
+      !aligned16(y))
+    return GLA_ERR_ALIGNMENT;
+  if (N * (D / 4) > (1ll << 40)) return GLA_ERR_UNSUPPORTED;
+  return gla::launch_conv_decode(state, x, weight, bias, y, N, D, stream) == cudaSuccess
+             ? GLA_OK
+             : GLA_ERR_CUDA;
+}
+
 }  // extern "C"

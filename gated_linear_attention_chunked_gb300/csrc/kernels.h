@@ -97,4 +97,17 @@ cudaError_t launch_head_norm_bwd(const float* dy, const float* o, const void* g,
                                  long long rows, int H, int n_tiers, float eps, int n_sm,
                                  cudaStream_t stream);
 
+// Depth-wise causal Conv1d (width 4) + SiLU and its 3-token state (conv.cu).  x [B,T,D] bf16
+// or fp32, w [D,4], bias [D] or null, init/fin [B,3,D] fp32 or null, D % 4 == 0.
+size_t conv_bwd_workspace_bytes(int B, int T, int D);
+cudaError_t launch_conv_fwd(const void* x, bool bf16, const float* w, const float* bias,
+                            const float* init, float* y, float* fin, int B, int T, int D,
+                            cudaStream_t stream);
+cudaError_t launch_conv_bwd(const void* x, bool bf16, const float* w, const float* bias,
+                            const float* init, const float* dy, float* dx, float* dinit,
+                            float* dw, float* db, float* part, int B, int T, int D,
+                            cudaStream_t stream);
+cudaError_t launch_conv_decode(float* state, const float* x, const float* w, const float* bias,
+                               float* y, long long n, int D, cudaStream_t stream);
+
 }  // namespace gla

@@ -282,6 +282,46 @@ GLA_API gla_status gla_head_norm_gate_bwd(const float* dy, const float* o, const
                                           long long n_tokens, int H, int dv,
                                           cudaStream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * Depth-wise causal Conv1d of width 4 with SiLU, in front of the QKVG
+ * projection ("i14 and the Laplace 3B architecture", "Normalization and
+ * convolution"), and its recurrent state of the last 3 inputs per sequence:
+ *
+ *   y_t[d] = SiLU(sum_{j=0..3} weight[d][j] x_{t-3+j}[d] + bias[d])
+ *
+ * with x_{-3..-1} = init_state (zeros if NULL) and final_state = x_{T-3..T-1}
+ * (the state to continue from).
+ *   x            [B,T,D] x_dtype (GLA_BF16 or GLA_FP32), D % 4 == 0
+ *   weight       [D,4] fp32       bias [D] fp32 or NULL (= 0)
+ *   init_state, final_state   [B,3,D] fp32 or NULL
+ *   y            [B,T,D] fp32 (written)
+ */
+GLA_API gla_status gla_conv_fwd(const void* x, gla_dtype x_dtype, const float* weight,
+                                const float* bias, const float* init_state, float* y,
+                                float* final_state, int B, int T, int D, cudaStream_t stream);
+
+/* Gradient for the scalar loss sum(y . dy): dz = dy SiLU'(z),
+ *   dx_s = sum_j weight[j] dz_{s+3-j}    (d_init_state: s = -3..-1; may be NULL)
+ *   d_weight[d][j] = sum_{b,t} dz_t x_{t-3+j},  d_bias[d] = sum_{b,t} dz_t (NULL: skipped)
+ * (summed in a fixed order: deterministic).  The final state is a copy of
+ * the last inputs: a caller that differentiates through it adds its gradient
+ * to dx itself.  dy, dx [B,T,D] fp32; workspace gla_conv_bwd_workspace_size()
+ * bytes, 256-byte aligned.
+ */
+GLA_API size_t gla_conv_bwd_workspace_size(int B, int T, int D);
+GLA_API gla_status gla_conv_bwd(const void* x, gla_dtype x_dtype, const float* weight,
+                                const float* bias, const float* init_state, const float* dy,
+                                float* dx, float* d_init_state, float* d_weight, float* d_bias,
+                                void* workspace, size_t workspace_bytes, int B, int T, int D,
+                                cudaStream_t stream);
+
+/* One decode token: state [N,3,D] fp32 holds x_{t-3..t-1} and becomes
+ * x_{t-2..t} (in place); x, y [N,D] fp32.  N counts sequences (x layers, if
+ * the caller lays a pool out as [N_seq, L, 3, D]). */
+GLA_API gla_status gla_conv_decode_step(float* state, const float* x, const float* weight,
+                                        const float* bias, float* y, long long N, int D,
+                                        cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -196,3 +196,50 @@ def head_norm_gate_bwd(dy, o, g, weight, n_tiers, eps):
     for h in range(H):
         d_w[tier[h]] += per_head[h]
     return d_o, dg, d_w
+
+
+# --------------------------------------------------------------------------- causal conv
+# Depth-wise causal Conv1d of width 4 + SiLU with its 3-input state (section "i14 and the
+# Laplace 3B architecture", "Normalization and convolution").  Plain fp64 numpy, the
+# definition written out: x_{-3..-1} is the state carried in.
+
+def conv_fwd(x, weight, bias=None, init_state=None):
+    """y_t[d] = SiLU(sum_{j=0..3} weight[d,j] x_{t-3+j}[d] + bias[d]).  x [B,T,D], weight
+    [D,4], bias [D], init_state [B,3,D] (x_{-3..-1}; zeros if None).  Returns (y,
+    final_state = x_{T-3..T-1})."""
+    x, w = np.asarray(x, np.float64), np.asarray(weight, np.float64)
+    B, T, D = x.shape
+    prev = np.zeros((B, 3, D)) if init_state is None else np.asarray(init_state, np.float64)
+    xe = np.concatenate([prev, x], axis=1)  # xe[:, t + 3] = x_t
+    z = np.zeros((B, T, D)) if bias is None else np.broadcast_to(np.asarray(bias, np.float64),
+                                                                  (B, T, D)).copy()
+    for j in range(4):
+        z += w[:, j] * xe[:, j:j + T]
+    return z / (1.0 + np.exp(-z)), xe[:, T:T + 3].copy()
+
+
+def conv_bwd(x, weight, dy, bias=None, init_state=None):
+    """Gradient of sum(y * dy) (hand-derived): returns (dx, d_init_state, d_weight, d_bias)."""
+    x, w, dy = (np.asarray(a, np.float64) for a in (x, weight, dy))
+    B, T, D = x.shape
+    prev = np.zeros((B, 3, D)) if init_state is None else np.asarray(init_state, np.float64)
+    xe = np.concatenate([prev, x], axis=1)
+    z = np.zeros((B, T, D)) if bias is None else np.broadcast_to(np.asarray(bias, np.float64),
+                                                                  (B, T, D)).copy()
+    for j in range(4):
+        z += w[:, j] * xe[:, j:j + T]
+    sg = 1.0 / (1.0 + np.exp(-z))
+    dz = dy * sg * (1.0 + z * (1.0 - sg))
+    dxe = np.zeros((B, T + 3, D))
+    dw = np.zeros((D, 4))
+    for j in range(4):
+        dxe[:, j:j + T] += w[:, j] * dz
+        dw[:, j] = np.sum(dz * xe[:, j:j + T], axis=(0, 1))
+    return dxe[:, 3:], dxe[:, :3], dw, np.sum(dz, axis=(0, 1))
+
+
+def conv_decode_step(state, x, weight, bias=None):
+    """One token: the forward with T = 1 from the 3-input state.  state [N,3,D], x [N,D].
+    Returns (y [N,D], new_state)."""
+    y, fin = conv_fwd(np.asarray(x, np.float64)[:, None], weight, bias, state)
+    return y[:, 0], fin

@@ -149,3 +149,17 @@ def test_head_norm_argument_checks(lib):
     assert lib.gla_head_norm_gate_bwd_workspace_size(0, 16, 192) == 0
     assert lib.gla_head_norm_gate_bwd(A16, A16, A16, 0, A16, 4, 1e-6, A16, A16, A16, None, 0,
                                       3, 16, 192, None) in (7, 4)  # needs a workspace
+
+
+def test_conv_argument_checks(lib):
+    def cf(B=1, T=8, D=16, dt=0, x=A16, w=A16, y=A16, init=None):
+        return lib.gla_conv_fwd(x, dt, w, None, init, y, None, B, T, D, None)
+    assert cf(D=6) == 2 and cf(dt=2) == 2
+    assert cf(B=0) == 1 and cf(T=0) == 1 and cf(D=0) == 1
+    assert cf(x=None) == 1 and cf(w=None) == 1 and cf(y=None) == 1
+    assert cf(x=A16 + 8) == 3 and cf(init=A16 + 4) == 3
+    assert lib.gla_conv_bwd_workspace_size(1, 8, 16) > 0
+    assert lib.gla_conv_bwd(A16, 0, A16, None, None, A16, A16, None, A16, None, None, 0, 1, 8, 16,
+                            None) == 7
+    assert lib.gla_conv_decode_step(A16, A16, A16, None, A16, 0, 16, None) == 0
+    assert lib.gla_conv_decode_step(A16, A16, A16, None, A16, 2, 6, None) == 2
