@@ -419,14 +419,15 @@ def run_conv(args):
     Dm = 3072
     gen = torch.Generator(device=dev)
     gen.manual_seed(55)
-    x = torch.randn(B, T, Dm, generator=gen, device=dev).bfloat16()
-    dy = torch.randn(B, T, Dm, generator=gen, device=dev)
+    Bc = args.batch
+    x = torch.randn(Bc, T, Dm, generator=gen, device=dev).bfloat16()
+    dy = torch.randn(Bc, T, Dm, generator=gen, device=dev)
     w = 0.5 * torch.randn(Dm, 4, generator=gen, device=dev)
     b = 0.1 * torch.randn(Dm, generator=gen, device=dev)
-    init = torch.randn(B, 3, Dm, generator=gen, device=dev)
-    y = torch.empty(B, T, Dm, device=dev)
-    ws = torch.empty(gla.load().gla_conv_bwd_workspace_size(B, T, Dm), dtype=torch.uint8, device=dev)
-    n_dec = N_SEQ * N_LAYERS
+    init = torch.randn(Bc, 3, Dm, generator=gen, device=dev)
+    y = torch.empty(Bc, T, Dm, device=dev)
+    ws = torch.empty(gla.load().gla_conv_bwd_workspace_size(Bc, T, Dm), dtype=torch.uint8, device=dev)
+    n_dec = args.n_seq * N_LAYERS
     st = torch.randn(n_dec, 3, Dm, generator=gen, device=dev)
     xd = torch.randn(n_dec, Dm, generator=gen, device=dev)
     yd = torch.empty_like(xd)
@@ -450,13 +451,13 @@ def run_conv(args):
     d_ms = timed(lambda: gla.conv_decode_step(st, xd, w, b, out=yd), n)
     if gla.get_device_error() != 0:
         raise RuntimeError("device error")
-    el = B * T * Dm
+    el = Bc * T * Dm
     fb, bb = el * (2 + 4), el * (2 + 4 + 4)          # x bf16 + y | x + dy + dx
     db_ = n_dec * Dm * (3 * 4 * 2 + 4 + 4)            # state r+w, x, y
     pk = peaks()
     gbs = lambda byts, ms: byts / (ms * 1e-3) / 1e9
-    print(json.dumps(dict(part="conv", workload="causal depth-wise conv k=4 + SiLU, B=32 T=2048 "
-                          "D=3072 (x bf16), decode over 1280 x 24 states", fwd_ms=f_ms,
+    print(json.dumps(dict(part="conv", workload=f"causal depth-wise conv k=4 + SiLU, B={Bc} T=2048 "
+                          f"D=3072 (x bf16), decode over {args.n_seq} x 24 states", fwd_ms=f_ms,
                           fwd_gbs=gbs(fb, f_ms), fwd_frac_hbm=gbs(fb, f_ms) / pk["hbm"], bwd_ms=b_ms,
                           bwd_gbs=gbs(bb, b_ms), bwd_frac_hbm=gbs(bb, b_ms) / pk["hbm"],
                           decode_ms=d_ms, decode_gbs=gbs(db_, d_ms),
@@ -473,7 +474,7 @@ def run_head_norm(args):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     gla.load()
-    n_tok, tiers = B * T, 4
+    n_tok, tiers = args.batch * T, 4
     gen = torch.Generator(device=dev)
     gen.manual_seed(99)
     o = torch.randn(n_tok, H, DV, generator=gen, device=dev)
@@ -505,8 +506,8 @@ def run_head_norm(args):
     fb = rows * (DV * 4 + DV * 2 + DV * 4)               # o, g in; y out
     bb = rows * (DV * 4 + DV * 4 + DV * 2 + 2 * DV * 4)  # dy, o, g in; d_o, dg out
     pk = peaks()
-    print(json.dumps(dict(part="norm", workload="head RMSNorm (4 tiers) + SiLU gate, B=32 T=2048 "
-                          "H=16: o, dy fp32, g bf16", fwd_ms=f_ms, fwd_gbs=fb / (f_ms * 1e-3) / 1e9,
+    print(json.dumps(dict(part="norm", workload=f"head RMSNorm (4 tiers) + SiLU gate, B={args.batch} "
+                          "T=2048 H=16: o, dy fp32, g bf16", fwd_ms=f_ms, fwd_gbs=fb / (f_ms * 1e-3) / 1e9,
                           fwd_frac_hbm=fb / (f_ms * 1e-3) / 1e9 / pk["hbm"], bwd_ms=b_ms,
                           bwd_gbs=bb / (b_ms * 1e-3) / 1e9,
                           bwd_frac_hbm=bb / (b_ms * 1e-3) / 1e9 / pk["hbm"],
@@ -523,11 +524,12 @@ def run_paged_decode(args):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     gla.load()
-    n_act = 1024
+    n_pages = args.n_seq
+    n_act = n_pages * 4 // 5
     gen = torch.Generator(device=dev)
     gen.manual_seed(777)
-    pool = torch.randn(N_SEQ, N_LAYERS, H, DK, DV, generator=gen, device=dev) * 0.05
-    page = torch.randperm(N_SEQ, generator=gen, device=dev)[:n_act].to(torch.int32)
+    pool = torch.randn(n_pages, N_LAYERS, H, DK, DV, generator=gen, device=dev) * 0.05
+    page = torch.randperm(n_pages, generator=gen, device=dev)[:n_act].to(torch.int32)
     q = torch.randn(n_act, N_LAYERS, H, DK, generator=gen, device=dev) * DK ** -0.5
     k = torch.randn(n_act, N_LAYERS, H, DK, generator=gen, device=dev)
     v = torch.randn(n_act, N_LAYERS, H, DV, generator=gen, device=dev)
@@ -550,8 +552,8 @@ def run_paged_decode(args):
     ms = e0.elapsed_time(e1) / n
     byts = n_act * N_LAYERS * H * DEC_BYTES_STATE
     pk = peaks()
-    print(json.dumps(dict(part="paged", workload="paged decode, 1024 active of 1280 pages x 24 x 16 "
-                          "fp32 states, shuffled page order", ms=ms, gbs=byts / (ms * 1e-3) / 1e9,
+    print(json.dumps(dict(part="paged", workload=f"paged decode, {n_act} active of {n_pages} pages "
+                          "x 24 x 16 fp32 states, shuffled page order", ms=ms, gbs=byts / (ms * 1e-3) / 1e9,
                           frac_hbm=byts / (ms * 1e-3) / 1e9 / pk["hbm"], peak_source=pk["src"])),
           flush=True)
     return 0
@@ -566,7 +568,7 @@ def run_long_prefill(args):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     lib = gla.load()
-    Bl, Tl = 2, 131072
+    Bl, Tl = 2, args.long_t
     gen = torch.Generator(device=dev)
     gen.manual_seed(4321)
     rn = lambda *sh, std=1.0: torch.randn(*sh, generator=gen, device=dev) * std
@@ -607,7 +609,7 @@ def run_long_prefill(args):
         raise RuntimeError("device error")
     byts = Bl * Tl * H * FWD_BYTES_TH
     pk = peaks()
-    print(json.dumps(dict(part="long", workload="long prefill fwd B=2 T=131072 H=16 bf16 in, fp32 out",
+    print(json.dumps(dict(part="long", workload=f"long prefill fwd B=2 T={Tl} H=16 bf16 in, fp32 out",
                           ms=seg_ms, tokens_per_s=Bl * Tl / (seg_ms * 1e-3),
                           gbs=byts / (seg_ms * 1e-3) / 1e9, frac_hbm=byts / (seg_ms * 1e-3) / 1e9 / pk["hbm"],
                           peak_source=pk["src"], workspace_bytes=nws, serial_ms=ser_ms)), flush=True)
@@ -628,6 +630,7 @@ def main():
                          "whole hot path")
     ap.add_argument("--batch", type=int, default=B, help="sequences of the training shape")
     ap.add_argument("--n-seq", type=int, default=N_SEQ, help="sequences of the serving pool")
+    ap.add_argument("--long-t", type=int, default=131072, help="tokens of the long prefill (--part long)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
