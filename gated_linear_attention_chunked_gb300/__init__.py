@@ -69,6 +69,8 @@ def load(path: str | None = None):
             lib.gla_chunk_bwd.argtypes = [_P] * 3 + [_I] + [_P] * 11 + [_S] + [_I] * 5 + [_P]
             lib.gla_chunk_bwd.restype = _I
             lib.gla_decode_step.argtypes = [_P] * 7 + [_I] * 5 + [_P]
+            lib.gla_wait_probe.argtypes = [_P]
+            lib.gla_wait_probe.restype = _I
             lib.gla_decode_step_paged.argtypes = [_P, _P] + [_I] * 4 + [_P] * 6 + [_I] * 4 + [_P]
             lib.gla_decode_step_paged.restype = _I
             lib.gla_chunk_fwd_paged.argtypes = ([_P] * 3 + [_I] + [_P] * 4 + [_I] * 4 + [_P] * 2 +
@@ -397,6 +399,12 @@ def conv_decode_step(state, x, weight, bias=None, *, out=None, stream=None):
 def get_device_error() -> int:
     """Read and clear the device error word (synchronises the device).  0 = none."""
     return load().gla_get_device_error()
+
+
+def wait_probe(stream=None) -> None:
+    """Launch the failure-path diagnostic (gla_wait_probe): a wait that nothing completes,
+    given up after the configured limit; get_device_error() then reads GLA_ERR_TIMEOUT."""
+    _check("gla_wait_probe", load().gla_wait_probe(_stream(stream)))
 
 
 def set_wait_timeout_ns(ns: int) -> None:

@@ -106,6 +106,18 @@ gla_status chunk_fwd_impl(const void* q, const void* k, const void* v, gla_dtype
   return e == cudaSuccess ? GLA_OK : GLA_ERR_CUDA;
 }
 
+
+// One thread waits on an mbarrier that nothing ever arrives on: the bounded wait gives up after
+// the configured limit and records DEV_TIMEOUT -- the failure path of every kernel's waits,
+// exercised without a fault.
+__global__ void wait_probe_kernel(gla::DevCtl ctl) {
+  __shared__ alignas(8) unsigned long long bar;
+  if (threadIdx.x == 0) {
+    gla::mbar_init(gla::smem_u32(&bar), 1);
+    gla::fence_barrier_init();
+    gla::mbar_wait(gla::smem_u32(&bar), 0, ctl);
+  }
+}
 }  // namespace
 
 namespace gla {
@@ -150,6 +162,14 @@ gla_status gla_get_device_error(void) {
 gla_status gla_set_wait_timeout_ns(unsigned long long ns) {
   g_wait_ns.store(ns ? ns : 2000000000ull);
   return GLA_OK;
+}
+
+gla_status gla_wait_probe(cudaStream_t stream) {
+  gla::DevCtl ctl;
+  gla_status st = ctl_for_current_device(&ctl);
+  if (st != GLA_OK) return st;
+  wait_probe_kernel<<<1, 32, 0, stream>>>(ctl);
+  return cudaGetLastError() == cudaSuccess ? GLA_OK : GLA_ERR_CUDA;
 }
 
 gla_status gla_decay_schedule(int H, double t_min, double t_max, float* log_decay) {

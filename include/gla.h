@@ -89,6 +89,14 @@ GLA_API gla_status gla_get_device_error(void);
  * Applies to calls made after it returns.  ns == 0 restores the default. */
 GLA_API gla_status gla_set_wait_timeout_ns(unsigned long long ns);
 
+/* Diagnostic of the failure path (no counterpart in the article): launches one
+ * thread that waits on a barrier nothing ever completes.  Its bounded wait gives
+ * up after the limit set by gla_set_wait_timeout_ns and sets the device error
+ * word, so that gla_get_device_error() then returns GLA_ERR_TIMEOUT and the
+ * context stays usable.  Takes about that limit to finish.  Asynchronous on
+ * `stream`. */
+GLA_API gla_status gla_wait_probe(cudaStream_t stream);
+
 /* Decay schedule ("Decay schedule" paragraph): half-lives
  *   T_h = t_min * (t_max / t_min)^(h / (H - 1))   (T_0 = t_min if H == 1)
  * and log_decay[h] = ln(2^(-1/T_h)) = -ln(2) / T_h, computed in double and
