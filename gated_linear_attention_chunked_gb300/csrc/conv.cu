@@ -13,10 +13,12 @@
 // Memory-bound streaming: one thread owns 4 consecutive channels of a 64-token tile and walks
 // its tokens with the 4-token window in registers (3-token halo, ~5 % re-read).  dw, db: per
 // tile partial sums, summed over tiles in a fixed order by a second kernel (deterministic).
-// (At ~100 registers two CTAs of 256 threads fit an SM and each thread has one 8-byte load in
-// flight per token: the prefill kernels reach about half of HBM bandwidth.)
+// Each thread issues the loads of 8 tokens before using the first, so that several DRAM
+// round trips overlap.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+
+#include <type_traits>
 
 #include "kernels.h"
 
@@ -37,6 +39,26 @@ __device__ __forceinline__ float4 load_x(const void* x, long long idx4) {  // 4 
     return __ldg(reinterpret_cast<const float4*>(x) + idx4);
   }
 }
+
+// raw 4-channel load (bf16: 8 bytes, fp32: 16 bytes) and its conversion, so that a group of
+// tokens' loads can all be issued before the first is used
+template <bool BF16>
+struct Raw {
+  using T = typename std::conditional<BF16, uint2, float4>::type;
+};
+template <bool BF16>
+__device__ __forceinline__ typename Raw<BF16>::T load_raw(const void* x, long long idx4) {
+  if constexpr (BF16) return __ldg(reinterpret_cast<const uint2*>(x) + idx4);
+  else return __ldg(reinterpret_cast<const float4*>(x) + idx4);
+}
+__device__ __forceinline__ float4 to_f4(uint2 u) {
+  return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
+                     __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u));
+}
+__device__ __forceinline__ float4 to_f4(float4 v) { return v; }
+
+constexpr int GRP = 8;      // tokens whose loads are issued together (forward)
+constexpr int GRP_BWD = 4;  // (backward: two loads per token, and two CTAs per SM)
 
 __device__ __forceinline__ float& at(float4& v, int j) {
   return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w;
@@ -97,16 +119,24 @@ conv_fwd_kernel(const void* __restrict__ x, const float* __restrict__ w,
   float4 win[K];
 #pragma unroll
   for (int j = 0; j < K - 1; ++j) win[j + 1] = x_at<BF16>(x, init, b, t0 - 3 + j, T, D4, d4);
-  for (int t = t0; t < t1; ++t) {
-    win[0] = win[1];
-    win[1] = win[2];
-    win[2] = win[3];
-    win[3] = load_x<BF16>(x, ((long long)b * T + t) * D4 + d4);
-    float4 z = conv4(f, win);
-    float4 o;
+  for (int tg = t0; tg < t1; tg += GRP) {
+    typename Raw<BF16>::T raw[GRP];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) at(o, c) = at(z, c) * sigm(at(z, c));
-    reinterpret_cast<float4*>(y)[((long long)b * T + t) * D4 + d4] = o;
+    for (int u = 0; u < GRP; ++u)
+      if (tg + u < t1) raw[u] = load_raw<BF16>(x, ((long long)b * T + tg + u) * D4 + d4);
+#pragma unroll
+    for (int u = 0; u < GRP; ++u) {
+      if (tg + u >= t1) break;
+      win[0] = win[1];
+      win[1] = win[2];
+      win[2] = win[3];
+      win[3] = to_f4(raw[u]);
+      float4 z = conv4(f, win);
+      float4 o;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) at(o, c) = at(z, c) * sigm(at(z, c));
+      reinterpret_cast<float4*>(y)[((long long)b * T + tg + u) * D4 + d4] = o;
+    }
   }
   if (fin && t1 == T) {  // the state after the call: x_{T-3..T-1}
 #pragma unroll
@@ -117,7 +147,7 @@ conv_fwd_kernel(const void* __restrict__ x, const float* __restrict__ w,
 
 // part[(b * n_tiles + tile)][d][5] = (dw[d][0..3], db[d]) over the tile's tokens
 template <bool BF16>
-__global__ void __launch_bounds__(THREADS)
+__global__ void __launch_bounds__(THREADS, 2)
 conv_bwd_kernel(const void* __restrict__ x, const float* __restrict__ w,
                 const float* __restrict__ bias, const float* __restrict__ init,
                 const float* __restrict__ dy, float* __restrict__ dx, float* __restrict__ dinit,
@@ -138,16 +168,29 @@ conv_bwd_kernel(const void* __restrict__ x, const float* __restrict__ w,
 #pragma unroll
   for (int j = 0; j < K; ++j) gw[j] = zero;
   // t runs to t1 + 2 so that dx_s for every s < t1 is complete (dz beyond T is 0)
-  for (int t = t0; t < t1 + 3; ++t) {
+  const int tend = t1 + 3;
+  for (int tg = t0; tg < tend; tg += GRP_BWD) {
+  typename Raw<BF16>::T rx[GRP_BWD];
+  float4 rg[GRP_BWD];
+#pragma unroll
+  for (int u = 0; u < GRP_BWD; ++u)
+    if (tg + u < tend && tg + u < T) {
+      rx[u] = load_raw<BF16>(x, ((long long)b * T + tg + u) * D4 + d4);
+      rg[u] = __ldg(reinterpret_cast<const float4*>(dy) + ((long long)b * T + tg + u) * D4 + d4);
+    }
+#pragma unroll
+  for (int u = 0; u < GRP_BWD; ++u) {
+    const int t = tg + u;
+    if (t >= tend) break;
 #pragma unroll
     for (int j = 0; j < K - 1; ++j) {
       win[j] = win[j + 1];
       dz[j] = dz[j + 1];
     }
     if (t < T) {
-      win[3] = load_x<BF16>(x, ((long long)b * T + t) * D4 + d4);
+      win[3] = to_f4(rx[u]);
       float4 z = conv4(f, win);
-      float4 g = __ldg(reinterpret_cast<const float4*>(dy) + ((long long)b * T + t) * D4 + d4);
+      float4 g = rg[u];
       float4 d;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
@@ -181,6 +224,7 @@ conv_bwd_kernel(const void* __restrict__ x, const float* __restrict__ w,
       else if (dinit)
         reinterpret_cast<float4*>(dinit)[((long long)b * 3 + (s + 3)) * D4 + d4] = g;
     }
+  }
   }
   float* p = part + ((long long)blockIdx.x * D + 4 * d4) * 5;
 #pragma unroll
