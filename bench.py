@@ -151,6 +151,21 @@ def oracle_sample(n_seq: int, seed: int = 2):
     return n_seq * T / dt, dt
 
 
+def reduce_max(values, dist, device):
+    """Element-wise max over ranks of this rank's values (timings): the slowest rank sets the
+    job's time.  dist None = one process."""
+    import torch
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
+def job_rate(world, units_per_rank, seconds):
+    """Whole-job throughput: the units every rank processed over the (max-over-ranks) time."""
+    return world * units_per_rank / seconds
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return 0
@@ -282,11 +297,8 @@ def run_gpu(args, rank, world, local_rank):
     tot_ms = [e[0].elapsed_time(e[3]) for e in evs]
     if gla.get_device_error() != 0:
         raise RuntimeError("device error in the timed region")
-    sums = torch.tensor([sum(fwd_ms), sum(bwd_ms), sum(dec_ms), sum(tot_ms)], device=dev,
-                        dtype=torch.float64)
-    if dist:
-        dist.all_reduce(sums, op=dist.ReduceOp.MAX)
-    fwd_t, bwd_t, dec_t, tot_t = (float(x) / args.steps for x in sums.cpu())  # ms per step
+    sums = reduce_max([sum(fwd_ms), sum(bwd_ms), sum(dec_ms), sum(tot_ms)], dist, dev)
+    fwd_t, bwd_t, dec_t, tot_t = (x / args.steps for x in sums)  # ms per step
     if args.part != "all":
         part_ms = dict(fwd=fwd_t, bwd=bwd_t, decode=dec_t)[args.part]
         if rank == 0:
@@ -296,7 +308,7 @@ def run_gpu(args, rank, world, local_rank):
             dist.destroy_process_group()
         return 0
     tokens = B * T
-    value = world * tokens / ((fwd_t + bwd_t) * 1e-3)
+    value = job_rate(world, tokens, (fwd_t + bwd_t) * 1e-3)
     dec_bytes = n_states * DEC_BYTES_STATE
     dec_gbs = dec_bytes / (dec_t * 1e-3) / 1e9
     th = B * T * H
@@ -365,10 +377,8 @@ def run_gpu(args, rank, world, local_rank):
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         e2e_run(e2e_steps)
-        tt = torch.tensor([time.perf_counter() - t0], device=dev, dtype=torch.float64)
-        if dist:
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e = dict(value=world * tokens * e2e_steps / float(tt.item()), unit="tokens/s",
+        tt = reduce_max([time.perf_counter() - t0], dist, dev)[0]
+        e2e = dict(value=job_rate(world, tokens * e2e_steps, tt), unit="tokens/s",
                    h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h,
                    path="pinned host q,k,v,dO -> gla chunk_fwd + chunk_bwd -> host d_aug; "
                         "next step's inputs copied on a second stream during this step's "

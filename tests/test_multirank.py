@@ -1,0 +1,66 @@
+"""The N > 1 path on the CPU (gloo, world size 2): every rank runs the same per-GPU workload
+(replicas: no collective on the data path); the only cross-rank steps are a barrier and the
+max over ranks of the timed region, and rank 0 alone prints the result line."""
+import json
+import multiprocessing as mp
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    sys.path.insert(0, ROOT)
+    import torch.distributed as dist
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import bench
+    # this rank's timings (ms): rank 1 is slower in the first entry, rank 0 in the second
+    vals = bench.reduce_max([10.0 + rank, 7.0 - 2 * rank], dist, "cpu")
+    rate = bench.job_rate(world, 65536, vals[0] * 1e-3)
+    dist.barrier()
+    q.put((rank, vals, rate))
+    dist.destroy_process_group()
+
+
+def test_max_over_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    out = dict()
+    for _ in procs:
+        r, vals, rate = q.get(timeout=120)
+        out[r] = (vals, rate)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert out[0] == out[1]  # every rank agrees
+    vals, rate = out[0]
+    assert vals == [11.0, 7.0]  # the slowest rank per entry
+    assert rate == pytest.approx(2 * 65536 / 0.011)  # both ranks' units over the max time
+
+
+def test_reference_arm_under_torchrun_prints_once():
+    port = _free_port()
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), "bench.py", "--impl",
+           "reference", "--gpus", "2", "--steps", "1", "--warmup", "3"]
+    r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
