@@ -66,21 +66,25 @@ head_norm_fwd_kernel(const float* __restrict__ o, const void* __restrict__ g,
     const long long row = row0 + (hw & 1);
     const bool live = row < rows;
     const int tier = (int)(row % H) / heads_per_tier;
-    float4 x[PER];
-    float ss = 0.f;
+    // every load of the row first, so that they overlap
+    float4 x[PER], gv[PER];
 #pragma unroll
     for (int p = 0; p < PER; ++p) {
       x[p] = live ? __ldg(reinterpret_cast<const float4*>(o + row * C) + lane + LANES * p)
                   : make_float4(0.f, 0.f, 0.f, 0.f);
+      gv[p] = live ? load_g<GBF16>(g, row, lane + LANES * p) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float ss = 0.f;
+#pragma unroll
+    for (int p = 0; p < PER; ++p)
 #pragma unroll
       for (int j = 0; j < 4; ++j) ss = fmaf(F4(x[p], j), F4(x[p], j), ss);
-    }
     const float r = 1.f / sqrtf(sum16(ss) / C + eps);
     if (!live) continue;
 #pragma unroll
     for (int p = 0; p < PER; ++p) {
       const int c4 = lane + LANES * p;
-      float4 gg = load_g<GBF16>(g, row, c4);
+      float4 gg = gv[p];
       float4 ww = __ldg(reinterpret_cast<const float4*>(w + tier * C) + c4);
       float4 out;
 #pragma unroll
@@ -119,23 +123,29 @@ head_norm_bwd_kernel(const float* __restrict__ dy, const float* __restrict__ o,
     const long long row = row0 + (hw & 1);
     const bool live = row < rows;
     const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
-    float4 x[PER];
-    float ss = 0.f;
+    // every load of the row first, so that they overlap
+    float4 x[PER], gv[PER], dv[PER];
 #pragma unroll
     for (int p = 0; p < PER; ++p) {
-      x[p] = live ? __ldg(reinterpret_cast<const float4*>(o + row * C) + lane + LANES * p) : zero;
+      const int c4 = lane + LANES * p;
+      x[p] = live ? __ldg(reinterpret_cast<const float4*>(o + row * C) + c4) : zero;
+      gv[p] = live ? load_g<GBF16>(g, row, c4) : zero;
+      dv[p] = live ? __ldg(reinterpret_cast<const float4*>(dy + row * C) + c4) : zero;
+    }
+    float ss = 0.f;
+#pragma unroll
+    for (int p = 0; p < PER; ++p)
 #pragma unroll
       for (int j = 0; j < 4; ++j) ss = fmaf(F4(x[p], j), F4(x[p], j), ss);
-    }
     const float r = 1.f / sqrtf(sum16(ss) / C + eps);
     float4 dn[PER];
     float dot = 0.f;  // sum_c dn_c n_c
 #pragma unroll
     for (int p = 0; p < PER; ++p) {
       const int c4 = lane + LANES * p;
-      float4 gg = live ? load_g<GBF16>(g, row, c4) : zero;
+      float4 gg = gv[p];
       float4 ww = wt[p];
-      float4 dd = live ? __ldg(reinterpret_cast<const float4*>(dy + row * C) + c4) : zero;
+      float4 dd = dv[p];
       float4 dgo;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
