@@ -417,6 +417,58 @@ def run_gpu(args, rank, world, local_rank):
     return 0
 
 
+def run_fused(args):
+    """--part fused: the forward followed by the standalone output epilogue, against the
+    forward with the epilogue fused in (y only, and y + o), at the training shape."""
+    import torch
+    import gated_linear_attention_chunked_gb300 as gla
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    gla.load()
+    Bf, tiers = args.batch, 4
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(31)
+    q = (torch.randn(Bf, T, H, DK, generator=gen, device=dev) * DK ** -0.5).bfloat16()
+    k = torch.randn(Bf, T, H, DK, generator=gen, device=dev).bfloat16()
+    v = torch.randn(Bf, T, H, DV, generator=gen, device=dev).bfloat16()
+    g = torch.randn(Bf, T, H, DV, generator=gen, device=dev).bfloat16()
+    a = 0.02 * torch.randn(H, DK, generator=gen, device=dev)
+    w = 1.0 + 0.2 * torch.randn(tiers, DV, generator=gen, device=dev)
+    gam = gla.decay_schedule(H).to(dev)
+    o = torch.empty(Bf, T, H, DV, device=dev)
+    y = torch.empty_like(o)
+    stream = torch.cuda.current_stream()
+
+    def timed(fn, n):
+        for _ in range(args.warmup):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n
+
+    def separate():
+        gla.chunk_fwd(q, k, v, gam, a, out=o, want_final_state=False)
+        gla.head_norm_gate(o, g, w, tiers, out=y)
+
+    n = max(args.steps, 5)
+    sep = timed(separate, n)
+    fy = timed(lambda: gla.chunk_fwd_gated(q, k, v, gam, a, g, w, tiers, want_final_state=False), n)
+    fyo = timed(lambda: gla.chunk_fwd_gated(q, k, v, gam, a, g, w, tiers, want_o=True,
+                                            want_final_state=False), n)
+    if gla.get_device_error() != 0:
+        raise RuntimeError("device error")
+    print(json.dumps(dict(part="fused", workload=f"GLA forward + output epilogue (4 tiers), B={Bf} "
+                          "T=2048 H=16, bf16 q,k,v,g", separate_ms=sep, fused_y_ms=fy,
+                          fused_y_and_o_ms=fyo, tokens_per_s_fused_y=Bf * T / (fy * 1e-3))),
+          flush=True)
+    return 0
+
+
 def run_conv(args):
     """--part conv: the causal depth-wise conv + SiLU at the training shape (B=32, T=2048,
     D=3072, x bf16), forward and gradient, and one decode step over 1280 sequences x 24 layers
@@ -635,7 +687,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seqs", type=int, default=8)
-    ap.add_argument("--part", choices=["all", "fwd", "bwd", "decode", "long", "paged", "norm", "conv"], default="all",
+    ap.add_argument("--part", choices=["all", "fwd", "bwd", "decode", "long", "paged", "norm", "conv", "fused"], default="all",
                     help="time one call alone (smaller profiling cases); the default is the "
                          "whole hot path")
     ap.add_argument("--batch", type=int, default=B, help="sequences of the training shape")
@@ -664,6 +716,8 @@ def main():
         return run_head_norm(args) if rank == 0 else 0
     if args.part == "conv":
         return run_conv(args) if rank == 0 else 0
+    if args.part == "fused":
+        return run_fused(args) if rank == 0 else 0
     return run_gpu(args, rank, world, local_rank)
 
 

@@ -85,6 +85,9 @@ def load(path: str | None = None):
             lib.gla_head_norm_gate_bwd.argtypes = ([_P] * 3 + [_I, _P, _I, _F] + [_P] * 4 + [_S] +
                                                    [_L, _I, _I, _P])
             lib.gla_head_norm_gate_bwd.restype = _I
+            lib.gla_chunk_fwd_gated.argtypes = ([_P] * 3 + [_I] + [_P] * 5 + [_I, _F] + [_P] * 5 +
+                                                [_S] + [_I] * 5 + [_P])
+            lib.gla_chunk_fwd_gated.restype = _I
             lib.gla_conv_fwd.argtypes = [_P, _I] + [_P] * 5 + [_I] * 3 + [_P]
             lib.gla_conv_fwd.restype = _I
             lib.gla_conv_bwd_workspace_size.argtypes = [_I] * 3
@@ -191,6 +194,32 @@ def chunk_fwd(q, k, v, log_decay, aug_balance, init_state=None, *, want_final_st
         0 if ws is None else ws.numel() * ws.element_size(), B, T, H, dk, dv, _stream(stream))
     _check("gla_chunk_fwd", rc)
     return out, final_state
+
+
+def chunk_fwd_gated(q, k, v, log_decay, aug_balance, g, norm_weight, n_tiers, eps=1e-6,
+                    init_state=None, *, want_o=False, want_rstd=True, want_final_state=True,
+                    workspace=None, stream=None):
+    """Chunked forward with the output epilogue fused in (gla_chunk_fwd_gated): g [B,T,H,192]
+    bf16, norm_weight [n_tiers,192].  Returns (y, rstd or None, o or None, final or None)."""
+    torch = _torch()
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    code = _dtype_code(q)
+    f = torch.float32
+    y = torch.empty((B, T, H, dv), dtype=f, device=q.device)
+    rstd = torch.empty((B, T, H), dtype=f, device=q.device) if want_rstd else None
+    o = torch.empty((B, T, H, dv), dtype=f, device=q.device) if want_o else None
+    fin = torch.empty((B, H, dk, dv), dtype=f, device=q.device) if want_final_state else None
+    ws = _workspace(load().gla_chunk_fwd_workspace_size(B, T, H, dk, dv, code), q.device, workspace)
+    rc = load().gla_chunk_fwd_gated(
+        _dev(q, "q"), _dev(k, "k", q.dtype), _dev(v, "v", q.dtype), code,
+        _dev(log_decay, "log_decay", f), _dev(aug_balance, "aug_balance", f),
+        _dev(init_state, "init_state", f), _dev(g, "g", torch.bfloat16),
+        _dev(norm_weight, "norm_weight", f), n_tiers, eps, _dev(y, "y", f), _dev(rstd, "rstd", f),
+        _dev(o, "o", f), _dev(fin, "final_state", f), _dev(ws, "workspace"),
+        0 if ws is None else ws.numel() * ws.element_size(), B, T, H, dk, dv, _stream(stream))
+    _check("gla_chunk_fwd_gated", rc)
+    return y, rstd, o, fin
 
 
 def chunk_bwd(q, k, v, log_decay, aug_balance, dO, init_state=None, d_final_state=None, *,

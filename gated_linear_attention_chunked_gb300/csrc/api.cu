@@ -64,10 +64,11 @@ gla_status chunk_fwd_impl(const void* q, const void* k, const void* v, gla_dtype
                           const float* log_decay, const float* aug_balance,
                           const float* init_state, float* o, float* final_state, void* workspace,
                           size_t workspace_bytes, int B, int T, int H, int dk, int dv,
-                          const gla::StatePages& sp, cudaStream_t stream) {
+                          const gla::StatePages& sp, cudaStream_t stream,
+                          const gla::OutGate& og = gla::OutGate{}) {
   gla_status st = check_chunk_sizes(B, T, H, dk, dv, in_dtype);
   if (st != GLA_OK) return st;
-  if (!q || !k || !v || !log_decay || !aug_balance || !o) return GLA_ERR_INVALID_ARG;
+  if (!q || !k || !v || !log_decay || !aug_balance || (!o && !og.g)) return GLA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(log_decay) ||
       !aligned16(aug_balance) || !aligned16(init_state) || !aligned16(o) ||
       !aligned16(final_state))
@@ -86,7 +87,7 @@ gla_status chunk_fwd_impl(const void* q, const void* k, const void* v, gla_dtype
   gla::FwdArgs a;
   a.q = q; a.k = k; a.v = v; a.bf16 = in_dtype == GLA_BF16;
   a.log_decay = log_decay; a.aug = aug_balance; a.init = init_state;
-  a.o = o; a.fin = final_state; a.B = B; a.T = T; a.H = H; a.sp = sp;
+  a.o = o; a.fin = final_state; a.B = B; a.T = T; a.H = H; a.sp = sp; a.og = og;
   if (in_dtype == GLA_FP32) {
     const size_t tok = (size_t)B * T * H;
     uint8_t* w = static_cast<uint8_t*>(workspace);
@@ -196,6 +197,29 @@ gla_status gla_chunk_fwd(const void* q, const void* k, const void* v, gla_dtype 
                          cudaStream_t stream) {
   return chunk_fwd_impl(q, k, v, in_dtype, log_decay, aug_balance, init_state, o, final_state,
                         workspace, workspace_bytes, B, T, H, dk, dv, gla::StatePages{}, stream);
+}
+
+gla_status gla_chunk_fwd_gated(const void* q, const void* k, const void* v, gla_dtype in_dtype,
+                               const float* log_decay, const float* aug_balance,
+                               const float* init_state, const void* g, const float* norm_weight,
+                               int n_tiers, float eps, float* y, float* rstd, float* o,
+                               float* final_state, void* workspace, size_t workspace_bytes, int B,
+                               int T, int H, int dk, int dv, cudaStream_t stream) {
+  if (!g || !norm_weight || !y) return GLA_ERR_INVALID_ARG;
+  if (H <= 0 || n_tiers <= 0 || H % n_tiers != 0 || !(eps >= 0.f) || !(eps < 1e30f))
+    return GLA_ERR_INVALID_ARG;
+  if (!aligned16(g) || !aligned16(norm_weight) || !aligned16(y) || !aligned16(rstd))
+    return GLA_ERR_ALIGNMENT;
+  gla::OutGate og;
+  og.g = static_cast<const uint16_t*>(g);
+  og.w = norm_weight;
+  og.y = y;
+  og.rstd = rstd;
+  og.eps = eps;
+  og.heads_per_tier = H / n_tiers;
+  og.want_o = o != nullptr;
+  return chunk_fwd_impl(q, k, v, in_dtype, log_decay, aug_balance, init_state, o, final_state,
+                        workspace, workspace_bytes, B, T, H, dk, dv, gla::StatePages{}, stream, og);
 }
 
 gla_status gla_chunk_fwd_paged(const void* q, const void* k, const void* v, gla_dtype in_dtype,

@@ -55,7 +55,8 @@ constexpr uint32_t OFF_ES = OFF_RED + 96;       // int es[2]: state-copy exponen
 constexpr uint32_t OFF_KV = OFF_ES + 16;        // float kvmax[2][8]: per-warp max|K'|, max|V|
 constexpr uint32_t OFF_A = OFF_KV + 64;         // float a[96]: aug_balance of the head
 constexpr uint32_t OFF_PW = OFF_A + 384;        // float pw[128] = lambda^d
-constexpr uint32_t SMEM_USED = OFF_PW + 512;
+constexpr uint32_t OFF_XCH = OFF_PW + 512;      // float xch[2][128]: row sums of o^2 (gated)
+constexpr uint32_t SMEM_USED = OFF_XCH + 1024;
 // The whole opt-in maximum is requested; the kernel aligns its base to 1024 bytes and
 // refuses to run (GLA_ERR_LAYOUT, before touching shared memory) if the padding that
 // takes would not fit.  The dynamic shared window normally starts 1024-aligned.
@@ -79,19 +80,21 @@ enum Bar : uint32_t {
   EP_S = 13,
   DRAIN = 14,
   RED = 15,  // exchange of the per-warp max|S| inside the emit group
+  QX = 16,   // 16..19 (gated output): the two warps of row quadrant q have their row sums
 };
 
 constexpr int THREADS = 448;
 constexpr int PRODUCER_WARP = 12, MMA_WARP = 13;
 constexpr int EMIT_THREADS = 256;  // warps 4..11
 
-template <bool BF16>
+template <bool BF16, bool GATED>
 __global__ void __launch_bounds__(THREADS, 1)
 fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
            const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o,
            const __grid_constant__ CUtensorMap map_fin, const float* __restrict__ log_decay,
            const float* __restrict__ aug, const float* __restrict__ init, float* __restrict__ out,
-           float* __restrict__ fin, int T, int H, int seg, StatePages sp, DevCtl ctl) {
+           float* __restrict__ fin, int T, int H, int seg, StatePages sp,
+           const __grid_constant__ CUtensorMap map_y, OutGate og, DevCtl ctl) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   Cta cta;
   cta.base = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -133,6 +136,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
     mbar_init(cta.bar(EP_O), EMIT_THREADS);     // emit group
     mbar_init(cta.bar(EP_S), EMIT_THREADS);     // emit group
     mbar_init(cta.bar(RED), EMIT_THREADS);      // emit group
+    for (int q = 0; q < 4; ++q) mbar_init(cta.bar(QX + q), 64);
     *cta.abort_flag() = 0;
     fence_barrier_init();
   }
@@ -477,7 +481,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
       // ---- output rows: o = 2^e D_O for columns [96hf, 96hf+96) (the self-augmentation
       // sigmoid(z) v is already in D_O through the diagonal of P''), TMA-stored
       uint8_t* const stage_o = base + OFF_STG + ew * 4096;
-      {
+      if constexpr (!GATED) {
         const float osc = pow2i(e_cur);
         const int row = b * T + c * C + 32 * q4;
         emit_rows_tma<6>(
@@ -490,6 +494,72 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
               for (int j = 0; j < 16; ++j) o[j] = __uint_as_float(r[j]) * osc;
             },
             [&](int k, uint32_t src) { tma_store_3d(&map_o, src, 96 * hf + 16 * k, h, row); });
+      } else {
+        // y = o r w[tier] SiLU(g), r = (mean over the row's 192 channels of o^2 + eps)^-1/2:
+        // pass 1 sums o^2 over this warp's 96 columns (writing o too if asked), the two warps
+        // of the row quadrant exchange their sums, pass 2 writes y
+        const float osc = pow2i(e_cur);
+        const int row = b * T + c * C + 32 * q4;
+        const long long tok = (long long)b * T + c * C + i;  // token row of this thread
+        float* xch = (float*)(base + OFF_XCH);
+        float ss = 0.f;
+        if (og.want_o) {
+          emit_rows_tma<6>(
+              stage_o, lane,
+              [&](int k, float (&o)[16]) {
+                uint32_t r[16];
+                tmem_ld16(trow + TM_O + 96 * hf + 16 * k, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                  o[j] = __uint_as_float(r[j]) * osc;
+                  ss = fmaf(o[j], o[j], ss);
+                }
+              },
+              [&](int k, uint32_t src) { tma_store_3d(&map_o, src, 96 * hf + 16 * k, h, row); });
+        } else {
+#pragma unroll 1
+          for (int k = 0; k < 6; ++k) {
+            uint32_t r[16];
+            tmem_ld16(trow + TM_O + 96 * hf + 16 * k, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float o = __uint_as_float(r[j]) * osc;
+              ss = fmaf(o, o, ss);
+            }
+          }
+        }
+        // the row's gate values, all 12 loads in flight together
+        const uint4* gp = reinterpret_cast<const uint4*>(og.g + (tok * H + h) * DV + 96 * hf);
+        uint4 gq[12];
+#pragma unroll
+        for (int u = 0; u < 12; ++u) gq[u] = __ldg(gp + u);
+        xch[hf * 128 + i] = ss;
+        mbar_arrive(cta.bar(QX + q4));
+        if (!(ok = wait(cta, cta.bar(QX + q4), par, ctl))) break;
+        const float rr = 1.f / sqrtf((xch[i] + xch[128 + i]) * (1.f / DV) + og.eps);
+        if (og.rstd && hf == 0) og.rstd[tok * H + h] = rr;
+        const float* wrow = og.w + (h / og.heads_per_tier) * DV + 96 * hf;
+        if (lane == 0) bulk_wait_read<0>();  // pass 1's stores have read the staging
+        __syncwarp();
+        emit_rows_tma<6>(
+            stage_o, lane,
+            [&](int k, float (&y)[16]) {
+              uint32_t r[16];
+              tmem_ld16(trow + TM_O + 96 * hf + 16 * k, r);
+              tmem_wait_ld();
+              const float f = osc * rr;
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const uint4 gv = j < 8 ? gq[2 * k] : gq[2 * k + 1];
+                const uint32_t w2 = (j & 7) < 2 ? gv.x : (j & 7) < 4 ? gv.y : (j & 7) < 6 ? gv.z : gv.w;
+                const float gj = ld16<true>((j & 1) ? (w2 >> 16) : (w2 & 0xFFFFu));
+                const float sl = gj / (1.f + expf(-gj));
+                y[j] = __uint_as_float(r[j]) * f * __ldg(wrow + 16 * k + j) * sl;
+              }
+            },
+            [&](int k, uint32_t src) { tma_store_3d(&map_y, src, 96 * hf + 16 * k, h, row); });
       }
       tc_fence_before();
       mbar_arrive(cta.bar(EP_O));
@@ -531,21 +601,25 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
 }  // namespace
 
 cudaError_t launch_chunk_fwd(const FwdArgs& a, DevCtl ctl, cudaStream_t stream) {
-  CUtensorMap mq, mk, mv, mo, mfin;
+  CUtensorMap mq, mk, mv, mo, mfin, my;
   const long long rows = (long long)a.B * a.T;
+  float* const o_any = a.o ? a.o : a.og.y;  // stand-in for a map that is never used
   if (!make_tmap_3d_16bit(&mq, a.q, DK, a.H, rows, 32, C, CU_TENSOR_MAP_SWIZZLE_64B, a.bf16) ||
       !make_tmap_3d_16bit(&mk, a.k, DK, a.H, rows, 32, C, CU_TENSOR_MAP_SWIZZLE_64B, a.bf16) ||
       !make_tmap_3d_16bit(&mv, a.v, DV, a.H, rows, 64, C, CU_TENSOR_MAP_SWIZZLE_128B, a.bf16) ||
-      !make_tmap_out_f32(&mo, a.o, DV, a.H, rows) ||
-      !make_tmap_state_f32(&mfin, a.fin ? (const void*)a.fin : (const void*)a.o,
+      !make_tmap_out_f32(&mo, o_any, DV, a.H, rows) ||
+      !make_tmap_out_f32(&my, a.og.y ? a.og.y : o_any, DV, a.H, rows) ||
+      !make_tmap_state_f32(&mfin, a.fin ? (const void*)a.fin : (const void*)o_any,
                            a.sp.page ? (long long)a.sp.n_pages * a.sp.pool_layers * a.H
                                      : (long long)(a.B / a.seg) * a.H))
     return cudaErrorInvalidValue;
-  auto kern = a.bf16 ? fwd_kernel<true> : fwd_kernel<false>;
+  const bool gated = a.og.g != nullptr;
+  auto kern = gated ? (a.bf16 ? fwd_kernel<true, true> : fwd_kernel<false, true>)
+                    : (a.bf16 ? fwd_kernel<true, false> : fwd_kernel<false, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
   kern<<<a.B * a.H, THREADS, SMEM_BYTES, stream>>>(mq, mk, mv, mo, mfin, a.log_decay, a.aug, a.init, a.o,
-                                                   a.fin, a.T, a.H, a.seg, a.sp, ctl);
+                                                   a.fin, a.T, a.H, a.seg, a.sp, my, a.og, ctl);
   return cudaGetLastError();
 }
 

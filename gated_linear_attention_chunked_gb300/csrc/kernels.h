@@ -3,6 +3,7 @@
 #include <cuda_runtime_api.h>
 
 #include <cstddef>
+#include <cstdint>
 
 #include "ptx.cuh"
 
@@ -34,6 +35,18 @@ struct StatePages {
   bool init_paged = false;
 };
 
+// Output epilogue fused into the chunked forward: y = o r w[h / heads_per_tier] SiLU(g) with
+// r = (mean_c o_c^2 + eps)^-1/2 per (token, head).  g == null: plain output o.
+struct OutGate {
+  const uint16_t* g = nullptr;  // [B*T, H, 192] bf16 gate stream (raw bits)
+  const float* w = nullptr;     // [n_tiers, 192]
+  float* y = nullptr;           // [B*T, H, 192] fp32
+  float* rstd = nullptr;        // [B*T, H] fp32 or null
+  float eps = 0.f;
+  int heads_per_tier = 1;
+  bool want_o = false;          // also write o
+};
+
 struct FwdArgs {
   const void* q;  // [B,T,H,96] 16-bit
   const void* k;
@@ -49,6 +62,7 @@ struct FwdArgs {
   // only the last segment of each writes its final state, to fin[b / seg].
   int seg = 1;
   StatePages sp;  // with sp.page: init and fin are the pool (see StatePages)
+  OutGate og;     // with og.g: the fused output epilogue (o written only if og.want_o)
 };
 // Returns cudaErrorInvalidValue if a tensor map cannot be encoded.
 cudaError_t launch_chunk_fwd(const FwdArgs& a, DevCtl ctl, cudaStream_t stream);

@@ -136,6 +136,27 @@ GLA_API gla_status gla_chunk_fwd(const void* q, const void* k, const void* v, gl
                          size_t workspace_bytes, int B, int T, int H, int dk, int dv,
                          cudaStream_t stream);
 
+/* gla_chunk_fwd_gated: the same forward with the mixer's output epilogue fused
+ * into it ("GLA mixer": a Head RMSNorm shared within each decay tier, then the
+ * SiLU(g) gate; see gla_head_norm_gate_fwd for the formula):
+ *   y[b,t,h,:] = o r w[h / (H / n_tiers), :] SiLU(g[b,t,h,:]),
+ *   r = 1 / sqrt(mean_c o^2 + eps)
+ * without o leaving the chip (o is also written if `o` is not NULL, as the
+ * epilogue's backward, gla_head_norm_gate_bwd, needs it).
+ *   g            [B,T,H,192] bf16       norm_weight [n_tiers,192] fp32
+ *   y            [B,T,H,192] fp32 (written)
+ *   rstd         [B,T,H] fp32 or NULL (written: r)
+ *   o            [B,T,H,192] fp32 or NULL;  other arguments as gla_chunk_fwd.
+ */
+GLA_API gla_status gla_chunk_fwd_gated(const void* q, const void* k, const void* v,
+                                       gla_dtype in_dtype, const float* log_decay,
+                                       const float* aug_balance, const float* init_state,
+                                       const void* g, const float* norm_weight, int n_tiers,
+                                       float eps, float* y, float* rstd, float* o,
+                                       float* final_state, void* workspace,
+                                       size_t workspace_bytes, int B, int T, int H, int dk,
+                                       int dv, cudaStream_t stream);
+
 /* ---------------------------------------------------------------------------
  * Chunked backward ("Challenge 3": the gradient through every sequential
  * state update), for the scalar loss  L = sum o.dO + <d_final_state, S_T>:

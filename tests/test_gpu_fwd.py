@@ -159,3 +159,43 @@ def test_fwd_segmented_path(env, B, T, H, seed):
     assert eo <= TOL_CHUNK and ef <= TOL_CHUNK
     assert rel_err(o2.cpu().numpy(), o_ref) <= TOL_CHUNK
     assert rel_err(f2.cpu().numpy(), fin_ref) <= TOL_CHUNK
+
+
+@pytest.mark.parametrize("B,T,H,n_tiers,want_o,seed", [
+    (2, 384, 4, 2, True, 41),      # serial scan, o written too
+    (1, 4096, 2, 1, False, 42),    # segment-parallel path, y only
+    (8, 2048, 16, 4, True, 43),    # one training-shape layer
+])
+def test_fwd_gated(env, B, T, H, n_tiers, want_o, seed):
+    """The forward with the output epilogue fused in: y (Head RMSNorm per tier, SiLU(g) gate)
+    and rstd against the oracle's forward followed by its epilogue; o, when written, is the
+    plain forward's output bit for bit, and y equals the standalone epilogue applied to it."""
+    import oracle
+    gla, torch = env
+    q, k, v = synth.qkv(seed, B, T, H)
+    a = synth.aug_balance(seed, (H, 96), 0.1)
+    init = synth.init_state(seed, B, H, 0.05)
+    g = synth.round_bf16(synth.normal(seed, synth.DO, (B, T, H, 192), 1.5))
+    w = 1.0 + synth.normal(seed, synth.A, (n_tiers, 192), 0.2)
+    qd, kd, vd, gd = (to_dev(x, torch.bfloat16) for x in (q, k, v, g))
+    gam = gla.decay_schedule(H).cuda()
+    ad, idd, wd = (to_dev(x, torch.float32) for x in (a, init, w))
+    y, rstd, o, fin = gla.chunk_fwd_gated(qd, kd, vd, gam, ad, gd, wd, n_tiers, 1e-6, idd,
+                                          want_o=want_o)
+    torch.cuda.synchronize()
+    assert gla.get_device_error() == 0
+    gam64 = gla.decay_schedule(H).numpy().astype(np.float64)
+    o_ref, fin_ref = oracle.fwd(q, k, v, gam64, a, init)
+    y_ref, r_ref = oracle.head_norm_gate(o_ref.reshape(B * T, H, 192), g.reshape(B * T, H, 192),
+                                         w, n_tiers, 1e-6)
+    ey = rel_err(y.cpu().numpy().reshape(B * T, H, 192), y_ref)
+    er = rel_err(rstd.cpu().numpy().reshape(B * T, H), r_ref)
+    ef = rel_err(fin.cpu().numpy(), fin_ref)
+    print(f"fwd gated B={B} T={T} H={H} tiers={n_tiers}: y {ey:.2e} rstd {er:.2e} final {ef:.2e}")
+    assert ey <= TOL_CHUNK and er <= TOL_CHUNK and ef <= TOL_CHUNK
+    if want_o:
+        o_plain, _ = gla.chunk_fwd(qd, kd, vd, gam, ad, idd)
+        y2, _ = gla.head_norm_gate(o_plain, gd, wd, n_tiers, 1e-6)
+        torch.cuda.synchronize()
+        assert torch.equal(o, o_plain)
+        assert rel_err(y.cpu().numpy(), y2.cpu().numpy()) <= 1e-5
