@@ -25,6 +25,9 @@
 //               columns: (1) the serial step -- S -> fp16(S * 2^-e') into the drained q/k
 //               slot (B operand of the next Q'' S) and D_S <- lambda^C D_S; (2) the output rows
 //               o = 2^e D_O as fp32, TMA-stored from per-warp staging.
+// The output MMA is issued in two parts: Q''S as soon as Q'' is in place (it releases the
+// slot of the state copy, so the next chunk's q, k load starts early), P''V once the masked
+// scores are in TMEM.
 // fp16 operands (11-bit significand) keep the long-memory heads accurate; the state copy is
 // scaled by a power of two e' chosen from a bound on max|S| so it never overflows fp16.
 #include <cuda_bf16.h>
@@ -81,6 +84,7 @@ enum Bar : uint32_t {
   DRAIN = 14,
   RED = 15,  // exchange of the per-warp max|S| inside the emit group
   QX = 16,   // 16..19 (gated output): the two warps of row quadrant q have their row sums
+  EP_Q = 20,  // convert group: Q'' of the chunk is in place (the Q''S MMA may start)
 };
 
 constexpr int THREADS = 448;
@@ -133,6 +137,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
     mbar_init(cta.bar(S_DONE), 1);
     mbar_init(cta.bar(DRAIN), 1);
     mbar_init(cta.bar(EP_CONV), 128);           // convert group
+    mbar_init(cta.bar(EP_Q), 128);              // convert group
     mbar_init(cta.bar(EP_O), EMIT_THREADS);     // emit group
     mbar_init(cta.bar(EP_S), EMIT_THREADS);     // emit group
     mbar_init(cta.bar(RED), EMIT_THREADS);      // emit group
@@ -211,7 +216,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                      smem_desc(st + OFF_K + off, 16, 512, SW_64), ID_QK, ks > 0);
         }
         mma_commit(cta.bar(P_DONE));
-        if (!wait(cta, cta.bar(EP_CONV), c & 1, ctl)) break;
+        if (!wait(cta, cta.bar(EP_Q), c & 1, ctl)) break;
         if (!wait(cta, cta.bar(EP_S), c & 1, ctl)) break;
         if (c >= 1 && !wait(cta, cta.bar(EP_O), (c - 1) & 1, ctl)) break;
         tc_fence_after();
@@ -221,13 +226,16 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
           mma_f16_ss(tmem + TM_O, smem_desc(st + OFF_Q + off, 16, 512, SW_64),
                      smem_desc(slot + ks * 2048, S_ATOM, 1024, SW_128), ID_QS, ks > 0);
         }
+        // the state copy has been read: the next chunk's q, k may load into that slot
+        mma_commit(cta.bar(QK_EMPTY + (s ^ 1)));
+        if (!wait(cta, cta.bar(EP_CONV), c & 1, ctl)) break;
+        tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {  // O += P'' V  (P'' from TMEM)
           mma_f16_ts(tmem + TM_O, tmem + TM_P + 8 * ks,
                      smem_desc(st + OFF_V + ks * 2048, V_BOX, 1024, SW_128), ID_PV, 1);
         }
         mma_commit(cta.bar(O_DONE));
-        mma_commit(cta.bar(QK_EMPTY + (s ^ 1)));
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {  // S += K'^T V
           mma_f16_ss(tmem + TM_S, smem_desc(st + OFF_K + ks * 1024, Q_BOX, 512, SW_64),
@@ -296,6 +304,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
         *(uint4*)(stg + OFF_Q + off) = qv;
         *(uint4*)(stg + OFF_K + off) = kv;
       }
+      // Q'' is in place: the Q''S MMA can run (and release the state copy's slot) while the
+      // masked scores are still being made
+      fence_proxy_async();
+      mbar_arrive(cta.bar(EP_Q));
       const float sg = sigmoid(z);
       // chunk maxima of |K'| and |V| (for the emit group's bound on the next state)
       {
