@@ -47,7 +47,7 @@ constexpr uint32_t OFF_STG = OFF_G + 3 * V_BOX;  // output staging, 12 warps x 2
 constexpr uint32_t OFF_CP = OFF_STG + 12 * 2048;  // state copy, 3 atoms x 12 KB
 constexpr uint32_t S_ATOM = 12288;
 constexpr uint32_t OFF_BAR = OFF_CP + 3 * S_ATOM;
-constexpr uint32_t NBAR = 18;
+constexpr uint32_t NBAR = 20;
 constexpr uint32_t OFF_TMEM = OFF_BAR + NBAR * 8;
 constexpr uint32_t OFF_ABORT = OFF_TMEM + 4;
 constexpr uint32_t OFF_RED = OFF_TMEM + 16;  // float red[3][12]: per-warp max|S|
@@ -76,6 +76,7 @@ enum Bar : uint32_t {
   DRAIN = 9,
   QG0 = 10,  // 10..13: quadrant q's three gate partial sums are in shared memory
   QS0 = 14,  // 14..17: quadrant q's three parts have read their score blocks
+  EP_C1 = 18,  // the fp16 operands are in place (the MMAs that need no masked score may run)
 };
 
 constexpr int THREADS = 448;
@@ -153,6 +154,7 @@ __device__ __forceinline__ void run_role(
     mbar_init(cta.bar(S_DONE), 1);
     mbar_init(cta.bar(DRAIN), 1);
     mbar_init(cta.bar(EP_CONV), EPI_THREADS);
+    mbar_init(cta.bar(EP_C1), EPI_THREADS);
     mbar_init(cta.bar(EP_X), EPI_THREADS);
     mbar_init(cta.bar(EP_S), EPI_THREADS);
     mbar_init(cta.bar(RED), EPI_THREADS);
@@ -230,7 +232,8 @@ __device__ __forceinline__ void run_role(
           }
         }
         mma_commit(cta.bar(P_DONE));
-        if (!wait(cta, cta.bar(EP_CONV), par, ctl)) break;
+        // ---- the MMAs that need no masked score, once the fp16 operands are in place
+        if (!wait(cta, cta.bar(EP_C1), par, ctl)) break;
         if (!wait(cta, cta.bar(EP_S), par, ctl)) break;
         if (t >= 1 && !wait(cta, cta.bar(EP_X), (t - 1) & 1, ctl)) break;
         tc_fence_after();
@@ -244,41 +247,24 @@ __device__ __forceinline__ void run_role(
                        smem_desc(sb + OFF_G + (ks >> 2) * V_BOX + (ks & 3) * 32, 16, 1024, SW_128),
                        smem_desc(CP + (ks >> 2) * S_ATOM + (ks & 3) * 32, 16, 1024, SW_128), ID1,
                        ks > 0);
-          //    + dP'' K  (A = dP'' from TMEM, K = j; B = K as [j][dk], MN-major)
-          constexpr uint32_t ID2 = idesc_f16(128, 96, false, false, false, true);
-#pragma unroll 1
-          for (int ks = 0; ks < 8; ++ks)
-            mma_f16_ts(tmem + TM_X, tmem + TM_P + 8 * ks,
-                       smem_desc(sb + OFF_K + ks * 1024, Q_BOX, 512, SW_64), ID2, 1);
         } else if constexpr (ROLE == R_DV) {
-          // dv = P''^T dO  (A = P''^T from TMEM, K = i; B = dO as [i][dv], MN-major)
+          // dv = K' dS  (A = K' K-major, K = dk; B = adjoint copy [dk][dv], MN-major)
           constexpr uint32_t ID1 = idesc_f16(128, 192, false, false, false, true);
-#pragma unroll 1
-          for (int ks = 0; ks < 8; ++ks)
-            mma_f16_ts(tmem + TM_X, tmem + TM_P + 8 * ks,
-                       smem_desc(sb + OFF_G + ks * 2048, V_BOX, 1024, SW_128), ID1, ks > 0);
-          //    + K' dS  (A = K' K-major, K = dk; B = adjoint copy [dk][dv], MN-major)
 #pragma unroll 1
           for (int ks = 0; ks < 6; ++ks)
             mma_f16_ss(tmem + TM_X,
                        smem_desc(sb + OFF_K + (ks >> 1) * Q_BOX + (ks & 1) * 32, 16, 512, SW_64),
-                       smem_desc(CP + ks * 2048, S_ATOM, 1024, SW_128), ID1, 1);
+                       smem_desc(CP + ks * 2048, S_ATOM, 1024, SW_128), ID1, ks > 0);
         } else {
-          // dk = dP''^T Q  (A = dP''^T from TMEM, K = i; B = Q as [i][dk], MN-major)
-          constexpr uint32_t ID1 = idesc_f16(128, 96, false, false, false, true);
-#pragma unroll 1
-          for (int ks = 0; ks < 8; ++ks)
-            mma_f16_ts(tmem + TM_X, tmem + TM_P + 8 * ks,
-                       smem_desc(sb + OFF_Q + ks * 1024, Q_BOX, 512, SW_64), ID1, ks > 0);
-          //    + V' dS^T  (A = V' K-major, K = dv; B = adjoint copy [dk][dv], K-major)
+          // dk = V' dS^T  (A = V' K-major, K = dv; B = adjoint copy [dk][dv], K-major)
           constexpr uint32_t ID2 = idesc_f16(128, 96, false, false, false, false);
 #pragma unroll 1
           for (int ks = 0; ks < 12; ++ks)
             mma_f16_ss(tmem + TM_X,
                        smem_desc(sb + OFF_V + (ks >> 2) * V_BOX + (ks & 3) * 32, 16, 1024, SW_128),
-                       smem_desc(CP + (ks >> 2) * S_ATOM + (ks & 3) * 32, 16, 1024, SW_128), ID2, 1);
+                       smem_desc(CP + (ks >> 2) * S_ATOM + (ks & 3) * 32, 16, 1024, SW_128), ID2,
+                       ks > 0);
         }
-        mma_commit(cta.bar(X_DONE));
         // state / adjoint update, M = 128 (96 key channels + padding rows never read)
         {
           constexpr uint32_t ID = idesc_f16(128, 192, false, false, true, true);
@@ -289,6 +275,32 @@ __device__ __forceinline__ void run_role(
             mma_f16_ss(tmem + TM_S, smem_desc(A + ks * 1024, Q_BOX, 512, SW_64),
                        smem_desc(B + ks * 2048, V_BOX, 1024, SW_128), ID, 1);
         }
+        // ---- the masked scores are in TMEM (and DQ's r q in place)
+        if (!wait(cta, cta.bar(EP_CONV), par, ctl)) break;
+        tc_fence_after();
+        if constexpr (ROLE == R_DQ) {
+          //    + dP'' K  (A = dP'' from TMEM, K = j; B = K as [j][dk], MN-major)
+          constexpr uint32_t ID2 = idesc_f16(128, 96, false, false, false, true);
+#pragma unroll 1
+          for (int ks = 0; ks < 8; ++ks)
+            mma_f16_ts(tmem + TM_X, tmem + TM_P + 8 * ks,
+                       smem_desc(sb + OFF_K + ks * 1024, Q_BOX, 512, SW_64), ID2, 1);
+        } else if constexpr (ROLE == R_DV) {
+          //    + P''^T dO  (A = P''^T from TMEM, K = i; B = dO as [i][dv], MN-major)
+          constexpr uint32_t ID1 = idesc_f16(128, 192, false, false, false, true);
+#pragma unroll 1
+          for (int ks = 0; ks < 8; ++ks)
+            mma_f16_ts(tmem + TM_X, tmem + TM_P + 8 * ks,
+                       smem_desc(sb + OFF_G + ks * 2048, V_BOX, 1024, SW_128), ID1, 1);
+        } else {
+          //    + dP''^T Q  (A = dP''^T from TMEM, K = i; B = Q as [i][dk], MN-major)
+          constexpr uint32_t ID1 = idesc_f16(128, 96, false, false, false, true);
+#pragma unroll 1
+          for (int ks = 0; ks < 8; ++ks)
+            mma_f16_ts(tmem + TM_X, tmem + TM_P + 8 * ks,
+                       smem_desc(sb + OFF_Q + ks * 1024, Q_BOX, 512, SW_64), ID1, 1);
+        }
+        mma_commit(cta.bar(X_DONE));
         if constexpr (ROLE == R_DQ) {
           // d_a: diag((r q)^T k) accumulated over every chunk (A = r q as [i][dk] MN-major,
           // B = K as [i][dk] MN-major); rows 96..127 are padding
@@ -459,6 +471,10 @@ __device__ __forceinline__ void run_role(
         convert_row<BF16, 8>(base + OFF_V, vg, lk, range_max);  // V' (A of V' dS^T)
         convert_row<BF16, 8>(base + OFF_G, vg, lq, bmax);       // dO'' (adjoint B)
       }
+      // every fp16 operand but DQ's r q is in place: the state MMA and the output MMA's
+      // state-copy part may run while the masked scores are made
+      fence_proxy_async();
+      mbar_arrive(cta.bar(EP_C1));
       range_max = fmaxf(range_max, fmaxf(amax, bmax));
       {
         float am = amax, bm = bmax;
