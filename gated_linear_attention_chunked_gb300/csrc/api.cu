@@ -30,7 +30,7 @@ bool valid_dtype(gla_dtype t) { return t == GLA_BF16 || t == GLA_FP16 || t == GL
 // Common checks of the chunked calls.
 gla_status check_chunk_sizes(int B, int T, int H, int dk, int dv, gla_dtype t) {
   if (B <= 0 || T <= 0 || H <= 0) return GLA_ERR_INVALID_ARG;
-  if (dk != gla::kDK || dv != gla::kDV || T % gla::kChunk != 0 || !valid_dtype(t))
+  if (dk != gla::kDK || dv != gla::kDV || !valid_dtype(t))
     return GLA_ERR_UNSUPPORTED;
   if ((long long)B * T > (1ll << 31) - 1 || (long long)B * H > (1ll << 31) - 1)
     return GLA_ERR_UNSUPPORTED;

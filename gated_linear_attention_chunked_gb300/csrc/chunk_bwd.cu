@@ -131,7 +131,8 @@ __device__ __forceinline__ void run_role(
   constexpr int NX = ROLE == R_DV ? 192 : 96;  // output columns
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int H = p.H, T = p.T, b = bh / H, h = bh % H;
-  const int nc = T / C;
+  // chunks of this sequence; the last one holds L_last = 1..C tokens (rows past T are zeros)
+  const int nc = (T + C - 1) / C, L_last = T - (nc - 1) * C;
   const float gamma = __ldg(p.log_decay + h);
   float* pw = (float*)(base + OFF_PW);
   float* red = (float*)(base + OFF_RED);
@@ -176,21 +177,20 @@ __device__ __forceinline__ void run_role(
   if (warp == PRODUCER_WARP) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      const int row0 = b * T;
       auto load = [&](int c, bool prefetch_only) {
-        const int row = row0 + c * C;
+        const int t0 = c * C;
         for (int j = 0; j < 3; ++j) {
           if (prefetch_only) {
-            tma_prefetch_3d(&map_q, 32 * j, h, row);
-            tma_prefetch_3d(&map_k, 32 * j, h, row);
-            if (ROLE != R_DV) tma_prefetch_3d(&map_v, 64 * j, h, row);
-            tma_prefetch_3d(&map_g, 64 * j, h, row);
+            tma_prefetch_4d(&map_q, 32 * j, h, t0, b);
+            tma_prefetch_4d(&map_k, 32 * j, h, t0, b);
+            if (ROLE != R_DV) tma_prefetch_4d(&map_v, 64 * j, h, t0, b);
+            tma_prefetch_4d(&map_g, 64 * j, h, t0, b);
           } else {
-            tma_load_3d(sb + OFF_Q + j * Q_BOX, &map_q, cta.bar(FULL), 32 * j, h, row);
-            tma_load_3d(sb + OFF_K + j * Q_BOX, &map_k, cta.bar(FULL), 32 * j, h, row);
+            tma_load_4d(sb + OFF_Q + j * Q_BOX, &map_q, cta.bar(FULL), 32 * j, h, t0, b);
+            tma_load_4d(sb + OFF_K + j * Q_BOX, &map_k, cta.bar(FULL), 32 * j, h, t0, b);
             if (ROLE != R_DV)
-              tma_load_3d(sb + OFF_V + j * V_BOX, &map_v, cta.bar(FULL), 64 * j, h, row);
-            tma_load_3d(sb + OFF_G + j * V_BOX, &map_g, cta.bar(FULL), 64 * j, h, row);
+              tma_load_4d(sb + OFF_V + j * V_BOX, &map_v, cta.bar(FULL), 64 * j, h, t0, b);
+            tma_load_4d(sb + OFF_G + j * V_BOX, &map_g, cta.bar(FULL), 64 * j, h, t0, b);
           }
         }
       };
@@ -326,8 +326,15 @@ __device__ __forceinline__ void run_role(
     const int i = 32 * q4 + lane;
     const uint32_t trow = tmem + ((uint32_t)(32 * q4) << 16);
     const float lam = pw[1], lamC = expf((float)C * gamma);
+    const float lamL = L_last == C ? lamC : pw[L_last];  // lambda^(tokens of the last chunk)
     const float lq = (i + 1 < C) ? pw[i + 1] : lamC;  // lambda^(row+1)
-    const float lk = pw[C - 1 - i];                   // lambda^(C-1-row)
+    const float lk_full = pw[C - 1 - i];              // lambda^(C-1-row)
+    // in the last chunk: lambda^(L_last-1-row), and 0 on the zero rows past T
+    const float lk_last = i < L_last ? pw[L_last - 1 - i] : 0.f;
+    // the decay applied to the state (adjoint) before step t's update is lambda^(tokens of
+    // chunk_at(t)): lamL only for the last chunk, which is the first step of the reverse scans
+    // and the last of the forward one
+    const float dec_first = (ROLE != R_DQ || nc == 1) ? lamL : lamC;  // step 0
     uint8_t* const stage = base + OFF_STG + warp * 2048;  // this warp's output staging
     auto qk = [&](int cc) { return qk_chunk(i, 4 * sub + cc); };  // this part's q/k chunks
     auto vg = [&](int cc) { return vg_chunk(i, 8 * sub + cc); };  // this part's v/dO chunks
@@ -335,8 +342,9 @@ __device__ __forceinline__ void run_role(
     bool bad = false;
 
     // state copy S * 2^-e (rows < 96, this part's 64 columns) into the copy buffer,
-    // D_S <- lambda^C S, and this warp's max|S| into red[use & 1]
-    auto publish_state = [&](int use, int e, const float* g_row, bool from_tmem) {
+    // D_S <- dec S (dec = lambda^(tokens of the chunk whose update follows)), and this warp's
+    // max|S| into red[use & 1]
+    auto publish_state = [&](int use, int e, float dec, const float* g_row, bool from_tmem) {
       float m = 0.f;
       if (q4 < 3) {
         const float sc = pow2i(-e);
@@ -365,7 +373,7 @@ __device__ __forceinline__ void run_role(
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             m = fmaxf(m, fabsf(r[j]));
-            u[j] = __float_as_uint(r[j] * lamC);
+            u[j] = __float_as_uint(r[j] * dec);
           }
           tmem_st32(trow + TM_S + col, u);
         }
@@ -406,7 +414,7 @@ __device__ __forceinline__ void run_role(
         bad = true;
         e_cur = 0;
       }
-      publish_state(0, e_cur, g_row0, false);
+      publish_state(0, e_cur, dec_first, g_row0, false);
     }
 
     // in-register fp16 copy of four q/k chunks of this part (x: 16-bit input words), scaled
@@ -428,6 +436,7 @@ __device__ __forceinline__ void run_role(
     for (int t = 0; t < nc && ok; ++t) {
       const uint32_t par = t & 1;
       const int c = chunk_at<ROLE>(t, nc);
+      const float lk = c == nc - 1 ? lk_last : lk_full;
       if (!(ok = wait(cta, cta.bar(FULL), par, ctl))) break;
       // ---- gate partial sum z = q.(a*k) over this part's 32 channels, fused with the fp16
       // copy of whichever of q, k the score MMA does not read (DQ: k, DK: q, both scale 1);
@@ -580,7 +589,7 @@ __device__ __forceinline__ void run_role(
       __syncwarp();
       {
         const float osc = pow2i(e_cur);
-        const int row = b * T + c * C + 32 * q4;
+        const int t0 = c * C + 32 * q4;  // first token of this warp's rows (boxes past T: none)
         constexpr int NCOL = NX / 3;  // 32 (DQ, DK) or 64 (DV)
         emit_rows_tma1<NCOL / 16>(
             stage, lane,
@@ -601,7 +610,9 @@ __device__ __forceinline__ void run_role(
                   x[j] = fmaf(__uint_as_float(r[j]), osc, rr * sa[col + j] * f8[j >> 3][j & 7]);
               }
             },
-            [&](int k, uint32_t src) { tma_store_3d(&map_out, src, NCOL * sub + 16 * k, h, row); });
+            [&](int k, uint32_t src) {
+              if (t0 < T) tma_store_4d(&map_out, src, NCOL * sub + 16 * k, h, t0, b);
+            });
       }
       tc_fence_before();
       mbar_arrive(cta.bar(EP_X));
@@ -611,14 +622,15 @@ __device__ __forceinline__ void run_role(
       int e_next = e_cur;
       if (t < nc - 1) {
         // bound on the next state: all parts' operand maxima and max|S| of this step's copy
+        // (decayed by this step's factor)
         if (!(ok = wait(cta, cta.bar(EP_CONV), par, ctl))) break;
-        e_next = state_exponent(lamC * max12(red + par * 12) +
+        e_next = state_exponent((t == 0 ? dec_first : lamC) * max12(red + par * 12) +
                                 (float)C * max12(abmax + par * 24) * max12(abmax + par * 24 + 12));
         if (e_next < 0) {
           bad = true;
           e_next = 0;
         }
-        publish_state(t + 1, e_next, nullptr, true);
+        publish_state(t + 1, e_next, (ROLE == R_DQ && t + 2 == nc) ? lamL : lamC, nullptr, true);
       }
       // ---- adjoint of the initial state (DV, after the last step = chunk 0)
       if (ROLE == R_DV && t == nc - 1 && p.want_dinit && q4 < 3) {
@@ -704,13 +716,13 @@ size_t chunk_bwd_workspace_bytes(int B, int T, int H) {
 
 cudaError_t launch_chunk_bwd(const BwdArgs& a, DevCtl ctl, cudaStream_t stream) {
   CUtensorMap mq, mk, mv, mg, mdq, mdk, mdv, mdi;
-  const long long rows = (long long)a.B * a.T;
-  if (!make_tmap_3d_16bit(&mq, a.q, DK, a.H, rows, 32, C, CU_TENSOR_MAP_SWIZZLE_64B, a.bf16) ||
-      !make_tmap_3d_16bit(&mk, a.k, DK, a.H, rows, 32, C, CU_TENSOR_MAP_SWIZZLE_64B, a.bf16) ||
-      !make_tmap_3d_16bit(&mv, a.v, DV, a.H, rows, 64, C, CU_TENSOR_MAP_SWIZZLE_128B, a.bf16) ||
-      !make_tmap_3d_16bit(&mg, a.dO, DV, a.H, rows, 64, C, CU_TENSOR_MAP_SWIZZLE_128B, a.bf16) ||
-      !make_tmap_out_f32(&mdq, a.dq, DK, a.H, rows) || !make_tmap_out_f32(&mdk, a.dk, DK, a.H, rows) ||
-      !make_tmap_out_f32(&mdv, a.dv, DV, a.H, rows) ||
+  if (!make_tmap_seq_16bit(&mq, a.q, DK, a.H, a.T, a.B, 32, C, CU_TENSOR_MAP_SWIZZLE_64B, a.bf16) ||
+      !make_tmap_seq_16bit(&mk, a.k, DK, a.H, a.T, a.B, 32, C, CU_TENSOR_MAP_SWIZZLE_64B, a.bf16) ||
+      !make_tmap_seq_16bit(&mv, a.v, DV, a.H, a.T, a.B, 64, C, CU_TENSOR_MAP_SWIZZLE_128B, a.bf16) ||
+      !make_tmap_seq_16bit(&mg, a.dO, DV, a.H, a.T, a.B, 64, C, CU_TENSOR_MAP_SWIZZLE_128B, a.bf16) ||
+      !make_tmap_seq_out_f32(&mdq, a.dq, DK, a.H, a.T, a.B) ||
+      !make_tmap_seq_out_f32(&mdk, a.dk, DK, a.H, a.T, a.B) ||
+      !make_tmap_seq_out_f32(&mdv, a.dv, DV, a.H, a.T, a.B) ||
       !make_tmap_state_f32(&mdi, a.dinit ? (const void*)a.dinit : (const void*)a.dv,
                            (long long)a.B * a.H))
     return cudaErrorInvalidValue;

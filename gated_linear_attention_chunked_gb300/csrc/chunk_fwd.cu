@@ -112,7 +112,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
   uint8_t* const base = cta.base;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int bh = blockIdx.x, b = bh / H, h = bh % H;
-  const int nc = T / C;
+  // chunks of this sequence; the last one holds L_last = 1..C tokens (rows past T are zeros)
+  const int nc = (T + C - 1) / C, L_last = T - (nc - 1) * C;
   const float gamma = __ldg(log_decay + h);
   float* pw = (float*)(base + OFF_PW);
   float* red = (float*)(base + OFF_RED);
@@ -159,21 +160,20 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
       prefetch_tensormap(&map_k);
       prefetch_tensormap(&map_v);
       prefetch_tensormap(&map_o);
-      const int row0 = b * T;
       int armed_qk[2] = {0, 0}, armed_v[2] = {0, 0};
       for (int c = 0; c < nc; ++c) {
         const uint32_t s = c & 1, st = cta.sb + s * STAGE;
-        const int row = row0 + c * C;
+        const int t0 = c * C;
         if (c >= 2 && !wait(cta, cta.bar(V_EMPTY + s), ((c >> 1) - 1) & 1, ctl)) break;
         mbar_arrive_expect_tx(cta.bar(V_FULL + s), V_BYTES);
         for (int j = 0; j < 3; ++j)
-          tma_load_3d(st + OFF_V + j * V_BOX, &map_v, cta.bar(V_FULL + s), 64 * j, h, row);
+          tma_load_4d(st + OFF_V + j * V_BOX, &map_v, cta.bar(V_FULL + s), 64 * j, h, t0, b);
         ++armed_v[s];
         if (c >= 1 && !wait(cta, cta.bar(QK_EMPTY + s), ((c - 1) >> 1) & 1, ctl)) break;
         mbar_arrive_expect_tx(cta.bar(QK_FULL + s), QK_BYTES);
         for (int j = 0; j < 3; ++j) {
-          tma_load_3d(st + OFF_Q + j * Q_BOX, &map_q, cta.bar(QK_FULL + s), 32 * j, h, row);
-          tma_load_3d(st + OFF_K + j * Q_BOX, &map_k, cta.bar(QK_FULL + s), 32 * j, h, row);
+          tma_load_4d(st + OFF_Q + j * Q_BOX, &map_q, cta.bar(QK_FULL + s), 32 * j, h, t0, b);
+          tma_load_4d(st + OFF_K + j * Q_BOX, &map_k, cta.bar(QK_FULL + s), 32 * j, h, t0, b);
         }
         ++armed_qk[s];
       }
@@ -243,10 +243,13 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
     const uint32_t trow = tmem + ((uint32_t)(32 * warp) << 16);
     const float lam = pw[1], lamC = expf((float)C * gamma);
     const float lq = (i + 1 < C) ? pw[i + 1] : lamC;  // lambda^(i+1)
-    const float lk = pw[C - 1 - i];                   // lambda^(C-1-i)
+    const float lk_full = pw[C - 1 - i];              // lambda^(C-1-i)
+    // in the last chunk (L_last tokens): lambda^(L_last-1-i), and 0 on the zero rows past T
+    const float lk_last = i < L_last ? pw[L_last - 1 - i] : 0.f;
     float range_max = 0.f;
     for (int c = 0; c < nc; ++c) {
       const uint32_t s = c & 1, par = c & 1;
+      const float lk = c == nc - 1 ? lk_last : lk_full;
       uint8_t* stg = base + s * STAGE;
       float vmax = 0.f, kmax = 0.f, qmax = 0.f;
       if (!wait(cta, cta.bar(V_FULL + s), (c >> 1) & 1, ctl)) break;
@@ -363,12 +366,14 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
     const int i = 32 * q4 + lane;
     const uint32_t trow = tmem + ((uint32_t)(32 * q4) << 16);
     const float lamC = expf((float)C * gamma);
+    const float lamL = L_last == C ? lamC : pw[L_last];  // lambda^(tokens of the last chunk)
     bool bad = false;
 
     // fp16 copy S * 2^-e of this warp's state rows / column half into the q/k slot at
-    // `slot_off`, D_S <- lambda^C S, and the warp's max|S| into red[use & 1].  Row i comes
-    // from TMEM (the state after the chunk's update) or from init_state (`g_row`).
-    auto publish_state = [&](uint32_t slot_off, int use, int e, const float* g_row,
+    // `slot_off`, D_S <- dec S (dec = lambda^(tokens of chunk `use`, whose update follows)),
+    // and the warp's max|S| into red[use & 1].  Row i comes from TMEM (the state after the
+    // chunk's update) or from init_state (`g_row`).
+    auto publish_state = [&](uint32_t slot_off, int use, int e, float dec, const float* g_row,
                              bool from_tmem) {
       float m = 0.f;
       if (q4 < 3) {
@@ -398,7 +403,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             m = fmaxf(m, fabsf(r[j]));
-            u[j] = __float_as_uint(r[j] * lamC);
+            u[j] = __float_as_uint(r[j] * dec);
           }
           tmem_st32(trow + TM_S + col, u);
         }
@@ -451,7 +456,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
         bad = true;
         e_cur = 0;
       }
-      publish_state(1 * STAGE + OFF_Q, 0, e_cur, g_row0, false);
+      publish_state(1 * STAGE + OFF_Q, 0, e_cur, nc == 1 ? lamL : lamC, g_row0, false);
     }
 
     for (int c = 0; c < nc && ok; ++c) {
@@ -477,14 +482,14 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
           bad = true;
           e_next = 0;
         }
-        publish_state(s * STAGE + OFF_Q, c + 1, e_next, nullptr, true);
+        publish_state(s * STAGE + OFF_Q, c + 1, e_next, c + 2 == nc ? lamL : lamC, nullptr, true);
       }
       // ---- output rows: o = 2^e D_O for columns [96hf, 96hf+96) (the self-augmentation
       // sigmoid(z) v is already in D_O through the diagonal of P''), TMA-stored
       uint8_t* const stage_o = base + OFF_STG + ew * 4096;
       if constexpr (!GATED) {
         const float osc = pow2i(e_cur);
-        const int row = b * T + c * C + 32 * q4;
+        const int t0 = c * C + 32 * q4;  // first token of this warp's rows (boxes past T: none)
         emit_rows_tma<6>(
             stage_o, lane,
             [&](int k, float (&o)[16]) {
@@ -494,13 +499,16 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
 #pragma unroll
               for (int j = 0; j < 16; ++j) o[j] = __uint_as_float(r[j]) * osc;
             },
-            [&](int k, uint32_t src) { tma_store_3d(&map_o, src, 96 * hf + 16 * k, h, row); });
+            [&](int k, uint32_t src) {
+              if (t0 < T) tma_store_4d(&map_o, src, 96 * hf + 16 * k, h, t0, b);
+            });
       } else {
         // y = o r w[tier] SiLU(g), r = (mean over the row's 192 channels of o^2 + eps)^-1/2:
         // pass 1 sums o^2 over this warp's 96 columns (writing o too if asked), the two warps
         // of the row quadrant exchange their sums, pass 2 writes y
         const float osc = pow2i(e_cur);
-        const int row = b * T + c * C + 32 * q4;
+        const int t0 = c * C + 32 * q4;  // first token of this warp's rows (boxes past T: none)
+        const bool live = c * C + i < T;  // this thread's row is a token of the sequence
         const long long tok = (long long)b * T + c * C + i;  // token row of this thread
         float* xch = (float*)(base + OFF_XCH);
         float ss = 0.f;
@@ -517,7 +525,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                   ss = fmaf(o[j], o[j], ss);
                 }
               },
-              [&](int k, uint32_t src) { tma_store_3d(&map_o, src, 96 * hf + 16 * k, h, row); });
+              [&](int k, uint32_t src) {
+                if (t0 < T) tma_store_4d(&map_o, src, 96 * hf + 16 * k, h, t0, b);
+              });
         } else {
 #pragma unroll 1
           for (int k = 0; k < 6; ++k) {
@@ -535,12 +545,12 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
         const uint4* gp = reinterpret_cast<const uint4*>(og.g + (tok * H + h) * DV + 96 * hf);
         uint4 gq[12];
 #pragma unroll
-        for (int u = 0; u < 12; ++u) gq[u] = __ldg(gp + u);
+        for (int u = 0; u < 12; ++u) gq[u] = live ? __ldg(gp + u) : make_uint4(0u, 0u, 0u, 0u);
         xch[hf * 128 + i] = ss;
         mbar_arrive(cta.bar(QX + q4));
         if (!(ok = wait(cta, cta.bar(QX + q4), par, ctl))) break;
         const float rr = 1.f / sqrtf((xch[i] + xch[128 + i]) * (1.f / DV) + og.eps);
-        if (og.rstd && hf == 0) og.rstd[tok * H + h] = rr;
+        if (og.rstd && hf == 0 && live) og.rstd[tok * H + h] = rr;
         const float* wrow = og.w + (h / og.heads_per_tier) * DV + 96 * hf;
         if (lane == 0) bulk_wait_read<0>();  // pass 1's stores have read the staging
         __syncwarp();
@@ -560,7 +570,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                 y[j] = __uint_as_float(r[j]) * f * __ldg(wrow + 16 * k + j) * sl;
               }
             },
-            [&](int k, uint32_t src) { tma_store_3d(&map_y, src, 96 * hf + 16 * k, h, row); });
+            [&](int k, uint32_t src) {
+              if (t0 < T) tma_store_4d(&map_y, src, 96 * hf + 16 * k, h, t0, b);
+            });
       }
       tc_fence_before();
       mbar_arrive(cta.bar(EP_O));
@@ -603,13 +615,12 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
 
 cudaError_t launch_chunk_fwd(const FwdArgs& a, DevCtl ctl, cudaStream_t stream) {
   CUtensorMap mq, mk, mv, mo, mfin, my;
-  const long long rows = (long long)a.B * a.T;
   float* const o_any = a.o ? a.o : a.og.y;  // stand-in for a map that is never used
-  if (!make_tmap_3d_16bit(&mq, a.q, DK, a.H, rows, 32, C, CU_TENSOR_MAP_SWIZZLE_64B, a.bf16) ||
-      !make_tmap_3d_16bit(&mk, a.k, DK, a.H, rows, 32, C, CU_TENSOR_MAP_SWIZZLE_64B, a.bf16) ||
-      !make_tmap_3d_16bit(&mv, a.v, DV, a.H, rows, 64, C, CU_TENSOR_MAP_SWIZZLE_128B, a.bf16) ||
-      !make_tmap_out_f32(&mo, o_any, DV, a.H, rows) ||
-      !make_tmap_out_f32(&my, a.og.y ? a.og.y : o_any, DV, a.H, rows) ||
+  if (!make_tmap_seq_16bit(&mq, a.q, DK, a.H, a.T, a.B, 32, C, CU_TENSOR_MAP_SWIZZLE_64B, a.bf16) ||
+      !make_tmap_seq_16bit(&mk, a.k, DK, a.H, a.T, a.B, 32, C, CU_TENSOR_MAP_SWIZZLE_64B, a.bf16) ||
+      !make_tmap_seq_16bit(&mv, a.v, DV, a.H, a.T, a.B, 64, C, CU_TENSOR_MAP_SWIZZLE_128B, a.bf16) ||
+      !make_tmap_seq_out_f32(&mo, o_any, DV, a.H, a.T, a.B) ||
+      !make_tmap_seq_out_f32(&my, a.og.y ? a.og.y : o_any, DV, a.H, a.T, a.B) ||
       !make_tmap_state_f32(&mfin, a.fin ? (const void*)a.fin : (const void*)o_any,
                            a.sp.page ? (long long)a.sp.n_pages * a.sp.pool_layers * a.H
                                      : (long long)(a.B / a.seg) * a.H))

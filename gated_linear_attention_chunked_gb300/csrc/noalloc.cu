@@ -52,7 +52,7 @@ gla_status gla_chunk_bwd_noalloc(const void* q, const void* k, const void* v, gl
                                  float* d_aug, float* d_init_state, int B, int T, int H, int dk_,
                                  int dv_, cudaStream_t stream) {
   if (B <= 0 || T <= 0 || H <= 0) return GLA_ERR_INVALID_ARG;
-  if (dk_ != gla::kDK || dv_ != gla::kDV || T % gla::kChunk != 0) return GLA_ERR_UNSUPPORTED;
+  if (dk_ != gla::kDK || dv_ != gla::kDV) return GLA_ERR_UNSUPPORTED;
   if (in_dtype != GLA_BF16 && in_dtype != GLA_FP16) return GLA_ERR_UNSUPPORTED;
   if ((long long)B * H > GLA_NOALLOC_MAX_BH) return GLA_ERR_WORKSPACE;
   if ((long long)B * T > (1ll << 31) - 1) return GLA_ERR_UNSUPPORTED;

@@ -233,6 +233,7 @@ __global__ void seg_combine_kernel(const float* __restrict__ init, const float* 
 int fwd_segments(int B, int T, int H, int n_sm) {
   const long long bh = (long long)B * H;
   const int nc = T / C;
+  if (T % C != 0) return 1;                  // a ragged last chunk: one serial scan
   if (n_sm <= 0 || 2 * bh > n_sm) return 1;  // enough (b, h) pairs to fill the GPU already
   int best = 1;
   for (int G = 2; G <= nc / MIN_SEGMENT_CHUNKS && bh * G <= n_sm; ++G)

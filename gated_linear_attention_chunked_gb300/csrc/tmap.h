@@ -1,4 +1,4 @@
-// tmap.h -- host-side construction of TMA tensor maps for the token-major [rows, H, d]
+// tmap.h -- host-side construction of TMA tensor maps for the token-major [B, T, H, d]
 // tensors the chunk kernels stream.  cuTensorMapEncodeTiled is fetched through the runtime's
 // driver entry point so that the library has no link-time dependency on libcuda.
 #pragma once
@@ -42,6 +42,39 @@ inline bool make_tmap_3d_16bit(CUtensorMap* map, const void* base, int d, int H,
   return r == CUDA_SUCCESS;
 }
 
+// A 16-bit tensor [B, T, H, d] viewed as 4-D (innermost first): {d, H, T, B}.  A box
+// {box_d, 1, box_rows, 1} is a tile of `box_rows` consecutive tokens of one head of one
+// sequence; rows past the sequence's T tokens load as zeros.
+inline bool make_tmap_seq_16bit(CUtensorMap* map, const void* base, int d, int H, int T, int B,
+                                int box_d, int box_rows, CUtensorMapSwizzle sw, bool is_bf16) {
+  auto fn = encode_tiled_fn();
+  if (!fn) return false;
+  cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)d * 2 * H, (cuuint64_t)d * 2 * H * T};
+  cuuint32_t box[4] = {(cuuint32_t)box_d, 1u, (cuuint32_t)box_rows, 1u};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(map, is_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                  4, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// fp32 token-major output [B, T, H, d] as 4-D {d, H, T, B}, stored from shared memory in boxes
+// of 16 channels x 32 consecutive tokens of one head (64-byte rows, 64-byte swizzle); rows past
+// the sequence's T tokens are not written.
+inline bool make_tmap_seq_out_f32(CUtensorMap* map, const void* base, int d, int H, int T, int B) {
+  auto fn = encode_tiled_fn();
+  if (!fn) return false;
+  cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)d * 4, (cuuint64_t)d * 4 * H, (cuuint64_t)d * 4 * H * T};
+  cuuint32_t box[4] = {16u, 1u, 32u, 1u};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // A generic 3-D tensor map: dims / box innermost first, strides in bytes of dims 1 and 2.
 inline bool make_tmap_3d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype,
                          const unsigned long long (&dims)[3], const unsigned long long (&strides)[2],
@@ -55,17 +88,6 @@ inline bool make_tmap_3d(CUtensorMap* map, const void* base, CUtensorMapDataType
   return fn(map, dtype, 3, const_cast<void*>(base), d, st, bx, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
             sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
          CUDA_SUCCESS;
-}
-
-// fp32 token-major output [rows, H, d] stored from shared memory in boxes of 16 channels x
-// 32 consecutive tokens of one head (64-byte rows, 64-byte swizzle).
-inline bool make_tmap_out_f32(CUtensorMap* map, const void* base, int d, int H, long long rows) {
-  const unsigned long long dims[3] = {(unsigned long long)d, (unsigned long long)H,
-                                      (unsigned long long)rows};
-  const unsigned long long strides[2] = {(unsigned long long)d * 4, (unsigned long long)d * 4 * H};
-  const unsigned box[3] = {16, 1, 32};
-  return make_tmap_3d(map, base, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dims, strides, box,
-                      CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 // fp32 states [BH, 96, 192] stored in boxes of 16 value channels x 32 key channels.

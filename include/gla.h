@@ -32,8 +32,9 @@
  *  - Layout: token-major and contiguous.  q, k: [B, T, H, dk]; v, o, dO:
  *    [B, T, H, dv]; states: [B, H, dk, dv] (row i = key channel, column n =
  *    value channel); aug_balance: [H, dk]; log_decay: [H].
- *  - Supported sizes: dk = 96, dv = 192 (the model's head sizes); T a
- *    multiple of the chunk size 128 for the chunked calls; B, T, H > 0.
+ *  - Supported sizes: dk = 96, dv = 192 (the model's head sizes); B, T, H > 0.
+ *    The chunked calls take any T: a sequence is ceil(T / 128) chunks and the
+ *    last one holds the remaining 1..128 tokens.
  *  - Alignment: every tensor pointer must be 16-byte aligned.
  *  - Decay: log_decay[h] = gamma_h = ln(lambda_h) (natural log, < 0 for a
  *    decaying head).  The decay is fixed, so there is no gradient for it.
@@ -58,7 +59,7 @@ extern "C" {
 typedef enum {
   GLA_OK = 0,
   GLA_ERR_INVALID_ARG = 1, /* null pointer where one is required, size <= 0 */
-  GLA_ERR_UNSUPPORTED = 2, /* dk != 96, dv != 192, T % 128 != 0, unknown dtype */
+  GLA_ERR_UNSUPPORTED = 2, /* dk != 96, dv != 192, unknown dtype, sizes past 2^31 tokens */
   GLA_ERR_ALIGNMENT = 3,   /* a tensor pointer is not 16-byte aligned */
   GLA_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed */
   GLA_ERR_TIMEOUT = 5,     /* device: a bounded wait inside a kernel gave up */
@@ -120,7 +121,7 @@ GLA_API gla_status gla_decay_schedule(int H, double t_min, double t_max, float* 
  *   workspace    device scratch, 256-byte aligned, of gla_chunk_fwd_workspace_size()
  *                bytes.  fp32 inputs need their fp16 copies there (GLA_ERR_WORKSPACE
  *                if it is smaller).  With few long sequences (2*B*H <= the current
- *                device's SM count and T >= 4096) the size also covers the
+ *                device's SM count, T >= 4096 and a multiple of 128) the size also covers the
  *                segment-parallel path: every segment's state sum in parallel, their
  *                recurrence, then the segments as independent sequences (the state
  *                recurrence is linear).  Given less (or NULL for 16-bit inputs), the

@@ -74,7 +74,8 @@ def fwd(lib, q=A16, k=A16, v=A16, dt=0, ld=A16, a=A16, init=None, o=A16, fin=Non
 def test_chunk_fwd_argument_checks(lib):
     assert fwd(lib, dk=64) == 2                      # unsupported head size
     assert fwd(lib, dv=128) == 2
-    assert fwd(lib, T=200) == 2                      # not a multiple of the chunk
+    assert fwd(lib, T=200, q=A16 + 8) == 3           # any T: the sizes pass, the next check fails
+    assert fwd(lib, B=1 << 20, T=1 << 12) == 2       # 2^32 tokens: beyond the index range
     assert fwd(lib, dt=7) == 2                       # unknown dtype
     assert fwd(lib, B=0) == 1 and fwd(lib, T=0) == 1 and fwd(lib, H=-1) == 1
     assert fwd(lib, q=None) == 1 and fwd(lib, o=None) == 1 and fwd(lib, a=None) == 1
@@ -94,7 +95,7 @@ def test_chunk_bwd_argument_checks(lib):
         return lib.gla_chunk_bwd(A16, A16, A16, 0, A16, A16, None, dO, None, dq, A16, A16, d_aug,
                                  None, None, 0, 1, T, 1, dk_, 192, None)
     assert bwd() == 2
-    assert bwd(dk_=96, T=100) == 2
+    assert bwd(dk_=96, T=100, dq=A16 + 2) == 3         # any T: the sizes pass
     assert bwd(dk_=96, dO=None) == 1
     assert bwd(dk_=96, d_aug=None) == 1
     assert bwd(dk_=96, dq=A16 + 2) == 3
@@ -134,7 +135,7 @@ def test_paged_argument_checks(lib):
     assert fwdp(layer=2) == 1 and fwdp(layer=-1) == 1 and fwdp(P=0) == 1
     assert fwdp(page=None) == 1 and fwdp(pool=None) == 1
     assert fwdp(page=A16 + 4) == 3
-    assert fwdp(T=100) == 2
+    assert fwdp(T=100, page=A16 + 4) == 3
 
 
 def test_head_norm_argument_checks(lib):

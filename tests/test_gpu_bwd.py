@@ -46,6 +46,12 @@ CASES = [
     (2, 384, 5, "bf16", 0.05, 0.05, 0.1, 32),
     (1, 256, 2, "fp16", 0.05, 0.02, 0.1, 33),
     (3, 640, 16, "bf16", 0.02, 0.01, 0.02, 34),
+    # ragged: the last chunk (the reverse scans' first) holds T mod 128 tokens
+    (2, 1, 3, "bf16", 0.05, 0.05, 0.1, 35),
+    (2, 77, 3, "bf16", 0.05, 0.05, 0.1, 36),
+    (2, 200, 16, "bf16", 0.02, 0.05, 0.02, 37),
+    (1, 300, 2, "fp32", 0.05, 0.05, 0.1, 38),
+    (3, 511, 5, "fp16", 0.02, 0.02, 0.1, 39),
 ]
 
 

@@ -44,6 +44,12 @@ CASES = [
     (1, 256, 2, "fp16", 0.05, 0.1, 13),
     (1, 256, 2, "fp32", 0.0, 0.1, 0),      # the tiny fp32 workload shape
     (3, 640, 16, "bf16", 0.02, 0.02, 14),  # all 16 decay tiers, 5 chunks
+    # ragged: the last chunk holds T mod 128 tokens (zero rows past T, its own decay powers)
+    (2, 1, 3, "bf16", 0.05, 0.1, 15),      # a single token per sequence
+    (2, 77, 3, "bf16", 0.05, 0.1, 16),     # one partial chunk
+    (2, 200, 16, "bf16", 0.05, 0.02, 17),  # a full chunk and 72 tokens, all decay tiers
+    (1, 300, 2, "fp32", 0.05, 0.1, 18),    # fp32 inputs
+    (3, 511, 5, "fp16", 0.02, 0.1, 19),    # four chunks, the last one 127 tokens
 ]
 
 
@@ -165,6 +171,7 @@ def test_fwd_segmented_path(env, B, T, H, seed):
     (2, 384, 4, 2, True, 41),      # serial scan, o written too
     (1, 4096, 2, 1, False, 42),    # segment-parallel path, y only
     (8, 2048, 16, 4, True, 43),    # one training-shape layer
+    (2, 200, 4, 2, True, 44),      # ragged last chunk: y, rstd and o stop at T
 ])
 def test_fwd_gated(env, B, T, H, n_tiers, want_o, seed):
     """The forward with the output epilogue fused in: y (Head RMSNorm per tier, SiLU(g) gate)
@@ -199,3 +206,29 @@ def test_fwd_gated(env, B, T, H, n_tiers, want_o, seed):
         torch.cuda.synchronize()
         assert torch.equal(o, o_plain)
         assert rel_err(y.cpu().numpy(), y2.cpu().numpy()) <= 1e-5
+
+
+def test_fwd_ragged_writes_nothing_past_t(env):
+    """With T = 200 the last chunk's rows 72..127 are padding: o and the final state match the
+    oracle, and the output buffer's elements right after the last sequence stay untouched."""
+    import oracle
+    gla, torch = env
+    B, T, H, seed = 2, 200, 3, 19
+    q, k, v = synth.qkv(seed, B, T, H)
+    a = synth.aug_balance(seed, (H, 96), 0.1)
+    init = synth.init_state(seed, B, H, 0.05)
+    n = B * T * H * 192
+    big = torch.full((n + 64 * H * 192,), float("nan"), dtype=torch.float32, device="cuda")
+    o = big[:n].view(B, T, H, 192)
+    fin = torch.empty((B, H, 96, 192), dtype=torch.float32, device="cuda")
+    gam = gla.decay_schedule(H)
+    gla.chunk_fwd(to_dev(q, torch.bfloat16), to_dev(k, torch.bfloat16), to_dev(v, torch.bfloat16),
+                  gam.cuda(), to_dev(a, torch.float32), to_dev(init, torch.float32), out=o,
+                  final_state=fin)
+    torch.cuda.synchronize()
+    assert gla.get_device_error() == 0
+    o_ref, fin_ref = oracle.fwd(q, k, v, gam.numpy().astype(np.float64), a, init)
+    eo, ef = rel_err(o.cpu().numpy(), o_ref), rel_err(fin.cpu().numpy(), fin_ref)
+    print(f"fwd ragged T={T}: o {eo:.2e} final {ef:.2e}")
+    assert eo <= TOL_CHUNK and ef <= TOL_CHUNK
+    assert torch.isnan(big[n:]).all()

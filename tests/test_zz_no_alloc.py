@@ -50,7 +50,7 @@ def test_noalloc_matches_workspace_backward_on_two_calls_in_a_row():
     gla, fn = _lib()
     stream = torch.cuda.current_stream().cuda_stream
     # two different problems back to back: the second reuses the array the first wrote
-    for (B, T, H, seed) in [(2, 384, 5, 41), (3, 256, 16, 42)]:
+    for (B, T, H, seed) in [(2, 384, 5, 41), (3, 256, 16, 42), (2, 200, 3, 43)]:
         q, k, v = synth.qkv(seed, B, T, H)
         dO = synth.grad_out(seed, B, T, H)
         a = synth.aug_balance(seed, (H, 96), 0.1)
