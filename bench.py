@@ -623,8 +623,9 @@ def run_paged_decode(args):
 
 def run_long_prefill(args):
     """--part long: the long-context prefill forward (B=2, T=131072, H=16, bf16, initial state
-    ~ N(0, 0.01)), through the public API with its workspace (segment-parallel path) and,
-    for comparison, without one (serial chunk scan)."""
+    ~ N(0, 0.01)), through the public API with its workspace (pairs cut into parts) and, for
+    comparison, without one (one serial chunk scan per pair); then the backward of the same
+    shape both ways."""
     import torch
     import gated_linear_attention_chunked_gb300 as gla
     dev = torch.device("cuda", 0)
@@ -667,6 +668,41 @@ def run_long_prefill(args):
 
     seg_ms = timed(ws.data_ptr(), nws, max(args.steps, 5))
     ser_ms = timed(None, 0, 3)
+    plan_f = gla.split_plan(Bl, Tl, H, False, torch.cuda.get_device_properties(dev).multi_processor_count)
+
+    # the backward of the same shape: with the workspace that lets pairs be cut, and with only
+    # the part it requires
+    dO = rn(Bl, Tl, H, DV).bfloat16()
+    dq, dk = torch.empty(Bl, Tl, H, DK, device=dev), torch.empty(Bl, Tl, H, DK, device=dev)
+    dv, dinit = torch.empty(Bl, Tl, H, DV, device=dev), torch.empty(Bl, H, DK, DV, device=dev)
+    d_a = torch.empty(H, DK, device=dev)
+    nwb = gla.chunk_bwd_workspace_size(Bl, Tl, H, gla.GLA_BF16)
+    wsb = torch.empty(nwb, dtype=torch.uint8, device=dev)
+    nwb_min = 256 * ((Bl * H * DK * 4 + 255) // 256)  # the d_aug partial sums only
+
+    def call_b(nb):
+        rc = lib.gla_chunk_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), gla.GLA_BF16,
+                               gam.data_ptr(), a.data_ptr(), init.data_ptr(), dO.data_ptr(), None,
+                               dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), d_a.data_ptr(),
+                               dinit.data_ptr(), wsb.data_ptr(), nb, Bl, Tl, H, DK, DV,
+                               stream.cuda_stream)
+        if rc != 0:
+            raise RuntimeError(gla.status_string(rc))
+
+    def timed_b(nb, n):
+        call_b(nb)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(n):
+            call_b(nb)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n
+
+    bwd_ms = timed_b(nwb, 3)
+    bwd_ser_ms = timed_b(nwb_min, 2)
+    plan_b = gla.split_plan(Bl, Tl, H, True, torch.cuda.get_device_properties(dev).multi_processor_count)
     if gla.get_device_error() != 0:
         raise RuntimeError("device error")
     byts = Bl * Tl * H * FWD_BYTES_TH
@@ -674,7 +710,9 @@ def run_long_prefill(args):
     print(json.dumps(dict(part="long", workload=f"long prefill fwd B=2 T={Tl} H=16 bf16 in, fp32 out",
                           ms=seg_ms, tokens_per_s=Bl * Tl / (seg_ms * 1e-3),
                           gbs=byts / (seg_ms * 1e-3) / 1e9, frac_hbm=byts / (seg_ms * 1e-3) / 1e9 / pk["hbm"],
-                          peak_source=pk["src"], workspace_bytes=nws, serial_ms=ser_ms)), flush=True)
+                          peak_source=pk["src"], workspace_bytes=nws, serial_ms=ser_ms,
+                          plan_fwd=plan_f, bwd_ms=bwd_ms, bwd_serial_ms=bwd_ser_ms,
+                          bwd_tokens_per_s=Bl * Tl / (bwd_ms * 1e-3), plan_bwd=plan_b)), flush=True)
     return 0
 
 

@@ -97,6 +97,10 @@ def load(path: str | None = None):
             lib.gla_conv_decode_step.argtypes = [_P] * 5 + [_L, _I, _P]
             lib.gla_conv_decode_step.restype = _I
             lib.gla_decode_step.restype = _I
+            lib.gla_chunk_split_plan.argtypes = [_I] * 5 + [_P, _P]
+            lib.gla_chunk_split_plan.restype = _I
+            lib.gla_set_split_parts.argtypes = [_I]
+            lib.gla_set_split_parts.restype = _I
             if path is not None:
                 return lib
             _lib = lib
@@ -438,3 +442,16 @@ def wait_probe(stream=None) -> None:
 
 def set_wait_timeout_ns(ns: int) -> None:
     _check("gla_set_wait_timeout_ns", load().gla_set_wait_timeout_ns(int(ns)))
+
+
+def split_plan(B: int, T: int, H: int, backward: bool, n_sm: int) -> tuple[int, int]:
+    """(whole_pairs, parts) of gla_chunk_split_plan: pairs whole_pairs.. are cut into parts."""
+    w, p = ctypes.c_int(), ctypes.c_int()
+    _check("gla_chunk_split_plan", load().gla_chunk_split_plan(
+        int(B), int(T), int(H), int(bool(backward)), int(n_sm), ctypes.byref(w), ctypes.byref(p)))
+    return w.value, p.value
+
+
+def set_split_parts(parts: int) -> None:
+    """gla_set_split_parts: 0 automatic, 1 never cut, p >= 2 cut into p parts."""
+    _check("gla_set_split_parts", load().gla_set_split_parts(int(parts)))

@@ -13,6 +13,7 @@ namespace {
 
 __device__ int g_device_error = 0;
 std::atomic<unsigned long long> g_wait_ns{2000000000ull};
+std::atomic<int> g_split_parts{0};  // gla_set_split_parts: 0 automatic, 1 never, p >= 2 forced
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
@@ -53,10 +54,34 @@ int sm_count() {
   return n;
 }
 
-// Bytes the forward must have (fp16 copies of fp32 inputs) and the segment-parallel path's
-// share on top, at the offset round256(must).
+// Bytes the forward must have (fp16 copies of fp32 inputs); the cut pairs' states go on top,
+// at the offset round256(must).
 size_t fwd_min_workspace(int B, int T, int H, gla_dtype in_dtype) {
   return in_dtype == GLA_FP32 ? half_copy_bytes(B, T, H, false) : 0;
+}
+
+constexpr size_t kStateBytes = (size_t)gla::kDK * gla::kDV * sizeof(float);
+
+// Bytes the backward must have: d_aug partial sums, then fp16 copies of fp32 inputs.
+size_t bwd_min_workspace(int B, int T, int H, gla_dtype in_dtype) {
+  size_t s = gla::chunk_bwd_workspace_bytes(B, T, H);
+  if (in_dtype == GLA_FP32) s += half_copy_bytes(B, T, H, true);
+  return s;
+}
+
+// How the last wave's pairs are cut on the current device (roles: 1 forward, 3 backward).
+gla::SplitPlan split_plan(int B, int T, int H, int roles, int n_sm) {
+  const int nc = (T + gla::kChunk - 1) / gla::kChunk;
+  return gla::plan_split((long long)B * H, nc, roles, n_sm, g_split_parts.load());
+}
+
+// Extra workspace of a plan: the forward's part states; the backward's part states, part
+// adjoints and d_aug partial sums (three 256-byte aligned arrays).
+size_t split_bytes(int B, int H, const gla::SplitPlan& plan, bool bwd) {
+  const long long slots = gla::split_slots((long long)B * H, plan);
+  if (!slots) return 0;
+  if (!bwd) return round256((size_t)slots * kStateBytes);
+  return 2 * round256((size_t)slots * kStateBytes) + round256((size_t)slots * gla::kDK * 4);
 }
 
 
@@ -76,11 +101,14 @@ gla_status chunk_fwd_impl(const void* q, const void* k, const void* v, gla_dtype
   const size_t must = fwd_min_workspace(B, T, H, in_dtype);
   if (must && (!workspace || workspace_bytes < must)) return GLA_ERR_WORKSPACE;
   if (must && !aligned256(workspace)) return GLA_ERR_ALIGNMENT;
-  // few long sequences: segment-parallel when the workspace has room for it
-  int G = gla::fwd_segments(B, T, H, sm_count());
-  if (G > 1 && !(workspace && aligned256(workspace) &&
-                 workspace_bytes >= round256(must) + gla::fwd_segment_workspace_bytes(B, H, G)))
-    G = 1;
+  // the pairs of a partial last wave (or all of few, long sequences) are cut into parts when
+  // the workspace has room for their starting states
+  gla::SplitPlan plan = split_plan(B, T, H, 1, sm_count());
+  const size_t extra = split_bytes(B, H, plan, false);
+  if (extra && !(workspace && aligned256(workspace) && workspace_bytes >= round256(must) + extra)) {
+    plan.whole = B * H;
+    plan.parts = 1;
+  }
   gla::DevCtl ctl;
   if ((st = ctl_for_current_device(&ctl)) != GLA_OK) return st;
 
@@ -100,11 +128,16 @@ gla_status chunk_fwd_impl(const void* q, const void* k, const void* v, gla_dtype
       return GLA_ERR_CUDA;
     a.q = hq; a.k = hk; a.v = hv; a.bf16 = false;
   }
-  const cudaError_t e =
-      G > 1 ? gla::launch_chunk_fwd_segmented(a, G, static_cast<uint8_t*>(workspace) + round256(must),
-                                              ctl, stream)
-            : gla::launch_chunk_fwd(a, ctl, stream);
-  return e == cudaSuccess ? GLA_OK : GLA_ERR_CUDA;
+  a.plan = plan;
+  if (plan.parts > 1) {
+    float* states = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + round256(must));
+    a.seg_init = states;
+    if (gla::launch_segment_states(nullptr, a.k, a.v, nullptr, a.bf16, log_decay, init_state,
+                                   nullptr, sp, states, nullptr, B, T, H, plan, ctl,
+                                   stream) != cudaSuccess)
+      return GLA_ERR_CUDA;
+  }
+  return gla::launch_chunk_fwd(a, ctl, stream) == cudaSuccess ? GLA_OK : GLA_ERR_CUDA;
 }
 
 
@@ -186,8 +219,8 @@ gla_status gla_decay_schedule(int H, double t_min, double t_max, float* log_deca
 size_t gla_chunk_fwd_workspace_size(int B, int T, int H, int dk, int dv, gla_dtype in_dtype) {
   if (check_chunk_sizes(B, T, H, dk, dv, in_dtype) != GLA_OK) return 0;
   const size_t must = fwd_min_workspace(B, T, H, in_dtype);
-  const int G = gla::fwd_segments(B, T, H, sm_count());
-  return G > 1 ? round256(must) + gla::fwd_segment_workspace_bytes(B, H, G) : must;
+  const size_t extra = split_bytes(B, H, split_plan(B, T, H, 1, sm_count()), false);
+  return extra ? round256(must) + extra : must;
 }
 
 gla_status gla_chunk_fwd(const void* q, const void* k, const void* v, gla_dtype in_dtype,
@@ -245,9 +278,26 @@ gla_status gla_chunk_fwd_paged(const void* q, const void* k, const void* v, gla_
 
 size_t gla_chunk_bwd_workspace_size(int B, int T, int H, int dk, int dv, gla_dtype in_dtype) {
   if (check_chunk_sizes(B, T, H, dk, dv, in_dtype) != GLA_OK) return 0;
-  size_t s = gla::chunk_bwd_workspace_bytes(B, T, H);
-  if (in_dtype == GLA_FP32) s += half_copy_bytes(B, T, H, true);
-  return s;
+  const size_t must = bwd_min_workspace(B, T, H, in_dtype);
+  const size_t extra = split_bytes(B, H, split_plan(B, T, H, 3, sm_count()), true);
+  return extra ? round256(must) + extra : must;
+}
+
+gla_status gla_set_split_parts(int parts) {
+  if (parts < 0) return GLA_ERR_INVALID_ARG;
+  g_split_parts.store(parts);
+  return GLA_OK;
+}
+
+gla_status gla_chunk_split_plan(int B, int T, int H, int backward, int n_sm, int* whole_pairs,
+                                int* parts) {
+  if (B <= 0 || T <= 0 || H <= 0 || n_sm <= 0 || !whole_pairs || !parts)
+    return GLA_ERR_INVALID_ARG;
+  if ((long long)B * H > (1ll << 31) - 1) return GLA_ERR_UNSUPPORTED;
+  const gla::SplitPlan plan = split_plan(B, T, H, backward ? 3 : 1, n_sm);
+  *whole_pairs = plan.whole;
+  *parts = plan.parts;
+  return GLA_OK;
 }
 
 gla_status gla_chunk_bwd(const void* q, const void* k, const void* v, gla_dtype in_dtype,
@@ -265,9 +315,17 @@ gla_status gla_chunk_bwd(const void* q, const void* k, const void* v, gla_dtype 
       !aligned16(d_final_state) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
       !aligned16(d_aug) || !aligned16(d_init_state))
     return GLA_ERR_ALIGNMENT;
-  const size_t need = gla_chunk_bwd_workspace_size(B, T, H, dk_, dv_, in_dtype);
+  const size_t need = bwd_min_workspace(B, T, H, in_dtype);
   if (need && (!workspace || workspace_bytes < need)) return GLA_ERR_WORKSPACE;
   if (need && !aligned256(workspace)) return GLA_ERR_ALIGNMENT;
+  // the pairs of a partial last wave (or all of few, long sequences) are cut into parts when
+  // the workspace has room for their starting states and adjoints
+  gla::SplitPlan plan = split_plan(B, T, H, 3, sm_count());
+  const size_t extra = split_bytes(B, H, plan, true);
+  if (extra && workspace_bytes < round256(need) + extra) {
+    plan.whole = B * H;
+    plan.parts = 1;
+  }
   gla::DevCtl ctl;
   if ((st = ctl_for_current_device(&ctl)) != GLA_OK) return st;
 
@@ -290,6 +348,18 @@ gla_status gla_chunk_bwd(const void* q, const void* k, const void* v, gla_dtype 
         gla::launch_to_half((const float*)dO, hd, (long long)(tok * dv_), ctl, stream) != cudaSuccess)
       return GLA_ERR_CUDA;
     a.q = hq; a.k = hk; a.v = hv; a.dO = hd; a.bf16 = false;
+  }
+  a.plan = plan;
+  if (plan.parts > 1) {
+    const size_t slots = (size_t)gla::split_slots((long long)B * H, plan);
+    uint8_t* w = static_cast<uint8_t*>(workspace) + round256(need);
+    a.seg_state = reinterpret_cast<float*>(w);
+    a.seg_adj = reinterpret_cast<float*>(w + round256(slots * kStateBytes));
+    a.da_split = reinterpret_cast<float*>(w + 2 * round256(slots * kStateBytes));
+    if (gla::launch_segment_states(a.q, a.k, a.v, a.dO, a.bf16, log_decay, init_state,
+                                   d_final_state, gla::StatePages{}, a.seg_state, a.seg_adj, B, T,
+                                   H, plan, ctl, stream) != cudaSuccess)
+      return GLA_ERR_CUDA;
   }
   return gla::launch_chunk_bwd(a, ctl, stream) == cudaSuccess ? GLA_OK : GLA_ERR_CUDA;
 }

@@ -88,9 +88,13 @@ struct BwdParams {
   const float* aug;
   const float* init;
   const float* dfin;
-  float* da_part;  // [B*H, 96]
+  float* da_part;  // [B*H, 96]: d_aug partial sums of the whole pairs
   int T, H;
   bool want_dinit;
+  SplitPlan plan;
+  const float* seg_state;  // cut pairs: state entering each part (DQ's start)
+  const float* seg_adj;    // cut pairs: adjoint leaving each part (DV's and DK's start)
+  float* da_split;         // cut pairs: d_aug partial sums per part, [96] each
 };
 
 template <int ROLE>
@@ -98,10 +102,10 @@ __device__ __forceinline__ constexpr uint32_t tile_bytes() {
   return ROLE == R_DV ? 6 * Q_BOX + 3 * V_BOX : 6 * Q_BOX + 6 * V_BOX;
 }
 
-// Chunk handled at step t of the role's scan.
+// Chunk handled at step t of the role's scan over chunks [c0, c0 + n).
 template <int ROLE>
-__device__ __forceinline__ int chunk_at(int t, int nc) {
-  return ROLE == R_DQ ? t : nc - 1 - t;
+__device__ __forceinline__ int chunk_at(int t, int c0, int n) {
+  return ROLE == R_DQ ? c0 + t : c0 + n - 1 - t;
 }
 
 // 16-byte chunk `cc` of row `i` of a 16-bit tile: q/k tiles have 3 boxes of 32 channels
@@ -125,7 +129,8 @@ __device__ __forceinline__ void unpack8(const uint4& x, float (&f)[8]) {
 
 template <int ROLE, bool BF16>
 __device__ __forceinline__ void run_role(
-    uint8_t* base, const Cta& cta, int bh, const BwdParams& p, const CUtensorMap& map_q,
+    uint8_t* base, const Cta& cta, int bh, int c0, int n, int cut_idx, const BwdParams& p,
+    const CUtensorMap& map_q,
     const CUtensorMap& map_k, const CUtensorMap& map_v, const CUtensorMap& map_g,
     const CUtensorMap& map_out, const CUtensorMap& map_dinit, const DevCtl& ctl) {
   constexpr int NX = ROLE == R_DV ? 192 : 96;  // output columns
@@ -195,19 +200,19 @@ __device__ __forceinline__ void run_role(
         }
       };
       int armed = 0;
-      for (int t = 0; t < nc; ++t) {
+      for (int t = 0; t < n; ++t) {
         if (t >= 1 && !wait(cta, cta.bar(EMPTY), (t - 1) & 1, ctl)) break;
         mbar_arrive_expect_tx(cta.bar(FULL), tile_bytes<ROLE>());
-        load(chunk_at<ROLE>(t, nc), false);
+        load(chunk_at<ROLE>(t, c0, n), false);
         ++armed;
-        if (t + 1 < nc) load(chunk_at<ROLE>(t + 1, nc), true);
+        if (t + 1 < n) load(chunk_at<ROLE>(t + 1, c0, n), true);
       }
       if (armed) mbar_wait(cta.bar(FULL), (armed - 1) & 1, ctl, DRAIN_NS);
     }
   } else if (warp == MMA_WARP) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      for (int t = 0; t < nc; ++t) {
+      for (int t = 0; t < n; ++t) {
         const uint32_t par = t & 1;
         if (!wait(cta, cta.bar(FULL), par, ctl)) break;
         tc_fence_after();
@@ -334,7 +339,8 @@ __device__ __forceinline__ void run_role(
     // the decay applied to the state (adjoint) before step t's update is lambda^(tokens of
     // chunk_at(t)): lamL only for the last chunk, which is the first step of the reverse scans
     // and the last of the forward one
-    const float dec_first = (ROLE != R_DQ || nc == 1) ? lamL : lamC;  // step 0
+    const float dec_first =
+        (ROLE == R_DQ ? c0 == nc - 1 : c0 + n == nc) ? lamL : lamC;  // step 0
     uint8_t* const stage = base + OFF_STG + warp * 2048;  // this warp's output staging
     auto qk = [&](int cc) { return qk_chunk(i, 4 * sub + cc); };  // this part's q/k chunks
     auto vg = [&](int cc) { return vg_chunk(i, 8 * sub + cc); };  // this part's v/dO chunks
@@ -357,7 +363,14 @@ __device__ __forceinline__ void run_role(
             tmem_wait_ld();
           } else {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) r[j] = g_row ? __ldg(g_row + col + j) : 0.f;
+            for (int j4 = 0; j4 < 8; ++j4) {  // 8 loads in flight (rows are 16-byte aligned)
+              const float4 x = g_row ? __ldg(reinterpret_cast<const float4*>(g_row + col) + j4)
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+              r[4 * j4] = x.x;
+              r[4 * j4 + 1] = x.y;
+              r[4 * j4 + 2] = x.z;
+              r[4 * j4 + 3] = x.w;
+            }
           }
 #pragma unroll
           for (int q8 = 0; q8 < 4; ++q8) {
@@ -394,14 +407,23 @@ __device__ __forceinline__ void run_role(
       return m;
     };
 
-    // initial state (DQ) or adjoint of the final state (DV, DK): its exact max first
-    const float* src0 = ROLE == R_DQ ? p.init : p.dfin;
-    const float* g_row0 = (src0 && i < DK) ? src0 + ((size_t)bh * DK + i) * DV : nullptr;
+    // starting state (DQ) or adjoint (DV, DK): the caller's initial state / d_final_state for
+    // a whole pair, the segment passes' for a part of a cut one; its exact max first
+    const float* src0 = cut_idx >= 0 ? (ROLE == R_DQ ? p.seg_state : p.seg_adj)
+                                     : (ROLE == R_DQ ? p.init : p.dfin);
+    const long long slot0 = cut_idx >= 0 ? cut_idx : bh;
+    const float* g_row0 = (src0 && i < DK) ? src0 + ((size_t)slot0 * DK + i) * DV : nullptr;
     int e_cur = 0;
     {
       float m = 0.f;
-      if (g_row0)
-        for (int j = 64 * sub; j < 64 * sub + 64; ++j) m = fmaxf(m, fabsf(__ldg(g_row0 + j)));
+      if (g_row0) {
+        const float4* g4 = reinterpret_cast<const float4*>(g_row0 + 64 * sub);
+#pragma unroll
+        for (int j4 = 0; j4 < 16; ++j4) {
+          const float4 x = __ldg(g4 + j4);
+          m = fmaxf(m, fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w))));
+        }
+      }
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
       if (lane == 0) red[24 + warp] = m;
@@ -433,9 +455,9 @@ __device__ __forceinline__ void run_role(
       }
     };
 
-    for (int t = 0; t < nc && ok; ++t) {
+    for (int t = 0; t < n && ok; ++t) {
       const uint32_t par = t & 1;
-      const int c = chunk_at<ROLE>(t, nc);
+      const int c = chunk_at<ROLE>(t, c0, n);
       const float lk = c == nc - 1 ? lk_last : lk_full;
       if (!(ok = wait(cta, cta.bar(FULL), par, ctl))) break;
       // ---- gate partial sum z = q.(a*k) over this part's 32 channels, fused with the fp16
@@ -620,7 +642,7 @@ __device__ __forceinline__ void run_role(
       if (!(ok = wait(cta, cta.bar(S_DONE), par, ctl))) break;
       tc_fence_after();
       int e_next = e_cur;
-      if (t < nc - 1) {
+      if (t < n - 1) {
         // bound on the next state: all parts' operand maxima and max|S| of this step's copy
         // (decayed by this step's factor)
         if (!(ok = wait(cta, cta.bar(EP_CONV), par, ctl))) break;
@@ -630,10 +652,11 @@ __device__ __forceinline__ void run_role(
           bad = true;
           e_next = 0;
         }
-        publish_state(t + 1, e_next, (ROLE == R_DQ && t + 2 == nc) ? lamL : lamC, nullptr, true);
+        publish_state(t + 1, e_next, (ROLE == R_DQ && c0 + t + 2 == nc) ? lamL : lamC, nullptr,
+                      true);
       }
       // ---- adjoint of the initial state (DV, after the last step = chunk 0)
-      if (ROLE == R_DV && t == nc - 1 && p.want_dinit && q4 < 3) {
+      if (ROLE == R_DV && t == n - 1 && c0 == 0 && p.want_dinit && q4 < 3) {
         if (lane == 0) bulk_wait_read<0>();
         __syncwarp();
         emit_rows_tma1<4>(
@@ -659,7 +682,8 @@ __device__ __forceinline__ void run_role(
       float dd = 0.f;
 #pragma unroll
       for (int j = 0; j < 32; ++j) dd = (j == lane) ? __uint_as_float(r[j]) : dd;
-      p.da_part[(size_t)bh * DK + 32 * q4 + lane] = dd;
+      float* da = cut_idx >= 0 ? p.da_split + (size_t)cut_idx * DK : p.da_part + (size_t)bh * DK;
+      da[32 * q4 + lane] = dd;
     }
     if (lane == 0) bulk_wait_all();
     __syncwarp();
@@ -687,23 +711,45 @@ bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
   cta.sb = smem_u32(cta.base);
   cta.bar_off = OFF_BAR;
   cta.abort_off = OFF_ABORT;
-  const int role = blockIdx.x % 3, bh = blockIdx.x / 3;
+  // three roles per pair; the whole pairs first, then the parts of the cut ones
+  const int nc = (p.T + C - 1) / C;
+  const int role = blockIdx.x % 3, w = blockIdx.x / 3;
+  const bool cut = w >= p.plan.whole;
+  const int cut_idx = cut ? w - p.plan.whole : -1;
+  const int part = cut ? cut_idx % p.plan.parts : 0;
+  const int bh = cut ? p.plan.whole + cut_idx / p.plan.parts : w;
+  const int c0 = cut ? part_begin(part, nc, p.plan.parts) : 0;
+  const int n = cut ? part_begin(part + 1, nc, p.plan.parts) - c0 : nc;
   if (role == R_DQ)
-    run_role<R_DQ, BF16>(cta.base, cta, bh, p, map_q, map_k, map_v, map_g, map_dq, map_dinit, ctl);
+    run_role<R_DQ, BF16>(cta.base, cta, bh, c0, n, cut_idx, p, map_q, map_k, map_v, map_g, map_dq,
+                         map_dinit, ctl);
   else if (role == R_DV)
-    run_role<R_DV, BF16>(cta.base, cta, bh, p, map_q, map_k, map_v, map_g, map_dv, map_dinit, ctl);
+    run_role<R_DV, BF16>(cta.base, cta, bh, c0, n, cut_idx, p, map_q, map_k, map_v, map_g, map_dv,
+                         map_dinit, ctl);
   else
-    run_role<R_DK, BF16>(cta.base, cta, bh, p, map_q, map_k, map_v, map_g, map_dk, map_dinit, ctl);
+    run_role<R_DK, BF16>(cta.base, cta, bh, c0, n, cut_idx, p, map_q, map_k, map_v, map_g, map_dk,
+                         map_dinit, ctl);
 }
 
-// d_aug[h, d] = sum over b of the per-(b, h) partial sums, in order of b (deterministic).
-__global__ void reduce_daug_kernel(const float* __restrict__ part, float* __restrict__ d_aug,
-                                   int B, int H) {
+// d_aug[h, d] = sum over b of the per-(b, h) partial sums (a cut pair's: its parts' in order),
+// in order of b (deterministic).
+__global__ void reduce_daug_kernel(const float* __restrict__ part, const float* __restrict__ split,
+                                   float* __restrict__ d_aug, int B, int H, SplitPlan plan) {
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= H * DK) return;
   const int h = idx / DK, d = idx % DK;
   float s = 0.f;
-  for (int b = 0; b < B; ++b) s += part[((size_t)b * H + h) * DK + d];
+  for (int b = 0; b < B; ++b) {
+    const int bh = b * H + h;
+    if (bh < plan.whole) {
+      s += part[(size_t)bh * DK + d];
+    } else {
+      float t = 0.f;
+      for (int j = 0; j < plan.parts; ++j)
+        t += split[((size_t)(bh - plan.whole) * plan.parts + j) * DK + d];
+      s += t;
+    }
+  }
   d_aug[idx] = s;
 }
 
@@ -735,13 +781,24 @@ cudaError_t launch_chunk_bwd(const BwdArgs& a, DevCtl ctl, cudaStream_t stream) 
   p.T = a.T;
   p.H = a.H;
   p.want_dinit = a.dinit != nullptr;
+  p.plan = a.plan;
+  if (p.plan.parts <= 1 || !a.seg_state || !a.seg_adj || !a.da_split) {
+    p.plan.whole = a.B * a.H;
+    p.plan.parts = 1;
+  }
+  p.seg_state = a.seg_state;
+  p.seg_adj = a.seg_adj;
+  p.da_split = a.da_split;
   auto kern = a.bf16 ? bwd_kernel<true> : bwd_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  kern<<<3 * a.B * a.H, THREADS, SMEM_BYTES, stream>>>(mq, mk, mv, mg, mdq, mdk, mdv, mdi, p, ctl);
+  const long long grid =
+      3 * (p.plan.whole + ((long long)a.B * a.H - p.plan.whole) * p.plan.parts);
+  kern<<<(unsigned)grid, THREADS, SMEM_BYTES, stream>>>(mq, mk, mv, mg, mdq, mdk, mdv, mdi, p, ctl);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const int n = a.H * DK;
-  reduce_daug_kernel<<<(n + 255) / 256, 256, 0, stream>>>(p.da_part, a.d_aug, a.B, a.H);
+  reduce_daug_kernel<<<(n + 255) / 256, 256, 0, stream>>>(p.da_part, p.da_split, a.d_aug, a.B, a.H,
+                                                         p.plan);
   return cudaGetLastError();
 }
 

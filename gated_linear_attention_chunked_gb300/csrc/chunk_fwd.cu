@@ -97,7 +97,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
            const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o,
            const __grid_constant__ CUtensorMap map_fin, const float* __restrict__ log_decay,
            const float* __restrict__ aug, const float* __restrict__ init, float* __restrict__ out,
-           float* __restrict__ fin, int T, int H, int seg, StatePages sp,
+           float* __restrict__ fin, int T, int H, SplitPlan plan,
+           const float* __restrict__ seg_init, StatePages sp,
            const __grid_constant__ CUtensorMap map_y, OutGate og, DevCtl ctl) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   Cta cta;
@@ -111,9 +112,15 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
   cta.abort_off = OFF_ABORT;
   uint8_t* const base = cta.base;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int bh = blockIdx.x, b = bh / H, h = bh % H;
-  // chunks of this sequence; the last one holds L_last = 1..C tokens (rows past T are zeros)
+  // chunks of a sequence; the last one holds L_last = 1..C tokens (rows past T are zeros)
   const int nc = (T + C - 1) / C, L_last = T - (nc - 1) * C;
+  // this CTA's pair and chunk range [c0, c0 + n): a whole pair, or part `part` of a cut one
+  const bool cut = (int)blockIdx.x >= plan.whole;
+  const int cut_idx = cut ? (int)blockIdx.x - plan.whole : 0;
+  const int part = cut_idx % plan.parts;
+  const int bh = cut ? plan.whole + cut_idx / plan.parts : (int)blockIdx.x, b = bh / H, h = bh % H;
+  const int c0 = cut ? part_begin(part, nc, plan.parts) : 0;
+  const int n = cut ? part_begin(part + 1, nc, plan.parts) - c0 : nc;
   const float gamma = __ldg(log_decay + h);
   float* pw = (float*)(base + OFF_PW);
   float* red = (float*)(base + OFF_RED);
@@ -161,9 +168,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
       prefetch_tensormap(&map_v);
       prefetch_tensormap(&map_o);
       int armed_qk[2] = {0, 0}, armed_v[2] = {0, 0};
-      for (int c = 0; c < nc; ++c) {
+      for (int c = 0; c < n; ++c) {  // c: step of this CTA, chunk c0 + c
         const uint32_t s = c & 1, st = cta.sb + s * STAGE;
-        const int t0 = c * C;
+        const int t0 = (c0 + c) * C;
         if (c >= 2 && !wait(cta, cta.bar(V_EMPTY + s), ((c >> 1) - 1) & 1, ctl)) break;
         mbar_arrive_expect_tx(cta.bar(V_FULL + s), V_BYTES);
         for (int j = 0; j < 3; ++j)
@@ -190,7 +197,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
       constexpr uint32_t ID_QS = idesc_f16(128, 192, false, false, false, true);
       constexpr uint32_t ID_PV = idesc_f16(128, 192, false, false, false, true);
       constexpr uint32_t ID_KV = idesc_f16(128, 192, false, false, true, true);
-      for (int c = 0; c < nc; ++c) {
+      for (int c = 0; c < n; ++c) {
         const uint32_t s = c & 1, st = cta.sb + s * STAGE;
         const uint32_t slot = cta.sb + (s ^ 1) * STAGE;  // state copy for this chunk
         if (!wait(cta, cta.bar(QK_FULL + s), (c >> 1) & 1, ctl)) break;
@@ -247,9 +254,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
     // in the last chunk (L_last tokens): lambda^(L_last-1-i), and 0 on the zero rows past T
     const float lk_last = i < L_last ? pw[L_last - 1 - i] : 0.f;
     float range_max = 0.f;
-    for (int c = 0; c < nc; ++c) {
+    for (int c = 0; c < n; ++c) {
       const uint32_t s = c & 1, par = c & 1;
-      const float lk = c == nc - 1 ? lk_last : lk_full;
+      const float lk = c0 + c == nc - 1 ? lk_last : lk_full;
       uint8_t* stg = base + s * STAGE;
       float vmax = 0.f, kmax = 0.f, qmax = 0.f;
       if (!wait(cta, cta.bar(V_FULL + s), (c >> 1) & 1, ctl)) break;
@@ -387,7 +394,14 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
             tmem_wait_ld();
           } else {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) r[j] = g_row ? __ldg(g_row + col + j) : 0.f;
+            for (int j4 = 0; j4 < 8; ++j4) {  // 8 loads in flight (rows are 16-byte aligned)
+              const float4 x = g_row ? __ldg(reinterpret_cast<const float4*>(g_row + col) + j4)
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+              r[4 * j4] = x.x;
+              r[4 * j4 + 1] = x.y;
+              r[4 * j4 + 2] = x.z;
+              r[4 * j4 + 3] = x.w;
+            }
           }
 #pragma unroll
           for (int q8 = 0; q8 < 4; ++q8) {
@@ -424,26 +438,37 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
       return m;
     };
 
-    // slot of this sequence's initial/final state: [b / seg][h] of the caller's arrays, or
-    // its page of a state pool
-    const int breal = b / seg;
-    long long zst = (long long)breal * H + h;
+    // slot of this sequence's initial/final state: [b][h] of the caller's arrays, or its page
+    // of a state pool
+    long long zst = (long long)b * H + h;
     bool page_ok = true;
     if (sp.page) {
-      const int pg = __ldg(sp.page + breal);
+      const int pg = __ldg(sp.page + b);
       page_ok = pg >= 0 && pg < sp.n_pages;
       zst = ((long long)pg * sp.pool_layers + sp.layer) * H + h;
-      if (!page_ok && tid == 128) record_error(ctl, DEV_RANGE);
+      if (!page_ok && tid == 128 && (!cut || part == plan.parts - 1)) record_error(ctl, DEV_RANGE);
     }
     const long long zinit = sp.init_paged ? zst : bh;
-    // initial state: its exponent needs its exact max first (one exchange in the group)
+    // starting state: the caller's (whole pair) or the one the segment passes left for this
+    // part; its exponent needs its exact max first (one exchange in the group)
     const float* g_row0 =
-        (init && page_ok && i < DK) ? init + ((size_t)zinit * DK + i) * DV : nullptr;
+        i >= DK ? nullptr
+        : cut   ? seg_init + ((size_t)cut_idx * DK + i) * DV
+        : (init && page_ok) ? init + ((size_t)zinit * DK + i) * DV
+                            : nullptr;
+    // the final state is this CTA's to write if it ends the sequence
+    const bool ends_seq = !cut || part == plan.parts - 1;
     int e_cur = 0;
     {
       float m = 0.f;
-      if (g_row0)
-        for (int j = 96 * hf; j < 96 * hf + 96; ++j) m = fmaxf(m, fabsf(__ldg(g_row0 + j)));
+      if (g_row0) {
+        const float4* g4 = reinterpret_cast<const float4*>(g_row0 + 96 * hf);
+#pragma unroll
+        for (int j4 = 0; j4 < 24; ++j4) {
+          const float4 x = __ldg(g4 + j4);
+          m = fmaxf(m, fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w))));
+        }
+      }
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
       if (lane == 0) red[16 + ew] = m;
@@ -456,10 +481,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
         bad = true;
         e_cur = 0;
       }
-      publish_state(1 * STAGE + OFF_Q, 0, e_cur, nc == 1 ? lamL : lamC, g_row0, false);
+      publish_state(1 * STAGE + OFF_Q, 0, e_cur, c0 == nc - 1 ? lamL : lamC, g_row0, false);
     }
 
-    for (int c = 0; c < nc && ok; ++c) {
+    for (int c = 0; c < n && ok; ++c) {
       const uint32_t s = c & 1, par = c & 1;
       if (!(ok = wait(cta, cta.bar(O_DONE), par, ctl))) break;
       if (!(ok = wait(cta, cta.bar(S_DONE), par, ctl))) break;
@@ -469,7 +494,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
       // from a bound, |S_{c+1}| <= lambda^C max|S_c| + 128 max|K'_c| max|V_c|, so the copy
       // needs a single pass over the state.
       int e_next = e_cur;
-      if (c < nc - 1) {
+      if (c < n - 1) {
         // every emit thread has stored its part of max|S_c| (EP_S phase c is complete)
         if (!(ok = wait(cta, cta.bar(EP_S), par, ctl))) break;
         const float ms = red_max(par);
@@ -482,14 +507,15 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
           bad = true;
           e_next = 0;
         }
-        publish_state(s * STAGE + OFF_Q, c + 1, e_next, c + 2 == nc ? lamL : lamC, nullptr, true);
+        publish_state(s * STAGE + OFF_Q, c + 1, e_next, c0 + c + 2 == nc ? lamL : lamC, nullptr,
+                      true);
       }
       // ---- output rows: o = 2^e D_O for columns [96hf, 96hf+96) (the self-augmentation
       // sigmoid(z) v is already in D_O through the diagonal of P''), TMA-stored
       uint8_t* const stage_o = base + OFF_STG + ew * 4096;
       if constexpr (!GATED) {
         const float osc = pow2i(e_cur);
-        const int t0 = c * C + 32 * q4;  // first token of this warp's rows (boxes past T: none)
+        const int t0 = (c0 + c) * C + 32 * q4;  // first token of this warp's rows (none past T)
         emit_rows_tma<6>(
             stage_o, lane,
             [&](int k, float (&o)[16]) {
@@ -507,9 +533,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
         // pass 1 sums o^2 over this warp's 96 columns (writing o too if asked), the two warps
         // of the row quadrant exchange their sums, pass 2 writes y
         const float osc = pow2i(e_cur);
-        const int t0 = c * C + 32 * q4;  // first token of this warp's rows (boxes past T: none)
-        const bool live = c * C + i < T;  // this thread's row is a token of the sequence
-        const long long tok = (long long)b * T + c * C + i;  // token row of this thread
+        const int t0 = (c0 + c) * C + 32 * q4;  // first token of this warp's rows (none past T)
+        const bool live = (c0 + c) * C + i < T;  // this thread's row is a token of the sequence
+        const long long tok = (long long)b * T + (c0 + c) * C + i;  // token row of this thread
         float* xch = (float*)(base + OFF_XCH);
         float ss = 0.f;
         if (og.want_o) {
@@ -577,8 +603,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
       tc_fence_before();
       mbar_arrive(cta.bar(EP_O));
       // ---- final state (after the last chunk), staged through the same rows
-      // (with seg > 1 the CTAs are segments of longer sequences: only the last one's counts)
-      if (c == nc - 1 && fin && q4 < 3 && b % seg == seg - 1 && page_ok) {
+      // (only the CTA that ends the sequence: a whole pair or the last part of a cut one)
+      if (c == n - 1 && fin && q4 < 3 && ends_seq && page_ok) {
         if (lane == 0) bulk_wait_read<0>();
         __syncwarp();
         emit_rows_tma<6>(
@@ -623,15 +649,22 @@ cudaError_t launch_chunk_fwd(const FwdArgs& a, DevCtl ctl, cudaStream_t stream) 
       !make_tmap_seq_out_f32(&my, a.og.y ? a.og.y : o_any, DV, a.H, a.T, a.B) ||
       !make_tmap_state_f32(&mfin, a.fin ? (const void*)a.fin : (const void*)o_any,
                            a.sp.page ? (long long)a.sp.n_pages * a.sp.pool_layers * a.H
-                                     : (long long)(a.B / a.seg) * a.H))
+                                     : (long long)a.B * a.H))
     return cudaErrorInvalidValue;
   const bool gated = a.og.g != nullptr;
   auto kern = gated ? (a.bf16 ? fwd_kernel<true, true> : fwd_kernel<false, true>)
                     : (a.bf16 ? fwd_kernel<true, false> : fwd_kernel<false, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  kern<<<a.B * a.H, THREADS, SMEM_BYTES, stream>>>(mq, mk, mv, mo, mfin, a.log_decay, a.aug, a.init, a.o,
-                                                   a.fin, a.T, a.H, a.seg, a.sp, my, a.og, ctl);
+  SplitPlan plan = a.plan;
+  if (plan.parts <= 1 || !a.seg_init) {
+    plan.whole = a.B * a.H;
+    plan.parts = 1;
+  }
+  const long long grid = plan.whole + ((long long)a.B * a.H - plan.whole) * plan.parts;
+  kern<<<(unsigned)grid, THREADS, SMEM_BYTES, stream>>>(mq, mk, mv, mo, mfin, a.log_decay, a.aug,
+                                                        a.init, a.o, a.fin, a.T, a.H, plan,
+                                                        a.seg_init, a.sp, my, a.og, ctl);
   return cudaGetLastError();
 }
 

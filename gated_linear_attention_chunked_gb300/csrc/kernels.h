@@ -47,6 +47,20 @@ struct OutGate {
   bool want_o = false;          // also write o
 };
 
+// How the (b, h) pairs of a chunked call are laid out over CTAs.  Pairs 0 .. whole-1 run whole
+// (one CTA per pair, or per pair and role in the backward, over all nc chunks); the last
+// BH - whole pairs -- the partial last wave -- are cut into `parts` consecutive chunk ranges,
+// part j covering chunks [j*nc/parts, (j+1)*nc/parts), each its own CTA that starts from the
+// state (forward) or adjoint (reverse) at its boundary, computed beforehand by the segment
+// passes (seg_scan.cu).  parts == 1: no pair is cut.
+struct SplitPlan {
+  int whole = 0;
+  int parts = 1;
+};
+__host__ __device__ inline int part_begin(int j, int nc, int parts) {
+  return (int)(((long long)j * nc) / parts);
+}
+
 struct FwdArgs {
   const void* q;  // [B,T,H,96] 16-bit
   const void* k;
@@ -56,11 +70,12 @@ struct FwdArgs {
   const float* aug;        // [H,96]
   const float* init;       // [B,H,96,192] or null
   float* o;                // [B,T,H,192]
-  float* fin;              // [B/seg,H,96,192] or null
+  float* fin;              // [B,H,96,192] or null
   int B, T, H;
-  // seg > 1: the B "sequences" are seg consecutive segments of each of B/seg longer ones;
-  // only the last segment of each writes its final state, to fin[b / seg].
-  int seg = 1;
+  SplitPlan plan;          // plan.whole = B*H unless some pairs are cut
+  // cut pairs: [(BH - whole) * parts][96][192], slot x*parts + j = the state entering part j
+  // of cut pair x (filled by the segment passes; slot x*parts is the pair's initial state)
+  const float* seg_init = nullptr;
   StatePages sp;  // with sp.page: init and fin are the pool (see StatePages)
   OutGate og;     // with og.g: the fused output epilogue (o written only if og.want_o)
 };
@@ -82,18 +97,35 @@ struct BwdArgs {
   float* dv;
   float* d_aug;
   float* dinit;
-  void* workspace;
+  void* workspace;          // d_aug partial sums of the whole pairs: [B*H][96] fp32
   size_t workspace_bytes;
   int B, T, H;
+  SplitPlan plan;           // plan.whole = B*H unless some pairs are cut
+  // cut pairs (x = pair - whole, slot x*parts + j for part j):
+  float* seg_state = nullptr;  // the state entering part j (the DQ role's start)
+  float* seg_adj = nullptr;    // the adjoint of the state leaving part j (DV, DK roles' start)
+  float* da_split = nullptr;   // d_aug partial sums of the parts, [96] each
 };
 size_t chunk_bwd_workspace_bytes(int B, int T, int H);
 
-// Segment-parallel forward for few, long sequences: the number of segments G (1 = not
-// worth it) for this shape on a device with n_sm SMs, the workspace it needs, and the call.
-int fwd_segments(int B, int T, int H, int n_sm);
-size_t fwd_segment_workspace_bytes(int B, int H, int G);
-cudaError_t launch_chunk_fwd_segmented(const FwdArgs& a, int G, void* workspace, DevCtl ctl,
-                                       cudaStream_t stream);
+// ---- splitting the last wave (seg_scan.cu)
+// The plan for B*H pairs of nc chunks with `roles` CTAs per pair (1 forward, 3 backward) on
+// n_sm SMs: cut the pairs of the partial last wave (all pairs if they do not fill the SMs)
+// into the number of parts that minimises the estimated time, passes included.  force_parts:
+// 0 chooses, 1 never cuts, p >= 2 cuts the last wave's pairs into min(p, nc) parts.
+SplitPlan plan_split(long long BH, int nc, int roles, int n_sm, int force_parts);
+// States the cut pairs need (each 96 x 192 fp32): (BH - whole) * parts.
+long long split_slots(long long BH, const SplitPlan& p);
+// The segment passes: U sums over the parts (forward direction for the states entering parts
+// 1.., reverse direction for the adjoints leaving parts ..p-2), then their recurrences, which
+// also place the initial state (init / pool page / zero) and the final-state adjoint (dfin /
+// zero) in the first and last slots.  states (adj) null: that direction is not computed.
+// q_or_null, dO_or_null are needed for the reverse direction only.
+cudaError_t launch_segment_states(const void* q, const void* k, const void* v, const void* dO,
+                                  bool bf16, const float* log_decay, const float* init,
+                                  const float* dfin, const StatePages& sp, float* states,
+                                  float* adj, int B, int T, int H, const SplitPlan& plan,
+                                  DevCtl ctl, cudaStream_t stream);
 
 // The device error word and wait limit of the current device (defined in api.cu).
 cudaError_t current_device_ctl(DevCtl* ctl);

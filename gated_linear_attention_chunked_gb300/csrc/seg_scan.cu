@@ -1,27 +1,33 @@
-// seg_scan.cu -- segment-parallel chunked forward for few, long sequences.
+// seg_scan.cu -- cutting (b, h) pairs into chunk ranges that run as separate CTAs.
 //
-// Method: the chunked forward ("Beyond the KV cache ... Laplace 3B ...", section "Challenge 1")
-// carries the state from chunk to chunk, so each (b, h) is a serial chain of T/128 steps and a
-// call with few (b, h) pairs -- long-context prefill -- leaves most SMs idle.  The state
-// recurrence S_t = lambda S_{t-1} + k_t v_t^T (section "i14 and the Laplace 3B architecture",
-// "GLA mixer") is linear, so for a sequence cut into G segments of L tokens, segment g ending
-// at token e_g,
+// Method: the chunked forward and backward ("Beyond the KV cache ... Laplace 3B ...", sections
+// "Challenge 1" and "Challenge 3") carry a state (forward) or its adjoint (backward) from chunk
+// to chunk, so each (b, h) is a serial chain of ceil(T/128) steps.  When the pairs do not fill
+// the last wave of SMs -- or there are fewer pairs than SMs, as in long-context prefill -- the
+// chains of the pairs in that wave are cut into parts.  The recurrence S_t = lambda S_{t-1} +
+// k_t v_t^T (section "i14 and the Laplace 3B architecture", "GLA mixer") is linear, and so is
+// its adjoint dS_{t-1} = lambda dS_t + q_t dO_t^T, so for a part j of L_j tokens, s_j its first
+// token and e_j its last,
 //
-//     S_{e_g} = lambda^L S_{e_{g-1}} + U_g,     U_g = sum_{t in g} lambda^(e_g - t) k_t v_t^T.
+//     S entering part j+1  = lambda^(L_j) S entering part j + U_j,
+//                            U_j  = sum_{t in j} lambda^(e_j - t) k_t v_t^T
+//     dS leaving part j-1  = lambda^(L_j) dS leaving part j + U'_j,
+//                            U'_j = sum_{t in j} lambda^(t - s_j + 1) q_t dO_t^T.
 //
-//   pass A  (seg_state_kernel, one CTA per (b, h, g) for every segment but the last): U_g on
-//           the tensor cores, K''^T V over the segment's chunks into one fp32 TMEM accumulator,
-//           the decay folded into the fp16 copy of k (row t scaled by lambda^(e_g - t));
-//   pass B  (seg_combine_kernel): the G-step recurrence above per (b, h), giving every
-//           segment's initial state (segment 0: the caller's, or zero);
-//   pass C  the ordinary chunked forward over the B*G segments as independent sequences --
-//           [B][T][H][d] is the same memory as [B*G][T/G][H][d] -- with only the last segment
-//           of each sequence writing the final state.
+//   pass A  (seg_sum_kernel, one CTA per cut pair and part): U_j (parts 0..p-2) or U'_j
+//           (parts 1..p-1) on the tensor cores, the pair's K''^T V or Q''^T dO over the part's
+//           chunks into one fp32 TMEM accumulator, the decay folded into the fp16 copy of k (q);
+//   pass B  (seg_link_kernel): the recurrences above per cut pair, giving every part its
+//           starting state (the caller's initial state, a pool page or zero for part 0) and
+//           its starting adjoint (d_final_state or zero for the last part);
+//   then    the chunked kernel runs the whole pairs and every part as its own CTA.
 //
-// Extra traffic: pass A reads k and v of all but the last segment (576 B per token-head).
+// Extra traffic: pass A reads k, v (q, dO) of all parts but the last (first).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
+
+#include <map>
 
 #include "kernels.h"
 #include "scan_common.cuh"
@@ -54,7 +60,6 @@ enum Bar : uint32_t {
 
 constexpr int THREADS = 192;  // warps 0..3 convert + epilogue (row = token = TMEM lane)
 constexpr int PRODUCER_WARP = 4, MMA_WARP = 5;
-constexpr int MIN_SEGMENT_CHUNKS = 16;  // shorter segments do not repay the extra pass
 
 // 16-byte chunk `cc` of row `i`: k has 3 boxes of 32 channels (64-byte rows), v 3 boxes of 64
 // channels (128-byte rows), v after k within a stage.
@@ -65,13 +70,15 @@ __device__ __forceinline__ uint32_t v_chunk(uint32_t i, int cc) {
   return 3 * K_BOX + (cc >> 3) * V_BOX + swz_off(i, cc & 7, 128);
 }
 
-// Pass A.  CTA (b, h, g) writes U_g to u_out[b*G + g + 1][h] (the slot of the initial state of
-// segment g + 1, which pass B then turns into that state in place).
+// Pass A.  CTA i < n_fwd: forward sum U_j of part j = i % (p-1) of cut pair x = i / (p-1),
+// into states[x*p + j + 1]; CTA i >= n_fwd: reverse sum U'_j of part j = 1 + i' % (p-1) (i' =
+// i - n_fwd), into adj[x*p + j - 1].  Those slots are then completed by pass B in place.
 template <bool BF16>
 __global__ void __launch_bounds__(THREADS, 1)
-seg_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
-                 const float* __restrict__ log_decay, float* __restrict__ u_out, int T, int H, int G,
-                 DevCtl ctl) {
+seg_sum_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
+               const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_g,
+               const float* __restrict__ log_decay, float* __restrict__ states,
+               float* __restrict__ adj, int T, int H, int whole, int parts, int n_fwd, DevCtl ctl) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   Cta cta;
   cta.base = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -84,9 +91,15 @@ seg_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constan
   cta.abort_off = OFF_ABORT;
   uint8_t* const base = cta.base;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int g = blockIdx.x % (G - 1), bh = blockIdx.x / (G - 1), b = bh / H, h = bh % H;
-  const int M = T / C / G;                     // chunks per segment
-  const int row0 = b * T + g * M * C;          // first token row of the segment
+  const bool rev = (int)blockIdx.x >= n_fwd;
+  const int idx = rev ? (int)blockIdx.x - n_fwd : (int)blockIdx.x;
+  const int x = idx / (parts - 1), j = idx % (parts - 1) + (rev ? 1 : 0);
+  const int bh = whole + x, b = bh / H, h = bh % H;
+  const int nc = (T + C - 1) / C;
+  const int c_lo = part_begin(j, nc, parts), c_hi = part_begin(j + 1, nc, parts);
+  const int M = c_hi - c_lo;  // chunks of the part (>= 1)
+  const CUtensorMap* map_a = rev ? &map_q : &map_k;
+  const CUtensorMap* map_b = rev ? &map_g : &map_v;
   const float gamma = __ldg(log_decay + h);
   float* pw = (float*)(base + OFF_PW);
   uint32_t* tmem_slot = (uint32_t*)(base + OFF_TMEM);
@@ -119,11 +132,11 @@ seg_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constan
         const int s = m % STAGES;
         if (m >= STAGES && !wait(cta, cta.bar(EMPTY + s), (m / STAGES - 1) & 1, ctl)) break;
         mbar_arrive_expect_tx(cta.bar(FULL + s), STAGE);
-        const int row = row0 + m * C;
+        const int t0 = (c_lo + m) * C;
         const uint32_t st = sb + s * STAGE;
-        for (int j = 0; j < 3; ++j) {
-          tma_load_3d(st + j * K_BOX, &map_k, cta.bar(FULL + s), 32 * j, h, row);
-          tma_load_3d(st + 3 * K_BOX + j * V_BOX, &map_v, cta.bar(FULL + s), 64 * j, h, row);
+        for (int jb = 0; jb < 3; ++jb) {
+          tma_load_4d(st + jb * K_BOX, map_a, cta.bar(FULL + s), 32 * jb, h, t0, b);
+          tma_load_4d(st + 3 * K_BOX + jb * V_BOX, map_b, cta.bar(FULL + s), 64 * jb, h, t0, b);
         }
         armed0 += s == 0;
         armed1 += s == 1;
@@ -136,8 +149,8 @@ seg_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constan
     }
   } else if (warp == MMA_WARP) {
     if (lane == 0) {
-      // U (rows = 96 key channels + 32 padding rows never read) += K''^T V, K = 16 tokens per
-      // instruction: A = k tile as [token][channel] (MN-major), B = v tile as [token][channel]
+      // U (rows = 96 key channels + 32 padding rows never read) += A''^T B, K = 16 tokens per
+      // instruction: A = k (q) tile as [token][channel] (MN-major), B = v (dO) tile likewise
       constexpr uint32_t ID = idesc_f16(128, 192, false, false, true, true);
       for (int m = 0; m < M; ++m) {
         const int s = m % STAGES;
@@ -155,27 +168,32 @@ seg_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constan
       mbar_wait(cta.bar(DONE), 0, ctl, DRAIN_NS);
     }
   } else {
-    // ---- warps 0..3: in-place fp16 operands of chunk m, row i = token i of the chunk:
-    // k scaled by lambda^(e_g - t) for its token t, v as it is
+    // ---- warps 0..3: in-place fp16 operands of chunk m, row i = token i of the chunk: k
+    // scaled by lambda^(e_j - t) (forward) or q by lambda^(t - s_j + 1) (reverse), v / dO as
+    // they are.  Rows past T are zeros (the tensor map's fill).
     const int i = tid;
+    const float lamC = expf((float)C * gamma);
+    const float row_w = rev ? (i + 1 < C ? pw[i + 1] : lamC) : pw[C - 1 - i];
     float vmax = 0.f;
     bool ok = true;
     for (int m = 0; m < M && ok; ++m) {
       const int s = m % STAGES;
       if (!(ok = wait(cta, cta.bar(FULL + s), (m / STAGES) & 1, ctl))) break;
       uint8_t* st = base + s * STAGE;
-      const float sk = expf(gamma * (float)(C * (M - 1 - m))) * pw[C - 1 - i];
+      const int whole_chunks = rev ? m : M - 1 - m;  // chunks between this one and s_j (e_j)
+      const float sk = expf(gamma * (float)(C * whole_chunks)) * row_w;
       convert_row<BF16, 12>(st, [&](int cc) { return k_chunk(i, cc); }, sk, vmax);
       convert_row<BF16, 24>(st, [&](int cc) { return v_chunk(i, cc); }, 1.f, vmax);
       fence_proxy_async();
       mbar_arrive(cta.bar(CONV + s));
     }
-    // ---- U_g out: rows 0..95 (warps 0..2), 192 fp32 each
+    // ---- the sum out: rows 0..95 (warps 0..2), 192 fp32 each
     if (ok) ok = wait(cta, cta.bar(DONE), 0, ctl);
     ok = __all_sync(0xffffffffu, ok && *cta.abort_flag() == 0);
     if (ok && warp < 3) {
       tc_fence_after();
-      float* dst = u_out + ((size_t)(b * G + g + 1) * H + h) * DK * DV + (size_t)i * DV;
+      const long long slot = (long long)x * parts + (rev ? j - 1 : j + 1);
+      float* dst = (rev ? adj : states) + (size_t)slot * DK * DV + (size_t)i * DV;
       const uint32_t trow = tmem + ((uint32_t)(32 * warp) << 16);
 #pragma unroll 1
       for (int cb = 0; cb < DV / 32; ++cb) {
@@ -183,10 +201,10 @@ seg_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constan
         tmem_ld32(trow + 32 * cb, r);
         tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 32; j += 4)
-          *reinterpret_cast<float4*>(dst + 32 * cb + j) =
-              make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
-                          __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
+        for (int jj = 0; jj < 32; jj += 4)
+          *reinterpret_cast<float4*>(dst + 32 * cb + jj) =
+              make_float4(__uint_as_float(r[jj]), __uint_as_float(r[jj + 1]),
+                          __uint_as_float(r[jj + 2]), __uint_as_float(r[jj + 3]));
       }
     }
     if (vmax >= 65504.f) record_error(ctl, DEV_RANGE);
@@ -200,75 +218,177 @@ seg_state_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constan
   }
 }
 
-// Pass B.  vinit[b*G + g][h] (g >= 1) holds U_{g-1} on entry and the initial state of segment
-// g on exit; vinit[b*G][h] receives the caller's initial state (or zeros).  One thread per
-// 4 consecutive state elements, walking the segments in order.
-__global__ void seg_combine_kernel(const float* __restrict__ init, const float* __restrict__ log_decay,
-                                   float* __restrict__ vinit, int H, int G, int L, StatePages sp) {
+// Pass B.  blockIdx.z = 0: states[x*p + j] (j >= 1) holds U_{j-1} on entry and the state
+// entering part j on exit; slot x*p receives the pair's initial state (or zeros).
+// blockIdx.z = 1: adj[x*p + j] (j <= p-2) holds U'_{j+1} on entry and the adjoint leaving
+// part j on exit; slot x*p + p-1 receives d_final_state (or zeros).  One thread per 4
+// consecutive state elements, walking the parts in order.
+__global__ void seg_link_kernel(const float* __restrict__ init, const float* __restrict__ dfin,
+                                const float* __restrict__ log_decay, float* __restrict__ states,
+                                float* __restrict__ adj, int T, int H, int whole, int parts,
+                                StatePages sp) {
   constexpr int N4 = DK * DV / 4;
-  const int bh = blockIdx.y, b = bh / H, h = bh % H;
+  const bool rev = blockIdx.z == 1;
+  float* const slots = rev ? adj : states;
+  if (!slots) return;
+  const int x = blockIdx.y, bh = whole + x, b = bh / H, h = bh % H;
   const int e = blockIdx.x * blockDim.x + threadIdx.x;
   if (e >= N4) return;
-  const float lamL = expf(__ldg(log_decay + h) * (float)L);  // lambda^L
-  long long zi = bh;  // slot of the caller's initial state: [b][h] or a pool page
-  if (sp.init_paged) {
-    const int pg = __ldg(sp.page + b);
-    zi = (pg >= 0 && pg < sp.n_pages) ? ((long long)pg * sp.pool_layers + sp.layer) * H + h : -1;
+  const float gamma = __ldg(log_decay + h);
+  const int nc = (T + C - 1) / C;
+  auto tokens = [&](int j) {  // tokens of part j
+    return min(part_begin(j + 1, nc, parts) * C, T) - part_begin(j, nc, parts) * C;
+  };
+  float4* out = reinterpret_cast<float4*>(slots) + (size_t)x * parts * N4 + e;
+  float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (!rev) {
+    long long zi = bh;  // slot of the caller's initial state: [b][h] or a pool page
+    if (sp.init_paged) {
+      const int pg = __ldg(sp.page + b);
+      zi = (pg >= 0 && pg < sp.n_pages) ? ((long long)pg * sp.pool_layers + sp.layer) * H + h : -1;
+    }
+    if (init && zi >= 0) s = __ldg(reinterpret_cast<const float4*>(init) + (size_t)zi * N4 + e);
+    out[0] = s;
+    for (int j = 1; j < parts; ++j) {
+      const float lam = expf(gamma * (float)tokens(j - 1));
+      const float4 u = out[(size_t)j * N4];
+      s = make_float4(fmaf(lam, s.x, u.x), fmaf(lam, s.y, u.y), fmaf(lam, s.z, u.z),
+                      fmaf(lam, s.w, u.w));
+      out[(size_t)j * N4] = s;
+    }
+  } else {
+    if (dfin) s = __ldg(reinterpret_cast<const float4*>(dfin) + (size_t)bh * N4 + e);
+    out[(size_t)(parts - 1) * N4] = s;
+    for (int j = parts - 2; j >= 0; --j) {
+      const float lam = expf(gamma * (float)tokens(j + 1));
+      const float4 u = out[(size_t)j * N4];
+      s = make_float4(fmaf(lam, s.x, u.x), fmaf(lam, s.y, u.y), fmaf(lam, s.z, u.z),
+                      fmaf(lam, s.w, u.w));
+      out[(size_t)j * N4] = s;
+    }
   }
-  float4 s = (init && zi >= 0) ? __ldg(reinterpret_cast<const float4*>(init) + (size_t)zi * N4 + e)
-                               : make_float4(0.f, 0.f, 0.f, 0.f);
-  float4* out = reinterpret_cast<float4*>(vinit);
-  out[((size_t)b * G * H + h) * N4 + e] = s;
-  for (int g = 1; g < G; ++g) {
-    float4* p = out + ((size_t)(b * G + g) * H + h) * N4 + e;
-    const float4 u = *p;
-    s = make_float4(fmaf(lamL, s.x, u.x), fmaf(lamL, s.y, u.y), fmaf(lamL, s.z, u.z),
-                    fmaf(lamL, s.w, u.w));
-    *p = s;
+}
+
+// Finish time of `jobs` equal jobs of length d, list-scheduled in order on n_sm SMs of which
+// n_hi become free at t_hi and the others at t_lo (t_lo <= t_hi); also the SMs' last finish.
+double list_finish(long long jobs, double d, int n_sm, int n_hi, double t_lo, double t_hi) {
+  std::map<double, long long> free_at;  // time -> SMs free from then on
+  if (n_sm - n_hi > 0) free_at[t_lo] += n_sm - n_hi;
+  if (n_hi > 0) free_at[t_hi] += n_hi;
+  while (jobs > 0) {
+    auto it = free_at.begin();
+    const double t = it->first;
+    const long long n = it->second;
+    free_at.erase(it);
+    const long long k = n < jobs ? n : jobs;
+    free_at[t + d] += k;
+    if (n > k) free_at[t] += n - k;
+    jobs -= k;
   }
+  return free_at.rbegin()->first;
 }
 
 }  // namespace
 
-int fwd_segments(int B, int T, int H, int n_sm) {
-  const long long bh = (long long)B * H;
-  const int nc = T / C;
-  if (T % C != 0) return 1;                  // a ragged last chunk: one serial scan
-  if (n_sm <= 0 || 2 * bh > n_sm) return 1;  // enough (b, h) pairs to fill the GPU already
-  int best = 1;
-  for (int G = 2; G <= nc / MIN_SEGMENT_CHUNKS && bh * G <= n_sm; ++G)
-    if (nc % G == 0) best = G;
-  return best;
+// Estimated costs in chunk steps of the main kernel (forward / backward), from GB300 launch
+// lists: a CTA's start and drain (its pipeline fill and the read of its starting state), one
+// chunk of a segment pass and a pass CTA's start, and the passes' two extra launches.  A cut
+// must promise kMinGain of the uncut time, the estimate being rough.
+namespace {
+constexpr double kCtaStart = 3.0;
+constexpr double kPassChunk[2] = {0.25, 0.2};
+constexpr double kPassStart = 2.0;
+constexpr double kPassLaunch = 2.0;
+constexpr double kMinGain = 0.95;
+constexpr int kMaxParts = 32;
+// Automatic cuts keep at least this many chunks per part: with shorter parts the start costs
+// and the spread of CTA times in a long grid (which already blurs a partial last wave) left
+// no measured gain at T = 2048.
+constexpr int kMinPartChunks = 16;
+}  // namespace
+
+SplitPlan plan_split(long long BH, int nc, int roles, int n_sm, int force_parts) {
+  SplitPlan none;
+  none.whole = (int)BH;
+  none.parts = 1;
+  if (nc < 2 || n_sm <= 0 || BH <= 0 || force_parts == 1) return none;
+  const long long ctas = (long long)roles * BH;
+  long long X;  // pairs to cut: those of the partial last wave, or all when one wave holds them
+  if (ctas <= n_sm) {
+    X = BH;
+  } else {
+    const long long rem = ctas % n_sm;
+    if (rem == 0) return none;
+    X = (rem + roles - 1) / roles;
+  }
+  const int bwd = roles > 1 ? 1 : 0;
+  const long long W = (long long)roles * (BH - X);  // whole CTAs, launched first
+  const double whole_len = nc + kCtaStart;
+  const double t_lo = (double)(W / n_sm) * whole_len;
+  const int n_hi = (int)(W % n_sm);
+  // p = 1: the X pairs run whole too
+  int best_p = 1;
+  const double uncut =
+      list_finish((long long)roles * X, whole_len, n_sm, n_hi, t_lo, t_lo + whole_len);
+  double best = uncut * kMinGain;
+  const int p_auto = nc / kMinPartChunks < kMaxParts ? nc / kMinPartChunks : kMaxParts;
+  const int p_max = force_parts >= 2 ? (force_parts < nc ? force_parts : nc) : p_auto;
+  for (int p = force_parts >= 2 ? p_max : 2; p <= p_max; ++p) {
+    const double part_len = (double)((nc + p - 1) / p) + kCtaStart;
+    const double main_t =
+        list_finish((long long)roles * X * p, part_len, n_sm, n_hi, t_lo, t_lo + whole_len);
+    const long long pre_ctas = X * (p - 1) * (bwd ? 2 : 1);
+    const double pre_len = (double)((nc + p - 1) / p) * kPassChunk[bwd] + kPassStart;
+    const double pre_t = (double)((pre_ctas + n_sm - 1) / n_sm) * pre_len + kPassLaunch;
+    const double total = main_t + pre_t;
+    if (force_parts >= 2 || total < best) {
+      best = total;
+      best_p = p;
+    }
+  }
+  if (best_p == 1) return none;
+  SplitPlan plan;
+  plan.whole = (int)(BH - X);
+  plan.parts = best_p;
+  return plan;
 }
 
-size_t fwd_segment_workspace_bytes(int B, int H, int G) {
-  return G > 1 ? (size_t)B * G * H * DK * DV * sizeof(float) : 0;
+long long split_slots(long long BH, const SplitPlan& p) {
+  return p.parts > 1 ? (BH - p.whole) * (long long)p.parts : 0;
 }
 
-cudaError_t launch_chunk_fwd_segmented(const FwdArgs& a, int G, void* workspace, DevCtl ctl,
-                                       cudaStream_t stream) {
-  float* vinit = static_cast<float*>(workspace);
-  CUtensorMap mk, mv;
-  const long long rows = (long long)a.B * a.T;
-  if (!make_tmap_3d_16bit(&mk, a.k, DK, a.H, rows, 32, C, CU_TENSOR_MAP_SWIZZLE_64B, a.bf16) ||
-      !make_tmap_3d_16bit(&mv, a.v, DV, a.H, rows, 64, C, CU_TENSOR_MAP_SWIZZLE_128B, a.bf16))
+cudaError_t launch_segment_states(const void* q, const void* k, const void* v, const void* dO,
+                                  bool bf16, const float* log_decay, const float* init,
+                                  const float* dfin, const StatePages& sp, float* states,
+                                  float* adj, int B, int T, int H, const SplitPlan& plan,
+                                  DevCtl ctl, cudaStream_t stream) {
+  const long long X = (long long)B * H - plan.whole;
+  if (plan.parts <= 1 || X <= 0) return cudaSuccess;
+  CUtensorMap mk, mv, mq, mg;
+  if (!make_tmap_seq_16bit(&mk, k, DK, H, T, B, 32, C, CU_TENSOR_MAP_SWIZZLE_64B, bf16) ||
+      !make_tmap_seq_16bit(&mv, v, DV, H, T, B, 64, C, CU_TENSOR_MAP_SWIZZLE_128B, bf16))
     return cudaErrorInvalidValue;
-  auto kern = a.bf16 ? seg_state_kernel<true> : seg_state_kernel<false>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-  if (e != cudaSuccess) return e;
-  kern<<<a.B * a.H * (G - 1), THREADS, SMEM_BYTES, stream>>>(mk, mv, a.log_decay, vinit, a.T, a.H,
-                                                             G, ctl);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  seg_combine_kernel<<<dim3((DK * DV / 4 + 255) / 256, a.B * a.H), 256, 0, stream>>>(
-      a.init, a.log_decay, vinit, a.H, G, a.T / G, a.sp);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  FwdArgs c = a;
-  c.B = a.B * G;
-  c.T = a.T / G;
-  c.init = vinit;
-  c.seg = G;
-  c.sp.init_paged = false;  // the segments' initial states are in the workspace
-  return launch_chunk_fwd(c, ctl, stream);
+  if (adj) {
+    if (!make_tmap_seq_16bit(&mq, q, DK, H, T, B, 32, C, CU_TENSOR_MAP_SWIZZLE_64B, bf16) ||
+        !make_tmap_seq_16bit(&mg, dO, DV, H, T, B, 64, C, CU_TENSOR_MAP_SWIZZLE_128B, bf16))
+      return cudaErrorInvalidValue;
+  } else {
+    mq = mk;  // stand-ins, never read
+    mg = mv;
+  }
+  const long long n_fwd = states ? X * (plan.parts - 1) : 0;
+  const long long n_rev = adj ? X * (plan.parts - 1) : 0;
+  if (n_fwd + n_rev > 0) {
+    auto kern = bf16 ? seg_sum_kernel<true> : seg_sum_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    kern<<<(unsigned)(n_fwd + n_rev), THREADS, SMEM_BYTES, stream>>>(
+        mk, mv, mq, mg, log_decay, states, adj, T, H, plan.whole, plan.parts, (int)n_fwd, ctl);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  seg_link_kernel<<<dim3((DK * DV / 4 + 255) / 256, (unsigned)X, 2), 256, 0, stream>>>(
+      init, dfin, log_decay, states, adj, T, H, plan.whole, plan.parts, sp);
+  return cudaGetLastError();
 }
 
 }  // namespace gla

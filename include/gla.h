@@ -120,13 +120,15 @@ GLA_API gla_status gla_decay_schedule(int H, double t_min, double t_max, float* 
  *   final_state  [B,H,96,192] fp32 or NULL   (written)
  *   workspace    device scratch, 256-byte aligned, of gla_chunk_fwd_workspace_size()
  *                bytes.  fp32 inputs need their fp16 copies there (GLA_ERR_WORKSPACE
- *                if it is smaller).  With few long sequences (2*B*H <= the current
- *                device's SM count, T >= 4096 and a multiple of 128) the size also covers the
- *                segment-parallel path: every segment's state sum in parallel, their
- *                recurrence, then the segments as independent sequences (the state
- *                recurrence is linear).  Given less (or NULL for 16-bit inputs), the
- *                call runs the serial chunk scan instead: same results up to rounding,
- *                fewer SMs busy.  The size depends on the device current at the call.
+ *                if it is smaller).  The size also covers cutting pairs into parts:
+ *                one CTA per (b, h) runs its chunks in order, and the pairs that would
+ *                leave the last wave of SMs partly empty (all pairs, when there are fewer
+ *                than SMs -- few long sequences) are cut into consecutive chunk ranges
+ *                that run as CTAs of their own, each starting from the state at its
+ *                boundary, which two short passes compute first (the state recurrence
+ *                is linear).  See gla_chunk_split_plan.  Given less (or NULL for 16-bit
+ *                inputs), no pair is cut: same results up to rounding, more time.  The
+ *                size depends on the device current at the call.
  * Arithmetic: the tensor cores take fp16 operands with fp32 accumulation; the
  * state is carried in fp32 across chunks.  Inputs must satisfy |x| < 65504.
  */
@@ -174,7 +176,12 @@ GLA_API gla_status gla_chunk_fwd_gated(const void* q, const void* k, const void*
  *   dq, dk        [B,T,H,96]  fp32 (written)    dv [B,T,H,192] fp32 (written)
  *   d_aug         [H,96] fp32 (written, summed over B and T)
  *   d_init_state  [B,H,96,192] fp32 or NULL (written)
- *   workspace     at least gla_chunk_bwd_workspace_size() bytes, 256-aligned
+ *   workspace     gla_chunk_bwd_workspace_size() bytes, 256-aligned: the d_aug partial
+ *                 sums (and fp16 copies of fp32 inputs) are required (GLA_ERR_WORKSPACE
+ *                 if the workspace cannot hold them); the rest lets pairs be cut into
+ *                 parts as in gla_chunk_fwd (each part of the backward's three scans
+ *                 starts from the state entering it, or the adjoint of the state leaving
+ *                 it).  Given only the required part, no pair is cut.
  */
 GLA_API size_t gla_chunk_bwd_workspace_size(int B, int T, int H, int dk, int dv, gla_dtype in_dtype);
 GLA_API gla_status gla_chunk_bwd(const void* q, const void* k, const void* v, gla_dtype in_dtype,
@@ -183,6 +190,22 @@ GLA_API gla_status gla_chunk_bwd(const void* q, const void* k, const void* v, gl
                          float* dq, float* dk, float* dv, float* d_aug, float* d_init_state,
                          void* workspace, size_t workspace_bytes, int B, int T, int H,
                          int dk_, int dv_, cudaStream_t stream);
+
+/* How the chunked calls lay (b, h) pairs out over CTAs (no counterpart in the article: a
+ * scheduling choice for the GPU).  Pairs 0 .. whole_pairs-1 run whole (one CTA per pair,
+ * three per pair in the backward); pairs whole_pairs .. B*H-1 are each cut into `parts`
+ * consecutive chunk ranges (part j: chunks [j*nc/parts, (j+1)*nc/parts), nc = ceil(T/128)).
+ * The cut is chosen to shorten the estimated time on a device with n_sm SMs: the pairs of a
+ * partial last wave, or all pairs when they do not fill one wave, into the number of parts
+ * (at most 32 and nc) that minimises the estimate.  parts == 1: nothing is cut.  A host query
+ * of the plan the calls use (with the current device's SM count); results do not depend on it
+ * beyond rounding.  Errors: GLA_ERR_INVALID_ARG for sizes or n_sm <= 0 or NULL outputs. */
+GLA_API gla_status gla_chunk_split_plan(int B, int T, int H, int backward, int n_sm,
+                                        int* whole_pairs, int* parts);
+/* Overrides the choice of gla_chunk_split_plan for calls made after it returns (process-wide):
+ * 0 = automatic (default), 1 = never cut, p >= 2 = cut the pairs it would consider into
+ * min(p, nc) parts.  GLA_ERR_INVALID_ARG for p < 0. */
+GLA_API gla_status gla_set_split_parts(int parts);
 
 /* ---------------------------------------------------------------------------
  * Chunked backward that allocates nothing and takes no workspace.
@@ -266,7 +289,7 @@ GLA_API gla_status gla_decode_step_paged(float* pool, const int* page, int n_act
  * slot.  page [B] int32 (device), distinct pages; a page outside [0, n_pages)
  * leaves its slot untouched and sets the device error word to GLA_ERR_RANGE.
  * Workspace: gla_chunk_fwd_workspace_size(B, T, H, ...) as for gla_chunk_fwd
- * (the segment-parallel path applies here too).
+ * (pairs are cut into parts here too).
  */
 GLA_API gla_status gla_chunk_fwd_paged(const void* q, const void* k, const void* v,
                                        gla_dtype in_dtype, const float* log_decay,

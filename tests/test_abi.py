@@ -164,3 +164,41 @@ def test_conv_argument_checks(lib):
                             None) == 7
     assert lib.gla_conv_decode_step(A16, A16, A16, None, A16, 0, 16, None) == 0
     assert lib.gla_conv_decode_step(A16, A16, A16, None, A16, 2, 6, None) == 2
+
+
+def test_split_plan_query(lib):
+    """The layout of (b, h) pairs over CTAs: a host function, no device needed."""
+    def plan(B, T, H, bwd, n_sm=152):
+        w, p = ctypes.c_int(), ctypes.c_int()
+        rc = lib.gla_chunk_split_plan(B, T, H, bwd, n_sm, ctypes.byref(w), ctypes.byref(p))
+        assert rc == 0
+        return w.value, p.value
+    assert lib.gla_set_split_parts(0) == 0
+    # T = 2048 (16 chunks): parts shorter than 16 chunks are never chosen, nothing is cut
+    assert plan(32, 2048, 16, 0) == (512, 1) and plan(32, 2048, 16, 1) == (512, 1)
+    # backward, three CTAs per pair: 192 = one wave + 40 CTAs -> the last 14 pairs cut
+    w, p = plan(4, 8192, 16, 1)
+    assert w == 50 and 2 <= p <= 4
+    # a multiple of the SM count: nothing to cut; one chunk: nothing to cut
+    assert plan(19, 2048, 8, 0) == (152, 1)
+    assert plan(4, 100, 3, 0) == (12, 1)
+    # few long sequences: every pair is cut, into at most 32 parts
+    w, p = plan(2, 131072, 16, 0)
+    assert w == 0 and 2 <= p <= 32
+    w, p = plan(2, 131072, 16, 1)
+    assert w == 0 and 2 <= p <= 32
+    # forced: 1 never cuts, p >= 2 cuts the considered pairs into min(p, chunks) parts (the
+    # pairs of the partial last wave: 56 of 512 forward, 6 of 512 backward)
+    try:
+        assert lib.gla_set_split_parts(1) == 0
+        assert plan(32, 2048, 16, 0) == (512, 1) and plan(2, 131072, 16, 1) == (32, 1)
+        assert lib.gla_set_split_parts(5) == 0
+        assert plan(32, 2048, 16, 0) == (456, 5) and plan(32, 2048, 16, 1) == (506, 5)
+        assert plan(1, 300, 2, 1) == (0, 3)          # 3 chunks: at most 3 parts
+        assert lib.gla_set_split_parts(-1) == 1
+    finally:
+        lib.gla_set_split_parts(0)
+    w, p = ctypes.c_int(), ctypes.c_int()
+    assert lib.gla_chunk_split_plan(0, 128, 1, 0, 152, ctypes.byref(w), ctypes.byref(p)) == 1
+    assert lib.gla_chunk_split_plan(1, 128, 1, 0, 0, ctypes.byref(w), ctypes.byref(p)) == 1
+    assert lib.gla_chunk_split_plan(1, 128, 1, 0, 152, None, ctypes.byref(p)) == 1
