@@ -26,7 +26,12 @@ What pins what (source: "Beyond the KV cache ... Laplace 3B ...", section
   * pin_chunked        -- an independent fp64 chunked restatement (intra-chunk
                           masked attention + inter-chunk state, section
                           "Challenge 1"), forward and backward, for several chunk
-                          sizes, equals the token recurrence.
+                          sizes, some leaving a shorter last chunk, equals the
+                          token recurrence.
+  * pin_parts          -- sequences cut into parts that each start from the state
+                          and adjoint the linear recurrences give at their
+                          boundaries (the decomposition the GPU's long-sequence
+                          path uses) equal the token recurrence.
 """
 from __future__ import annotations
 
@@ -263,27 +268,34 @@ def pin_decode(lib):
 # ---------------------------------------------------------------------------
 # Independent chunked restatement (test only): intra-chunk masked attention plus
 # the inter-chunk state, and the chunked backward with a reverse state-adjoint
-# scan.  D_ij = lambda^(i-j) for i >= j; Lq = lambda^(i+1); Lk = lambda^(C-1-j).
+# scan.  A chunk of L tokens (the last one may be shorter than C) uses
+# D_ij = lambda^(i-j) for i >= j, Lq = lambda^(i+1), Lk = lambda^(L-1-j), and
+# advances the state by lambda^L.
+
+def _chunk_consts(lam, L):
+    i = np.arange(L)
+    D = np.where(i[:, None] >= i[None, :], lam ** (i[:, None] - i[None, :]), 0.0)
+    return D, lam ** (i + 1), lam ** (L - 1 - i)
+
 
 def chunked_fwd(q, k, v, gamma, a, init, C):
     B, T, H, dk = q.shape
     dv = v.shape[-1]
     o = np.zeros((B, T, H, dv))
     fin = np.zeros((B, H, dk, dv))
-    i = np.arange(C)
     for b in range(B):
         for h in range(H):
             lam = np.exp(gamma[h])
-            D = np.where(i[:, None] >= i[None, :], lam ** (i[:, None] - i[None, :]), 0.0)
-            Lq, Lk = lam ** (i + 1), lam ** (C - 1 - i)
             S = np.zeros((dk, dv)) if init is None else init[b, h].copy()
-            for c in range(T // C):
-                sl = slice(c * C, (c + 1) * C)
+            for c0 in range(0, T, C):
+                L = min(C, T - c0)
+                D, Lq, Lk = _chunk_consts(lam, L)
+                sl = slice(c0, c0 + L)
                 Q, K, V = q[b, sl, h], k[b, sl, h], v[b, sl, h]
                 P = (Q @ K.T) * D
                 sg = _sig(np.sum(Q * a[h] * K, 1))
                 o[b, sl, h] = P @ V + (Lq[:, None] * Q) @ S + sg[:, None] * V
-                S = lam ** C * S + (Lk[:, None] * K).T @ V
+                S = lam ** L * S + (Lk[:, None] * K).T @ V
             fin[b, h] = S
     return o, fin
 
@@ -294,22 +306,23 @@ def chunked_bwd(q, k, v, gamma, a, init, dO, dfin, C):
     dq, dk_, dv_ = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
     da = np.zeros((H, dk))
     dinit = np.zeros((B, H, dk, dv))
-    i = np.arange(C)
-    nc = T // C
+    starts = list(range(0, T, C))
     for b in range(B):
         for h in range(H):
             lam = np.exp(gamma[h])
-            D = np.where(i[:, None] >= i[None, :], lam ** (i[:, None] - i[None, :]), 0.0)
-            Lq, Lk = lam ** (i + 1), lam ** (C - 1 - i)
             S = np.zeros((dk, dv)) if init is None else init[b, h].copy()
             states = []
-            for c in range(nc):
-                sl = slice(c * C, (c + 1) * C)
+            for c0 in starts:
+                L = min(C, T - c0)
+                _, _, Lk = _chunk_consts(lam, L)
+                sl = slice(c0, c0 + L)
                 states.append(S)
-                S = lam ** C * S + (Lk[:, None] * k[b, sl, h]).T @ v[b, sl, h]
+                S = lam ** L * S + (Lk[:, None] * k[b, sl, h]).T @ v[b, sl, h]
             dS = np.zeros((dk, dv)) if dfin is None else dfin[b, h].copy()
-            for c in reversed(range(nc)):
-                sl = slice(c * C, (c + 1) * C)
+            for c, c0 in reversed(list(enumerate(starts))):
+                L = min(C, T - c0)
+                D, Lq, Lk = _chunk_consts(lam, L)
+                sl = slice(c0, c0 + L)
                 Q, K, V, G = q[b, sl, h], k[b, sl, h], v[b, sl, h], dO[b, sl, h]
                 Sm = states[c]
                 P = (Q @ K.T) * D
@@ -320,9 +333,55 @@ def chunked_bwd(q, k, v, gamma, a, init, dO, dfin, C):
                 dk_[b, sl, h] = dP.T @ Q + Lk[:, None] * (V @ dS.T) + r[:, None] * (a[h] * Q)
                 dv_[b, sl, h] = P.T @ G + Lk[:, None] * (K @ dS) + sg[:, None] * G
                 da[h] += np.sum(r[:, None] * Q * K, 0)
-                dS = lam ** C * dS + Q.T @ (Lq[:, None] * G)
+                dS = lam ** L * dS + Q.T @ (Lq[:, None] * G)
             dinit[b, h] = dS
     return dict(dq=dq, dk=dk_, dv=dv_, d_a=da, d_init_state=dinit)
+
+
+# Cut into parts (test only): a sequence of nc chunks cut into p consecutive chunk ranges
+# (part j: chunks [j*nc/p, (j+1)*nc/p)), each run from its own starting state and adjoint,
+# which follow from the linear recurrences
+#   S entering part j+1 = lambda^(L_j) S entering part j + sum_{t in j} lambda^(e_j - t) k_t v_t^T
+#   dS leaving part j-1 = lambda^(L_j) dS leaving part j + sum_{t in j} lambda^(t - s_j + 1) q_t dO_t^T
+# (s_j, e_j: first and last token of part j, L_j its tokens).
+def parts_fwd_bwd(q, k, v, gamma, a, init, dO, dfin, C, p):
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    nc = -(-T // C)
+    bounds = [min((j * nc // p) * C, T) for j in range(p + 1)]
+    S_in = np.zeros((p, B, H, dk, dv))
+    dS_out = np.zeros((p, B, H, dk, dv))
+    for b in range(B):
+        for h in range(H):
+            lam = np.exp(gamma[h])
+            S_in[0, b, h] = 0.0 if init is None else init[b, h]
+            for j in range(p - 1):
+                s, e = bounds[j], bounds[j + 1]
+                w = lam ** (e - 1 - np.arange(s, e))
+                U = (w[:, None] * k[b, s:e, h]).T @ v[b, s:e, h]
+                S_in[j + 1, b, h] = lam ** (e - s) * S_in[j, b, h] + U
+            dS_out[p - 1, b, h] = 0.0 if dfin is None else dfin[b, h]
+            for j in range(p - 1, 0, -1):
+                s, e = bounds[j], bounds[j + 1]
+                w = lam ** (np.arange(s, e) - s + 1)
+                U = (w[:, None] * q[b, s:e, h]).T @ dO[b, s:e, h]
+                dS_out[j - 1, b, h] = lam ** (e - s) * dS_out[j, b, h] + U
+    o = np.zeros((B, T, H, dv))
+    g = dict(dq=np.zeros_like(q), dk=np.zeros_like(k), dv=np.zeros_like(v),
+             d_a=np.zeros((H, dk)), d_init_state=None)
+    fin = None
+    for j in range(p):
+        s, e = bounds[j], bounds[j + 1]
+        cut = lambda x: x[:, s:e]
+        oj, fin = chunked_fwd(cut(q), cut(k), cut(v), gamma, a, S_in[j], C)
+        o[:, s:e] = oj
+        gj = chunked_bwd(cut(q), cut(k), cut(v), gamma, a, S_in[j], cut(dO), dS_out[j], C)
+        for n in ("dq", "dk", "dv"):
+            g[n][:, s:e] = gj[n]
+        g["d_a"] += gj["d_a"]
+        if j == 0:
+            g["d_init_state"] = gj["d_init_state"]
+    return o, fin, g
 
 
 def pin_chunked(lib):
@@ -334,13 +393,35 @@ def pin_chunked(lib):
     o, fin = oracle.fwd(q, k, v, gamma, a, init, lib=lib)
     g = oracle.bwd(q, k, v, gamma, a, dO, init, dfin, lib=lib)
     worst = 0.0
-    for C in (1, 4, 16, 32):
+    # C = 5 and 12 leave a shorter last chunk (32 = 6*5 + 2 = 2*12 + 8)
+    for C in (1, 4, 5, 12, 16, 32):
         oc, fc = chunked_fwd(q, k, v, gamma, a, init, C)
         gc = chunked_bwd(q, k, v, gamma, a, init, dO, dfin, C)
         worst = max(worst, _rel(oc, o), _rel(fc, fin), *[_rel(gc[n], g[n]) for n in g])
     return worst < 1e-11, f"max rel {worst:.2e}"
 
 
+def pin_parts(lib):
+    """Pairs cut into parts, each run from the state and adjoint the linear recurrences give at
+    its boundary, equal the token recurrence (forward, every gradient, d_init and the final
+    state); parts of unequal length and a ragged last chunk included."""
+    B, T, H, dk, dv = 2, 45, 3, 6, 5
+    q, k, v, gamma, a, init = _rand_problem(21, B, T, H, dk, dv, t_max=32.0, lib=lib)
+    r = _rng(22)
+    dO = r.standard_normal((B, T, H, dv))
+    dfin = r.standard_normal((B, H, dk, dv))
+    o, fin = oracle.fwd(q, k, v, gamma, a, init, lib=lib)
+    g = oracle.bwd(q, k, v, gamma, a, dO, init, dfin, lib=lib)
+    worst = 0.0
+    for C, p in ((4, 2), (4, 3), (4, 12), (8, 5), (16, 3)):  # 45 tokens: 12, 6 or 3 chunks
+        if p > -(-T // C):
+            continue
+        op, fp, gp = parts_fwd_bwd(q, k, v, gamma, a, init, dO, dfin, C, p)
+        worst = max(worst, _rel(op, o), _rel(fp, fin), *[_rel(gp[n], g[n]) for n in g])
+    return worst < 1e-11, f"max rel {worst:.2e}"
+
+
 ALL_PINS = dict(decay=pin_decay, closed_form=pin_closed_form, aug_zero=pin_aug_zero,
                 lambda_one=pin_lambda_one, fd=pin_fd, init_zero=pin_init_zero,
-                state_carry=pin_state_carry, decode=pin_decode, chunked=pin_chunked)
+                state_carry=pin_state_carry, decode=pin_decode, chunked=pin_chunked,
+                parts=pin_parts)
