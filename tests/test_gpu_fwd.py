@@ -133,20 +133,20 @@ def test_fwd_long_prefill_workload(env):
 
 @pytest.mark.parametrize("B,T,H,seed", [(1, 4096, 2, 31), (1, 8192, 3, 32)])
 def test_fwd_segmented_path(env, B, T, H, seed):
-    """Few long sequences take the segment-parallel path (the state sum of every segment but
-    the last in parallel, their recurrence, then the segments as independent sequences).  It
-    must match the oracle, initial and final state included, and the serial path, which the
-    same call takes when it is given no workspace."""
+    """Few long sequences have their pairs cut into parts (the state sums of the parts in
+    parallel, their recurrence, then every part as its own CTA).  The call must match the
+    oracle, initial and final state included, and one chain per pair, which the same call
+    runs when it is given no workspace."""
     import oracle
     gla, torch = env
-    assert gla.chunk_fwd_workspace_size(B, T, H, gla.GLA_BF16) > 0, "shape not segmented"
+    assert gla.chunk_fwd_workspace_size(B, T, H, gla.GLA_BF16) > 0, "pairs not cut"
     q, k, v = synth.qkv(seed, B, T, H)
     a = synth.aug_balance(seed, (H, 96), 0.1)
     init = synth.init_state(seed, B, H, 0.05)
     o, fin, (q, k, v, gam64) = run_fwd(env, q, k, v, a, init, H, "bf16")
     o_ref, fin_ref = oracle.fwd(q, k, v, gam64, a, init)
     eo, ef = rel_err(o, o_ref), rel_err(fin, fin_ref)
-    # the serial path: same call through the C ABI without a workspace
+    # one chain per pair: same call through the C ABI without a workspace
     lib = gla.load()
     qd, kd, vd = (to_dev(x, torch.bfloat16) for x in (q, k, v))
     gam = gla.decay_schedule(H).cuda()
@@ -161,7 +161,7 @@ def test_fwd_segmented_path(env, B, T, H, seed):
     torch.cuda.synchronize()
     assert gla.get_device_error() == 0
     es = rel_err(o, o2.cpu().numpy())
-    print(f"fwd segmented B={B} T={T} H={H}: o {eo:.2e} final {ef:.2e} vs serial {es:.2e}")
+    print(f"fwd cut B={B} T={T} H={H}: o {eo:.2e} final {ef:.2e} vs uncut {es:.2e}")
     assert eo <= TOL_CHUNK and ef <= TOL_CHUNK
     assert rel_err(o2.cpu().numpy(), o_ref) <= TOL_CHUNK
     assert rel_err(f2.cpu().numpy(), fin_ref) <= TOL_CHUNK
@@ -169,7 +169,7 @@ def test_fwd_segmented_path(env, B, T, H, seed):
 
 @pytest.mark.parametrize("B,T,H,n_tiers,want_o,seed", [
     (2, 384, 4, 2, True, 41),      # serial scan, o written too
-    (1, 4096, 2, 1, False, 42),    # segment-parallel path, y only
+    (1, 4096, 2, 1, False, 42),    # pairs cut into parts, y only
     (8, 2048, 16, 4, True, 43),    # one training-shape layer
     (2, 200, 4, 2, True, 44),      # ragged last chunk: y, rstd and o stop at T
 ])

@@ -92,7 +92,7 @@ def test_decode_paged_bad_page_touches_nothing(env):
 @pytest.mark.parametrize("B,T,H,P,PL,layer,from_pool,seed", [
     (3, 384, 4, 6, 2, 1, True, 53),    # serial scan, initial states from the pool
     (2, 256, 3, 4, 3, 0, False, 54),   # starting from zero: the pages' contents are ignored
-    (1, 4096, 2, 4, 1, 0, True, 55),   # segment-parallel path (2 segments)
+    (1, 4096, 2, 4, 1, 0, True, 55),   # few long sequences: pairs cut into parts
     (2, 300, 3, 4, 2, 1, True, 56),    # ragged last chunk
 ])
 def test_chunk_fwd_paged(env, B, T, H, P, PL, layer, from_pool, seed):
