@@ -738,17 +738,16 @@ __global__ void reduce_daug_kernel(const float* __restrict__ part, const float* 
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= H * DK) return;
   const int h = idx / DK, d = idx % DK;
+  // whole pairs are b*H + h < whole: b < b_whole (a straight loop keeps the loads in flight)
+  const int b_whole = min(B, (plan.whole - h + H - 1) / H);
   float s = 0.f;
-  for (int b = 0; b < B; ++b) {
-    const int bh = b * H + h;
-    if (bh < plan.whole) {
-      s += part[(size_t)bh * DK + d];
-    } else {
-      float t = 0.f;
-      for (int j = 0; j < plan.parts; ++j)
-        t += split[((size_t)(bh - plan.whole) * plan.parts + j) * DK + d];
-      s += t;
-    }
+#pragma unroll 8
+  for (int b = 0; b < b_whole; ++b) s += part[((size_t)b * H + h) * DK + d];
+  for (int b = b_whole; b < B; ++b) {
+    const size_t x = (size_t)b * H + h - plan.whole;
+    float t = 0.f;
+    for (int j = 0; j < plan.parts; ++j) t += split[(x * plan.parts + j) * DK + d];
+    s += t;
   }
   d_aug[idx] = s;
 }
