@@ -202,3 +202,40 @@ def test_split_plan_query(lib):
     assert lib.gla_chunk_split_plan(0, 128, 1, 0, 152, ctypes.byref(w), ctypes.byref(p)) == 1
     assert lib.gla_chunk_split_plan(1, 128, 1, 0, 0, ctypes.byref(w), ctypes.byref(p)) == 1
     assert lib.gla_chunk_split_plan(1, 128, 1, 0, 152, None, ctypes.byref(p)) == 1
+
+
+def test_split_plan_invariants(lib):
+    """For random shapes and SM counts: whole_pairs <= B*H; 1 <= parts <= min(32, chunks)
+    (min(p, chunks) when forced); nothing cut means every pair whole; the cut pairs are those of
+    the partial last wave (all pairs when one wave holds every CTA); automatic cuts keep at
+    least 16 chunks per part."""
+    rng = np.random.default_rng(5)
+    w, p = ctypes.c_int(), ctypes.c_int()
+    try:
+        for trial in range(400):
+            B, H = int(rng.integers(1, 65)), int(rng.integers(1, 33))
+            T = int(rng.integers(1, 40000))
+            n_sm = int(rng.choice([1, 7, 100, 132, 152, 160]))
+            bwd = int(rng.integers(0, 2))
+            force = int(rng.choice([0, 0, 0, 1, 2, 5, 40]))
+            assert lib.gla_set_split_parts(force) == 0
+            assert lib.gla_chunk_split_plan(B, T, H, bwd, n_sm, ctypes.byref(w), ctypes.byref(p)) == 0
+            whole, parts = w.value, p.value
+            BH, nc, roles = B * H, -(-T // 128), 3 if bwd else 1
+            assert 0 <= whole <= BH and 1 <= parts
+            if parts == 1:
+                assert whole == BH
+                continue
+            assert parts <= min(force if force >= 2 else 32, nc)
+            if force == 0:
+                assert nc // parts >= 16
+            if force >= 2:
+                assert parts == min(force, nc)
+            cut = BH - whole
+            if roles * BH <= n_sm:
+                assert cut == BH
+            else:
+                rem = (roles * BH) % n_sm
+                assert rem and cut == -(-rem // roles)
+    finally:
+        lib.gla_set_split_parts(0)
