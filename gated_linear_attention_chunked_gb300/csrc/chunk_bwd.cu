@@ -43,7 +43,9 @@ enum Role : int { R_DQ = 0, R_DV = 1, R_DK = 2 };
 
 constexpr uint32_t Q_BOX = 8192, V_BOX = 16384;
 constexpr uint32_t OFF_Q = 0, OFF_K = 3 * Q_BOX, OFF_V = 6 * Q_BOX, OFF_G = OFF_V + 3 * V_BOX;
-constexpr uint32_t OFF_STG = OFF_G + 3 * V_BOX;  // output staging, 12 warps x 2 KB
+// output staging, 4 KB (two 2 KB buffers) per warp: the row quadrant 3 warps here, the others
+// in their own rows of the state copy buffer (free between the output MMA and the next copy)
+constexpr uint32_t OFF_STG = OFF_G + 3 * V_BOX;
 constexpr uint32_t OFF_CP = OFF_STG + 12 * 2048;  // state copy, 3 atoms x 12 KB
 constexpr uint32_t S_ATOM = 12288;
 constexpr uint32_t OFF_BAR = OFF_CP + 3 * S_ATOM;
@@ -341,7 +343,11 @@ __device__ __forceinline__ void run_role(
     // and the last of the forward one
     const float dec_first =
         (ROLE == R_DQ ? c0 == nc - 1 : c0 + n == nc) ? lamL : lamC;  // step 0
-    uint8_t* const stage = base + OFF_STG + warp * 2048;  // this warp's output staging
+    // this warp's output staging, 4 KB: for q4 < 3 exactly the rows of the state copy that this
+    // warp itself writes (rows 32 q4.. of atom `sub`), so only its own stores must have read
+    // them before its next copy; the row quadrant 3 warps use the separate staging area
+    uint8_t* const stage = q4 < 3 ? base + OFF_CP + sub * S_ATOM + q4 * 4096
+                                  : base + OFF_STG + sub * 4096;
     auto qk = [&](int cc) { return qk_chunk(i, 4 * sub + cc); };  // this part's q/k chunks
     auto vg = [&](int cc) { return vg_chunk(i, 8 * sub + cc); };  // this part's v/dO chunks
     float range_max = 0.f;
@@ -613,7 +619,7 @@ __device__ __forceinline__ void run_role(
         const float osc = pow2i(e_cur);
         const int t0 = c * C + 32 * q4;  // first token of this warp's rows (boxes past T: none)
         constexpr int NCOL = NX / 3;  // 32 (DQ, DK) or 64 (DV)
-        emit_rows_tma1<NCOL / 16>(
+        emit_rows_tma<NCOL / 16>(
             stage, lane,
             [&](int k, float (&x)[16]) {
               const int col = NCOL * sub + 16 * k;
@@ -652,6 +658,9 @@ __device__ __forceinline__ void run_role(
           bad = true;
           e_next = 0;
         }
+        // the output rows' stores have read this warp's staging, which the copy overwrites
+        if (lane == 0) bulk_wait_read<0>();
+        __syncwarp();
         publish_state(t + 1, e_next, (ROLE == R_DQ && c0 + t + 2 == nc) ? lamL : lamC, nullptr,
                       true);
       }
@@ -659,7 +668,7 @@ __device__ __forceinline__ void run_role(
       if (ROLE == R_DV && t == n - 1 && c0 == 0 && p.want_dinit && q4 < 3) {
         if (lane == 0) bulk_wait_read<0>();
         __syncwarp();
-        emit_rows_tma1<4>(
+        emit_rows_tma<4>(
             stage, lane,
             [&](int k, float (&f)[16]) {
               uint32_t r[16];
