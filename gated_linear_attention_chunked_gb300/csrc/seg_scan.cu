@@ -299,12 +299,12 @@ constexpr double kCtaStart = 3.0;
 constexpr double kPassChunk[2] = {0.25, 0.2};
 constexpr double kPassStart = 2.0;
 constexpr double kPassLaunch = 2.0;
-constexpr double kMinGain = 0.95;
+constexpr double kMinGain = 0.97;
 constexpr int kMaxParts = 32;
-// Automatic cuts keep at least this many chunks per part: with shorter parts the start costs
-// and the spread of CTA times in a long grid (which already blurs a partial last wave) left
-// no measured gain at T = 2048.
-constexpr int kMinPartChunks = 16;
+// Automatic cuts keep at least this many chunks per part.  (At T = 2048 a sweep of 1, 2 and 4
+// parts over B = 8..40 matched the estimate's ratios to about 3 %: cutting pays when the last
+// wave is nearly empty -- backward B = 16, 32; forward B = 12, 40 -- and costs otherwise.)
+constexpr int kMinPartChunks = 4;
 }  // namespace
 
 SplitPlan plan_split(long long BH, int nc, int roles, int n_sm, int force_parts) {

@@ -174,8 +174,13 @@ def test_split_plan_query(lib):
         assert rc == 0
         return w.value, p.value
     assert lib.gla_set_split_parts(0) == 0
-    # T = 2048 (16 chunks): parts shorter than 16 chunks are never chosen, nothing is cut
-    assert plan(32, 2048, 16, 0) == (512, 1) and plan(32, 2048, 16, 1) == (512, 1)
+    # T = 2048 (16 chunks), B = 32: the forward's last wave is 56 of 152 CTAs full, not cut; the
+    # backward's 1536 CTAs leave 16 for an eleventh wave: its 6 pairs are cut (>= 4 chunks a part)
+    assert plan(32, 2048, 16, 0) == (512, 1)
+    w, p = plan(32, 2048, 16, 1)
+    assert w == 506 and 2 <= p <= 4
+    # a last wave more than half full is not worth cutting
+    assert plan(24, 2048, 16, 0) == (384, 1) and plan(24, 2048, 16, 1) == (384, 1)
     # backward, three CTAs per pair: 192 = one wave + 40 CTAs -> the last 14 pairs cut
     w, p = plan(4, 8192, 16, 1)
     assert w == 50 and 2 <= p <= 4
@@ -208,7 +213,7 @@ def test_split_plan_invariants(lib):
     """For random shapes and SM counts: whole_pairs <= B*H; 1 <= parts <= min(32, chunks)
     (min(p, chunks) when forced); nothing cut means every pair whole; the cut pairs are those of
     the partial last wave (all pairs when one wave holds every CTA); automatic cuts keep at
-    least 16 chunks per part."""
+    least 4 chunks per part."""
     rng = np.random.default_rng(5)
     w, p = ctypes.c_int(), ctypes.c_int()
     try:
@@ -228,7 +233,7 @@ def test_split_plan_invariants(lib):
                 continue
             assert parts <= min(force if force >= 2 else 32, nc)
             if force == 0:
-                assert nc // parts >= 16
+                assert nc // parts >= 4
             if force >= 2:
                 assert parts == min(force, nc)
             cut = BH - whole
