@@ -312,7 +312,12 @@ def run_gpu(args, rank, world, local_rank):
     dec_bytes = n_states * DEC_BYTES_STATE
     dec_gbs = dec_bytes / (dec_t * 1e-3) / 1e9
     th = B * T * H
-    gpu_launches_per_step = 4  # chunk fwd, chunk bwd, d_aug reduction, decode
+    # our kernels per step: chunk fwd, chunk bwd, d_aug reduction, decode, and the two segment
+    # passes of each chunked call whose plan cuts pairs into parts
+    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+    cut_f = gla.split_plan(B, T, H, False, n_sm)[1] > 1
+    cut_b = gla.split_plan(B, T, H, True, n_sm)[1] > 1
+    gpu_launches_per_step = 4 + 2 * int(cut_f) + 2 * int(cut_b)
 
     def roof(bound, achieved, peak, unit, traffic):
         return dict(bound=bound, achieved=achieved, peak=peak, unit=unit, frac=achieved / peak,
@@ -407,7 +412,9 @@ def run_gpu(args, rank, world, local_rank):
         parts_ms=dict(chunk_fwd=fwd_t, chunk_bwd=bwd_t, decode=dec_t),
         roofline_chunk_fwd=roof_fwd, roofline_chunk_bwd=roof_bwd,
         cpu_baseline=cpu, e2e=e2e, gpu_launches=gpu_launches_per_step * args.steps,
-        gpu_launches_detail="per step: chunk fwd, chunk bwd, d_aug reduction, decode",
+        gpu_launches_detail="per step: chunk fwd, chunk bwd, d_aug reduction, decode"
+                            + (", fwd segment passes (2)" if cut_f else "")
+                            + (", bwd segment passes (2)" if cut_b else ""),
         clocks=clocks, wall_s_timed=t_wall,
     )
     if rank == 0:
