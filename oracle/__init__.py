@@ -17,7 +17,7 @@ Laplace 3B architecture" ("GLA mixer", "Decay schedule", "Decay schedule's
 reach") and section "Challenge 3" (backward through the sequential updates).
 
 Pins (tests/test_oracle_*.py): brute-force closed form, central finite
-differences, the printed decay values, the a=0 half-strength skip, the lambda=1
+differences, the printed decay values, the a=0 half value skip, the lambda=1
 reduction to causal linear attention, state-carry and init-zero invariants,
 decode/forward consistency and an independent chunked restatement.  Every
 function here is pinned; none is "parity unpinned".

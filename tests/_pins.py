@@ -12,9 +12,9 @@ What pins what (source: "Beyond the KV cache ... Laplace 3B ...", section
   * pin_closed_form    -- brute force o_t = sum_{s<=t} lambda^(t-s) (q_t.k_s) v_s
                           + lambda^(t+1) S_0^T q_t + sigmoid(z_t) v_t (0-based t),
                           and S_T in closed form.
-  * pin_aug_zero       -- "at initialization a = 0, which gives a half-strength
-                          skip of the value": q = 0 gives o = v/2 exactly, and
-                          with a = 0 the aug term is exactly v/2.
+  * pin_aug_zero       -- the article's initialisation a = 0 passes half of the
+                          value through: q = 0 gives o = v/2 exactly, and with
+                          a = 0 the aug term is exactly v/2.
   * pin_lambda_one     -- lambda = 1, S_0 = 0, a = 0 reduces to the textbook
                           causal (unnormalised) linear attention tril(QK^T)V + v/2.
   * pin_fd             -- central finite differences of the scalar loss for
