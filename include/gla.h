@@ -22,7 +22,10 @@
  *    pointers unless a comment says "host".  The library allocates no device
  *    memory; scratch comes from the caller's `workspace`.
  *  - Streams: calls enqueue work on `stream` (NULL = legacy default stream)
- *    and return without synchronising.
+ *    and return without synchronising.  gla_chunk_fwd, gla_chunk_bwd and
+ *    gla_decode_step can be captured into a CUDA graph (stream capture) once
+ *    the device has run them eagerly: a replay gives exactly the results of
+ *    the same calls made then on the captured buffers' contents.
  *  - Errors: argument errors are returned before anything is launched, as
  *    GLA_ERR_INVALID_ARG / GLA_ERR_UNSUPPORTED / GLA_ERR_ALIGNMENT /
  *    GLA_ERR_WORKSPACE.  A failed launch returns GLA_ERR_CUDA.  Errors found
