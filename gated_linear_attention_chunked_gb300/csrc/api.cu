@@ -477,8 +477,10 @@ gla_status gla_conv_fwd(const void* x, gla_dtype x_dtype, const float* weight, c
   if (st != GLA_OK) return st;
   if (!y) return GLA_ERR_INVALID_ARG;
   if (!aligned16(y) || !aligned16(final_state)) return GLA_ERR_ALIGNMENT;
+  gla::DevCtl ctl;
+  if ((st = ctl_for_current_device(&ctl)) != GLA_OK) return st;
   return gla::launch_conv_fwd(x, x_dtype == GLA_BF16, weight, bias, init_state, y, final_state,
-                              B, T, D, stream) == cudaSuccess
+                              B, T, D, ctl, stream) == cudaSuccess
              ? GLA_OK
              : GLA_ERR_CUDA;
 }
@@ -501,9 +503,11 @@ gla_status gla_conv_bwd(const void* x, gla_dtype x_dtype, const float* weight, c
   const size_t need = gla_conv_bwd_workspace_size(B, T, D);
   if (!workspace || workspace_bytes < need) return GLA_ERR_WORKSPACE;
   if (!aligned256(workspace)) return GLA_ERR_ALIGNMENT;
+  gla::DevCtl ctl;
+  if ((st = ctl_for_current_device(&ctl)) != GLA_OK) return st;
   return gla::launch_conv_bwd(x, x_dtype == GLA_BF16, weight, bias, init_state, dy, dx,
                               d_init_state, d_weight, d_bias, static_cast<float*>(workspace), B,
-                              T, D, stream) == cudaSuccess
+                              T, D, ctl, stream) == cudaSuccess
              ? GLA_OK
              : GLA_ERR_CUDA;
 }

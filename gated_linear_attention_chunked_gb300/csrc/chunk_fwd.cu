@@ -592,7 +592,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                 const uint4 gv = j < 8 ? gq[2 * k] : gq[2 * k + 1];
                 const uint32_t w2 = (j & 7) < 2 ? gv.x : (j & 7) < 4 ? gv.y : (j & 7) < 6 ? gv.z : gv.w;
                 const float gj = ld16<true>((j & 1) ? (w2 >> 16) : (w2 & 0xFFFFu));
-                const float sl = gj / (1.f + expf(-gj));
+                const float sl = __fdividef(gj, 1.f + __expf(-gj));
                 y[j] = __uint_as_float(r[j]) * f * __ldg(wrow + 16 * k + j) * sl;
               }
             },

@@ -63,7 +63,9 @@ constexpr int GRP_BWD = 4;  // (backward: two loads per token, and two CTAs per 
 __device__ __forceinline__ float& at(float4& v, int j) {
   return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w;
 }
-__device__ __forceinline__ float sigm(float x) { return 1.f / (1.f + expf(-x)); }
+// logistic function with the fast intrinsics (a few ulp; the conv is issue bound, and the
+// IEEE division and full-range expf were most of its instructions)
+__device__ __forceinline__ float sigm(float x) { return __fdividef(1.f, 1.f + __expf(-x)); }
 
 // x_t for token t of sequence b (t < 0: the initial state, row t + 3; zeros without one)
 template <bool BF16>
@@ -139,6 +141,100 @@ conv_fwd_kernel(const void* __restrict__ x, const float* __restrict__ w,
     }
   }
   if (fin && t1 == T) {  // the state after the call: x_{T-3..T-1}
+#pragma unroll
+    for (int j = 0; j < 3; ++j)
+      reinterpret_cast<float4*>(fin)[((long long)b * 3 + j) * D4 + d4] = win[j + 1];
+  }
+}
+
+// The forward with x staged through shared memory: each token's channel block of the CTA (4
+// channels per thread, DC = 1024 channels) is one contiguous row that a single bulk copy moves
+// into a ring of NST stages of SG tokens, so ~64 KB per CTA are in flight without holding
+// registers (the register version above keeps 8 tokens of loads in flight per thread and was
+// latency bound).  Thread 0 issues the copies and refills a stage once every thread has read it.
+// Requires rows of 16-byte multiples: D % 8 == 0 for bf16 x, D % 4 == 0 for fp32 x.
+constexpr int SG = 8;                  // tokens per stage
+constexpr int NST = 4;                 // stages
+constexpr int DC = 4 * THREADS;        // channels per CTA
+constexpr uint64_t CONV_DRAIN_NS = 4000000000ull;
+template <bool BF16>
+constexpr uint32_t staged_fwd_smem() { return NST * SG * DC * (BF16 ? 2 : 4) + 2 * NST * 8; }
+
+template <bool BF16>
+__global__ void __launch_bounds__(THREADS)
+conv_fwd_staged_kernel(const void* __restrict__ x, const float* __restrict__ w,
+                       const float* __restrict__ bias, const float* __restrict__ init,
+                       float* __restrict__ y, float* __restrict__ fin, int T, int D, DevCtl ctl) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  constexpr int ES = BF16 ? 2 : 4;
+  constexpr uint32_t ROW = DC * ES, STAGE = SG * ROW;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NST * STAGE);  // full[NST], empty[NST]
+  const int D4 = D / 4, c0 = blockIdx.y * DC, nch = min(DC, D - c0);
+  const int d4 = c0 / 4 + threadIdx.x;
+  const bool active = 4 * (int)threadIdx.x < nch;
+  const int n_tiles = (T + TT - 1) / TT;
+  const int b = blockIdx.x / n_tiles, t0 = (blockIdx.x % n_tiles) * TT;
+  const int t1 = min(t0 + TT, T), ng = (t1 - t0 + SG - 1) / SG;
+  const uint32_t row_bytes = (uint32_t)nch * ES, sb = smem_u32(smem);
+  auto full = [&](int st) { return smem_u32(bars + st); };
+  auto empty = [&](int st) { return smem_u32(bars + NST + st); };
+  const uint8_t* xrow = static_cast<const uint8_t*>(x) + ((size_t)b * T * D + c0) * ES;
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < NST; ++st) {
+      mbar_init(full(st), 1);
+      mbar_init(empty(st), THREADS);
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+  int issued = 0;  // groups whose copies thread 0 has issued
+  auto issue = [&](int g) {
+    const int st = g % NST, ta = t0 + g * SG, tb = min(ta + SG, t1);
+    mbar_arrive_expect_tx(full(st), (uint32_t)(tb - ta) * row_bytes);
+    for (int t = ta; t < tb; ++t)
+      bulk_load(sb + st * STAGE + (t - ta) * ROW, xrow + (size_t)t * D * ES, row_bytes, full(st));
+    issued = g + 1;
+  };
+  if (threadIdx.x == 0)
+    for (int g = 0; g < NST && g < ng; ++g) issue(g);
+  Filt f;
+  float4 win[K];
+  if (active) {
+    f = load_filter(w, bias, d4);
+#pragma unroll
+    for (int j = 0; j < K - 1; ++j) win[j + 1] = x_at<BF16>(x, init, b, t0 - 3 + j, T, D4, d4);
+  }
+  int consumed = 0;
+  for (int g = 0; g < ng; ++g) {
+    const int st = g % NST, ta = t0 + g * SG, tb = min(ta + SG, t1);
+    if (!mbar_wait(full(st), (g / NST) & 1, ctl)) break;
+    consumed = g + 1;
+    if (active) {
+      const uint8_t* rows = smem + st * STAGE + threadIdx.x * 4 * ES;
+#pragma unroll 4
+      for (int t = ta; t < tb; ++t) {
+        win[0] = win[1];
+        win[1] = win[2];
+        win[2] = win[3];
+        if constexpr (BF16) win[3] = to_f4(*reinterpret_cast<const uint2*>(rows + (t - ta) * ROW));
+        else win[3] = *reinterpret_cast<const float4*>(rows + (t - ta) * ROW);
+        float4 z = conv4(f, win);
+        float4 o;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) at(o, c) = at(z, c) * sigm(at(z, c));
+        reinterpret_cast<float4*>(y)[((long long)b * T + t) * D4 + d4] = o;
+      }
+    }
+    mbar_arrive(empty(st));
+    if (threadIdx.x == 0 && g + NST < ng) {
+      if (!mbar_wait(empty(st), (g / NST) & 1, ctl)) break;
+      issue(g + NST);
+    }
+  }
+  // no copy may still be landing when the CTA exits (only after a wait gave up)
+  if (threadIdx.x == 0)
+    for (int g = consumed; g < issued; ++g) mbar_wait(full(g % NST), (g / NST) & 1, ctl, CONV_DRAIN_NS);
+  if (active && fin && t1 == T && consumed == ng) {  // the state after the call: x_{T-3..T-1}
 #pragma unroll
     for (int j = 0; j < 3; ++j)
       reinterpret_cast<float4*>(fin)[((long long)b * 3 + j) * D4 + d4] = win[j + 1];
@@ -235,6 +331,152 @@ conv_bwd_kernel(const void* __restrict__ x, const float* __restrict__ w,
   }
 }
 
+// The backward with x and dy staged through shared memory the same way (their rows of the
+// CTA's channel block, NSTB stages of SGB tokens): same arithmetic as conv_bwd_kernel.
+constexpr int SGB = 4;   // tokens per stage (backward)
+constexpr int NSTB = 4;  // stages (backward)
+template <bool BF16>
+constexpr uint32_t staged_bwd_smem() { return NSTB * SGB * DC * ((BF16 ? 2 : 4) + 4) + 2 * NSTB * 8; }
+
+template <bool BF16>
+__global__ void __launch_bounds__(THREADS, 2)
+conv_bwd_staged_kernel(const void* __restrict__ x, const float* __restrict__ w,
+                       const float* __restrict__ bias, const float* __restrict__ init,
+                       const float* __restrict__ dy, float* __restrict__ dx,
+                       float* __restrict__ dinit, float* __restrict__ part, int T, int D,
+                       DevCtl ctl) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  constexpr int ES = BF16 ? 2 : 4;
+  constexpr uint32_t XROW = DC * ES, GROW = DC * 4, STAGE = SGB * (XROW + GROW);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NSTB * STAGE);  // full[NSTB], empty[NSTB]
+  const int D4 = D / 4, c0 = blockIdx.y * DC, nch = min(DC, D - c0);
+  const int d4 = c0 / 4 + threadIdx.x;
+  const bool active = 4 * (int)threadIdx.x < nch;
+  const int n_tiles = (T + TT - 1) / TT;
+  const int b = blockIdx.x / n_tiles, t0 = (blockIdx.x % n_tiles) * TT;
+  const int t1 = min(t0 + TT, T);
+  // t runs to t1 + 2 so that dx_s for every s < t1 is complete (dz beyond T is 0); the rows of
+  // tokens t0 .. tload-1 come through the ring
+  const int tend = t1 + 3, tload = min(tend, T), ng = (tload - t0 + SGB - 1) / SGB;
+  const uint32_t xbytes = (uint32_t)nch * ES, gbytes = (uint32_t)nch * 4, sb = smem_u32(smem);
+  auto full = [&](int st) { return smem_u32(bars + st); };
+  auto empty = [&](int st) { return smem_u32(bars + NSTB + st); };
+  const uint8_t* xrow = static_cast<const uint8_t*>(x) + ((size_t)b * T * D + c0) * ES;
+  const uint8_t* grow = reinterpret_cast<const uint8_t*>(dy) + ((size_t)b * T * D + c0) * 4;
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < NSTB; ++st) {
+      mbar_init(full(st), 1);
+      mbar_init(empty(st), THREADS);
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+  int issued = 0;
+  auto issue = [&](int g) {
+    const int st = g % NSTB, ta = t0 + g * SGB, tb = min(ta + SGB, tload);
+    mbar_arrive_expect_tx(full(st), (uint32_t)(tb - ta) * (xbytes + gbytes));
+    for (int t = ta; t < tb; ++t) {
+      bulk_load(sb + st * STAGE + (t - ta) * XROW, xrow + (size_t)t * D * ES, xbytes, full(st));
+      bulk_load(sb + st * STAGE + SGB * XROW + (t - ta) * GROW, grow + (size_t)t * D * 4, gbytes,
+                full(st));
+    }
+    issued = g + 1;
+  };
+  if (threadIdx.x == 0)
+    for (int g = 0; g < NSTB && g < ng; ++g) issue(g);
+  const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+  Filt f;
+  float4 win[K], dz[K];  // dz[0..3] = dz_{t-3..t} after step t
+  float4 gw[K], gb = zero;
+#pragma unroll
+  for (int j = 0; j < K; ++j) {
+    dz[j] = zero;
+    gw[j] = zero;
+  }
+  if (active) {
+    f = load_filter(w, bias, d4);
+#pragma unroll
+    for (int j = 0; j < K - 1; ++j) win[j + 1] = x_at<BF16>(x, init, b, t0 - 3 + j, T, D4, d4);
+  }
+  // one token: shift the windows, dz_t (zero past T), the tile's weight and bias sums, dx_{t-3}
+  auto step = [&](int t, float4 xv, float4 g, bool in_seq) {
+#pragma unroll
+    for (int j = 0; j < K - 1; ++j) {
+      win[j] = win[j + 1];
+      dz[j] = dz[j + 1];
+    }
+    if (in_seq) {
+      win[3] = xv;
+      float4 z = conv4(f, win);
+      float4 d;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const float zc = at(z, c), sg = sigm(zc);
+        at(d, c) = at(g, c) * sg * (1.f + zc * (1.f - sg));
+      }
+      dz[3] = d;
+      if (t < t1) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          at(gb, c) += at(d, c);
+#pragma unroll
+          for (int j = 0; j < K; ++j) at(gw[j], c) = fmaf(at(d, c), at(win[j], c), at(gw[j], c));
+        }
+      }
+    } else {
+      win[3] = zero;
+      dz[3] = zero;
+    }
+    const int s = t - 3;
+    if ((s >= t0 || (t0 == 0 && s >= -3)) && s < t1) {
+      float4 o = zero;
+#pragma unroll
+      for (int j = 0; j < K; ++j)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) at(o, c) = fmaf(at(f.w[j], c), at(dz[3 - j], c), at(o, c));
+      if (s >= 0)
+        reinterpret_cast<float4*>(dx)[((long long)b * T + s) * D4 + d4] = o;
+      else if (dinit)
+        reinterpret_cast<float4*>(dinit)[((long long)b * 3 + (s + 3)) * D4 + d4] = o;
+    }
+  };
+  int consumed = 0;
+  for (int g = 0; g < ng; ++g) {
+    const int st = g % NSTB, ta = t0 + g * SGB, tb = min(ta + SGB, tload);
+    if (!mbar_wait(full(st), (g / NSTB) & 1, ctl)) break;
+    consumed = g + 1;
+    if (active) {
+      const uint8_t* xs = smem + st * STAGE + threadIdx.x * 4 * ES;
+      const uint8_t* gs = smem + st * STAGE + SGB * XROW + threadIdx.x * 16;
+      for (int t = ta; t < tb; ++t) {
+        float4 xv;
+        if constexpr (BF16) xv = to_f4(*reinterpret_cast<const uint2*>(xs + (t - ta) * XROW));
+        else xv = *reinterpret_cast<const float4*>(xs + (t - ta) * XROW);
+        step(t, xv, *reinterpret_cast<const float4*>(gs + (t - ta) * GROW), true);
+      }
+    }
+    mbar_arrive(empty(st));
+    if (threadIdx.x == 0 && g + NSTB < ng) {
+      if (!mbar_wait(empty(st), (g / NSTB) & 1, ctl)) break;
+      issue(g + NSTB);
+    }
+  }
+  if (threadIdx.x == 0)
+    for (int g = consumed; g < issued; ++g)
+      mbar_wait(full(g % NSTB), (g / NSTB) & 1, ctl, CONV_DRAIN_NS);
+  if (consumed < ng) return;
+  if (active) {
+    for (int t = tload; t < tend; ++t) step(t, zero, zero, false);  // past T: dz = 0
+    float* p = part + ((long long)blockIdx.x * D + 4 * d4) * 5;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+#pragma unroll
+      for (int j = 0; j < K; ++j) p[c * 5 + j] = at(gw[j], c);
+      p[c * 5 + 4] = at(gb, c);
+    }
+  }
+}
+
 // dw[d][j], db[d] = sums over the n_parts tiles, in order
 __global__ void conv_reduce_kernel(const float* __restrict__ part, float* __restrict__ dw,
                                    float* __restrict__ db, int n_parts, int D) {
@@ -277,7 +519,25 @@ size_t conv_bwd_workspace_bytes(int B, int T, int D) {
 
 cudaError_t launch_conv_fwd(const void* x, bool bf16, const float* w, const float* bias,
                             const float* init, float* y, float* fin, int B, int T, int D,
-                            cudaStream_t stream) {
+                            DevCtl ctl, cudaStream_t stream) {
+  if (D % (bf16 ? 8 : 4) == 0) {  // rows of 16-byte multiples: the staged kernel
+    const dim3 grid(B * ((T + TT - 1) / TT), (D + DC - 1) / DC);
+    cudaError_t e;
+    if (bf16) {
+      e = cudaFuncSetAttribute(conv_fwd_staged_kernel<true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, staged_fwd_smem<true>());
+      if (e != cudaSuccess) return e;
+      conv_fwd_staged_kernel<true><<<grid, THREADS, staged_fwd_smem<true>(), stream>>>(
+          x, w, bias, init, y, fin, T, D, ctl);
+    } else {
+      e = cudaFuncSetAttribute(conv_fwd_staged_kernel<false>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, staged_fwd_smem<false>());
+      if (e != cudaSuccess) return e;
+      conv_fwd_staged_kernel<false><<<grid, THREADS, staged_fwd_smem<false>(), stream>>>(
+          x, w, bias, init, y, fin, T, D, ctl);
+    }
+    return cudaGetLastError();
+  }
   const dim3 grid(B * ((T + TT - 1) / TT), (D / 4 + THREADS - 1) / THREADS);
   if (bf16)
     conv_fwd_kernel<true><<<grid, THREADS, 0, stream>>>(x, w, bias, init, y, fin, T, D);
@@ -289,8 +549,28 @@ cudaError_t launch_conv_fwd(const void* x, bool bf16, const float* w, const floa
 cudaError_t launch_conv_bwd(const void* x, bool bf16, const float* w, const float* bias,
                             const float* init, const float* dy, float* dx, float* dinit,
                             float* dw, float* db, float* part, int B, int T, int D,
-                            cudaStream_t stream) {
+                            DevCtl ctl, cudaStream_t stream) {
   const int n_tiles = (T + TT - 1) / TT;
+  if (D % (bf16 ? 8 : 4) == 0) {  // rows of 16-byte multiples: the staged kernel
+    const dim3 grid(B * n_tiles, (D + DC - 1) / DC);
+    cudaError_t e;
+    if (bf16) {
+      e = cudaFuncSetAttribute(conv_bwd_staged_kernel<true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, staged_bwd_smem<true>());
+      if (e != cudaSuccess) return e;
+      conv_bwd_staged_kernel<true><<<grid, THREADS, staged_bwd_smem<true>(), stream>>>(
+          x, w, bias, init, dy, dx, dinit, part, T, D, ctl);
+    } else {
+      e = cudaFuncSetAttribute(conv_bwd_staged_kernel<false>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, staged_bwd_smem<false>());
+      if (e != cudaSuccess) return e;
+      conv_bwd_staged_kernel<false><<<grid, THREADS, staged_bwd_smem<false>(), stream>>>(
+          x, w, bias, init, dy, dx, dinit, part, T, D, ctl);
+    }
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    conv_reduce_kernel<<<(D * 5 + 255) / 256, 256, 0, stream>>>(part, dw, db, B * n_tiles, D);
+    return cudaGetLastError();
+  }
   const dim3 grid(B * n_tiles, (D / 4 + THREADS - 1) / THREADS);
   if (bf16)
     conv_bwd_kernel<true><<<grid, THREADS, 0, stream>>>(x, w, bias, init, dy, dx, dinit, part, T, D);

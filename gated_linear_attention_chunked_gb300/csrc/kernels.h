@@ -148,11 +148,11 @@ cudaError_t launch_head_norm_bwd(const float* dy, const float* o, const void* g,
 size_t conv_bwd_workspace_bytes(int B, int T, int D);
 cudaError_t launch_conv_fwd(const void* x, bool bf16, const float* w, const float* bias,
                             const float* init, float* y, float* fin, int B, int T, int D,
-                            cudaStream_t stream);
+                            DevCtl ctl, cudaStream_t stream);
 cudaError_t launch_conv_bwd(const void* x, bool bf16, const float* w, const float* bias,
                             const float* init, const float* dy, float* dx, float* dinit,
                             float* dw, float* db, float* part, int B, int T, int D,
-                            cudaStream_t stream);
+                            DevCtl ctl, cudaStream_t stream);
 cudaError_t launch_conv_decode(float* state, const float* x, const float* w, const float* bias,
                                float* y, long long n, int D, cudaStream_t stream);
 

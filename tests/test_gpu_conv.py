@@ -36,6 +36,9 @@ def _inputs(seed, B, T, D, bf16, with_init, with_bias):
     (1, 2, 8, False, True, True, 82),        # shorter than the state
     (3, 200, 3072, True, False, False, 83),  # the model width, no state, no bias
     (4, 2048, 3072, True, True, True, 84),   # training shape (B=4 of 32)
+    (2, 130, 1032, True, False, True, 86),   # a last channel block of 8 (staged forward)
+    (2, 70, 1028, True, True, True, 85),     # bf16 rows not 16-byte multiples: register forward
+    (2, 100, 200, False, True, False, 87),   # fp32 x, staged forward
 ])
 def test_conv_matches_oracle(env, B, T, D, bf16, with_init, with_bias, seed):
     import oracle
