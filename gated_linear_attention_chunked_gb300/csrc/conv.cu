@@ -211,8 +211,7 @@ conv_fwd_staged_kernel(const void* __restrict__ x, const float* __restrict__ w,
     consumed = g + 1;
     if (active) {
       const uint8_t* rows = smem + st * STAGE + threadIdx.x * 4 * ES;
-#pragma unroll 4
-      for (int t = ta; t < tb; ++t) {
+      auto tok = [&](int t) {
         win[0] = win[1];
         win[1] = win[2];
         win[2] = win[3];
@@ -223,6 +222,12 @@ conv_fwd_staged_kernel(const void* __restrict__ x, const float* __restrict__ w,
 #pragma unroll
         for (int c = 0; c < 4; ++c) at(o, c) = at(z, c) * sigm(at(z, c));
         reinterpret_cast<float4*>(y)[((long long)b * T + t) * D4 + d4] = o;
+      };
+      if (tb - ta == SG) {  // a full stage: unrolled, so the window shifts become renames
+#pragma unroll
+        for (int u = 0; u < SG; ++u) tok(ta + u);
+      } else {
+        for (int t = ta; t < tb; ++t) tok(t);
       }
     }
     mbar_arrive(empty(st));
@@ -448,11 +453,17 @@ conv_bwd_staged_kernel(const void* __restrict__ x, const float* __restrict__ w,
     if (active) {
       const uint8_t* xs = smem + st * STAGE + threadIdx.x * 4 * ES;
       const uint8_t* gs = smem + st * STAGE + SGB * XROW + threadIdx.x * 16;
-      for (int t = ta; t < tb; ++t) {
+      auto tok = [&](int t) {
         float4 xv;
         if constexpr (BF16) xv = to_f4(*reinterpret_cast<const uint2*>(xs + (t - ta) * XROW));
         else xv = *reinterpret_cast<const float4*>(xs + (t - ta) * XROW);
         step(t, xv, *reinterpret_cast<const float4*>(gs + (t - ta) * GROW), true);
+      };
+      if (tb - ta == SGB) {  // a full stage: unrolled, so the window shifts become renames
+#pragma unroll
+        for (int u = 0; u < SGB; ++u) tok(ta + u);
+      } else {
+        for (int t = ta; t < tb; ++t) tok(t);
       }
     }
     mbar_arrive(empty(st));
