@@ -158,35 +158,6 @@ __device__ __forceinline__ int state_exponent(float m) {
   return ex > 14 ? ex - 14 : 0;
 }
 
-// Store 32 rows x NC (16 or 32) fp32 columns held one row per lane (`r`) to global memory
-// with row-contiguous writes: the warp transposes through a staging area of 32 x NC x 4
-// bytes (16-byte chunks XOR-swizzled by row), then each store instruction writes whole
-// row segments (4 rows x 128 B, or 8 rows x 64 B).  `row_ptr(rr)` is the address of this
-// block's first column in row rr (0..31).
-template <int NC, typename RowPtr>
-__device__ __forceinline__ void store_rows_coalesced(uint8_t* stage, const float* r, int lane,
-                                                     RowPtr row_ptr) {
-  static_assert(NC == 16 || NC == 32, "block width");
-  constexpr int CH = NC / 4;            // 16-byte chunks per row
-  constexpr int RB = NC * 4;            // row bytes
-  constexpr int RPI = 32 / CH;          // rows per store instruction
-  // chunk swizzle by row: 8 consecutive rows cover all 32 banks in both phases
-  auto key = [](int row) { return CH == 4 ? (row >> 1) & 3 : row & 7; };
-#pragma unroll
-  for (int c = 0; c < CH; ++c)
-    *reinterpret_cast<float4*>(stage + lane * RB + ((c ^ key(lane)) << 4)) =
-        make_float4(r[4 * c], r[4 * c + 1], r[4 * c + 2], r[4 * c + 3]);
-  __syncwarp();
-#pragma unroll
-  for (int k = 0; k < CH; ++k) {
-    const int rr = RPI * k + lane / CH, c = lane % CH;
-    const float4 x =
-        *reinterpret_cast<const float4*>(stage + rr * RB + ((c ^ key(rr)) << 4));
-    *reinterpret_cast<float4*>(row_ptr(rr) + 4 * c) = x;
-  }
-  __syncwarp();
-}
-
 // Write 32 rows x 16 fp32 columns (one row per lane, `r`) into a 2 KB staging buffer in
 // the layout a 64-byte-swizzled TMA box {16, 1, 32} expects: row rr at rr * 64 bytes, its
 // 16-byte chunk c at position c ^ ((rr >> 1) & 3).  `buf` must be 512-byte aligned.
@@ -211,29 +182,6 @@ __device__ __forceinline__ void emit_rows_tma(uint8_t* buf0, int lane, Produce p
     produce(k, r);
     if (k >= 2) {  // the store that last read this buffer must have finished reading it
       if (lane == 0) bulk_wait_read<1>();
-      __syncwarp();
-    }
-    stage_rows16_sw64(buf, r, lane);
-    fence_proxy_async();
-    __syncwarp();
-    if (lane == 0) {
-      store(k, smem_u32(buf));
-      bulk_commit();
-    }
-  }
-}
-
-// As emit_rows_tma, with a single 2 KB staging buffer (for callers short of shared memory):
-// before a block reuses the buffer, the previous block's TMA store must have read it.
-template <int NBLK16, typename Produce, typename Store>
-__device__ __forceinline__ void emit_rows_tma1(uint8_t* buf, int lane, Produce produce,
-                                               Store store) {
-#pragma unroll
-  for (int k = 0; k < NBLK16; ++k) {
-    float r[16];
-    produce(k, r);
-    if (k >= 1) {
-      if (lane == 0) bulk_wait_read<0>();
       __syncwarp();
     }
     stage_rows16_sw64(buf, r, lane);
