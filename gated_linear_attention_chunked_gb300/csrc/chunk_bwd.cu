@@ -619,13 +619,17 @@ __device__ __forceinline__ void run_role(
         const float osc = pow2i(e_cur);
         const int t0 = c * C + 32 * q4;  // first token of this warp's rows (boxes past T: none)
         constexpr int NCOL = NX / 3;  // 32 (DQ, DK) or 64 (DV)
+        uint32_t rbuf[2][16];  // blocks read in pairs: one TMEM round trip per two blocks
         emit_rows_tma<NCOL / 16>(
             stage, lane,
             [&](int k, float (&x)[16]) {
               const int col = NCOL * sub + 16 * k;
-              uint32_t r[16];
-              tmem_ld16(trow + TM_X + col, r);
-              tmem_wait_ld();
+              if ((k & 1) == 0) {
+                tmem_ld16(trow + TM_X + col, rbuf[0]);
+                if (k + 1 < NCOL / 16) tmem_ld16(trow + TM_X + col + 16, rbuf[1]);
+                tmem_wait_ld();
+              }
+              const uint32_t (&r)[16] = rbuf[k & 1];
               if constexpr (ROLE == R_DV) {
 #pragma unroll
                 for (int j = 0; j < 16; ++j) x[j] = __uint_as_float(r[j]) * osc;
