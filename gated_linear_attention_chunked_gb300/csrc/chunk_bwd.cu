@@ -17,15 +17,17 @@
 //                            (sigmoid(z) dO enters through the diagonal of P''^T)
 //   role DK  reverse order : score dP^T = V dO^T, out dk = dP''^T Q + V' dS^T, adjoint dS += Q^T dO''
 // (X'' denotes an fp16 copy of X scaled by its decay factors; scores are masked with D and
-// scaled by 2^-e in fp32 before their fp16 copy.)  Warp layout as in the forward:
-//   warp 12 TMA producer (single stage: q, k, v, dO tiles of one chunk, L2 prefetch of the next),
-//   warp 13 tcgen05 issuer + TMEM owner (D_X [0,192) output, D_S [192,384) state,
+// scaled by 2^-e in fp32 before their fp16 copy.)  Warp layout:
+//   warp 16 TMA producer (one buffer of the q, k, v, dO tiles of a chunk, in two groups with
+//           barriers of their own, so the tiles the state update reads last are refilled
+//           first; L2 prefetch of the next chunk),
+//   warp 17 tcgen05 issuer + TMEM owner (D_X [0,192) output, D_S [192,384) state,
 //           D_P [384,512) score),
-//   warps 0..11 epilogue, three warps per row quadrant (row = token = TMEM lane), each with a
-//           third of the row: gate dot products, in-place fp16 operands, then (part 0) the
-//           masked score copy written back into TMEM as an MMA operand; after the MMAs, the
-//           release of the tiles, the next state copy (the serial step) and the output rows,
-//           TMA-stored from per-warp staging.
+//   warps 0..15 epilogue, four warps per row quadrant (row = token = TMEM lane), each with a
+//           quarter of the row: gate dot products, in-place fp16 operands, two blocks of the
+//           masked score copy written back into TMEM as an MMA operand; then the next state
+//           copy (the serial step) while the output MMA's TMEM-operand part runs, and the
+//           output rows, TMA-stored from per-warp staging.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -43,20 +45,18 @@ enum Role : int { R_DQ = 0, R_DV = 1, R_DK = 2 };
 
 constexpr uint32_t Q_BOX = 8192, V_BOX = 16384;
 constexpr uint32_t OFF_Q = 0, OFF_K = 3 * Q_BOX, OFF_V = 6 * Q_BOX, OFF_G = OFF_V + 3 * V_BOX;
-// output staging, 4 KB (two 2 KB buffers) per warp: the row quadrant 3 warps here, the others
-// in their own rows of the state copy buffer (free between the output MMA and the next copy)
-constexpr uint32_t OFF_STG = OFF_G + 3 * V_BOX;
-constexpr uint32_t OFF_CP = OFF_STG + 12 * 2048;  // state copy, 3 atoms x 12 KB
+constexpr uint32_t OFF_CP = OFF_G + 3 * V_BOX;  // state copy, 3 atoms x 12 KB
 constexpr uint32_t S_ATOM = 12288;
-constexpr uint32_t OFF_BAR = OFF_CP + 3 * S_ATOM;
-constexpr uint32_t NBAR = 20;
+constexpr uint32_t OFF_STG = OFF_CP + 3 * S_ATOM;  // output staging, 2 KB per epilogue warp
+constexpr uint32_t OFF_BAR = OFF_STG + 16 * 2048;
+constexpr uint32_t NBAR = 21;
 constexpr uint32_t OFF_TMEM = OFF_BAR + NBAR * 8;
 constexpr uint32_t OFF_ABORT = OFF_TMEM + 4;
-constexpr uint32_t OFF_RED = OFF_TMEM + 16;  // float red[3][12]: per-warp max|S|
-constexpr uint32_t OFF_ES = OFF_RED + 144;   // int es[2]
-constexpr uint32_t OFF_AB = OFF_ES + 16;     // float abmax[2][24]: state-MMA operand maxima
-constexpr uint32_t OFF_GP = OFF_AB + 192;    // float gate_part[3][128]: gate partial sums
-constexpr uint32_t OFF_DP = OFF_GP + 1536;   // float dpv[128]: dO.v per row (DQ, DK)
+constexpr uint32_t OFF_RED = OFF_TMEM + 16;  // float red[3][16]: per-warp max|S|
+constexpr uint32_t OFF_ES = OFF_RED + 192;   // int es[2]
+constexpr uint32_t OFF_AB = OFF_ES + 16;     // float abmax[2][32]: state-MMA operand maxima
+constexpr uint32_t OFF_GP = OFF_AB + 256;    // float gate_part[4][128]: gate partial sums
+constexpr uint32_t OFF_DP = OFF_GP + 2048;   // float dpv[128]: dO.v per row (DQ, DK)
 constexpr uint32_t OFF_A = OFF_DP + 512;     // float a[96]
 constexpr uint32_t OFF_PW = OFF_A + 384;     // float pw[128]
 constexpr uint32_t SMEM_USED = OFF_PW + 512;
@@ -65,25 +65,31 @@ static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 constexpr uint32_t TM_X = 0, TM_A = 96, TM_S = 192, TM_P = 384;  // TM_A: d_a (DQ role)
 
+// A chunk's tiles come in two groups with barriers of their own: the early group holds the
+// tiles whose last reader is the state (adjoint) update, so the next chunk's copies of them
+// start while this chunk's masked scores are made; the late group holds the rest.
 enum Bar : uint32_t {
-  FULL = 0,
-  EMPTY = 1,  // tiles free: state MMA done + emit group done with them
-  P_DONE = 2,
-  X_DONE = 3,
-  S_DONE = 4,
-  EP_CONV = 5,
-  EP_X = 6,
-  EP_S = 7,
-  RED = 8,
-  DRAIN = 9,
-  QG0 = 10,  // 10..13: quadrant q's three gate partial sums are in shared memory
-  QS0 = 14,  // 14..17: quadrant q's three parts have read their score blocks
-  EP_C1 = 18,  // the fp16 operands are in place (the MMAs that need no masked score may run)
+  FULL_E = 0,   // early tiles landed
+  FULL_L = 1,   // late tiles landed
+  EMPTY_E = 2,  // early tiles free: the state (adjoint) update has read them
+  EMPTY_L = 3,  // late tiles free: the output MMAs are done and the epilogue has its operands
+  P_DONE = 4,
+  X_DONE = 5,
+  S_DONE = 6,  // the state (adjoint) update is done
+  EP_CONV = 7,
+  EP_X = 8,
+  EP_S = 9,
+  RED = 10,
+  DRAIN = 11,
+  QG0 = 12,  // 12..15: quadrant q's four gate partial sums are in shared memory
+  QS0 = 16,  // 16..19: quadrant q's four parts have read their score blocks
+  EP_C1 = 20,  // the fp16 operands are in place (the MMAs that need no masked score may run)
 };
 
-constexpr int THREADS = 448;
-constexpr int PRODUCER_WARP = 12, MMA_WARP = 13;
-constexpr int EPI_THREADS = 384;  // warps 0..11
+constexpr int NEPI = 16;  // epilogue warps: four per TMEM lane quadrant
+constexpr int THREADS = (NEPI + 2) * 32;
+constexpr int PRODUCER_WARP = NEPI, MMA_WARP = NEPI + 1;
+constexpr int EPI_THREADS = NEPI * 32;
 
 struct BwdParams {
   const float* log_decay;
@@ -99,9 +105,21 @@ struct BwdParams {
   float* da_split;         // cut pairs: d_aug partial sums per part, [96] each
 };
 
+enum Tile : int { T_Q = 0, T_K = 1, T_V = 2, T_G = 3 };
+
+// Group of a tile for a role: 0 early, 1 late, -1 not loaded.  DQ: v, dO are last read by the
+// state update (K^T V') and the output MMA's state part (dO'' S^T); DK: k (gate only), v, dO;
+// DV: q, k.  The late tiles are read by the output MMA's TMEM-operand part or by the rows.
 template <int ROLE>
-__device__ __forceinline__ constexpr uint32_t tile_bytes() {
-  return ROLE == R_DV ? 6 * Q_BOX + 3 * V_BOX : 6 * Q_BOX + 6 * V_BOX;
+__device__ __forceinline__ constexpr int tile_group(int tile) {
+  if (ROLE == R_DQ) return tile == T_V || tile == T_G ? 0 : 1;
+  if (ROLE == R_DK) return tile == T_Q ? 1 : 0;
+  return tile == T_V ? -1 : (tile == T_G ? 1 : 0);
+}
+template <int ROLE>
+__device__ __forceinline__ constexpr uint32_t group_bytes(int g) {
+  return (tile_group<ROLE>(T_Q) == g ? 3 * Q_BOX : 0) + (tile_group<ROLE>(T_K) == g ? 3 * Q_BOX : 0) +
+         (tile_group<ROLE>(T_V) == g ? 3 * V_BOX : 0) + (tile_group<ROLE>(T_G) == g ? 3 * V_BOX : 0);
 }
 
 // Chunk handled at step t of the role's scan over chunks [c0, c0 + n).
@@ -127,6 +145,13 @@ __device__ __forceinline__ void unpack8(const uint4& x, float (&f)[8]) {
     f[2 * e] = ld16<SRC_BF16>(w[e] & 0xFFFFu);
     f[2 * e + 1] = ld16<SRC_BF16>(w[e] >> 16);
   }
+}
+
+__device__ __forceinline__ float max16(const float* v) {
+  float m = v[0];
+#pragma unroll
+  for (int w = 1; w < 16; ++w) m = fmaxf(m, v[w]);
+  return m;
 }
 
 template <int ROLE, bool BF16>
@@ -155,8 +180,10 @@ __device__ __forceinline__ void run_role(
     tmem_relinquish();
   }
   if (tid == PRODUCER_WARP * 32) {
-    mbar_init(cta.bar(FULL), 1);
-    mbar_init(cta.bar(EMPTY), 1 + EPI_THREADS);
+    mbar_init(cta.bar(FULL_E), 1);
+    mbar_init(cta.bar(FULL_L), 1);
+    mbar_init(cta.bar(EMPTY_E), 1);
+    mbar_init(cta.bar(EMPTY_L), 1 + EPI_THREADS);
     mbar_init(cta.bar(P_DONE), 1);
     mbar_init(cta.bar(X_DONE), 1);
     mbar_init(cta.bar(S_DONE), 1);
@@ -167,8 +194,8 @@ __device__ __forceinline__ void run_role(
     mbar_init(cta.bar(EP_S), EPI_THREADS);
     mbar_init(cta.bar(RED), EPI_THREADS);
     for (int q = 0; q < 4; ++q) {
-      mbar_init(cta.bar(QG0 + q), 96);
-      mbar_init(cta.bar(QS0 + q), 96);
+      mbar_init(cta.bar(QG0 + q), 128);
+      mbar_init(cta.bar(QS0 + q), 128);
     }
     *cta.abort_flag() = 0;
     fence_barrier_init();
@@ -184,41 +211,57 @@ __device__ __forceinline__ void run_role(
   if (warp == PRODUCER_WARP) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      auto load = [&](int c, bool prefetch_only) {
+      // the tiles of group g of chunk c (or an L2 prefetch of them)
+      auto load = [&](int c, int g, bool prefetch_only) {
         const int t0 = c * C;
+        const uint32_t bar = cta.bar(g == 0 ? FULL_E : FULL_L);
         for (int j = 0; j < 3; ++j) {
           if (prefetch_only) {
-            tma_prefetch_4d(&map_q, 32 * j, h, t0, b);
-            tma_prefetch_4d(&map_k, 32 * j, h, t0, b);
-            if (ROLE != R_DV) tma_prefetch_4d(&map_v, 64 * j, h, t0, b);
-            tma_prefetch_4d(&map_g, 64 * j, h, t0, b);
+            if (tile_group<ROLE>(T_Q) == g) tma_prefetch_4d(&map_q, 32 * j, h, t0, b);
+            if (tile_group<ROLE>(T_K) == g) tma_prefetch_4d(&map_k, 32 * j, h, t0, b);
+            if (tile_group<ROLE>(T_V) == g) tma_prefetch_4d(&map_v, 64 * j, h, t0, b);
+            if (tile_group<ROLE>(T_G) == g) tma_prefetch_4d(&map_g, 64 * j, h, t0, b);
           } else {
-            tma_load_4d(sb + OFF_Q + j * Q_BOX, &map_q, cta.bar(FULL), 32 * j, h, t0, b);
-            tma_load_4d(sb + OFF_K + j * Q_BOX, &map_k, cta.bar(FULL), 32 * j, h, t0, b);
-            if (ROLE != R_DV)
-              tma_load_4d(sb + OFF_V + j * V_BOX, &map_v, cta.bar(FULL), 64 * j, h, t0, b);
-            tma_load_4d(sb + OFF_G + j * V_BOX, &map_g, cta.bar(FULL), 64 * j, h, t0, b);
+            if (tile_group<ROLE>(T_Q) == g)
+              tma_load_4d(sb + OFF_Q + j * Q_BOX, &map_q, bar, 32 * j, h, t0, b);
+            if (tile_group<ROLE>(T_K) == g)
+              tma_load_4d(sb + OFF_K + j * Q_BOX, &map_k, bar, 32 * j, h, t0, b);
+            if (tile_group<ROLE>(T_V) == g)
+              tma_load_4d(sb + OFF_V + j * V_BOX, &map_v, bar, 64 * j, h, t0, b);
+            if (tile_group<ROLE>(T_G) == g)
+              tma_load_4d(sb + OFF_G + j * V_BOX, &map_g, bar, 64 * j, h, t0, b);
           }
         }
       };
-      int armed = 0;
+      int armed_e = 0, armed_l = 0;
       for (int t = 0; t < n; ++t) {
-        if (t >= 1 && !wait(cta, cta.bar(EMPTY), (t - 1) & 1, ctl)) break;
-        mbar_arrive_expect_tx(cta.bar(FULL), tile_bytes<ROLE>());
-        load(chunk_at<ROLE>(t, c0, n), false);
-        ++armed;
-        if (t + 1 < n) load(chunk_at<ROLE>(t + 1, c0, n), true);
+        const int c = chunk_at<ROLE>(t, c0, n);
+        if (t >= 1 && !wait(cta, cta.bar(EMPTY_E), (t - 1) & 1, ctl)) break;
+        mbar_arrive_expect_tx(cta.bar(FULL_E), group_bytes<ROLE>(0));
+        load(c, 0, false);
+        ++armed_e;
+        if (t >= 1 && !wait(cta, cta.bar(EMPTY_L), (t - 1) & 1, ctl)) break;
+        mbar_arrive_expect_tx(cta.bar(FULL_L), group_bytes<ROLE>(1));
+        load(c, 1, false);
+        ++armed_l;
+        if (t + 1 < n) {
+          load(chunk_at<ROLE>(t + 1, c0, n), 0, true);
+          load(chunk_at<ROLE>(t + 1, c0, n), 1, true);
+        }
       }
-      if (armed) mbar_wait(cta.bar(FULL), (armed - 1) & 1, ctl, DRAIN_NS);
+      if (armed_e) mbar_wait(cta.bar(FULL_E), (armed_e - 1) & 1, ctl, DRAIN_NS);
+      if (armed_l) mbar_wait(cta.bar(FULL_L), (armed_l - 1) & 1, ctl, DRAIN_NS);
     }
   } else if (warp == MMA_WARP) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       for (int t = 0; t < n; ++t) {
         const uint32_t par = t & 1;
-        if (!wait(cta, cta.bar(FULL), par, ctl)) break;
+        if (!wait(cta, cta.bar(FULL_E), par, ctl)) break;
+        // the previous chunk's TMEM-operand MMAs have read D_P
+        if (t >= 1 && !wait(cta, cta.bar(X_DONE), (t - 1) & 1, ctl)) break;
         tc_fence_after();
-        // score (inputs as given, bf16 or fp16)
+        // score (inputs as given, bf16 or fp16; early tiles)
         if constexpr (ROLE == R_DQ || ROLE == R_DK) {
           // DQ: dP = dO V^T (A = dO, B = V);  DK: dP^T = V dO^T (A = V, B = dO); K = 192
           constexpr uint32_t ID = idesc_f16(128, 128, BF16, BF16, false, false);
@@ -243,6 +286,7 @@ __device__ __forceinline__ void run_role(
         if (!wait(cta, cta.bar(EP_C1), par, ctl)) break;
         if (!wait(cta, cta.bar(EP_S), par, ctl)) break;
         if (t >= 1 && !wait(cta, cta.bar(EP_X), (t - 1) & 1, ctl)) break;
+        if (!wait(cta, cta.bar(FULL_L), par, ctl)) break;
         tc_fence_after();
         const uint32_t CP = sb + OFF_CP;
         if constexpr (ROLE == R_DQ) {
@@ -282,6 +326,8 @@ __device__ __forceinline__ void run_role(
             mma_f16_ss(tmem + TM_S, smem_desc(A + ks * 1024, Q_BOX, 512, SW_64),
                        smem_desc(B + ks * 2048, V_BOX, 1024, SW_128), ID, 1);
         }
+        mma_commit(cta.bar(EMPTY_E));  // the early tiles' last readers are the MMAs above
+        mma_commit(cta.bar(S_DONE));
         // ---- the masked scores are in TMEM (and DQ's r q in place)
         if (!wait(cta, cta.bar(EP_CONV), par, ctl)) break;
         tc_fence_after();
@@ -317,18 +363,17 @@ __device__ __forceinline__ void run_role(
             mma_f16_ss(tmem + TM_A, smem_desc(sb + OFF_Q + ks * 1024, Q_BOX, 512, SW_64),
                        smem_desc(sb + OFF_K + ks * 1024, Q_BOX, 512, SW_64), ID, (t > 0 || ks > 0));
         }
-        mma_commit(cta.bar(S_DONE));
-        mma_commit(cta.bar(EMPTY));
+        mma_commit(cta.bar(EMPTY_L));
       }
       mma_commit(cta.bar(DRAIN));
       mbar_wait(cta.bar(DRAIN), 0, ctl, DRAIN_NS);
     }
   } else {
-    // ------------------------------------------------------------------ epilogue warps 0..11
+    // ------------------------------------------------------------------ epilogue warps 0..15
     // Warp w serves rows 32q..32q+31 (q = w & 3, one row per thread = TMEM lane) and part
-    // sub = w >> 2 (0..2) of the work on each row: a third of the channels for the gate dot
-    // products and the in-place conversions, a third of the columns of the state copy and of
-    // the output rows.  The masked score copy (TMEM, in place) is done by part 0.
+    // sub = w >> 2 (0..3) of the work on each row: a quarter of the channels for the gate dot
+    // products and the in-place conversions, two of the eight 16-column score blocks, a quarter
+    // of the columns of the state copy and of the output rows.
     const int q4 = warp & 3, sub = warp >> 2;
     const int i = 32 * q4 + lane;
     const uint32_t trow = tmem + ((uint32_t)(32 * q4) << 16);
@@ -343,74 +388,64 @@ __device__ __forceinline__ void run_role(
     // and the last of the forward one
     const float dec_first =
         (ROLE == R_DQ ? c0 == nc - 1 : c0 + n == nc) ? lamL : lamC;  // step 0
-    // this warp's output staging, 4 KB: for q4 < 3 exactly the rows of the state copy that this
-    // warp itself writes (rows 32 q4.. of atom `sub`), so only its own stores must have read
-    // them before its next copy; the row quadrant 3 warps use the separate staging area
-    uint8_t* const stage = q4 < 3 ? base + OFF_CP + sub * S_ATOM + q4 * 4096
-                                  : base + OFF_STG + sub * 4096;
-    auto qk = [&](int cc) { return qk_chunk(i, 4 * sub + cc); };  // this part's q/k chunks
-    auto vg = [&](int cc) { return vg_chunk(i, 8 * sub + cc); };  // this part's v/dO chunks
+    uint8_t* const stage = base + OFF_STG + warp * 2048;  // two 1 KB output staging buffers
+    auto qk = [&](int cc) { return qk_chunk(i, 3 * sub + cc); };  // this part's q/k chunks
+    auto vg = [&](int cc) { return vg_chunk(i, 6 * sub + cc); };  // this part's v/dO chunks
     float range_max = 0.f;
     bool bad = false;
 
-    // state copy S * 2^-e (rows < 96, this part's 64 columns) into the copy buffer,
+    // state copy S * 2^-e (rows < 96, this part's 48 columns) into the copy buffer,
     // D_S <- dec S (dec = lambda^(tokens of the chunk whose update follows)), and this warp's
     // max|S| into red[use & 1]
     auto publish_state = [&](int use, int e, float dec, const float* g_row, bool from_tmem) {
       float m = 0.f;
       if (q4 < 3) {
         const float sc = pow2i(-e);
-        float r[32];
-#pragma unroll 1
-        for (int nb = 0; nb < 2; ++nb) {
-          const int col = 64 * sub + 32 * nb;
-          if (from_tmem) {
-            tmem_ld32(trow + TM_S + col, *reinterpret_cast<uint32_t(*)[32]>(r));
-            tmem_wait_ld();
-          } else {
+        const int col = 48 * sub;
+        uint32_t r[48];
+        if (from_tmem) {
+          tmem_ld32(trow + TM_S + col, *reinterpret_cast<uint32_t(*)[32]>(r));
+          tmem_ld16(trow + TM_S + col + 32, *reinterpret_cast<uint32_t(*)[16]>(r + 32));
+          tmem_wait_ld();
+        } else {
 #pragma unroll
-            for (int j4 = 0; j4 < 8; ++j4) {  // 8 loads in flight (rows are 16-byte aligned)
-              const float4 x = g_row ? __ldg(reinterpret_cast<const float4*>(g_row + col) + j4)
-                                     : make_float4(0.f, 0.f, 0.f, 0.f);
-              r[4 * j4] = x.x;
-              r[4 * j4 + 1] = x.y;
-              r[4 * j4 + 2] = x.z;
-              r[4 * j4 + 3] = x.w;
-            }
+          for (int j4 = 0; j4 < 12; ++j4) {  // 12 loads in flight (rows are 16-byte aligned)
+            const float4 x = g_row ? __ldg(reinterpret_cast<const float4*>(g_row + col) + j4)
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+            r[4 * j4] = __float_as_uint(x.x);
+            r[4 * j4 + 1] = __float_as_uint(x.y);
+            r[4 * j4 + 2] = __float_as_uint(x.z);
+            r[4 * j4 + 3] = __float_as_uint(x.w);
           }
-#pragma unroll
-          for (int q8 = 0; q8 < 4; ++q8) {
-            const int n = col + 8 * q8;
-            uint4 pk;
-            pk.x = pack_h2(r[8 * q8 + 0] * sc, r[8 * q8 + 1] * sc);
-            pk.y = pack_h2(r[8 * q8 + 2] * sc, r[8 * q8 + 3] * sc);
-            pk.z = pack_h2(r[8 * q8 + 4] * sc, r[8 * q8 + 5] * sc);
-            pk.w = pack_h2(r[8 * q8 + 6] * sc, r[8 * q8 + 7] * sc);
-            *(uint4*)(base + OFF_CP + (n >> 6) * S_ATOM + swz_off(i, (n & 63) >> 3, 128)) = pk;
-          }
-          uint32_t u[32];
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            m = fmaxf(m, fabsf(r[j]));
-            u[j] = __float_as_uint(r[j] * dec);
-          }
-          tmem_st32(trow + TM_S + col, u);
         }
+#pragma unroll
+        for (int q8 = 0; q8 < 6; ++q8) {
+          const int nn = col + 8 * q8;
+          const float* f = reinterpret_cast<const float*>(r + 8 * q8);
+          uint4 pk;
+          pk.x = pack_h2(f[0] * sc, f[1] * sc);
+          pk.y = pack_h2(f[2] * sc, f[3] * sc);
+          pk.z = pack_h2(f[4] * sc, f[5] * sc);
+          pk.w = pack_h2(f[6] * sc, f[7] * sc);
+          *(uint4*)(base + OFF_CP + (nn >> 6) * S_ATOM + swz_off(i, (nn & 63) >> 3, 128)) = pk;
+        }
+#pragma unroll
+        for (int j = 0; j < 48; ++j) {
+          const float x = __uint_as_float(r[j]);
+          m = fmaxf(m, fabsf(x));
+          r[j] = __float_as_uint(x * dec);
+        }
+        tmem_st32(trow + TM_S + col, *reinterpret_cast<uint32_t(*)[32]>(r));
+        tmem_st16(trow + TM_S + col + 32, *reinterpret_cast<uint32_t(*)[16]>(r + 32));
         tmem_wait_st();
       }
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-      if (lane == 0) red[(use & 1) * 12 + warp] = m;
+      if (lane == 0) red[(use & 1) * 16 + warp] = m;
       if (tid == 0) es[use & 1] = e;
       fence_proxy_async();
       tc_fence_before();
       mbar_arrive(cta.bar(EP_S));
-    };
-    auto max12 = [&](const float* v) {
-      float m = v[0];
-#pragma unroll
-      for (int w = 1; w < 12; ++w) m = fmaxf(m, v[w]);
-      return m;
     };
 
     // starting state (DQ) or adjoint (DV, DK): the caller's initial state / d_final_state for
@@ -423,21 +458,21 @@ __device__ __forceinline__ void run_role(
     {
       float m = 0.f;
       if (g_row0) {
-        const float4* g4 = reinterpret_cast<const float4*>(g_row0 + 64 * sub);
+        const float4* g4 = reinterpret_cast<const float4*>(g_row0 + 48 * sub);
 #pragma unroll
-        for (int j4 = 0; j4 < 16; ++j4) {
+        for (int j4 = 0; j4 < 12; ++j4) {
           const float4 x = __ldg(g4 + j4);
           m = fmaxf(m, fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w))));
         }
       }
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-      if (lane == 0) red[24 + warp] = m;
+      if (lane == 0) red[32 + warp] = m;
       mbar_arrive(cta.bar(RED));
     }
     bool ok = wait(cta, cta.bar(RED), 0, ctl);
     if (ok) {
-      e_cur = state_exponent(max12(red + 24));
+      e_cur = state_exponent(max16(red + 32));
       if (e_cur < 0) {
         bad = true;
         e_cur = 0;
@@ -445,11 +480,11 @@ __device__ __forceinline__ void run_role(
       publish_state(0, e_cur, dec_first, g_row0, false);
     }
 
-    // in-register fp16 copy of four q/k chunks of this part (x: 16-bit input words), scaled
+    // in-register fp16 copy of three q/k chunks of this part (x: 16-bit input words), scaled
     // by s and stored back in place
-    auto cvt4 = [&](uint4 (&x)[4], uint32_t tile_off, float s, float& vmax) {
+    auto cvt3 = [&](uint4 (&x)[3], uint32_t tile_off, float s, float& vmax) {
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
+      for (int cc = 0; cc < 3; ++cc) {
         uint32_t* w = reinterpret_cast<uint32_t*>(&x[cc]);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -465,26 +500,27 @@ __device__ __forceinline__ void run_role(
       const uint32_t par = t & 1;
       const int c = chunk_at<ROLE>(t, c0, n);
       const float lk = c == nc - 1 ? lk_last : lk_full;
-      if (!(ok = wait(cta, cta.bar(FULL), par, ctl))) break;
-      // ---- gate partial sum z = q.(a*k) over this part's 32 channels, fused with the fp16
+      if (!(ok = wait(cta, cta.bar(FULL_E), par, ctl))) break;
+      if (!(ok = wait(cta, cta.bar(FULL_L), par, ctl))) break;
+      // ---- gate partial sum z = q.(a*k) over this part's 24 channels, fused with the fp16
       // copy of whichever of q, k the score MMA does not read (DQ: k, DK: q, both scale 1);
       // DV's score reads both, so DV converts them once the score MMA is done
       float amax = 0.f, bmax = 0.f;  // A and B operands of the state MMA
-      uint4 xq[4], xk[4];
+      uint4 xq[3], xk[3];
       {
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
+        for (int cc = 0; cc < 3; ++cc) {
           xq[cc] = *(const uint4*)(base + OFF_Q + qk(cc));
           xk[cc] = *(const uint4*)(base + OFF_K + qk(cc));
         }
         float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
+        for (int cc = 0; cc < 3; ++cc) {
           const uint32_t* xw = reinterpret_cast<const uint32_t*>(&xq[cc]);
           const uint32_t* yw = reinterpret_cast<const uint32_t*>(&xk[cc]);
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const int d = 32 * sub + 8 * cc + 2 * e;
+            const int d = 24 * sub + 8 * cc + 2 * e;
             acc0 = fmaf(ld16<BF16>(xw[e] & 0xFFFFu) * sa[d], ld16<BF16>(yw[e] & 0xFFFFu), acc0);
             acc1 = fmaf(ld16<BF16>(xw[e] >> 16) * sa[d + 1], ld16<BF16>(yw[e] >> 16), acc1);
           }
@@ -492,21 +528,21 @@ __device__ __forceinline__ void run_role(
         gate_part[sub * 128 + i] = acc0 + acc1;
         mbar_arrive(cta.bar(QG0 + q4));
       }
-      if constexpr (ROLE == R_DQ) cvt4(xk, OFF_K, 1.f, amax);  // K (state A, dP''K B)
-      if constexpr (ROLE == R_DK) cvt4(xq, OFF_Q, 1.f, amax);  // Q (adjoint A, dP''^T Q B)
-      if constexpr (ROLE == R_DV) convert_row<BF16, 8>(base + OFF_G, vg, 1.f, bmax);  // dO
+      if constexpr (ROLE == R_DQ) cvt3(xk, OFF_K, 1.f, amax);  // K (state A, dP''K B)
+      if constexpr (ROLE == R_DK) cvt3(xq, OFF_Q, 1.f, amax);  // Q (adjoint A, dP''^T Q B)
+      if constexpr (ROLE == R_DV) convert_row<BF16, 6, 3>(base + OFF_G, vg, 1.f, bmax);  // dO
       // ---- once the score MMA has read its 16-bit tiles: their fp16 copies
       if (!(ok = wait(cta, cta.bar(P_DONE), par, ctl))) break;
       tc_fence_after();
       if constexpr (ROLE == R_DQ) {
-        convert_row<BF16, 8>(base + OFF_V, vg, lk, bmax);       // V' (state B)
-        convert_row<BF16, 8>(base + OFF_G, vg, lq, range_max);  // dO'' (A of dO'' S^T)
+        convert_row<BF16, 6, 3>(base + OFF_V, vg, lk, bmax);       // V' (state B)
+        convert_row<BF16, 6, 3>(base + OFF_G, vg, lq, range_max);  // dO'' (A of dO'' S^T)
       } else if constexpr (ROLE == R_DV) {
-        convert_row<BF16, 4>(base + OFF_Q, qk, lq, amax);       // Q'' (adjoint A)
-        convert_row<BF16, 4>(base + OFF_K, qk, lk, range_max);  // K' (A of K' dS)
+        convert_row<BF16, 3, 3>(base + OFF_Q, qk, lq, amax);       // Q'' (adjoint A)
+        convert_row<BF16, 3, 3>(base + OFF_K, qk, lk, range_max);  // K' (A of K' dS)
       } else {
-        convert_row<BF16, 8>(base + OFF_V, vg, lk, range_max);  // V' (A of V' dS^T)
-        convert_row<BF16, 8>(base + OFF_G, vg, lq, bmax);       // dO'' (adjoint B)
+        convert_row<BF16, 6, 3>(base + OFF_V, vg, lk, range_max);  // V' (A of V' dS^T)
+        convert_row<BF16, 6, 3>(base + OFF_G, vg, lq, bmax);       // dO'' (adjoint B)
       }
       // every fp16 operand but DQ's r q is in place: the state MMA and the output MMA's
       // state-copy part may run while the masked scores are made
@@ -521,54 +557,55 @@ __device__ __forceinline__ void run_role(
           bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, off));
         }
         if (lane == 0) {
-          abmax[par * 24 + warp] = am;
-          abmax[par * 24 + 12 + warp] = bm;
+          abmax[par * 32 + warp] = am;
+          abmax[par * 32 + 16 + warp] = bm;
         }
       }
-      // ---- the row's gate: the three partial sums
+      // ---- the row's gate: the four partial sums
       if (!(ok = wait(cta, cta.bar(QG0 + q4), par, ctl))) break;
-      const float sg = sigmoid(gate_part[i] + gate_part[128 + i] + gate_part[256 + i]);
+      const float sg =
+          sigmoid((gate_part[i] + gate_part[128 + i]) + (gate_part[256 + i] + gate_part[384 + i]));
       // ---- masked score copy, scaled by 2^-e of this step's state copy: this part's 16-column
-      // blocks hb = sub, sub+3, sub+6 of the quadrant's rows, packed to fp16 pairs in registers.
+      // blocks hb = sub, sub+4 of the quadrant's rows, packed to fp16 pairs in registers.
       // Block hb's pairs go to 32-bit columns 8hb..8hb+7, inside block hb/2's fp32 columns, so
-      // the three parts of a quadrant finish reading before any of them writes.
+      // the four parts of a quadrant finish reading before any of them writes.
       if (!(ok = wait(cta, cta.bar(EP_S), par, ctl))) break;
       {
         const float psc = pow2i(-es[par]);
         float pmax = 0.f;
-        uint32_t pk[3][8];
+        uint32_t pk[2][8];
 #pragma unroll
-        for (int m = 0; m < 3; ++m) {
-          const int hb = sub + 3 * m;
-          const int c0 = 16 * hb;
+        for (int m = 0; m < 2; ++m) {
+          const int hb = sub + 4 * m;
+          const int cb = 16 * hb;
           // DQ keeps columns j <= i (rows = queries i), DV and DK columns i >= j (rows = keys j)
-          const bool live = hb < 8 && (ROLE == R_DQ ? hb <= 2 * q4 + 1 : hb >= 2 * q4);
+          const bool live = ROLE == R_DQ ? hb <= 2 * q4 + 1 : hb >= 2 * q4;
           float sc[16];
           if (live) {
             uint32_t r[16];
-            tmem_ld16(trow + TM_P + c0, r);
+            tmem_ld16(trow + TM_P + cb, r);
             tmem_wait_ld();
             float dg = 0.f;
             if constexpr (ROLE == R_DQ) {
-              float f = pw[max(i - (c0 + 15), 0)] * psc;  // going left from min(i, c0+15)
+              float f = pw[max(i - (cb + 15), 0)] * psc;  // going left from min(i, cb+15)
 #pragma unroll
               for (int u = 15; u >= 0; --u) {
-                const bool in = c0 + u <= i;
+                const bool in = cb + u <= i;
                 sc[u] = in ? __uint_as_float(r[u]) * f : 0.f;
                 f = in ? f * lam : f;
-                dg = (c0 + u == i) ? __uint_as_float(r[u]) : dg;
+                dg = (cb + u == i) ? __uint_as_float(r[u]) : dg;
               }
             } else {
-              float f = pw[max(c0 - i, 0)] * psc;  // going right from max(j, c0)
+              float f = pw[max(cb - i, 0)] * psc;  // going right from max(j, cb)
 #pragma unroll
               for (int u = 0; u < 16; ++u) {
-                const bool in = c0 + u >= i;
+                const bool in = cb + u >= i;
                 sc[u] = in ? __uint_as_float(r[u]) * f : 0.f;
                 f = in ? f * lam : f;
-                dg = (c0 + u == i) ? __uint_as_float(r[u]) : dg;
+                dg = (cb + u == i) ? __uint_as_float(r[u]) : dg;
                 // DV: the self-augmentation sigmoid(z_j) dO_j rides on the diagonal, so that
                 // P''^T dO includes it: (P^T + diag(sigmoid(z))) 2^-e
-                if (ROLE == R_DV && c0 + u == i) sc[u] += sg * psc;
+                if (ROLE == R_DV && cb + u == i) sc[u] += sg * psc;
               }
             }
             // DQ, DK: the score's diagonal is dO_i . v_i, the gate's other factor
@@ -589,66 +626,27 @@ __device__ __forceinline__ void run_role(
         if (!(ok = wait(cta, cta.bar(QS0 + q4), par, ctl))) break;
         tc_fence_after();
 #pragma unroll
-        for (int m = 0; m < 3; ++m)
-          if (sub + 3 * m < 8) tmem_st8(trow + TM_P + 8 * (sub + 3 * m), pk[m]);
+        for (int m = 0; m < 2; ++m) tmem_st8(trow + TM_P + 8 * (sub + 4 * m), pk[m]);
         tmem_wait_st();
       }
       float rr = 0.f;  // r = sigmoid'(z) (dO.v) (DQ, DK)
       if constexpr (ROLE != R_DV) rr = sg * (1.f - sg) * dpv[i];
-      if constexpr (ROLE == R_DQ) convert_row<BF16, 4>(base + OFF_Q, qk, rr, range_max);  // r q
+      if constexpr (ROLE == R_DQ) convert_row<BF16, 3, 3>(base + OFF_Q, qk, rr, range_max);  // r q
       fence_proxy_async();
       tc_fence_before();
       mbar_arrive(cta.bar(EP_CONV));
-
-      // ---- output MMAs done: take the self-augmentation operand (DQ: k, DK: q, this part's 32
-      // channels) and release the tiles (the state MMA's commit completes the release), so the
-      // next chunk's loads overlap the rest of this step.  DV's term is inside D_X already.
-      if (!(ok = wait(cta, cta.bar(X_DONE), par, ctl))) break;
-      tc_fence_after();
-      uint4 vv[4];
+      // ---- the self-augmentation operand of the rows (DQ: k, DK: q, this part's 24 channels,
+      // fp16) into registers; then this warp is done with the late tiles.  DV's term is inside
+      // D_X already.
+      uint4 vv[3];
       if constexpr (ROLE != R_DV) {
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch) vv[ch] = *(const uint4*)(base + (ROLE == R_DQ ? OFF_K : OFF_Q) + qk(ch));
+        for (int ch = 0; ch < 3; ++ch)
+          vv[ch] = *(const uint4*)(base + (ROLE == R_DQ ? OFF_K : OFF_Q) + qk(ch));
       }
-      mbar_arrive(cta.bar(EMPTY));
-      // ---- output rows, this part's columns: x = 2^e D_X (+ r (a * k|q) for DQ, DK), while
-      // the state MMA runs
-      if (lane == 0) bulk_wait_read<0>();  // the staging buffer is free again
-      __syncwarp();
-      {
-        const float osc = pow2i(e_cur);
-        const int t0 = c * C + 32 * q4;  // first token of this warp's rows (boxes past T: none)
-        constexpr int NCOL = NX / 3;  // 32 (DQ, DK) or 64 (DV)
-        uint32_t rbuf[2][16];  // blocks read in pairs: one TMEM round trip per two blocks
-        emit_rows_tma<NCOL / 16>(
-            stage, lane,
-            [&](int k, float (&x)[16]) {
-              const int col = NCOL * sub + 16 * k;
-              if ((k & 1) == 0) {
-                tmem_ld16(trow + TM_X + col, rbuf[0]);
-                if (k + 1 < NCOL / 16) tmem_ld16(trow + TM_X + col + 16, rbuf[1]);
-                tmem_wait_ld();
-              }
-              const uint32_t (&r)[16] = rbuf[k & 1];
-              if constexpr (ROLE == R_DV) {
-#pragma unroll
-                for (int j = 0; j < 16; ++j) x[j] = __uint_as_float(r[j]) * osc;
-              } else {
-                float f8[2][8];
-                unpack8<false>(vv[2 * k], f8[0]);
-                unpack8<false>(vv[2 * k + 1], f8[1]);
-#pragma unroll
-                for (int j = 0; j < 16; ++j)
-                  x[j] = fmaf(__uint_as_float(r[j]), osc, rr * sa[col + j] * f8[j >> 3][j & 7]);
-              }
-            },
-            [&](int k, uint32_t src) {
-              if (t0 < T) tma_store_4d(&map_out, src, NCOL * sub + 16 * k, h, t0, b);
-            });
-      }
-      tc_fence_before();
-      mbar_arrive(cta.bar(EP_X));
-      // ---- the state MMA ran: next state copy (the serial step)
+      mbar_arrive(cta.bar(EMPTY_L));
+      // ---- the state update ran: next state copy (the serial step), while the output MMA's
+      // TMEM-operand part runs
       if (!(ok = wait(cta, cta.bar(S_DONE), par, ctl))) break;
       tc_fence_after();
       int e_next = e_cur;
@@ -656,38 +654,76 @@ __device__ __forceinline__ void run_role(
         // bound on the next state: all parts' operand maxima and max|S| of this step's copy
         // (decayed by this step's factor)
         if (!(ok = wait(cta, cta.bar(EP_CONV), par, ctl))) break;
-        e_next = state_exponent((t == 0 ? dec_first : lamC) * max12(red + par * 12) +
-                                (float)C * max12(abmax + par * 24) * max12(abmax + par * 24 + 12));
+        e_next = state_exponent((t == 0 ? dec_first : lamC) * max16(red + par * 16) +
+                                (float)C * max16(abmax + par * 32) * max16(abmax + par * 32 + 16));
         if (e_next < 0) {
           bad = true;
           e_next = 0;
         }
-        // the output rows' stores have read this warp's staging, which the copy overwrites
-        if (lane == 0) bulk_wait_read<0>();
-        __syncwarp();
         publish_state(t + 1, e_next, (ROLE == R_DQ && c0 + t + 2 == nc) ? lamL : lamC, nullptr,
                       true);
       }
+      // ---- output rows, this part's columns: x = 2^e D_X (+ r (a * k|q) for DQ, DK)
+      if (!(ok = wait(cta, cta.bar(X_DONE), par, ctl))) break;
+      tc_fence_after();
+      if (lane == 0) bulk_wait_read<0>();  // the staging buffers are free again
+      __syncwarp();
+      {
+        const float osc = pow2i(e_cur);
+        const int t0 = c * C + 32 * q4;  // first token of this warp's rows (boxes past T: none)
+        constexpr int NCOL = NX / 4;  // 24 (DQ, DK) or 48 (DV)
+        uint32_t rbuf[16];  // blocks read in pairs: one TMEM round trip per two blocks
+        emit_rows8_tma<NCOL / 8>(
+            stage, lane,
+            [&](int k, float (&x)[8]) {
+              const int col = NCOL * sub + 8 * k;
+              if ((k & 1) == 0) {
+                if (k + 1 < NCOL / 8)
+                  tmem_ld16(trow + TM_X + col, rbuf);
+                else
+                  tmem_ld8(trow + TM_X + col, *reinterpret_cast<uint32_t(*)[8]>(rbuf));
+                tmem_wait_ld();
+              }
+              const uint32_t* r = rbuf + 8 * (k & 1);
+              if constexpr (ROLE == R_DV) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) x[j] = __uint_as_float(r[j]) * osc;
+              } else {
+                float f8[8];
+                unpack8<false>(vv[k], f8);
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                  x[j] = fmaf(__uint_as_float(r[j]), osc, rr * sa[col + j] * f8[j]);
+              }
+            },
+            [&](int k, uint32_t src) {
+              if (t0 < T) tma_store_4d(&map_out, src, NCOL * sub + 8 * k, h, t0, b);
+            });
+      }
+      tc_fence_before();
+      mbar_arrive(cta.bar(EP_X));
       // ---- adjoint of the initial state (DV, after the last step = chunk 0)
       if (ROLE == R_DV && t == n - 1 && c0 == 0 && p.want_dinit && q4 < 3) {
         if (lane == 0) bulk_wait_read<0>();
         __syncwarp();
-        emit_rows_tma<4>(
+        uint32_t rb[16];
+        emit_rows8_tma<6>(
             stage, lane,
-            [&](int k, float (&f)[16]) {
-              uint32_t r[16];
-              tmem_ld16(trow + TM_S + 64 * sub + 16 * k, r);
-              tmem_wait_ld();
+            [&](int k, float (&f)[8]) {
+              if ((k & 1) == 0) {
+                tmem_ld16(trow + TM_S + 48 * sub + 8 * k, rb);
+                tmem_wait_ld();
+              }
 #pragma unroll
-              for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(r[j]);
+              for (int j = 0; j < 8; ++j) f[j] = __uint_as_float(rb[8 * (k & 1) + j]);
             },
-            [&](int k, uint32_t src) { tma_store_3d(&map_dinit, src, 64 * sub + 16 * k, 32 * q4, bh); });
+            [&](int k, uint32_t src) { tma_store_3d(&map_dinit, src, 48 * sub + 8 * k, 32 * q4, bh); });
       }
       e_cur = e_next;
     }
     // DQ: d_a of this (b, h) is the diagonal of the accumulated (r q)^T k; row d (lane of
-    // quadrant d / 32) takes column d
-    if (ROLE == R_DQ && ok && sub == 0 && q4 < 3) {
+    // quadrant d / 32) takes column d, once the last step's d_a MMAs are done
+    if (ROLE == R_DQ && ok && sub == 0 && q4 < 3 && wait(cta, cta.bar(EMPTY_L), (n - 1) & 1, ctl)) {
       tc_fence_after();
       uint32_t r[32];
       tmem_ld32(trow + TM_A + 32 * q4, r);
@@ -778,11 +814,11 @@ cudaError_t launch_chunk_bwd(const BwdArgs& a, DevCtl ctl, cudaStream_t stream) 
       !make_tmap_seq_16bit(&mk, a.k, DK, a.H, a.T, a.B, 32, C, CU_TENSOR_MAP_SWIZZLE_64B, a.bf16) ||
       !make_tmap_seq_16bit(&mv, a.v, DV, a.H, a.T, a.B, 64, C, CU_TENSOR_MAP_SWIZZLE_128B, a.bf16) ||
       !make_tmap_seq_16bit(&mg, a.dO, DV, a.H, a.T, a.B, 64, C, CU_TENSOR_MAP_SWIZZLE_128B, a.bf16) ||
-      !make_tmap_seq_out_f32(&mdq, a.dq, DK, a.H, a.T, a.B) ||
-      !make_tmap_seq_out_f32(&mdk, a.dk, DK, a.H, a.T, a.B) ||
-      !make_tmap_seq_out_f32(&mdv, a.dv, DV, a.H, a.T, a.B) ||
+      !make_tmap_seq_out_f32(&mdq, a.dq, DK, a.H, a.T, a.B, 8) ||
+      !make_tmap_seq_out_f32(&mdk, a.dk, DK, a.H, a.T, a.B, 8) ||
+      !make_tmap_seq_out_f32(&mdv, a.dv, DV, a.H, a.T, a.B, 8) ||
       !make_tmap_state_f32(&mdi, a.dinit ? (const void*)a.dinit : (const void*)a.dv,
-                           (long long)a.B * a.H))
+                           (long long)a.B * a.H, 8))
     return cudaErrorInvalidValue;
   BwdParams p;
   p.log_decay = a.log_decay;

@@ -86,19 +86,19 @@ __device__ __forceinline__ void scale_chunk_to_half(uint4* p, float s, float& vm
   *p = x;
 }
 
-// Convert NCH 16-byte chunks of one tile row in place (scale s, to fp16), four chunks at a
+// Convert NCH 16-byte chunks of one tile row in place (scale s, to fp16), G chunks at a
 // time with their loads issued together so that the shared-memory latency overlaps.
 // `off(c)` is the byte offset of chunk c.
-template <bool SRC_BF16, int NCH, typename Off>
+template <bool SRC_BF16, int NCH, int G = 4, typename Off>
 __device__ __forceinline__ void convert_row(uint8_t* tile, Off off, float s, float& vmax) {
-  static_assert(NCH % 4 == 0, "chunks in groups of four");
-#pragma unroll 1  // batches of four chunks; a rolled loop keeps the code small
-  for (int c0 = 0; c0 < NCH; c0 += 4) {
-    uint4 x[4];
+  static_assert(NCH % G == 0, "whole batches of chunks");
+#pragma unroll 1  // batches of G chunks; a rolled loop keeps the code small
+  for (int c0 = 0; c0 < NCH; c0 += G) {
+    uint4 x[G];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) x[u] = *(const uint4*)(tile + off(c0 + u));
+    for (int u = 0; u < G; ++u) x[u] = *(const uint4*)(tile + off(c0 + u));
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < G; ++u) {
       uint32_t* w = reinterpret_cast<uint32_t*>(&x[u]);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -108,7 +108,7 @@ __device__ __forceinline__ void convert_row(uint8_t* tile, Off off, float s, flo
       }
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u) *(uint4*)(tile + off(c0 + u)) = x[u];
+    for (int u = 0; u < G; ++u) *(uint4*)(tile + off(c0 + u)) = x[u];
   }
 }
 
@@ -185,6 +185,36 @@ __device__ __forceinline__ void emit_rows_tma(uint8_t* buf0, int lane, Produce p
       __syncwarp();
     }
     stage_rows16_sw64(buf, r, lane);
+    fence_proxy_async();
+    __syncwarp();
+    if (lane == 0) {
+      store(k, smem_u32(buf));
+      bulk_commit();
+    }
+  }
+}
+
+// Emit a warp's 32 rows x (8 * NBLK8) fp32 columns, produced block by block by
+// `produce(k, r)` (8 columns of block k), through two 1 KB staging buffers (`buf0`,
+// `buf0 + 1024`) and TMA stores of 32-byte-swizzled boxes {8, 1, 32}: row rr at rr * 32
+// bytes, its two 16-byte chunks exchanged when bit 2 of rr is set.  `buf0` must be 256-byte
+// aligned.  Called by all 32 lanes; lane 0 issues the stores.
+template <int NBLK8, typename Produce, typename Store>
+__device__ __forceinline__ void emit_rows8_tma(uint8_t* buf0, int lane, Produce produce,
+                                               Store store) {
+#pragma unroll
+  for (int k = 0; k < NBLK8; ++k) {
+    uint8_t* buf = buf0 + (k & 1) * 1024;
+    float r[8];
+    produce(k, r);
+    if (k >= 2) {  // the store that last read this buffer must have finished reading it
+      if (lane == 0) bulk_wait_read<1>();
+      __syncwarp();
+    }
+    const int sw = (lane >> 2) & 1;
+    *reinterpret_cast<float4*>(buf + lane * 32 + (sw << 4)) = make_float4(r[0], r[1], r[2], r[3]);
+    *reinterpret_cast<float4*>(buf + lane * 32 + ((sw ^ 1) << 4)) =
+        make_float4(r[4], r[5], r[6], r[7]);
     fence_proxy_async();
     __syncwarp();
     if (lane == 0) {

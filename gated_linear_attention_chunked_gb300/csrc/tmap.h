@@ -42,17 +42,20 @@ inline bool make_tmap_seq_16bit(CUtensorMap* map, const void* base, int d, int H
 }
 
 // fp32 token-major output [B, T, H, d] as 4-D {d, H, T, B}, stored from shared memory in boxes
-// of 16 channels x 32 consecutive tokens of one head (64-byte rows, 64-byte swizzle); rows past
-// the sequence's T tokens are not written.
-inline bool make_tmap_seq_out_f32(CUtensorMap* map, const void* base, int d, int H, int T, int B) {
+// of `box_d` (16 or 8) channels x 32 consecutive tokens of one head (64-byte rows with a 64-byte
+// swizzle, or 32-byte rows with a 32-byte swizzle); rows past the sequence's T tokens are not
+// written.
+inline bool make_tmap_seq_out_f32(CUtensorMap* map, const void* base, int d, int H, int T, int B,
+                                  int box_d = 16) {
   auto fn = encode_tiled_fn();
   if (!fn) return false;
   cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
   cuuint64_t strides[3] = {(cuuint64_t)d * 4, (cuuint64_t)d * 4 * H, (cuuint64_t)d * 4 * H * T};
-  cuuint32_t box[4] = {16u, 1u, 32u, 1u};
+  cuuint32_t box[4] = {(cuuint32_t)box_d, 1u, 32u, 1u};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void*>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            box_d == 8 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -71,13 +74,14 @@ inline bool make_tmap_3d(CUtensorMap* map, const void* base, CUtensorMapDataType
          CUDA_SUCCESS;
 }
 
-// fp32 states [BH, 96, 192] stored in boxes of 16 value channels x 32 key channels.
-inline bool make_tmap_state_f32(CUtensorMap* map, const void* base, long long bh) {
+// fp32 states [BH, 96, 192] stored in boxes of `box_c` (16 or 8) value channels x 32 key
+// channels (64- or 32-byte swizzle, as the output maps).
+inline bool make_tmap_state_f32(CUtensorMap* map, const void* base, long long bh, int box_c = 16) {
   const unsigned long long dims[3] = {192, 96, (unsigned long long)bh};
   const unsigned long long strides[2] = {192 * 4, 192 * 96 * 4};
-  const unsigned box[3] = {16, 32, 1};
+  const unsigned box[3] = {(unsigned)box_c, 32, 1};
   return make_tmap_3d(map, base, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dims, strides, box,
-                      CU_TENSOR_MAP_SWIZZLE_64B);
+                      box_c == 8 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 }  // namespace gla
