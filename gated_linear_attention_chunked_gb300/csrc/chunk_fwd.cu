@@ -7,21 +7,22 @@
 //   S_{c+1} = lambda^C S_c + K^T Lk V                        (the only serial step)
 //
 // One CTA owns one (b, h) and walks its chunks in order; the fp32 state never leaves the chip.
-//   warp 12     TMA producer: q, k tiles (3 boxes of 32 channels, 64-byte swizzle) and v tiles
+//   warp 16     TMA producer: q, k tiles (3 boxes of 32 channels, 64-byte swizzle) and v tiles
 //               (3 boxes of 64 channels, 128-byte swizzle) into a 2-stage ring (no L2
 //               prefetch: measured, it slowed the loads it was meant to hide).
-//   warp 13     tcgen05 issuer (one thread) and TMEM owner (512 columns):
+//   warp 17     tcgen05 issuer (one thread) and TMEM owner (512 columns):
 //                 D_P [384,512)  P = Q K^T (bf16/fp16 inputs as given); the masked fp16
 //                                copy P'' is written back in place (64 columns) and read
 //                                from TMEM as the A operand of P'' V
 //                 D_O [  0,192)  O = Q'' S_c + P'' V           (fp16 operands)
 //                 D_S [192,384)  S = lambda^C S + K'^T V       (fp16 operands, fp32 state;
 //                                rows 96..127 are padding and never read)
-//   warps 0..3  convert group, thread = token row i (= TMEM lane), one chunk ahead of the
+//   warps 0..7  convert group, thread = token row i (= TMEM lane), two warps per row
+//               quadrant splitting the channels and score blocks, one chunk ahead of the
 //               emit group: V -> fp16 in place; z = q.(a*k); Q'' = fp16(lambda^(i+1) q) and
 //               K' = fp16(lambda^(127-i) k) in place; P'' = fp16((mask(P) + diag(sigmoid(z)))
 //               * 2^-e) into TMEM -- the self-augmentation rides on the diagonal of P''.
-//   warps 4..11 emit group, same rows, two warps per row quadrant splitting the value
+//   warps 8..15 emit group, same rows, two warps per row quadrant splitting the value
 //               columns: (1) the serial step -- S -> fp16(S * 2^-e') into the drained q/k
 //               slot (B operand of the next Q'' S) and D_S <- lambda^C D_S; (2) the output rows
 //               o = 2^e D_O as fp32, TMA-stored from per-warp staging.
@@ -50,16 +51,17 @@ constexpr uint32_t STAGE = OFF_V + 3 * V_BOX;  // 98304
 constexpr uint32_t OFF_STG = 2 * STAGE;        // output staging, 8 emit warps x 4 KB
 constexpr uint32_t S_ATOM = 12288;             // state copy: 3 atoms of 96 rows x 128 B
 constexpr uint32_t OFF_BAR = OFF_STG + 8 * 4096;
-constexpr uint32_t NBAR = 24;
+constexpr uint32_t NBAR = 32;
 constexpr uint32_t OFF_TMEM = OFF_BAR + NBAR * 8;
 constexpr uint32_t OFF_ABORT = OFF_TMEM + 4;
 constexpr uint32_t OFF_RED = OFF_TMEM + 16;     // float red[3][8]: per-warp max|S|
 constexpr uint32_t OFF_ES = OFF_RED + 96;       // int es[2]: state-copy exponent per chunk parity
-constexpr uint32_t OFF_KV = OFF_ES + 16;        // float kvmax[2][8]: per-warp max|K'|, max|V|
-constexpr uint32_t OFF_A = OFF_KV + 64;         // float a[96]: aug_balance of the head
+constexpr uint32_t OFF_KV = OFF_ES + 16;        // float kvmax[2][16]: per-warp max|K'|, max|V|
+constexpr uint32_t OFF_A = OFF_KV + 128;        // float a[96]: aug_balance of the head
 constexpr uint32_t OFF_PW = OFF_A + 384;        // float pw[128] = lambda^d
 constexpr uint32_t OFF_XCH = OFF_PW + 512;      // float xch[2][128]: row sums of o^2 (gated)
-constexpr uint32_t SMEM_USED = OFF_XCH + 1024;
+constexpr uint32_t OFF_ZX = OFF_XCH + 1024;     // float zx[128]: second-half gate partial sums
+constexpr uint32_t SMEM_USED = OFF_ZX + 512;
 // The whole opt-in maximum is requested; the kernel aligns its base to 1024 bytes and
 // refuses to run (GLA_ERR_LAYOUT, before touching shared memory) if the padding that
 // takes would not fit.  The dynamic shared window normally starts 1024-aligned.
@@ -85,11 +87,14 @@ enum Bar : uint32_t {
   RED = 15,  // exchange of the per-warp max|S| inside the emit group
   QX = 16,   // 16..19 (gated output): the two warps of row quadrant q have their row sums
   EP_Q = 20,  // convert group: Q'' of the chunk is in place (the Q''S MMA may start)
+  ZX0 = 24,   // 24..27: quadrant q's second convert warp has written its gate partial sums
+  QS0 = 28,   // 28..31: both convert warps of quadrant q have read their score blocks
 };
 
-constexpr int THREADS = 448;
-constexpr int PRODUCER_WARP = 12, MMA_WARP = 13;
-constexpr int EMIT_THREADS = 256;  // warps 4..11
+constexpr int THREADS = 576;
+constexpr int PRODUCER_WARP = 16, MMA_WARP = 17;
+constexpr int CONVERT_THREADS = 256;  // warps 0..7
+constexpr int EMIT_THREADS = 256;     // warps 8..15
 
 template <bool BF16, bool GATED>
 __global__ void __launch_bounds__(THREADS, 1)
@@ -144,12 +149,16 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
     mbar_init(cta.bar(O_DONE), 1);
     mbar_init(cta.bar(S_DONE), 1);
     mbar_init(cta.bar(DRAIN), 1);
-    mbar_init(cta.bar(EP_CONV), 128);           // convert group
-    mbar_init(cta.bar(EP_Q), 128);              // convert group
+    mbar_init(cta.bar(EP_CONV), CONVERT_THREADS);
+    mbar_init(cta.bar(EP_Q), CONVERT_THREADS);
     mbar_init(cta.bar(EP_O), EMIT_THREADS);     // emit group
     mbar_init(cta.bar(EP_S), EMIT_THREADS);     // emit group
     mbar_init(cta.bar(RED), EMIT_THREADS);      // emit group
-    for (int q = 0; q < 4; ++q) mbar_init(cta.bar(QX + q), 64);
+    for (int q = 0; q < 4; ++q) {
+      mbar_init(cta.bar(QX + q), 64);
+      mbar_init(cta.bar(ZX0 + q), 32);
+      mbar_init(cta.bar(QS0 + q), 64);
+    }
     *cta.abort_flag() = 0;
     fence_barrier_init();
   }
@@ -243,16 +252,29 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
       mma_commit(cta.bar(DRAIN));
       mbar_wait(cta.bar(DRAIN), 0, ctl, DRAIN_NS);
     }
-  } else if (warp < 4) {
+  } else if (warp < 8) {
     // ------------------------------------------------------------------ convert group
-    // Row i of chunk c: gate dot product, in-place fp16 operands, masked scores.
-    const int i = tid;  // token row == TMEM lane (warp w serves lanes 32w..32w+31)
-    const uint32_t trow = tmem + ((uint32_t)(32 * warp) << 16);
+    // Warp w serves rows 32q..32q+31 (q = w & 3, thread = token row i = TMEM lane) and half
+    // hv = w >> 2 of the work on them: v chunks 12hv..12hv+11, q/k chunks 6hv..6hv+5 (with
+    // their part of the gate dot product), and some of the eight 16-column score blocks.
+    // Half 0 owns the quadrant's two diagonal blocks (and so adds the self-augmentation, for
+    // which it takes half 1's gate partial sums); the blocks below the diagonal are shared
+    // out so that the busiest quadrant gives each half four; each half zero-fills the blocks
+    // above the diagonal of its parity.
+    const int q4 = warp & 3, hv = warp >> 2;
+    const int i = 32 * q4 + lane;
+    const uint32_t trow = tmem + ((uint32_t)(32 * q4) << 16);
     const float lam = pw[1], lamC = expf((float)C * gamma);
     const float lq = (i + 1 < C) ? pw[i + 1] : lamC;  // lambda^(i+1)
     const float lk_full = pw[C - 1 - i];              // lambda^(C-1-i)
     // in the last chunk (L_last tokens): lambda^(L_last-1-i), and 0 on the zero rows past T
     const float lk_last = i < L_last ? pw[L_last - 1 - i] : 0.f;
+    float* zx = (float*)(base + OFF_ZX);
+    // this warp's blocks at or below the diagonal: hb_first + m for half 1, the diagonal pair
+    // then 0, 1, ... for half 0
+    const int below = max(0, q4 - 1);  // half 0 takes the blocks hb < below
+    const int nlive = hv == 0 ? 2 + below : 2 * q4 - below;
+    auto live_block = [&](int m) { return hv == 0 ? (m < 2 ? 2 * q4 + m : m - 2) : below + m; };
     float range_max = 0.f;
     for (int c = 0; c < n; ++c) {
       const uint32_t s = c & 1, par = c & 1;
@@ -262,12 +284,12 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
       if (!wait(cta, cta.bar(V_FULL + s), (c >> 1) & 1, ctl)) break;
       if constexpr (BF16) {  // v -> fp16 in place (exact for |v| in the fp16 normal range)
 #pragma unroll 4
-        for (int cc = 0; cc < 24; ++cc)
+        for (int cc = 12 * hv; cc < 12 * hv + 12; ++cc)
           scale_chunk_to_half<true>(
               (uint4*)(stg + OFF_V + (cc >> 3) * V_BOX + swz_off(i, cc & 7, 128)), 1.f, vmax);
       } else {
 #pragma unroll 4
-        for (int cc = 0; cc < 24; ++cc) {
+        for (int cc = 12 * hv; cc < 12 * hv + 12; ++cc) {
           const uint4 x = *(const uint4*)(stg + OFF_V + (cc >> 3) * V_BOX + swz_off(i, cc & 7, 128));
           const uint32_t* w = (const uint32_t*)&x;
 #pragma unroll
@@ -279,7 +301,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
       tc_fence_after();
       float z = 0.f;
 #pragma unroll 2
-      for (int cc = 0; cc < 12; ++cc) {  // channels 8cc..8cc+7
+      for (int cc = 6 * hv; cc < 6 * hv + 6; ++cc) {  // channels 8cc..8cc+7
         const uint32_t off = (cc >> 2) * Q_BOX + swz_off(i, cc & 3, 64);
         uint4 qv = *(uint4*)(stg + OFF_Q + off);
         uint4 kv = *(uint4*)(stg + OFF_K + off);
@@ -303,11 +325,14 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
         *(uint4*)(stg + OFF_Q + off) = qv;
         *(uint4*)(stg + OFF_K + off) = kv;
       }
+      if (hv == 1) {  // half 0 adds the diagonal term: it needs the whole gate sum
+        zx[i] = z;
+        mbar_arrive(cta.bar(ZX0 + q4));
+      }
       // Q'' is in place: the Q''S MMA can run (and release the state copy's slot) while the
       // masked scores are still being made
       fence_proxy_async();
       mbar_arrive(cta.bar(EP_Q));
-      const float sg = sigmoid(z);
       // chunk maxima of |K'| and |V| (for the emit group's bound on the next state)
       {
         float km = kmax, vm = vmax;
@@ -317,46 +342,56 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
           vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, off));
         }
         if (lane == 0) {
-          kvmax[par * 8 + warp] = km;
-          kvmax[par * 8 + 4 + warp] = vm;
+          kvmax[par * 16 + warp] = km;
+          kvmax[par * 16 + 8 + warp] = vm;
         }
       }
       // the state exponent of this chunk (and P'' of the previous chunk consumed)
       if (!wait(cta, cta.bar(EP_S), par, ctl)) break;
+      float sg = 0.f;
+      if (hv == 0) {
+        if (!wait(cta, cta.bar(ZX0 + q4), par, ctl)) break;
+        sg = sigmoid(z + zx[i]);
+      }
       const float psc = pow2i(-es[par]);
       float pmax = 0.f;
       {
-        uint32_t r[32];
-#pragma unroll 1
-        for (int jb = 0; jb < 4; ++jb) {
-          const int j0 = 32 * jb;
-          float p[32];
-          if (jb <= warp) {  // block touches columns j <= i for this warp's rows
-            tmem_ld32(trow + TM_P + j0, r);
-            tmem_wait_ld();
-            // lambda^(i-j) by repeated multiplication going left from j = min(i, j0+31)
-            float f = pw[max(i - (j0 + 31), 0)] * psc;
+        uint32_t pk[4][8];
 #pragma unroll
-            for (int u = 31; u >= 0; --u) {
-              const bool in = j0 + u <= i;
+        for (int m = 0; m < 4; ++m) {
+          if (m < nlive) {
+            const int cb = 16 * live_block(m);
+            uint32_t r[16];
+            tmem_ld16(trow + TM_P + cb, r);
+            tmem_wait_ld();
+            // lambda^(i-j) by repeated multiplication going left from j = min(i, cb+15)
+            float f = pw[max(i - (cb + 15), 0)] * psc;
+            float p[16];
+#pragma unroll
+            for (int u = 15; u >= 0; --u) {
+              const bool in = cb + u <= i;
               p[u] = in ? __uint_as_float(r[u]) * f : 0.f;
               f = in ? f * lam : f;
               // the self-augmentation sigmoid(z_i) v_i rides on the diagonal, so P'' V
               // includes it: (P o D + diag(sigmoid(z))) 2^-e
-              if (jb == warp && u == lane) p[u] += sg * psc;
+              if (cb + u == i) p[u] += sg * psc;
               pmax = fmaxf(pmax, fabsf(p[u]));
             }
-          } else {
 #pragma unroll
-            for (int u = 0; u < 32; ++u) p[u] = 0.f;
+            for (int u = 0; u < 8; ++u) pk[m][u] = pack_h2(p[2 * u], p[2 * u + 1]);
           }
-          // fp16 pairs, in place over the fp32 scores: this block's 16 packed columns land on
-          // fp32 columns 16jb..16jb+15, which blocks <= jb have already read
-          uint32_t pk[16];
-#pragma unroll
-          for (int u = 0; u < 16; ++u) pk[u] = pack_h2(p[2 * u], p[2 * u + 1]);
-          tmem_st16(trow + TM_P + 16 * jb, pk);
         }
+        // fp16 pairs, in place over the fp32 scores: block hb's 8 packed columns land on fp32
+        // columns 8hb..8hb+7, inside block hb/2, so both warps of the quadrant read first
+        tc_fence_before();
+        mbar_arrive(cta.bar(QS0 + q4));
+        if (!wait(cta, cta.bar(QS0 + q4), par, ctl)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+          if (m < nlive) tmem_st8(trow + TM_P + 8 * live_block(m), pk[m]);
+        const uint32_t zero8[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+        for (int hb = 2 * q4 + 2 + hv; hb < 8; hb += 2) tmem_st8(trow + TM_P + 8 * hb, zero8);
       }
       range_max = fmaxf(range_max, fmaxf(fmaxf(vmax, kmax), fmaxf(qmax, pmax)));
       tmem_wait_st();
@@ -367,9 +402,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
     if (range_max >= 65504.f) record_error(ctl, DEV_RANGE);
   } else if (warp < PRODUCER_WARP) {
     // ------------------------------------------------------------------ emit group
-    // Warp w serves rows 32(w&3)..+31 and value columns [96hf, 96hf+96), hf = (w-4)>>2.
+    // Warp w serves rows 32(w&3)..+31 and value columns [96hf, 96hf+96), hf = (w-8)>>2.
     // State copy for the next chunk (the serial chain, first), then the output rows.
-    const int q4 = warp & 3, hf = (warp - 4) >> 2, ew = warp - 4;
+    const int q4 = warp & 3, hf = (warp - 8) >> 2, ew = warp - 8;
     const int i = 32 * q4 + lane;
     const uint32_t trow = tmem + ((uint32_t)(32 * q4) << 16);
     const float lamC = expf((float)C * gamma);
@@ -426,7 +461,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
       if (lane == 0) red[(use & 1) * 8 + ew] = m;
-      if (tid == 128) es[use & 1] = e;
+      if (ew == 0 && lane == 0) es[use & 1] = e;
       fence_proxy_async();
       tc_fence_before();
       mbar_arrive(cta.bar(EP_S));
@@ -446,7 +481,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
       const int pg = __ldg(sp.page + b);
       page_ok = pg >= 0 && pg < sp.n_pages;
       zst = ((long long)pg * sp.pool_layers + sp.layer) * H + h;
-      if (!page_ok && tid == 128 && (!cut || part == plan.parts - 1)) record_error(ctl, DEV_RANGE);
+      if (!page_ok && ew == 0 && lane == 0 && (!cut || part == plan.parts - 1))
+        record_error(ctl, DEV_RANGE);
     }
     const long long zinit = sp.init_paged ? zst : bh;
     // starting state: the caller's (whole pair) or the one the segment passes left for this
@@ -498,10 +534,12 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
         // every emit thread has stored its part of max|S_c| (EP_S phase c is complete)
         if (!(ok = wait(cta, cta.bar(EP_S), par, ctl))) break;
         const float ms = red_max(par);
-        const float km = fmaxf(fmaxf(kvmax[par * 8 + 0], kvmax[par * 8 + 1]),
-                               fmaxf(kvmax[par * 8 + 2], kvmax[par * 8 + 3]));
-        const float vm = fmaxf(fmaxf(kvmax[par * 8 + 4], kvmax[par * 8 + 5]),
-                               fmaxf(kvmax[par * 8 + 6], kvmax[par * 8 + 7]));
+        float km = kvmax[par * 16], vm = kvmax[par * 16 + 8];
+#pragma unroll
+        for (int w = 1; w < 8; ++w) {
+          km = fmaxf(km, kvmax[par * 16 + w]);
+          vm = fmaxf(vm, kvmax[par * 16 + 8 + w]);
+        }
         e_next = state_exponent(lamC * ms + (float)C * km * vm);
         if (e_next < 0) {
           bad = true;
