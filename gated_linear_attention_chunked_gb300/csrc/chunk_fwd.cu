@@ -7,22 +7,23 @@
 //   S_{c+1} = lambda^C S_c + K^T Lk V                        (the only serial step)
 //
 // One CTA owns one (b, h) and walks its chunks in order; the fp32 state never leaves the chip.
-//   warp 16     TMA producer: q, k tiles (3 boxes of 32 channels, 64-byte swizzle) and v tiles
+//   producer  TMA producer: q, k tiles (3 boxes of 32 channels, 64-byte swizzle) and v tiles
 //               (3 boxes of 64 channels, 128-byte swizzle) into a 2-stage ring (no L2
 //               prefetch: measured, it slowed the loads it was meant to hide).
-//   warp 17     tcgen05 issuer (one thread) and TMEM owner (512 columns):
+//   MMA warp  tcgen05 issuer (one thread) and TMEM owner (512 columns):
 //                 D_P [384,512)  P = Q K^T (bf16/fp16 inputs as given); the masked fp16
 //                                copy P'' is written back in place (64 columns) and read
 //                                from TMEM as the A operand of P'' V
 //                 D_O [  0,192)  O = Q'' S_c + P'' V           (fp16 operands)
 //                 D_S [192,384)  S = lambda^C S + K'^T V       (fp16 operands, fp32 state;
 //                                rows 96..127 are padding and never read)
-//   warps 0..7  convert group, thread = token row i (= TMEM lane), two warps per row
-//               quadrant splitting the channels and score blocks, one chunk ahead of the
+//   convert     warps 0..7 (the plain forward: two per row quadrant splitting the channels
+//               and score blocks) or 0..3 (with the fused output epilogue: one per quadrant),
+//               thread = token row i (= TMEM lane), one chunk ahead of the
 //               emit group: V -> fp16 in place; z = q.(a*k); Q'' = fp16(lambda^(i+1) q) and
 //               K' = fp16(lambda^(127-i) k) in place; P'' = fp16((mask(P) + diag(sigmoid(z)))
 //               * 2^-e) into TMEM -- the self-augmentation rides on the diagonal of P''.
-//   warps 8..15 emit group, same rows, two warps per row quadrant splitting the value
+//   emit        the next 8 warps, same rows, two warps per row quadrant splitting the value
 //               columns: (1) the serial step -- S -> fp16(S * 2^-e') into the drained q/k
 //               slot (B operand of the next Q'' S) and D_S <- lambda^C D_S; (2) the output rows
 //               o = 2^e D_O as fp32, TMA-stored from per-warp staging.
@@ -91,13 +92,22 @@ enum Bar : uint32_t {
   QS0 = 28,   // 28..31: both convert warps of quadrant q have read their score blocks
 };
 
-constexpr int THREADS = 576;
-constexpr int PRODUCER_WARP = 16, MMA_WARP = 17;
-constexpr int CONVERT_THREADS = 256;  // warps 0..7
-constexpr int EMIT_THREADS = 256;     // warps 8..15
+// Warp layout by variant: CW convert warps per row quadrant (warps 0..4CW-1), then 8 emit
+// warps, the TMA producer and the MMA issuer.  The plain forward splits the convert work over
+// two warps per quadrant (18 warps, 96 registers); the forward with the fused output epilogue,
+// whose emit warps need more registers, keeps one (14 warps, 128 registers).
+template <bool GATED>
+struct Layout {
+  static constexpr int CW = GATED ? 1 : 2;
+  static constexpr int CONVERT_WARPS = 4 * CW;
+  static constexpr int PRODUCER_WARP = CONVERT_WARPS + 8, MMA_WARP = PRODUCER_WARP + 1;
+  static constexpr int THREADS = (MMA_WARP + 1) * 32;
+  static constexpr int CONVERT_THREADS = 32 * CONVERT_WARPS;
+};
+constexpr int EMIT_THREADS = 256;  // 8 emit warps
 
 template <bool BF16, bool GATED>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(Layout<GATED>::THREADS, 1)
 fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
            const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o,
            const __grid_constant__ CUtensorMap map_fin, const float* __restrict__ log_decay,
@@ -117,6 +127,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
   cta.abort_off = OFF_ABORT;
   uint8_t* const base = cta.base;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  using L = Layout<GATED>;
+  constexpr int CW = L::CW, CONVERT_WARPS = L::CONVERT_WARPS;
+  constexpr int PRODUCER_WARP = L::PRODUCER_WARP, MMA_WARP = L::MMA_WARP;
   // chunks of a sequence; the last one holds L_last = 1..C tokens (rows past T are zeros)
   const int nc = (T + C - 1) / C, L_last = T - (nc - 1) * C;
   // this CTA's pair and chunk range [c0, c0 + n): a whole pair, or part `part` of a cut one
@@ -149,15 +162,15 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
     mbar_init(cta.bar(O_DONE), 1);
     mbar_init(cta.bar(S_DONE), 1);
     mbar_init(cta.bar(DRAIN), 1);
-    mbar_init(cta.bar(EP_CONV), CONVERT_THREADS);
-    mbar_init(cta.bar(EP_Q), CONVERT_THREADS);
+    mbar_init(cta.bar(EP_CONV), L::CONVERT_THREADS);
+    mbar_init(cta.bar(EP_Q), L::CONVERT_THREADS);
     mbar_init(cta.bar(EP_O), EMIT_THREADS);     // emit group
     mbar_init(cta.bar(EP_S), EMIT_THREADS);     // emit group
     mbar_init(cta.bar(RED), EMIT_THREADS);      // emit group
     for (int q = 0; q < 4; ++q) {
       mbar_init(cta.bar(QX + q), 64);
       mbar_init(cta.bar(ZX0 + q), 32);
-      mbar_init(cta.bar(QS0 + q), 64);
+      mbar_init(cta.bar(QS0 + q), 32 * CW);
     }
     *cta.abort_flag() = 0;
     fence_barrier_init();
@@ -252,15 +265,15 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
       mma_commit(cta.bar(DRAIN));
       mbar_wait(cta.bar(DRAIN), 0, ctl, DRAIN_NS);
     }
-  } else if (warp < 8) {
+  } else if (warp < CONVERT_WARPS) {
     // ------------------------------------------------------------------ convert group
-    // Warp w serves rows 32q..32q+31 (q = w & 3, thread = token row i = TMEM lane) and half
-    // hv = w >> 2 of the work on them: v chunks 12hv..12hv+11, q/k chunks 6hv..6hv+5 (with
-    // their part of the gate dot product), and some of the eight 16-column score blocks.
-    // Half 0 owns the quadrant's two diagonal blocks (and so adds the self-augmentation, for
-    // which it takes half 1's gate partial sums); the blocks below the diagonal are shared
-    // out so that the busiest quadrant gives each half four; each half zero-fills the blocks
-    // above the diagonal of its parity.
+    // Warp w serves rows 32q..32q+31 (q = w & 3, thread = token row i = TMEM lane) and part
+    // hv = w >> 2 of CW of the work on them: v chunks, q/k chunks (with their part of the gate
+    // dot product) and some of the eight 16-column score blocks.  With two parts, part 0 owns
+    // the quadrant's two diagonal blocks (and so adds the self-augmentation, for which it
+    // takes part 1's gate partial sums); the blocks below the diagonal are shared out so that
+    // the busiest quadrant gives each part four; each part zero-fills the blocks above the
+    // diagonal of its parity.
     const int q4 = warp & 3, hv = warp >> 2;
     const int i = 32 * q4 + lane;
     const uint32_t trow = tmem + ((uint32_t)(32 * q4) << 16);
@@ -272,9 +285,12 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
     float* zx = (float*)(base + OFF_ZX);
     // this warp's blocks at or below the diagonal: hb_first + m for half 1, the diagonal pair
     // then 0, 1, ... for half 0
-    const int below = max(0, q4 - 1);  // half 0 takes the blocks hb < below
-    const int nlive = hv == 0 ? 2 + below : 2 * q4 - below;
-    auto live_block = [&](int m) { return hv == 0 ? (m < 2 ? 2 * q4 + m : m - 2) : below + m; };
+    constexpr int NV = 24 / CW, MAXB = 8 / CW;  // v chunks and live score blocks per part
+    const int below = max(0, q4 - 1);  // with two parts, part 0 takes the blocks hb < below
+    const int nlive = CW == 1 ? 2 * q4 + 2 : hv == 0 ? 2 + below : 2 * q4 - below;
+    auto live_block = [&](int m) {
+      return CW == 1 ? m : hv == 0 ? (m < 2 ? 2 * q4 + m : m - 2) : below + m;
+    };
     float range_max = 0.f;
     for (int c = 0; c < n; ++c) {
       const uint32_t s = c & 1, par = c & 1;
@@ -284,12 +300,12 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
       if (!wait(cta, cta.bar(V_FULL + s), (c >> 1) & 1, ctl)) break;
       if constexpr (BF16) {  // v -> fp16 in place (exact for |v| in the fp16 normal range)
 #pragma unroll 4
-        for (int cc = 12 * hv; cc < 12 * hv + 12; ++cc)
+        for (int cc = NV * hv; cc < NV * hv + NV; ++cc)
           scale_chunk_to_half<true>(
               (uint4*)(stg + OFF_V + (cc >> 3) * V_BOX + swz_off(i, cc & 7, 128)), 1.f, vmax);
       } else {
 #pragma unroll 4
-        for (int cc = 12 * hv; cc < 12 * hv + 12; ++cc) {
+        for (int cc = NV * hv; cc < NV * hv + NV; ++cc) {
           const uint4 x = *(const uint4*)(stg + OFF_V + (cc >> 3) * V_BOX + swz_off(i, cc & 7, 128));
           const uint32_t* w = (const uint32_t*)&x;
 #pragma unroll
@@ -299,9 +315,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
       if (!wait(cta, cta.bar(P_DONE), par, ctl)) break;
       if (!wait(cta, cta.bar(QK_FULL + s), (c >> 1) & 1, ctl)) break;
       tc_fence_after();
-      float z = 0.f;
-#pragma unroll 2
-      for (int cc = 6 * hv; cc < 6 * hv + 6; ++cc) {  // channels 8cc..8cc+7
+      // channels 8cc..8cc+7 of q, k: their part of the gate sum into `zacc`, Q'' and K' in place
+      auto qk_chunk = [&](int cc, float& zacc) {
         const uint32_t off = (cc >> 2) * Q_BOX + swz_off(i, cc & 3, 64);
         uint4 qv = *(uint4*)(stg + OFF_Q + off);
         uint4 kv = *(uint4*)(stg + OFF_K + off);
@@ -314,8 +329,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
         for (int e2 = 0; e2 < 4; ++e2) {
           const float q0 = ld16<BF16>(qw[e2] & 0xFFFFu), q1 = ld16<BF16>(qw[e2] >> 16);
           const float k0 = ld16<BF16>(kw[e2] & 0xFFFFu), k1 = ld16<BF16>(kw[e2] >> 16);
-          z = fmaf(av[2 * e2] * q0, k0, z);
-          z = fmaf(av[2 * e2 + 1] * q1, k1, z);
+          zacc = fmaf(av[2 * e2] * q0, k0, zacc);
+          zacc = fmaf(av[2 * e2 + 1] * q1, k1, zacc);
           const float x0 = q0 * lq, x1 = q1 * lq, y0 = k0 * lk, y1 = k1 * lk;
           qmax = fmaxf(qmax, fmaxf(fabsf(x0), fabsf(x1)));
           kmax = fmaxf(kmax, fmaxf(fabsf(y0), fabsf(y1)));
@@ -324,8 +339,17 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
         }
         *(uint4*)(stg + OFF_Q + off) = qv;
         *(uint4*)(stg + OFF_K + off) = kv;
+      };
+      // the gate sum is always formed as (channels 0..47) + (channels 48..95), whichever
+      // layout, so both give bit-identical outputs
+      float z = 0.f, z_hi = 0.f;
+#pragma unroll 2
+      for (int cc = 6 * hv; cc < 6 * hv + 6; ++cc) qk_chunk(cc, z);
+      if constexpr (CW == 1) {
+#pragma unroll 2
+        for (int cc = 6; cc < 12; ++cc) qk_chunk(cc, z_hi);
       }
-      if (hv == 1) {  // half 0 adds the diagonal term: it needs the whole gate sum
+      if (CW == 2 && hv == 1) {  // part 0 adds the diagonal term: it needs the whole gate sum
         zx[i] = z;
         mbar_arrive(cta.bar(ZX0 + q4));
       }
@@ -349,16 +373,21 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
       // the state exponent of this chunk (and P'' of the previous chunk consumed)
       if (!wait(cta, cta.bar(EP_S), par, ctl)) break;
       float sg = 0.f;
-      if (hv == 0) {
+      if (CW == 1) {
+        sg = sigmoid(z + z_hi);
+      } else if (hv == 0) {
         if (!wait(cta, cta.bar(ZX0 + q4), par, ctl)) break;
         sg = sigmoid(z + zx[i]);
       }
       const float psc = pow2i(-es[par]);
       float pmax = 0.f;
       {
-        uint32_t pk[4][8];
+        // fp16 pairs, in place over the fp32 scores: block hb's 8 packed columns land on fp32
+        // columns 8hb..8hb+7, inside block hb/2.  One warp per quadrant takes its blocks in
+        // increasing order, so it writes each as soon as it is made; with two, both read first.
+        uint32_t pk[CW == 1 ? 1 : MAXB][8];
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
+        for (int m = 0; m < MAXB; ++m) {
           if (m < nlive) {
             const int cb = 16 * live_block(m);
             uint32_t r[16];
@@ -377,21 +406,23 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
               if (cb + u == i) p[u] += sg * psc;
               pmax = fmaxf(pmax, fabsf(p[u]));
             }
+            uint32_t(&dst)[8] = pk[CW == 1 ? 0 : m];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) pk[m][u] = pack_h2(p[2 * u], p[2 * u + 1]);
+            for (int u = 0; u < 8; ++u) dst[u] = pack_h2(p[2 * u], p[2 * u + 1]);
+            if constexpr (CW == 1) tmem_st8(trow + TM_P + cb / 2, dst);
           }
         }
-        // fp16 pairs, in place over the fp32 scores: block hb's 8 packed columns land on fp32
-        // columns 8hb..8hb+7, inside block hb/2, so both warps of the quadrant read first
-        tc_fence_before();
-        mbar_arrive(cta.bar(QS0 + q4));
-        if (!wait(cta, cta.bar(QS0 + q4), par, ctl)) break;
-        tc_fence_after();
+        if constexpr (CW == 2) {
+          tc_fence_before();
+          mbar_arrive(cta.bar(QS0 + q4));
+          if (!wait(cta, cta.bar(QS0 + q4), par, ctl)) break;
+          tc_fence_after();
 #pragma unroll
-        for (int m = 0; m < 4; ++m)
-          if (m < nlive) tmem_st8(trow + TM_P + 8 * live_block(m), pk[m]);
+          for (int m = 0; m < MAXB; ++m)
+            if (m < nlive) tmem_st8(trow + TM_P + 8 * live_block(m), pk[m]);
+        }
         const uint32_t zero8[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-        for (int hb = 2 * q4 + 2 + hv; hb < 8; hb += 2) tmem_st8(trow + TM_P + 8 * hb, zero8);
+        for (int hb = 2 * q4 + 2 + hv; hb < 8; hb += CW) tmem_st8(trow + TM_P + 8 * hb, zero8);
       }
       range_max = fmaxf(range_max, fmaxf(fmaxf(vmax, kmax), fmaxf(qmax, pmax)));
       tmem_wait_st();
@@ -404,7 +435,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
     // ------------------------------------------------------------------ emit group
     // Warp w serves rows 32(w&3)..+31 and value columns [96hf, 96hf+96), hf = (w-8)>>2.
     // State copy for the next chunk (the serial chain, first), then the output rows.
-    const int q4 = warp & 3, hf = (warp - 8) >> 2, ew = warp - 8;
+    const int q4 = warp & 3, hf = (warp - CONVERT_WARPS) >> 2, ew = warp - CONVERT_WARPS;
     const int i = 32 * q4 + lane;
     const uint32_t trow = tmem + ((uint32_t)(32 * q4) << 16);
     const float lamC = expf((float)C * gamma);
@@ -536,7 +567,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
         const float ms = red_max(par);
         float km = kvmax[par * 16], vm = kvmax[par * 16 + 8];
 #pragma unroll
-        for (int w = 1; w < 8; ++w) {
+        for (int w = 1; w < CONVERT_WARPS; ++w) {
           km = fmaxf(km, kvmax[par * 16 + w]);
           vm = fmaxf(vm, kvmax[par * 16 + 8 + w]);
         }
@@ -700,7 +731,7 @@ cudaError_t launch_chunk_fwd(const FwdArgs& a, DevCtl ctl, cudaStream_t stream) 
     plan.parts = 1;
   }
   const long long grid = plan.whole + ((long long)a.B * a.H - plan.whole) * plan.parts;
-  kern<<<(unsigned)grid, THREADS, SMEM_BYTES, stream>>>(mq, mk, mv, mo, mfin, a.log_decay, a.aug,
+  kern<<<(unsigned)grid, gated ? Layout<true>::THREADS : Layout<false>::THREADS, SMEM_BYTES, stream>>>(mq, mk, mv, mo, mfin, a.log_decay, a.aug,
                                                         a.init, a.o, a.fin, a.T, a.H, plan,
                                                         a.seg_init, a.sp, my, a.og, ctl);
   return cudaGetLastError();
