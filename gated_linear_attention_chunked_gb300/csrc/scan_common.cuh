@@ -1,9 +1,9 @@
-// scan_common.cuh -- pieces shared by the chunk-scan kernels (forward and the backward
-// roles): the bounded wait with a CTA-wide abort flag, 16-bit conversions, the power-of-two
-// scaled fp16 copy of a fp32 state row, and the coalesced store of fp32 output rows.
+// scan_common.cuh -- pieces shared by the chunk-scan kernels (forward, the backward roles and
+// the segment passes): the bounded wait with a CTA-wide abort flag, 16-bit conversions, the
+// power-of-two exponent of a state copy, and the TMA emission of fp32 output rows.
 //
-// Epilogue layout used by every scan kernel: 8 warps, warp w owns TMEM lane quadrant
-// q = w & 3 (token rows 32q..32q+31, one row per thread) and column half hf = w >> 2.
+// In every scan kernel an epilogue warp w reads TMEM lane quadrant q = w & 3 (token rows
+// 32q..32q+31, one row per thread); the kernels differ in how many warps share a quadrant.
 #pragma once
 #include <cuda_fp16.h>
 
@@ -13,7 +13,6 @@ namespace gla {
 namespace scan {
 
 constexpr int C = 128, DK = 96, DV = 192;
-constexpr int EPI_WARPS = 8, EPI_THREADS = 256;
 constexpr uint64_t DRAIN_NS = 4000000000ull;  // limit of the exit-time drain waits
 
 struct Cta {
