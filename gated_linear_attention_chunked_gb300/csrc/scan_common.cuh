@@ -196,28 +196,41 @@ __device__ __forceinline__ void emit_rows_tma(uint8_t* buf0, int lane, Produce p
 // Emit a warp's 32 rows x (8 * NBLK8) fp32 columns, produced block by block by
 // `produce(k, r)` (8 columns of block k), through two 1 KB staging buffers (`buf0`,
 // `buf0 + 1024`) and TMA stores of 32-byte-swizzled boxes {8, 1, 32}: row rr at rr * 32
-// bytes, its two 16-byte chunks exchanged when bit 2 of rr is set.  `buf0` must be 256-byte
-// aligned.  Called by all 32 lanes; lane 0 issues the stores.
+// bytes, its two 16-byte chunks exchanged when bit 2 of rr is set.  Blocks go two at a time:
+// both staged, one proxy fence, both stores in one bulk group; the next pair reuses the
+// buffers once those stores have read them.  `store(k, smem)` issues the TMA store of block
+// k.  `buf0` must be 256-byte aligned.  Called by all 32 lanes; lane 0 issues the stores.
 template <int NBLK8, typename Produce, typename Store>
 __device__ __forceinline__ void emit_rows8_tma(uint8_t* buf0, int lane, Produce produce,
                                                Store store) {
+  const int sw = (lane >> 2) & 1;
 #pragma unroll
-  for (int k = 0; k < NBLK8; ++k) {
-    uint8_t* buf = buf0 + (k & 1) * 1024;
-    float r[8];
-    produce(k, r);
-    if (k >= 2) {  // the store that last read this buffer must have finished reading it
-      if (lane == 0) bulk_wait_read<1>();
+  for (int k0 = 0; k0 < NBLK8; k0 += 2) {
+    const int nb = k0 + 1 < NBLK8 ? 2 : 1;
+    float r[2][8];
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+      if (j < nb) produce(k0 + j, r[j]);
+    if (k0 >= 2) {  // the previous pair's stores must have finished reading the buffers
+      if (lane == 0) bulk_wait_read<0>();
       __syncwarp();
     }
-    const int sw = (lane >> 2) & 1;
-    *reinterpret_cast<float4*>(buf + lane * 32 + (sw << 4)) = make_float4(r[0], r[1], r[2], r[3]);
-    *reinterpret_cast<float4*>(buf + lane * 32 + ((sw ^ 1) << 4)) =
-        make_float4(r[4], r[5], r[6], r[7]);
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      if (j < nb) {
+        uint8_t* buf = buf0 + j * 1024;
+        *reinterpret_cast<float4*>(buf + lane * 32 + (sw << 4)) =
+            make_float4(r[j][0], r[j][1], r[j][2], r[j][3]);
+        *reinterpret_cast<float4*>(buf + lane * 32 + ((sw ^ 1) << 4)) =
+            make_float4(r[j][4], r[j][5], r[j][6], r[j][7]);
+      }
+    }
     fence_proxy_async();
     __syncwarp();
     if (lane == 0) {
-      store(k, smem_u32(buf));
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+        if (j < nb) store(k0 + j, smem_u32(buf0 + j * 1024));
       bulk_commit();
     }
   }
