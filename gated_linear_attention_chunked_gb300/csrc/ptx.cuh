@@ -257,11 +257,6 @@ __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-// Named barrier over `nthreads` threads (a multiple of 32), id 1..15.
-__device__ __forceinline__ void named_bar(uint32_t id, uint32_t nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
 // ---------------------------------------------------------------------------------------
 // Descriptors.
 //

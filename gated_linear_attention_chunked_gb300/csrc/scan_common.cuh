@@ -111,42 +111,6 @@ __device__ __forceinline__ void convert_row(uint8_t* tile, Off off, float s, flo
   }
 }
 
-// sum_e w_e x_e y_e over NCH 16-byte chunks of two rows of 16-bit data (w_e = wt[8c + e], or
-// 1 without weights), loading four chunks at a time and keeping four partial sums so that
-// neither the loads nor the multiply-adds form one long dependent chain.
-template <bool SRC_BF16, int NCH, bool WEIGHTED, typename OffX, typename OffY>
-__device__ __forceinline__ float dot_rows(const uint8_t* tx, OffX offx, const uint8_t* ty, OffY offy,
-                                          const float* wt) {
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-  for (int c0 = 0; c0 < NCH; c0 += 4) {
-    uint4 x[4], y[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      x[u] = *(const uint4*)(tx + offx(c0 + u));
-      y[u] = *(const uint4*)(ty + offy(c0 + u));
-    }
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const uint32_t* xw = reinterpret_cast<const uint32_t*>(&x[u]);
-      const uint32_t* yw = reinterpret_cast<const uint32_t*>(&y[u]);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int d = 8 * (c0 + u) + 2 * e;
-        float x0 = ld16<SRC_BF16>(xw[e] & 0xFFFFu), x1 = ld16<SRC_BF16>(xw[e] >> 16);
-        const float y0 = ld16<SRC_BF16>(yw[e] & 0xFFFFu), y1 = ld16<SRC_BF16>(yw[e] >> 16);
-        if constexpr (WEIGHTED) {
-          x0 *= wt[d];
-          x1 *= wt[d + 1];
-        }
-        acc[u] = fmaf(x0, y0, acc[u]);
-        acc[u] = fmaf(x1, y1, acc[u]);
-      }
-    }
-  }
-  return (acc[0] + acc[1]) + (acc[2] + acc[3]);
-}
-
 // Power-of-two exponent e >= 0 such that m * 2^-e < 2^14 (fp16 copy with headroom).
 // Returns -1 for a non-finite m.
 __device__ __forceinline__ int state_exponent(float m) {
