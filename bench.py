@@ -35,8 +35,9 @@ N_SEQ, N_LAYERS = 1280, 24
 WORKLOAD = ("GLA chunked fwd+bwd B=32 T=2048 H=16 dk=96 dv=192 chunk=128 bf16-in/fp32-out, "
             "plus one decode step over 1280 seqs x 24 layers x 16 heads of 96x192 fp32 states")
 # Algorithmic work per unit (what the calls must move / compute at minimum)
-FWD_BYTES_TH = (96 + 96 + 192) * 2 + 192 * 4             # bf16 q,k,v in, fp32 o out = 1536
-BWD_BYTES_TH = (96 + 96 + 192 + 192) * 2 + (96 + 96 + 192) * 4  # + dO in, fp32 dq,dk,dv = 2688
+# the training step saves the gate sigmoid(z) (fp32 per token-head) in the forward for the backward
+FWD_BYTES_TH = (96 + 96 + 192) * 2 + 192 * 4 + 4         # bf16 q,k,v in, fp32 o, gate out = 1540
+BWD_BYTES_TH = (96 + 96 + 192 + 192) * 2 + 4 + (96 + 96 + 192) * 4  # + dO, gate in; dq,dk,dv = 2692
 FWD_FLOPS_TH = 2 * (128 * 96 + 128 * 192 + 96 * 192 + 96 * 192)  # QK^T, PV, QS, K^T V = 147456
 BWD_FLOPS_TH = 319488                                     # 9 dense chunk matmuls per token-head
 DEC_BYTES_STATE = 2 * 96 * 192 * 4 + (96 + 96 + 192 + 192) * 4  # state r+w, q,k,v,o = 149760
@@ -231,8 +232,10 @@ def run_gpu(args, rank, world, local_rank):
         dO = randn(Bn, T, H, DV, dtype=torch.bfloat16)
         o = torch.empty(Bn, T, H, DV, device=dev)
         fin = torch.empty(Bn, H, DK, DV, device=dev)
+        gate = torch.empty(Bn, H, T, device=dev)  # sigmoid(z), saved by the forward
         ws = torch.empty(max(1, gla.chunk_bwd_workspace_size(Bn, T, H, gla.GLA_BF16)),
                          dtype=torch.uint8, device=dev)
+        gla.chunk_fwd(q, k, v, gam, a, out=o, final_state=fin, gate=gate)  # a backward alone reads it
 
     # ---- serving pool: 1280 x 24 x 16 states, warmed by 64 recurrent steps from zero
     if do_dec:
@@ -261,11 +264,11 @@ def run_gpu(args, rank, world, local_rank):
         if evs:
             evs[0].record(stream)
         if do_fwd:
-            gla.chunk_fwd(q, k, v, gam, a, out=o, final_state=fin)
+            gla.chunk_fwd(q, k, v, gam, a, out=o, final_state=fin, gate=gate)
         if evs:
             evs[1].record(stream)
         if do_bwd:
-            gla.chunk_bwd(q, k, v, gam, a, dO, workspace=ws)
+            gla.chunk_bwd(q, k, v, gam, a, dO, gate=gate, workspace=ws)
         if evs:
             evs[2].record(stream)
         if do_dec:
@@ -369,8 +372,8 @@ def run_gpu(args, rank, world, local_rank):
                     copied[i].record(copy_stream)
                 stream.wait_event(copied[i])
                 bq, bk, bv, bdO = bufs[i]
-                gla.chunk_fwd(bq, bk, bv, gam, a, out=o, final_state=fin)
-                _, _, _, daug, _ = gla.chunk_bwd(bq, bk, bv, gam, a, bdO, workspace=ws,
+                gla.chunk_fwd(bq, bk, bv, gam, a, out=o, final_state=fin, gate=gate)
+                _, _, _, daug, _ = gla.chunk_bwd(bq, bk, bv, gam, a, bdO, gate=gate, workspace=ws,
                                                  want_d_init_state=False)
                 consumed[i].record(stream)
                 h_daug[s_].copy_(daug, non_blocking=True)
@@ -650,6 +653,7 @@ def run_long_prefill(args):
     gam = gla.decay_schedule(H).to(dev)
     o = torch.empty(Bl, Tl, H, DV, device=dev)
     fin = torch.empty(Bl, H, DK, DV, device=dev)
+    gl = torch.empty(Bl, H, Tl, device=dev)  # the gate, saved for the backward below
     nws = gla.chunk_fwd_workspace_size(Bl, Tl, H, gla.GLA_BF16)
     ws = torch.empty(max(nws, 256), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
@@ -657,7 +661,8 @@ def run_long_prefill(args):
     def call(w, nb):
         rc = lib.gla_chunk_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), gla.GLA_BF16,
                                gam.data_ptr(), a.data_ptr(), init.data_ptr(), o.data_ptr(),
-                               fin.data_ptr(), w, nb, Bl, Tl, H, DK, DV, stream.cuda_stream)
+                               fin.data_ptr(), gl.data_ptr(), w, nb, Bl, Tl, H, DK, DV,
+                               stream.cuda_stream)
         if rc != 0:
             raise RuntimeError(gla.status_string(rc))
 
@@ -690,9 +695,9 @@ def run_long_prefill(args):
     def call_b(nb):
         rc = lib.gla_chunk_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), gla.GLA_BF16,
                                gam.data_ptr(), a.data_ptr(), init.data_ptr(), dO.data_ptr(), None,
-                               dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), d_a.data_ptr(),
-                               dinit.data_ptr(), wsb.data_ptr(), nb, Bl, Tl, H, DK, DV,
-                               stream.cuda_stream)
+                               gl.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                               d_a.data_ptr(), dinit.data_ptr(), wsb.data_ptr(), nb, Bl, Tl, H,
+                               DK, DV, stream.cuda_stream)
         if rc != 0:
             raise RuntimeError(gla.status_string(rc))
 

@@ -62,11 +62,11 @@ def load(path: str | None = None):
             lib.gla_decay_schedule.restype = _I
             lib.gla_chunk_fwd_workspace_size.argtypes = [_I] * 6
             lib.gla_chunk_fwd_workspace_size.restype = _S
-            lib.gla_chunk_fwd.argtypes = [_P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _S] + [_I] * 5 + [_P]
+            lib.gla_chunk_fwd.argtypes = [_P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _P, _S] + [_I] * 5 + [_P]
             lib.gla_chunk_fwd.restype = _I
             lib.gla_chunk_bwd_workspace_size.argtypes = [_I] * 6
             lib.gla_chunk_bwd_workspace_size.restype = _S
-            lib.gla_chunk_bwd.argtypes = [_P] * 3 + [_I] + [_P] * 11 + [_S] + [_I] * 5 + [_P]
+            lib.gla_chunk_bwd.argtypes = [_P] * 3 + [_I] + [_P] * 12 + [_S] + [_I] * 5 + [_P]
             lib.gla_chunk_bwd.restype = _I
             lib.gla_decode_step.argtypes = [_P] * 7 + [_I] * 5 + [_P]
             lib.gla_wait_probe.argtypes = [_P]
@@ -177,9 +177,10 @@ def _workspace(nbytes, device, workspace):
 
 
 def chunk_fwd(q, k, v, log_decay, aug_balance, init_state=None, *, want_final_state=True,
-              out=None, final_state=None, workspace=None, stream=None):
+              out=None, final_state=None, gate=None, workspace=None, stream=None):
     """Chunked forward (gla_chunk_fwd).  q,k [B,T,H,96], v [B,T,H,192] (bf16/fp16/fp32);
-    log_decay [H], aug_balance [H,96], init_state [B,H,96,192] fp32 (optional).
+    log_decay [H], aug_balance [H,96], init_state [B,H,96,192] fp32 (optional); gate: an
+    fp32 [B,H,T] tensor that receives sigmoid(q.(a*k)) for chunk_bwd (optional).
     Returns (o fp32 [B,T,H,192], final_state fp32 [B,H,96,192] or None)."""
     torch = _torch()
     B, T, H, dk = q.shape
@@ -189,13 +190,16 @@ def chunk_fwd(q, k, v, log_decay, aug_balance, init_state=None, *, want_final_st
         out = torch.empty((B, T, H, dv), dtype=torch.float32, device=q.device)
     if final_state is None and want_final_state:
         final_state = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
+    if gate is not None and tuple(gate.shape) != (B, H, T):
+        raise ValueError(f"gate must be [B,H,T] = {(B, H, T)}, got {tuple(gate.shape)}")
     ws = _workspace(load().gla_chunk_fwd_workspace_size(B, T, H, dk, dv, code), q.device, workspace)
     rc = load().gla_chunk_fwd(
         _dev(q, "q"), _dev(k, "k", q.dtype), _dev(v, "v", q.dtype), code,
         _dev(log_decay, "log_decay", torch.float32), _dev(aug_balance, "aug_balance", torch.float32),
         _dev(init_state, "init_state", torch.float32), _dev(out, "o", torch.float32),
-        _dev(final_state, "final_state", torch.float32), _dev(ws, "workspace"),
-        0 if ws is None else ws.numel() * ws.element_size(), B, T, H, dk, dv, _stream(stream))
+        _dev(final_state, "final_state", torch.float32), _dev(gate, "gate", torch.float32),
+        _dev(ws, "workspace"), 0 if ws is None else ws.numel() * ws.element_size(), B, T, H, dk,
+        dv, _stream(stream))
     _check("gla_chunk_fwd", rc)
     return out, final_state
 
@@ -227,8 +231,10 @@ def chunk_fwd_gated(q, k, v, log_decay, aug_balance, g, norm_weight, n_tiers, ep
 
 
 def chunk_bwd(q, k, v, log_decay, aug_balance, dO, init_state=None, d_final_state=None, *,
-              want_d_init_state=True, workspace=None, stream=None):
-    """Chunked backward (gla_chunk_bwd).  Returns (dq, dk, dv, d_aug, d_init_state), fp32."""
+              gate=None, want_d_init_state=True, workspace=None, stream=None):
+    """Chunked backward (gla_chunk_bwd).  gate: the fp32 [B,H,T] sigmoid(q.(a*k)) that
+    chunk_fwd saved (optional; recomputed if None).  Returns (dq, dk, dv, d_aug, d_init_state),
+    fp32."""
     torch = _torch()
     B, T, H, dk = q.shape
     dv = v.shape[-1]
@@ -239,12 +245,15 @@ def chunk_bwd(q, k, v, log_decay, aug_balance, dO, init_state=None, d_final_stat
     dv_ = torch.empty((B, T, H, dv), **f32)
     d_aug = torch.empty((H, dk), **f32)
     dinit = torch.empty((B, H, dk, dv), **f32) if want_d_init_state else None
+    if gate is not None and tuple(gate.shape) != (B, H, T):
+        raise ValueError(f"gate must be [B,H,T] = {(B, H, T)}, got {tuple(gate.shape)}")
     ws = _workspace(load().gla_chunk_bwd_workspace_size(B, T, H, dk, dv, code), q.device, workspace)
     rc = load().gla_chunk_bwd(
         _dev(q, "q"), _dev(k, "k", q.dtype), _dev(v, "v", q.dtype), code,
         _dev(log_decay, "log_decay", torch.float32), _dev(aug_balance, "aug_balance", torch.float32),
         _dev(init_state, "init_state", torch.float32), _dev(dO, "dO", q.dtype),
-        _dev(d_final_state, "d_final_state", torch.float32), _dev(dq, "dq"), _dev(dk_, "dk"),
+        _dev(d_final_state, "d_final_state", torch.float32), _dev(gate, "gate", torch.float32),
+        _dev(dq, "dq"), _dev(dk_, "dk"),
         _dev(dv_, "dv"), _dev(d_aug, "d_aug"), _dev(dinit, "d_init_state"), _dev(ws, "workspace"),
         0 if ws is None else ws.numel() * ws.element_size(), B, T, H, dk, dv, _stream(stream))
     _check("gla_chunk_bwd", rc)

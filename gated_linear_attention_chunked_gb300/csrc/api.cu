@@ -16,6 +16,7 @@ std::atomic<unsigned long long> g_wait_ns{2000000000ull};
 std::atomic<int> g_split_parts{0};  // gla_set_split_parts: 0 automatic, 1 never, p >= 2 forced
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 bool aligned256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
 size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
 
@@ -90,13 +91,13 @@ gla_status chunk_fwd_impl(const void* q, const void* k, const void* v, gla_dtype
                           const float* init_state, float* o, float* final_state, void* workspace,
                           size_t workspace_bytes, int B, int T, int H, int dk, int dv,
                           const gla::StatePages& sp, cudaStream_t stream,
-                          const gla::OutGate& og = gla::OutGate{}) {
+                          const gla::OutGate& og = gla::OutGate{}, float* gate = nullptr) {
   gla_status st = check_chunk_sizes(B, T, H, dk, dv, in_dtype);
   if (st != GLA_OK) return st;
   if (!q || !k || !v || !log_decay || !aug_balance || (!o && !og.g)) return GLA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(log_decay) ||
       !aligned16(aug_balance) || !aligned16(init_state) || !aligned16(o) ||
-      !aligned16(final_state))
+      !aligned16(final_state) || !aligned4(gate))
     return GLA_ERR_ALIGNMENT;
   const size_t must = fwd_min_workspace(B, T, H, in_dtype);
   if (must && (!workspace || workspace_bytes < must)) return GLA_ERR_WORKSPACE;
@@ -115,7 +116,7 @@ gla_status chunk_fwd_impl(const void* q, const void* k, const void* v, gla_dtype
   gla::FwdArgs a;
   a.q = q; a.k = k; a.v = v; a.bf16 = in_dtype == GLA_BF16;
   a.log_decay = log_decay; a.aug = aug_balance; a.init = init_state;
-  a.o = o; a.fin = final_state; a.B = B; a.T = T; a.H = H; a.sp = sp; a.og = og;
+  a.o = o; a.fin = final_state; a.B = B; a.T = T; a.H = H; a.sp = sp; a.og = og; a.gate = gate;
   if (in_dtype == GLA_FP32) {
     const size_t tok = (size_t)B * T * H;
     uint8_t* w = static_cast<uint8_t*>(workspace);
@@ -225,11 +226,12 @@ size_t gla_chunk_fwd_workspace_size(int B, int T, int H, int dk, int dv, gla_dty
 
 gla_status gla_chunk_fwd(const void* q, const void* k, const void* v, gla_dtype in_dtype,
                          const float* log_decay, const float* aug_balance,
-                         const float* init_state, float* o, float* final_state, void* workspace,
-                         size_t workspace_bytes, int B, int T, int H, int dk, int dv,
-                         cudaStream_t stream) {
+                         const float* init_state, float* o, float* final_state, float* gate,
+                         void* workspace, size_t workspace_bytes, int B, int T, int H, int dk,
+                         int dv, cudaStream_t stream) {
   return chunk_fwd_impl(q, k, v, in_dtype, log_decay, aug_balance, init_state, o, final_state,
-                        workspace, workspace_bytes, B, T, H, dk, dv, gla::StatePages{}, stream);
+                        workspace, workspace_bytes, B, T, H, dk, dv, gla::StatePages{}, stream,
+                        gla::OutGate{}, gate);
 }
 
 gla_status gla_chunk_fwd_gated(const void* q, const void* k, const void* v, gla_dtype in_dtype,
@@ -303,7 +305,8 @@ gla_status gla_chunk_split_plan(int B, int T, int H, int backward, int n_sm, int
 gla_status gla_chunk_bwd(const void* q, const void* k, const void* v, gla_dtype in_dtype,
                          const float* log_decay, const float* aug_balance,
                          const float* init_state, const void* dO, const float* d_final_state,
-                         float* dq, float* dk, float* dv, float* d_aug, float* d_init_state,
+                         const float* gate, float* dq, float* dk, float* dv, float* d_aug,
+                         float* d_init_state,
                          void* workspace, size_t workspace_bytes, int B, int T, int H, int dk_,
                          int dv_, cudaStream_t stream) {
   gla_status st = check_chunk_sizes(B, T, H, dk_, dv_, in_dtype);
@@ -313,7 +316,7 @@ gla_status gla_chunk_bwd(const void* q, const void* k, const void* v, gla_dtype 
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(log_decay) ||
       !aligned16(aug_balance) || !aligned16(init_state) || !aligned16(dO) ||
       !aligned16(d_final_state) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
-      !aligned16(d_aug) || !aligned16(d_init_state))
+      !aligned16(d_aug) || !aligned16(d_init_state) || !aligned4(gate))
     return GLA_ERR_ALIGNMENT;
   const size_t need = bwd_min_workspace(B, T, H, in_dtype);
   if (need && (!workspace || workspace_bytes < need)) return GLA_ERR_WORKSPACE;
@@ -332,7 +335,7 @@ gla_status gla_chunk_bwd(const void* q, const void* k, const void* v, gla_dtype 
   gla::BwdArgs a;
   a.q = q; a.k = k; a.v = v; a.dO = dO; a.bf16 = in_dtype == GLA_BF16;
   a.log_decay = log_decay; a.aug = aug_balance; a.init = init_state; a.dfin = d_final_state;
-  a.dq = dq; a.dk = dk; a.dv = dv; a.d_aug = d_aug; a.dinit = d_init_state;
+  a.dq = dq; a.dk = dk; a.dv = dv; a.d_aug = d_aug; a.dinit = d_init_state; a.gate = gate;
   a.workspace = workspace; a.workspace_bytes = gla::chunk_bwd_workspace_bytes(B, T, H);
   a.B = B; a.T = T; a.H = H;
   if (in_dtype == GLA_FP32) {

@@ -103,6 +103,7 @@ struct BwdParams {
   const float* seg_state;  // cut pairs: state entering each part (DQ's start)
   const float* seg_adj;    // cut pairs: adjoint leaving each part (DV's and DK's start)
   float* da_split;         // cut pairs: d_aug partial sums per part, [96] each
+  const float* gate;       // [B,H,T] sigmoid(z) saved by the forward, or null (recomputed)
 };
 
 enum Tile : int { T_Q = 0, T_K = 1, T_V = 2, T_G = 3 };
@@ -154,7 +155,9 @@ __device__ __forceinline__ float max16(const float* v) {
   return m;
 }
 
-template <int ROLE, bool BF16>
+// SAVED: the gate sigmoid(z) comes from p.gate (saved by the forward) instead of being
+// recomputed; a template parameter so that each variant gets its own register allocation.
+template <int ROLE, bool BF16, bool SAVED>
 __device__ __forceinline__ void run_role(
     uint8_t* base, const Cta& cta, int bh, int c0, int n, int cut_idx, const BwdParams& p,
     const CUtensorMap& map_q,
@@ -500,19 +503,27 @@ __device__ __forceinline__ void run_role(
       const uint32_t par = t & 1;
       const int c = chunk_at<ROLE>(t, c0, n);
       const float lk = c == nc - 1 ? lk_last : lk_full;
+      // the saved gate of this row (issued before the waits; rows past T, all zeros, have
+      // sigmoid(0))
+      float sg_saved = 0.5f;
+      if (SAVED && c * C + i < T) sg_saved = __ldg(p.gate + (size_t)bh * T + c * C + i);
       if (!(ok = wait(cta, cta.bar(FULL_E), par, ctl))) break;
       if (!(ok = wait(cta, cta.bar(FULL_L), par, ctl))) break;
-      // ---- gate partial sum z = q.(a*k) over this part's 24 channels, fused with the fp16
-      // copy of whichever of q, k the score MMA does not read (DQ: k, DK: q, both scale 1);
-      // DV's score reads both, so DV converts them once the score MMA is done
+      // ---- gate partial sum z = q.(a*k) over this part's 24 channels (unless the gate is
+      // given), fused with the fp16 copy of whichever of q, k the score MMA does not read
+      // (DQ: k, DK: q, both scale 1); DV's score reads both, so DV converts them once the
+      // score MMA is done
       float amax = 0.f, bmax = 0.f;  // A and B operands of the state MMA
       uint4 xq[3], xk[3];
-      {
+      if (!SAVED || ROLE == R_DK) {
 #pragma unroll
-        for (int cc = 0; cc < 3; ++cc) {
-          xq[cc] = *(const uint4*)(base + OFF_Q + qk(cc));
-          xk[cc] = *(const uint4*)(base + OFF_K + qk(cc));
-        }
+        for (int cc = 0; cc < 3; ++cc) xq[cc] = *(const uint4*)(base + OFF_Q + qk(cc));
+      }
+      if (!SAVED || ROLE == R_DQ) {
+#pragma unroll
+        for (int cc = 0; cc < 3; ++cc) xk[cc] = *(const uint4*)(base + OFF_K + qk(cc));
+      }
+      if (!SAVED) {
         float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
         for (int cc = 0; cc < 3; ++cc) {
@@ -561,10 +572,12 @@ __device__ __forceinline__ void run_role(
           abmax[par * 32 + 16 + warp] = bm;
         }
       }
-      // ---- the row's gate: the four partial sums
-      if (!(ok = wait(cta, cta.bar(QG0 + q4), par, ctl))) break;
-      const float sg =
-          sigmoid((gate_part[i] + gate_part[128 + i]) + (gate_part[256 + i] + gate_part[384 + i]));
+      // ---- the row's gate: the saved one, or the four partial sums
+      float sg = sg_saved;
+      if (!SAVED) {
+        if (!(ok = wait(cta, cta.bar(QG0 + q4), par, ctl))) break;
+        sg = sigmoid((gate_part[i] + gate_part[128 + i]) + (gate_part[256 + i] + gate_part[384 + i]));
+      }
       // ---- masked score copy, scaled by 2^-e of this step's state copy: this part's 16-column
       // blocks hb = sub, sub+4 of the quadrant's rows, packed to fp16 pairs in registers.
       // Block hb's pairs go to 32-bit columns 8hb..8hb+7, inside block hb/2's fp32 columns, so
@@ -747,7 +760,7 @@ __device__ __forceinline__ void run_role(
   }
 }
 
-template <bool BF16>
+template <bool BF16, bool SAVED>
 __global__ void __launch_bounds__(THREADS, 1)
 bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
            const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_g,
@@ -770,13 +783,13 @@ bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
   const int c0 = cut ? part_begin(part, nc, p.plan.parts) : 0;
   const int n = cut ? part_begin(part + 1, nc, p.plan.parts) - c0 : nc;
   if (role == R_DQ)
-    run_role<R_DQ, BF16>(cta.base, cta, bh, c0, n, cut_idx, p, map_q, map_k, map_v, map_g, map_dq,
+    run_role<R_DQ, BF16, SAVED>(cta.base, cta, bh, c0, n, cut_idx, p, map_q, map_k, map_v, map_g, map_dq,
                          map_dinit, ctl);
   else if (role == R_DV)
-    run_role<R_DV, BF16>(cta.base, cta, bh, c0, n, cut_idx, p, map_q, map_k, map_v, map_g, map_dv,
+    run_role<R_DV, BF16, SAVED>(cta.base, cta, bh, c0, n, cut_idx, p, map_q, map_k, map_v, map_g, map_dv,
                          map_dinit, ctl);
   else
-    run_role<R_DK, BF16>(cta.base, cta, bh, c0, n, cut_idx, p, map_q, map_k, map_v, map_g, map_dk,
+    run_role<R_DK, BF16, SAVED>(cta.base, cta, bh, c0, n, cut_idx, p, map_q, map_k, map_v, map_g, map_dk,
                          map_dinit, ctl);
 }
 
@@ -837,7 +850,9 @@ cudaError_t launch_chunk_bwd(const BwdArgs& a, DevCtl ctl, cudaStream_t stream) 
   p.seg_state = a.seg_state;
   p.seg_adj = a.seg_adj;
   p.da_split = a.da_split;
-  auto kern = a.bf16 ? bwd_kernel<true> : bwd_kernel<false>;
+  p.gate = a.gate;
+  auto kern = a.gate ? (a.bf16 ? bwd_kernel<true, true> : bwd_kernel<false, true>)
+                     : (a.bf16 ? bwd_kernel<true, false> : bwd_kernel<false, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const long long grid =

@@ -114,7 +114,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
            const float* __restrict__ aug, const float* __restrict__ init, float* __restrict__ out,
            float* __restrict__ fin, int T, int H, SplitPlan plan,
            const float* __restrict__ seg_init, StatePages sp,
-           const __grid_constant__ CUtensorMap map_y, OutGate og, DevCtl ctl) {
+           const __grid_constant__ CUtensorMap map_y, OutGate og, float* __restrict__ gate_out,
+           DevCtl ctl) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   Cta cta;
   cta.base = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -378,6 +379,12 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
       } else if (hv == 0) {
         if (!wait(cta, cta.bar(ZX0 + q4), par, ctl)) break;
         sg = sigmoid(z + zx[i]);
+      }
+      // the gate, saved for the backward if asked (the warp that holds the whole sum); head
+      // major [B,H,T], so a warp's 32 rows are one contiguous 128-byte store
+      if (gate_out && (CW == 1 || hv == 0)) {
+        const int t = (c0 + c) * C + i;
+        if (t < T) gate_out[((size_t)b * H + h) * T + t] = sg;
       }
       const float psc = pow2i(-es[par]);
       float pmax = 0.f;
@@ -731,9 +738,10 @@ cudaError_t launch_chunk_fwd(const FwdArgs& a, DevCtl ctl, cudaStream_t stream) 
     plan.parts = 1;
   }
   const long long grid = plan.whole + ((long long)a.B * a.H - plan.whole) * plan.parts;
-  kern<<<(unsigned)grid, gated ? Layout<true>::THREADS : Layout<false>::THREADS, SMEM_BYTES, stream>>>(mq, mk, mv, mo, mfin, a.log_decay, a.aug,
+  const unsigned threads = gated ? Layout<true>::THREADS : Layout<false>::THREADS;
+  kern<<<(unsigned)grid, threads, SMEM_BYTES, stream>>>(mq, mk, mv, mo, mfin, a.log_decay, a.aug,
                                                         a.init, a.o, a.fin, a.T, a.H, plan,
-                                                        a.seg_init, a.sp, my, a.og, ctl);
+                                                        a.seg_init, a.sp, my, a.og, a.gate, ctl);
   return cudaGetLastError();
 }
 

@@ -78,6 +78,7 @@ struct FwdArgs {
   const float* seg_init = nullptr;
   StatePages sp;  // with sp.page: init and fin are the pool (see StatePages)
   OutGate og;     // with og.g: the fused output epilogue (o written only if og.want_o)
+  float* gate = nullptr;  // [B,H,T] or null: sigmoid(z) per head and token, written
 };
 // Returns cudaErrorInvalidValue if a tensor map cannot be encoded.
 cudaError_t launch_chunk_fwd(const FwdArgs& a, DevCtl ctl, cudaStream_t stream);
@@ -105,6 +106,8 @@ struct BwdArgs {
   float* seg_state = nullptr;  // the state entering part j (the DQ role's start)
   float* seg_adj = nullptr;    // the adjoint of the state leaving part j (DV, DK roles' start)
   float* da_split = nullptr;   // d_aug partial sums of the parts, [96] each
+  const float* gate = nullptr;  // [B,H,T] or null: sigmoid(z) per head and token, read
+                                // instead of recomputing the gate
 };
 size_t chunk_bwd_workspace_bytes(int B, int T, int H);
 

@@ -48,9 +48,9 @@ extern "C" {
 gla_status gla_chunk_bwd_noalloc(const void* q, const void* k, const void* v, gla_dtype in_dtype,
                                  const float* log_decay, const float* aug_balance,
                                  const float* init_state, const void* dO,
-                                 const float* d_final_state, float* dq, float* dk, float* dv,
-                                 float* d_aug, float* d_init_state, int B, int T, int H, int dk_,
-                                 int dv_, cudaStream_t stream) {
+                                 const float* d_final_state, const float* gate, float* dq,
+                                 float* dk, float* dv, float* d_aug, float* d_init_state, int B,
+                                 int T, int H, int dk_, int dv_, cudaStream_t stream) {
   if (B <= 0 || T <= 0 || H <= 0) return GLA_ERR_INVALID_ARG;
   if (dk_ != gla::kDK || dv_ != gla::kDV) return GLA_ERR_UNSUPPORTED;
   if (in_dtype != GLA_BF16 && in_dtype != GLA_FP16) return GLA_ERR_UNSUPPORTED;
@@ -61,7 +61,8 @@ gla_status gla_chunk_bwd_noalloc(const void* q, const void* k, const void* v, gl
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(log_decay) ||
       !aligned16(aug_balance) || !aligned16(init_state) || !aligned16(dO) ||
       !aligned16(d_final_state) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
-      !aligned16(d_aug) || !aligned16(d_init_state))
+      !aligned16(d_aug) || !aligned16(d_init_state) ||
+      (reinterpret_cast<uintptr_t>(gate) & 3u) != 0)
     return GLA_ERR_ALIGNMENT;
   void* scratch = nullptr;
   if (scratch_address(&scratch) != GLA_OK) return GLA_ERR_CUDA;
@@ -71,7 +72,7 @@ gla_status gla_chunk_bwd_noalloc(const void* q, const void* k, const void* v, gl
   gla::BwdArgs a;
   a.q = q; a.k = k; a.v = v; a.dO = dO; a.bf16 = in_dtype == GLA_BF16;
   a.log_decay = log_decay; a.aug = aug_balance; a.init = init_state; a.dfin = d_final_state;
-  a.dq = dq; a.dk = dk; a.dv = dv; a.d_aug = d_aug; a.dinit = d_init_state;
+  a.dq = dq; a.dk = dk; a.dv = dv; a.d_aug = d_aug; a.dinit = d_init_state; a.gate = gate;
   // Every partial sum the reduction reads is written by this call's kernel first, so the
   // contents left by an earlier call never need clearing.
   a.workspace = scratch;

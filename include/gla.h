@@ -121,6 +121,10 @@ GLA_API gla_status gla_decay_schedule(int H, double t_min, double t_max, float* 
  *   init_state   [B,H,96,192] fp32 or NULL   (read only)
  *   o            [B,T,H,192] fp32 (written)
  *   final_state  [B,H,96,192] fp32 or NULL   (written)
+ *   gate         [B,H,T] fp32 or NULL (written: sigmoid(z_t), z_t = q_t . (a_h * k_t), the
+ *                self-augmentation gate, head-major so that a chunk's values are contiguous;
+ *                4-byte aligned) -- an activation a training step saves for gla_chunk_bwd,
+ *                which then need not recompute it
  *   workspace    device scratch, 256-byte aligned, of gla_chunk_fwd_workspace_size()
  *                bytes.  fp32 inputs need their fp16 copies there (GLA_ERR_WORKSPACE
  *                if it is smaller).  The size also covers cutting pairs into parts:
@@ -138,9 +142,9 @@ GLA_API gla_status gla_decay_schedule(int H, double t_min, double t_max, float* 
 GLA_API size_t gla_chunk_fwd_workspace_size(int B, int T, int H, int dk, int dv, gla_dtype in_dtype);
 GLA_API gla_status gla_chunk_fwd(const void* q, const void* k, const void* v, gla_dtype in_dtype,
                          const float* log_decay, const float* aug_balance,
-                         const float* init_state, float* o, float* final_state, void* workspace,
-                         size_t workspace_bytes, int B, int T, int H, int dk, int dv,
-                         cudaStream_t stream);
+                         const float* init_state, float* o, float* final_state, float* gate,
+                         void* workspace, size_t workspace_bytes, int B, int T, int H, int dk,
+                         int dv, cudaStream_t stream);
 
 /* gla_chunk_fwd_gated: the same forward with the mixer's output epilogue fused
  * into it ("GLA mixer": a Head RMSNorm shared within each decay tier, then the
@@ -176,6 +180,9 @@ GLA_API gla_status gla_chunk_fwd_gated(const void* q, const void* k, const void*
  *   q, k, v, in_dtype, log_decay, aug_balance, init_state: as in the forward
  *   dO            [B,T,H,192] in_dtype
  *   d_final_state [B,H,96,192] fp32 or NULL (= zeros)
+ *   gate          [B,H,T] fp32 or NULL: sigmoid(z_t) as gla_chunk_fwd writes it (4-byte
+ *                 aligned); given, the backward reads it instead of recomputing z_t (the
+ *                 results then follow the values given); NULL: recomputed
  *   dq, dk        [B,T,H,96]  fp32 (written)    dv [B,T,H,192] fp32 (written)
  *   d_aug         [H,96] fp32 (written, summed over B and T)
  *   d_init_state  [B,H,96,192] fp32 or NULL (written)
@@ -190,7 +197,8 @@ GLA_API size_t gla_chunk_bwd_workspace_size(int B, int T, int H, int dk, int dv,
 GLA_API gla_status gla_chunk_bwd(const void* q, const void* k, const void* v, gla_dtype in_dtype,
                          const float* log_decay, const float* aug_balance,
                          const float* init_state, const void* dO, const float* d_final_state,
-                         float* dq, float* dk, float* dv, float* d_aug, float* d_init_state,
+                         const float* gate, float* dq, float* dk, float* dv, float* d_aug,
+                         float* d_init_state,
                          void* workspace, size_t workspace_bytes, int B, int T, int H,
                          int dk_, int dv_, cudaStream_t stream);
 
@@ -236,10 +244,10 @@ GLA_API gla_status gla_set_split_parts(int parts);
 GLA_API gla_status gla_chunk_bwd_noalloc(const void* q, const void* k, const void* v,
                                          gla_dtype in_dtype, const float* log_decay,
                                          const float* aug_balance, const float* init_state,
-                                         const void* dO, const float* d_final_state, float* dq,
-                                         float* dk, float* dv, float* d_aug,
-                                         float* d_init_state, int B, int T, int H, int dk_,
-                                         int dv_, cudaStream_t stream);
+                                         const void* dO, const float* d_final_state,
+                                         const float* gate, float* dq, float* dk, float* dv,
+                                         float* d_aug, float* d_init_state, int B, int T, int H,
+                                         int dk_, int dv_, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
  * One recurrent decode step for a pool of N sequences x L layers x H heads

@@ -108,6 +108,15 @@ def fwd(q, k, v, gamma, a, init_state=None, nthreads: int = 0, lib=None):
     return o, fin
 
 
+def gate(q, k, a):
+    """The self-augmentation gate sigmoid(z_t), z_t = sum_c a_hc q_tc k_tc ("GLA mixer":
+    the value skip weighted by the sigmoid of q against the balanced k), in fp64 numpy.
+    q, k [B,T,H,dk]; a [H,dk]; returns [B,T,H] -- what the forward saves for the backward."""
+    q, k, a = (np.asarray(x, np.float64) for x in (q, k, a))
+    z = np.einsum("bthc,hc,bthc->bth", q, a, k)
+    return 1.0 / (1.0 + np.exp(-z))
+
+
 def bwd(q, k, v, gamma, a, dO, init_state=None, d_final_state=None, nthreads: int = 0, lib=None):
     """Hand-derived backward.  Returns dict dq, dk, dv, d_a [H,dk], d_init_state [B,H,dk,dv]."""
     lib = lib or load()

@@ -66,9 +66,10 @@ def test_decay_schedule_rejects(lib):
 A16 = 0x1000  # a 16-byte aligned fake address; never dereferenced by the checks below
 
 
-def fwd(lib, q=A16, k=A16, v=A16, dt=0, ld=A16, a=A16, init=None, o=A16, fin=None, ws=None,
-        wsb=0, B=1, T=128, H=1, dk=96, dv=192):
-    return lib.gla_chunk_fwd(q, k, v, dt, ld, a, init, o, fin, ws, wsb, B, T, H, dk, dv, None)
+def fwd(lib, q=A16, k=A16, v=A16, dt=0, ld=A16, a=A16, init=None, o=A16, fin=None, gate=None,
+        ws=None, wsb=0, B=1, T=128, H=1, dk=96, dv=192):
+    return lib.gla_chunk_fwd(q, k, v, dt, ld, a, init, o, fin, gate, ws, wsb, B, T, H, dk, dv,
+                             None)
 
 
 def test_chunk_fwd_argument_checks(lib):
@@ -81,6 +82,7 @@ def test_chunk_fwd_argument_checks(lib):
     assert fwd(lib, q=None) == 1 and fwd(lib, o=None) == 1 and fwd(lib, a=None) == 1
     assert fwd(lib, q=A16 + 8) == 3                  # misaligned
     assert fwd(lib, init=A16 + 4) == 3
+    assert fwd(lib, gate=A16 + 2) == 3               # the saved gate: 4-byte aligned fp32
     # fp32 inputs need a workspace for their fp16 copies
     assert gla.chunk_fwd_workspace_size(1, 128, 1, gla.GLA_FP32) > 0
     assert gla.chunk_fwd_workspace_size(1, 128, 1, gla.GLA_BF16) == 0
@@ -91,13 +93,14 @@ def test_chunk_fwd_argument_checks(lib):
 
 
 def test_chunk_bwd_argument_checks(lib):
-    def bwd(dO=A16, dq=A16, dk_=64, T=128, d_aug=A16):
-        return lib.gla_chunk_bwd(A16, A16, A16, 0, A16, A16, None, dO, None, dq, A16, A16, d_aug,
-                                 None, None, 0, 1, T, 1, dk_, 192, None)
+    def bwd(dO=A16, dq=A16, dk_=64, T=128, d_aug=A16, gate=None):
+        return lib.gla_chunk_bwd(A16, A16, A16, 0, A16, A16, None, dO, None, gate, dq, A16, A16,
+                                 d_aug, None, None, 0, 1, T, 1, dk_, 192, None)
     assert bwd() == 2
     assert bwd(dk_=96, T=100, dq=A16 + 2) == 3         # any T: the sizes pass
     assert bwd(dk_=96, dO=None) == 1
     assert bwd(dk_=96, d_aug=None) == 1
+    assert bwd(dk_=96, gate=A16 + 1) == 3
     assert bwd(dk_=96, dq=A16 + 2) == 3
 
 

@@ -26,7 +26,7 @@ def _lib():
     _build.build()
     lib = gla.load()
     fn = lib.gla_chunk_bwd_noalloc
-    fn.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] + [ctypes.c_void_p] * 10 + \
+    fn.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] + [ctypes.c_void_p] * 11 + \
         [ctypes.c_int] * 5 + [ctypes.c_void_p]
     fn.restype = ctypes.c_int
     return gla, fn
@@ -34,7 +34,7 @@ def _lib():
 
 def test_noalloc_rejects_sizes_beyond_its_array_and_fp32_inputs():
     _, fn = _lib()
-    args = [A16] * 3 + [0] + [A16] * 10
+    args = [A16] * 3 + [0] + [A16] * 11
     # B * H = 2049 > the fixed scratch: refused before anything is launched
     assert fn(*args, 2049, 128, 1, 96, 192, None) == GLA_ERR_WORKSPACE
     assert fn(*args, 129, 128, 16, 96, 192, None) == GLA_ERR_WORKSPACE
@@ -67,7 +67,7 @@ def test_noalloc_matches_workspace_backward_on_two_calls_in_a_row():
                torch.full((H, 96), float("nan"), **f32),
                torch.full((B, H, 96, 192), float("nan"), **f32)]
         rc = fn(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), gla.GLA_BF16, gam.data_ptr(),
-                ad.data_ptr(), id_.data_ptr(), gd.data_ptr(), fd.data_ptr(),
+                ad.data_ptr(), id_.data_ptr(), gd.data_ptr(), fd.data_ptr(), None,
                 *[x.data_ptr() for x in out], B, T, H, 96, 192, stream)
         assert rc == 0, gla.status_string(rc)
         torch.cuda.synchronize()
