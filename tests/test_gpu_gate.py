@@ -39,6 +39,8 @@ CASES = [
     (2, 700, 2, "bf16", 3, 73),     # pairs cut into 3 parts, ragged
     (1, 384, 2, "fp16", 0, 74),
     (1, 200, 2, "fp32", 0, 75),
+    (2, 1, 3, "bf16", 0, 78),       # a single token per sequence
+    (2, 77, 3, "bf16", 0, 79),      # one partial chunk
 ]
 
 
@@ -140,3 +142,32 @@ def test_no_workspace_backward_reads_the_gate(env):
     assert gla.get_device_error() == 0
     for name, x, r in zip(NAMES, out, ref):
         assert torch.equal(x, r), f"{name} differs between the no-workspace and workspace calls"
+
+
+def test_saved_gate_at_the_training_shape(env):
+    """B=8, T=2048, H=16 (one training-shape layer): the backward that reads the forward's gate
+    against the one that recomputes it (they differ only by the rounding of the gate's dot
+    product), and the gate against the oracle's on sampled rows."""
+    import oracle
+    gla, torch = env
+    B, T, H, seed = 8, 2048, 16, 80
+    q, k, v = synth.qkv(seed, B, T, H)
+    dO = synth.grad_out(seed, B, T, H)
+    a = synth.aug_balance(seed, (H, 96), 0.02)
+    qd, kd, vd, gd = (to_dev(x, torch.bfloat16) for x in (q, k, v, dO))
+    ad = to_dev(a, torch.float32)
+    gam = gla.decay_schedule(H).cuda()
+    gate = torch.empty((B, H, T), dtype=torch.float32, device="cuda")
+    gla.chunk_fwd(qd, kd, vd, gam, ad, gate=gate)
+    g_saved = gla.chunk_bwd(qd, kd, vd, gam, ad, gd, gate=gate)
+    g_rec = gla.chunk_bwd(qd, kd, vd, gam, ad, gd)
+    torch.cuda.synchronize()
+    assert gla.get_device_error() == 0
+    vs_rec = {n: rel_err(x.cpu().numpy(), y.cpu().numpy()) for n, x, y in zip(NAMES, g_saved, g_rec)}
+    rows = np.random.default_rng(seed).integers(0, T, 64)
+    g_ref = oracle.gate(q[:, rows], k[:, rows], a)  # [B, 64, H]
+    eg = float(np.abs(gate.cpu().numpy()[:, :, rows] - g_ref.transpose(0, 2, 1)).max())
+    print(f"saved gate B={B} T={T} H={H}: gate {eg:.1e} | vs recomputed " +
+          " ".join(f"{n} {e:.1e}" for n, e in vs_rec.items()))
+    assert eg <= GATE_TOL["bf16"]
+    assert all(e <= 1e-3 for e in vs_rec.values()), vs_rec
