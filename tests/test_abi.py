@@ -247,3 +247,17 @@ def test_split_plan_invariants(lib):
                 assert rem and cut == -(-rem // roles)
     finally:
         lib.gla_set_split_parts(0)
+
+
+def test_binding_checks_the_gate_shape():
+    """The saved gate is head-major [B,H,T]; the binding refuses any other shape before it
+    touches a device (so this runs on the CPU)."""
+    import torch
+    B, T, H = 2, 256, 3
+    q = torch.zeros(B, T, H, 96, dtype=torch.bfloat16)
+    v = torch.zeros(B, T, H, 192, dtype=torch.bfloat16)
+    lg, a = torch.zeros(H), torch.zeros(H, 96)
+    with pytest.raises(ValueError, match=r"gate must be \[B,H,T\]"):
+        gla.chunk_fwd(q, q, v, lg, a, gate=torch.zeros(B, T, H))
+    with pytest.raises(ValueError, match=r"gate must be \[B,H,T\]"):
+        gla.chunk_bwd(q, q, v, lg, a, v, gate=torch.zeros(B, T, H))
