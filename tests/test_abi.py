@@ -261,3 +261,22 @@ def test_binding_checks_the_gate_shape():
         gla.chunk_fwd(q, q, v, lg, a, gate=torch.zeros(B, T, H))
     with pytest.raises(ValueError, match=r"gate must be \[B,H,T\]"):
         gla.chunk_bwd(q, q, v, lg, a, v, gate=torch.zeros(B, T, H))
+
+
+def test_binding_argument_lists_match_the_header():
+    """Every entry point the binding declares takes as many arguments as include/gla.h gives
+    it (a parameter added to one and not the other would shift every argument after it)."""
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    src = open(os.path.join(root, "include", "gla.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    decls = dict(re.findall(r"GLA_API\s+[\w\s\*]+?\b(gla_\w+)\s*\(([^)]*)\)\s*;", src))
+    lib = gla.load()
+    checked = 0
+    for name, params in decls.items():
+        argtypes = getattr(lib, name).argtypes
+        if argtypes is None:  # not declared by the binding (called only from C)
+            continue
+        n = 0 if params.strip() in ("", "void") else params.count(",") + 1
+        assert len(argtypes) == n, f"{name}: header {n} parameters, binding {len(argtypes)}"
+        checked += 1
+    assert checked >= 15, checked
