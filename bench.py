@@ -2,7 +2,9 @@
 
 One step = the whole hot path on its two workloads:
   * chunked forward + backward at the training shape B=32, T=2048, H=16, dk=96, dv=192
-    (bf16 inputs, fp32 outputs) -- `value` is its throughput in tokens/s;
+    (bf16 inputs, fp32 outputs; the forward saves the gate sigmoid(q.(a*k)) and the backward
+    reads it, as a training step keeps its saved activations) -- `value` is its throughput in
+    tokens/s;
   * one recurrent decode step over the serving pool of 1,280 sequences x 24 layers x 16
     heads of 96x192 fp32 states (36.2 GB resident in HBM) -- reported in `decode` as GB/s.
 
