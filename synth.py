@@ -95,7 +95,7 @@ def decode_token(seed: int, N: int, L: int, H: int, step: int = 0):
 
 
 # The five workloads.  "seed" keys every stream of that workload.
-CONFIGS = {
+WORKLOADS = {
     "tiny_fp32": dict(B=1, T=256, H=2, dtype="fp32", a_std=0.1, init_std=0.0, seed=0,
                       bwd=True),
     "layer_fwd": dict(B=8, T=2048, H=16, dtype="bf16", a_std=0.0, init_std=0.0, seed=1,
@@ -114,7 +114,7 @@ def chunk_inputs(name: str, B: int | None = None, T: int | None = None):
     """All inputs of a chunked workload (optionally with B or T overridden for a
     smaller case of the same recipe).  float32 arrays; bf16 workloads hold
     bf16-representable values."""
-    c = dict(CONFIGS[name])
+    c = dict(WORKLOADS[name])
     if B is not None:
         c["B"] = B
     if T is not None:
