@@ -19,8 +19,10 @@ reach") and section "Challenge 3" (backward through the sequential updates).
 Pins (tests/test_oracle_*.py): brute-force closed form, central finite
 differences, the printed decay values, the a=0 half value skip, the lambda=1
 reduction to causal linear attention, state-carry and init-zero invariants,
-decode/forward consistency and an independent chunked restatement.  Every
-function here is pinned; none is "parity unpinned".
+decode/forward consistency and an independent chunked restatement; the gate
+(the activation the forward saves) against the forward's own first-token value
+skip and the a=0 half value.  Every function here is pinned; none is "parity
+unpinned".
 """
 from __future__ import annotations
 
