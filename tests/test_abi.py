@@ -280,3 +280,25 @@ def test_binding_argument_lists_match_the_header():
         assert len(argtypes) == n, f"{name}: header {n} parameters, binding {len(argtypes)}"
         checked += 1
     assert checked >= 15, checked
+
+
+def test_header_compiles_as_plain_c(tmp_path):
+    """include/gla.h is a C header (plain pointers, sizes, enums, no C++ or torch types): a C99
+    translation unit that includes it and references every entry point compiles."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    cuda_inc = "/usr/local/cuda/include"
+    if not gcc or not os.path.isdir(cuda_inc):
+        pytest.skip("needs gcc and the CUDA headers")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    hdr = open(os.path.join(root, "include", "gla.h")).read()
+    names = sorted(set(re.findall(r"GLA_API\s+[\w\s\*]+?\b(gla_\w+)\s*\(", hdr)))
+    src = tmp_path / "use_header.c"
+    src.write_text('#include "gla.h"\nvoid* table[] = {\n' +
+                   "".join(f"  (void*){n},\n" for n in names) + "};\nint main(void) { return 0; }\n")
+    r = subprocess.run([gcc, "-std=c99", "-Wall", "-Werror=implicit-function-declaration",
+                        "-fsyntax-only", "-I", os.path.join(root, "include"), "-I", cuda_inc,
+                        str(src)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    assert len(names) >= 20, names
