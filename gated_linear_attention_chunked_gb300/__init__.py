@@ -10,6 +10,8 @@ Functions (same names as the C ABI, without the ``gla_`` prefix):
   chunk_fwd(q, k, v, log_decay, aug_balance, ...)     -> (o, final_state)
   chunk_bwd(q, k, v, log_decay, aug_balance, dO, ...) -> (dq, dk, dv, d_aug, d_init_state)
   decode_step(state, q, k, v, log_decay, aug_balance) -> o  (state updated in place)
+  chunk_state_sum, chunk_adjoint_sum, state_link     (a sequence cut into slices across ranks;
+                                                      seqshard.py runs the exchange)
   get_device_error(), set_wait_timeout_ns(ns), status_string(code)
 """
 from __future__ import annotations
@@ -101,6 +103,14 @@ def load(path: str | None = None):
             lib.gla_chunk_split_plan.restype = _I
             lib.gla_set_split_parts.argtypes = [_I]
             lib.gla_set_split_parts.restype = _I
+            lib.gla_chunk_state_sum.argtypes = [_P, _P, _I, _P, _P] + [_I] * 5 + [_P]
+            lib.gla_chunk_state_sum.restype = _I
+            lib.gla_chunk_adjoint_sum.argtypes = [_P, _P, _I, _P, _P] + [_I] * 5 + [_P]
+            lib.gla_chunk_adjoint_sum.restype = _I
+            lib.gla_state_link.argtypes = [_P, _P, _I, _I, _I, _P, _P, _P] + [_I] * 4 + [_P]
+            lib.gla_state_link.restype = _I
+            lib.gla_chunk_bwd_noalloc.argtypes = [_P] * 3 + [_I] + [_P] * 11 + [_I] * 5 + [_P]
+            lib.gla_chunk_bwd_noalloc.restype = _I
             if path is not None:
                 return lib
             _lib = lib
@@ -436,6 +446,61 @@ def conv_decode_step(state, x, weight, bias=None, *, out=None, stream=None):
                                      _dev(y, "y", f), n, D, _stream(stream))
     _check("gla_conv_decode_step", rc)
     return y
+
+
+def chunk_state_sum(k, v, log_decay, *, out=None, stream=None):
+    """gla_chunk_state_sum: U[b,h] = sum_t lambda_h^(T-1-t) k_t v_t^T over the T tokens given
+    (k [B,T,H,96], v [B,T,H,192], bf16 or fp16).  Returns U fp32 [B,H,96,192]."""
+    torch = _torch()
+    B, T, H, dk = k.shape
+    dv = v.shape[-1]
+    f = torch.float32
+    if out is None:
+        out = torch.empty((B, H, dk, dv), dtype=f, device=k.device)
+    rc = load().gla_chunk_state_sum(_dev(k, "k"), _dev(v, "v", k.dtype), _dtype_code(k),
+                                    _dev(log_decay, "log_decay", f), _dev(out, "U", f), B, T, H,
+                                    dk, dv, _stream(stream))
+    _check("gla_chunk_state_sum", rc)
+    return out
+
+
+def chunk_adjoint_sum(q, dO, log_decay, *, out=None, stream=None):
+    """gla_chunk_adjoint_sum: U'[b,h] = sum_t lambda_h^(t+1) q_t dO_t^T (q [B,T,H,96], dO
+    [B,T,H,192], bf16 or fp16).  Returns U' fp32 [B,H,96,192]."""
+    torch = _torch()
+    B, T, H, dk = q.shape
+    dv = dO.shape[-1]
+    f = torch.float32
+    if out is None:
+        out = torch.empty((B, H, dk, dv), dtype=f, device=q.device)
+    rc = load().gla_chunk_adjoint_sum(_dev(q, "q"), _dev(dO, "dO", q.dtype), _dtype_code(q),
+                                      _dev(log_decay, "log_decay", f), _dev(out, "U", f), B, T,
+                                      H, dk, dv, _stream(stream))
+    _check("gla_chunk_adjoint_sum", rc)
+    return out
+
+
+def state_link(U_all, lens, slice_index, log_decay, boundary=None, *, reverse=False, out=None,
+               stream=None):
+    """gla_state_link: the state entering slice `slice_index` (reverse=False; boundary = the
+    initial state) or the adjoint of the state leaving it (reverse=True; boundary =
+    d_final_state) of a sequence cut into slices of `lens` tokens, from every slice's sums
+    U_all fp32 [n_slices,B,H,96,192].  Returns fp32 [B,H,96,192]."""
+    torch = _torch()
+    n, B, H, dk, dv = U_all.shape
+    lens = [int(x) for x in lens]
+    if len(lens) != n:
+        raise ValueError(f"lens must have {n} entries")
+    f = torch.float32
+    if out is None:
+        out = torch.empty((B, H, dk, dv), dtype=f, device=U_all.device)
+    host_lens = (ctypes.c_int * n)(*lens)
+    rc = load().gla_state_link(_dev(U_all, "U_all", f), ctypes.addressof(host_lens), n,
+                               int(slice_index), 1 if reverse else 0,
+                               _dev(log_decay, "log_decay", f), _dev(boundary, "boundary", f),
+                               _dev(out, "out", f), B, H, dk, dv, _stream(stream))
+    _check("gla_state_link", rc)
+    return out
 
 
 def get_device_error() -> int:

@@ -367,6 +367,62 @@ gla_status gla_chunk_bwd(const void* q, const void* k, const void* v, gla_dtype 
   return gla::launch_chunk_bwd(a, ctl, stream) == cudaSuccess ? GLA_OK : GLA_ERR_CUDA;
 }
 
+gla_status gla_chunk_state_sum(const void* k, const void* v, gla_dtype in_dtype,
+                               const float* log_decay, float* U, int B, int T, int H, int dk,
+                               int dv, cudaStream_t stream) {
+  gla_status st = check_chunk_sizes(B, T, H, dk, dv, in_dtype);
+  if (st != GLA_OK) return st;
+  if (in_dtype == GLA_FP32) return GLA_ERR_UNSUPPORTED;
+  if (!k || !v || !log_decay || !U) return GLA_ERR_INVALID_ARG;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(log_decay) || !aligned16(U))
+    return GLA_ERR_ALIGNMENT;
+  gla::DevCtl ctl;
+  if ((st = ctl_for_current_device(&ctl)) != GLA_OK) return st;
+  return gla::launch_slice_sums(k, v, in_dtype == GLA_BF16, false, log_decay, U, B, T, H, ctl,
+                                stream) == cudaSuccess
+             ? GLA_OK
+             : GLA_ERR_CUDA;
+}
+
+gla_status gla_chunk_adjoint_sum(const void* q, const void* dO, gla_dtype in_dtype,
+                                 const float* log_decay, float* U, int B, int T, int H, int dk,
+                                 int dv, cudaStream_t stream) {
+  gla_status st = check_chunk_sizes(B, T, H, dk, dv, in_dtype);
+  if (st != GLA_OK) return st;
+  if (in_dtype == GLA_FP32) return GLA_ERR_UNSUPPORTED;
+  if (!q || !dO || !log_decay || !U) return GLA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(dO) || !aligned16(log_decay) || !aligned16(U))
+    return GLA_ERR_ALIGNMENT;
+  gla::DevCtl ctl;
+  if ((st = ctl_for_current_device(&ctl)) != GLA_OK) return st;
+  return gla::launch_slice_sums(q, dO, in_dtype == GLA_BF16, true, log_decay, U, B, T, H, ctl,
+                                stream) == cudaSuccess
+             ? GLA_OK
+             : GLA_ERR_CUDA;
+}
+
+gla_status gla_state_link(const float* U_all, const int* lens, int n_slices, int slice,
+                          int reverse, const float* log_decay, const float* boundary, float* out,
+                          int B, int H, int dk, int dv, cudaStream_t stream) {
+  if (B <= 0 || H <= 0 || n_slices <= 0 || slice < 0 || slice >= n_slices)
+    return GLA_ERR_INVALID_ARG;
+  if (dk != gla::kDK || dv != gla::kDV || n_slices > gla::kMaxShards) return GLA_ERR_UNSUPPORTED;
+  if ((long long)B * H > 65535) return GLA_ERR_UNSUPPORTED;
+  if (!U_all || !lens || !log_decay || !out) return GLA_ERR_INVALID_ARG;
+  if (!aligned16(U_all) || !aligned16(log_decay) || !aligned16(boundary) || !aligned16(out))
+    return GLA_ERR_ALIGNMENT;
+  gla::ShardLens L;
+  L.n = n_slices;
+  for (int j = 0; j < n_slices; ++j) {
+    if (lens[j] <= 0) return GLA_ERR_INVALID_ARG;
+    L.len[j] = lens[j];
+  }
+  return gla::launch_shard_link(U_all, L, slice, reverse != 0, log_decay, boundary, out, B, H,
+                                stream) == cudaSuccess
+             ? GLA_OK
+             : GLA_ERR_CUDA;
+}
+
 gla_status gla_decode_step(float* state, const float* q, const float* k, const float* v,
                            const float* log_decay, const float* aug_balance, float* o, int N,
                            int L, int H, int dk, int dv, cudaStream_t stream) {

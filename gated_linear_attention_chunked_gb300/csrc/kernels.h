@@ -130,6 +130,24 @@ cudaError_t launch_segment_states(const void* q, const void* k, const void* v, c
                                   float* adj, int B, int T, int H, const SplitPlan& plan,
                                   DevCtl ctl, cudaStream_t stream);
 
+// ---- sequence-sharded calls (seg_scan.cu): a sequence cut into consecutive slices, one per
+// rank.  launch_slice_sums: per (b, h) of this rank's slice of T tokens, U = sum_t
+// lambda^(T-1-t) k_t v_t^T (reverse == false; a = k, b = v) or U' = sum_t lambda^(t+1) q_t dO_t^T
+// (reverse; a = q, b = dO), into out [B*H][96][192].  launch_shard_link: the state entering
+// slice `rank` (forward) or the adjoint of the state leaving it (reverse) from all slices' sums
+// U [n][B*H][96][192] and the caller's boundary (initial state / d_final_state, or null).
+constexpr int kMaxShards = 256;
+struct ShardLens {
+  int n = 0;
+  int len[kMaxShards];
+};
+cudaError_t launch_slice_sums(const void* a, const void* b, bool bf16, bool reverse,
+                              const float* log_decay, float* out, int B, int T, int H, DevCtl ctl,
+                              cudaStream_t stream);
+cudaError_t launch_shard_link(const float* U, const ShardLens& lens, int rank, bool reverse,
+                              const float* log_decay, const float* boundary, float* out, int B,
+                              int H, cudaStream_t stream);
+
 // The device error word and wait limit of the current device (defined in api.cu).
 cudaError_t current_device_ctl(DevCtl* ctl);
 cudaError_t launch_chunk_bwd(const BwdArgs& a, DevCtl ctl, cudaStream_t stream);

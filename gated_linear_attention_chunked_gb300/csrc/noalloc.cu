@@ -9,8 +9,6 @@
 // that loads the library holds until the process exits.
 #include <cuda_runtime.h>
 
-#include <mutex>
-
 #include "gla.h"
 #include "kernels.h"
 
@@ -19,23 +17,15 @@ namespace {
 // Scratch for B * H <= GLA_NOALLOC_MAX_BH partial-sum rows of 96 floats (768 KiB).
 static __device__ __align__(256) float g_noalloc_scratch[GLA_NOALLOC_MAX_BH * 96];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void* g_scratch_addr[kMaxDevices] = {};
-
-// Device address of the scratch array on the current device, looked up once per device
-// with that device current.  The array's name in host code is only a stand-in for the
+// Device address of the scratch array in the current device's context, looked up on every
+// call with that device current (the lookup is a cheap table read once the module is loaded,
+// and a context that was reset and created again may place the module elsewhere, so no
+// address is kept between calls).  The array's name in host code is only a stand-in for the
 // symbol; a kernel must be given the address returned here.
 gla_status scratch_address(void** scratch) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GLA_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_addr[dev]) {
-    void* s = nullptr;
-    if (cudaGetSymbolAddress(&s, g_noalloc_scratch) != cudaSuccess || !s) return GLA_ERR_CUDA;
-    g_scratch_addr[dev] = s;
-  }
-  *scratch = g_scratch_addr[dev];
+  void* s = nullptr;
+  if (cudaGetSymbolAddress(&s, g_noalloc_scratch) != cudaSuccess || !s) return GLA_ERR_CUDA;
+  *scratch = s;
   return GLA_OK;
 }
 

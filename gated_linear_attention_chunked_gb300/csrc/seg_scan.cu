@@ -73,12 +73,16 @@ __device__ __forceinline__ uint32_t v_chunk(uint32_t i, int cc) {
 // Pass A.  CTA i < n_fwd: forward sum U_j of part j = i % (p-1) of cut pair x = i / (p-1),
 // into states[x*p + j + 1]; CTA i >= n_fwd: reverse sum U'_j of part j = 1 + i' % (p-1) (i' =
 // i - n_fwd), into adj[x*p + j - 1].  Those slots are then completed by pass B in place.
+// full != 0 (a sequence-sharded call's slice sums): one CTA per pair bh, its one part being
+// the whole sequence; CTA i < n_fwd writes U of pair i into states[i], CTA i >= n_fwd U' of
+// pair i - n_fwd into adj[i - n_fwd].
 template <bool BF16>
 __global__ void __launch_bounds__(THREADS, 1)
 seg_sum_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
                const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_g,
                const float* __restrict__ log_decay, float* __restrict__ states,
-               float* __restrict__ adj, int T, int H, int whole, int parts, int n_fwd, DevCtl ctl) {
+               float* __restrict__ adj, int T, int H, int whole, int parts, int n_fwd, int full,
+               DevCtl ctl) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   Cta cta;
   cta.base = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -93,11 +97,13 @@ seg_sum_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant_
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool rev = (int)blockIdx.x >= n_fwd;
   const int idx = rev ? (int)blockIdx.x - n_fwd : (int)blockIdx.x;
-  const int x = idx / (parts - 1), j = idx % (parts - 1) + (rev ? 1 : 0);
+  const int x = full ? idx : idx / (parts - 1), j = full ? 0 : idx % (parts - 1) + (rev ? 1 : 0);
   const int bh = whole + x, b = bh / H, h = bh % H;
   const int nc = (T + C - 1) / C;
-  const int c_lo = part_begin(j, nc, parts), c_hi = part_begin(j + 1, nc, parts);
+  const int c_lo = full ? 0 : part_begin(j, nc, parts), c_hi = full ? nc : part_begin(j + 1, nc, parts);
   const int M = c_hi - c_lo;  // chunks of the part (>= 1)
+  // tokens of the part's last chunk (C unless it is the sequence's ragged last chunk)
+  const int last_len = min(c_hi * C, T) - (c_hi - 1) * C;
   const CUtensorMap* map_a = rev ? &map_q : &map_k;
   const CUtensorMap* map_b = rev ? &map_g : &map_v;
   const float gamma = __ldg(log_decay + h);
@@ -170,18 +176,24 @@ seg_sum_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant_
   } else {
     // ---- warps 0..3: in-place fp16 operands of chunk m, row i = token i of the chunk: k
     // scaled by lambda^(e_j - t) (forward) or q by lambda^(t - s_j + 1) (reverse), v / dO as
-    // they are.  Rows past T are zeros (the tensor map's fill).
+    // they are.  Rows past T are zeros (the tensor map's fill); in the forward direction e_j
+    // is the part's last token, so a ragged last chunk weighs its rows by
+    // lambda^(last_len - 1 - i) and its rows past T by 0.
     const int i = tid;
     const float lamC = expf((float)C * gamma);
     const float row_w = rev ? (i + 1 < C ? pw[i + 1] : lamC) : pw[C - 1 - i];
+    const float row_w_last = rev ? row_w : (i < last_len ? pw[last_len - 1 - i] : 0.f);
     float vmax = 0.f;
     bool ok = true;
     for (int m = 0; m < M && ok; ++m) {
       const int s = m % STAGES;
       if (!(ok = wait(cta, cta.bar(FULL + s), (m / STAGES) & 1, ctl))) break;
       uint8_t* st = base + s * STAGE;
-      const int whole_chunks = rev ? m : M - 1 - m;  // chunks between this one and s_j (e_j)
-      const float sk = expf(gamma * (float)(C * whole_chunks)) * row_w;
+      // reverse: the chunks between this one and s_j; forward: the tokens after this chunk up
+      // to e_j (whole chunks, then the last chunk's last_len)
+      const float sk = rev ? expf(gamma * (float)(C * m)) * row_w
+                           : (m == M - 1 ? row_w_last
+                                         : expf(gamma * (float)(C * (M - 2 - m) + last_len)) * row_w);
       convert_row<BF16, 12>(st, [&](int cc) { return k_chunk(i, cc); }, sk, vmax);
       convert_row<BF16, 24>(st, [&](int cc) { return v_chunk(i, cc); }, 1.f, vmax);
       fence_proxy_async();
@@ -192,7 +204,7 @@ seg_sum_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant_
     ok = __all_sync(0xffffffffu, ok && *cta.abort_flag() == 0);
     if (ok && warp < 3) {
       tc_fence_after();
-      const long long slot = (long long)x * parts + (rev ? j - 1 : j + 1);
+      const long long slot = full ? (long long)x : (long long)x * parts + (rev ? j - 1 : j + 1);
       float* dst = (rev ? adj : states) + (size_t)slot * DK * DV + (size_t)i * DV;
       const uint32_t trow = tmem + ((uint32_t)(32 * warp) << 16);
 #pragma unroll 1
@@ -267,6 +279,32 @@ __global__ void seg_link_kernel(const float* __restrict__ init, const float* __r
       out[(size_t)j * N4] = s;
     }
   }
+}
+
+// The state entering slice `rank` of a sequence cut into consecutive slices across ranks
+// (forward), or the adjoint of the state leaving it (reverse), from every slice's sum:
+//   forward  S_0 = boundary;      S_{j+1} = lambda^(len_j) S_j + U_j;      out = S_rank
+//   reverse  A_{R-1} = boundary;  A_{j-1} = lambda^(len_j) A_j + U'_j;     out = A_rank
+// U [R][B*H][96*192].  One thread per 4 consecutive state elements, walking the slices in
+// order (the same recurrences as pass B, over slices instead of parts).
+__global__ void shard_link_kernel(const float* __restrict__ U, const float* __restrict__ boundary,
+                                  const float* __restrict__ log_decay, float* __restrict__ out,
+                                  ShardLens lens, int rank, int reverse, int BH, int H) {
+  constexpr int N4 = DK * DV / 4;
+  const int bh = blockIdx.y, e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= N4) return;
+  const float gamma = __ldg(log_decay + bh % H);
+  const float4* u4 = reinterpret_cast<const float4*>(U) + e;
+  float4 s = boundary ? __ldg(reinterpret_cast<const float4*>(boundary) + (size_t)bh * N4 + e)
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+  const int j0 = reverse ? lens.n - 1 : 0, j1 = reverse ? rank : rank, step = reverse ? -1 : 1;
+  for (int j = j0; j != j1; j += step) {
+    const float lam = expf(gamma * (float)lens.len[j]);
+    const float4 u = __ldg(u4 + ((size_t)j * BH + bh) * N4);
+    s = make_float4(fmaf(lam, s.x, u.x), fmaf(lam, s.y, u.y), fmaf(lam, s.z, u.z),
+                    fmaf(lam, s.w, u.w));
+  }
+  reinterpret_cast<float4*>(out)[(size_t)bh * N4 + e] = s;
 }
 
 // Finish time of `jobs` equal jobs of length d, list-scheduled in order on n_sm SMs of which
@@ -383,11 +421,38 @@ cudaError_t launch_segment_states(const void* q, const void* k, const void* v, c
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     kern<<<(unsigned)(n_fwd + n_rev), THREADS, SMEM_BYTES, stream>>>(
-        mk, mv, mq, mg, log_decay, states, adj, T, H, plan.whole, plan.parts, (int)n_fwd, ctl);
+        mk, mv, mq, mg, log_decay, states, adj, T, H, plan.whole, plan.parts, (int)n_fwd, 0, ctl);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   seg_link_kernel<<<dim3((DK * DV / 4 + 255) / 256, (unsigned)X, 2), 256, 0, stream>>>(
       init, dfin, log_decay, states, adj, T, H, plan.whole, plan.parts, sp);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_slice_sums(const void* a, const void* b, bool bf16, bool reverse,
+                              const float* log_decay, float* out, int B, int T, int H, DevCtl ctl,
+                              cudaStream_t stream) {
+  // a, b = k, v (forward: U of the slice) or q, dO (reverse: U' of the slice)
+  CUtensorMap ma, mb;
+  if (!make_tmap_seq_16bit(&ma, a, DK, H, T, B, 32, C, CU_TENSOR_MAP_SWIZZLE_64B, bf16) ||
+      !make_tmap_seq_16bit(&mb, b, DV, H, T, B, 64, C, CU_TENSOR_MAP_SWIZZLE_128B, bf16))
+    return cudaErrorInvalidValue;
+  const long long n = (long long)B * H;
+  auto kern = bf16 ? seg_sum_kernel<true> : seg_sum_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  kern<<<(unsigned)n, THREADS, SMEM_BYTES, stream>>>(
+      ma, mb, ma, mb, log_decay, reverse ? nullptr : out, reverse ? out : nullptr, T, H, 0, 2,
+      reverse ? 0 : (int)n, 1, ctl);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_shard_link(const float* U, const ShardLens& lens, int rank, bool reverse,
+                              const float* log_decay, const float* boundary, float* out, int B,
+                              int H, cudaStream_t stream) {
+  const int BH = B * H;
+  shard_link_kernel<<<dim3((DK * DV / 4 + 255) / 256, (unsigned)BH), 256, 0, stream>>>(
+      U, boundary, log_decay, out, lens, rank, reverse ? 1 : 0, BH, H);
   return cudaGetLastError();
 }
 

@@ -73,7 +73,10 @@ typedef enum {
 
 /* Element type of the q, k, v, dO inputs.  Outputs and states are fp32. */
 typedef enum {
-  GLA_BF16 = 0, /* bfloat16 */
+  GLA_BF16 = 0, /* bfloat16.  The chunked calls' tensor cores take fp16 operands, so they
+                   need |x| < 65504 for every input element, and the masked scores they form
+                   (scaled with the state copy) within that range too; a violation is
+                   reported as GLA_ERR_RANGE, not returned as a silent overflow */
   GLA_FP32 = 1, /* float32: converted to fp16 on the device (|x| < 65504) */
   GLA_FP16 = 2  /* IEEE half */
 } gla_dtype;
@@ -219,6 +222,51 @@ GLA_API gla_status gla_chunk_split_plan(int B, int T, int H, int backward, int n
 GLA_API gla_status gla_set_split_parts(int parts);
 
 /* ---------------------------------------------------------------------------
+ * A long sequence cut into consecutive slices, one per rank (GPU), for long-context
+ * prefill and its backward.  Section "Challenge 1" carries one state from chunk to chunk,
+ * and section "Inference optimization on Trainium2" keeps that state fixed in size whatever
+ * the prompt's length; the recurrence S_t = lambda S_{t-1} + k_t v_t^T ("GLA mixer") is
+ * linear, so a slice j of len_j tokens contributes
+ *     S leaving slice j = lambda^(len_j) S entering slice j + U_j,
+ *         U_j  = sum_{t in j} lambda^(e_j - t) k_t v_t^T           (e_j: its last token)
+ * and, in the backward ("Challenge 3"), with A_j the adjoint of the state leaving slice j,
+ *     A_{j-1} = lambda^(len_j) A_j + U'_j,
+ *         U'_j = sum_{t in j} lambda^(t - s_j + 1) q_t dO_t^T      (s_j: its first token).
+ * Each rank computes its slice's sums, the ranks exchange them (one all-gather of
+ * B*H*96*192 floats each), and each rank then runs gla_chunk_fwd / gla_chunk_bwd on its own
+ * slice from the state (adjoint) gla_state_link gives it.  The library makes no collective
+ * call itself: the exchange is the caller's (for example NCCL through torch.distributed).
+ *
+ * gla_chunk_state_sum:   U[b,h]  = sum_t lambda_h^(T-1-t) k_t v_t^T   over this call's T tokens
+ * gla_chunk_adjoint_sum: U'[b,h] = sum_t lambda_h^(t+1) q_t dO_t^T
+ *   k, q [B,T,H,96] and v, dO [B,T,H,192] in_dtype (GLA_BF16 or GLA_FP16; GLA_FP32 ->
+ *   GLA_ERR_UNSUPPORTED); log_decay [H]; U [B,H,96,192] fp32 (written).  Tensor cores with
+ *   fp16 operands and fp32 accumulation, as the chunked calls (|x| < 65504, GLA_ERR_RANGE).
+ *   U equals the final state of gla_chunk_fwd from a zero initial state; U' equals the
+ *   d_init_state of gla_chunk_bwd with a zero d_final_state.
+ *
+ * gla_state_link: out[b,h] for slice `slice` of n_slices (1 <= n_slices <= 256) slices of
+ *   lens[0..n_slices-1] tokens (a HOST int array, every entry >= 1):
+ *     reverse == 0:  S_0 = boundary (initial state, NULL = zeros), S_{j+1} = lambda^(len_j) S_j
+ *                    + U_j; out = S_slice, the state entering the slice
+ *     reverse != 0:  A_{n-1} = boundary (d_final_state, NULL = zeros), A_{j-1} =
+ *                    lambda^(len_j) A_j + U'_j; out = A_slice, the adjoint of the state
+ *                    leaving the slice
+ *   U_all [n_slices,B,H,96,192] fp32 (slice j's sums at index j, as an all-gather lays them
+ *   out; only the entries the recurrence reaches are read); boundary, out [B,H,96,192] fp32.
+ *   B*H <= 65535.
+ */
+GLA_API gla_status gla_chunk_state_sum(const void* k, const void* v, gla_dtype in_dtype,
+                                       const float* log_decay, float* U, int B, int T, int H,
+                                       int dk, int dv, cudaStream_t stream);
+GLA_API gla_status gla_chunk_adjoint_sum(const void* q, const void* dO, gla_dtype in_dtype,
+                                         const float* log_decay, float* U, int B, int T, int H,
+                                         int dk, int dv, cudaStream_t stream);
+GLA_API gla_status gla_state_link(const float* U_all, const int* lens, int n_slices, int slice,
+                                  int reverse, const float* log_decay, const float* boundary,
+                                  float* out, int B, int H, int dk, int dv, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Chunked backward that allocates nothing and takes no workspace.
  *
  * The article has no counterpart to this call; it exists for callers that cannot give the
@@ -233,8 +281,10 @@ GLA_API gla_status gla_set_split_parts(int parts);
  *    Inputs must be GLA_BF16 or GLA_FP16 (fp32 inputs need a workspace for their fp16
  *    copies): GLA_ERR_UNSUPPORTED otherwise.  Other checks and errors as gla_chunk_bwd;
  *    device errors go to the same error word (gla_get_device_error()).
- *  - The first call on each device looks up the array's device address (cudaGetSymbolAddress,
- *    which may load the module); make that first call before any stream capture.
+ *  - Every call looks up the array's device address in the current device's context
+ *    (cudaGetSymbolAddress, with the return code checked), so a context that was reset and
+ *    created again is handled.  The first call on a device may load the library's module
+ *    there; make that first call before any stream capture.
  *  - Every call on a device shares the one array, and a call leaves its partial sums in it.
  *    Each call overwrites every entry it later reads, so nothing needs clearing, but calls
  *    that overlap on the GPU (in flight at once, e.g. on two streams) race on the array:

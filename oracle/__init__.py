@@ -19,7 +19,9 @@ reach") and section "Challenge 3" (backward through the sequential updates).
 Pins (tests/test_oracle_*.py): brute-force closed form, central finite
 differences, the printed decay values, the a=0 half value skip, the lambda=1
 reduction to causal linear attention, state-carry and init-zero invariants,
-decode/forward consistency and an independent chunked restatement; the gate
+decode/forward consistency and an independent chunked restatement; the slice sums and
+their link (a sequence cut into slices) against the forward's state and the backward's
+adjoint at every slice boundary; the gate
 (the activation the forward saves) against the forward's own first-token value
 skip and the a=0 half value.  Every function here is pinned; none is "parity
 unpinned".
@@ -135,6 +137,43 @@ def bwd(q, k, v, gamma, a, dO, init_state=None, d_final_state=None, nthreads: in
     if rc != 0:
         raise ValueError("oracle_bwd: bad sizes")
     return out
+
+
+# --------------------------------------------------------------------------- slices of a sequence
+# A long sequence cut into consecutive slices (long-context prefill across ranks): the state
+# recurrence S_t = lambda S_{t-1} + k_t v_t^T ("GLA mixer") and its adjoint are linear, so a
+# slice acts on the state entering it through lambda^len and one summed term.  Each function
+# is the definition written out with the token recurrence above (section "Challenge 1": the
+# state carried across chunks; section "Challenge 3": the backward through the updates).
+
+def slice_state_sum(k, v, gamma, lib=None):
+    """U[b,h] = sum_t lambda_h^(T-1-t) k_t v_t^T: the state the recurrence reaches from a zero
+    state over these tokens (the forward's final state with q = 0, a = 0).  [B,H,dk,dv]."""
+    k = np.asarray(k, np.float64)
+    z = np.zeros_like(k)
+    return fwd(z, k, v, gamma, np.zeros(k.shape[2:]), lib=lib)[1]
+
+
+def slice_adjoint_sum(q, dO, gamma, lib=None):
+    """U'[b,h] = sum_t lambda_h^(t+1) q_t dO_t^T: the adjoint of the state entering these
+    tokens when nothing flows in from after them (the backward's d_init_state with a zero
+    d_final_state; k and v do not enter it).  [B,H,dk,dv]."""
+    q, dO = np.asarray(q, np.float64), np.asarray(dO, np.float64)
+    return bwd(q, np.zeros_like(q), np.zeros_like(dO), gamma, np.zeros(q.shape[2:]), dO,
+               lib=lib)["d_init_state"]
+
+
+def state_link(U_all, lens, rank, gamma, boundary=None, reverse=False):
+    """The state entering slice `rank` (forward: S_0 = boundary, S_{j+1} = lambda^len_j S_j +
+    U_j) or the adjoint of the state leaving it (reverse: A_{n-1} = boundary, A_{j-1} =
+    lambda^len_j A_j + U'_j), slices of `lens` tokens, U_all [n,B,H,dk,dv]."""
+    U = np.asarray(U_all, np.float64)
+    lam = np.exp(np.asarray(gamma, np.float64))[None, :, None, None]  # per head
+    s = np.zeros(U.shape[1:]) if boundary is None else np.array(boundary, np.float64)
+    order = range(len(lens) - 1, rank, -1) if reverse else range(rank)
+    for j in order:
+        s = lam ** int(lens[j]) * s + U[j]
+    return s
 
 
 def decode_step(state, q, k, v, gamma, a, nthreads: int = 0, lib=None):

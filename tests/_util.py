@@ -36,3 +36,14 @@ def as_dtype_values(x, name: str):
     if name == "fp16":
         return x.astype(np.float16).astype(np.float32)
     return np.asarray(x, np.float32)
+
+
+def oracle_decays(H: int, t_min: float = 1.0, t_max: float = 2048.0):
+    """The oracle's log-decays rounded to fp32, for both sides of a parity test: returns
+    (a host float32 torch tensor [H] for the library, the same values as fp64 numpy for the
+    oracle).  The library's own schedule is checked against these values separately."""
+    import torch
+
+    import oracle
+    g32 = oracle.decay_schedule(H, t_min, t_max).astype(np.float32)
+    return torch.from_numpy(g32.copy()), g32.astype(np.float64)

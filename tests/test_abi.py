@@ -302,3 +302,41 @@ def test_header_compiles_as_plain_c(tmp_path):
                         str(src)], capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
     assert len(names) >= 20, names
+
+
+def test_slice_call_argument_checks(lib):
+    def ssum(k=A16, v=A16, dt=0, ld=A16, U=A16, B=1, T=128, H=1, dk=96, dv=192):
+        return lib.gla_chunk_state_sum(k, v, dt, ld, U, B, T, H, dk, dv, None)
+
+    def asum(q=A16, dO=A16, dt=0, ld=A16, U=A16, B=1, T=128, H=1, dk=96, dv=192):
+        return lib.gla_chunk_adjoint_sum(q, dO, dt, ld, U, B, T, H, dk, dv, None)
+
+    for f in (ssum, asum):
+        assert f(dk=64) == 2 and f(dv=96) == 2
+        assert f(dt=1) == 2                         # fp32 inputs: no workspace for fp16 copies
+        assert f(B=0) == 1 and f(T=0) == 1 and f(H=0) == 1
+        assert f(U=None) == 1 and f(ld=None) == 1
+        assert f(U=A16 + 4) == 3 and f(T=77, ld=A16 + 8) == 3  # any T: the next check fails
+    lens = (ctypes.c_int * 3)(5, 7, 9)
+    bad_lens = (ctypes.c_int * 3)(5, 0, 9)
+
+    def link(U=A16, L=lens, n=3, r=1, rev=0, ld=A16, bnd=None, out=A16, B=1, H=1, dk=96, dv=192):
+        return lib.gla_state_link(U, None if L is None else ctypes.addressof(L), n, r, rev, ld,
+                                  bnd, out, B, H, dk, dv, None)
+
+    assert link(r=3) == 1 and link(r=-1) == 1 and link(n=0, r=0) == 1
+    assert link(L=bad_lens) == 1 and link(L=None) == 1 and link(out=None) == 1
+    assert link(n=257, r=0) == 2 and link(dk=64) == 2 and link(B=65536, H=2) == 2
+    assert link(bnd=A16 + 4) == 3 and link(U=A16 + 8) == 3
+
+
+def test_sharded_binding_keeps_the_library_in_the_product_path():
+    """seqshard's default ops are the library's calls (no CPU arithmetic in the product path)."""
+    import inspect
+
+    from gated_linear_attention_chunked_gb300 import seqshard
+    src = inspect.getsource(seqshard)
+    assert "oracle" not in src and "numpy" not in src
+    ops = seqshard.KernelOps()
+    for name in ("state_sum", "adjoint_sum", "link", "fwd", "bwd"):
+        assert callable(getattr(ops, name))

@@ -3,7 +3,7 @@ import numpy as np
 import pytest
 
 import synth
-from _util import TOL_CHUNK, as_dtype_values, rel_err, to_dev
+from _util import TOL_CHUNK, as_dtype_values, rel_err, to_dev, oracle_decays
 
 pytestmark = pytest.mark.gpu
 
@@ -27,8 +27,8 @@ def run_bwd(env, q, k, v, a, dO, init, dfin, H, dtype):
     gla, torch = env
     td = getattr(torch, TDT[dtype])
     q, k, v, dO = (as_dtype_values(x, dtype) for x in (q, k, v, dO))
-    gam = gla.decay_schedule(H)
-    gam64 = oracle.decay_schedule(H).astype(np.float32).astype(np.float64)
+    gam = oracle_decays(H)[0]
+    gam64 = oracle_decays(H)[1]
     f32 = lambda x: None if x is None else to_dev(x, torch.float32)
     dq, dk, dv, da, dinit = gla.chunk_bwd(to_dev(q, td), to_dev(k, td), to_dev(v, td), gam.cuda(),
                                           f32(a), to_dev(dO, td), f32(init), f32(dfin))

@@ -3,7 +3,7 @@ import numpy as np
 import pytest
 
 import synth
-from _util import TOL_DECODE, rel_err
+from _util import TOL_DECODE, rel_err, oracle_decays
 
 pytestmark = pytest.mark.gpu
 
@@ -31,8 +31,8 @@ def test_decode_small(env, N, L, H):
     st = (rng.standard_normal((N, L, H, 96, 192)) * 0.5).astype(np.float32)
     q, k, v = synth.decode_token(9, N, L, H)
     a = synth.aug_balance(9, (L, H, 96), 0.3)
-    gam = gla.decay_schedule(H)
-    gam64 = oracle.decay_schedule(H).astype(np.float32).astype(np.float64)
+    gam = oracle_decays(H)[0]
+    gam64 = oracle_decays(H)[1]
     st_d = _t(torch, st)
     o = gla.decode_step(st_d, _t(torch, q), _t(torch, k), _t(torch, v), gam.cuda(), _t(torch, a))
     o_ref, st_ref = oracle.decode_step(st, q, k, v, gam64, a)
@@ -49,8 +49,8 @@ def test_decode_consecutive_steps_carry_the_state(env):
     q1, k1, v1 = synth.decode_token(5, N, L, H, step=0)
     q2, k2, v2 = synth.decode_token(5, N, L, H, step=1)
     a = synth.aug_balance(5, (L, H, 96), 0.02)
-    gam = gla.decay_schedule(H)
-    gam64 = oracle.decay_schedule(H).astype(np.float32).astype(np.float64)
+    gam = oracle_decays(H)[0]
+    gam64 = oracle_decays(H)[1]
     st = np.zeros((N, L, H, 96, 192), np.float32)
     st_d = _t(torch, st)
     gla.decode_step(st_d, _t(torch, q1), _t(torch, k1), _t(torch, v1), gam.cuda(), _t(torch, a))
@@ -79,14 +79,15 @@ def test_decode_full_serving_pool(env):
     """The serving workload: 1,280 sequences x 24 layers x 16 heads of 96x192 fp32 states
     (36.2 GB) resident in HBM, one new token per sequence, launched as the benchmark does.
     Every 64th sequence (all layers and heads) is checked against the oracle after 1 and
-    after 100 consecutive steps; every output is checked finite."""
+    after 100 consecutive steps, each step with a new token for those sequences; every output
+    is checked finite."""
     import oracle
     gla, torch = env
     cfg = synth.DECODE
     N, L, H = cfg["N"], cfg["L"], cfg["H"]
     seqs = list(range(0, N, 64))
-    gam = gla.decay_schedule(H)
-    gam64 = oracle.decay_schedule(H).astype(np.float32).astype(np.float64)
+    gam = oracle_decays(H)[0]
+    gam64 = oracle_decays(H)[1]
     a = synth.aug_balance(cfg["seed"], (L, H, 96), cfg["a_std"])
     st0 = warm_state(gam64, a, seqs, L, H, cfg)
     pool = torch.empty((N, L, H, 96, 192), dtype=torch.float32, device="cuda")
@@ -105,9 +106,15 @@ def test_decode_full_serving_pool(env):
     es = rel_err(pool[sub].cpu().numpy(), st_ref)
     print(f"decode pool step 1: o {eo:.2e} state {es:.2e}")
     assert eo <= TOL_DECODE and es <= TOL_DECODE
-    for _ in range(99):
+    # steps 2..100: a new token per step for the checked sequences (its own seeded stream per
+    # step), so their states move in 100 directions; the unchecked ones repeat their token
+    idx = torch.tensor(sub, device="cuda")
+    for s in range(1, 100):
+        qs, ks, vs = synth.decode_token(cfg["seed"], len(sub), L, H, step=s)
+        for dst, src in ((qd, qs), (kd, ks), (vd, vs)):
+            dst.index_copy_(0, idx, torch.from_numpy(src).cuda())
         gla.decode_step(pool, qd, kd, vd, gam.cuda(), ad, out=o)
-        o_ref, st_ref = oracle.decode_step(st_ref, q[sub], k[sub], v[sub], gam64, a)
+        o_ref, st_ref = oracle.decode_step(st_ref, qs, ks, vs, gam64, a)
     torch.cuda.synchronize()
     eo = rel_err(o[sub].cpu().numpy(), o_ref)
     es = rel_err(pool[sub].cpu().numpy(), st_ref)

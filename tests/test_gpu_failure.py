@@ -7,7 +7,7 @@ import numpy as np
 import pytest
 
 import synth
-from _util import TOL_CHUNK, rel_err, to_dev
+from _util import TOL_CHUNK, rel_err, to_dev, oracle_decays
 
 pytestmark = pytest.mark.gpu
 
@@ -39,9 +39,9 @@ def test_wait_gives_up_and_reports_timeout():
     q, k, v = synth.qkv(91, B, T, H)
     a = synth.aug_balance(91, (H, 96), 0.1)
     o, _ = gla.chunk_fwd(to_dev(q, torch.bfloat16), to_dev(k, torch.bfloat16),
-                         to_dev(v, torch.bfloat16), gla.decay_schedule(H).cuda(),
+                         to_dev(v, torch.bfloat16), oracle_decays(H)[0].cuda(),
                          to_dev(a, torch.float32))
     torch.cuda.synchronize()
     assert gla.get_device_error() == 0
-    o_ref, _ = oracle.fwd(q, k, v, gla.decay_schedule(H).numpy().astype(np.float64), a)
+    o_ref, _ = oracle.fwd(q, k, v, oracle_decays(H)[1], a)
     assert rel_err(o.cpu().numpy(), o_ref) <= TOL_CHUNK

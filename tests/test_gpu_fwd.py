@@ -3,7 +3,7 @@ import numpy as np
 import pytest
 
 import synth
-from _util import TOL_CHUNK, as_dtype_values, rel_err, to_dev
+from _util import TOL_CHUNK, as_dtype_values, rel_err, to_dev, oracle_decays
 
 pytestmark = pytest.mark.gpu
 
@@ -27,8 +27,8 @@ def run_fwd(env, q, k, v, a, init, H, dtype):
     gla, torch = env
     td = getattr(torch, TDT[dtype])
     q, k, v = (as_dtype_values(x, dtype) for x in (q, k, v))
-    gam = gla.decay_schedule(H)
-    gam64 = oracle.decay_schedule(H).astype(np.float32).astype(np.float64)
+    gam = oracle_decays(H)[0]
+    gam64 = oracle_decays(H)[1]
     init_d = None if init is None else to_dev(init, torch.float32)
     o, fin = gla.chunk_fwd(to_dev(q, td), to_dev(k, td), to_dev(v, td), gam.cuda(),
                            to_dev(a, torch.float32), init_d)
@@ -149,7 +149,7 @@ def test_fwd_segmented_path(env, B, T, H, seed):
     # one chain per pair: same call through the C ABI without a workspace
     lib = gla.load()
     qd, kd, vd = (to_dev(x, torch.bfloat16) for x in (q, k, v))
-    gam = gla.decay_schedule(H).cuda()
+    gam = oracle_decays(H)[0].cuda()
     ad, idd = to_dev(a, torch.float32), to_dev(init, torch.float32)
     o2 = torch.empty((B, T, H, 192), dtype=torch.float32, device="cuda")
     f2 = torch.empty((B, H, 96, 192), dtype=torch.float32, device="cuda")
@@ -185,13 +185,13 @@ def test_fwd_gated(env, B, T, H, n_tiers, want_o, seed):
     g = synth.round_bf16(synth.normal(seed, synth.DO, (B, T, H, 192), 1.5))
     w = 1.0 + synth.normal(seed, synth.A, (n_tiers, 192), 0.2)
     qd, kd, vd, gd = (to_dev(x, torch.bfloat16) for x in (q, k, v, g))
-    gam = gla.decay_schedule(H).cuda()
+    gam = oracle_decays(H)[0].cuda()
     ad, idd, wd = (to_dev(x, torch.float32) for x in (a, init, w))
     y, rstd, o, fin = gla.chunk_fwd_gated(qd, kd, vd, gam, ad, gd, wd, n_tiers, 1e-6, idd,
                                           want_o=want_o)
     torch.cuda.synchronize()
     assert gla.get_device_error() == 0
-    gam64 = gla.decay_schedule(H).numpy().astype(np.float64)
+    gam64 = oracle_decays(H)[1]
     o_ref, fin_ref = oracle.fwd(q, k, v, gam64, a, init)
     y_ref, r_ref = oracle.head_norm_gate(o_ref.reshape(B * T, H, 192), g.reshape(B * T, H, 192),
                                          w, n_tiers, 1e-6)
@@ -221,7 +221,7 @@ def test_fwd_ragged_writes_nothing_past_t(env):
     big = torch.full((n + 64 * H * 192,), float("nan"), dtype=torch.float32, device="cuda")
     o = big[:n].view(B, T, H, 192)
     fin = torch.empty((B, H, 96, 192), dtype=torch.float32, device="cuda")
-    gam = gla.decay_schedule(H)
+    gam = oracle_decays(H)[0]
     gla.chunk_fwd(to_dev(q, torch.bfloat16), to_dev(k, torch.bfloat16), to_dev(v, torch.bfloat16),
                   gam.cuda(), to_dev(a, torch.float32), to_dev(init, torch.float32), out=o,
                   final_state=fin)

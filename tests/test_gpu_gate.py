@@ -9,7 +9,7 @@ import numpy as np
 import pytest
 
 import synth
-from _util import TOL_CHUNK, rel_err, to_dev
+from _util import TOL_CHUNK, rel_err, to_dev, oracle_decays
 
 pytestmark = pytest.mark.gpu
 
@@ -56,8 +56,8 @@ def test_saved_gate_forward_and_backward(env, B, T, H, dtype, parts, seed):
     a = synth.aug_balance(seed, (H, 96), 0.3)
     init = synth.init_state(seed, B, H, 0.05)
     dfin = synth.normal(seed, synth.DFIN, (B, H, 96, 192), 0.05)
-    gam = gla.decay_schedule(H).cuda()
-    gam64 = gla.decay_schedule(H).numpy().astype(np.float64)
+    gam = oracle_decays(H)[0].cuda()
+    gam64 = oracle_decays(H)[1]
     qd, kd, vd, gd = (to_dev(x, td) for x in (q, k, v, dO))
     ad, idd, fd = (to_dev(x, torch.float32) for x in (a, init, dfin))
     gla.set_split_parts(parts)
@@ -98,7 +98,7 @@ def test_backward_follows_the_gate_it_is_given(env):
     a = synth.aug_balance(seed, (H, 96), 0.3)
     qd, kd, vd, gd = (to_dev(x, torch.bfloat16) for x in (q, k, v, dO))
     gate = torch.full((B, H, T), 0.5, dtype=torch.float32, device="cuda")
-    _, _, _, d_aug, _ = gla.chunk_bwd(qd, kd, vd, gla.decay_schedule(H).cuda(),
+    _, _, _, d_aug, _ = gla.chunk_bwd(qd, kd, vd, oracle_decays(H)[0].cuda(),
                                       to_dev(a, torch.float32), gd, gate=gate)
     torch.cuda.synchronize()
     assert gla.get_device_error() == 0
@@ -117,7 +117,7 @@ def test_no_workspace_backward_reads_the_gate(env):
     a = synth.aug_balance(seed, (H, 96), 0.3)
     qd, kd, vd, gd = (to_dev(x, torch.bfloat16) for x in (q, k, v, dO))
     ad = to_dev(a, torch.float32)
-    gam = gla.decay_schedule(H).cuda()
+    gam = oracle_decays(H)[0].cuda()
     gate = torch.empty((B, H, T), dtype=torch.float32, device="cuda")
     gla.chunk_fwd(qd, kd, vd, gam, ad, gate=gate)
     gla.set_split_parts(1)  # the no-workspace call never cuts pairs: compare like with like
@@ -156,7 +156,7 @@ def test_saved_gate_at_the_training_shape(env):
     a = synth.aug_balance(seed, (H, 96), 0.02)
     qd, kd, vd, gd = (to_dev(x, torch.bfloat16) for x in (q, k, v, dO))
     ad = to_dev(a, torch.float32)
-    gam = gla.decay_schedule(H).cuda()
+    gam = oracle_decays(H)[0].cuda()
     gate = torch.empty((B, H, T), dtype=torch.float32, device="cuda")
     gla.chunk_fwd(qd, kd, vd, gam, ad, gate=gate)
     g_saved = gla.chunk_bwd(qd, kd, vd, gam, ad, gd, gate=gate)

@@ -6,7 +6,7 @@ import numpy as np
 import pytest
 
 import synth
-from _util import to_dev
+from _util import to_dev, oracle_decays
 
 pytestmark = pytest.mark.gpu
 
@@ -36,7 +36,7 @@ def test_capture_and_replay_matches_eager(env):
     gla.set_split_parts(3)  # cut every pair into 3 parts: the segment passes run in the graph
     try:
         a = to_dev(synth.aug_balance(1, (H, 96), 0.1), torch.float32)
-        gam = gla.decay_schedule(H).cuda()
+        gam = oracle_decays(H)[0].cuda()
         bufs = [to_dev(x, torch.bfloat16) for x in _inputs(1, B, T, H)[:4]]
         inits = [to_dev(x, torch.float32) for x in _inputs(1, B, T, H)[4:]]
         rng = np.random.default_rng(2)

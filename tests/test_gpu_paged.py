@@ -5,7 +5,7 @@ import numpy as np
 import pytest
 
 import synth
-from _util import TOL_CHUNK, TOL_DECODE, rel_err, to_dev
+from _util import TOL_CHUNK, TOL_DECODE, rel_err, to_dev, oracle_decays
 
 pytestmark = pytest.mark.gpu
 
@@ -42,7 +42,7 @@ def test_decode_paged_matches_oracle(env):
     page = np.array([7, 2, 0, 5, 3], np.int32)  # any order, no padding
     pool = _pool(51, P, PL, H)
     q, k, v, a = _decode_inputs(51, len(page), L, H)
-    gam = gla.decay_schedule(H)
+    gam = oracle_decays(H)[0]
     gam64 = gam.numpy().astype(np.float64)
     pool_d = to_dev(pool, torch.float32)
     o = gla.decode_step_paged(pool_d, to_dev(page, torch.int32), to_dev(q, torch.float32),
@@ -71,7 +71,7 @@ def test_decode_paged_bad_page_touches_nothing(env):
     page = np.array([2, 99], np.int32)
     pool = _pool(52, P, PL, H)
     q, k, v, a = _decode_inputs(52, 2, L, H)
-    gam = gla.decay_schedule(H)
+    gam = oracle_decays(H)[0]
     pool_d = to_dev(pool, torch.float32)
     o = torch.full((2, L, H, 192), float("nan"), device="cuda")
     gla.decode_step_paged(pool_d, to_dev(page, torch.int32), to_dev(q, torch.float32),
@@ -103,7 +103,7 @@ def test_chunk_fwd_paged(env, B, T, H, P, PL, layer, from_pool, seed):
     pool = _pool(seed, P, PL, H)
     q, k, v = synth.qkv(seed, B, T, H)
     a = synth.aug_balance(seed, (H, 96), 0.1)
-    gam = gla.decay_schedule(H)
+    gam = oracle_decays(H)[0]
     gam64 = gam.numpy().astype(np.float64)
     pool_d = to_dev(pool, torch.float32)
     o = gla.chunk_fwd_paged(to_dev(q, torch.bfloat16), to_dev(k, torch.bfloat16),
@@ -131,7 +131,7 @@ def test_prefill_then_decode_matches_one_forward(env):
     T, H, P = 256, 4, 3
     q, k, v = synth.qkv(56, 1, T + 1, H)
     a = synth.aug_balance(56, (H, 96), 0.1)
-    gam = gla.decay_schedule(H)
+    gam = oracle_decays(H)[0]
     gam64 = gam.numpy().astype(np.float64)
     pool_d = torch.zeros((P, 1, H, 96, 192), device="cuda")
     page = to_dev(np.array([1], np.int32), torch.int32)

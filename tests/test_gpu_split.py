@@ -7,7 +7,7 @@ import numpy as np
 import pytest
 
 import synth
-from _util import TOL_CHUNK, rel_err, to_dev
+from _util import TOL_CHUNK, rel_err, to_dev, oracle_decays
 
 pytestmark = pytest.mark.gpu
 
@@ -56,7 +56,7 @@ def _run(env, parts, q, k, v, dO, a, init, dfin, H, dtype):
     td = dict(bf16=torch.bfloat16, fp16=torch.float16, fp32=torch.float32)[dtype]
     gla.set_split_parts(parts)
     try:
-        gam = gla.decay_schedule(H).cuda()
+        gam = oracle_decays(H)[0].cuda()
         qd, kd, vd, gd = (to_dev(x, td) for x in (q, k, v, dO))
         ad, idd, fd = (to_dev(x, torch.float32) for x in (a, init, dfin))
         o, fin = gla.chunk_fwd(qd, kd, vd, gam, ad, idd)
@@ -84,7 +84,7 @@ def test_cut_pairs_match_oracle_and_uncut(env, B, T, H, parts, dtype, seed):
     q, k, v, dO, a, init, dfin = _inputs(seed, B, T, H, dtype)
     o, fin, g = _run(env, parts, q, k, v, dO, a, init, dfin, H, dtype)
     o1, fin1, g1 = _run(env, 1, q, k, v, dO, a, init, dfin, H, dtype)
-    gam64 = gla.decay_schedule(H).numpy().astype(np.float64)
+    gam64 = oracle_decays(H)[1]
     o_ref, fin_ref = oracle.fwd(q, k, v, gam64, a, init)
     ref = oracle.bwd(q, k, v, gam64, a, dO, init, dfin)
     errs = dict(o=rel_err(o, o_ref), final=rel_err(fin, fin_ref))
@@ -114,7 +114,7 @@ def test_whole_and_cut_pairs_in_one_launch(env):
         gla.set_split_parts(0)
     q, k, v, dO, a, init, dfin = _inputs(seed, B, T, H, "bf16")
     o, fin, g = _run(env, 2, q, k, v, dO, a, init, dfin, H, "bf16")
-    gam64 = gla.decay_schedule(H).numpy().astype(np.float64)
+    gam64 = oracle_decays(H)[1]
     o_ref, fin_ref = oracle.fwd(q, k, v, gam64, a, init)
     ref = oracle.bwd(q, k, v, gam64, a, dO, init, dfin)
     errs = dict(o=rel_err(o, o_ref), final=rel_err(fin, fin_ref))
@@ -137,7 +137,7 @@ def test_cut_pairs_paged_and_gated(env):
     pool = synth.normal(seed, synth.INIT, (P, PL, H, 96, 192), 0.05).astype(np.float32)
     q, k, v = synth.qkv(seed, B, T, H)
     a = synth.aug_balance(seed, (H, 96), 0.1)
-    gam = gla.decay_schedule(H)
+    gam = oracle_decays(H)[0]
     gam64 = gam.numpy().astype(np.float64)
     g_in = synth.round_bf16(synth.normal(seed, synth.DO, (B, T, H, 192), 1.5))
     w = 1.0 + synth.normal(seed, synth.A, (1, 192), 0.2)
