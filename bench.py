@@ -154,6 +154,43 @@ def oracle_sample(n_seq: int, seed: int = 2):
     return n_seq * T / dt, dt
 
 
+def oracle_decode_sample(every: int = 64, steps: int = 3, seed: int = 3):
+    """Time the fp64 oracle's decode step over every `every`-th sequence of the serving pool
+    (all 24 layers x 16 heads each); returns (states per second, states, seconds)."""
+    import numpy as np
+
+    import oracle
+    import synth
+    n = len(range(0, N_SEQ, every))
+    rng = np.random.default_rng(seed)
+    st = rng.standard_normal((n, N_LAYERS, H, DK, DV)) * 0.5
+    q, k, v = synth.decode_token(seed, n, N_LAYERS, H)
+    a = synth.aug_balance(seed, (N_LAYERS, H, DK), 0.02)
+    g = oracle.decay_schedule(H).astype(np.float32).astype(np.float64)
+    oracle.decode_step(st, q, k, v, g, a)  # warm-up (page-in, thread start)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        _, st = oracle.decode_step(st, q, k, v, g, a)
+    dt = time.perf_counter() - t0
+    n_states = n * N_LAYERS * H
+    return n_states * steps / dt, n_states, dt
+
+
+def oracle_long_prefill_sample(t_sample: int = 8192, seed: int = 4):
+    """Time the fp64 oracle's forward over the first `t_sample` tokens of both long-prefill
+    sequences (B=2, H=16, with the initial state); returns (tokens per second, seconds)."""
+    import numpy as np
+
+    import oracle
+    import synth
+    x = synth.chunk_inputs("long_prefill", T=t_sample)
+    g = oracle.decay_schedule(H).astype(np.float32).astype(np.float64)
+    t0 = time.perf_counter()
+    oracle.fwd(x["q"], x["k"], x["v"], g, x["a"], x["init_state"])
+    dt = time.perf_counter() - t0
+    return 2 * t_sample / dt, dt
+
+
 def reduce_max(values, dist, device):
     """Element-wise max over ranks of this rank's values (timings): the slowest rank sets the
     job's time.  dist None = one process."""
@@ -351,7 +388,7 @@ def run_gpu(args, rank, world, local_rank):
     # other of two device buffers while step s computes (host->device is ~5.8 ms per step
     # here, the kernels ~2 ms).  The clock starts before the first copy and stops after the
     # last read-back has landed.
-    e2e = None
+    e2e = e2e_full_readback = None
     if not args.no_e2e:
         hq, hk, hv, hdO = (x.cpu().pin_memory() for x in (q, k, v, dO))
         e2e_steps = max(3, min(args.steps, 10))
@@ -390,17 +427,93 @@ def run_gpu(args, rank, world, local_rank):
         tt = reduce_max([time.perf_counter() - t0], dist, dev)[0]
         e2e = dict(value=job_rate(world, tokens * e2e_steps, tt), unit="tokens/s",
                    h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h,
-                   path="pinned host q,k,v,dO -> gla chunk_fwd + chunk_bwd -> host d_aug; "
-                        "next step's inputs copied on a second stream during this step's "
-                        "kernels (two device buffers)")
-        del bufs
+                   path="pinned host q,k,v,dO -> gla chunk_fwd + chunk_bwd -> host d_aug. "
+                        "Returned to the host: d_aug, the step's parameter gradient (the "
+                        "mixer's only trained parameter; the decay is fixed) -- the scalar-"
+                        "like result a training step reads back; o and dq, dk, dv feed "
+                        "device-side projections and stay in HBM (e2e_full_readback copies "
+                        "them back too). Next step's inputs copied on a second stream during "
+                        "this step's kernels (two device buffers)")
 
-    cpu = None
+        # the same loop with every output copied back to pinned host memory each step: o,
+        # dq, dk, dv and d_aug (the device->host copy of step s runs on a third stream while
+        # step s+1 computes; its outputs go to the other of two device buffers)
+        outs = [dict(o=torch.empty_like(o)) for _ in range(2)]
+        shapes = dict(o=(Bn, T, H, DV), dq=(Bn, T, H, DK), dk=(Bn, T, H, DK), dv=(Bn, T, H, DV))
+        h_out = {n_: torch.empty(sh, dtype=torch.float32).pin_memory() for n_, sh in shapes.items()}
+        d2h_full = sum(x.numel() * 4 for x in h_out.values()) + H * DK * 4
+        back_stream = torch.cuda.Stream(device=dev)
+        computed = [torch.cuda.Event() for _ in range(2)]
+        read = [torch.cuda.Event() for _ in range(2)]
+        ws_full = torch.empty(max(1, gla.chunk_bwd_workspace_size(Bn, T, H, gla.GLA_BF16)),
+                              dtype=torch.uint8, device=dev)
+
+        def e2e_full(nsteps):
+            for s_ in range(nsteps):
+                i = s_ % 2
+                with torch.cuda.stream(copy_stream):
+                    if s_ >= 2:
+                        copy_stream.wait_event(consumed[i])
+                    for d, hsrc in zip(bufs[i], (hq, hk, hv, hdO)):
+                        d.copy_(hsrc, non_blocking=True)
+                    copied[i].record(copy_stream)
+                stream.wait_event(copied[i])
+                if s_ >= 2:
+                    stream.wait_event(read[i])  # step s-2's outputs have left buffer i
+                bq, bk, bv, bdO = bufs[i]
+                ob = outs[i]
+                gla.chunk_fwd(bq, bk, bv, gam, a, out=ob["o"], final_state=fin, gate=gate)
+                dq_, dk_, dv_, daug, _ = gla.chunk_bwd(bq, bk, bv, gam, a, bdO, gate=gate,
+                                                       workspace=ws_full,
+                                                       want_d_init_state=False)
+                consumed[i].record(stream)
+                ob["dq"], ob["dk"], ob["dv"] = dq_, dk_, dv_
+                for x_ in (dq_, dk_, dv_, daug):  # read on back_stream: keep until it has
+                    x_.record_stream(back_stream)
+                computed[i].record(stream)
+                with torch.cuda.stream(back_stream):
+                    back_stream.wait_event(computed[i])
+                    for n_ in ("o", "dq", "dk", "dv"):
+                        h_out[n_].copy_(ob[n_], non_blocking=True)
+                    h_daug[s_ % e2e_steps].copy_(daug, non_blocking=True)
+                    read[i].record(back_stream)
+            torch.cuda.synchronize()
+
+        e2e_full(2)  # warm-up
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        e2e_full(e2e_steps)
+        tf_ = reduce_max([time.perf_counter() - t0], dist, dev)[0]
+        e2e_full_readback = dict(
+            value=job_rate(world, tokens * e2e_steps, tf_), unit="tokens/s",
+            h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h_full,
+            path="pinned host q,k,v,dO -> gla chunk_fwd + chunk_bwd -> pinned host o, dq, dk, "
+                 "dv, d_aug every step (device->host on a third stream, overlapping the next "
+                 "step; bound by the host link)")
+        del bufs, outs
+
+    cpu = cpu_dec = cpu_long = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cores = os.cpu_count() or 1
         rate, dt = oracle_sample(args.cpu_seqs)
-        cpu = dict(value=rate, unit="tokens/s", cores=os.cpu_count() or 1, kind="oracle",
+        cpu = dict(value=rate, unit="tokens/s", cores=cores, kind="oracle",
                    sample=f"fp64 oracle fwd+bwd over {args.cpu_seqs} of the 32 sequences "
                           f"(T=2048, H=16) = {args.cpu_seqs * T} tokens, {dt:.1f} s")
+        st_rate, n_st, dtd = oracle_decode_sample()
+        cpu_dec = dict(value=st_rate * DEC_BYTES_STATE / 1e9, unit="GB/s", cores=cores,
+                       kind="oracle", states_per_s=st_rate,
+                       ms_per_step_extrapolated=1e3 * n_states / st_rate,
+                       sample=f"fp64 oracle decode step over every 64th sequence of the pool "
+                              f"({n_st} states: 20 sequences x 24 layers x 16 heads), 3 steps, "
+                              f"{dtd:.1f} s; GB/s counts the same algorithmic bytes as the GPU "
+                              f"line; ms_per_step_extrapolated = the whole 1280-sequence pool at "
+                              f"this rate (linear extrapolation)")
+        lp_rate, dtl = oracle_long_prefill_sample()
+        cpu_long = dict(value=lp_rate, unit="tokens/s", cores=cores, kind="oracle",
+                        sample=f"fp64 oracle forward over the first 8192 of the 131072 tokens of "
+                               f"both long-prefill sequences (H=16, initial state), {dtl:.1f} s")
 
     clocks = clk.summary()
     line = dict(
@@ -416,7 +529,9 @@ def run_gpu(args, rank, world, local_rank):
                     frac_of_hbm=dec_gbs / pk["hbm"], peak_source=pk["src"]),
         parts_ms=dict(chunk_fwd=fwd_t, chunk_bwd=bwd_t, decode=dec_t),
         roofline_chunk_fwd=roof_fwd, roofline_chunk_bwd=roof_bwd,
-        cpu_baseline=cpu, e2e=e2e, gpu_launches=gpu_launches_per_step * args.steps,
+        cpu_baseline=cpu, cpu_baseline_decode=cpu_dec, cpu_baseline_long_prefill=cpu_long,
+        e2e=e2e, e2e_full_readback=e2e_full_readback,
+        gpu_launches=gpu_launches_per_step * args.steps,
         gpu_launches_detail="per step: chunk fwd, chunk bwd, d_aug reduction, decode"
                             + (", fwd segment passes (2)" if cut_f else "")
                             + (", bwd segment passes (2)" if cut_b else ""),
@@ -738,7 +853,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-seqs", type=int, default=8)
+    ap.add_argument("--cpu-seqs", type=int, default=32,
+                    help="sequences of the training workload the CPU oracle baseline times")
     ap.add_argument("--part", choices=["all", "fwd", "bwd", "decode", "long", "paged", "norm", "conv", "fused"], default="all",
                     help="time one call alone (smaller profiling cases); the default is the "
                          "whole hot path")

@@ -473,7 +473,7 @@ __device__ __forceinline__ void run_role(
       if (lane == 0) red[32 + warp] = m;
       mbar_arrive(cta.bar(RED));
     }
-    bool ok = wait(cta, cta.bar(RED), 0, ctl);
+    bool ok = wait_warp(cta, cta.bar(RED), 0, ctl);
     if (ok) {
       e_cur = state_exponent(max16(red + 32));
       if (e_cur < 0) {
@@ -507,8 +507,8 @@ __device__ __forceinline__ void run_role(
       // sigmoid(0))
       float sg_saved = 0.5f;
       if (SAVED && c * C + i < T) sg_saved = __ldg(p.gate + (size_t)bh * T + c * C + i);
-      if (!(ok = wait(cta, cta.bar(FULL_E), par, ctl))) break;
-      if (!(ok = wait(cta, cta.bar(FULL_L), par, ctl))) break;
+      if (!(ok = wait_warp(cta, cta.bar(FULL_E), par, ctl))) break;
+      if (!(ok = wait_warp(cta, cta.bar(FULL_L), par, ctl))) break;
       // ---- gate partial sum z = q.(a*k) over this part's 24 channels (unless the gate is
       // given), fused with the fp16 copy of whichever of q, k the score MMA does not read
       // (DQ: k, DK: q, both scale 1); DV's score reads both, so DV converts them once the
@@ -543,7 +543,7 @@ __device__ __forceinline__ void run_role(
       if constexpr (ROLE == R_DK) cvt3(xq, OFF_Q, 1.f, amax);  // Q (adjoint A, dP''^T Q B)
       if constexpr (ROLE == R_DV) convert_row<BF16, 6, 3>(base + OFF_G, vg, 1.f, bmax);  // dO
       // ---- once the score MMA has read its 16-bit tiles: their fp16 copies
-      if (!(ok = wait(cta, cta.bar(P_DONE), par, ctl))) break;
+      if (!(ok = wait_warp(cta, cta.bar(P_DONE), par, ctl))) break;
       tc_fence_after();
       if constexpr (ROLE == R_DQ) {
         convert_row<BF16, 6, 3>(base + OFF_V, vg, lk, bmax);       // V' (state B)
@@ -575,14 +575,14 @@ __device__ __forceinline__ void run_role(
       // ---- the row's gate: the saved one, or the four partial sums
       float sg = sg_saved;
       if (!SAVED) {
-        if (!(ok = wait(cta, cta.bar(QG0 + q4), par, ctl))) break;
+        if (!(ok = wait_warp(cta, cta.bar(QG0 + q4), par, ctl))) break;
         sg = sigmoid((gate_part[i] + gate_part[128 + i]) + (gate_part[256 + i] + gate_part[384 + i]));
       }
       // ---- masked score copy, scaled by 2^-e of this step's state copy: this part's 16-column
       // blocks hb = sub, sub+4 of the quadrant's rows, packed to fp16 pairs in registers.
       // Block hb's pairs go to 32-bit columns 8hb..8hb+7, inside block hb/2's fp32 columns, so
       // the four parts of a quadrant finish reading before any of them writes.
-      if (!(ok = wait(cta, cta.bar(EP_S), par, ctl))) break;
+      if (!(ok = wait_warp(cta, cta.bar(EP_S), par, ctl))) break;
       {
         const float psc = pow2i(-es[par]);
         float pmax = 0.f;
@@ -636,7 +636,7 @@ __device__ __forceinline__ void run_role(
         range_max = fmaxf(range_max, pmax);
         tc_fence_before();
         mbar_arrive(cta.bar(QS0 + q4));
-        if (!(ok = wait(cta, cta.bar(QS0 + q4), par, ctl))) break;
+        if (!(ok = wait_warp(cta, cta.bar(QS0 + q4), par, ctl))) break;
         tc_fence_after();
 #pragma unroll
         for (int m = 0; m < 2; ++m) tmem_st8(trow + TM_P + 8 * (sub + 4 * m), pk[m]);
@@ -660,13 +660,13 @@ __device__ __forceinline__ void run_role(
       mbar_arrive(cta.bar(EMPTY_L));
       // ---- the state update ran: next state copy (the serial step), while the output MMA's
       // TMEM-operand part runs
-      if (!(ok = wait(cta, cta.bar(S_DONE), par, ctl))) break;
+      if (!(ok = wait_warp(cta, cta.bar(S_DONE), par, ctl))) break;
       tc_fence_after();
       int e_next = e_cur;
       if (t < n - 1) {
         // bound on the next state: all parts' operand maxima and max|S| of this step's copy
         // (decayed by this step's factor)
-        if (!(ok = wait(cta, cta.bar(EP_CONV), par, ctl))) break;
+        if (!(ok = wait_warp(cta, cta.bar(EP_CONV), par, ctl))) break;
         e_next = state_exponent((t == 0 ? dec_first : lamC) * max16(red + par * 16) +
                                 (float)C * max16(abmax + par * 32) * max16(abmax + par * 32 + 16));
         if (e_next < 0) {
@@ -677,7 +677,7 @@ __device__ __forceinline__ void run_role(
                       true);
       }
       // ---- output rows, this part's columns: x = 2^e D_X (+ r (a * k|q) for DQ, DK)
-      if (!(ok = wait(cta, cta.bar(X_DONE), par, ctl))) break;
+      if (!(ok = wait_warp(cta, cta.bar(X_DONE), par, ctl))) break;
       tc_fence_after();
       if (lane == 0) bulk_wait_read<0>();  // the staging buffers are free again
       __syncwarp();
@@ -736,7 +736,7 @@ __device__ __forceinline__ void run_role(
     }
     // DQ: d_a of this (b, h) is the diagonal of the accumulated (r q)^T k; row d (lane of
     // quadrant d / 32) takes column d, once the last step's d_a MMAs are done
-    if (ROLE == R_DQ && ok && sub == 0 && q4 < 3 && wait(cta, cta.bar(EMPTY_L), (n - 1) & 1, ctl)) {
+    if (ROLE == R_DQ && ok && sub == 0 && q4 < 3 && wait_warp(cta, cta.bar(EMPTY_L), (n - 1) & 1, ctl)) {
       tc_fence_after();
       uint32_t r[32];
       tmem_ld32(trow + TM_A + 32 * q4, r);

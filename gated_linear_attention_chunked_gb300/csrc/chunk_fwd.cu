@@ -298,7 +298,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
       const float lk = c0 + c == nc - 1 ? lk_last : lk_full;
       uint8_t* stg = base + s * STAGE;
       float vmax = 0.f, kmax = 0.f, qmax = 0.f;
-      if (!wait(cta, cta.bar(V_FULL + s), (c >> 1) & 1, ctl)) break;
+      if (!wait_warp(cta, cta.bar(V_FULL + s), (c >> 1) & 1, ctl)) break;
       if constexpr (BF16) {  // v -> fp16 in place (exact for |v| in the fp16 normal range)
 #pragma unroll 4
         for (int cc = NV * hv; cc < NV * hv + NV; ++cc)
@@ -313,8 +313,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
           for (int e2 = 0; e2 < 4; ++e2) vmax = fmaxf(vmax, fmaxf(fabsf(h_lo(w[e2])), fabsf(h_hi(w[e2]))));
         }
       }
-      if (!wait(cta, cta.bar(P_DONE), par, ctl)) break;
-      if (!wait(cta, cta.bar(QK_FULL + s), (c >> 1) & 1, ctl)) break;
+      if (!wait_warp(cta, cta.bar(P_DONE), par, ctl)) break;
+      if (!wait_warp(cta, cta.bar(QK_FULL + s), (c >> 1) & 1, ctl)) break;
       tc_fence_after();
       // channels 8cc..8cc+7 of q, k: their part of the gate sum into `zacc`, Q'' and K' in place
       auto qk_chunk = [&](int cc, float& zacc) {
@@ -372,12 +372,12 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
         }
       }
       // the state exponent of this chunk (and P'' of the previous chunk consumed)
-      if (!wait(cta, cta.bar(EP_S), par, ctl)) break;
+      if (!wait_warp(cta, cta.bar(EP_S), par, ctl)) break;
       float sg = 0.f;
       if (CW == 1) {
         sg = sigmoid(z + z_hi);
       } else if (hv == 0) {
-        if (!wait(cta, cta.bar(ZX0 + q4), par, ctl)) break;
+        if (!wait_warp(cta, cta.bar(ZX0 + q4), par, ctl)) break;
         sg = sigmoid(z + zx[i]);
       }
       // the gate, saved for the backward if asked (the warp that holds the whole sum); head
@@ -422,7 +422,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
         if constexpr (CW == 2) {
           tc_fence_before();
           mbar_arrive(cta.bar(QS0 + q4));
-          if (!wait(cta, cta.bar(QS0 + q4), par, ctl)) break;
+          if (!wait_warp(cta, cta.bar(QS0 + q4), par, ctl)) break;
           tc_fence_after();
 #pragma unroll
           for (int m = 0; m < MAXB; ++m)
@@ -548,7 +548,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
       if (lane == 0) red[16 + ew] = m;
       mbar_arrive(cta.bar(RED));
     }
-    bool ok = wait(cta, cta.bar(RED), 0, ctl);
+    bool ok = wait_warp(cta, cta.bar(RED), 0, ctl);
     if (ok) {
       e_cur = state_exponent(red_max(2));
       if (e_cur < 0) {
@@ -560,9 +560,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
 
     for (int c = 0; c < n && ok; ++c) {
       const uint32_t s = c & 1, par = c & 1;
-      if (!(ok = wait(cta, cta.bar(O_DONE), par, ctl))) break;
-      if (!(ok = wait(cta, cta.bar(S_DONE), par, ctl))) break;
-      if (!(ok = wait(cta, cta.bar(EP_CONV), par, ctl))) break;
+      if (!(ok = wait_warp(cta, cta.bar(O_DONE), par, ctl))) break;
+      if (!(ok = wait_warp(cta, cta.bar(S_DONE), par, ctl))) break;
+      if (!(ok = wait_warp(cta, cta.bar(EP_CONV), par, ctl))) break;
       tc_fence_after();
       // ---- next chunk's state copy first: it is on the serial chain.  Its exponent comes
       // from a bound, |S_{c+1}| <= lambda^C max|S_c| + 128 max|K'_c| max|V_c|, so the copy
@@ -570,7 +570,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
       int e_next = e_cur;
       if (c < n - 1) {
         // every emit thread has stored its part of max|S_c| (EP_S phase c is complete)
-        if (!(ok = wait(cta, cta.bar(EP_S), par, ctl))) break;
+        if (!(ok = wait_warp(cta, cta.bar(EP_S), par, ctl))) break;
         const float ms = red_max(par);
         float km = kvmax[par * 16], vm = kvmax[par * 16 + 8];
 #pragma unroll
@@ -650,7 +650,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
         for (int u = 0; u < 12; ++u) gq[u] = live ? __ldg(gp + u) : make_uint4(0u, 0u, 0u, 0u);
         xch[hf * 128 + i] = ss;
         mbar_arrive(cta.bar(QX + q4));
-        if (!(ok = wait(cta, cta.bar(QX + q4), par, ctl))) break;
+        if (!(ok = wait_warp(cta, cta.bar(QX + q4), par, ctl))) break;
         const float rr = 1.f / sqrtf((xch[i] + xch[128 + i]) * (1.f / DV) + og.eps);
         if (og.rstd && hf == 0 && live) og.rstd[tok * H + h] = rr;
         const float* wrow = og.w + (h / og.heads_per_tier) * DV + 96 * hf;

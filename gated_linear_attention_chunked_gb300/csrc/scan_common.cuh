@@ -52,6 +52,16 @@ __device__ __forceinline__ bool wait(const Cta& cta, uint32_t bar, uint32_t pari
   return wait_slow(cta.abort_flag(), bar, parity, ctl.err, ctl.wait_ns);
 }
 
+// The bounded wait as taken by all 32 lanes of a warp, with one outcome for the whole warp:
+// false on every lane if any lane's wait gave up (or saw the abort flag).  A lane can see the
+// barrier complete while another lane of its warp gives up at the same instant; the vote keeps
+// the warp on one path, so the warp-collective instructions after it (shuffles, the
+// .sync.aligned TMEM loads and stores, __syncwarp) are never reached by part of a warp.
+__device__ __forceinline__ bool wait_warp(const Cta& cta, uint32_t bar, uint32_t parity,
+                                          const DevCtl& ctl) {
+  return __all_sync(0xffffffffu, wait(cta, bar, parity, ctl));
+}
+
 template <bool BF16>
 __device__ __forceinline__ float ld16(uint32_t bits16) {
   if constexpr (BF16) return __uint_as_float(bits16 << 16);

@@ -45,3 +45,48 @@ def test_wait_gives_up_and_reports_timeout():
     assert gla.get_device_error() == 0
     o_ref, _ = oracle.fwd(q, k, v, oracle_decays(H)[1], a)
     assert rel_err(o.cpu().numpy(), o_ref) <= TOL_CHUNK
+
+
+@pytest.mark.parametrize("case", ["fwd", "bwd", "cut_fwd", "cut_bwd"])
+def test_chunk_kernel_waits_give_up_and_the_next_call_is_correct(case):
+    """The chunk kernels' own waits run out: with a 1 ns limit every wait that does not find
+    its barrier complete at once gives up, raises the CTA's abort flag, and every role leaves
+    its loop on one path per warp (the epilogue warps vote), drains its copies and MMAs and
+    frees its tensor memory.  The host reads GLA_ERR_TIMEOUT; with the limit restored the next
+    forward and backward are correct."""
+    import torch
+    assert torch.cuda.is_available(), "GPU test without a CUDA device"
+    import gated_linear_attention_chunked_gb300 as gla
+    from gated_linear_attention_chunked_gb300 import _build
+    _build.build()
+    gla.load()
+    import oracle
+    B, H = 1, 2
+    T = 4000 if case.startswith("cut") else 512  # 4000: the pairs are cut into parts
+    q, k, v = synth.qkv(95, B, T, H)
+    dO = synth.grad_out(95, B, T, H)
+    a = synth.aug_balance(95, (H, 96), 0.1)
+    gam, gam64 = oracle_decays(H)
+    qd, kd, vd, gd = (to_dev(x, torch.bfloat16) for x in (q, k, v, dO))
+    ad = to_dev(a, torch.float32)
+    assert gla.get_device_error() == 0
+    try:
+        gla.set_wait_timeout_ns(1)
+        if case.endswith("fwd"):
+            gla.chunk_fwd(qd, kd, vd, gam.cuda(), ad)
+        else:
+            gla.chunk_bwd(qd, kd, vd, gam.cuda(), ad, gd)
+        torch.cuda.synchronize()
+        assert gla.get_device_error() == GLA_ERR_TIMEOUT
+    finally:
+        gla.set_wait_timeout_ns(0)
+    o, fin = gla.chunk_fwd(qd, kd, vd, gam.cuda(), ad)
+    g = gla.chunk_bwd(qd, kd, vd, gam.cuda(), ad, gd)
+    torch.cuda.synchronize()
+    assert gla.get_device_error() == 0
+    o_ref, fin_ref = oracle.fwd(q, k, v, gam64, a)
+    ref = oracle.bwd(q, k, v, gam64, a, dO)
+    assert rel_err(o.cpu().numpy(), o_ref) <= TOL_CHUNK
+    assert rel_err(fin.cpu().numpy(), fin_ref) <= TOL_CHUNK
+    for x, n in zip(g, ("dq", "dk", "dv", "d_a", "d_init_state")):
+        assert rel_err(x.cpu().numpy(), ref[n]) <= TOL_CHUNK, n
