@@ -154,7 +154,7 @@ def oracle_sample(n_seq: int, seed: int = 2):
     return n_seq * T / dt, dt
 
 
-def oracle_decode_sample(every: int = 64, steps: int = 3, seed: int = 3):
+def oracle_decode_sample(every: int = 64, steps: int = 40, seed: int = 3):
     """Time the fp64 oracle's decode step over every `every`-th sequence of the serving pool
     (all 24 layers x 16 heads each); returns (states per second, states, seconds)."""
     import numpy as np
@@ -176,7 +176,7 @@ def oracle_decode_sample(every: int = 64, steps: int = 3, seed: int = 3):
     return n_states * steps / dt, n_states, dt
 
 
-def oracle_long_prefill_sample(t_sample: int = 8192, seed: int = 4):
+def oracle_long_prefill_sample(t_sample: int = 65536, seed: int = 4):
     """Time the fp64 oracle's forward over the first `t_sample` tokens of both long-prefill
     sequences (B=2, H=16, with the initial state); returns (tokens per second, seconds)."""
     import numpy as np
@@ -506,13 +506,13 @@ def run_gpu(args, rank, world, local_rank):
                        kind="oracle", states_per_s=st_rate,
                        ms_per_step_extrapolated=1e3 * n_states / st_rate,
                        sample=f"fp64 oracle decode step over every 64th sequence of the pool "
-                              f"({n_st} states: 20 sequences x 24 layers x 16 heads), 3 steps, "
+                              f"({n_st} states: 20 sequences x 24 layers x 16 heads), 40 steps, "
                               f"{dtd:.1f} s; GB/s counts the same algorithmic bytes as the GPU "
                               f"line; ms_per_step_extrapolated = the whole 1280-sequence pool at "
                               f"this rate (linear extrapolation)")
         lp_rate, dtl = oracle_long_prefill_sample()
         cpu_long = dict(value=lp_rate, unit="tokens/s", cores=cores, kind="oracle",
-                        sample=f"fp64 oracle forward over the first 8192 of the 131072 tokens of "
+                        sample=f"fp64 oracle forward over the first 65536 of the 131072 tokens of "
                                f"both long-prefill sequences (H=16, initial state), {dtl:.1f} s")
 
     clocks = clk.summary()

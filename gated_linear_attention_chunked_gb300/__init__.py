@@ -103,6 +103,8 @@ def load(path: str | None = None):
             lib.gla_chunk_split_plan.restype = _I
             lib.gla_set_split_parts.argtypes = [_I]
             lib.gla_set_split_parts.restype = _I
+            lib.gla_set_stall_step.argtypes = [_I]
+            lib.gla_set_stall_step.restype = _I
             lib.gla_chunk_state_sum.argtypes = [_P, _P, _I, _P, _P] + [_I] * 5 + [_P]
             lib.gla_chunk_state_sum.restype = _I
             lib.gla_chunk_adjoint_sum.argtypes = [_P, _P, _I, _P, _P] + [_I] * 5 + [_P]
@@ -516,6 +518,12 @@ def wait_probe(stream=None) -> None:
 
 def set_wait_timeout_ns(ns: int) -> None:
     _check("gla_set_wait_timeout_ns", load().gla_set_wait_timeout_ns(int(ns)))
+
+
+def set_stall_step(step: int) -> None:
+    """gla_set_stall_step: the chunk kernels' MMA issuer stalls at chunk step `step` (its
+    bounded wait then gives up: the give-up path's diagnostic); -1 turns it off."""
+    _check("gla_set_stall_step", load().gla_set_stall_step(int(step)))
 
 
 def split_plan(B: int, T: int, H: int, backward: bool, n_sm: int) -> tuple[int, int]:

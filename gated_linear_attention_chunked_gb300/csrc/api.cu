@@ -14,6 +14,7 @@ namespace {
 __device__ int g_device_error = 0;
 std::atomic<unsigned long long> g_wait_ns{2000000000ull};
 std::atomic<int> g_split_parts{0};  // gla_set_split_parts: 0 automatic, 1 never, p >= 2 forced
+std::atomic<int> g_stall_step{-1};  // gla_set_stall_step: the give-up path's diagnostic
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
@@ -24,6 +25,7 @@ gla_status ctl_for_current_device(gla::DevCtl* ctl) {
   if (cudaGetSymbolAddress(reinterpret_cast<void**>(&ctl->err), g_device_error) != cudaSuccess)
     return GLA_ERR_CUDA;
   ctl->wait_ns = g_wait_ns.load();
+  ctl->stall_step = g_stall_step.load();
   return GLA_OK;
 }
 
@@ -159,6 +161,7 @@ namespace gla {
 cudaError_t current_device_ctl(DevCtl* ctl) {
   cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void**>(&ctl->err), g_device_error);
   ctl->wait_ns = g_wait_ns.load();
+  ctl->stall_step = g_stall_step.load();
   return e;
 }
 }  // namespace gla
@@ -196,6 +199,11 @@ gla_status gla_get_device_error(void) {
 
 gla_status gla_set_wait_timeout_ns(unsigned long long ns) {
   g_wait_ns.store(ns ? ns : 2000000000ull);
+  return GLA_OK;
+}
+
+gla_status gla_set_stall_step(int step) {
+  g_stall_step.store(step < 0 ? -1 : step);
   return GLA_OK;
 }
 

@@ -260,6 +260,12 @@ __device__ __forceinline__ void run_role(
     if (lane == 0) {
       for (int t = 0; t < n; ++t) {
         const uint32_t par = t & 1;
+        // the give-up path's diagnostic: the drain barrier's first phase completes only after
+        // this loop, so this bounded wait runs out and the CTA gives up
+        if (t == ctl.stall_step) {
+          wait(cta, cta.bar(DRAIN), 0, ctl);
+          break;
+        }
         if (!wait(cta, cta.bar(FULL_E), par, ctl)) break;
         // the previous chunk's TMEM-operand MMAs have read D_P
         if (t >= 1 && !wait(cta, cta.bar(X_DONE), (t - 1) & 1, ctl)) break;

@@ -223,6 +223,12 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
       for (int c = 0; c < n; ++c) {
         const uint32_t s = c & 1, st = cta.sb + s * STAGE;
         const uint32_t slot = cta.sb + (s ^ 1) * STAGE;  // state copy for this chunk
+        // the give-up path's diagnostic: the drain barrier's first phase completes only after
+        // this loop, so this bounded wait runs out and the CTA gives up
+        if (c == ctl.stall_step) {
+          wait(cta, cta.bar(DRAIN), 0, ctl);
+          break;
+        }
         if (!wait(cta, cta.bar(QK_FULL + s), (c >> 1) & 1, ctl)) break;
         // P'' of the previous chunk lives in D_P's columns: P'' V must be done before Q K^T
         // overwrites them

@@ -16,6 +16,8 @@ enum : int { DEV_OK = 0, DEV_TIMEOUT = 5, DEV_RANGE = 6, DEV_LAYOUT = 8 };
 struct DevCtl {
   int* err;                    // device error word
   unsigned long long wait_ns;  // limit of every bounded wait
+  int stall_step = -1;         // >= 0: the chunk kernels' MMA issuer stalls at this chunk step
+                               // (the give-up path's diagnostic, gla_set_stall_step)
 };
 
 __device__ __forceinline__ void record_error(const DevCtl& ctl, int code) {

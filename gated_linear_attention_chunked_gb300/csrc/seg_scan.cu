@@ -160,6 +160,10 @@ seg_sum_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant_
       constexpr uint32_t ID = idesc_f16(128, 192, false, false, true, true);
       for (int m = 0; m < M; ++m) {
         const int s = m % STAGES;
+        if (m == ctl.stall_step) {  // the give-up path's diagnostic (see the chunk kernels)
+          wait(cta, cta.bar(DONE), 0, ctl);
+          break;
+        }
         if (!wait(cta, cta.bar(CONV + s), (m / STAGES) & 1, ctl)) break;
         tc_fence_after();
         const uint32_t st = sb + s * STAGE;

@@ -104,6 +104,19 @@ GLA_API gla_status gla_set_wait_timeout_ns(unsigned long long ns);
  * `stream`. */
 GLA_API gla_status gla_wait_probe(cudaStream_t stream);
 
+/* Diagnostic of the chunk kernels' give-up path (no counterpart in the article).  For calls
+ * made after it returns (process-wide), the tensor-core issuer of every CTA of the chunked
+ * forward, backward and segment-pass kernels, on reaching chunk step `step` of its loop,
+ * waits on a barrier whose phase completes only after that loop.  The bounded wait gives up
+ * after the limit of gla_set_wait_timeout_ns, records GLA_ERR_TIMEOUT and raises the CTA's
+ * abort flag; every role then leaves its loop (one path per warp), drains its copies and
+ * tensor-core work, frees its tensor memory and exits.  The call's outputs are then
+ * undefined; the context stays usable.  step < 0 (the default) turns it off.  No fault,
+ * trap or unbounded wait is involved.  The mbarrier wait instruction suspends the waiting
+ * thread until the phase completes (up to a hardware limit), so ordinary waits end before
+ * any limit of the timer can be checked: a stall like this is what makes a wait run out. */
+GLA_API gla_status gla_set_stall_step(int step);
+
 /* Decay schedule ("Decay schedule" paragraph): half-lives
  *   T_h = t_min * (t_max / t_min)^(h / (H - 1))   (T_0 = t_min if H == 1)
  * and log_decay[h] = ln(2^(-1/T_h)) = -ln(2) / T_h, computed in double and

@@ -47,13 +47,15 @@ def test_wait_gives_up_and_reports_timeout():
     assert rel_err(o.cpu().numpy(), o_ref) <= TOL_CHUNK
 
 
-@pytest.mark.parametrize("case", ["fwd", "bwd", "cut_fwd", "cut_bwd"])
-def test_chunk_kernel_waits_give_up_and_the_next_call_is_correct(case):
-    """The chunk kernels' own waits run out: with a 1 ns limit every wait that does not find
-    its barrier complete at once gives up, raises the CTA's abort flag, and every role leaves
-    its loop on one path per warp (the epilogue warps vote), drains its copies and MMAs and
-    frees its tensor memory.  The host reads GLA_ERR_TIMEOUT; with the limit restored the next
-    forward and backward are correct."""
+@pytest.mark.parametrize("case,step", [("fwd", 0), ("fwd", 2), ("bwd", 0), ("bwd", 3),
+                                       ("cut_fwd", 1), ("cut_bwd", 1)])
+def test_chunk_kernel_waits_give_up_and_the_next_call_is_correct(case, step):
+    """The chunk kernels' own waits run out: with gla_set_stall_step the tensor-core issuer of
+    every CTA waits, at chunk step `step`, on a barrier that completes only after its loop, so
+    its bounded wait (2 ms here) gives up and raises the CTA's abort flag.  Every role then
+    leaves its loop on one path per warp (the epilogue warps vote), drains its copies and
+    MMAs and frees its tensor memory.  The host reads GLA_ERR_TIMEOUT; with the diagnostic off
+    the next forward and backward are correct."""
     import torch
     assert torch.cuda.is_available(), "GPU test without a CUDA device"
     import gated_linear_attention_chunked_gb300 as gla
@@ -62,7 +64,7 @@ def test_chunk_kernel_waits_give_up_and_the_next_call_is_correct(case):
     gla.load()
     import oracle
     B, H = 1, 2
-    T = 4000 if case.startswith("cut") else 512  # 4000: the pairs are cut into parts
+    T = 4000 if case.startswith("cut") else 640  # 4000: the pairs are cut into parts
     q, k, v = synth.qkv(95, B, T, H)
     dO = synth.grad_out(95, B, T, H)
     a = synth.aug_balance(95, (H, 96), 0.1)
@@ -71,14 +73,19 @@ def test_chunk_kernel_waits_give_up_and_the_next_call_is_correct(case):
     ad = to_dev(a, torch.float32)
     assert gla.get_device_error() == 0
     try:
-        gla.set_wait_timeout_ns(1)
+        gla.set_wait_timeout_ns(2_000_000)
+        gla.set_stall_step(step)
+        t0 = time.perf_counter()
         if case.endswith("fwd"):
             gla.chunk_fwd(qd, kd, vd, gam.cuda(), ad)
         else:
             gla.chunk_bwd(qd, kd, vd, gam.cuda(), ad, gd)
         torch.cuda.synchronize()
+        dt = time.perf_counter() - t0
         assert gla.get_device_error() == GLA_ERR_TIMEOUT
+        assert dt < 5.0
     finally:
+        gla.set_stall_step(-1)
         gla.set_wait_timeout_ns(0)
     o, fin = gla.chunk_fwd(qd, kd, vd, gam.cuda(), ad)
     g = gla.chunk_bwd(qd, kd, vd, gam.cuda(), ad, gd)
