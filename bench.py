@@ -206,6 +206,49 @@ def job_rate(world, units_per_rank, seconds):
     return world * units_per_rank / seconds
 
 
+def run_cpu_configs(args):
+    """--cpu-configs: the fp64 oracle timed on this host's cores on every workload -- tiny
+    fp32 fwd+bwd (whole), the layer forward B=8 (whole), the training fwd+bwd B=32 (whole),
+    the decode step (every 64th sequence of the pool, extrapolated) and the long prefill (the
+    first 65536 of 131072 tokens of both sequences).  One JSON line; the CPU baseline the
+    GPU numbers are reported beside."""
+    import numpy as np
+
+    import oracle
+    import synth
+    cores = os.cpu_count() or 1
+    try:
+        import platform
+        cpu = platform.processor() or platform.machine()
+    except Exception:  # noqa: BLE001 - informational only
+        cpu = "unknown"
+    out = dict(part="cpu_configs", cores=cores, cpu=cpu, unit_note="tokens/s unless stated")
+
+    def timed(fn):
+        t0 = time.perf_counter()
+        fn()
+        return time.perf_counter() - t0
+
+    x = synth.chunk_inputs("tiny_fp32")
+    g2 = oracle.decay_schedule(2).astype(np.float32).astype(np.float64)
+    dt = timed(lambda: (oracle.fwd(x["q"], x["k"], x["v"], g2, x["a"]),
+                        oracle.bwd(x["q"], x["k"], x["v"], g2, x["a"], x["dO"])))
+    out["tiny_fp32_fwd_bwd"] = dict(s=dt, tokens_per_s=256 / dt)
+    g = oracle.decay_schedule(H).astype(np.float32).astype(np.float64)
+    x = synth.chunk_inputs("layer_fwd_aug")
+    dt = timed(lambda: oracle.fwd(x["q"], x["k"], x["v"], g, x["a"]))
+    out["layer_fwd_B8"] = dict(s=dt, tokens_per_s=8 * T / dt)
+    rate, dt = oracle_sample(32)
+    out["train_fwd_bwd_B32"] = dict(s=dt, tokens_per_s=rate)
+    st_rate, n_st, dt = oracle_decode_sample()
+    out["decode_pool"] = dict(s=dt, states=n_st, steps=40, gbs=st_rate * DEC_BYTES_STATE / 1e9,
+                              ms_per_step_extrapolated=1e3 * N_SEQ * N_LAYERS * H / st_rate)
+    rate, dt = oracle_long_prefill_sample()
+    out["long_prefill_fwd_sample"] = dict(s=dt, tokens=2 * 65536, tokens_per_s=rate)
+    print(json.dumps(out), flush=True)
+    return 0
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return 0
@@ -853,6 +896,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-configs", action="store_true",
+                    help="time the fp64 CPU oracle on every workload (no GPU work)")
     ap.add_argument("--cpu-seqs", type=int, default=32,
                     help="sequences of the training workload the CPU oracle baseline times")
     ap.add_argument("--part", choices=["all", "fwd", "bwd", "decode", "long", "paged", "norm", "conv", "fused"], default="all",
@@ -874,6 +919,8 @@ def main():
         print("bench.py: for --gpus N > 1 launch with torch.distributed.run (one rank per GPU)",
               file=sys.stderr)
         return 2
+    if args.cpu_configs:
+        return run_cpu_configs(args) if rank == 0 else 0
     if args.impl == "reference":
         return run_reference(args, rank, world)
     if args.part == "long":
