@@ -38,8 +38,11 @@ WORKLOAD = ("GLA chunked fwd+bwd B=32 T=2048 H=16 dk=96 dv=192 chunk=128 bf16-in
             "plus one decode step over 1280 seqs x 24 layers x 16 heads of 96x192 fp32 states")
 # Algorithmic work per unit (what the calls must move / compute at minimum)
 # the training step saves the gate sigmoid(z) (fp32 per token-head) in the forward for the backward
+# and the state copies (36,864 B fp16 + a 4-byte exponent per chunk of 128 tokens, 288.03 B per
+# token-head), written by the forward and read by the backward's dq part
 FWD_BYTES_TH = (96 + 96 + 192) * 2 + 192 * 4 + 4         # bf16 q,k,v in, fp32 o, gate out = 1540
 BWD_BYTES_TH = (96 + 96 + 192 + 192) * 2 + 4 + (96 + 96 + 192) * 4  # + dO, gate in; dq,dk,dv = 2692
+SAVED_BYTES_TH = (96 * 192 * 2 + 4) / 128                 # state copies: 288.03
 FWD_FLOPS_TH = 2 * (128 * 96 + 128 * 192 + 96 * 192 + 96 * 192)  # QK^T, PV, QS, K^T V = 147456
 BWD_FLOPS_TH = 319488                                     # 9 dense chunk matmuls per token-head
 DEC_BYTES_STATE = 2 * 96 * 192 * 4 + (96 + 96 + 192 + 192) * 4  # state r+w, q,k,v,o = 149760
@@ -315,9 +318,12 @@ def run_gpu(args, rank, world, local_rank):
         o = torch.empty(Bn, T, H, DV, device=dev)
         fin = torch.empty(Bn, H, DK, DV, device=dev)
         gate = torch.empty(Bn, H, T, device=dev)  # sigmoid(z), saved by the forward
+        saved = (torch.empty(gla.chunk_saved_states_size(Bn, T, H), dtype=torch.uint8, device=dev)
+                 if args.saved_states else None)  # the state copies, saved by the forward
         ws = torch.empty(max(1, gla.chunk_bwd_workspace_size(Bn, T, H, gla.GLA_BF16)),
                          dtype=torch.uint8, device=dev)
-        gla.chunk_fwd(q, k, v, gam, a, out=o, final_state=fin, gate=gate)  # a backward alone reads it
+        # a backward alone reads what this forward saves
+        gla.chunk_fwd(q, k, v, gam, a, out=o, final_state=fin, gate=gate, saved_states=saved)
 
     # ---- serving pool: 1280 x 24 x 16 states, warmed by 64 recurrent steps from zero
     if do_dec:
@@ -346,11 +352,11 @@ def run_gpu(args, rank, world, local_rank):
         if evs:
             evs[0].record(stream)
         if do_fwd:
-            gla.chunk_fwd(q, k, v, gam, a, out=o, final_state=fin, gate=gate)
+            gla.chunk_fwd(q, k, v, gam, a, out=o, final_state=fin, gate=gate, saved_states=saved)
         if evs:
             evs[1].record(stream)
         if do_bwd:
-            gla.chunk_bwd(q, k, v, gam, a, dO, gate=gate, workspace=ws)
+            gla.chunk_bwd(q, k, v, gam, a, dO, gate=gate, saved_states=saved, workspace=ws)
         if evs:
             evs[2].record(stream)
         if do_dec:
@@ -414,8 +420,10 @@ def run_gpu(args, rank, world, local_rank):
     roofline = roof("hbm", dec_gbs, pk["hbm"], "GB/s",
                     None if tr_dec is None else tr_dec["bytes_per_unit"] * n_states)
     roofline["kernel"] = "decode_kernel (dominant: largest share of the step time)"
-    fwd_gbs = th * FWD_BYTES_TH / (fwd_t * 1e-3) / 1e9
-    bwd_gbs = th * BWD_BYTES_TH / (bwd_t * 1e-3) / 1e9
+    fb_th = FWD_BYTES_TH + (SAVED_BYTES_TH if args.saved_states else 0.0)
+    bb_th = BWD_BYTES_TH + (SAVED_BYTES_TH if args.saved_states else 0.0)
+    fwd_gbs = th * fb_th / (fwd_t * 1e-3) / 1e9
+    bwd_gbs = th * bb_th / (bwd_t * 1e-3) / 1e9
     roof_fwd = roof("hbm", fwd_gbs, pk["hbm"], "GB/s",
                     None if tr_fwd is None else tr_fwd["bytes_per_unit"] * th)
     roof_fwd["tensor"] = dict(achieved=th * FWD_FLOPS_TH / (fwd_t * 1e-3) / 1e12, peak=pk["bf16"],
@@ -454,8 +462,10 @@ def run_gpu(args, rank, world, local_rank):
                     copied[i].record(copy_stream)
                 stream.wait_event(copied[i])
                 bq, bk, bv, bdO = bufs[i]
-                gla.chunk_fwd(bq, bk, bv, gam, a, out=o, final_state=fin, gate=gate)
-                _, _, _, daug, _ = gla.chunk_bwd(bq, bk, bv, gam, a, bdO, gate=gate, workspace=ws,
+                gla.chunk_fwd(bq, bk, bv, gam, a, out=o, final_state=fin, gate=gate,
+                              saved_states=saved)
+                _, _, _, daug, _ = gla.chunk_bwd(bq, bk, bv, gam, a, bdO, gate=gate,
+                                                 saved_states=saved, workspace=ws,
                                                  want_d_init_state=False)
                 consumed[i].record(stream)
                 h_daug[s_].copy_(daug, non_blocking=True)
@@ -505,9 +515,10 @@ def run_gpu(args, rank, world, local_rank):
                     stream.wait_event(read[i])  # step s-2's outputs have left buffer i
                 bq, bk, bv, bdO = bufs[i]
                 ob = outs[i]
-                gla.chunk_fwd(bq, bk, bv, gam, a, out=ob["o"], final_state=fin, gate=gate)
+                gla.chunk_fwd(bq, bk, bv, gam, a, out=ob["o"], final_state=fin, gate=gate,
+                              saved_states=saved)
                 dq_, dk_, dv_, daug, _ = gla.chunk_bwd(bq, bk, bv, gam, a, bdO, gate=gate,
-                                                       workspace=ws_full,
+                                                       saved_states=saved, workspace=ws_full,
                                                        want_d_init_state=False)
                 consumed[i].record(stream)
                 ob["dq"], ob["dk"], ob["dv"] = dq_, dk_, dv_
@@ -821,7 +832,7 @@ def run_long_prefill(args):
     def call(w, nb):
         rc = lib.gla_chunk_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), gla.GLA_BF16,
                                gam.data_ptr(), a.data_ptr(), init.data_ptr(), o.data_ptr(),
-                               fin.data_ptr(), gl.data_ptr(), w, nb, Bl, Tl, H, DK, DV,
+                               fin.data_ptr(), gl.data_ptr(), None, 0, w, nb, Bl, Tl, H, DK, DV,
                                stream.cuda_stream)
         if rc != 0:
             raise RuntimeError(gla.status_string(rc))
@@ -855,7 +866,7 @@ def run_long_prefill(args):
     def call_b(nb):
         rc = lib.gla_chunk_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), gla.GLA_BF16,
                                gam.data_ptr(), a.data_ptr(), init.data_ptr(), dO.data_ptr(), None,
-                               gl.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                               gl.data_ptr(), None, 0, dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
                                d_a.data_ptr(), dinit.data_ptr(), wsb.data_ptr(), nb, Bl, Tl, H,
                                DK, DV, stream.cuda_stream)
         if rc != 0:
@@ -896,6 +907,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-saved-states", dest="saved_states", action="store_false",
+                    help="the training step without the forward's saved state copies")
     ap.add_argument("--cpu-configs", action="store_true",
                     help="time the fp64 CPU oracle on every workload (no GPU work)")
     ap.add_argument("--cpu-seqs", type=int, default=32,

@@ -64,11 +64,15 @@ def load(path: str | None = None):
             lib.gla_decay_schedule.restype = _I
             lib.gla_chunk_fwd_workspace_size.argtypes = [_I] * 6
             lib.gla_chunk_fwd_workspace_size.restype = _S
-            lib.gla_chunk_fwd.argtypes = [_P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _P, _S] + [_I] * 5 + [_P]
+            lib.gla_chunk_fwd.argtypes = ([_P, _P, _P, _I] + [_P] * 6 + [_P, _S, _P, _S] +
+                                          [_I] * 5 + [_P])
             lib.gla_chunk_fwd.restype = _I
             lib.gla_chunk_bwd_workspace_size.argtypes = [_I] * 6
             lib.gla_chunk_bwd_workspace_size.restype = _S
-            lib.gla_chunk_bwd.argtypes = [_P] * 3 + [_I] + [_P] * 12 + [_S] + [_I] * 5 + [_P]
+            lib.gla_chunk_bwd.argtypes = ([_P] * 3 + [_I] + [_P] * 7 + [_S] + [_P] * 6 + [_S] +
+                                          [_I] * 5 + [_P])
+            lib.gla_chunk_saved_states_size.argtypes = [_I] * 3
+            lib.gla_chunk_saved_states_size.restype = _S
             lib.gla_chunk_bwd.restype = _I
             lib.gla_decode_step.argtypes = [_P] * 7 + [_I] * 5 + [_P]
             lib.gla_wait_probe.argtypes = [_P]
@@ -188,11 +192,28 @@ def _workspace(nbytes, device, workspace):
     return torch.empty(nbytes, dtype=torch.uint8, device=device)
 
 
+def chunk_saved_states_size(B, T, H) -> int:
+    """Bytes of the state copies a forward saves for the backward (gla_chunk_saved_states_size)."""
+    return load().gla_chunk_saved_states_size(B, T, H)
+
+
+def _saved(t, nbytes, name):
+    if t is None:
+        return None, 0
+    have = t.numel() * t.element_size()
+    if have < nbytes:
+        raise ValueError(f"{name} holds {have} bytes, {nbytes} needed")
+    return _dev(t, name), have
+
+
 def chunk_fwd(q, k, v, log_decay, aug_balance, init_state=None, *, want_final_state=True,
-              out=None, final_state=None, gate=None, workspace=None, stream=None):
+              out=None, final_state=None, gate=None, saved_states=None, workspace=None,
+              stream=None):
     """Chunked forward (gla_chunk_fwd).  q,k [B,T,H,96], v [B,T,H,192] (bf16/fp16/fp32);
     log_decay [H], aug_balance [H,96], init_state [B,H,96,192] fp32 (optional); gate: an
-    fp32 [B,H,T] tensor that receives sigmoid(q.(a*k)) for chunk_bwd (optional).
+    fp32 [B,H,T] tensor that receives sigmoid(q.(a*k)) for chunk_bwd (optional);
+    saved_states: a uint8 device tensor of chunk_saved_states_size(B, T, H) bytes that receives
+    the chunks' state copies for chunk_bwd (optional).
     Returns (o fp32 [B,T,H,192], final_state fp32 [B,H,96,192] or None)."""
     torch = _torch()
     B, T, H, dk = q.shape
@@ -205,13 +226,14 @@ def chunk_fwd(q, k, v, log_decay, aug_balance, init_state=None, *, want_final_st
     if gate is not None and tuple(gate.shape) != (B, H, T):
         raise ValueError(f"gate must be [B,H,T] = {(B, H, T)}, got {tuple(gate.shape)}")
     ws = _workspace(load().gla_chunk_fwd_workspace_size(B, T, H, dk, dv, code), q.device, workspace)
+    sp, sb = _saved(saved_states, chunk_saved_states_size(B, T, H), "saved_states")
     rc = load().gla_chunk_fwd(
         _dev(q, "q"), _dev(k, "k", q.dtype), _dev(v, "v", q.dtype), code,
         _dev(log_decay, "log_decay", torch.float32), _dev(aug_balance, "aug_balance", torch.float32),
         _dev(init_state, "init_state", torch.float32), _dev(out, "o", torch.float32),
         _dev(final_state, "final_state", torch.float32), _dev(gate, "gate", torch.float32),
-        _dev(ws, "workspace"), 0 if ws is None else ws.numel() * ws.element_size(), B, T, H, dk,
-        dv, _stream(stream))
+        sp, sb, _dev(ws, "workspace"), 0 if ws is None else ws.numel() * ws.element_size(), B, T,
+        H, dk, dv, _stream(stream))
     _check("gla_chunk_fwd", rc)
     return out, final_state
 
@@ -243,10 +265,10 @@ def chunk_fwd_gated(q, k, v, log_decay, aug_balance, g, norm_weight, n_tiers, ep
 
 
 def chunk_bwd(q, k, v, log_decay, aug_balance, dO, init_state=None, d_final_state=None, *,
-              gate=None, want_d_init_state=True, workspace=None, stream=None):
+              gate=None, saved_states=None, want_d_init_state=True, workspace=None, stream=None):
     """Chunked backward (gla_chunk_bwd).  gate: the fp32 [B,H,T] sigmoid(q.(a*k)) that
-    chunk_fwd saved (optional; recomputed if None).  Returns (dq, dk, dv, d_aug, d_init_state),
-    fp32."""
+    chunk_fwd saved (optional; recomputed if None); saved_states: the state copies chunk_fwd
+    saved for the same inputs (optional).  Returns (dq, dk, dv, d_aug, d_init_state), fp32."""
     torch = _torch()
     B, T, H, dk = q.shape
     dv = v.shape[-1]
@@ -260,12 +282,13 @@ def chunk_bwd(q, k, v, log_decay, aug_balance, dO, init_state=None, d_final_stat
     if gate is not None and tuple(gate.shape) != (B, H, T):
         raise ValueError(f"gate must be [B,H,T] = {(B, H, T)}, got {tuple(gate.shape)}")
     ws = _workspace(load().gla_chunk_bwd_workspace_size(B, T, H, dk, dv, code), q.device, workspace)
+    sp, sb = _saved(saved_states, chunk_saved_states_size(B, T, H), "saved_states")
     rc = load().gla_chunk_bwd(
         _dev(q, "q"), _dev(k, "k", q.dtype), _dev(v, "v", q.dtype), code,
         _dev(log_decay, "log_decay", torch.float32), _dev(aug_balance, "aug_balance", torch.float32),
         _dev(init_state, "init_state", torch.float32), _dev(dO, "dO", q.dtype),
         _dev(d_final_state, "d_final_state", torch.float32), _dev(gate, "gate", torch.float32),
-        _dev(dq, "dq"), _dev(dk_, "dk"),
+        sp, sb, _dev(dq, "dq"), _dev(dk_, "dk"),
         _dev(dv_, "dv"), _dev(d_aug, "d_aug"), _dev(dinit, "d_init_state"), _dev(ws, "workspace"),
         0 if ws is None else ws.numel() * ws.element_size(), B, T, H, dk, dv, _stream(stream))
     _check("gla_chunk_bwd", rc)

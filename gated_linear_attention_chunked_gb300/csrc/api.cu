@@ -93,9 +93,12 @@ gla_status chunk_fwd_impl(const void* q, const void* k, const void* v, gla_dtype
                           const float* init_state, float* o, float* final_state, void* workspace,
                           size_t workspace_bytes, int B, int T, int H, int dk, int dv,
                           const gla::StatePages& sp, cudaStream_t stream,
-                          const gla::OutGate& og = gla::OutGate{}, float* gate = nullptr) {
+                          const gla::OutGate& og = gla::OutGate{}, float* gate = nullptr,
+                          void* saved = nullptr, size_t saved_bytes = 0) {
   gla_status st = check_chunk_sizes(B, T, H, dk, dv, in_dtype);
   if (st != GLA_OK) return st;
+  if (saved && saved_bytes < gla::saved_states_bytes(B, T, H)) return GLA_ERR_WORKSPACE;
+  if (!aligned256(saved)) return GLA_ERR_ALIGNMENT;
   if (!q || !k || !v || !log_decay || !aug_balance || (!o && !og.g)) return GLA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(log_decay) ||
       !aligned16(aug_balance) || !aligned16(init_state) || !aligned16(o) ||
@@ -119,6 +122,7 @@ gla_status chunk_fwd_impl(const void* q, const void* k, const void* v, gla_dtype
   a.q = q; a.k = k; a.v = v; a.bf16 = in_dtype == GLA_BF16;
   a.log_decay = log_decay; a.aug = aug_balance; a.init = init_state;
   a.o = o; a.fin = final_state; a.B = B; a.T = T; a.H = H; a.sp = sp; a.og = og; a.gate = gate;
+  a.saved = gla::saved_states_at(saved, B, T, H);
   if (in_dtype == GLA_FP32) {
     const size_t tok = (size_t)B * T * H;
     uint8_t* w = static_cast<uint8_t*>(workspace);
@@ -232,14 +236,20 @@ size_t gla_chunk_fwd_workspace_size(int B, int T, int H, int dk, int dv, gla_dty
   return extra ? round256(must) + extra : must;
 }
 
+size_t gla_chunk_saved_states_size(int B, int T, int H) {
+  if (B <= 0 || T <= 0 || H <= 0 || (long long)B * T > (1ll << 31) - 1) return 0;
+  return gla::saved_states_bytes(B, T, H);
+}
+
 gla_status gla_chunk_fwd(const void* q, const void* k, const void* v, gla_dtype in_dtype,
                          const float* log_decay, const float* aug_balance,
                          const float* init_state, float* o, float* final_state, float* gate,
-                         void* workspace, size_t workspace_bytes, int B, int T, int H, int dk,
-                         int dv, cudaStream_t stream) {
+                         void* saved_states, size_t saved_states_bytes, void* workspace,
+                         size_t workspace_bytes, int B, int T, int H, int dk, int dv,
+                         cudaStream_t stream) {
   return chunk_fwd_impl(q, k, v, in_dtype, log_decay, aug_balance, init_state, o, final_state,
                         workspace, workspace_bytes, B, T, H, dk, dv, gla::StatePages{}, stream,
-                        gla::OutGate{}, gate);
+                        gla::OutGate{}, gate, saved_states, saved_states_bytes);
 }
 
 gla_status gla_chunk_fwd_gated(const void* q, const void* k, const void* v, gla_dtype in_dtype,
@@ -313,12 +323,15 @@ gla_status gla_chunk_split_plan(int B, int T, int H, int backward, int n_sm, int
 gla_status gla_chunk_bwd(const void* q, const void* k, const void* v, gla_dtype in_dtype,
                          const float* log_decay, const float* aug_balance,
                          const float* init_state, const void* dO, const float* d_final_state,
-                         const float* gate, float* dq, float* dk, float* dv, float* d_aug,
-                         float* d_init_state,
+                         const float* gate, const void* saved_states, size_t saved_states_bytes,
+                         float* dq, float* dk, float* dv, float* d_aug, float* d_init_state,
                          void* workspace, size_t workspace_bytes, int B, int T, int H, int dk_,
                          int dv_, cudaStream_t stream) {
   gla_status st = check_chunk_sizes(B, T, H, dk_, dv_, in_dtype);
   if (st != GLA_OK) return st;
+  if (saved_states && saved_states_bytes < gla::saved_states_bytes(B, T, H))
+    return GLA_ERR_WORKSPACE;
+  if (!aligned256(saved_states)) return GLA_ERR_ALIGNMENT;
   if (!q || !k || !v || !log_decay || !aug_balance || !dO || !dq || !dk || !dv || !d_aug)
     return GLA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(log_decay) ||
@@ -344,6 +357,7 @@ gla_status gla_chunk_bwd(const void* q, const void* k, const void* v, gla_dtype 
   a.q = q; a.k = k; a.v = v; a.dO = dO; a.bf16 = in_dtype == GLA_BF16;
   a.log_decay = log_decay; a.aug = aug_balance; a.init = init_state; a.dfin = d_final_state;
   a.dq = dq; a.dk = dk; a.dv = dv; a.d_aug = d_aug; a.dinit = d_init_state; a.gate = gate;
+  a.saved = gla::saved_states_at(const_cast<void*>(saved_states), B, T, H);
   a.workspace = workspace; a.workspace_bytes = gla::chunk_bwd_workspace_bytes(B, T, H);
   a.B = B; a.T = T; a.H = H;
   if (in_dtype == GLA_FP32) {
@@ -367,6 +381,9 @@ gla_status gla_chunk_bwd(const void* q, const void* k, const void* v, gla_dtype 
     a.seg_state = reinterpret_cast<float*>(w);
     a.seg_adj = reinterpret_cast<float*>(w + round256(slots * kStateBytes));
     a.da_split = reinterpret_cast<float*>(w + 2 * round256(slots * kStateBytes));
+    // with the forward's saved state copies the DQ role needs no starting states: only the
+    // adjoints (DV, DK) are summed and linked
+    if (a.saved.copy) a.seg_state = nullptr;
     if (gla::launch_segment_states(a.q, a.k, a.v, a.dO, a.bf16, log_decay, init_state,
                                    d_final_state, gla::StatePages{}, a.seg_state, a.seg_adj, B, T,
                                    H, plan, ctl, stream) != cudaSuccess)

@@ -104,6 +104,7 @@ struct BwdParams {
   const float* seg_adj;    // cut pairs: adjoint leaving each part (DV's and DK's start)
   float* da_split;         // cut pairs: d_aug partial sums per part, [96] each
   const float* gate;       // [B,H,T] sigmoid(z) saved by the forward, or null (recomputed)
+  SavedStates saved;       // the forward's state copies (DQ reads them instead of scanning)
 };
 
 enum Tile : int { T_Q = 0, T_K = 1, T_V = 2, T_G = 3 };
@@ -117,16 +118,20 @@ __device__ __forceinline__ constexpr int tile_group(int tile) {
   if (ROLE == R_DK) return tile == T_Q ? 1 : 0;
   return tile == T_V ? -1 : (tile == T_G ? 1 : 0);
 }
-template <int ROLE>
+template <int ROLE, bool SC>
 __device__ __forceinline__ constexpr uint32_t group_bytes(int g) {
   return (tile_group<ROLE>(T_Q) == g ? 3 * Q_BOX : 0) + (tile_group<ROLE>(T_K) == g ? 3 * Q_BOX : 0) +
-         (tile_group<ROLE>(T_V) == g ? 3 * V_BOX : 0) + (tile_group<ROLE>(T_G) == g ? 3 * V_BOX : 0);
+         (tile_group<ROLE>(T_V) == g ? 3 * V_BOX : 0) + (tile_group<ROLE>(T_G) == g ? 3 * V_BOX : 0) +
+         (SC && ROLE == R_DQ && g == 0 ? (uint32_t)kCopyBytes : 0u);  // the saved state copy
 }
 
-// Chunk handled at step t of the role's scan over chunks [c0, c0 + n).
-template <int ROLE>
+// Chunk handled at step t of the role's scan over chunks [c0, c0 + n): DQ scans forward when
+// it carries the state itself; with the forward's saved state copies it has no chain and runs
+// in reverse with DV and DK, so the three roles of a pair read each chunk at about the same
+// time and share its tiles through L2.
+template <int ROLE, bool SC>
 __device__ __forceinline__ int chunk_at(int t, int c0, int n) {
-  return ROLE == R_DQ ? c0 + t : c0 + n - 1 - t;
+  return ROLE == R_DQ && !SC ? c0 + t : c0 + n - 1 - t;
 }
 
 // 16-byte chunk `cc` of row `i` of a 16-bit tile: q/k tiles have 3 boxes of 32 channels
@@ -157,7 +162,7 @@ __device__ __forceinline__ float max16(const float* v) {
 
 // SAVED: the gate sigmoid(z) comes from p.gate (saved by the forward) instead of being
 // recomputed; a template parameter so that each variant gets its own register allocation.
-template <int ROLE, bool BF16, bool SAVED>
+template <int ROLE, bool BF16, bool SAVED, bool SC>
 __device__ __forceinline__ void run_role(
     uint8_t* base, const Cta& cta, int bh, int c0, int n, int cut_idx, const BwdParams& p,
     const CUtensorMap& map_q,
@@ -235,21 +240,23 @@ __device__ __forceinline__ void run_role(
               tma_load_4d(sb + OFF_G + j * V_BOX, &map_g, bar, 64 * j, h, t0, b);
           }
         }
+        if (SC && ROLE == R_DQ && g == 0 && !prefetch_only)  // the state copy S_c 2^-e_c
+          bulk_load(sb + OFF_CP, p.saved.copy + ((size_t)bh * nc + c) * kCopyBytes, kCopyBytes, bar);
       };
       int armed_e = 0, armed_l = 0;
       for (int t = 0; t < n; ++t) {
-        const int c = chunk_at<ROLE>(t, c0, n);
+        const int c = chunk_at<ROLE, SC>(t, c0, n);
         if (t >= 1 && !wait(cta, cta.bar(EMPTY_E), (t - 1) & 1, ctl)) break;
-        mbar_arrive_expect_tx(cta.bar(FULL_E), group_bytes<ROLE>(0));
+        mbar_arrive_expect_tx(cta.bar(FULL_E), group_bytes<ROLE, SC>(0));
         load(c, 0, false);
         ++armed_e;
         if (t >= 1 && !wait(cta, cta.bar(EMPTY_L), (t - 1) & 1, ctl)) break;
-        mbar_arrive_expect_tx(cta.bar(FULL_L), group_bytes<ROLE>(1));
+        mbar_arrive_expect_tx(cta.bar(FULL_L), group_bytes<ROLE, SC>(1));
         load(c, 1, false);
         ++armed_l;
         if (t + 1 < n) {
-          load(chunk_at<ROLE>(t + 1, c0, n), 0, true);
-          load(chunk_at<ROLE>(t + 1, c0, n), 1, true);
+          load(chunk_at<ROLE, SC>(t + 1, c0, n), 0, true);
+          load(chunk_at<ROLE, SC>(t + 1, c0, n), 1, true);
         }
       }
       if (armed_e) mbar_wait(cta.bar(FULL_E), (armed_e - 1) & 1, ctl, DRAIN_NS);
@@ -293,7 +300,7 @@ __device__ __forceinline__ void run_role(
         mma_commit(cta.bar(P_DONE));
         // ---- the MMAs that need no masked score, once the fp16 operands are in place
         if (!wait(cta, cta.bar(EP_C1), par, ctl)) break;
-        if (!wait(cta, cta.bar(EP_S), par, ctl)) break;
+        if (!(SC && ROLE == R_DQ) && !wait(cta, cta.bar(EP_S), par, ctl)) break;
         if (t >= 1 && !wait(cta, cta.bar(EP_X), (t - 1) & 1, ctl)) break;
         if (!wait(cta, cta.bar(FULL_L), par, ctl)) break;
         tc_fence_after();
@@ -325,8 +332,9 @@ __device__ __forceinline__ void run_role(
                        smem_desc(CP + (ks >> 2) * S_ATOM + (ks & 3) * 32, 16, 1024, SW_128), ID2,
                        ks > 0);
         }
-        // state / adjoint update, M = 128 (96 key channels + padding rows never read)
-        {
+        // state / adjoint update, M = 128 (96 key channels + padding rows never read); DQ
+        // with the forward's saved copies has no state to carry
+        if constexpr (!(SC && ROLE == R_DQ)) {
           constexpr uint32_t ID = idesc_f16(128, 192, false, false, true, true);
           const uint32_t A = sb + (ROLE == R_DQ ? OFF_K : OFF_Q);  // K^T (DQ) or Q''^T / Q^T
           const uint32_t B = sb + (ROLE == R_DQ ? OFF_V : OFF_G);  // V' (DQ) or dO / dO''
@@ -479,8 +487,8 @@ __device__ __forceinline__ void run_role(
       if (lane == 0) red[32 + warp] = m;
       mbar_arrive(cta.bar(RED));
     }
-    bool ok = wait_warp(cta, cta.bar(RED), 0, ctl);
-    if (ok) {
+    bool ok = SC && ROLE == R_DQ ? true : wait_warp(cta, cta.bar(RED), 0, ctl);
+    if (ok && !(SC && ROLE == R_DQ)) {
       e_cur = state_exponent(max16(red + 32));
       if (e_cur < 0) {
         bad = true;
@@ -507,12 +515,14 @@ __device__ __forceinline__ void run_role(
 
     for (int t = 0; t < n && ok; ++t) {
       const uint32_t par = t & 1;
-      const int c = chunk_at<ROLE>(t, c0, n);
+      const int c = chunk_at<ROLE, SC>(t, c0, n);
       const float lk = c == nc - 1 ? lk_last : lk_full;
       // the saved gate of this row (issued before the waits; rows past T, all zeros, have
       // sigmoid(0))
       float sg_saved = 0.5f;
       if (SAVED && c * C + i < T) sg_saved = __ldg(p.gate + (size_t)bh * T + c * C + i);
+      // DQ with the forward's saved copies: the exponent of this chunk's copy
+      if (SC && ROLE == R_DQ) e_cur = __ldg(p.saved.exp + (size_t)bh * nc + c);
       if (!(ok = wait_warp(cta, cta.bar(FULL_E), par, ctl))) break;
       if (!(ok = wait_warp(cta, cta.bar(FULL_L), par, ctl))) break;
       // ---- gate partial sum z = q.(a*k) over this part's 24 channels (unless the gate is
@@ -552,7 +562,7 @@ __device__ __forceinline__ void run_role(
       if (!(ok = wait_warp(cta, cta.bar(P_DONE), par, ctl))) break;
       tc_fence_after();
       if constexpr (ROLE == R_DQ) {
-        convert_row<BF16, 6, 3>(base + OFF_V, vg, lk, bmax);       // V' (state B)
+        if constexpr (!SC) convert_row<BF16, 6, 3>(base + OFF_V, vg, lk, bmax);  // V' (state B)
         convert_row<BF16, 6, 3>(base + OFF_G, vg, lq, range_max);  // dO'' (A of dO'' S^T)
       } else if constexpr (ROLE == R_DV) {
         convert_row<BF16, 3, 3>(base + OFF_Q, qk, lq, amax);       // Q'' (adjoint A)
@@ -588,9 +598,9 @@ __device__ __forceinline__ void run_role(
       // blocks hb = sub, sub+4 of the quadrant's rows, packed to fp16 pairs in registers.
       // Block hb's pairs go to 32-bit columns 8hb..8hb+7, inside block hb/2's fp32 columns, so
       // the four parts of a quadrant finish reading before any of them writes.
-      if (!(ok = wait_warp(cta, cta.bar(EP_S), par, ctl))) break;
+      if (!(SC && ROLE == R_DQ) && !(ok = wait_warp(cta, cta.bar(EP_S), par, ctl))) break;
       {
-        const float psc = pow2i(-es[par]);
+        const float psc = pow2i(-(SC && ROLE == R_DQ ? e_cur : es[par]));
         float pmax = 0.f;
         uint32_t pk[2][8];
 #pragma unroll
@@ -666,10 +676,10 @@ __device__ __forceinline__ void run_role(
       mbar_arrive(cta.bar(EMPTY_L));
       // ---- the state update ran: next state copy (the serial step), while the output MMA's
       // TMEM-operand part runs
-      if (!(ok = wait_warp(cta, cta.bar(S_DONE), par, ctl))) break;
-      tc_fence_after();
       int e_next = e_cur;
-      if (t < n - 1) {
+      if (!(SC && ROLE == R_DQ) && !(ok = wait_warp(cta, cta.bar(S_DONE), par, ctl))) break;
+      tc_fence_after();
+      if (!(SC && ROLE == R_DQ) && t < n - 1) {
         // bound on the next state: all parts' operand maxima and max|S| of this step's copy
         // (decayed by this step's factor)
         if (!(ok = wait_warp(cta, cta.bar(EP_CONV), par, ctl))) break;
@@ -766,7 +776,7 @@ __device__ __forceinline__ void run_role(
   }
 }
 
-template <bool BF16, bool SAVED>
+template <bool BF16, bool SAVED, bool SC>
 __global__ void __launch_bounds__(THREADS, 1)
 bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
            const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_g,
@@ -789,13 +799,13 @@ bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
   const int c0 = cut ? part_begin(part, nc, p.plan.parts) : 0;
   const int n = cut ? part_begin(part + 1, nc, p.plan.parts) - c0 : nc;
   if (role == R_DQ)
-    run_role<R_DQ, BF16, SAVED>(cta.base, cta, bh, c0, n, cut_idx, p, map_q, map_k, map_v, map_g, map_dq,
+    run_role<R_DQ, BF16, SAVED, SC>(cta.base, cta, bh, c0, n, cut_idx, p, map_q, map_k, map_v, map_g, map_dq,
                          map_dinit, ctl);
   else if (role == R_DV)
-    run_role<R_DV, BF16, SAVED>(cta.base, cta, bh, c0, n, cut_idx, p, map_q, map_k, map_v, map_g, map_dv,
+    run_role<R_DV, BF16, SAVED, false>(cta.base, cta, bh, c0, n, cut_idx, p, map_q, map_k, map_v, map_g, map_dv,
                          map_dinit, ctl);
   else
-    run_role<R_DK, BF16, SAVED>(cta.base, cta, bh, c0, n, cut_idx, p, map_q, map_k, map_v, map_g, map_dk,
+    run_role<R_DK, BF16, SAVED, false>(cta.base, cta, bh, c0, n, cut_idx, p, map_q, map_k, map_v, map_g, map_dk,
                          map_dinit, ctl);
 }
 
@@ -849,7 +859,8 @@ cudaError_t launch_chunk_bwd(const BwdArgs& a, DevCtl ctl, cudaStream_t stream) 
   p.H = a.H;
   p.want_dinit = a.dinit != nullptr;
   p.plan = a.plan;
-  if (p.plan.parts <= 1 || !a.seg_state || !a.seg_adj || !a.da_split) {
+  const bool sc = a.saved.copy != nullptr;  // DQ reads the forward's state copies
+  if (p.plan.parts <= 1 || (!a.seg_state && !sc) || !a.seg_adj || !a.da_split) {
     p.plan.whole = a.B * a.H;
     p.plan.parts = 1;
   }
@@ -857,8 +868,14 @@ cudaError_t launch_chunk_bwd(const BwdArgs& a, DevCtl ctl, cudaStream_t stream) 
   p.seg_adj = a.seg_adj;
   p.da_split = a.da_split;
   p.gate = a.gate;
-  auto kern = a.gate ? (a.bf16 ? bwd_kernel<true, true> : bwd_kernel<false, true>)
-                     : (a.bf16 ? bwd_kernel<true, false> : bwd_kernel<false, false>);
+  p.saved = a.saved;
+  using Kern = decltype(&bwd_kernel<true, true, true>);
+  const Kern kerns[2][2][2] = {
+      {{bwd_kernel<false, false, false>, bwd_kernel<false, false, true>},
+       {bwd_kernel<false, true, false>, bwd_kernel<false, true, true>}},
+      {{bwd_kernel<true, false, false>, bwd_kernel<true, false, true>},
+       {bwd_kernel<true, true, false>, bwd_kernel<true, true, true>}}};
+  const Kern kern = kerns[a.bf16 ? 1 : 0][a.gate ? 1 : 0][sc ? 1 : 0];
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const long long grid =

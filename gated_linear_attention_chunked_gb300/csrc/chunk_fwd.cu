@@ -115,7 +115,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
            float* __restrict__ fin, int T, int H, SplitPlan plan,
            const float* __restrict__ seg_init, StatePages sp,
            const __grid_constant__ CUtensorMap map_y, OutGate og, float* __restrict__ gate_out,
-           DevCtl ctl) {
+           SavedStates saved, DevCtl ctl) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   Cta cta;
   cta.base = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -251,6 +251,13 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
           mma_f16_ss(tmem + TM_O, smem_desc(st + OFF_Q + off, 16, 512, SW_64),
                      smem_desc(slot + ks * 2048, S_ATOM, 1024, SW_128), ID_QS, ks > 0);
         }
+        // the state copy this Q''S reads, saved for the backward: one bulk store from the
+        // slot, read out before the slot is released for the next chunk's q, k
+        if (saved.copy) {
+          bulk_store(saved.copy + ((size_t)bh * nc + c0 + c) * kCopyBytes, slot, kCopyBytes);
+          bulk_commit();
+          bulk_wait_read<0>();
+        }
         // the state copy has been read: the next chunk's q, k may load into that slot
         mma_commit(cta.bar(QK_EMPTY + (s ^ 1)));
         if (!wait(cta, cta.bar(EP_CONV), c & 1, ctl)) break;
@@ -271,6 +278,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
       }
       mma_commit(cta.bar(DRAIN));
       mbar_wait(cta.bar(DRAIN), 0, ctl, DRAIN_NS);
+      if (saved.copy) bulk_wait_all();  // the saved copies have reached global memory
     }
   } else if (warp < CONVERT_WARPS) {
     // ------------------------------------------------------------------ convert group
@@ -505,7 +513,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
       if (lane == 0) red[(use & 1) * 8 + ew] = m;
-      if (ew == 0 && lane == 0) es[use & 1] = e;
+      if (ew == 0 && lane == 0) {
+        es[use & 1] = e;
+        if (saved.exp) saved.exp[(size_t)bh * nc + c0 + use] = e;
+      }
       fence_proxy_async();
       tc_fence_before();
       mbar_arrive(cta.bar(EP_S));
@@ -747,7 +758,8 @@ cudaError_t launch_chunk_fwd(const FwdArgs& a, DevCtl ctl, cudaStream_t stream) 
   const unsigned threads = gated ? Layout<true>::THREADS : Layout<false>::THREADS;
   kern<<<(unsigned)grid, threads, SMEM_BYTES, stream>>>(mq, mk, mv, mo, mfin, a.log_decay, a.aug,
                                                         a.init, a.o, a.fin, a.T, a.H, plan,
-                                                        a.seg_init, a.sp, my, a.og, a.gate, ctl);
+                                                        a.seg_init, a.sp, my, a.og, a.gate,
+                                                        a.saved, ctl);
   return cudaGetLastError();
 }
 

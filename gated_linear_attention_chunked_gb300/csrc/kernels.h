@@ -61,6 +61,31 @@ __host__ __device__ inline int part_begin(int j, int nc, int parts) {
   return (int)(((long long)j * nc) / parts);
 }
 
+// A chunked forward's state copies, saved for the backward (an activation of the training
+// step, like the gate): per (b, h) pair and chunk c, the fp16 copy S_c 2^-e_c of the state
+// entering the chunk -- the B operand the forward's Q''S product reads -- as the tensor cores'
+// shared-memory image (three 64-column atoms of 96 key rows x 128 bytes, 128-byte swizzle), and
+// its exponent e_c.  With them the backward's DQ role needs no state scan of its own.
+constexpr int kCopyBytes = 36864;
+struct SavedStates {
+  uint8_t* copy = nullptr;  // [B*H][nc][kCopyBytes]
+  int* exp = nullptr;       // [B*H][nc]
+};
+// Bytes of the saved states of B*H pairs of T tokens: the copies, 256-aligned, then the
+// exponents.
+inline size_t saved_states_bytes(int B, int T, int H) {
+  const size_t n = (size_t)B * H * ((T + kChunk - 1) / kChunk);
+  return ((n * kCopyBytes + 255) & ~(size_t)255) + n * sizeof(int);
+}
+inline SavedStates saved_states_at(void* base, int B, int T, int H) {
+  SavedStates s;
+  if (!base) return s;
+  const size_t n = (size_t)B * H * ((T + kChunk - 1) / kChunk);
+  s.copy = static_cast<uint8_t*>(base);
+  s.exp = reinterpret_cast<int*>(s.copy + ((n * kCopyBytes + 255) & ~(size_t)255));
+  return s;
+}
+
 struct FwdArgs {
   const void* q;  // [B,T,H,96] 16-bit
   const void* k;
@@ -79,6 +104,7 @@ struct FwdArgs {
   StatePages sp;  // with sp.page: init and fin are the pool (see StatePages)
   OutGate og;     // with og.g: the fused output epilogue (o written only if og.want_o)
   float* gate = nullptr;  // [B,H,T] or null: sigmoid(z) per head and token, written
+  SavedStates saved;      // copy == null: not saved
 };
 // Returns cudaErrorInvalidValue if a tensor map cannot be encoded.
 cudaError_t launch_chunk_fwd(const FwdArgs& a, DevCtl ctl, cudaStream_t stream);
@@ -108,6 +134,8 @@ struct BwdArgs {
   float* da_split = nullptr;   // d_aug partial sums of the parts, [96] each
   const float* gate = nullptr;  // [B,H,T] or null: sigmoid(z) per head and token, read
                                 // instead of recomputing the gate
+  SavedStates saved;            // copy != null: the forward's state copies; the DQ role reads
+                                // them instead of scanning the state itself
 };
 size_t chunk_bwd_workspace_bytes(int B, int T, int H);
 

@@ -141,6 +141,12 @@ GLA_API gla_status gla_decay_schedule(int H, double t_min, double t_max, float* 
  *                self-augmentation gate, head-major so that a chunk's values are contiguous;
  *                4-byte aligned) -- an activation a training step saves for gla_chunk_bwd,
  *                which then need not recompute it
+ *   saved_states device buffer or NULL, 256-byte aligned, of saved_states_bytes >=
+ *                gla_chunk_saved_states_size(B, T, H) (GLA_ERR_WORKSPACE if smaller): written
+ *                with every chunk's fp16 state copy S_c 2^-e_c -- the operand the chunked form
+ *                multiplies the chunk's queries with ("Challenge 1") -- and e_c, 36,868 bytes per
+ *                chunk of each (b, h), an activation a training step saves for gla_chunk_bwd,
+ *                whose dq part then needs no state scan of its own
  *   workspace    device scratch, 256-byte aligned, of gla_chunk_fwd_workspace_size()
  *                bytes.  fp32 inputs need their fp16 copies there (GLA_ERR_WORKSPACE
  *                if it is smaller).  The size also covers cutting pairs into parts:
@@ -156,11 +162,13 @@ GLA_API gla_status gla_decay_schedule(int H, double t_min, double t_max, float* 
  * state is carried in fp32 across chunks.  Inputs must satisfy |x| < 65504.
  */
 GLA_API size_t gla_chunk_fwd_workspace_size(int B, int T, int H, int dk, int dv, gla_dtype in_dtype);
+GLA_API size_t gla_chunk_saved_states_size(int B, int T, int H);
 GLA_API gla_status gla_chunk_fwd(const void* q, const void* k, const void* v, gla_dtype in_dtype,
                          const float* log_decay, const float* aug_balance,
                          const float* init_state, float* o, float* final_state, float* gate,
-                         void* workspace, size_t workspace_bytes, int B, int T, int H, int dk,
-                         int dv, cudaStream_t stream);
+                         void* saved_states, size_t saved_states_bytes, void* workspace,
+                         size_t workspace_bytes, int B, int T, int H, int dk, int dv,
+                         cudaStream_t stream);
 
 /* gla_chunk_fwd_gated: the same forward with the mixer's output epilogue fused
  * into it ("GLA mixer": a Head RMSNorm shared within each decay tier, then the
@@ -199,6 +207,10 @@ GLA_API gla_status gla_chunk_fwd_gated(const void* q, const void* k, const void*
  *   gate          [B,H,T] fp32 or NULL: sigmoid(z_t) as gla_chunk_fwd writes it (4-byte
  *                 aligned); given, the backward reads it instead of recomputing z_t (the
  *                 results then follow the values given); NULL: recomputed
+ *   saved_states  NULL, or what gla_chunk_fwd wrote there for the same q, k, v, log_decay and
+ *                 init_state (size and alignment as there): the dq part reads the state copies
+ *                 instead of recomputing the state scan, and its chunks run in the same order
+ *                 as the other two parts'
  *   dq, dk        [B,T,H,96]  fp32 (written)    dv [B,T,H,192] fp32 (written)
  *   d_aug         [H,96] fp32 (written, summed over B and T)
  *   d_init_state  [B,H,96,192] fp32 or NULL (written)
@@ -213,8 +225,8 @@ GLA_API size_t gla_chunk_bwd_workspace_size(int B, int T, int H, int dk, int dv,
 GLA_API gla_status gla_chunk_bwd(const void* q, const void* k, const void* v, gla_dtype in_dtype,
                          const float* log_decay, const float* aug_balance,
                          const float* init_state, const void* dO, const float* d_final_state,
-                         const float* gate, float* dq, float* dk, float* dv, float* d_aug,
-                         float* d_init_state,
+                         const float* gate, const void* saved_states, size_t saved_states_bytes,
+                         float* dq, float* dk, float* dv, float* d_aug, float* d_init_state,
                          void* workspace, size_t workspace_bytes, int B, int T, int H,
                          int dk_, int dv_, cudaStream_t stream);
 

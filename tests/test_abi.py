@@ -68,8 +68,8 @@ A16 = 0x1000  # a 16-byte aligned fake address; never dereferenced by the checks
 
 def fwd(lib, q=A16, k=A16, v=A16, dt=0, ld=A16, a=A16, init=None, o=A16, fin=None, gate=None,
         ws=None, wsb=0, B=1, T=128, H=1, dk=96, dv=192):
-    return lib.gla_chunk_fwd(q, k, v, dt, ld, a, init, o, fin, gate, ws, wsb, B, T, H, dk, dv,
-                             None)
+    return lib.gla_chunk_fwd(q, k, v, dt, ld, a, init, o, fin, gate, None, 0, ws, wsb, B, T, H,
+                             dk, dv, None)
 
 
 def test_chunk_fwd_argument_checks(lib):
@@ -94,7 +94,8 @@ def test_chunk_fwd_argument_checks(lib):
 
 def test_chunk_bwd_argument_checks(lib):
     def bwd(dO=A16, dq=A16, dk_=64, T=128, d_aug=A16, gate=None):
-        return lib.gla_chunk_bwd(A16, A16, A16, 0, A16, A16, None, dO, None, gate, dq, A16, A16,
+        return lib.gla_chunk_bwd(A16, A16, A16, 0, A16, A16, None, dO, None, gate, None, 0, dq,
+                                 A16, A16,
                                  d_aug, None, None, 0, 1, T, 1, dk_, 192, None)
     assert bwd() == 2
     assert bwd(dk_=96, T=100, dq=A16 + 2) == 3         # any T: the sizes pass

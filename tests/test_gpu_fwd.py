@@ -155,7 +155,7 @@ def test_fwd_segmented_path(env, B, T, H, seed):
     f2 = torch.empty((B, H, 96, 192), dtype=torch.float32, device="cuda")
     rc = lib.gla_chunk_fwd(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), gla.GLA_BF16,
                            gam.data_ptr(), ad.data_ptr(), idd.data_ptr(), o2.data_ptr(),
-                           f2.data_ptr(), None, None, 0, B, T, H, 96, 192,
+                           f2.data_ptr(), None, None, 0, None, 0, B, T, H, 96, 192,
                            torch.cuda.current_stream().cuda_stream)
     assert rc == 0, gla.status_string(rc)
     torch.cuda.synchronize()
