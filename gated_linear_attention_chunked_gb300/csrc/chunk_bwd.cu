@@ -562,14 +562,16 @@ __device__ __forceinline__ void run_role(
       if (!(ok = wait_warp(cta, cta.bar(P_DONE), par, ctl))) break;
       tc_fence_after();
       if constexpr (ROLE == R_DQ) {
-        if constexpr (!SC) convert_row<BF16, 6, 3>(base + OFF_V, vg, lk, bmax);  // V' (state B)
-        convert_row<BF16, 6, 3>(base + OFF_G, vg, lq, range_max);  // dO'' (A of dO'' S^T)
+        if constexpr (!SC)  // V' (state B), dO'' (A of dO'' S^T)
+          convert_rows2<BF16, 6, 3>(base + OFF_V, vg, lk, bmax, base + OFF_G, vg, lq, range_max);
+        else
+          convert_row<BF16, 6, 3>(base + OFF_G, vg, lq, range_max);
       } else if constexpr (ROLE == R_DV) {
-        convert_row<BF16, 3, 3>(base + OFF_Q, qk, lq, amax);       // Q'' (adjoint A)
-        convert_row<BF16, 3, 3>(base + OFF_K, qk, lk, range_max);  // K' (A of K' dS)
+        // Q'' (adjoint A), K' (A of K' dS)
+        convert_rows2<BF16, 3, 3>(base + OFF_Q, qk, lq, amax, base + OFF_K, qk, lk, range_max);
       } else {
-        convert_row<BF16, 6, 3>(base + OFF_V, vg, lk, range_max);  // V' (A of V' dS^T)
-        convert_row<BF16, 6, 3>(base + OFF_G, vg, lq, bmax);       // dO'' (adjoint B)
+        // V' (A of V' dS^T), dO'' (adjoint B)
+        convert_rows2<BF16, 6, 3>(base + OFF_V, vg, lk, range_max, base + OFF_G, vg, lq, bmax);
       }
       // every fp16 operand but DQ's r q is in place: the state MMA and the output MMA's
       // state-copy part may run while the masked scores are made

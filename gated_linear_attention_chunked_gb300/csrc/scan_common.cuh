@@ -121,6 +121,42 @@ __device__ __forceinline__ void convert_row(uint8_t* tile, Off off, float s, flo
   }
 }
 
+// Two rows' conversions interleaved (tile a scaled by sa, tile b by sb), G chunks of each per
+// batch, so that 2G shared-memory loads are in flight together.
+template <bool SRC_BF16, int NCH, int G, typename OffA, typename OffB>
+__device__ __forceinline__ void convert_rows2(uint8_t* ta, OffA offa, float sa, float& ma,
+                                              uint8_t* tb, OffB offb, float sb, float& mb) {
+  static_assert(NCH % G == 0, "whole batches of chunks");
+#pragma unroll 1
+  for (int c0 = 0; c0 < NCH; c0 += G) {
+    uint4 x[G], y[G];
+#pragma unroll
+    for (int u = 0; u < G; ++u) {
+      x[u] = *(const uint4*)(ta + offa(c0 + u));
+      y[u] = *(const uint4*)(tb + offb(c0 + u));
+    }
+#pragma unroll
+    for (int u = 0; u < G; ++u) {
+      uint32_t* w = reinterpret_cast<uint32_t*>(&x[u]);
+      uint32_t* z = reinterpret_cast<uint32_t*>(&y[u]);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float a0 = ld16<SRC_BF16>(w[e] & 0xFFFFu) * sa, a1 = ld16<SRC_BF16>(w[e] >> 16) * sa;
+        const float b0 = ld16<SRC_BF16>(z[e] & 0xFFFFu) * sb, b1 = ld16<SRC_BF16>(z[e] >> 16) * sb;
+        ma = fmaxf(ma, fmaxf(fabsf(a0), fabsf(a1)));
+        mb = fmaxf(mb, fmaxf(fabsf(b0), fabsf(b1)));
+        w[e] = pack_h2(a0, a1);
+        z[e] = pack_h2(b0, b1);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < G; ++u) {
+      *(uint4*)(ta + offa(c0 + u)) = x[u];
+      *(uint4*)(tb + offb(c0 + u)) = y[u];
+    }
+  }
+}
+
 // Power-of-two exponent e >= 0 such that m * 2^-e < 2^14 (fp16 copy with headroom).
 // Returns -1 for a non-finite m.
 __device__ __forceinline__ int state_exponent(float m) {
