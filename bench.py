@@ -886,6 +886,25 @@ def run_long_prefill(args):
     bwd_ms = timed_b(nwb, 3)
     bwd_ser_ms = timed_b(nwb_min, 2)
     plan_b = gla.split_plan(Bl, Tl, H, True, torch.cuda.get_device_properties(dev).multi_processor_count)
+
+    # the same shape as a training step: the forward also saves its state copies (1.2 GB here)
+    # and the backward reads them, so its dq part needs no state scan
+    saved = torch.empty(gla.chunk_saved_states_size(Bl, Tl, H), dtype=torch.uint8, device=dev)
+    gla.chunk_fwd(q, k, v, gam, a, init, out=o, final_state=fin, gate=gl, saved_states=saved,
+                  workspace=ws)
+
+    def train_bwd():
+        gla.chunk_bwd(q, k, v, gam, a, dO, init, gate=gl, saved_states=saved, workspace=wsb)
+
+    train_bwd()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(3):
+        train_bwd()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    bwd_saved_ms = e0.elapsed_time(e1) / 3
     if gla.get_device_error() != 0:
         raise RuntimeError("device error")
     byts = Bl * Tl * H * FWD_BYTES_TH
@@ -895,7 +914,8 @@ def run_long_prefill(args):
                           gbs=byts / (seg_ms * 1e-3) / 1e9, frac_hbm=byts / (seg_ms * 1e-3) / 1e9 / pk["hbm"],
                           peak_source=pk["src"], workspace_bytes=nws, serial_ms=ser_ms,
                           plan_fwd=plan_f, bwd_ms=bwd_ms, bwd_serial_ms=bwd_ser_ms,
-                          bwd_tokens_per_s=Bl * Tl / (bwd_ms * 1e-3), plan_bwd=plan_b)), flush=True)
+                          bwd_tokens_per_s=Bl * Tl / (bwd_ms * 1e-3), plan_bwd=plan_b,
+                          bwd_saved_states_ms=bwd_saved_ms)), flush=True)
     return 0
 
 

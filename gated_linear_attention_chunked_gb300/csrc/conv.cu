@@ -67,6 +67,28 @@ __device__ __forceinline__ float& at(float4& v, int j) {
 // IEEE division and full-range expf were most of its instructions)
 __device__ __forceinline__ float sigm(float x) { return __fdividef(1.f, 1.f + __expf(-x)); }
 
+// Four channels' arithmetic as two packed fp32 pairs: each lane is the same IEEE operation
+// (round to nearest) as the scalar one, in half the instructions -- the conv is issue bound.
+__device__ __forceinline__ float2 lo2(float4 v) { return make_float2(v.x, v.y); }
+__device__ __forceinline__ float2 hi2(float4 v) { return make_float2(v.z, v.w); }
+__device__ __forceinline__ float4 cat4(float2 a, float2 b) { return make_float4(a.x, a.y, b.x, b.y); }
+__device__ __forceinline__ float4 fma4(float4 a, float4 b, float4 c) {  // a * b + c
+  return cat4(__ffma2_rn(lo2(a), lo2(b), lo2(c)), __ffma2_rn(hi2(a), hi2(b), hi2(c)));
+}
+__device__ __forceinline__ float4 mul4(float4 a, float4 b) {
+  return cat4(__fmul2_rn(lo2(a), lo2(b)), __fmul2_rn(hi2(a), hi2(b)));
+}
+__device__ __forceinline__ float4 add4(float4 a, float4 b) {
+  return cat4(__fadd2_rn(lo2(a), lo2(b)), __fadd2_rn(hi2(a), hi2(b)));
+}
+// dz = dy SiLU'(z) = dy s (1 + z (1 - s)), s = sigmoid(z), for four channels
+__device__ __forceinline__ float4 silu_grad4(float4 z, float4 dy) {
+  const float4 s = make_float4(sigm(z.x), sigm(z.y), sigm(z.z), sigm(z.w));
+  const float4 one = make_float4(1.f, 1.f, 1.f, 1.f), neg = make_float4(-1.f, -1.f, -1.f, -1.f);
+  const float4 one_minus_s = fma4(s, neg, one);
+  return mul4(mul4(dy, s), fma4(z, one_minus_s, one));
+}
+
 // x_t for token t of sequence b (t < 0: the initial state, row t + 3; zeros without one)
 template <bool BF16>
 __device__ __forceinline__ float4 x_at(const void* x, const float* init, int b, int t, int T,
@@ -100,9 +122,7 @@ __device__ __forceinline__ Filt load_filter(const float* w, const float* bias, i
 __device__ __forceinline__ float4 conv4(Filt& f, float4 (&win)[K]) {
   float4 z = f.b;
 #pragma unroll
-  for (int j = 0; j < K; ++j)
-#pragma unroll
-    for (int c = 0; c < 4; ++c) at(z, c) = fmaf(at(f.w[j], c), at(win[j], c), at(z, c));
+  for (int j = 0; j < K; ++j) z = fma4(f.w[j], win[j], z);
   return z;
 }
 
@@ -290,22 +310,12 @@ conv_bwd_kernel(const void* __restrict__ x, const float* __restrict__ w,
     }
     if (t < T) {
       win[3] = to_f4(rx[u]);
-      float4 z = conv4(f, win);
-      float4 g = rg[u];
-      float4 d;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const float zc = at(z, c), sg = sigm(zc);
-        at(d, c) = at(g, c) * sg * (1.f + zc * (1.f - sg));
-      }
+      const float4 d = silu_grad4(conv4(f, win), rg[u]);
       dz[3] = d;
       if (t < t1) {  // this tile's tokens: weight and bias gradients
+        gb = add4(gb, d);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          at(gb, c) += at(d, c);
-#pragma unroll
-          for (int j = 0; j < K; ++j) at(gw[j], c) = fmaf(at(d, c), at(win[j], c), at(gw[j], c));
-        }
+        for (int j = 0; j < K; ++j) gw[j] = fma4(d, win[j], gw[j]);
       }
     } else {
       win[3] = zero;
@@ -317,9 +327,7 @@ conv_bwd_kernel(const void* __restrict__ x, const float* __restrict__ w,
       if (s >= t1) continue;
       float4 g = zero;
 #pragma unroll
-      for (int j = 0; j < K; ++j)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) at(g, c) = fmaf(at(f.w[j], c), at(dz[3 - j], c), at(g, c));
+      for (int j = 0; j < K; ++j) g = fma4(f.w[j], dz[3 - j], g);
       if (s >= 0)
         reinterpret_cast<float4*>(dx)[((long long)b * T + s) * D4 + d4] = g;
       else if (dinit)
@@ -412,21 +420,12 @@ conv_bwd_staged_kernel(const void* __restrict__ x, const float* __restrict__ w,
     }
     if (in_seq) {
       win[3] = xv;
-      float4 z = conv4(f, win);
-      float4 d;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const float zc = at(z, c), sg = sigm(zc);
-        at(d, c) = at(g, c) * sg * (1.f + zc * (1.f - sg));
-      }
+      const float4 d = silu_grad4(conv4(f, win), g);
       dz[3] = d;
       if (t < t1) {
+        gb = add4(gb, d);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          at(gb, c) += at(d, c);
-#pragma unroll
-          for (int j = 0; j < K; ++j) at(gw[j], c) = fmaf(at(d, c), at(win[j], c), at(gw[j], c));
-        }
+        for (int j = 0; j < K; ++j) gw[j] = fma4(d, win[j], gw[j]);
       }
     } else {
       win[3] = zero;
@@ -436,9 +435,7 @@ conv_bwd_staged_kernel(const void* __restrict__ x, const float* __restrict__ w,
     if ((s >= t0 || (t0 == 0 && s >= -3)) && s < t1) {
       float4 o = zero;
 #pragma unroll
-      for (int j = 0; j < K; ++j)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) at(o, c) = fmaf(at(f.w[j], c), at(dz[3 - j], c), at(o, c));
+      for (int j = 0; j < K; ++j) o = fma4(f.w[j], dz[3 - j], o);
       if (s >= 0)
         reinterpret_cast<float4*>(dx)[((long long)b * T + s) * D4 + d4] = o;
       else if (dinit)
