@@ -407,7 +407,7 @@ def run_gpu(args, rank, world, local_rank):
     # passes of each chunked call whose plan cuts pairs into parts
     n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
     cut_f = gla.split_plan(B, T, H, False, n_sm)[1] > 1
-    cut_b = gla.split_plan(B, T, H, True, n_sm)[1] > 1
+    cut_b = gla.split_plan(B, T, H, 2 if args.saved_states else 1, n_sm)[1] > 1
     gpu_launches_per_step = 4 + 2 * int(cut_f) + 2 * int(cut_b)
 
     def roof(bound, achieved, peak, unit, traffic):
@@ -885,7 +885,8 @@ def run_long_prefill(args):
 
     bwd_ms = timed_b(nwb, 3)
     bwd_ser_ms = timed_b(nwb_min, 2)
-    plan_b = gla.split_plan(Bl, Tl, H, True, torch.cuda.get_device_properties(dev).multi_processor_count)
+    n_sm_l = torch.cuda.get_device_properties(dev).multi_processor_count
+    plan_b = gla.split_plan(Bl, Tl, H, 1, n_sm_l)
 
     # the same shape as a training step: the forward also saves its state copies (1.2 GB here)
     # and the backward reads them, so its dq part needs no state scan
@@ -915,7 +916,8 @@ def run_long_prefill(args):
                           peak_source=pk["src"], workspace_bytes=nws, serial_ms=ser_ms,
                           plan_fwd=plan_f, bwd_ms=bwd_ms, bwd_serial_ms=bwd_ser_ms,
                           bwd_tokens_per_s=Bl * Tl / (bwd_ms * 1e-3), plan_bwd=plan_b,
-                          bwd_saved_states_ms=bwd_saved_ms)), flush=True)
+                          bwd_saved_states_ms=bwd_saved_ms,
+                          plan_bwd_saved_states=gla.split_plan(Bl, Tl, H, 2, n_sm_l))), flush=True)
     return 0
 
 

@@ -549,11 +549,13 @@ def set_stall_step(step: int) -> None:
     _check("gla_set_stall_step", load().gla_set_stall_step(int(step)))
 
 
-def split_plan(B: int, T: int, H: int, backward: bool, n_sm: int) -> tuple[int, int]:
-    """(whole_pairs, parts) of gla_chunk_split_plan: pairs whole_pairs.. are cut into parts."""
+def split_plan(B: int, T: int, H: int, backward: int, n_sm: int) -> tuple[int, int]:
+    """(whole_pairs, parts) of gla_chunk_split_plan: pairs whole_pairs.. are cut into parts.
+    backward: 0 (False) the forward, 1 (True) the backward, 2 the backward reading the
+    forward's saved state copies."""
     w, p = ctypes.c_int(), ctypes.c_int()
     _check("gla_chunk_split_plan", load().gla_chunk_split_plan(
-        int(B), int(T), int(H), int(bool(backward)), int(n_sm), ctypes.byref(w), ctypes.byref(p)))
+        int(B), int(T), int(H), int(backward), int(n_sm), ctypes.byref(w), ctypes.byref(p)))
     return w.value, p.value
 
 

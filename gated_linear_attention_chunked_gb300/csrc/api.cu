@@ -2,6 +2,7 @@
 // error word, and the launches on the caller's stream.  No device memory is allocated here.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -72,10 +73,12 @@ size_t bwd_min_workspace(int B, int T, int H, gla_dtype in_dtype) {
   return s;
 }
 
-// How the last wave's pairs are cut on the current device (roles: 1 forward, 3 backward).
-gla::SplitPlan split_plan(int B, int T, int H, int roles, int n_sm) {
+// How the last wave's pairs are cut on the current device (roles: 1 forward, 3 backward;
+// pass_dirs: 1 for the forward and a backward reading the forward's state copies, 2 for a
+// backward that scans the state itself).
+gla::SplitPlan split_plan(int B, int T, int H, int roles, int n_sm, int pass_dirs) {
   const int nc = (T + gla::kChunk - 1) / gla::kChunk;
-  return gla::plan_split((long long)B * H, nc, roles, n_sm, g_split_parts.load());
+  return gla::plan_split((long long)B * H, nc, roles, n_sm, g_split_parts.load(), pass_dirs);
 }
 
 // Extra workspace of a plan: the forward's part states; the backward's part states, part
@@ -109,7 +112,7 @@ gla_status chunk_fwd_impl(const void* q, const void* k, const void* v, gla_dtype
   if (must && !aligned256(workspace)) return GLA_ERR_ALIGNMENT;
   // the pairs of a partial last wave (or all of few, long sequences) are cut into parts when
   // the workspace has room for their starting states
-  gla::SplitPlan plan = split_plan(B, T, H, 1, sm_count());
+  gla::SplitPlan plan = split_plan(B, T, H, 1, sm_count(), 1);
   const size_t extra = split_bytes(B, H, plan, false);
   if (extra && !(workspace && aligned256(workspace) && workspace_bytes >= round256(must) + extra)) {
     plan.whole = B * H;
@@ -232,7 +235,7 @@ gla_status gla_decay_schedule(int H, double t_min, double t_max, float* log_deca
 size_t gla_chunk_fwd_workspace_size(int B, int T, int H, int dk, int dv, gla_dtype in_dtype) {
   if (check_chunk_sizes(B, T, H, dk, dv, in_dtype) != GLA_OK) return 0;
   const size_t must = fwd_min_workspace(B, T, H, in_dtype);
-  const size_t extra = split_bytes(B, H, split_plan(B, T, H, 1, sm_count()), false);
+  const size_t extra = split_bytes(B, H, split_plan(B, T, H, 1, sm_count(), 1), false);
   return extra ? round256(must) + extra : must;
 }
 
@@ -299,7 +302,11 @@ gla_status gla_chunk_fwd_paged(const void* q, const void* k, const void* v, gla_
 size_t gla_chunk_bwd_workspace_size(int B, int T, int H, int dk, int dv, gla_dtype in_dtype) {
   if (check_chunk_sizes(B, T, H, dk, dv, in_dtype) != GLA_OK) return 0;
   const size_t must = bwd_min_workspace(B, T, H, in_dtype);
-  const size_t extra = split_bytes(B, H, split_plan(B, T, H, 3, sm_count()), true);
+  // enough for either backward: the one that scans the state itself and the one that reads
+  // the forward's state copies (whose cheaper segment passes may favour more parts)
+  const int n_sm = sm_count();
+  const size_t extra = std::max(split_bytes(B, H, split_plan(B, T, H, 3, n_sm, 2), true),
+                                split_bytes(B, H, split_plan(B, T, H, 3, n_sm, 1), true));
   return extra ? round256(must) + extra : must;
 }
 
@@ -314,7 +321,8 @@ gla_status gla_chunk_split_plan(int B, int T, int H, int backward, int n_sm, int
   if (B <= 0 || T <= 0 || H <= 0 || n_sm <= 0 || !whole_pairs || !parts)
     return GLA_ERR_INVALID_ARG;
   if ((long long)B * H > (1ll << 31) - 1) return GLA_ERR_UNSUPPORTED;
-  const gla::SplitPlan plan = split_plan(B, T, H, backward ? 3 : 1, n_sm);
+  const gla::SplitPlan plan =
+      split_plan(B, T, H, backward ? 3 : 1, n_sm, backward == 1 ? 2 : 1);
   *whole_pairs = plan.whole;
   *parts = plan.parts;
   return GLA_OK;
@@ -344,7 +352,7 @@ gla_status gla_chunk_bwd(const void* q, const void* k, const void* v, gla_dtype 
   if (need && !aligned256(workspace)) return GLA_ERR_ALIGNMENT;
   // the pairs of a partial last wave (or all of few, long sequences) are cut into parts when
   // the workspace has room for their starting states and adjoints
-  gla::SplitPlan plan = split_plan(B, T, H, 3, sm_count());
+  gla::SplitPlan plan = split_plan(B, T, H, 3, sm_count(), saved_states ? 1 : 2);
   const size_t extra = split_bytes(B, H, plan, true);
   if (extra && workspace_bytes < round256(need) + extra) {
     plan.whole = B * H;

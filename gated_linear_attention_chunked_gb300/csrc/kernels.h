@@ -144,7 +144,9 @@ size_t chunk_bwd_workspace_bytes(int B, int T, int H);
 // n_sm SMs: cut the pairs of the partial last wave (all pairs if they do not fill the SMs)
 // into the number of parts that minimises the estimated time, passes included.  force_parts:
 // 0 chooses, 1 never cuts, p >= 2 cuts the last wave's pairs into min(p, nc) parts.
-SplitPlan plan_split(long long BH, int nc, int roles, int n_sm, int force_parts);
+// pass_dirs: the directions the segment passes sum (the forward and a backward reading the
+// forward's state copies need one; a backward that scans the state itself, two).
+SplitPlan plan_split(long long BH, int nc, int roles, int n_sm, int force_parts, int pass_dirs);
 // States the cut pairs need (each 96 x 192 fp32): (BH - whole) * parts.
 long long split_slots(long long BH, const SplitPlan& p);
 // The segment passes: U sums over the parts (forward direction for the states entering parts

@@ -349,7 +349,7 @@ constexpr int kMaxParts = 32;
 constexpr int kMinPartChunks = 4;
 }  // namespace
 
-SplitPlan plan_split(long long BH, int nc, int roles, int n_sm, int force_parts) {
+SplitPlan plan_split(long long BH, int nc, int roles, int n_sm, int force_parts, int pass_dirs) {
   SplitPlan none;
   none.whole = (int)BH;
   none.parts = 1;
@@ -379,7 +379,7 @@ SplitPlan plan_split(long long BH, int nc, int roles, int n_sm, int force_parts)
     const double part_len = (double)((nc + p - 1) / p) + kCtaStart;
     const double main_t =
         list_finish((long long)roles * X * p, part_len, n_sm, n_hi, t_lo, t_lo + whole_len);
-    const long long pre_ctas = X * (p - 1) * (bwd ? 2 : 1);
+    const long long pre_ctas = X * (p - 1) * pass_dirs;
     const double pre_len = (double)((nc + p - 1) / p) * kPassChunk[bwd] + kPassStart;
     const double pre_t = (double)((pre_ctas + n_sm - 1) / n_sm) * pre_len + kPassLaunch;
     const double total = main_t + pre_t;

@@ -238,7 +238,10 @@ GLA_API gla_status gla_chunk_bwd(const void* q, const void* k, const void* v, gl
  * partial last wave, or all pairs when they do not fill one wave, into the number of parts
  * (at most 32 and nc) that minimises the estimate.  parts == 1: nothing is cut.  A host query
  * of the plan the calls use (with the current device's SM count); results do not depend on it
- * beyond rounding.  Errors: GLA_ERR_INVALID_ARG for sizes or n_sm <= 0 or NULL outputs. */
+ * beyond rounding.  backward: 0 the forward, 1 the backward, 2 the backward reading the
+ * forward's saved state copies (its segment passes sum one direction instead of two, so it
+ * may cut into more parts; gla_chunk_bwd_workspace_size covers both backward plans).
+ * Errors: GLA_ERR_INVALID_ARG for sizes or n_sm <= 0 or NULL outputs. */
 GLA_API gla_status gla_chunk_split_plan(int B, int T, int H, int backward, int n_sm,
                                         int* whole_pairs, int* parts);
 /* Overrides the choice of gla_chunk_split_plan for calls made after it returns (process-wide):

@@ -196,6 +196,10 @@ def test_split_plan_query(lib):
     assert w == 0 and 2 <= p <= 32
     w, p = plan(2, 131072, 16, 1)
     assert w == 0 and 2 <= p <= 32
+    # the backward reading the forward's state copies sums its segment passes in one direction
+    # only, so the cheaper passes let it cut the long pairs into more parts
+    w2, p2 = plan(2, 131072, 16, 2)
+    assert w2 == 0 and p <= p2 <= 32
     # forced: 1 never cuts, p >= 2 cuts the considered pairs into min(p, chunks) parts (the
     # pairs of the partial last wave: 56 of 512 forward, 6 of 512 backward)
     try:
@@ -225,7 +229,7 @@ def test_split_plan_invariants(lib):
             B, H = int(rng.integers(1, 65)), int(rng.integers(1, 33))
             T = int(rng.integers(1, 40000))
             n_sm = int(rng.choice([1, 7, 100, 132, 152, 160]))
-            bwd = int(rng.integers(0, 2))
+            bwd = int(rng.integers(0, 3))  # 2: the backward reading saved state copies
             force = int(rng.choice([0, 0, 0, 1, 2, 5, 40]))
             assert lib.gla_set_split_parts(force) == 0
             assert lib.gla_chunk_split_plan(B, T, H, bwd, n_sm, ctypes.byref(w), ctypes.byref(p)) == 0
