@@ -296,6 +296,8 @@ def run_gpu(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     gla.load()
+    gla.set_pass_overlap(args.pass_overlap)
+    gla.set_split_parts(args.split_parts)
     dist = None
     if world > 1:
         import torch.distributed as dist
@@ -812,6 +814,8 @@ def run_long_prefill(args):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     lib = gla.load()
+    gla.set_pass_overlap(args.pass_overlap)
+    gla.set_split_parts(args.split_parts)
     Bl, Tl = 2, args.long_t
     gen = torch.Generator(device=dev)
     gen.manual_seed(4321)
@@ -931,6 +935,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-saved-states", dest="saved_states", action="store_false",
                     help="the training step without the forward's saved state copies")
+    ap.add_argument("--no-pass-overlap", dest="pass_overlap", action="store_false",
+                    help="segment passes before the whole pairs on the caller's stream")
+    ap.add_argument("--split-parts", type=int, default=0,
+                    help="gla_set_split_parts: 0 automatic, 1 never cut, p >= 2 forced")
     ap.add_argument("--cpu-configs", action="store_true",
                     help="time the fp64 CPU oracle on every workload (no GPU work)")
     ap.add_argument("--cpu-seqs", type=int, default=32,

@@ -107,6 +107,8 @@ def load(path: str | None = None):
             lib.gla_chunk_split_plan.restype = _I
             lib.gla_set_split_parts.argtypes = [_I]
             lib.gla_set_split_parts.restype = _I
+            lib.gla_set_pass_overlap.argtypes = [_I]
+            lib.gla_set_pass_overlap.restype = _I
             lib.gla_set_stall_step.argtypes = [_I]
             lib.gla_set_stall_step.restype = _I
             lib.gla_chunk_state_sum.argtypes = [_P, _P, _I, _P, _P] + [_I] * 5 + [_P]
@@ -562,3 +564,9 @@ def split_plan(B: int, T: int, H: int, backward: int, n_sm: int) -> tuple[int, i
 def set_split_parts(parts: int) -> None:
     """gla_set_split_parts: 0 automatic, 1 never cut, p >= 2 cut into p parts."""
     _check("gla_set_split_parts", load().gla_set_split_parts(int(parts)))
+
+
+def set_pass_overlap(on: bool) -> None:
+    """gla_set_pass_overlap: segment passes beside the whole pairs (True, the default) or
+    before them on the caller's stream (False)."""
+    _check("gla_set_pass_overlap", load().gla_set_pass_overlap(1 if on else 0))

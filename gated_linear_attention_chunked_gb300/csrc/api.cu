@@ -16,6 +16,7 @@ __device__ int g_device_error = 0;
 std::atomic<unsigned long long> g_wait_ns{2000000000ull};
 std::atomic<int> g_split_parts{0};  // gla_set_split_parts: 0 automatic, 1 never, p >= 2 forced
 std::atomic<int> g_stall_step{-1};  // gla_set_stall_step: the give-up path's diagnostic
+std::atomic<int> g_pass_overlap{1};  // gla_set_pass_overlap: segment passes beside the whole pairs
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
@@ -78,7 +79,8 @@ size_t bwd_min_workspace(int B, int T, int H, gla_dtype in_dtype) {
 // backward that scans the state itself).
 gla::SplitPlan split_plan(int B, int T, int H, int roles, int n_sm, int pass_dirs) {
   const int nc = (T + gla::kChunk - 1) / gla::kChunk;
-  return gla::plan_split((long long)B * H, nc, roles, n_sm, g_split_parts.load(), pass_dirs);
+  return gla::plan_split((long long)B * H, nc, roles, n_sm, g_split_parts.load(), pass_dirs,
+                         g_pass_overlap.load() != 0);
 }
 
 // Extra workspace of a plan: the forward's part states; the backward's part states, part
@@ -117,6 +119,7 @@ gla_status chunk_fwd_impl(const void* q, const void* k, const void* v, gla_dtype
   if (extra && !(workspace && aligned256(workspace) && workspace_bytes >= round256(must) + extra)) {
     plan.whole = B * H;
     plan.parts = 1;
+    plan.overlap = false;
   }
   gla::DevCtl ctl;
   if ((st = ctl_for_current_device(&ctl)) != GLA_OK) return st;
@@ -140,6 +143,8 @@ gla_status chunk_fwd_impl(const void* q, const void* k, const void* v, gla_dtype
   }
   a.plan = plan;
   if (plan.parts > 1) {
+    // the segment passes; with plan.overlap the chunked kernel, launched as their programmatic
+    // dependent, runs its whole pairs beside them
     float* states = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + round256(must));
     a.seg_init = states;
     if (gla::launch_segment_states(nullptr, a.k, a.v, nullptr, a.bf16, log_decay, init_state,
@@ -316,6 +321,11 @@ gla_status gla_set_split_parts(int parts) {
   return GLA_OK;
 }
 
+gla_status gla_set_pass_overlap(int on) {
+  g_pass_overlap.store(on ? 1 : 0);
+  return GLA_OK;
+}
+
 gla_status gla_chunk_split_plan(int B, int T, int H, int backward, int n_sm, int* whole_pairs,
                                 int* parts) {
   if (B <= 0 || T <= 0 || H <= 0 || n_sm <= 0 || !whole_pairs || !parts)
@@ -357,6 +367,7 @@ gla_status gla_chunk_bwd(const void* q, const void* k, const void* v, gla_dtype 
   if (extra && workspace_bytes < round256(need) + extra) {
     plan.whole = B * H;
     plan.parts = 1;
+    plan.overlap = false;
   }
   gla::DevCtl ctl;
   if ((st = ctl_for_current_device(&ctl)) != GLA_OK) return st;
@@ -392,6 +403,7 @@ gla_status gla_chunk_bwd(const void* q, const void* k, const void* v, gla_dtype 
     // with the forward's saved state copies the DQ role needs no starting states: only the
     // adjoints (DV, DK) are summed and linked
     if (a.saved.copy) a.seg_state = nullptr;
+    // the segment passes (with plan.overlap beside the whole pairs: see the forward)
     if (gla::launch_segment_states(a.q, a.k, a.v, a.dO, a.bf16, log_decay, init_state,
                                    d_final_state, gla::StatePages{}, a.seg_state, a.seg_adj, B, T,
                                    H, plan, ctl, stream) != cudaSuccess)

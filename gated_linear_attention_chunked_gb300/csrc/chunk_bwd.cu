@@ -110,18 +110,21 @@ struct BwdParams {
 enum Tile : int { T_Q = 0, T_K = 1, T_V = 2, T_G = 3 };
 
 // Group of a tile for a role: 0 early, 1 late, -1 not loaded.  DQ: v, dO are last read by the
-// state update (K^T V') and the output MMA's state part (dO'' S^T); DK: k (gate only), v, dO;
-// DV: q, k.  The late tiles are read by the output MMA's TMEM-operand part or by the rows.
-template <int ROLE>
+// state update (K^T V') and the output MMA's state part (dO'' S^T); DK: k (gate only: not
+// loaded when the gate is given), v, dO; DV: q, k.  The late tiles are read by the output
+// MMA's TMEM-operand part or by the rows.
+template <int ROLE, bool SAVED>
 __device__ __forceinline__ constexpr int tile_group(int tile) {
   if (ROLE == R_DQ) return tile == T_V || tile == T_G ? 0 : 1;
-  if (ROLE == R_DK) return tile == T_Q ? 1 : 0;
+  if (ROLE == R_DK) return tile == T_Q ? 1 : (SAVED && tile == T_K ? -1 : 0);
   return tile == T_V ? -1 : (tile == T_G ? 1 : 0);
 }
-template <int ROLE, bool SC>
+template <int ROLE, bool SAVED, bool SC>
 __device__ __forceinline__ constexpr uint32_t group_bytes(int g) {
-  return (tile_group<ROLE>(T_Q) == g ? 3 * Q_BOX : 0) + (tile_group<ROLE>(T_K) == g ? 3 * Q_BOX : 0) +
-         (tile_group<ROLE>(T_V) == g ? 3 * V_BOX : 0) + (tile_group<ROLE>(T_G) == g ? 3 * V_BOX : 0) +
+  return (tile_group<ROLE, SAVED>(T_Q) == g ? 3 * Q_BOX : 0) +
+         (tile_group<ROLE, SAVED>(T_K) == g ? 3 * Q_BOX : 0) +
+         (tile_group<ROLE, SAVED>(T_V) == g ? 3 * V_BOX : 0) +
+         (tile_group<ROLE, SAVED>(T_G) == g ? 3 * V_BOX : 0) +
          (SC && ROLE == R_DQ && g == 0 ? (uint32_t)kCopyBytes : 0u);  // the saved state copy
 }
 
@@ -225,18 +228,18 @@ __device__ __forceinline__ void run_role(
         const uint32_t bar = cta.bar(g == 0 ? FULL_E : FULL_L);
         for (int j = 0; j < 3; ++j) {
           if (prefetch_only) {
-            if (tile_group<ROLE>(T_Q) == g) tma_prefetch_4d(&map_q, 32 * j, h, t0, b);
-            if (tile_group<ROLE>(T_K) == g) tma_prefetch_4d(&map_k, 32 * j, h, t0, b);
-            if (tile_group<ROLE>(T_V) == g) tma_prefetch_4d(&map_v, 64 * j, h, t0, b);
-            if (tile_group<ROLE>(T_G) == g) tma_prefetch_4d(&map_g, 64 * j, h, t0, b);
+            if (tile_group<ROLE, SAVED>(T_Q) == g) tma_prefetch_4d(&map_q, 32 * j, h, t0, b);
+            if (tile_group<ROLE, SAVED>(T_K) == g) tma_prefetch_4d(&map_k, 32 * j, h, t0, b);
+            if (tile_group<ROLE, SAVED>(T_V) == g) tma_prefetch_4d(&map_v, 64 * j, h, t0, b);
+            if (tile_group<ROLE, SAVED>(T_G) == g) tma_prefetch_4d(&map_g, 64 * j, h, t0, b);
           } else {
-            if (tile_group<ROLE>(T_Q) == g)
+            if (tile_group<ROLE, SAVED>(T_Q) == g)
               tma_load_4d(sb + OFF_Q + j * Q_BOX, &map_q, bar, 32 * j, h, t0, b);
-            if (tile_group<ROLE>(T_K) == g)
+            if (tile_group<ROLE, SAVED>(T_K) == g)
               tma_load_4d(sb + OFF_K + j * Q_BOX, &map_k, bar, 32 * j, h, t0, b);
-            if (tile_group<ROLE>(T_V) == g)
+            if (tile_group<ROLE, SAVED>(T_V) == g)
               tma_load_4d(sb + OFF_V + j * V_BOX, &map_v, bar, 64 * j, h, t0, b);
-            if (tile_group<ROLE>(T_G) == g)
+            if (tile_group<ROLE, SAVED>(T_G) == g)
               tma_load_4d(sb + OFF_G + j * V_BOX, &map_g, bar, 64 * j, h, t0, b);
           }
         }
@@ -247,11 +250,11 @@ __device__ __forceinline__ void run_role(
       for (int t = 0; t < n; ++t) {
         const int c = chunk_at<ROLE, SC>(t, c0, n);
         if (t >= 1 && !wait(cta, cta.bar(EMPTY_E), (t - 1) & 1, ctl)) break;
-        mbar_arrive_expect_tx(cta.bar(FULL_E), group_bytes<ROLE, SC>(0));
+        mbar_arrive_expect_tx(cta.bar(FULL_E), group_bytes<ROLE, SAVED, SC>(0));
         load(c, 0, false);
         ++armed_e;
         if (t >= 1 && !wait(cta, cta.bar(EMPTY_L), (t - 1) & 1, ctl)) break;
-        mbar_arrive_expect_tx(cta.bar(FULL_L), group_bytes<ROLE, SC>(1));
+        mbar_arrive_expect_tx(cta.bar(FULL_L), group_bytes<ROLE, SAVED, SC>(1));
         load(c, 1, false);
         ++armed_l;
         if (t + 1 < n) {
@@ -800,6 +803,9 @@ bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
   const int bh = cut ? p.plan.whole + cut_idx / p.plan.parts : w;
   const int c0 = cut ? part_begin(part, nc, p.plan.parts) : 0;
   const int n = cut ? part_begin(part + 1, nc, p.plan.parts) - c0 : nc;
+  // a part starts from the states the segment passes leave: when this grid is launched as
+  // their programmatic dependent it may be running before they finish (whole pairs need none)
+  if (cut) griddep_wait();
   if (role == R_DQ)
     run_role<R_DQ, BF16, SAVED, SC>(cta.base, cta, bh, c0, n, cut_idx, p, map_q, map_k, map_v, map_g, map_dq,
                          map_dinit, ctl);
@@ -865,6 +871,7 @@ cudaError_t launch_chunk_bwd(const BwdArgs& a, DevCtl ctl, cudaStream_t stream) 
   if (p.plan.parts <= 1 || (!a.seg_state && !sc) || !a.seg_adj || !a.da_split) {
     p.plan.whole = a.B * a.H;
     p.plan.parts = 1;
+    p.plan.overlap = false;
   }
   p.seg_state = a.seg_state;
   p.seg_adj = a.seg_adj;
@@ -882,8 +889,13 @@ cudaError_t launch_chunk_bwd(const BwdArgs& a, DevCtl ctl, cudaStream_t stream) 
   if (e != cudaSuccess) return e;
   const long long grid =
       3 * (p.plan.whole + ((long long)a.B * a.H - p.plan.whole) * p.plan.parts);
-  kern<<<(unsigned)grid, THREADS, SMEM_BYTES, stream>>>(mq, mk, mv, mg, mdq, mdk, mdv, mdi, p, ctl);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  {
+    // with plan.overlap: the segment passes' programmatic dependent (see the forward)
+    PdlLaunch L(dim3((unsigned)grid), dim3(THREADS), SMEM_BYTES, stream, p.plan.overlap);
+    if ((e = cudaLaunchKernelEx(&L.cfg, kern, mq, mk, mv, mg, mdq, mdk, mdv, mdi, p, ctl)) !=
+        cudaSuccess)
+      return e;
+  }
   const int n = a.H * DK;
   reduce_daug_kernel<<<(n + 255) / 256, 256, 0, stream>>>(p.da_part, p.da_split, a.d_aug, a.B, a.H,
                                                          p.plan);

@@ -140,6 +140,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
   const int bh = cut ? plan.whole + cut_idx / plan.parts : (int)blockIdx.x, b = bh / H, h = bh % H;
   const int c0 = cut ? part_begin(part, nc, plan.parts) : 0;
   const int n = cut ? part_begin(part + 1, nc, plan.parts) - c0 : nc;
+  // a part starts from the state the segment passes leave: when this grid is launched as their
+  // programmatic dependent it may be running before they finish (whole pairs need nothing)
+  if (cut) griddep_wait();
   const float gamma = __ldg(log_decay + h);
   float* pw = (float*)(base + OFF_PW);
   float* red = (float*)(base + OFF_RED);
@@ -753,14 +756,16 @@ cudaError_t launch_chunk_fwd(const FwdArgs& a, DevCtl ctl, cudaStream_t stream) 
   if (plan.parts <= 1 || !a.seg_init) {
     plan.whole = a.B * a.H;
     plan.parts = 1;
+    plan.overlap = false;
   }
   const long long grid = plan.whole + ((long long)a.B * a.H - plan.whole) * plan.parts;
   const unsigned threads = gated ? Layout<true>::THREADS : Layout<false>::THREADS;
-  kern<<<(unsigned)grid, threads, SMEM_BYTES, stream>>>(mq, mk, mv, mo, mfin, a.log_decay, a.aug,
-                                                        a.init, a.o, a.fin, a.T, a.H, plan,
-                                                        a.seg_init, a.sp, my, a.og, a.gate,
-                                                        a.saved, ctl);
-  return cudaGetLastError();
+  // with plan.overlap the kernel is the segment passes' programmatic dependent: its whole pairs
+  // start beside the passes, its parts wait for them (griddep_wait)
+  PdlLaunch L(dim3((unsigned)grid), dim3(threads), SMEM_BYTES, stream, plan.overlap);
+  return cudaLaunchKernelEx(&L.cfg, kern, mq, mk, mv, mo, mfin, a.log_decay, a.aug, a.init, a.o,
+                            a.fin, a.T, a.H, plan, a.seg_init, a.sp, my, a.og, a.gate, a.saved,
+                            ctl);
 }
 
 }  // namespace gla

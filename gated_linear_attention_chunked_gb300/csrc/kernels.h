@@ -53,9 +53,32 @@ struct OutGate {
 // part j covering chunks [j*nc/parts, (j+1)*nc/parts), each its own CTA that starts from the
 // state (forward) or adjoint (reverse) at its boundary, computed beforehand by the segment
 // passes (seg_scan.cu).  parts == 1: no pair is cut.
+// Launch configuration of a kernel that may be a programmatic dependent of the grid ahead of
+// it on the stream (pdl): it may then start while that grid finishes, and reads what that grid
+// writes only after griddep_wait.  Used in place (cfg points at attr).
+struct PdlLaunch {
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute attr[1];
+  PdlLaunch(dim3 grid, dim3 block, size_t smem, cudaStream_t stream, bool pdl) {
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+  }
+  PdlLaunch(const PdlLaunch&) = delete;
+};
+
 struct SplitPlan {
   int whole = 0;
   int parts = 1;
+  // the segment passes overlap the whole pairs: each pass and then the chunked kernel is
+  // launched as a programmatic dependent of the launch before it, so the chunked kernel's whole
+  // pairs start beside the passes and only its parts wait for them (griddep_wait)
+  bool overlap = false;
 };
 __host__ __device__ inline int part_begin(int j, int nc, int parts) {
   return (int)(((long long)j * nc) / parts);
@@ -145,15 +168,20 @@ size_t chunk_bwd_workspace_bytes(int B, int T, int H);
 // into the number of parts that minimises the estimated time, passes included.  force_parts:
 // 0 chooses, 1 never cuts, p >= 2 cuts the last wave's pairs into min(p, nc) parts.
 // pass_dirs: the directions the segment passes sum (the forward and a backward reading the
-// forward's state copies need one; a backward that scans the state itself, two).
-SplitPlan plan_split(long long BH, int nc, int roles, int n_sm, int force_parts, int pass_dirs);
+// forward's state copies need one; a backward that scans the state itself, two).  overlap:
+// the passes may run beside the whole pairs' CTAs (programmatic dependent launches, see
+// SplitPlan::overlap) instead of before them; the plan then says whether they do.
+SplitPlan plan_split(long long BH, int nc, int roles, int n_sm, int force_parts, int pass_dirs,
+                     bool overlap);
 // States the cut pairs need (each 96 x 192 fp32): (BH - whole) * parts.
 long long split_slots(long long BH, const SplitPlan& p);
 // The segment passes: U sums over the parts (forward direction for the states entering parts
 // 1.., reverse direction for the adjoints leaving parts ..p-2), then their recurrences, which
 // also place the initial state (init / pool page / zero) and the final-state adjoint (dfin /
 // zero) in the first and last slots.  states (adj) null: that direction is not computed.
-// q_or_null, dO_or_null are needed for the reverse direction only.
+// q_or_null, dO_or_null are needed for the reverse direction only.  With plan.overlap pass B
+// is pass A's programmatic dependent and runs on at most 16 CTAs (which wait beside pass A's),
+// so that the chunked kernel launched next as its dependent can start its whole pairs at once.
 cudaError_t launch_segment_states(const void* q, const void* k, const void* v, const void* dO,
                                   bool bf16, const float* log_decay, const float* init,
                                   const float* dfin, const StatePages& sp, float* states,

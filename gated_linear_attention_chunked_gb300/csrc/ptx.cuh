@@ -151,6 +151,16 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
 }
 
 // ---------------------------------------------------------------------------------------
+// Programmatic dependent launch: a grid launched with programmatic stream serialization may
+// start before the grid ahead of it on the stream has finished, once every CTA of that grid
+// has signalled (or exited); griddepcontrol.wait then blocks until the grid ahead has
+// completed and its memory operations are visible.  Both are no-ops for a plain launch.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------------------
 // tcgen05: tensor memory
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),

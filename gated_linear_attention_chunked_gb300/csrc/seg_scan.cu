@@ -83,6 +83,8 @@ seg_sum_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant_
                const float* __restrict__ log_decay, float* __restrict__ states,
                float* __restrict__ adj, int T, int H, int whole, int parts, int n_fwd, int full,
                DevCtl ctl) {
+  // pass B may start (it waits for these sums), and with it the chunked kernel's whole pairs
+  griddep_launch_dependents();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   Cta cta;
   cta.base = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -239,17 +241,22 @@ seg_sum_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant_
 // blockIdx.z = 1: adj[x*p + j] (j <= p-2) holds U'_{j+1} on entry and the adjoint leaving
 // part j on exit; slot x*p + p-1 receives d_final_state (or zeros).  One thread per 4
 // consecutive state elements, walking the parts in order.
-__global__ void seg_link_kernel(const float* __restrict__ init, const float* __restrict__ dfin,
-                                const float* __restrict__ log_decay, float* __restrict__ states,
-                                float* __restrict__ adj, int T, int H, int whole, int parts,
-                                StatePages sp) {
+constexpr int LINK_THREADS = 1024;
+// Pass B's CTAs when it overlaps the chunked kernel: few enough to wait beside pass A's
+constexpr int LINK_CTAS_OVERLAP = 16;
+
+// One item of pass B: elements 4e .. 4e+3 of cut pair x's starting states (rev = 0) or
+// adjoints (rev = 1), walking the pair's parts in order.
+__device__ __forceinline__ void link_one(const float* __restrict__ init,
+                                         const float* __restrict__ dfin,
+                                         const float* __restrict__ log_decay,
+                                         float* __restrict__ states, float* __restrict__ adj,
+                                         int T, int H, int whole, int parts, const StatePages& sp,
+                                         int rev, int x, int e) {
   constexpr int N4 = DK * DV / 4;
-  const bool rev = blockIdx.z == 1;
   float* const slots = rev ? adj : states;
   if (!slots) return;
-  const int x = blockIdx.y, bh = whole + x, b = bh / H, h = bh % H;
-  const int e = blockIdx.x * blockDim.x + threadIdx.x;
-  if (e >= N4) return;
+  const int bh = whole + x, b = bh / H, h = bh % H;
   const float gamma = __ldg(log_decay + h);
   const int nc = (T + C - 1) / C;
   auto tokens = [&](int j) {  // tokens of part j
@@ -283,6 +290,24 @@ __global__ void seg_link_kernel(const float* __restrict__ init, const float* __r
       out[(size_t)j * N4] = s;
     }
   }
+}
+
+// Pass B: every (direction, cut pair, 4 state elements) item, grid-stride.
+__global__ void __launch_bounds__(LINK_THREADS)
+seg_link_kernel(const float* __restrict__ init, const float* __restrict__ dfin,
+                const float* __restrict__ log_decay, float* __restrict__ states,
+                float* __restrict__ adj, int T, int H, int whole, int parts, StatePages sp,
+                int X) {
+  // a chunked kernel launched as this grid's dependent may start its whole pairs; the sums are
+  // read once pass A is complete
+  griddep_launch_dependents();
+  griddep_wait();
+  constexpr int N4 = DK * DV / 4;
+  const long long per_dir = (long long)X * N4;
+  for (long long it = (long long)blockIdx.x * LINK_THREADS + threadIdx.x; it < 2 * per_dir;
+       it += (long long)gridDim.x * LINK_THREADS)
+    link_one(init, dfin, log_decay, states, adj, T, H, whole, parts, sp, (int)(it / per_dir),
+             (int)(it % per_dir / N4), (int)(it % N4));
 }
 
 // The state entering slice `rank` of a sequence cut into consecutive slices across ranks
@@ -349,7 +374,8 @@ constexpr int kMaxParts = 32;
 constexpr int kMinPartChunks = 4;
 }  // namespace
 
-SplitPlan plan_split(long long BH, int nc, int roles, int n_sm, int force_parts, int pass_dirs) {
+SplitPlan plan_split(long long BH, int nc, int roles, int n_sm, int force_parts, int pass_dirs,
+                     bool overlap) {
   SplitPlan none;
   none.whole = (int)BH;
   none.parts = 1;
@@ -381,7 +407,14 @@ SplitPlan plan_split(long long BH, int nc, int roles, int n_sm, int force_parts,
         list_finish((long long)roles * X * p, part_len, n_sm, n_hi, t_lo, t_lo + whole_len);
     const long long pre_ctas = X * (p - 1) * pass_dirs;
     const double pre_len = (double)((nc + p - 1) / p) * kPassChunk[bwd] + kPassStart;
-    const double pre_t = (double)((pre_ctas + n_sm - 1) / n_sm) * pre_len + kPassLaunch;
+    const double pre_serial = (double)((pre_ctas + n_sm - 1) / n_sm) * pre_len + kPassLaunch;
+    double pre_t = pre_serial;
+    if (overlap && W >= n_sm) {
+      // beside at least a wave of whole CTAs the passes take only their share of the SMs'
+      // time (their CTAs start first, the whole CTAs on the other SMs); the parts wait for
+      // them only if they end after the whole CTAs
+      pre_t = (double)pre_ctas * pre_len / n_sm + (pre_serial > t_lo ? pre_serial - t_lo : 0.0);
+    }
     const double total = main_t + pre_t;
     if (force_parts >= 2 || total < best) {
       best = total;
@@ -392,6 +425,7 @@ SplitPlan plan_split(long long BH, int nc, int roles, int n_sm, int force_parts,
   SplitPlan plan;
   plan.whole = (int)(BH - X);
   plan.parts = best_p;
+  plan.overlap = overlap && W >= n_sm;
   return plan;
 }
 
@@ -428,9 +462,12 @@ cudaError_t launch_segment_states(const void* q, const void* k, const void* v, c
         mk, mv, mq, mg, log_decay, states, adj, T, H, plan.whole, plan.parts, (int)n_fwd, 0, ctl);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  seg_link_kernel<<<dim3((DK * DV / 4 + 255) / 256, (unsigned)X, 2), 256, 0, stream>>>(
-      init, dfin, log_decay, states, adj, T, H, plan.whole, plan.parts, sp);
-  return cudaGetLastError();
+  const long long items = 2LL * X * (DK * DV / 4);
+  long long ctas = (items + LINK_THREADS - 1) / LINK_THREADS;
+  if (plan.overlap && ctas > LINK_CTAS_OVERLAP) ctas = LINK_CTAS_OVERLAP;
+  PdlLaunch L(dim3((unsigned)ctas), dim3(LINK_THREADS), 0, stream, plan.overlap);
+  return cudaLaunchKernelEx(&L.cfg, seg_link_kernel, init, dfin, log_decay, states, adj, T, H,
+                            plan.whole, plan.parts, sp, (int)X);
 }
 
 cudaError_t launch_slice_sums(const void* a, const void* b, bool bf16, bool reverse,

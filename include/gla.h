@@ -248,6 +248,16 @@ GLA_API gla_status gla_chunk_split_plan(int B, int T, int H, int backward, int n
  * 0 = automatic (default), 1 = never cut, p >= 2 = cut the pairs it would consider into
  * min(p, nc) parts.  GLA_ERR_INVALID_ARG for p < 0. */
 GLA_API gla_status gla_set_split_parts(int parts);
+/* How a call that cuts pairs into parts orders its launches (process-wide; a scheduling choice
+ * for the GPU, no counterpart in the article).  on != 0 (the default): when the whole pairs
+ * fill at least one wave of SMs, the segment passes and the chunked kernel are chained as
+ * programmatic dependent launches on the caller's stream -- the chunked kernel starts its
+ * whole pairs' CTAs beside the passes, and each part's CTA waits (griddepcontrol.wait) for the
+ * passes before it reads the state they leave; everything stays on the caller's stream, which
+ * sees the call's results complete as before.  on == 0: the passes, then the chunked kernel,
+ * each after the previous launch has finished.  The results are the same either way; the plan
+ * (gla_chunk_split_plan) counts the passes as overlapped when on != 0.  Returns GLA_OK. */
+GLA_API gla_status gla_set_pass_overlap(int on);
 
 /* ---------------------------------------------------------------------------
  * A long sequence cut into consecutive slices, one per rank (GPU), for long-context
