@@ -168,3 +168,45 @@ def test_cut_pairs_paged_and_gated(env):
     touched = np.zeros((P, PL), bool)
     touched[page, layer] = True
     assert np.array_equal(new[~touched], pool[~touched])
+
+
+def test_pass_overlap_matches_serial_order(env):
+    """With a full wave of whole pairs the segment passes run beside them (the chunked kernel a
+    programmatic dependent of the passes, its parts waiting for them); with
+    gla_set_pass_overlap(0) the passes run first.  The kernels and their arithmetic are the
+    same, so every output is bit-identical between the two orders -- plain and training path
+    (saved gate and state copies)."""
+    gla, torch = env
+    B, T, H, seed = 10, 256, 16, 68
+    if n_sm(torch) != 152:
+        pytest.skip("the layout of this case assumes 152 SMs")
+    q, k, v, dO, a, init, dfin = _inputs(seed, B, T, H, "bf16")
+    gam = oracle_decays(H)[0].cuda()
+    qd, kd, vd, gd = (to_dev(x, torch.bfloat16) for x in (q, k, v, dO))
+    ad, idd, fd = (to_dev(x, torch.float32) for x in (a, init, dfin))
+
+    def run(overlap):
+        gla.set_pass_overlap(overlap)
+        gla.set_split_parts(2)
+        try:
+            out = []
+            o, fin = gla.chunk_fwd(qd, kd, vd, gam, ad, idd)
+            out += [o, fin, *gla.chunk_bwd(qd, kd, vd, gam, ad, gd, idd, fd)]
+            gate = torch.empty(B, H, T, device="cuda")
+            saved = torch.empty(gla.chunk_saved_states_size(B, T, H), dtype=torch.uint8,
+                                device="cuda")
+            o2, fin2 = gla.chunk_fwd(qd, kd, vd, gam, ad, idd, gate=gate, saved_states=saved)
+            out += [o2, fin2, gate,
+                    *gla.chunk_bwd(qd, kd, vd, gam, ad, gd, idd, fd, gate=gate,
+                                   saved_states=saved)]
+            torch.cuda.synchronize()
+            assert gla.get_device_error() == 0
+            return [x.cpu().numpy() for x in out]
+        finally:
+            gla.set_split_parts(0)
+            gla.set_pass_overlap(True)
+
+    on, off = run(True), run(False)
+    names = ["o", "final", *NAMES, "o_saved", "final_saved", "gate", *(n + "_saved" for n in NAMES)]
+    diff = [n for n, x, y in zip(names, on, off) if not np.array_equal(x, y)]
+    assert not diff, f"outputs differ between the launch orders: {diff}"
