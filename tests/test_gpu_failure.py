@@ -48,14 +48,18 @@ def test_wait_gives_up_and_reports_timeout():
 
 
 @pytest.mark.parametrize("case,step", [("fwd", 0), ("fwd", 2), ("bwd", 0), ("bwd", 3),
-                                       ("cut_fwd", 1), ("cut_bwd", 1)])
+                                       ("cut_fwd", 1), ("cut_bwd", 1),
+                                       ("overlap_fwd", 0), ("overlap_bwd", 0)])
 def test_chunk_kernel_waits_give_up_and_the_next_call_is_correct(case, step):
     """The chunk kernels' own waits run out: with gla_set_stall_step the tensor-core issuer of
     every CTA waits, at chunk step `step`, on a barrier that completes only after its loop, so
     its bounded wait (2 ms here) gives up and raises the CTA's abort flag.  Every role then
     leaves its loop on one path per warp (the epilogue warps vote), drains its copies and
     MMAs and frees its tensor memory.  The host reads GLA_ERR_TIMEOUT; with the diagnostic off
-    the next forward and backward are correct."""
+    the next forward and backward are correct.  The cut_* cases cut every pair (the segment
+    passes run first); the overlap_* cases have a full wave of whole pairs and 8 cut ones, so
+    the passes and the chunked kernel are chained as programmatic dependent launches: the
+    passes' own waits give up, they complete, and the parts' griddepcontrol.wait returns."""
     import torch
     assert torch.cuda.is_available(), "GPU test without a CUDA device"
     import gated_linear_attention_chunked_gb300 as gla
@@ -65,6 +69,10 @@ def test_chunk_kernel_waits_give_up_and_the_next_call_is_correct(case, step):
     import oracle
     B, H = 1, 2
     T = 4000 if case.startswith("cut") else 640  # 4000: the pairs are cut into parts
+    if case.startswith("overlap"):
+        if torch.cuda.get_device_properties(0).multi_processor_count != 152:
+            pytest.skip("the layout of this case assumes 152 SMs")
+        B, H, T = 10, 16, 256  # 160 pairs: 152 whole, the last 8 cut in 2 (forced)
     q, k, v = synth.qkv(95, B, T, H)
     dO = synth.grad_out(95, B, T, H)
     a = synth.aug_balance(95, (H, 96), 0.1)
@@ -73,6 +81,9 @@ def test_chunk_kernel_waits_give_up_and_the_next_call_is_correct(case, step):
     ad = to_dev(a, torch.float32)
     assert gla.get_device_error() == 0
     try:
+        if case.startswith("overlap"):
+            gla.set_split_parts(2)
+            assert gla.split_plan(B, T, H, case.endswith("bwd"), 152) == (152, 2)
         gla.set_wait_timeout_ns(2_000_000)
         gla.set_stall_step(step)
         t0 = time.perf_counter()
@@ -87,6 +98,7 @@ def test_chunk_kernel_waits_give_up_and_the_next_call_is_correct(case, step):
     finally:
         gla.set_stall_step(-1)
         gla.set_wait_timeout_ns(0)
+        gla.set_split_parts(0)
     o, fin = gla.chunk_fwd(qd, kd, vd, gam.cuda(), ad)
     g = gla.chunk_bwd(qd, kd, vd, gam.cuda(), ad, gd)
     torch.cuda.synchronize()
