@@ -438,22 +438,28 @@ __device__ __forceinline__ void run_role(
             r[4 * j4 + 3] = __float_as_uint(x.w);
           }
         }
+        const float2 sc2 = make_float2(sc, sc), dec2 = make_float2(dec, dec);
 #pragma unroll
         for (int q8 = 0; q8 < 6; ++q8) {
           const int nn = col + 8 * q8;
-          const float* f = reinterpret_cast<const float*>(r + 8 * q8);
-          uint4 pk;
-          pk.x = pack_h2(f[0] * sc, f[1] * sc);
-          pk.y = pack_h2(f[2] * sc, f[3] * sc);
-          pk.z = pack_h2(f[4] * sc, f[5] * sc);
-          pk.w = pack_h2(f[6] * sc, f[7] * sc);
-          *(uint4*)(base + OFF_CP + (nn >> 6) * S_ATOM + swz_off(i, (nn & 63) >> 3, 128)) = pk;
+          uint32_t w[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const float2 x = make_float2(__uint_as_float(r[8 * q8 + 2 * u]),
+                                         __uint_as_float(r[8 * q8 + 2 * u + 1]));
+            const float2 y = __fmul2_rn(x, sc2);
+            w[u] = pack_h2(y.x, y.y);
+          }
+          *(uint4*)(base + OFF_CP + (nn >> 6) * S_ATOM + swz_off(i, (nn & 63) >> 3, 128)) =
+              make_uint4(w[0], w[1], w[2], w[3]);
         }
 #pragma unroll
-        for (int j = 0; j < 48; ++j) {
-          const float x = __uint_as_float(r[j]);
-          m = fmaxf(m, fabsf(x));
-          r[j] = __float_as_uint(x * dec);
+        for (int j = 0; j < 48; j += 2) {
+          const float2 x = make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1]));
+          m = fmaxf(m, fmaxf(fabsf(x.x), fabsf(x.y)));
+          const float2 y = __fmul2_rn(x, dec2);
+          r[j] = __float_as_uint(y.x);
+          r[j + 1] = __float_as_uint(y.y);
         }
         tmem_st32(trow + TM_S + col, *reinterpret_cast<uint32_t(*)[32]>(r));
         tmem_st16(trow + TM_S + col + 32, *reinterpret_cast<uint32_t(*)[16]>(r + 32));
@@ -614,8 +620,30 @@ __device__ __forceinline__ void run_role(
           const int cb = 16 * hb;
           // DQ keeps columns j <= i (rows = queries i), DV and DK columns i >= j (rows = keys j)
           const bool live = ROLE == R_DQ ? hb <= 2 * q4 + 1 : hb >= 2 * q4;
+          // every element of the block is kept for all 32 rows of the quadrant (all but the two
+          // blocks on the diagonal): no per-element mask, no diagonal (warp-uniform)
+          const bool full = ROLE == R_DQ ? hb <= 2 * q4 - 1 : hb >= 2 * q4 + 2;
           float sc[16];
-          if (live) {
+          if (full) {
+            uint32_t r[16];
+            tmem_ld16(trow + TM_P + cb, r);
+            tmem_wait_ld();
+            if constexpr (ROLE == R_DQ) {
+              float f = pw[i - (cb + 15)] * psc;  // going left from cb+15
+#pragma unroll
+              for (int u = 15; u >= 0; --u) {
+                sc[u] = __uint_as_float(r[u]) * f;
+                f = f * lam;
+              }
+            } else {
+              float f = pw[cb - i] * psc;  // going right from cb
+#pragma unroll
+              for (int u = 0; u < 16; ++u) {
+                sc[u] = __uint_as_float(r[u]) * f;
+                f = f * lam;
+              }
+            }
+          } else if (live) {
             uint32_t r[16];
             tmem_ld16(trow + TM_P + cb, r);
             tmem_wait_ld();

@@ -175,7 +175,8 @@ def test_pass_overlap_matches_serial_order(env):
     programmatic dependent of the passes, its parts waiting for them); with
     gla_set_pass_overlap(0) the passes run first.  The kernels and their arithmetic are the
     same, so every output is bit-identical between the two orders -- plain and training path
-    (saved gate and state copies)."""
+    (saved gate and state copies), the forward with the fused output epilogue and the
+    prefill into a state pool."""
     gla, torch = env
     B, T, H, seed = 10, 256, 16, 68
     if n_sm(torch) != 152:
@@ -184,6 +185,11 @@ def test_pass_overlap_matches_serial_order(env):
     gam = oracle_decays(H)[0].cuda()
     qd, kd, vd, gd = (to_dev(x, torch.bfloat16) for x in (q, k, v, dO))
     ad, idd, fd = (to_dev(x, torch.float32) for x in (a, init, dfin))
+    g_in = to_dev(synth.normal(seed, synth.DO, (B, T, H, 192), 1.5), torch.bfloat16)
+    w_n = to_dev(1.0 + synth.normal(seed, synth.A, (4, 192), 0.2), torch.float32)
+    P = B + 3  # a pool of 13 pages of 2 layers; sequence b uses page[b]
+    pool = to_dev(synth.normal(seed, synth.INIT, (P, 2, H, 96, 192), 0.05), torch.float32)
+    page = to_dev(np.random.default_rng(seed).permutation(P)[:B].astype(np.int32), torch.int32)
 
     def run(overlap):
         gla.set_pass_overlap(overlap)
@@ -199,6 +205,11 @@ def test_pass_overlap_matches_serial_order(env):
             out += [o2, fin2, gate,
                     *gla.chunk_bwd(qd, kd, vd, gam, ad, gd, idd, fd, gate=gate,
                                    saved_states=saved)]
+            y, rstd, o3, fin3 = gla.chunk_fwd_gated(qd, kd, vd, gam, ad, g_in, w_n, 4, 1e-6, idd,
+                                                    want_o=True)
+            pool_d = pool.clone()
+            o4 = gla.chunk_fwd_paged(qd, kd, vd, gam, ad, pool_d, page, 1, init_from_pool=True)
+            out += [y, rstd, o3, fin3, o4, pool_d]
             torch.cuda.synchronize()
             assert gla.get_device_error() == 0
             return [x.cpu().numpy() for x in out]
@@ -207,6 +218,8 @@ def test_pass_overlap_matches_serial_order(env):
             gla.set_pass_overlap(True)
 
     on, off = run(True), run(False)
-    names = ["o", "final", *NAMES, "o_saved", "final_saved", "gate", *(n + "_saved" for n in NAMES)]
+    names = ["o", "final", *NAMES, "o_saved", "final_saved", "gate",
+             *(n + "_saved" for n in NAMES), "gated_y", "gated_rstd", "gated_o", "gated_final",
+             "paged_o", "paged_pool"]
     diff = [n for n, x, y in zip(names, on, off) if not np.array_equal(x, y)]
     assert not diff, f"outputs differ between the launch orders: {diff}"
