@@ -50,18 +50,19 @@ constexpr uint32_t S_ATOM = 12288;
 constexpr uint32_t OFF_STG = OFF_CP + 3 * S_ATOM;  // output staging, 2 KB per epilogue warp
 constexpr uint32_t OFF_BAR = OFF_STG + 16 * 2048;
 constexpr uint32_t NBAR = 21;
-constexpr uint32_t OFF_TMEM = OFF_BAR + NBAR * 8;
+constexpr uint32_t OFF_TMEM = (OFF_BAR + NBAR * 8 + 15) & ~15u;  // 16-byte aligned from here
 constexpr uint32_t OFF_ABORT = OFF_TMEM + 4;
 constexpr uint32_t OFF_RED = OFF_TMEM + 16;  // float red[3][16]: per-warp max|S|
 constexpr uint32_t OFF_ES = OFF_RED + 192;   // int es[2]
 constexpr uint32_t OFF_AB = OFF_ES + 16;     // float abmax[2][32]: state-MMA operand maxima
 constexpr uint32_t OFF_GP = OFF_AB + 256;    // float gate_part[4][128]: gate partial sums
 constexpr uint32_t OFF_DP = OFF_GP + 2048;   // float dpv[128]: dO.v per row (DQ, DK)
-constexpr uint32_t OFF_A = OFF_DP + 512;     // float a[96]
+constexpr uint32_t OFF_A = OFF_DP + 512;     // float a[96] (read as float4)
 constexpr uint32_t OFF_PW = OFF_A + 384;     // float pw[128]
 constexpr uint32_t SMEM_USED = OFF_PW + 512;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+static_assert(OFF_A % 16 == 0, "a[] is read as float4");
 
 constexpr uint32_t TM_X = 0, TM_A = 96, TM_S = 192, TM_P = 384;  // TM_A: d_a (DQ role)
 
@@ -754,8 +755,12 @@ __device__ __forceinline__ void run_role(
                 float f8[8];
                 unpack8<false>(vv[k], f8);
 #pragma unroll
+                const float4 a0 = *reinterpret_cast<const float4*>(sa + col);
+                const float4 a1 = *reinterpret_cast<const float4*>(sa + col + 4);
+                const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
                 for (int j = 0; j < 8; ++j)
-                  x[j] = fmaf(__uint_as_float(r[j]), osc, rr * sa[col + j] * f8[j]);
+                  x[j] = fmaf(__uint_as_float(r[j]), osc, rr * av[j] * f8[j]);
               }
             },
             [&](int k, uint32_t src) {
