@@ -408,9 +408,12 @@ def run_gpu(args, rank, world, local_rank):
     # our kernels per step: chunk fwd, chunk bwd, d_aug reduction, decode, and the two segment
     # passes of each chunked call whose plan cuts pairs into parts
     n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
-    cut_f = gla.split_plan(B, T, H, False, n_sm)[1] > 1
-    cut_b = gla.split_plan(B, T, H, 2 if args.saved_states else 1, n_sm)[1] > 1
-    gpu_launches_per_step = 4 + 2 * int(cut_f) + 2 * int(cut_b)
+    # segment passes of a cut call: the sum pass, and the link pass unless there are two parts
+    parts_f = gla.split_plan(B, T, H, False, n_sm)[1]
+    parts_b = gla.split_plan(B, T, H, 2 if args.saved_states else 1, n_sm)[1]
+    pass_f = 0 if parts_f <= 1 else (1 if parts_f == 2 else 2)
+    pass_b = 0 if parts_b <= 1 else (1 if parts_b == 2 else 2)
+    gpu_launches_per_step = 4 + pass_f + pass_b
 
     def roof(bound, achieved, peak, unit, traffic):
         return dict(bound=bound, achieved=achieved, peak=peak, unit=unit, frac=achieved / peak,
@@ -589,8 +592,8 @@ def run_gpu(args, rank, world, local_rank):
         e2e=e2e, e2e_full_readback=e2e_full_readback,
         gpu_launches=gpu_launches_per_step * args.steps,
         gpu_launches_detail="per step: chunk fwd, chunk bwd, d_aug reduction, decode"
-                            + (", fwd segment passes (2)" if cut_f else "")
-                            + (", bwd segment passes (2)" if cut_b else ""),
+                            + (f", fwd segment passes ({pass_f})" if pass_f else "")
+                            + (f", bwd segment passes ({pass_b})" if pass_b else ""),
         clocks=clocks, wall_s_timed=t_wall,
     )
     if rank == 0:

@@ -79,6 +79,10 @@ struct SplitPlan {
   // launched as a programmatic dependent of the launch before it, so the chunked kernel's whole
   // pairs start beside the passes and only its parts wait for them (griddep_wait)
   bool overlap = false;
+  // CTAs of the sum pass (0: one per summed part).  Beside the whole pairs the pass walks
+  // several parts per CTA, so that the SMs it holds at the start stay few enough for every
+  // part of the last wave to start on an SM that began with a whole pair.
+  int pass_ctas = 0;
 };
 __host__ __device__ inline int part_begin(int j, int nc, int parts) {
   return (int)(((long long)j * nc) / parts);
@@ -179,9 +183,11 @@ long long split_slots(long long BH, const SplitPlan& p);
 // 1.., reverse direction for the adjoints leaving parts ..p-2), then their recurrences, which
 // also place the initial state (init / pool page / zero) and the final-state adjoint (dfin /
 // zero) in the first and last slots.  states (adj) null: that direction is not computed.
-// q_or_null, dO_or_null are needed for the reverse direction only.  With plan.overlap pass B
-// is pass A's programmatic dependent and runs on at most 16 CTAs (which wait beside pass A's),
-// so that the chunked kernel launched next as its dependent can start its whole pairs at once.
+// q_or_null, dO_or_null are needed for the reverse direction only.  With two parts the sum
+// pass applies the one step of each recurrence itself and pass B is not launched.  With
+// plan.overlap pass B is pass A's programmatic dependent and runs on at most 16 CTAs (which
+// wait beside pass A's), so that the chunked kernel launched next as its dependent can start
+// its whole pairs at once; pass A runs on plan.pass_ctas CTAs.
 cudaError_t launch_segment_states(const void* q, const void* k, const void* v, const void* dO,
                                   bool bf16, const float* log_decay, const float* init,
                                   const float* dfin, const StatePages& sp, float* states,

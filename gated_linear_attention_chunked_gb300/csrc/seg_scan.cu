@@ -14,12 +14,14 @@
 //     dS leaving part j-1  = lambda^(L_j) dS leaving part j + U'_j,
 //                            U'_j = sum_{t in j} lambda^(t - s_j + 1) q_t dO_t^T.
 //
-//   pass A  (seg_sum_kernel, one CTA per cut pair and part): U_j (parts 0..p-2) or U'_j
-//           (parts 1..p-1) on the tensor cores, the pair's K''^T V or Q''^T dO over the part's
-//           chunks into one fp32 TMEM accumulator, the decay folded into the fp16 copy of k (q);
+//   pass A  (seg_sum_kernel, one item per cut pair and part, a CTA taking one or several in
+//           turn): U_j (parts 0..p-2) or U'_j (parts 1..p-1) on the tensor cores, the pair's
+//           K''^T V or Q''^T dO over the part's chunks into one fp32 TMEM accumulator, the decay
+//           folded into the fp16 copy of k (q);
 //   pass B  (seg_link_kernel): the recurrences above per cut pair, giving every part its
 //           starting state (the caller's initial state, a pool page or zero for part 0) and
-//           its starting adjoint (d_final_state or zero for the last part);
+//           its starting adjoint (d_final_state or zero for the last part) -- with two parts
+//           one step per direction, which pass A's items take themselves (no pass B);
 //   then    the chunked kernel runs the whole pairs and every part as its own CTA.
 //
 // Extra traffic: pass A reads k, v (q, dO) of all parts but the last (first).
@@ -27,6 +29,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <map>
 
 #include "kernels.h"
@@ -46,8 +49,7 @@ constexpr uint32_t OFF_BAR = STAGES * STAGE;
 constexpr uint32_t NBAR = 10;
 constexpr uint32_t OFF_TMEM = OFF_BAR + NBAR * 8;
 constexpr uint32_t OFF_ABORT = OFF_TMEM + 4;
-constexpr uint32_t OFF_PW = OFF_TMEM + 16;  // float pw[128] = lambda^i
-constexpr uint32_t SMEM_USED = OFF_PW + 512;
+constexpr uint32_t SMEM_USED = OFF_TMEM + 16;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // + alignment of the dynamic base
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
@@ -70,19 +72,46 @@ __device__ __forceinline__ uint32_t v_chunk(uint32_t i, int cc) {
   return 3 * K_BOX + (cc >> 3) * V_BOX + swz_off(i, cc & 7, 128);
 }
 
-// Pass A.  CTA i < n_fwd: forward sum U_j of part j = i % (p-1) of cut pair x = i / (p-1),
-// into states[x*p + j + 1]; CTA i >= n_fwd: reverse sum U'_j of part j = 1 + i' % (p-1) (i' =
-// i - n_fwd), into adj[x*p + j - 1].  Those slots are then completed by pass B in place.
-// full != 0 (a sequence-sharded call's slice sums): one CTA per pair bh, its one part being
-// the whole sequence; CTA i < n_fwd writes U of pair i into states[i], CTA i >= n_fwd U' of
-// pair i - n_fwd into adj[i - n_fwd].
+// Item `it` of pass A: it < n_fwd is the forward sum U_j of part j = it % (p-1) of cut pair
+// x = it / (p-1), into states[x*p + j + 1]; it >= n_fwd the reverse sum U'_j of part
+// j = 1 + it' % (p-1) (it' = it - n_fwd), into adj[x*p + j - 1].  Those slots are then
+// completed by pass B in place -- or, with two parts (`fold`), by the item itself.
+// full != 0 (a sequence-sharded call's slice sums): one item per pair bh, its one part being
+// the whole sequence; item it < n_fwd writes U of pair it into states[it], it >= n_fwd U' of
+// pair it - n_fwd into adj[it - n_fwd].
+struct SumItem {
+  bool rev;
+  int x, j, bh, b, h, c_lo, c_hi;
+};
+__device__ __forceinline__ SumItem sum_item(int it, int n_fwd, int full, int whole, int parts,
+                                            int H, int nc) {
+  SumItem I;
+  I.rev = it >= n_fwd;
+  const int idx = I.rev ? it - n_fwd : it;
+  I.x = full ? idx : idx / (parts - 1);
+  I.j = full ? 0 : idx % (parts - 1) + (I.rev ? 1 : 0);
+  I.bh = whole + I.x;
+  I.b = I.bh / H;
+  I.h = I.bh % H;
+  I.c_lo = full ? 0 : part_begin(I.j, nc, parts);
+  I.c_hi = full ? nc : part_begin(I.j + 1, nc, parts);
+  return I;
+}
+
+// Pass A.  The CTA takes items blockIdx.x, blockIdx.x + gridDim.x, ... in order; its TMA ring
+// runs on across them (the next item's first chunks load while this one's sum is written out).
+// fold (two parts, not full): the item also applies its pair's one recurrence step, as pass B
+// would: forward, states[x*2] = S_0 (the caller's initial state, its pool page or zeros) and
+// states[x*2 + 1] = lambda^(L_0) S_0 + U_0; reverse, adj[x*2 + 1] = A_1 (d_final_state or
+// zeros) and adj[x*2] = lambda^(L_1) A_1 + U'_1.
 template <bool BF16>
 __global__ void __launch_bounds__(THREADS, 1)
 seg_sum_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
                const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_g,
                const float* __restrict__ log_decay, float* __restrict__ states,
-               float* __restrict__ adj, int T, int H, int whole, int parts, int n_fwd, int full,
-               DevCtl ctl) {
+               float* __restrict__ adj, const float* __restrict__ init,
+               const float* __restrict__ dfin, StatePages sp, int T, int H, int whole, int parts,
+               int n_fwd, int n_items, int full, int fold, DevCtl ctl) {
   // pass B may start (it waits for these sums), and with it the chunked kernel's whole pairs
   griddep_launch_dependents();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -97,19 +126,8 @@ seg_sum_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant_
   cta.abort_off = OFF_ABORT;
   uint8_t* const base = cta.base;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const bool rev = (int)blockIdx.x >= n_fwd;
-  const int idx = rev ? (int)blockIdx.x - n_fwd : (int)blockIdx.x;
-  const int x = full ? idx : idx / (parts - 1), j = full ? 0 : idx % (parts - 1) + (rev ? 1 : 0);
-  const int bh = whole + x, b = bh / H, h = bh % H;
   const int nc = (T + C - 1) / C;
-  const int c_lo = full ? 0 : part_begin(j, nc, parts), c_hi = full ? nc : part_begin(j + 1, nc, parts);
-  const int M = c_hi - c_lo;  // chunks of the part (>= 1)
-  // tokens of the part's last chunk (C unless it is the sequence's ragged last chunk)
-  const int last_len = min(c_hi * C, T) - (c_hi - 1) * C;
-  const CUtensorMap* map_a = rev ? &map_q : &map_k;
-  const CUtensorMap* map_b = rev ? &map_g : &map_v;
-  const float gamma = __ldg(log_decay + h);
-  float* pw = (float*)(base + OFF_PW);
+  const int it0 = (int)blockIdx.x, it_step = (int)gridDim.x;
   uint32_t* tmem_slot = (uint32_t*)(base + OFF_TMEM);
 
   if (warp == MMA_WARP) {
@@ -126,29 +144,38 @@ seg_sum_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant_
     *cta.abort_flag() = 0;
     fence_barrier_init();
   }
-  if (tid < C) pw[tid] = expf((float)tid * gamma);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint32_t sb = cta.sb;
 
+  // g: this CTA's chunk step over all its items (ring stage g % STAGES, phase g / STAGES)
   if (warp == PRODUCER_WARP) {
     if (lane == 0) {
       int armed0 = 0, armed1 = 0, armed2 = 0;  // loads issued per stage
-      for (int m = 0; m < M; ++m) {
-        const int s = m % STAGES;
-        if (m >= STAGES && !wait(cta, cta.bar(EMPTY + s), (m / STAGES - 1) & 1, ctl)) break;
-        mbar_arrive_expect_tx(cta.bar(FULL + s), STAGE);
-        const int t0 = (c_lo + m) * C;
-        const uint32_t st = sb + s * STAGE;
-        for (int jb = 0; jb < 3; ++jb) {
-          tma_load_4d(st + jb * K_BOX, map_a, cta.bar(FULL + s), 32 * jb, h, t0, b);
-          tma_load_4d(st + 3 * K_BOX + jb * V_BOX, map_b, cta.bar(FULL + s), 64 * jb, h, t0, b);
+      bool ok = true;
+      int g = 0;
+      for (int it = it0; it < n_items && ok; it += it_step) {
+        const SumItem I = sum_item(it, n_fwd, full, whole, parts, H, nc);
+        const CUtensorMap* map_a = I.rev ? &map_q : &map_k;
+        const CUtensorMap* map_b = I.rev ? &map_g : &map_v;
+        for (int m = 0; m < I.c_hi - I.c_lo; ++m, ++g) {
+          const int s = g % STAGES;
+          if (g >= STAGES && !(ok = wait(cta, cta.bar(EMPTY + s), (g / STAGES - 1) & 1, ctl)))
+            break;
+          mbar_arrive_expect_tx(cta.bar(FULL + s), STAGE);
+          const int t0 = (I.c_lo + m) * C;
+          const uint32_t st = sb + s * STAGE;
+          for (int jb = 0; jb < 3; ++jb) {
+            tma_load_4d(st + jb * K_BOX, map_a, cta.bar(FULL + s), 32 * jb, I.h, t0, I.b);
+            tma_load_4d(st + 3 * K_BOX + jb * V_BOX, map_b, cta.bar(FULL + s), 64 * jb, I.h, t0,
+                        I.b);
+          }
+          armed0 += s == 0;
+          armed1 += s == 1;
+          armed2 += s == 2;
         }
-        armed0 += s == 0;
-        armed1 += s == 1;
-        armed2 += s == 2;
       }
       // no copy may still be landing when the CTA exits
       if (armed0) mbar_wait(cta.bar(FULL + 0), (armed0 - 1) & 1, ctl, DRAIN_NS);
@@ -158,71 +185,130 @@ seg_sum_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant_
   } else if (warp == MMA_WARP) {
     if (lane == 0) {
       // U (rows = 96 key channels + 32 padding rows never read) += A''^T B, K = 16 tokens per
-      // instruction: A = k (q) tile as [token][channel] (MN-major), B = v (dO) tile likewise
+      // instruction: A = k (q) tile as [token][channel] (MN-major), B = v (dO) tile likewise.
+      // One DONE phase per item; the next item's first MMA overwrites the accumulator, which
+      // the convert warps have read out before they release that item's first stage (CONV).
       constexpr uint32_t ID = idesc_f16(128, 192, false, false, true, true);
-      for (int m = 0; m < M; ++m) {
-        const int s = m % STAGES;
-        if (m == ctl.stall_step) {  // the give-up path's diagnostic (see the chunk kernels)
-          wait(cta, cta.bar(DONE), 0, ctl);
-          break;
-        }
-        if (!wait(cta, cta.bar(CONV + s), (m / STAGES) & 1, ctl)) break;
-        tc_fence_after();
-        const uint32_t st = sb + s * STAGE;
+      bool ok = true;
+      int g = 0, k = 0, commits = 0;
+      for (int it = it0; it < n_items && ok; it += it_step, ++k) {
+        const SumItem I = sum_item(it, n_fwd, full, whole, parts, H, nc);
+        for (int m = 0; m < I.c_hi - I.c_lo; ++m, ++g) {
+          const int s = g % STAGES;
+          if (g == ctl.stall_step) {  // the give-up path's diagnostic (see the chunk kernels):
+            // DONE's phase k completes only after this item's MMAs, so the wait runs out
+            wait(cta, cta.bar(DONE), k & 1, ctl);
+            ok = false;
+            break;
+          }
+          if (!(ok = wait(cta, cta.bar(CONV + s), (g / STAGES) & 1, ctl))) break;
+          tc_fence_after();
+          const uint32_t st = sb + s * STAGE;
 #pragma unroll 1
-        for (int ks = 0; ks < 8; ++ks)
-          mma_f16_ss(tmem, smem_desc(st + ks * 1024, K_BOX, 512, SW_64),
-                     smem_desc(st + 3 * K_BOX + ks * 2048, V_BOX, 1024, SW_128), ID,
-                     (m > 0 || ks > 0) ? 1u : 0u);
-        mma_commit(cta.bar(EMPTY + s));
+          for (int ks = 0; ks < 8; ++ks)
+            mma_f16_ss(tmem, smem_desc(st + ks * 1024, K_BOX, 512, SW_64),
+                       smem_desc(st + 3 * K_BOX + ks * 2048, V_BOX, 1024, SW_128), ID,
+                       (m > 0 || ks > 0) ? 1u : 0u);
+          mma_commit(cta.bar(EMPTY + s));
+        }
+        if (ok) {
+          mma_commit(cta.bar(DONE));
+          ++commits;
+        }
       }
+      // every MMA issued (the items' and any an abort left behind) has completed before the
+      // accumulator is freed: one more commit, whose phase nothing else waits for
       mma_commit(cta.bar(DONE));
-      mbar_wait(cta.bar(DONE), 0, ctl, DRAIN_NS);
+      mbar_wait(cta.bar(DONE), commits & 1, ctl, DRAIN_NS);
     }
   } else {
     // ---- warps 0..3: in-place fp16 operands of chunk m, row i = token i of the chunk: k
     // scaled by lambda^(e_j - t) (forward) or q by lambda^(t - s_j + 1) (reverse), v / dO as
     // they are.  Rows past T are zeros (the tensor map's fill); in the forward direction e_j
     // is the part's last token, so a ragged last chunk weighs its rows by
-    // lambda^(last_len - 1 - i) and its rows past T by 0.
+    // lambda^(last_len - 1 - i) and its rows past T by 0.  Every wait is voted per warp, so
+    // a warp stays on one path through the items and its collective TMEM loads.
     const int i = tid;
-    const float lamC = expf((float)C * gamma);
-    const float row_w = rev ? (i + 1 < C ? pw[i + 1] : lamC) : pw[C - 1 - i];
-    const float row_w_last = rev ? row_w : (i < last_len ? pw[last_len - 1 - i] : 0.f);
     float vmax = 0.f;
     bool ok = true;
-    for (int m = 0; m < M && ok; ++m) {
-      const int s = m % STAGES;
-      if (!(ok = wait(cta, cta.bar(FULL + s), (m / STAGES) & 1, ctl))) break;
-      uint8_t* st = base + s * STAGE;
-      // reverse: the chunks between this one and s_j; forward: the tokens after this chunk up
-      // to e_j (whole chunks, then the last chunk's last_len)
-      const float sk = rev ? expf(gamma * (float)(C * m)) * row_w
-                           : (m == M - 1 ? row_w_last
-                                         : expf(gamma * (float)(C * (M - 2 - m) + last_len)) * row_w);
-      convert_row<BF16, 12>(st, [&](int cc) { return k_chunk(i, cc); }, sk, vmax);
-      convert_row<BF16, 24>(st, [&](int cc) { return v_chunk(i, cc); }, 1.f, vmax);
-      fence_proxy_async();
-      mbar_arrive(cta.bar(CONV + s));
-    }
-    // ---- the sum out: rows 0..95 (warps 0..2), 192 fp32 each
-    if (ok) ok = wait(cta, cta.bar(DONE), 0, ctl);
-    ok = __all_sync(0xffffffffu, ok && *cta.abort_flag() == 0);
-    if (ok && warp < 3) {
-      tc_fence_after();
-      const long long slot = full ? (long long)x : (long long)x * parts + (rev ? j - 1 : j + 1);
-      float* dst = (rev ? adj : states) + (size_t)slot * DK * DV + (size_t)i * DV;
-      const uint32_t trow = tmem + ((uint32_t)(32 * warp) << 16);
+    int g = 0, k = 0;
+    for (int it = it0; it < n_items && ok; it += it_step, ++k) {
+      const SumItem I = sum_item(it, n_fwd, full, whole, parts, H, nc);
+      const int M = I.c_hi - I.c_lo;  // chunks of the part (>= 1)
+      // tokens of the part, and of its last chunk (C unless it is the sequence's ragged one)
+      const int len = min(I.c_hi * C, T) - I.c_lo * C;
+      const int last_len = min(I.c_hi * C, T) - (I.c_hi - 1) * C;
+      const float gamma = __ldg(log_decay + I.h);
+      // lambda^d as exp(d gamma), d = i + 1 (reverse) or C - 1 - i (forward)
+      const float row_w = expf((float)(I.rev ? i + 1 : C - 1 - i) * gamma);
+      const float row_w_last =
+          I.rev ? row_w : (i < last_len ? expf((float)(last_len - 1 - i) * gamma) : 0.f);
+      for (int m = 0; m < M; ++m, ++g) {
+        const int s = g % STAGES;
+        if (!(ok = wait_warp(cta, cta.bar(FULL + s), (g / STAGES) & 1, ctl))) break;
+        uint8_t* st = base + s * STAGE;
+        // reverse: the chunks between this one and s_j; forward: the tokens after this chunk
+        // up to e_j (whole chunks, then the last chunk's last_len)
+        const float sk = I.rev ? expf(gamma * (float)(C * m)) * row_w
+                               : (m == M - 1 ? row_w_last
+                                             : expf(gamma * (float)(C * (M - 2 - m) + last_len)) *
+                                                   row_w);
+        convert_row<BF16, 12>(st, [&](int cc) { return k_chunk(i, cc); }, sk, vmax);
+        convert_row<BF16, 24>(st, [&](int cc) { return v_chunk(i, cc); }, 1.f, vmax);
+        fence_proxy_async();
+        tc_fence_before();  // (the previous item's TMEM loads come before this stage's MMAs)
+        mbar_arrive(cta.bar(CONV + s));
+      }
+      // ---- the sum out: rows 0..95 (warps 0..2), 192 fp32 each
+      if (ok) ok = wait_warp(cta, cta.bar(DONE), k & 1, ctl);
+      ok = __all_sync(0xffffffffu, ok && *cta.abort_flag() == 0);
+      if (ok && warp < 3) {
+        tc_fence_after();
+        float* const out = I.rev ? adj : states;
+        const long long slot =
+            full ? (long long)I.x : (long long)I.x * parts + (I.rev ? I.j - 1 : I.j + 1);
+        float* dst = out + (size_t)slot * DK * DV + (size_t)i * DV;
+        // fold: the boundary row (the pair's initial state or d_final_state; null = zeros),
+        // its slot, and lambda^(tokens of this part)
+        const float* bnd = nullptr;
+        float* dst0 = nullptr;
+        float lam = 0.f;
+        if (fold) {
+          dst0 = out + ((size_t)I.x * parts + (I.rev ? parts - 1 : 0)) * DK * DV + (size_t)i * DV;
+          lam = expf(gamma * (float)len);
+          if (I.rev) {
+            if (dfin) bnd = dfin + ((size_t)I.bh * DK + i) * DV;
+          } else {
+            long long zi = I.bh;  // [b][h] of the caller's initial states, or a pool page
+            if (sp.init_paged) {
+              const int pg = __ldg(sp.page + I.b);
+              zi = (pg >= 0 && pg < sp.n_pages)
+                       ? ((long long)pg * sp.pool_layers + sp.layer) * H + I.h
+                       : -1;
+            }
+            if (init && zi >= 0) bnd = init + ((size_t)zi * DK + i) * DV;
+          }
+        }
 #pragma unroll 1
-      for (int cb = 0; cb < DV / 32; ++cb) {
-        uint32_t r[32];
-        tmem_ld32(trow + 32 * cb, r);
-        tmem_wait_ld();
+        for (int cb = 0; cb < DV / 32; ++cb) {
+          uint32_t r[32];
+          tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16) + 32 * cb, r);
+          tmem_wait_ld();
 #pragma unroll
-        for (int jj = 0; jj < 32; jj += 4)
-          *reinterpret_cast<float4*>(dst + 32 * cb + jj) =
-              make_float4(__uint_as_float(r[jj]), __uint_as_float(r[jj + 1]),
-                          __uint_as_float(r[jj + 2]), __uint_as_float(r[jj + 3]));
+          for (int jj = 0; jj < 32; jj += 4) {
+            float4 u = make_float4(__uint_as_float(r[jj]), __uint_as_float(r[jj + 1]),
+                                   __uint_as_float(r[jj + 2]), __uint_as_float(r[jj + 3]));
+            if (fold) {
+              const float4 b4 =
+                  bnd ? __ldg(reinterpret_cast<const float4*>(bnd + 32 * cb + jj))
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+              *reinterpret_cast<float4*>(dst0 + 32 * cb + jj) = b4;
+              u = make_float4(fmaf(lam, b4.x, u.x), fmaf(lam, b4.y, u.y), fmaf(lam, b4.z, u.z),
+                              fmaf(lam, b4.w, u.w));
+            }
+            *reinterpret_cast<float4*>(dst + 32 * cb + jj) = u;
+          }
+        }
       }
     }
     if (vmax >= 65504.f) record_error(ctl, DEV_RANGE);
@@ -372,6 +458,18 @@ constexpr int kMaxParts = 32;
 // parts over B = 8..40 matched the estimate's ratios to about 3 %: cutting pays when the last
 // wave is nearly empty -- backward B = 16, 32; forward B = 12, 40 -- and costs otherwise.)
 constexpr int kMinPartChunks = 4;
+
+// CTAs of a sum pass of `items` parts beside the whole CTAs: the SMs the last wave's `tail`
+// part CTAs leave over (the others start with a whole CTA, so all the parts find an SM free at
+// about the same time), but enough to end within half the whole CTAs' waves (t_lo steps).
+long long pass_width(long long items, long long tail, double pre_len, double t_lo, int n_sm) {
+  long long w = n_sm - tail;
+  const long long w_min =
+      t_lo > 0.0 ? (long long)std::ceil((double)items * pre_len * 2.0 / t_lo) : items;
+  if (w < w_min) w = w_min;
+  if (w > items) w = items;
+  return w < 1 ? 1 : w;
+}
 }  // namespace
 
 SplitPlan plan_split(long long BH, int nc, int roles, int n_sm, int force_parts, int pass_dirs,
@@ -407,12 +505,14 @@ SplitPlan plan_split(long long BH, int nc, int roles, int n_sm, int force_parts,
         list_finish((long long)roles * X * p, part_len, n_sm, n_hi, t_lo, t_lo + whole_len);
     const long long pre_ctas = X * (p - 1) * pass_dirs;
     const double pre_len = (double)((nc + p - 1) / p) * kPassChunk[bwd] + kPassStart;
-    const double pre_serial = (double)((pre_ctas + n_sm - 1) / n_sm) * pre_len + kPassLaunch;
-    double pre_t = pre_serial;
+    const double launches = p == 2 ? kPassLaunch / 2 : kPassLaunch;  // two parts: no pass B
+    double pre_t = (double)((pre_ctas + n_sm - 1) / n_sm) * pre_len + launches;
     if (overlap && W >= n_sm) {
       // beside at least a wave of whole CTAs the passes take only their share of the SMs'
       // time (their CTAs start first, the whole CTAs on the other SMs); the parts wait for
       // them only if they end after the whole CTAs
+      const long long width = pass_width(pre_ctas, roles * X * p, pre_len, t_lo, n_sm);
+      const double pre_serial = (double)((pre_ctas + width - 1) / width) * pre_len + launches;
       pre_t = (double)pre_ctas * pre_len / n_sm + (pre_serial > t_lo ? pre_serial - t_lo : 0.0);
     }
     const double total = main_t + pre_t;
@@ -426,6 +526,11 @@ SplitPlan plan_split(long long BH, int nc, int roles, int n_sm, int force_parts,
   plan.whole = (int)(BH - X);
   plan.parts = best_p;
   plan.overlap = overlap && W >= n_sm;
+  if (plan.overlap) {
+    const long long items = X * (best_p - 1) * pass_dirs;
+    const double pre_len = (double)((nc + best_p - 1) / best_p) * kPassChunk[bwd] + kPassStart;
+    plan.pass_ctas = (int)pass_width(items, roles * X * best_p, pre_len, t_lo, n_sm);
+  }
   return plan;
 }
 
@@ -454,14 +559,21 @@ cudaError_t launch_segment_states(const void* q, const void* k, const void* v, c
   }
   const long long n_fwd = states ? X * (plan.parts - 1) : 0;
   const long long n_rev = adj ? X * (plan.parts - 1) : 0;
-  if (n_fwd + n_rev > 0) {
+  const long long n_items = n_fwd + n_rev;
+  // two parts: one recurrence step per direction, which the sum pass takes itself
+  const bool fold = plan.parts == 2;
+  if (n_items > 0) {
     auto kern = bf16 ? seg_sum_kernel<true> : seg_sum_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    kern<<<(unsigned)(n_fwd + n_rev), THREADS, SMEM_BYTES, stream>>>(
-        mk, mv, mq, mg, log_decay, states, adj, T, H, plan.whole, plan.parts, (int)n_fwd, 0, ctl);
+    const long long grid =
+        plan.pass_ctas > 0 && plan.pass_ctas < n_items ? plan.pass_ctas : n_items;
+    kern<<<(unsigned)grid, THREADS, SMEM_BYTES, stream>>>(
+        mk, mv, mq, mg, log_decay, states, adj, init, dfin, sp, T, H, plan.whole, plan.parts,
+        (int)n_fwd, (int)n_items, 0, fold ? 1 : 0, ctl);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
+  if (fold) return cudaSuccess;
   const long long items = 2LL * X * (DK * DV / 4);
   long long ctas = (items + LINK_THREADS - 1) / LINK_THREADS;
   if (plan.overlap && ctas > LINK_CTAS_OVERLAP) ctas = LINK_CTAS_OVERLAP;
@@ -483,8 +595,8 @@ cudaError_t launch_slice_sums(const void* a, const void* b, bool bf16, bool reve
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
   kern<<<(unsigned)n, THREADS, SMEM_BYTES, stream>>>(
-      ma, mb, ma, mb, log_decay, reverse ? nullptr : out, reverse ? out : nullptr, T, H, 0, 2,
-      reverse ? 0 : (int)n, 1, ctl);
+      ma, mb, ma, mb, log_decay, reverse ? nullptr : out, reverse ? out : nullptr, nullptr,
+      nullptr, StatePages{}, T, H, 0, 2, reverse ? 0 : (int)n, (int)n, 1, 0, ctl);
   return cudaGetLastError();
 }
 

@@ -178,15 +178,15 @@ def test_split_plan_query(lib):
         assert rc == 0
         return w.value, p.value
     assert lib.gla_set_split_parts(0) == 0
-    # T = 2048 (16 chunks), B = 32: the forward's last wave is 56 of 152 CTAs full.  With the
-    # segment passes beside the whole pairs (the default) its pairs are cut in two: the passes
-    # cost only their share of the SMs and the parts halve the tail; with the passes before the
-    # whole pairs (on the caller's stream) cutting does not pay.  The backward's 1536 CTAs leave
-    # 16 for an eleventh wave: its 6 pairs are cut (>= 4 chunks a part) either way.
+    # T = 2048 (16 chunks), B = 32: the forward's last wave is 56 of 152 CTAs full.  Its pairs
+    # are cut in two whether the segment passes run beside the whole pairs (the default: they
+    # cost only their share of the SMs) or before them: with two parts the sum pass is the only
+    # extra launch.  The backward's 1536 CTAs leave 16 for an eleventh wave: its 6 pairs are cut
+    # (>= 4 chunks a part) either way.
     assert plan(32, 2048, 16, 0) == (456, 2)
     try:
         assert lib.gla_set_pass_overlap(0) == 0
-        assert plan(32, 2048, 16, 0) == (512, 1)
+        assert plan(32, 2048, 16, 0) == (456, 2)
         w, p = plan(32, 2048, 16, 1)
         assert w == 506 and 2 <= p <= 4
     finally:
