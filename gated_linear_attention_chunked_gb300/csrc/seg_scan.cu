@@ -46,8 +46,8 @@ constexpr uint32_t K_BOX = 8192;                   // 128 rows x 32 channels x 2
 constexpr uint32_t V_BOX = 16384;                  // 128 rows x 64 channels x 2 B, 128-B swizzle
 constexpr uint32_t STAGE = 3 * K_BOX + 3 * V_BOX;  // k then v of one chunk: 72 KB
 constexpr uint32_t OFF_BAR = STAGES * STAGE;
-constexpr uint32_t NBAR = 10;
-constexpr uint32_t OFF_TMEM = OFF_BAR + NBAR * 8;
+constexpr uint32_t NBAR = 11;
+constexpr uint32_t OFF_TMEM = (OFF_BAR + NBAR * 8 + 15) & ~15u;
 constexpr uint32_t OFF_ABORT = OFF_TMEM + 4;
 constexpr uint32_t SMEM_USED = OFF_TMEM + 16;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // + alignment of the dynamic base
@@ -57,7 +57,8 @@ enum Bar : uint32_t {
   FULL = 0,   // 0..2: stage s landed
   CONV = 3,   // 3..5: stage s converted to fp16 operands
   EMPTY = 6,  // 6..8: the MMAs of stage s are done
-  DONE = 9,   // every MMA is done
+  DONE = 9,   // every MMA of the current item is done (one phase per item)
+  DRAIN = 10,  // every MMA the CTA issued is done (the MMA thread's own wait before exit)
 };
 
 constexpr int THREADS = 192;  // warps 0..3 convert + epilogue (row = token = TMEM lane)
@@ -141,6 +142,7 @@ seg_sum_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant_
       mbar_init(cta.bar(EMPTY + s), 1);
     }
     mbar_init(cta.bar(DONE), 1);
+    mbar_init(cta.bar(DRAIN), 1);
     *cta.abort_flag() = 0;
     fence_barrier_init();
   }
@@ -190,7 +192,7 @@ seg_sum_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant_
       // the convert warps have read out before they release that item's first stage (CONV).
       constexpr uint32_t ID = idesc_f16(128, 192, false, false, true, true);
       bool ok = true;
-      int g = 0, k = 0, commits = 0;
+      int g = 0, k = 0;
       for (int it = it0; it < n_items && ok; it += it_step, ++k) {
         const SumItem I = sum_item(it, n_fwd, full, whole, parts, H, nc);
         for (int m = 0; m < I.c_hi - I.c_lo; ++m, ++g) {
@@ -211,15 +213,13 @@ seg_sum_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant_
                        (m > 0 || ks > 0) ? 1u : 0u);
           mma_commit(cta.bar(EMPTY + s));
         }
-        if (ok) {
-          mma_commit(cta.bar(DONE));
-          ++commits;
-        }
+        if (ok) mma_commit(cta.bar(DONE));
       }
       // every MMA issued (the items' and any an abort left behind) has completed before the
-      // accumulator is freed: one more commit, whose phase nothing else waits for
-      mma_commit(cta.bar(DONE));
-      mbar_wait(cta.bar(DONE), commits & 1, ctl, DRAIN_NS);
+      // accumulator is freed.  Its own barrier: one more phase of DONE could complete before a
+      // convert warp has seen the last item's, which would then look incomplete to it.
+      mma_commit(cta.bar(DRAIN));
+      mbar_wait(cta.bar(DRAIN), 0, ctl, DRAIN_NS);
     }
   } else {
     // ---- warps 0..3: in-place fp16 operands of chunk m, row i = token i of the chunk: k
