@@ -151,6 +151,22 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
   float* sa = (float*)(base + OFF_A);
   uint32_t* tmem_slot = (uint32_t*)(base + OFF_TMEM);
 
+  // the TMA copies of step c (chunk c0 + c) into ring stage c & 1 (the producer thread)
+  auto load_v = [&](int c) {
+    const uint32_t s = c & 1, st = cta.sb + s * STAGE;
+    mbar_arrive_expect_tx(cta.bar(V_FULL + s), V_BYTES);
+    for (int j = 0; j < 3; ++j)
+      tma_load_4d(st + OFF_V + j * V_BOX, &map_v, cta.bar(V_FULL + s), 64 * j, h, (c0 + c) * C, b);
+  };
+  auto load_qk = [&](int c) {
+    const uint32_t s = c & 1, st = cta.sb + s * STAGE;
+    mbar_arrive_expect_tx(cta.bar(QK_FULL + s), QK_BYTES);
+    for (int j = 0; j < 3; ++j) {
+      tma_load_4d(st + OFF_Q + j * Q_BOX, &map_q, cta.bar(QK_FULL + s), 32 * j, h, (c0 + c) * C, b);
+      tma_load_4d(st + OFF_K + j * Q_BOX, &map_k, cta.bar(QK_FULL + s), 32 * j, h, (c0 + c) * C, b);
+    }
+  };
+
   if (warp == MMA_WARP) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
@@ -178,6 +194,16 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
     }
     *cta.abort_flag() = 0;
     fence_barrier_init();
+    // the first tiles load while the CTA finishes setting up (the initialised barriers made
+    // visible to the async proxy first): v, q, k of step 0 and v of step 1 -- q, k of step 1
+    // go into the slot of step 0's state copy and wait for its Q''S (QK_EMPTY)
+    fence_proxy_async();
+    prefetch_tensormap(&map_q);
+    prefetch_tensormap(&map_k);
+    prefetch_tensormap(&map_v);
+    load_v(0);
+    load_qk(0);
+    if (n > 1) load_v(1);
   }
   if (tid < C) pw[tid] = expf((float)tid * gamma);  // lambda^d, d = 0..127
   if (tid < DK) sa[tid] = __ldg(aug + h * DK + tid);
@@ -189,25 +215,18 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
   if (warp == PRODUCER_WARP) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      prefetch_tensormap(&map_q);
-      prefetch_tensormap(&map_k);
-      prefetch_tensormap(&map_v);
       prefetch_tensormap(&map_o);
-      int armed_qk[2] = {0, 0}, armed_v[2] = {0, 0};
-      for (int c = 0; c < n; ++c) {  // c: step of this CTA, chunk c0 + c
-        const uint32_t s = c & 1, st = cta.sb + s * STAGE;
-        const int t0 = (c0 + c) * C;
-        if (c >= 2 && !wait(cta, cta.bar(V_EMPTY + s), ((c >> 1) - 1) & 1, ctl)) break;
-        mbar_arrive_expect_tx(cta.bar(V_FULL + s), V_BYTES);
-        for (int j = 0; j < 3; ++j)
-          tma_load_4d(st + OFF_V + j * V_BOX, &map_v, cta.bar(V_FULL + s), 64 * j, h, t0, b);
-        ++armed_v[s];
-        if (c >= 1 && !wait(cta, cta.bar(QK_EMPTY + s), ((c - 1) >> 1) & 1, ctl)) break;
-        mbar_arrive_expect_tx(cta.bar(QK_FULL + s), QK_BYTES);
-        for (int j = 0; j < 3; ++j) {
-          tma_load_4d(st + OFF_Q + j * Q_BOX, &map_q, cta.bar(QK_FULL + s), 32 * j, h, t0, b);
-          tma_load_4d(st + OFF_K + j * Q_BOX, &map_k, cta.bar(QK_FULL + s), 32 * j, h, t0, b);
+      // steps 0 (v, q, k) and 1 (v) were issued before the CTA's barrier
+      int armed_qk[2] = {1, 0}, armed_v[2] = {1, n > 1 ? 1 : 0};
+      for (int c = 1; c < n; ++c) {  // c: step of this CTA, chunk c0 + c
+        const uint32_t s = c & 1;
+        if (c >= 2) {
+          if (!wait(cta, cta.bar(V_EMPTY + s), ((c >> 1) - 1) & 1, ctl)) break;
+          load_v(c);
+          ++armed_v[s];
         }
+        if (!wait(cta, cta.bar(QK_EMPTY + s), ((c - 1) >> 1) & 1, ctl)) break;
+        load_qk(c);
         ++armed_qk[s];
       }
       // drain: every armed load has landed before the CTA may exit
