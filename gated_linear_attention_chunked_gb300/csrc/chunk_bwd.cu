@@ -836,6 +836,9 @@ bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
   const int bh = cut ? p.plan.whole + cut_idx / p.plan.parts : w;
   const int c0 = cut ? part_begin(part, nc, p.plan.parts) : 0;
   const int n = cut ? part_begin(part + 1, nc, p.plan.parts) - c0 : nc;
+  // the d_aug reduction, launched next as this grid's programmatic dependent, may start once
+  // every CTA has (it waits for this grid to finish)
+  griddep_launch_dependents();
   // a part starts from the states the segment passes leave: when this grid is launched as
   // their programmatic dependent it may be running before they finish (whole pairs need none)
   if (cut) griddep_wait();
@@ -850,25 +853,34 @@ bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                          map_dinit, ctl);
 }
 
-// d_aug[h, d] = sum over b of the per-(b, h) partial sums (a cut pair's: its parts' in order),
-// in order of b (deterministic).
-__global__ void reduce_daug_kernel(const float* __restrict__ part, const float* __restrict__ split,
-                                   float* __restrict__ d_aug, int B, int H, SplitPlan plan) {
-  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= H * DK) return;
+// d_aug[h, d] = sum over b of the per-(b, h) partial sums (a cut pair's: its parts' in order).
+// One warp per output: lane l adds b = l, l + 32, ... in order, then a fixed shuffle tree, whose
+// lane 0 writes (deterministic).  Launched as the chunked kernel's programmatic dependent, so its
+// launch overlaps that kernel's last wave; it waits for the kernel's partial sums.
+constexpr int RED_WARPS = 8;
+__global__ void __launch_bounds__(RED_WARPS * 32)
+reduce_daug_kernel(const float* __restrict__ part, const float* __restrict__ split,
+                   float* __restrict__ d_aug, int B, int H, SplitPlan plan) {
+  griddep_wait();
+  const int idx = blockIdx.x * RED_WARPS + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (idx >= H * DK) return;  // (a whole warp)
   const int h = idx / DK, d = idx % DK;
-  // whole pairs are b*H + h < whole: b < b_whole (a straight loop keeps the loads in flight)
+  // whole pairs are b*H + h < whole: b < b_whole
   const int b_whole = min(B, (plan.whole - h + H - 1) / H);
   float s = 0.f;
-#pragma unroll 8
-  for (int b = 0; b < b_whole; ++b) s += part[((size_t)b * H + h) * DK + d];
-  for (int b = b_whole; b < B; ++b) {
-    const size_t x = (size_t)b * H + h - plan.whole;
+  for (int b = lane; b < B; b += 32) {
     float t = 0.f;
-    for (int j = 0; j < plan.parts; ++j) t += split[(x * plan.parts + j) * DK + d];
+    if (b < b_whole) {
+      t = part[((size_t)b * H + h) * DK + d];
+    } else {
+      const size_t x = (size_t)b * H + h - plan.whole;
+      for (int j = 0; j < plan.parts; ++j) t += split[(x * plan.parts + j) * DK + d];
+    }
     s += t;
   }
-  d_aug[idx] = s;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+  if (lane == 0) d_aug[idx] = s;
 }
 
 }  // namespace
@@ -930,9 +942,9 @@ cudaError_t launch_chunk_bwd(const BwdArgs& a, DevCtl ctl, cudaStream_t stream) 
       return e;
   }
   const int n = a.H * DK;
-  reduce_daug_kernel<<<(n + 255) / 256, 256, 0, stream>>>(p.da_part, p.da_split, a.d_aug, a.B, a.H,
-                                                         p.plan);
-  return cudaGetLastError();
+  PdlLaunch R(dim3((n + RED_WARPS - 1) / RED_WARPS), dim3(RED_WARPS * 32), 0, stream, true);
+  return cudaLaunchKernelEx(&R.cfg, reduce_daug_kernel, (const float*)p.da_part,
+                            (const float*)p.da_split, a.d_aug, a.B, a.H, p.plan);
 }
 
 }  // namespace gla
