@@ -113,7 +113,8 @@ seg_sum_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant_
                float* __restrict__ adj, const float* __restrict__ init,
                const float* __restrict__ dfin, StatePages sp, int T, int H, int whole, int parts,
                int n_fwd, int n_items, int full, int fold, DevCtl ctl) {
-  // pass B may start (it waits for these sums), and with it the chunked kernel's whole pairs
+  // the next launch may start: pass B (which waits for these sums) or, with two parts, the
+  // chunked kernel, whose whole pairs need nothing from this pass
   griddep_launch_dependents();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   Cta cta;
