@@ -212,9 +212,9 @@ def job_rate(world, units_per_rank, seconds):
 def run_cpu_configs(args):
     """--cpu-configs: the fp64 oracle timed on this host's cores on every workload -- tiny
     fp32 fwd+bwd (whole), the layer forward B=8 (whole), the training fwd+bwd B=32 (whole),
-    the decode step (every 64th sequence of the pool, extrapolated) and the long prefill (the
-    first 65536 of 131072 tokens of both sequences).  One JSON line; the CPU baseline the
-    GPU numbers are reported beside."""
+    the decode step (every 64th sequence of the pool, extrapolated) and the long prefill
+    (whole: both sequences of 131072 tokens).  One JSON line; the CPU baseline the GPU numbers
+    are reported beside."""
     import numpy as np
 
     import oracle
@@ -246,8 +246,8 @@ def run_cpu_configs(args):
     st_rate, n_st, dt = oracle_decode_sample()
     out["decode_pool"] = dict(s=dt, states=n_st, steps=40, gbs=st_rate * DEC_BYTES_STATE / 1e9,
                               ms_per_step_extrapolated=1e3 * N_SEQ * N_LAYERS * H / st_rate)
-    rate, dt = oracle_long_prefill_sample()
-    out["long_prefill_fwd_sample"] = dict(s=dt, tokens=2 * 65536, tokens_per_s=rate)
+    rate, dt = oracle_long_prefill_sample(t_sample=131072)
+    out["long_prefill_fwd"] = dict(s=dt, tokens=2 * 131072, tokens_per_s=rate)
     print(json.dumps(out), flush=True)
     return 0
 
