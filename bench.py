@@ -807,6 +807,87 @@ def run_paged_decode(args):
     return 0
 
 
+def run_shard(args):
+    """--part shard: what one rank runs when the long prefill (B=2, T=--long-t, H=16, bf16,
+    initial state) is cut into R consecutive slices across R GPUs (--shard-ranks), measured on
+    this GPU: the slice's state sum, the link of the gathered sums into the state entering the
+    slice, the forward on the slice; then the adjoint sum, the reverse link and the backward.
+    The last rank is timed (its forward link walks every slice before it).  The all-gather of
+    the sums between those steps (B*H*73,728 B per rank each way) and the all-reduce of d_aug
+    are not run: one GPU, so no multi-GPU time exists; the gathered sums are stand-ins of the
+    right shape."""
+    import torch
+    import gated_linear_attention_chunked_gb300 as gla
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    gla.load()
+    R, Bl, Tl = args.shard_ranks, 2, args.long_t
+    if R < 2 or Tl % R:
+        raise SystemExit("--shard-ranks must be >= 2 and divide --long-t")
+    Ts, r = Tl // R, R - 1
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(4322)
+    rn = lambda *sh, std=1.0: torch.randn(*sh, generator=gen, device=dev) * std
+    q = rn(Bl, Ts, H, DK, std=DK ** -0.5).bfloat16()
+    k = rn(Bl, Ts, H, DK).bfloat16()
+    v = rn(Bl, Ts, H, DV).bfloat16()
+    dO = rn(Bl, Ts, H, DV).bfloat16()
+    init = rn(Bl, H, DK, DV, std=0.01)
+    dfin = rn(Bl, H, DK, DV, std=0.01)
+    a = rn(H, DK, std=0.02)
+    gam = gla.decay_schedule(H).to(dev)
+    U_all = rn(R, Bl, H, DK, DV, std=0.01)   # the all-gather's result (stand-ins)
+    Ua_all = rn(R, Bl, H, DK, DV, std=0.01)
+    lens = [Ts] * R
+    s_in = torch.empty(Bl, H, DK, DV, device=dev)
+    a_out = torch.empty(Bl, H, DK, DV, device=dev)
+    o = torch.empty(Bl, Ts, H, DV, device=dev)
+    fin = torch.empty(Bl, H, DK, DV, device=dev)
+    gate = torch.empty(Bl, H, Ts, device=dev)
+    ws_f = torch.empty(max(gla.chunk_fwd_workspace_size(Bl, Ts, H, gla.GLA_BF16), 256),
+                       dtype=torch.uint8, device=dev)
+    ws_b = torch.empty(max(gla.chunk_bwd_workspace_size(Bl, Ts, H, gla.GLA_BF16), 256),
+                       dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    steps = {
+        "fwd_state_sum": lambda: gla.chunk_state_sum(k, v, gam, out=U_all[r]),
+        "fwd_link": lambda: gla.state_link(U_all, lens, r, gam, init, out=s_in),
+        "fwd_slice": lambda: gla.chunk_fwd(q, k, v, gam, a, s_in, out=o, final_state=fin,
+                                           gate=gate, workspace=ws_f),
+        "bwd_adjoint_sum": lambda: gla.chunk_adjoint_sum(q, dO, gam, out=Ua_all[r]),
+        "bwd_link": lambda: gla.state_link(Ua_all, lens, r, gam, dfin, reverse=True, out=a_out),
+        "bwd_slice": lambda: gla.chunk_bwd(q, k, v, gam, a, dO, s_in, a_out, gate=gate,
+                                           workspace=ws_b),
+    }
+    n = max(args.steps, 10)
+    ms = {}
+    for name, fn in steps.items():
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms[name] = e0.elapsed_time(e1) / n
+    if gla.get_device_error() != 0:
+        raise RuntimeError("device error in the sharded steps")
+    f_ms = ms["fwd_state_sum"] + ms["fwd_link"] + ms["fwd_slice"]
+    b_ms = ms["bwd_adjoint_sum"] + ms["bwd_link"] + ms["bwd_slice"]
+    print(json.dumps(dict(
+        part="shard", workload=f"long prefill B={Bl} T={Tl} H={H} bf16 cut into {R} slices of "
+        f"{Ts} tokens, one per rank; rank {r} timed on one GPU without the exchange",
+        ranks=R, slice_tokens=Ts, ms=ms, fwd_rank_ms=f_ms, bwd_rank_ms=b_ms,
+        exchange_bytes_per_rank=Bl * H * DK * DV * 4,
+        fwd_tokens_per_s_all_ranks_without_exchange=R * Bl * Ts / (f_ms * 1e-3),
+        bwd_tokens_per_s_all_ranks_without_exchange=R * Bl * Ts / (b_ms * 1e-3),
+        note="unmeasured: the all-gather and the d_aug all-reduce (one GPU per run)")),
+        flush=True)
+    return 0
+
+
 def run_long_prefill(args):
     """--part long: the long-context prefill forward (B=2, T=131072, H=16, bf16, initial state
     ~ N(0, 0.01)), through the public API with its workspace (pairs cut into parts) and, for
@@ -946,12 +1027,14 @@ def main():
                     help="time the fp64 CPU oracle on every workload (no GPU work)")
     ap.add_argument("--cpu-seqs", type=int, default=32,
                     help="sequences of the training workload the CPU oracle baseline times")
-    ap.add_argument("--part", choices=["all", "fwd", "bwd", "decode", "long", "paged", "norm", "conv", "fused"], default="all",
+    ap.add_argument("--part", choices=["all", "fwd", "bwd", "decode", "long", "paged", "norm", "conv", "fused", "shard"], default="all",
                     help="time one call alone (smaller profiling cases); the default is the "
                          "whole hot path")
     ap.add_argument("--batch", type=int, default=B, help="sequences of the training shape")
     ap.add_argument("--n-seq", type=int, default=N_SEQ, help="sequences of the serving pool")
-    ap.add_argument("--long-t", type=int, default=131072, help="tokens of the long prefill (--part long)")
+    ap.add_argument("--long-t", type=int, default=131072, help="tokens of the long prefill (--part long, shard)")
+    ap.add_argument("--shard-ranks", type=int, default=8,
+                    help="--part shard: ranks the long prefill is cut across (one slice each)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -979,6 +1062,8 @@ def main():
         return run_conv(args) if rank == 0 else 0
     if args.part == "fused":
         return run_fused(args) if rank == 0 else 0
+    if args.part == "shard":
+        return run_shard(args) if rank == 0 else 0
     return run_gpu(args, rank, world, local_rank)
 
 

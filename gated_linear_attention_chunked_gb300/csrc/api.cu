@@ -423,8 +423,8 @@ gla_status gla_chunk_state_sum(const void* k, const void* v, gla_dtype in_dtype,
     return GLA_ERR_ALIGNMENT;
   gla::DevCtl ctl;
   if ((st = ctl_for_current_device(&ctl)) != GLA_OK) return st;
-  return gla::launch_slice_sums(k, v, in_dtype == GLA_BF16, false, log_decay, U, B, T, H, ctl,
-                                stream) == cudaSuccess
+  return gla::launch_slice_sums(k, v, in_dtype == GLA_BF16, false, log_decay, U, B, T, H,
+                                sm_count(), ctl, stream) == cudaSuccess
              ? GLA_OK
              : GLA_ERR_CUDA;
 }
@@ -440,8 +440,8 @@ gla_status gla_chunk_adjoint_sum(const void* q, const void* dO, gla_dtype in_dty
     return GLA_ERR_ALIGNMENT;
   gla::DevCtl ctl;
   if ((st = ctl_for_current_device(&ctl)) != GLA_OK) return st;
-  return gla::launch_slice_sums(q, dO, in_dtype == GLA_BF16, true, log_decay, U, B, T, H, ctl,
-                                stream) == cudaSuccess
+  return gla::launch_slice_sums(q, dO, in_dtype == GLA_BF16, true, log_decay, U, B, T, H,
+                                sm_count(), ctl, stream) == cudaSuccess
              ? GLA_OK
              : GLA_ERR_CUDA;
 }

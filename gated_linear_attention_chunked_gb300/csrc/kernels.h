@@ -206,8 +206,8 @@ struct ShardLens {
   int len[kMaxShards];
 };
 cudaError_t launch_slice_sums(const void* a, const void* b, bool bf16, bool reverse,
-                              const float* log_decay, float* out, int B, int T, int H, DevCtl ctl,
-                              cudaStream_t stream);
+                              const float* log_decay, float* out, int B, int T, int H, int n_sm,
+                              DevCtl ctl, cudaStream_t stream);
 cudaError_t launch_shard_link(const float* U, const ShardLens& lens, int rank, bool reverse,
                               const float* log_decay, const float* boundary, float* out, int B,
                               int H, cudaStream_t stream);

@@ -77,19 +77,21 @@ __device__ __forceinline__ uint32_t v_chunk(uint32_t i, int cc) {
 // x = it / (p-1), into states[x*p + j + 1]; it >= n_fwd the reverse sum U'_j of part
 // j = 1 + it' % (p-1) (it' = it - n_fwd), into adj[x*p + j - 1].  Those slots are then
 // completed by pass B in place -- or, with two parts (`fold`), by the item itself.
-// full != 0 (a sequence-sharded call's slice sums): one item per pair bh, its one part being
-// the whole sequence; item it < n_fwd writes U of pair it into states[it], it >= n_fwd U' of
-// pair it - n_fwd into adj[it - n_fwd].
+// full != 0 (a sequence-sharded call's slice sums): ncol items per pair bh, its one part being
+// the whole sequence and item `nb` of the pair summing value columns [nb*192/ncol, ...) only
+// (ncol = 1 or 3: a third is one 64-column v box); items it < n_fwd write U of pair it / ncol
+// into states, it >= n_fwd U' of pair (it - n_fwd) / ncol into adj.
 struct SumItem {
   bool rev;
-  int x, j, bh, b, h, c_lo, c_hi;
+  int x, j, nb, bh, b, h, c_lo, c_hi;
 };
-__device__ __forceinline__ SumItem sum_item(int it, int n_fwd, int full, int whole, int parts,
-                                            int H, int nc) {
+__device__ __forceinline__ SumItem sum_item(int it, int n_fwd, int full, int ncol, int whole,
+                                            int parts, int H, int nc) {
   SumItem I;
   I.rev = it >= n_fwd;
   const int idx = I.rev ? it - n_fwd : it;
-  I.x = full ? idx : idx / (parts - 1);
+  I.x = full ? idx / ncol : idx / (parts - 1);
+  I.nb = full ? idx % ncol : 0;
   I.j = full ? 0 : idx % (parts - 1) + (I.rev ? 1 : 0);
   I.bh = whole + I.x;
   I.b = I.bh / H;
@@ -112,7 +114,7 @@ seg_sum_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant_
                const float* __restrict__ log_decay, float* __restrict__ states,
                float* __restrict__ adj, const float* __restrict__ init,
                const float* __restrict__ dfin, StatePages sp, int T, int H, int whole, int parts,
-               int n_fwd, int n_items, int full, int fold, DevCtl ctl) {
+               int n_fwd, int n_items, int full, int ncol, int fold, DevCtl ctl) {
   // the next launch may start: pass B (which waits for these sums) or, with two parts, the
   // chunked kernel, whose whole pairs need nothing from this pass
   griddep_launch_dependents();
@@ -160,20 +162,22 @@ seg_sum_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant_
       bool ok = true;
       int g = 0;
       for (int it = it0; it < n_items && ok; it += it_step) {
-        const SumItem I = sum_item(it, n_fwd, full, whole, parts, H, nc);
+        const SumItem I = sum_item(it, n_fwd, full, ncol, whole, parts, H, nc);
         const CUtensorMap* map_a = I.rev ? &map_q : &map_k;
         const CUtensorMap* map_b = I.rev ? &map_g : &map_v;
         for (int m = 0; m < I.c_hi - I.c_lo; ++m, ++g) {
           const int s = g % STAGES;
           if (g >= STAGES && !(ok = wait(cta, cta.bar(EMPTY + s), (g / STAGES - 1) & 1, ctl)))
             break;
-          mbar_arrive_expect_tx(cta.bar(FULL + s), STAGE);
+          // k (q) whole; v (dO) whole, or the one 64-column box of this item's column third
+          mbar_arrive_expect_tx(cta.bar(FULL + s), 3 * K_BOX + (ncol == 3 ? 1 : 3) * V_BOX);
           const int t0 = (I.c_lo + m) * C;
           const uint32_t st = sb + s * STAGE;
           for (int jb = 0; jb < 3; ++jb) {
             tma_load_4d(st + jb * K_BOX, map_a, cta.bar(FULL + s), 32 * jb, I.h, t0, I.b);
-            tma_load_4d(st + 3 * K_BOX + jb * V_BOX, map_b, cta.bar(FULL + s), 64 * jb, I.h, t0,
-                        I.b);
+            if (ncol == 1 || jb == 0)
+              tma_load_4d(st + 3 * K_BOX + jb * V_BOX, map_b, cta.bar(FULL + s),
+                          64 * (ncol == 3 ? I.nb : jb), I.h, t0, I.b);
           }
           armed0 += s == 0;
           armed1 += s == 1;
@@ -191,11 +195,13 @@ seg_sum_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant_
       // instruction: A = k (q) tile as [token][channel] (MN-major), B = v (dO) tile likewise.
       // One DONE phase per item; the next item's first MMA overwrites the accumulator, which
       // the convert warps have read out before they release that item's first stage (CONV).
-      constexpr uint32_t ID = idesc_f16(128, 192, false, false, true, true);
+      constexpr uint32_t ID192 = idesc_f16(128, 192, false, false, true, true);
+      constexpr uint32_t ID64 = idesc_f16(128, 64, false, false, true, true);
+      const uint32_t ID = ncol == 3 ? ID64 : ID192;
       bool ok = true;
       int g = 0, k = 0;
       for (int it = it0; it < n_items && ok; it += it_step, ++k) {
-        const SumItem I = sum_item(it, n_fwd, full, whole, parts, H, nc);
+        const SumItem I = sum_item(it, n_fwd, full, ncol, whole, parts, H, nc);
         for (int m = 0; m < I.c_hi - I.c_lo; ++m, ++g) {
           const int s = g % STAGES;
           if (g == ctl.stall_step) {  // the give-up path's diagnostic (see the chunk kernels):
@@ -234,7 +240,7 @@ seg_sum_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant_
     bool ok = true;
     int g = 0, k = 0;
     for (int it = it0; it < n_items && ok; it += it_step, ++k) {
-      const SumItem I = sum_item(it, n_fwd, full, whole, parts, H, nc);
+      const SumItem I = sum_item(it, n_fwd, full, ncol, whole, parts, H, nc);
       const int M = I.c_hi - I.c_lo;  // chunks of the part (>= 1)
       // tokens of the part, and of its last chunk (C unless it is the sequence's ragged one)
       const int len = min(I.c_hi * C, T) - I.c_lo * C;
@@ -255,7 +261,10 @@ seg_sum_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant_
                                              : expf(gamma * (float)(C * (M - 2 - m) + last_len)) *
                                                    row_w);
         convert_row<BF16, 12>(st, [&](int cc) { return k_chunk(i, cc); }, sk, vmax);
-        convert_row<BF16, 24>(st, [&](int cc) { return v_chunk(i, cc); }, 1.f, vmax);
+        if (ncol == 3)
+          convert_row<BF16, 8>(st, [&](int cc) { return v_chunk(i, cc); }, 1.f, vmax);
+        else
+          convert_row<BF16, 24>(st, [&](int cc) { return v_chunk(i, cc); }, 1.f, vmax);
         fence_proxy_async();
         tc_fence_before();  // (the previous item's TMEM loads come before this stage's MMAs)
         mbar_arrive(cta.bar(CONV + s));
@@ -268,7 +277,8 @@ seg_sum_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant_
         float* const out = I.rev ? adj : states;
         const long long slot =
             full ? (long long)I.x : (long long)I.x * parts + (I.rev ? I.j - 1 : I.j + 1);
-        float* dst = out + (size_t)slot * DK * DV + (size_t)i * DV;
+        const int ncols = DV / ncol;  // this item's value columns, from column ncols * nb
+        float* dst = out + (size_t)slot * DK * DV + (size_t)i * DV + (size_t)ncols * I.nb;
         // fold: the boundary row (the pair's initial state or d_final_state; null = zeros),
         // its slot, and lambda^(tokens of this part)
         const float* bnd = nullptr;
@@ -291,7 +301,7 @@ seg_sum_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant_
           }
         }
 #pragma unroll 1
-        for (int cb = 0; cb < DV / 32; ++cb) {
+        for (int cb = 0; cb < ncols / 32; ++cb) {
           uint32_t r[32];
           tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16) + 32 * cb, r);
           tmem_wait_ld();
@@ -571,7 +581,7 @@ cudaError_t launch_segment_states(const void* q, const void* k, const void* v, c
         plan.pass_ctas > 0 && plan.pass_ctas < n_items ? plan.pass_ctas : n_items;
     kern<<<(unsigned)grid, THREADS, SMEM_BYTES, stream>>>(
         mk, mv, mq, mg, log_decay, states, adj, init, dfin, sp, T, H, plan.whole, plan.parts,
-        (int)n_fwd, (int)n_items, 0, fold ? 1 : 0, ctl);
+        (int)n_fwd, (int)n_items, 0, 1, fold ? 1 : 0, ctl);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (fold) return cudaSuccess;
@@ -584,20 +594,24 @@ cudaError_t launch_segment_states(const void* q, const void* k, const void* v, c
 }
 
 cudaError_t launch_slice_sums(const void* a, const void* b, bool bf16, bool reverse,
-                              const float* log_decay, float* out, int B, int T, int H, DevCtl ctl,
-                              cudaStream_t stream) {
+                              const float* log_decay, float* out, int B, int T, int H, int n_sm,
+                              DevCtl ctl, cudaStream_t stream) {
   // a, b = k, v (forward: U of the slice) or q, dO (reverse: U' of the slice)
   CUtensorMap ma, mb;
   if (!make_tmap_seq_16bit(&ma, a, DK, H, T, B, 32, C, CU_TENSOR_MAP_SWIZZLE_64B, bf16) ||
       !make_tmap_seq_16bit(&mb, b, DV, H, T, B, 64, C, CU_TENSOR_MAP_SWIZZLE_128B, bf16))
     return cudaErrorInvalidValue;
   const long long n = (long long)B * H;
+  // fewer pairs than SMs: each pair's sum in three CTAs, one 64-column third of the value
+  // channels each (k is read three times; every CTA writes its own columns, so no workspace)
+  const int ncol = n < n_sm ? 3 : 1;
+  const long long items = n * ncol;
   auto kern = bf16 ? seg_sum_kernel<true> : seg_sum_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  kern<<<(unsigned)n, THREADS, SMEM_BYTES, stream>>>(
+  kern<<<(unsigned)items, THREADS, SMEM_BYTES, stream>>>(
       ma, mb, ma, mb, log_decay, reverse ? nullptr : out, reverse ? out : nullptr, nullptr,
-      nullptr, StatePages{}, T, H, 0, 2, reverse ? 0 : (int)n, (int)n, 1, 0, ctl);
+      nullptr, StatePages{}, T, H, 0, 2, reverse ? 0 : (int)items, (int)items, 1, ncol, 0, ctl);
   return cudaGetLastError();
 }
 

@@ -30,6 +30,8 @@ def env():
     (2, 300, 16, "bf16", 83),   # ragged last chunk, all decay tiers
     (1, 1, 4, "fp16", 84),      # a single token
     (2, 4000, 5, "fp16", 85),   # many chunks, ragged
+    (10, 256, 16, "bf16", 86),  # 160 pairs, not fewer than the SMs: one CTA per pair (fewer
+                                # pairs split each sum into three 64-column CTAs)
 ])
 def test_slice_sums_match_oracle(env, B, T, H, dtype, seed):
     import oracle
