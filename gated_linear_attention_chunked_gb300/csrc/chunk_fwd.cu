@@ -9,7 +9,8 @@
 // One CTA owns one (b, h) and walks its chunks in order; the fp32 state never leaves the chip.
 //   producer  TMA producer: q, k tiles (3 boxes of 32 channels, 64-byte swizzle) and v tiles
 //               (3 boxes of 64 channels, 128-byte swizzle) into a 2-stage ring (no L2
-//               prefetch: measured, it slowed the loads it was meant to hide).
+//               prefetch: measured, it slowed the loads it was meant to hide); the first
+//               tiles are issued by the thread that initialises the barriers, during setup.
 //   MMA warp  tcgen05 issuer (one thread) and TMEM owner (512 columns):
 //                 D_P [384,512)  P = Q K^T (bf16/fp16 inputs as given); the masked fp16
 //                                copy P'' is written back in place (64 columns) and read
