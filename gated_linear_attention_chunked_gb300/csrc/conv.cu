@@ -280,6 +280,7 @@ conv_bwd_kernel(const void* __restrict__ x, const float* __restrict__ w,
                 const float* __restrict__ bias, const float* __restrict__ init,
                 const float* __restrict__ dy, float* __restrict__ dx, float* __restrict__ dinit,
                 float* __restrict__ part, int T, int D) {
+  griddep_launch_dependents();  // the reduction launched next waits for this whole grid
   const int D4 = D / 4, d4 = blockIdx.y * THREADS + threadIdx.x;
   if (d4 >= D4) return;
   const int n_tiles = (T + TT - 1) / TT;
@@ -365,6 +366,7 @@ conv_bwd_staged_kernel(const void* __restrict__ x, const float* __restrict__ w,
                        const float* __restrict__ dy, float* __restrict__ dx,
                        float* __restrict__ dinit, float* __restrict__ part, int T, int D,
                        DevCtl ctl) {
+  griddep_launch_dependents();  // the reduction launched next waits for this whole grid
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr int ES = BF16 ? 2 : 4;
   constexpr uint32_t XROW = DC * ES, GROW = DC * 4, STAGE = SGB * (XROW + GROW);
@@ -497,16 +499,41 @@ conv_bwd_staged_kernel(const void* __restrict__ x, const float* __restrict__ w,
   }
 }
 
-// dw[d][j], db[d] = sums over the n_parts tiles, in order
-__global__ void conv_reduce_kernel(const float* __restrict__ part, float* __restrict__ dw,
-                                   float* __restrict__ db, int n_parts, int D) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;  // d * 5 + j
-  if (i >= D * 5) return;
+// dw[d][j], db[d] = sums over the n_parts tiles.  One CTA of RED_WARPS warps per 32
+// consecutive outputs i = d * 5 + j: warp w adds tiles w, w + RED_WARPS, ... in order (each
+// load a coalesced 128-byte row of the partial sums), then one thread per output adds the
+// warps' sums in order (a fixed order: deterministic).  Launched as the backward kernel's
+// programmatic dependent: it waits for that grid before reading the partial sums.
+constexpr int RED_WARPS = 32;
+__global__ void __launch_bounds__(RED_WARPS * 32)
+conv_reduce_kernel(const float* __restrict__ part, float* __restrict__ dw,
+                   float* __restrict__ db, int n_parts, int D) {
+  __shared__ float acc[RED_WARPS][33];
+  griddep_wait();
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int i = blockIdx.x * 32 + lane;  // d * 5 + j
+  const bool live = i < D * 5;
   float s = 0.f;
-  for (int q = 0; q < n_parts; ++q) s += part[(size_t)q * D * 5 + i];
-  const int d = i / 5, j = i % 5;
-  if (j < K) dw[d * K + j] = s;
-  else if (db) db[d] = s;
+  if (live) {
+#pragma unroll 8
+    for (int q = wid; q < n_parts; q += RED_WARPS) s += part[(size_t)q * D * 5 + i];
+  }
+  acc[wid][lane] = s;
+  __syncthreads();
+  if (wid == 0 && live) {
+    float t = 0.f;
+#pragma unroll 8
+    for (int w = 0; w < RED_WARPS; ++w) t += acc[w][lane];
+    const int d = i / 5, j = i % 5;
+    if (j < K) dw[d * K + j] = t;
+    else if (db) db[d] = t;
+  }
+}
+
+cudaError_t launch_conv_reduce(const float* part, float* dw, float* db, int n_parts, int D,
+                               cudaStream_t stream) {
+  PdlLaunch R(dim3((D * 5 + 31) / 32), dim3(RED_WARPS * 32), 0, stream, true);
+  return cudaLaunchKernelEx(&R.cfg, conv_reduce_kernel, part, dw, db, n_parts, D);
 }
 
 __global__ void __launch_bounds__(THREADS)
@@ -588,8 +615,7 @@ cudaError_t launch_conv_bwd(const void* x, bool bf16, const float* w, const floa
           x, w, bias, init, dy, dx, dinit, part, T, D, ctl);
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    conv_reduce_kernel<<<(D * 5 + 255) / 256, 256, 0, stream>>>(part, dw, db, B * n_tiles, D);
-    return cudaGetLastError();
+    return launch_conv_reduce(part, dw, db, B * n_tiles, D, stream);
   }
   const dim3 grid(B * n_tiles, (D / 4 + THREADS - 1) / THREADS);
   if (bf16)
@@ -599,8 +625,7 @@ cudaError_t launch_conv_bwd(const void* x, bool bf16, const float* w, const floa
                                                           D);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  conv_reduce_kernel<<<(D * 5 + 255) / 256, 256, 0, stream>>>(part, dw, db, B * n_tiles, D);
-  return cudaGetLastError();
+  return launch_conv_reduce(part, dw, db, B * n_tiles, D, stream);
 }
 
 cudaError_t launch_conv_decode(float* state, const float* x, const float* w, const float* bias,
