@@ -107,6 +107,7 @@ head_norm_bwd_kernel(const float* __restrict__ dy, const float* __restrict__ o,
                      const void* __restrict__ g, const float* __restrict__ w,
                      float* __restrict__ d_o, float* __restrict__ dg, float* __restrict__ part,
                      long long rows, int H, int heads_per_tier, int n_tiers, float eps) {
+  griddep_launch_dependents();  // the dw reduction launched next waits for this whole grid
   __shared__ float4 sacc[ROWS_PER_CTA][C4];
   __shared__ int stier[ROWS_PER_CTA];
   const int lane = threadIdx.x % LANES, hw = threadIdx.x / LANES;
@@ -183,14 +184,31 @@ head_norm_bwd_kernel(const float* __restrict__ dy, const float* __restrict__ o,
   }
 }
 
-// dw[i] = sum over CTAs b, in order, of part[b][i]
-__global__ void head_norm_dw_reduce(const float* __restrict__ part, float* __restrict__ dw,
-                                    int n_parts, int n) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= n) return;
+// dw[i] = sum over the CTAs' partial sums part[b][i].  One CTA of RED_WARPS warps per 32
+// consecutive outputs: warp w adds b = w, w + RED_WARPS, ... in order (coalesced rows), then
+// one thread per output adds the warps' sums in order (a fixed order: deterministic).
+// Launched as the backward kernel's programmatic dependent: it waits for that grid first.
+constexpr int RED_WARPS = 32;
+__global__ void __launch_bounds__(RED_WARPS * 32)
+head_norm_dw_reduce(const float* __restrict__ part, float* __restrict__ dw, int n_parts, int n) {
+  __shared__ float acc[RED_WARPS][33];
+  griddep_wait();
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int i = blockIdx.x * 32 + lane;
+  const bool live = i < n;
   float s = 0.f;
-  for (int b = 0; b < n_parts; ++b) s += part[(size_t)b * n + i];
-  dw[i] = s;
+  if (live) {
+#pragma unroll 8
+    for (int b = wid; b < n_parts; b += RED_WARPS) s += part[(size_t)b * n + i];
+  }
+  acc[wid][lane] = s;
+  __syncthreads();
+  if (wid == 0 && live) {
+    float t = 0.f;
+#pragma unroll 8
+    for (int w = 0; w < RED_WARPS; ++w) t += acc[w][lane];
+    dw[i] = t;
+  }
 }
 
 // CTAs for `rows` rows: at most 8 per SM, and a multiple of H / gcd(16, H) so that the grid
@@ -241,8 +259,8 @@ cudaError_t launch_head_norm_bwd(const float* dy, const float* o, const void* g,
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int n = n_tiers * C;
-  head_norm_dw_reduce<<<(n + 127) / 128, 128, 0, stream>>>(part, dw, grid, n);
-  return cudaGetLastError();
+  PdlLaunch R(dim3((n + 31) / 32), dim3(RED_WARPS * 32), 0, stream, true);
+  return cudaLaunchKernelEx(&R.cfg, head_norm_dw_reduce, (const float*)part, dw, grid, n);
 }
 
 }  // namespace gla
