@@ -361,6 +361,27 @@ __device__ __forceinline__ void link_one(const float* __restrict__ init,
   };
   float4* out = reinterpret_cast<float4*>(slots) + (size_t)x * parts * N4 + e;
   float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+  // the steps in order, their sums loaded LB at a time ahead of the chain (each slot is read
+  // before the step that overwrites it)
+  constexpr int LB = 4;
+  auto walk = [&](int first, int n_steps, int dir, int tok_off) {
+    for (int q0 = 0; q0 < n_steps; q0 += LB) {
+      float4 u[LB];
+#pragma unroll
+      for (int q = 0; q < LB; ++q)
+        if (q0 + q < n_steps) u[q] = out[(size_t)(first + dir * (q0 + q)) * N4];
+#pragma unroll
+      for (int q = 0; q < LB; ++q) {
+        if (q0 + q < n_steps) {
+          const int j = first + dir * (q0 + q);
+          const float lam = expf(gamma * (float)tokens(j + tok_off));
+          s = make_float4(fmaf(lam, s.x, u[q].x), fmaf(lam, s.y, u[q].y), fmaf(lam, s.z, u[q].z),
+                          fmaf(lam, s.w, u[q].w));
+          out[(size_t)j * N4] = s;
+        }
+      }
+    }
+  };
   if (!rev) {
     long long zi = bh;  // slot of the caller's initial state: [b][h] or a pool page
     if (sp.init_paged) {
@@ -369,23 +390,11 @@ __device__ __forceinline__ void link_one(const float* __restrict__ init,
     }
     if (init && zi >= 0) s = __ldg(reinterpret_cast<const float4*>(init) + (size_t)zi * N4 + e);
     out[0] = s;
-    for (int j = 1; j < parts; ++j) {
-      const float lam = expf(gamma * (float)tokens(j - 1));
-      const float4 u = out[(size_t)j * N4];
-      s = make_float4(fmaf(lam, s.x, u.x), fmaf(lam, s.y, u.y), fmaf(lam, s.z, u.z),
-                      fmaf(lam, s.w, u.w));
-      out[(size_t)j * N4] = s;
-    }
+    walk(1, parts - 1, 1, -1);  // j = 1 .. p-1: S_j = lambda^(L_{j-1}) S_{j-1} + U_{j-1}
   } else {
     if (dfin) s = __ldg(reinterpret_cast<const float4*>(dfin) + (size_t)bh * N4 + e);
     out[(size_t)(parts - 1) * N4] = s;
-    for (int j = parts - 2; j >= 0; --j) {
-      const float lam = expf(gamma * (float)tokens(j + 1));
-      const float4 u = out[(size_t)j * N4];
-      s = make_float4(fmaf(lam, s.x, u.x), fmaf(lam, s.y, u.y), fmaf(lam, s.z, u.z),
-                      fmaf(lam, s.w, u.w));
-      out[(size_t)j * N4] = s;
-    }
+    walk(parts - 2, parts - 1, -1, 1);  // j = p-2 .. 0: A_j = lambda^(L_{j+1}) A_{j+1} + U'_{j+1}
   }
 }
 
