@@ -199,6 +199,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
     // visible to the async proxy first): v, q, k of step 0 and v of step 1 -- q, k of step 1
     // go into the slot of step 0's state copy and wait for its Q''S (QK_EMPTY)
     fence_proxy_async();
+    // a part's starting state (72 KB, read twice by the emit warps) starts on its way to L2
+    if (cut) bulk_prefetch_l2(seg_init + (size_t)cut_idx * DK * DV, DK * DV * sizeof(float));
     prefetch_tensormap(&map_q);
     prefetch_tensormap(&map_k);
     prefetch_tensormap(&map_v);
