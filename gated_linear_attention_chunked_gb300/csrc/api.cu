@@ -88,7 +88,8 @@ gla::SplitPlan split_plan(int B, int T, int H, int roles, int n_sm, int pass_dir
 size_t split_bytes(int B, int H, const gla::SplitPlan& plan, bool bwd) {
   const long long slots = gla::split_slots((long long)B * H, plan);
   if (!slots) return 0;
-  if (!bwd) return round256((size_t)slots * kStateBytes);
+  // (the forward: the states, then with two parts each state's row-group maxima)
+  if (!bwd) return round256((size_t)slots * kStateBytes) + round256((size_t)slots * 4 * 4);
   return 2 * round256((size_t)slots * kStateBytes) + round256((size_t)slots * gla::kDK * 4);
 }
 
@@ -146,10 +147,16 @@ gla_status chunk_fwd_impl(const void* q, const void* k, const void* v, gla_dtype
     // the segment passes; with plan.overlap the chunked kernel, launched as their programmatic
     // dependent, runs its whole pairs beside them
     float* states = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + round256(must));
+    float* maxes = plan.parts == 2
+                       ? reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(states) +
+                                                  round256((size_t)gla::split_slots((long long)B * H, plan) *
+                                                           kStateBytes))
+                       : nullptr;
     a.seg_init = states;
+    a.seg_max = maxes;
     if (gla::launch_segment_states(nullptr, a.k, a.v, nullptr, a.bf16, log_decay, init_state,
-                                   nullptr, sp, states, nullptr, B, T, H, plan, ctl,
-                                   stream) != cudaSuccess)
+                                   nullptr, sp, states, nullptr, B, T, H, plan, ctl, stream,
+                                   maxes) != cudaSuccess)
       return GLA_ERR_CUDA;
   }
   return gla::launch_chunk_fwd(a, ctl, stream) == cudaSuccess ? GLA_OK : GLA_ERR_CUDA;

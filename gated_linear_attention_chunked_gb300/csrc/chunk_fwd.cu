@@ -114,7 +114,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
            const __grid_constant__ CUtensorMap map_fin, const float* __restrict__ log_decay,
            const float* __restrict__ aug, const float* __restrict__ init, float* __restrict__ out,
            float* __restrict__ fin, int T, int H, SplitPlan plan,
-           const float* __restrict__ seg_init, StatePages sp,
+           const float* __restrict__ seg_init, const float* __restrict__ seg_max, StatePages sp,
            const __grid_constant__ CUtensorMap map_y, OutGate og, float* __restrict__ gate_out,
            SavedStates saved, DevCtl ctl) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -575,7 +575,13 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
     // the final state is this CTA's to write if it ends the sequence
     const bool ends_seq = !cut || part == plan.parts - 1;
     int e_cur = 0;
-    {
+    bool ok = true;
+    if (cut && seg_max) {
+      // the sum pass left this part's max |state| (its three 32-row groups): the same exponent
+      // without a pass over the state or the exchange
+      const float* pm = seg_max + (size_t)cut_idx * 4;
+      e_cur = state_exponent(fmaxf(fmaxf(__ldg(pm), __ldg(pm + 1)), __ldg(pm + 2)));
+    } else {
       float m = 0.f;
       if (g_row0) {
         const float4* g4 = reinterpret_cast<const float4*>(g_row0 + 96 * hf);
@@ -589,10 +595,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
       for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
       if (lane == 0) red[16 + ew] = m;
       mbar_arrive(cta.bar(RED));
+      ok = wait_warp(cta, cta.bar(RED), 0, ctl);
+      if (ok) e_cur = state_exponent(red_max(2));
     }
-    bool ok = wait_warp(cta, cta.bar(RED), 0, ctl);
     if (ok) {
-      e_cur = state_exponent(red_max(2));
       if (e_cur < 0) {
         bad = true;
         e_cur = 0;
@@ -786,8 +792,8 @@ cudaError_t launch_chunk_fwd(const FwdArgs& a, DevCtl ctl, cudaStream_t stream) 
   // start beside the passes, its parts wait for them (griddep_wait)
   PdlLaunch L(dim3((unsigned)grid), dim3(threads), SMEM_BYTES, stream, plan.overlap);
   return cudaLaunchKernelEx(&L.cfg, kern, mq, mk, mv, mo, mfin, a.log_decay, a.aug, a.init, a.o,
-                            a.fin, a.T, a.H, plan, a.seg_init, a.sp, my, a.og, a.gate, a.saved,
-                            ctl);
+                            a.fin, a.T, a.H, plan, a.seg_init, plan.parts == 2 ? a.seg_max : nullptr,
+                            a.sp, my, a.og, a.gate, a.saved, ctl);
 }
 
 }  // namespace gla

@@ -128,6 +128,9 @@ struct FwdArgs {
   // cut pairs: [(BH - whole) * parts][96][192], slot x*parts + j = the state entering part j
   // of cut pair x (filled by the segment passes; slot x*parts is the pair's initial state)
   const float* seg_init = nullptr;
+  // with two parts: per part slot, the three row groups' max |state| of its starting state,
+  // [slot][4] (written by the sum pass; null: the kernel finds the max itself)
+  const float* seg_max = nullptr;
   StatePages sp;  // with sp.page: init and fin are the pool (see StatePages)
   OutGate og;     // with og.g: the fused output epilogue (o written only if og.want_o)
   float* gate = nullptr;  // [B,H,T] or null: sigmoid(z) per head and token, written
@@ -188,11 +191,13 @@ long long split_slots(long long BH, const SplitPlan& p);
 // plan.overlap pass B is pass A's programmatic dependent and runs on at most 16 CTAs (which
 // wait beside pass A's), so that the chunked kernel launched next as its dependent can start
 // its whole pairs at once; pass A runs on plan.pass_ctas CTAs.
+// state_max (forward direction, two parts only, may be null): [slot][4] receives the max
+// |state| of each starting state's three 32-row groups.
 cudaError_t launch_segment_states(const void* q, const void* k, const void* v, const void* dO,
                                   bool bf16, const float* log_decay, const float* init,
                                   const float* dfin, const StatePages& sp, float* states,
                                   float* adj, int B, int T, int H, const SplitPlan& plan,
-                                  DevCtl ctl, cudaStream_t stream);
+                                  DevCtl ctl, cudaStream_t stream, float* state_max = nullptr);
 
 // ---- sequence-sharded calls (seg_scan.cu): a sequence cut into consecutive slices, one per
 // rank.  launch_slice_sums: per (b, h) of this rank's slice of T tokens, U = sum_t

@@ -106,15 +106,18 @@ __device__ __forceinline__ SumItem sum_item(int it, int n_fwd, int full, int nco
 // fold (two parts, not full): the item also applies its pair's one recurrence step, as pass B
 // would: forward, states[x*2] = S_0 (the caller's initial state, its pool page or zeros) and
 // states[x*2 + 1] = lambda^(L_0) S_0 + U_0; reverse, adj[x*2 + 1] = A_1 (d_final_state or
-// zeros) and adj[x*2] = lambda^(L_1) A_1 + U'_1.
+// zeros) and adj[x*2] = lambda^(L_1) A_1 + U'_1; and, given state_max, each forward slot's
+// three 32-row groups' max |state| into state_max[slot][0..2] (one per epilogue warp, so no
+// warp waits on another).
 template <bool BF16>
 __global__ void __launch_bounds__(THREADS, 1)
 seg_sum_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
                const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_g,
                const float* __restrict__ log_decay, float* __restrict__ states,
                float* __restrict__ adj, const float* __restrict__ init,
-               const float* __restrict__ dfin, StatePages sp, int T, int H, int whole, int parts,
-               int n_fwd, int n_items, int full, int ncol, int fold, DevCtl ctl) {
+               const float* __restrict__ dfin, StatePages sp, float* __restrict__ state_max,
+               int T, int H, int whole, int parts, int n_fwd, int n_items, int full, int ncol,
+               int fold, DevCtl ctl) {
   // the next launch may start: pass B (which waits for these sums) or, with two parts, the
   // chunked kernel, whose whole pairs need nothing from this pass
   griddep_launch_dependents();
@@ -300,6 +303,7 @@ seg_sum_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant_
             if (init && zi >= 0) bnd = init + ((size_t)zi * DK + i) * DV;
           }
         }
+        float m0 = 0.f, m1 = 0.f;  // max |S_0|, |S_1| over this thread's row (forward fold)
 #pragma unroll 1
         for (int cb = 0; cb < ncols / 32; ++cb) {
           uint32_t r[32];
@@ -316,8 +320,21 @@ seg_sum_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant_
               *reinterpret_cast<float4*>(dst0 + 32 * cb + jj) = b4;
               u = make_float4(fmaf(lam, b4.x, u.x), fmaf(lam, b4.y, u.y), fmaf(lam, b4.z, u.z),
                               fmaf(lam, b4.w, u.w));
+              m0 = fmaxf(m0, fmaxf(fmaxf(fabsf(b4.x), fabsf(b4.y)), fmaxf(fabsf(b4.z), fabsf(b4.w))));
+              m1 = fmaxf(m1, fmaxf(fmaxf(fabsf(u.x), fabsf(u.y)), fmaxf(fabsf(u.z), fabsf(u.w))));
             }
             *reinterpret_cast<float4*>(dst + 32 * cb + jj) = u;
+          }
+        }
+        if (fold && !I.rev && state_max) {  // the row group's maxima of both starting states
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) {
+            m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, off));
+            m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, off));
+          }
+          if (lane == 0) {
+            state_max[((size_t)I.x * parts + 0) * 4 + warp] = m0;
+            state_max[((size_t)I.x * parts + 1) * 4 + warp] = m1;
           }
         }
       }
@@ -562,7 +579,7 @@ cudaError_t launch_segment_states(const void* q, const void* k, const void* v, c
                                   bool bf16, const float* log_decay, const float* init,
                                   const float* dfin, const StatePages& sp, float* states,
                                   float* adj, int B, int T, int H, const SplitPlan& plan,
-                                  DevCtl ctl, cudaStream_t stream) {
+                                  DevCtl ctl, cudaStream_t stream, float* state_max) {
   const long long X = (long long)B * H - plan.whole;
   if (plan.parts <= 1 || X <= 0) return cudaSuccess;
   CUtensorMap mk, mv, mq, mg;
@@ -589,8 +606,8 @@ cudaError_t launch_segment_states(const void* q, const void* k, const void* v, c
     const long long grid =
         plan.pass_ctas > 0 && plan.pass_ctas < n_items ? plan.pass_ctas : n_items;
     kern<<<(unsigned)grid, THREADS, SMEM_BYTES, stream>>>(
-        mk, mv, mq, mg, log_decay, states, adj, init, dfin, sp, T, H, plan.whole, plan.parts,
-        (int)n_fwd, (int)n_items, 0, 1, fold ? 1 : 0, ctl);
+        mk, mv, mq, mg, log_decay, states, adj, init, dfin, sp, fold ? state_max : nullptr, T, H,
+        plan.whole, plan.parts, (int)n_fwd, (int)n_items, 0, 1, fold ? 1 : 0, ctl);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (fold) return cudaSuccess;
@@ -620,7 +637,8 @@ cudaError_t launch_slice_sums(const void* a, const void* b, bool bf16, bool reve
   if (e != cudaSuccess) return e;
   kern<<<(unsigned)items, THREADS, SMEM_BYTES, stream>>>(
       ma, mb, ma, mb, log_decay, reverse ? nullptr : out, reverse ? out : nullptr, nullptr,
-      nullptr, StatePages{}, T, H, 0, 2, reverse ? 0 : (int)items, (int)items, 1, ncol, 0, ctl);
+      nullptr, StatePages{}, nullptr, T, H, 0, 2, reverse ? 0 : (int)items, (int)items, 1, ncol, 0,
+      ctl);
   return cudaGetLastError();
 }
 
