@@ -88,7 +88,7 @@ gla::SplitPlan split_plan(int B, int T, int H, int roles, int n_sm, int pass_dir
 size_t split_bytes(int B, int H, const gla::SplitPlan& plan, bool bwd) {
   const long long slots = gla::split_slots((long long)B * H, plan);
   if (!slots) return 0;
-  // (the forward: the states, then with two parts each state's row-group maxima)
+  // (the forward: the states, then each state's partial maxima)
   if (!bwd) return round256((size_t)slots * kStateBytes) + round256((size_t)slots * 4 * 4);
   return 2 * round256((size_t)slots * kStateBytes) + round256((size_t)slots * gla::kDK * 4);
 }
@@ -147,10 +147,14 @@ gla_status chunk_fwd_impl(const void* q, const void* k, const void* v, gla_dtype
     // the segment passes; with plan.overlap the chunked kernel, launched as their programmatic
     // dependent, runs its whole pairs beside them
     float* states = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + round256(must));
-    float* maxes = plan.parts == 2
-                       ? reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(states) +
-                                                  round256((size_t)gla::split_slots((long long)B * H, plan) *
-                                                           kStateBytes))
+    // the starting states' maxima: from the two-part sum pass, or from pass B when the passes
+    // run before the chunked kernel (beside the whole pairs pass B's extra work would delay the
+    // SMs it holds, which measured slower than the parts' saving)
+    float* maxes = plan.parts == 2 || !plan.overlap
+                       ? reinterpret_cast<float*>(
+                             reinterpret_cast<uint8_t*>(states) +
+                             round256((size_t)gla::split_slots((long long)B * H, plan) *
+                                      kStateBytes))
                        : nullptr;
     a.seg_init = states;
     a.seg_max = maxes;

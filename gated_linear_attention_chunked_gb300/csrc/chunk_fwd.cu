@@ -577,7 +577,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
     int e_cur = 0;
     bool ok = true;
     if (cut && seg_max) {
-      // the sum pass left this part's max |state| (its three 32-row groups): the same exponent
+      // the segment passes left this part's max |state| (as partial maxima): the same exponent
       // without a pass over the state or the exchange
       const float* pm = seg_max + (size_t)cut_idx * 4;
       e_cur = state_exponent(fmaxf(fmaxf(__ldg(pm), __ldg(pm + 1)), __ldg(pm + 2)));
@@ -792,8 +792,8 @@ cudaError_t launch_chunk_fwd(const FwdArgs& a, DevCtl ctl, cudaStream_t stream) 
   // start beside the passes, its parts wait for them (griddep_wait)
   PdlLaunch L(dim3((unsigned)grid), dim3(threads), SMEM_BYTES, stream, plan.overlap);
   return cudaLaunchKernelEx(&L.cfg, kern, mq, mk, mv, mo, mfin, a.log_decay, a.aug, a.init, a.o,
-                            a.fin, a.T, a.H, plan, a.seg_init, plan.parts == 2 ? a.seg_max : nullptr,
-                            a.sp, my, a.og, a.gate, a.saved, ctl);
+                            a.fin, a.T, a.H, plan, a.seg_init, a.seg_max, a.sp, my, a.og, a.gate,
+                            a.saved, ctl);
 }
 
 }  // namespace gla

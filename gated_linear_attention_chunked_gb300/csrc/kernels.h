@@ -128,8 +128,8 @@ struct FwdArgs {
   // cut pairs: [(BH - whole) * parts][96][192], slot x*parts + j = the state entering part j
   // of cut pair x (filled by the segment passes; slot x*parts is the pair's initial state)
   const float* seg_init = nullptr;
-  // with two parts: per part slot, the three row groups' max |state| of its starting state,
-  // [slot][4] (written by the sum pass; null: the kernel finds the max itself)
+  // per part slot, max |state| of its starting state as up to four partial maxima [slot][4]
+  // (written by the segment passes; null: the kernel finds the max itself)
   const float* seg_max = nullptr;
   StatePages sp;  // with sp.page: init and fin are the pool (see StatePages)
   OutGate og;     // with og.g: the fused output epilogue (o written only if og.want_o)
@@ -191,8 +191,9 @@ long long split_slots(long long BH, const SplitPlan& p);
 // plan.overlap pass B is pass A's programmatic dependent and runs on at most 16 CTAs (which
 // wait beside pass A's), so that the chunked kernel launched next as its dependent can start
 // its whole pairs at once; pass A runs on plan.pass_ctas CTAs.
-// state_max (forward direction, two parts only, may be null): [slot][4] receives the max
-// |state| of each starting state's three 32-row groups.
+// state_max (forward direction, may be null): [slot][4] receives partial maxima of each
+// starting state: with two parts its three 32-row groups' max |state| (entries 0..2), with
+// more the whole state's max |state| (entry 0, the others 0).
 cudaError_t launch_segment_states(const void* q, const void* k, const void* v, const void* dO,
                                   bool bf16, const float* log_decay, const float* init,
                                   const float* dfin, const StatePages& sp, float* states,

@@ -326,6 +326,11 @@ seg_sum_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant_
             *reinterpret_cast<float4*>(dst + 32 * cb + jj) = u;
           }
         }
+        if (!fold && !I.rev && state_max && warp == 0 && lane < 4) {
+          // pass B fills this item's slot's max (and slot 0's, with part 0) by atomicMax
+          state_max[((size_t)I.x * parts + I.j + 1) * 4 + lane] = 0.f;
+          if (I.j == 0) state_max[((size_t)I.x * parts) * 4 + lane] = 0.f;
+        }
         if (fold && !I.rev && state_max) {  // the row group's maxima of both starting states
 #pragma unroll
           for (int off = 16; off > 0; off >>= 1) {
@@ -360,13 +365,15 @@ constexpr int LINK_THREADS = 1024;
 constexpr int LINK_CTAS_OVERLAP = 16;
 
 // One item of pass B: elements 4e .. 4e+3 of cut pair x's starting states (rev = 0) or
-// adjoints (rev = 1), walking the pair's parts in order.
+// adjoints (rev = 1), walking the pair's parts in order.  MAX: also note each forward
+// state's max |state| in state_max (a separate instantiation, so the plain link is unchanged).
+template <bool MAX>
 __device__ __forceinline__ void link_one(const float* __restrict__ init,
                                          const float* __restrict__ dfin,
                                          const float* __restrict__ log_decay,
                                          float* __restrict__ states, float* __restrict__ adj,
                                          int T, int H, int whole, int parts, const StatePages& sp,
-                                         int rev, int x, int e) {
+                                         unsigned* state_max, int rev, int x, int e) {
   constexpr int N4 = DK * DV / 4;
   float* const slots = rev ? adj : states;
   if (!slots) return;
@@ -378,6 +385,16 @@ __device__ __forceinline__ void link_one(const float* __restrict__ init,
   };
   float4* out = reinterpret_cast<float4*>(slots) + (size_t)x * parts * N4 + e;
   float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+  // forward direction, given state_max: slot j's max |state| -- the warp's 128 elements (one
+  // pair: items come in whole warps) reduced, then one atomicMax of the bits (non-negative
+  // floats order as their bit patterns, so the result does not depend on the order)
+  auto note_max = [&](int j) {
+    if (!MAX || rev) return;
+    float m = fmaxf(fmaxf(fabsf(s.x), fabsf(s.y)), fmaxf(fabsf(s.z), fabsf(s.w)));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    if ((threadIdx.x & 31) == 0) atomicMax(state_max + ((size_t)x * parts + j) * 4, __float_as_uint(m));
+  };
   // the steps in order, their sums loaded LB at a time ahead of the chain (each slot is read
   // before the step that overwrites it)
   constexpr int LB = 4;
@@ -395,6 +412,7 @@ __device__ __forceinline__ void link_one(const float* __restrict__ init,
           s = make_float4(fmaf(lam, s.x, u[q].x), fmaf(lam, s.y, u[q].y), fmaf(lam, s.z, u[q].z),
                           fmaf(lam, s.w, u[q].w));
           out[(size_t)j * N4] = s;
+          note_max(j);
         }
       }
     }
@@ -407,6 +425,7 @@ __device__ __forceinline__ void link_one(const float* __restrict__ init,
     }
     if (init && zi >= 0) s = __ldg(reinterpret_cast<const float4*>(init) + (size_t)zi * N4 + e);
     out[0] = s;
+    note_max(0);
     walk(1, parts - 1, 1, -1);  // j = 1 .. p-1: S_j = lambda^(L_{j-1}) S_{j-1} + U_{j-1}
   } else {
     if (dfin) s = __ldg(reinterpret_cast<const float4*>(dfin) + (size_t)bh * N4 + e);
@@ -416,11 +435,12 @@ __device__ __forceinline__ void link_one(const float* __restrict__ init,
 }
 
 // Pass B: every (direction, cut pair, 4 state elements) item, grid-stride.
+template <bool MAX>
 __global__ void __launch_bounds__(LINK_THREADS)
 seg_link_kernel(const float* __restrict__ init, const float* __restrict__ dfin,
                 const float* __restrict__ log_decay, float* __restrict__ states,
                 float* __restrict__ adj, int T, int H, int whole, int parts, StatePages sp,
-                int X) {
+                unsigned* __restrict__ state_max, int X) {
   // a chunked kernel launched as this grid's dependent may start its whole pairs; the sums are
   // read once pass A is complete
   griddep_launch_dependents();
@@ -429,8 +449,8 @@ seg_link_kernel(const float* __restrict__ init, const float* __restrict__ dfin,
   const long long per_dir = (long long)X * N4;
   for (long long it = (long long)blockIdx.x * LINK_THREADS + threadIdx.x; it < 2 * per_dir;
        it += (long long)gridDim.x * LINK_THREADS)
-    link_one(init, dfin, log_decay, states, adj, T, H, whole, parts, sp, (int)(it / per_dir),
-             (int)(it % per_dir / N4), (int)(it % N4));
+    link_one<MAX>(init, dfin, log_decay, states, adj, T, H, whole, parts, sp, state_max,
+                  (int)(it / per_dir), (int)(it % per_dir / N4), (int)(it % N4));
 }
 
 // The state entering slice `rank` of a sequence cut into consecutive slices across ranks
@@ -606,8 +626,8 @@ cudaError_t launch_segment_states(const void* q, const void* k, const void* v, c
     const long long grid =
         plan.pass_ctas > 0 && plan.pass_ctas < n_items ? plan.pass_ctas : n_items;
     kern<<<(unsigned)grid, THREADS, SMEM_BYTES, stream>>>(
-        mk, mv, mq, mg, log_decay, states, adj, init, dfin, sp, fold ? state_max : nullptr, T, H,
-        plan.whole, plan.parts, (int)n_fwd, (int)n_items, 0, 1, fold ? 1 : 0, ctl);
+        mk, mv, mq, mg, log_decay, states, adj, init, dfin, sp, state_max, T, H, plan.whole,
+        plan.parts, (int)n_fwd, (int)n_items, 0, 1, fold ? 1 : 0, ctl);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (fold) return cudaSuccess;
@@ -615,8 +635,9 @@ cudaError_t launch_segment_states(const void* q, const void* k, const void* v, c
   long long ctas = (items + LINK_THREADS - 1) / LINK_THREADS;
   if (plan.overlap && ctas > LINK_CTAS_OVERLAP) ctas = LINK_CTAS_OVERLAP;
   PdlLaunch L(dim3((unsigned)ctas), dim3(LINK_THREADS), 0, stream, plan.overlap);
-  return cudaLaunchKernelEx(&L.cfg, seg_link_kernel, init, dfin, log_decay, states, adj, T, H,
-                            plan.whole, plan.parts, sp, (int)X);
+  auto kern = state_max ? seg_link_kernel<true> : seg_link_kernel<false>;
+  return cudaLaunchKernelEx(&L.cfg, kern, init, dfin, log_decay, states, adj, T, H, plan.whole,
+                            plan.parts, sp, reinterpret_cast<unsigned*>(state_max), (int)X);
 }
 
 cudaError_t launch_slice_sums(const void* a, const void* b, bool bf16, bool reverse,
