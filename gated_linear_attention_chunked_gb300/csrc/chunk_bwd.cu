@@ -827,9 +827,11 @@ bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
   cta.sb = smem_u32(cta.base);
   cta.bar_off = OFF_BAR;
   cta.abort_off = OFF_ABORT;
-  // three roles per pair; the whole pairs first, then the parts of the cut ones
+  // three roles per pair, adjacent so that they read each chunk's tiles at about the same time
+  // (through L2), the longest first -- DV, DK, then DQ -- so that the launch's last CTAs tend to
+  // be the short ones; the whole pairs first, then the parts of the cut ones
   const int nc = (p.T + C - 1) / C;
-  const int role = blockIdx.x % 3, w = blockIdx.x / 3;
+  const int role = ((int)blockIdx.x + 1) % 3, w = blockIdx.x / 3;
   const bool cut = w >= p.plan.whole;
   const int cut_idx = cut ? w - p.plan.whole : -1;
   const int part = cut ? cut_idx % p.plan.parts : 0;
