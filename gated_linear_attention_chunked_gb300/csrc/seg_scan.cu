@@ -633,7 +633,14 @@ cudaError_t launch_segment_states(const void* q, const void* k, const void* v, c
   if (fold) return cudaSuccess;
   const long long items = 2LL * X * (DK * DV / 4);
   long long ctas = (items + LINK_THREADS - 1) / LINK_THREADS;
-  if (plan.overlap && ctas > LINK_CTAS_OVERLAP) ctas = LINK_CTAS_OVERLAP;
+  if (plan.overlap) {
+    // beside the whole pairs: about four items of the directions computed per thread, on at
+    // most LINK_CTAS_OVERLAP CTAs (they hold their SMs while they wait for pass A)
+    const long long work = (long long)((states ? 1 : 0) + (adj ? 1 : 0)) * X * (DK * DV / 4);
+    ctas = (work + 4LL * LINK_THREADS - 1) / (4LL * LINK_THREADS);
+    if (ctas > LINK_CTAS_OVERLAP) ctas = LINK_CTAS_OVERLAP;
+    if (ctas < 1) ctas = 1;
+  }
   PdlLaunch L(dim3((unsigned)ctas), dim3(LINK_THREADS), 0, stream, plan.overlap);
   auto kern = state_max ? seg_link_kernel<true> : seg_link_kernel<false>;
   return cudaLaunchKernelEx(&L.cfg, kern, init, dfin, log_decay, states, adj, T, H, plan.whole,
