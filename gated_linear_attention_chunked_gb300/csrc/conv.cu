@@ -10,8 +10,9 @@
 // Gradient for the scalar loss sum(y . dy), with dz = dy SiLU'(z):
 //   dx_s = sum_j w[j] dz_{s+3-j}   (s = -3..-1: the initial state),
 //   dw[d][j] = sum_{b,t} dz_t x_{t-3+j},  db[d] = sum_{b,t} dz_t.
-// Memory-bound streaming: one thread owns 4 consecutive channels of a 64-token tile and walks
-// its tokens with the 4-token window in registers (3-token halo, ~5 % re-read).  dw, db: per
+// Memory-bound streaming: one thread owns 4 consecutive channels of a 64-token tile (2 in the
+// staged backward) and walks its tokens with the 4-token window in registers (3-token halo,
+// ~5 % re-read).  dw, db: per
 // tile partial sums, summed over tiles in a fixed order by a second kernel (deterministic).
 // Each thread issues the loads of 8 tokens before using the first, so that several DRAM
 // round trips overlap.
@@ -352,28 +353,71 @@ conv_bwd_kernel(const void* __restrict__ x, const float* __restrict__ w,
   }
 }
 
-// The backward with x and dy staged through shared memory the same way (their rows of the
-// CTA's channel block, NSTB stages of SGB tokens): same arithmetic as conv_bwd_kernel.
+// The backward's ring: NSTB stages of SGB tokens of x and dy rows.
 constexpr int SGB = 4;   // tokens per stage (backward)
 constexpr int NSTB = 4;  // stages (backward)
+
+// The backward with x and dy staged through shared memory (their rows of the CTA's 512
+// channels, NSTB stages of SGB tokens, refilled by a producer warp), two channels per thread:
+// a thread's windows, dz and weight-gradient sums are fp32 pairs, small enough that three CTAs
+// fit an SM (with four channels per thread, 1,024 per CTA, two did).  The same arithmetic as
+// conv_bwd_kernel.
+constexpr int DC2 = 2 * THREADS;  // channels per CTA
 template <bool BF16>
-constexpr uint32_t staged_bwd_smem() { return NSTB * SGB * DC * ((BF16 ? 2 : 4) + 4) + 2 * NSTB * 8; }
+constexpr uint32_t staged_bwd2_smem() {
+  return NSTB * SGB * DC2 * ((BF16 ? 2 : 4) + 4) + 2 * NSTB * 8;
+}
+struct Filt2 {
+  float2 w[K];  // tap j of the 2 channels
+  float2 b;
+};
+__device__ __forceinline__ Filt2 load_filter2(const float* w, const float* bias, int d2) {
+  const float4 w0 = __ldg(reinterpret_cast<const float4*>(w) + 2 * d2);  // channel 2 d2
+  const float4 w1 = __ldg(reinterpret_cast<const float4*>(w) + 2 * d2 + 1);
+  Filt2 f;
+  f.w[0] = make_float2(w0.x, w1.x);
+  f.w[1] = make_float2(w0.y, w1.y);
+  f.w[2] = make_float2(w0.z, w1.z);
+  f.w[3] = make_float2(w0.w, w1.w);
+  f.b = bias ? __ldg(reinterpret_cast<const float2*>(bias) + d2) : make_float2(0.f, 0.f);
+  return f;
+}
+__device__ __forceinline__ float2 bf2_to_f2(uint32_t u) {
+  return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
+}
+// x_t for token t of sequence b, channels 2 d2 and 2 d2 + 1 (t < 0: the initial state)
+template <bool BF16>
+__device__ __forceinline__ float2 x_at2(const void* x, const float* init, int b, int t, int T,
+                                        int D2, int d2) {
+  const long long i = ((long long)b * T + t) * D2 + d2;
+  if (t >= 0) {
+    if constexpr (BF16) return bf2_to_f2(__ldg(reinterpret_cast<const uint32_t*>(x) + i));
+    else return __ldg(reinterpret_cast<const float2*>(x) + i);
+  }
+  if (!init) return make_float2(0.f, 0.f);
+  return __ldg(reinterpret_cast<const float2*>(init) + ((long long)b * 3 + (t + 3)) * D2 + d2);
+}
+__device__ __forceinline__ float2 silu_grad2(float2 z, float2 dy) {
+  const float2 s = make_float2(sigm(z.x), sigm(z.y));
+  const float2 one_minus_s = __ffma2_rn(s, make_float2(-1.f, -1.f), make_float2(1.f, 1.f));
+  return __fmul2_rn(__fmul2_rn(dy, s), __ffma2_rn(z, one_minus_s, make_float2(1.f, 1.f)));
+}
 
 template <bool BF16>
-__global__ void __launch_bounds__(THREADS + 32, 2)
-conv_bwd_staged_kernel(const void* __restrict__ x, const float* __restrict__ w,
-                       const float* __restrict__ bias, const float* __restrict__ init,
-                       const float* __restrict__ dy, float* __restrict__ dx,
-                       float* __restrict__ dinit, float* __restrict__ part, int T, int D,
-                       DevCtl ctl) {
+__global__ void __launch_bounds__(THREADS + 32, 3)
+conv_bwd_staged2_kernel(const void* __restrict__ x, const float* __restrict__ w,
+                        const float* __restrict__ bias, const float* __restrict__ init,
+                        const float* __restrict__ dy, float* __restrict__ dx,
+                        float* __restrict__ dinit, float* __restrict__ part, int T, int D,
+                        DevCtl ctl) {
   griddep_launch_dependents();  // the reduction launched next waits for this whole grid
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr int ES = BF16 ? 2 : 4;
-  constexpr uint32_t XROW = DC * ES, GROW = DC * 4, STAGE = SGB * (XROW + GROW);
+  constexpr uint32_t XROW = DC2 * ES, GROW = DC2 * 4, STAGE = SGB * (XROW + GROW);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NSTB * STAGE);  // full[NSTB], empty[NSTB]
-  const int D4 = D / 4, c0 = blockIdx.y * DC, nch = min(DC, D - c0);
-  const int d4 = c0 / 4 + threadIdx.x;
-  const bool active = 4 * (int)threadIdx.x < nch;
+  const int D2 = D / 2, c0 = blockIdx.y * DC2, nch = min(DC2, D - c0);
+  const int d2 = c0 / 2 + threadIdx.x;
+  const bool active = 2 * (int)threadIdx.x < nch;
   const int n_tiles = (T + TT - 1) / TT;
   const int b = blockIdx.x / n_tiles, t0 = (blockIdx.x % n_tiles) * TT;
   const int t1 = min(t0 + TT, T);
@@ -418,22 +462,22 @@ conv_bwd_staged_kernel(const void* __restrict__ x, const float* __restrict__ w,
     }
     return;
   }
-  const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
-  Filt f;
-  float4 win[K], dz[K];  // dz[0..3] = dz_{t-3..t} after step t
-  float4 gw[K], gb = zero;
+  const float2 zero = make_float2(0.f, 0.f);
+  Filt2 f;
+  float2 win[K], dz[K];  // dz[0..3] = dz_{t-3..t} after step t
+  float2 gw[K], gb = zero;
 #pragma unroll
   for (int j = 0; j < K; ++j) {
     dz[j] = zero;
     gw[j] = zero;
   }
   if (active) {
-    f = load_filter(w, bias, d4);
+    f = load_filter2(w, bias, d2);
 #pragma unroll
-    for (int j = 0; j < K - 1; ++j) win[j + 1] = x_at<BF16>(x, init, b, t0 - 3 + j, T, D4, d4);
+    for (int j = 0; j < K - 1; ++j) win[j + 1] = x_at2<BF16>(x, init, b, t0 - 3 + j, T, D2, d2);
   }
   // one token: shift the windows, dz_t (zero past T), the tile's weight and bias sums, dx_{t-3}
-  auto step = [&](int t, float4 xv, float4 g, bool in_seq) {
+  auto step = [&](int t, float2 xv, float2 g, bool in_seq) {
 #pragma unroll
     for (int j = 0; j < K - 1; ++j) {
       win[j] = win[j + 1];
@@ -441,12 +485,15 @@ conv_bwd_staged_kernel(const void* __restrict__ x, const float* __restrict__ w,
     }
     if (in_seq) {
       win[3] = xv;
-      const float4 d = silu_grad4(conv4(f, win), g);
+      float2 z = f.b;
+#pragma unroll
+      for (int j = 0; j < K; ++j) z = __ffma2_rn(f.w[j], win[j], z);
+      const float2 d = silu_grad2(z, g);
       dz[3] = d;
       if (t < t1) {
-        gb = add4(gb, d);
+        gb = __fadd2_rn(gb, d);
 #pragma unroll
-        for (int j = 0; j < K; ++j) gw[j] = fma4(d, win[j], gw[j]);
+        for (int j = 0; j < K; ++j) gw[j] = __ffma2_rn(d, win[j], gw[j]);
       }
     } else {
       win[3] = zero;
@@ -454,13 +501,13 @@ conv_bwd_staged_kernel(const void* __restrict__ x, const float* __restrict__ w,
     }
     const int s = t - 3;
     if ((s >= t0 || (t0 == 0 && s >= -3)) && s < t1) {
-      float4 o = zero;
+      float2 o = zero;
 #pragma unroll
-      for (int j = 0; j < K; ++j) o = fma4(f.w[j], dz[3 - j], o);
+      for (int j = 0; j < K; ++j) o = __ffma2_rn(f.w[j], dz[3 - j], o);
       if (s >= 0)
-        reinterpret_cast<float4*>(dx)[((long long)b * T + s) * D4 + d4] = o;
+        reinterpret_cast<float2*>(dx)[((long long)b * T + s) * D2 + d2] = o;
       else if (dinit)
-        reinterpret_cast<float4*>(dinit)[((long long)b * 3 + (s + 3)) * D4 + d4] = o;
+        reinterpret_cast<float2*>(dinit)[((long long)b * 3 + (s + 3)) * D2 + d2] = o;
     }
   };
   int consumed = 0;
@@ -469,13 +516,13 @@ conv_bwd_staged_kernel(const void* __restrict__ x, const float* __restrict__ w,
     if (!mbar_wait(full(st), (g / NSTB) & 1, ctl)) break;
     consumed = g + 1;
     if (active) {
-      const uint8_t* xs = smem + st * STAGE + threadIdx.x * 4 * ES;
-      const uint8_t* gs = smem + st * STAGE + SGB * XROW + threadIdx.x * 16;
+      const uint8_t* xs = smem + st * STAGE + threadIdx.x * 2 * ES;
+      const uint8_t* gs = smem + st * STAGE + SGB * XROW + threadIdx.x * 8;
       auto tok = [&](int t) {
-        float4 xv;
-        if constexpr (BF16) xv = to_f4(*reinterpret_cast<const uint2*>(xs + (t - ta) * XROW));
-        else xv = *reinterpret_cast<const float4*>(xs + (t - ta) * XROW);
-        step(t, xv, *reinterpret_cast<const float4*>(gs + (t - ta) * GROW), true);
+        float2 xv;
+        if constexpr (BF16) xv = bf2_to_f2(*reinterpret_cast<const uint32_t*>(xs + (t - ta) * XROW));
+        else xv = *reinterpret_cast<const float2*>(xs + (t - ta) * XROW);
+        step(t, xv, *reinterpret_cast<const float2*>(gs + (t - ta) * GROW), true);
       };
       if (tb - ta == SGB) {  // a full stage: unrolled, so the window shifts become renames
 #pragma unroll
@@ -489,13 +536,14 @@ conv_bwd_staged_kernel(const void* __restrict__ x, const float* __restrict__ w,
   if (consumed < ng) return;
   if (active) {
     for (int t = tload; t < tend; ++t) step(t, zero, zero, false);  // past T: dz = 0
-    float* p = part + ((long long)blockIdx.x * D + 4 * d4) * 5;
+    float* p = part + ((long long)blockIdx.x * D + 2 * d2) * 5;
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-#pragma unroll
-      for (int j = 0; j < K; ++j) p[c * 5 + j] = at(gw[j], c);
-      p[c * 5 + 4] = at(gb, c);
+    for (int j = 0; j < K; ++j) {
+      p[j] = gw[j].x;
+      p[5 + j] = gw[j].y;
     }
+    p[4] = gb.x;
+    p[9] = gb.y;
   }
 }
 
@@ -599,19 +647,19 @@ cudaError_t launch_conv_bwd(const void* x, bool bf16, const float* w, const floa
                             DevCtl ctl, cudaStream_t stream) {
   const int n_tiles = (T + TT - 1) / TT;
   if (D % (bf16 ? 8 : 4) == 0) {  // rows of 16-byte multiples: the staged kernel
-    const dim3 grid(B * n_tiles, (D + DC - 1) / DC);
+    const dim3 grid(B * n_tiles, (D + DC2 - 1) / DC2);
     cudaError_t e;
     if (bf16) {
-      e = cudaFuncSetAttribute(conv_bwd_staged_kernel<true>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, staged_bwd_smem<true>());
+      e = cudaFuncSetAttribute(conv_bwd_staged2_kernel<true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, staged_bwd2_smem<true>());
       if (e != cudaSuccess) return e;
-      conv_bwd_staged_kernel<true><<<grid, THREADS + 32, staged_bwd_smem<true>(), stream>>>(
+      conv_bwd_staged2_kernel<true><<<grid, THREADS + 32, staged_bwd2_smem<true>(), stream>>>(
           x, w, bias, init, dy, dx, dinit, part, T, D, ctl);
     } else {
-      e = cudaFuncSetAttribute(conv_bwd_staged_kernel<false>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, staged_bwd_smem<false>());
+      e = cudaFuncSetAttribute(conv_bwd_staged2_kernel<false>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, staged_bwd2_smem<false>());
       if (e != cudaSuccess) return e;
-      conv_bwd_staged_kernel<false><<<grid, THREADS + 32, staged_bwd_smem<false>(), stream>>>(
+      conv_bwd_staged2_kernel<false><<<grid, THREADS + 32, staged_bwd2_smem<false>(), stream>>>(
           x, w, bias, init, dy, dx, dinit, part, T, D, ctl);
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
