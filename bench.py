@@ -551,6 +551,36 @@ def run_gpu(args, rank, world, local_rank):
             path="pinned host q,k,v,dO -> gla chunk_fwd + chunk_bwd -> pinned host o, dq, dk, "
                  "dv, d_aug every step (device->host on a third stream, overlapping the next "
                  "step; bound by the host link)")
+
+        # the host link alone: the same copies with nothing else running (best of 3), so that
+        # each e2e figure can be read against the rate the link gives here
+        def link_ms(pairs):
+            best = float("inf")
+            for _ in range(3):
+                torch.cuda.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                with torch.cuda.stream(copy_stream):
+                    e0.record(copy_stream)
+                    for dst, src in pairs:
+                        dst.copy_(src, non_blocking=True)
+                    e1.record(copy_stream)
+                e1.synchronize()
+                best = min(best, e0.elapsed_time(e1))
+            return best
+
+        h2d_ms = link_ms(list(zip(bufs[0], (hq, hk, hv, hdO))))
+        d2h_ms = link_ms([(h_out[n_], outs[0][n_]) for n_ in ("o", "dq", "dk", "dv")])
+        h2d_gbs, d2h_gbs = h2d / h2d_ms / 1e6, (d2h_full - d2h) / d2h_ms / 1e6
+        e2e_ms, full_ms = 1e3 * tt / e2e_steps, 1e3 * tf_ / e2e_steps
+        e2e["link"] = dict(h2d_gbs=h2d_gbs, bound_ms=h2d_ms, ms_per_step=e2e_ms,
+                           frac=h2d_ms / e2e_ms,
+                           note="host->device copy of the step's inputs alone (best of 3); "
+                                "frac = that time / the e2e time per step")
+        bound_full = max(h2d_ms, d2h_ms)
+        e2e_full_readback["link"] = dict(h2d_gbs=h2d_gbs, d2h_gbs=d2h_gbs, bound_ms=bound_full,
+                                         ms_per_step=full_ms, frac=bound_full / full_ms,
+                                         note="the slower direction's copies alone (best of 3); "
+                                              "frac = that time / the e2e time per step")
         del bufs, outs
 
     cpu = cpu_dec = cpu_long = None
