@@ -754,7 +754,6 @@ __device__ __forceinline__ void run_role(
               } else {
                 float f8[8];
                 unpack8<false>(vv[k], f8);
-#pragma unroll
                 const float4 a0 = *reinterpret_cast<const float4*>(sa + col);
                 const float4 a1 = *reinterpret_cast<const float4*>(sa + col + 4);
                 const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
