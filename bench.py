@@ -438,6 +438,34 @@ def run_gpu(args, rank, world, local_rank):
     roof_bwd["tensor"] = dict(achieved=th * BWD_FLOPS_TH / (bwd_t * 1e-3) / 1e12, peak=pk["bf16"],
                               unit="TFLOP/s", frac=th * BWD_FLOPS_TH / (bwd_t * 1e-3) / 1e12 / pk["bf16"])
 
+    # each chunk call alone: the same call 20 times back to back after the step loop (CUDA
+    # events on the launching stream; inputs > L2), next to its time inside the step above
+    def alone_ms(fn, n=20):
+        for _ in range(3):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return reduce_max([e0.elapsed_time(e1) / n], dist, dev)[0]
+
+    for roof_, ms_, by_ in (
+            (roof_fwd, alone_ms(lambda: gla.chunk_fwd(q, k, v, gam, a, out=o, final_state=fin,
+                                                      gate=gate, saved_states=saved)), fb_th),
+            (roof_bwd, alone_ms(lambda: gla.chunk_bwd(q, k, v, gam, a, dO, gate=gate,
+                                                      saved_states=saved, workspace=ws)), bb_th)):
+        roof_["alone"] = dict(ms=ms_, achieved=th * by_ / (ms_ * 1e-3) / 1e9, unit="GB/s",
+                              frac=th * by_ / (ms_ * 1e-3) / 1e9 / pk["hbm"],
+                              note="the same call 20 times back to back after the step loop; "
+                                   "the fields above are its time inside the step")
+    if gla.get_device_error() != 0:
+        raise RuntimeError("device error in the chunk calls timed alone")
+
     # ---- end to end through the public API: pinned host inputs -> HBM -> fwd+bwd -> d_aug.
     # Every step copies its own inputs from pinned host memory and reads its d_aug back; as
     # in a training loop's prefetch, the copy of step s+1 runs on a second stream into the
