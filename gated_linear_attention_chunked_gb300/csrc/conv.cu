@@ -27,7 +27,9 @@ namespace gla {
 namespace {
 
 constexpr int K = 4;        // filter width
-constexpr int TT = 64;      // tokens per tile
+constexpr int TT = 64;      // tokens per tile (forward)
+constexpr int TTB = 128;    // tokens per tile (backward: half the weight-gradient partial sums
+                            // and halo re-reads of 64; 256 measured slower)
 constexpr int THREADS = 256;
 
 template <bool BF16>
@@ -284,9 +286,9 @@ conv_bwd_kernel(const void* __restrict__ x, const float* __restrict__ w,
   griddep_launch_dependents();  // the reduction launched next waits for this whole grid
   const int D4 = D / 4, d4 = blockIdx.y * THREADS + threadIdx.x;
   if (d4 >= D4) return;
-  const int n_tiles = (T + TT - 1) / TT;
-  const int b = blockIdx.x / n_tiles, t0 = (blockIdx.x % n_tiles) * TT;
-  const int t1 = min(t0 + TT, T);
+  const int n_tiles = (T + TTB - 1) / TTB;
+  const int b = blockIdx.x / n_tiles, t0 = (blockIdx.x % n_tiles) * TTB;
+  const int t1 = min(t0 + TTB, T);
   Filt f = load_filter(w, bias, d4);
   float4 win[K], dz[K];  // dz[0..3] = dz_{t-3..t} after step t
   const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -418,9 +420,9 @@ conv_bwd_staged2_kernel(const void* __restrict__ x, const float* __restrict__ w,
   const int D2 = D / 2, c0 = blockIdx.y * DC2, nch = min(DC2, D - c0);
   const int d2 = c0 / 2 + threadIdx.x;
   const bool active = 2 * (int)threadIdx.x < nch;
-  const int n_tiles = (T + TT - 1) / TT;
-  const int b = blockIdx.x / n_tiles, t0 = (blockIdx.x % n_tiles) * TT;
-  const int t1 = min(t0 + TT, T);
+  const int n_tiles = (T + TTB - 1) / TTB;
+  const int b = blockIdx.x / n_tiles, t0 = (blockIdx.x % n_tiles) * TTB;
+  const int t1 = min(t0 + TTB, T);
   // t runs to t1 + 2 so that dx_s for every s < t1 is complete (dz beyond T is 0); the rows of
   // tokens t0 .. tload-1 come through the ring
   const int tend = t1 + 3, tload = min(tend, T), ng = (tload - t0 + SGB - 1) / SGB;
@@ -609,7 +611,7 @@ conv_decode_kernel(float* __restrict__ state, const float* __restrict__ x,
 }  // namespace
 
 size_t conv_bwd_workspace_bytes(int B, int T, int D) {
-  return (size_t)B * ((T + TT - 1) / TT) * D * 5 * sizeof(float);
+  return (size_t)B * ((T + TTB - 1) / TTB) * D * 5 * sizeof(float);
 }
 
 cudaError_t launch_conv_fwd(const void* x, bool bf16, const float* w, const float* bias,
@@ -645,7 +647,7 @@ cudaError_t launch_conv_bwd(const void* x, bool bf16, const float* w, const floa
                             const float* init, const float* dy, float* dx, float* dinit,
                             float* dw, float* db, float* part, int B, int T, int D,
                             DevCtl ctl, cudaStream_t stream) {
-  const int n_tiles = (T + TT - 1) / TT;
+  const int n_tiles = (T + TTB - 1) / TTB;
   if (D % (bf16 ? 8 : 4) == 0) {  // rows of 16-byte multiples: the staged kernel
     const dim3 grid(B * n_tiles, (D + DC2 - 1) / DC2);
     cudaError_t e;
