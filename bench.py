@@ -34,8 +34,12 @@ if ROOT not in sys.path:
 METRIC = "GLA fwd+bwd tokens/s (H=16,T=2048) and decode-step GB/s vs HBM roofline"
 B, T, H, DK, DV = 32, 2048, 16, 96, 192
 N_SEQ, N_LAYERS = 1280, 24
-WORKLOAD = ("GLA chunked fwd+bwd B=32 T=2048 H=16 dk=96 dv=192 chunk=128 bf16-in/fp32-out, "
-            "plus one decode step over 1280 seqs x 24 layers x 16 heads of 96x192 fp32 states")
+def workload_name(b: int = B, n_seq: int = N_SEQ) -> str:
+    return (f"GLA chunked fwd+bwd B={b} T=2048 H=16 dk=96 dv=192 chunk=128 bf16-in/fp32-out, "
+            f"plus one decode step over {n_seq} seqs x 24 layers x 16 heads of 96x192 fp32 states")
+
+
+WORKLOAD = workload_name()
 # Algorithmic work per unit (what the calls must move / compute at minimum)
 # the training step saves the gate sigmoid(z) (fp32 per token-head) in the forward for the backward
 # and the state copies (36,864 B fp16 + a 4-byte exponent per chunk of 128 tokens, 288.03 B per
@@ -400,17 +404,17 @@ def run_gpu(args, rank, world, local_rank):
         if dist:
             dist.destroy_process_group()
         return 0
-    tokens = B * T
+    tokens = Bn * T  # the batch actually run (32 unless --batch says otherwise)
     value = job_rate(world, tokens, (fwd_t + bwd_t) * 1e-3)
     dec_bytes = n_states * DEC_BYTES_STATE
     dec_gbs = dec_bytes / (dec_t * 1e-3) / 1e9
-    th = B * T * H
+    th = Bn * T * H
     # our kernels per step: chunk fwd, chunk bwd, d_aug reduction, decode, and the two segment
     # passes of each chunked call whose plan cuts pairs into parts
     n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
     # segment passes of a cut call: the sum pass, and the link pass unless there are two parts
-    parts_f = gla.split_plan(B, T, H, False, n_sm)[1]
-    parts_b = gla.split_plan(B, T, H, 2 if args.saved_states else 1, n_sm)[1]
+    parts_f = gla.split_plan(Bn, T, H, False, n_sm)[1]
+    parts_b = gla.split_plan(Bn, T, H, 2 if args.saved_states else 1, n_sm)[1]
     pass_f = 0 if parts_f <= 1 else (1 if parts_f == 2 else 2)
     pass_b = 0 if parts_b <= 1 else (1 if parts_b == 2 else 2)
     gpu_launches_per_step = 4 + pass_f + pass_b
@@ -644,8 +648,8 @@ def run_gpu(args, rank, world, local_rank):
         warmup=args.warmup, ms_per_step=tot_t, higher_is_better=True, scaling="weak",
         vs_baseline=None, dtype="f16-mma/f32-acc (bf16 in, fp32 out); decode f32",
         data="synthetic (seeded Gaussians with the workloads' shapes and scales)",
-        config=dict(workload=WORKLOAD, B=B, T=T, H=H, dk=DK, dv=DV, chunk=128,
-                    decode_pool=[N_SEQ, N_LAYERS, H, DK, DV], parallelism=f"replicas x{world}",
+        config=dict(workload=workload_name(Bn, Ns), B=Bn, T=T, H=H, dk=DK, dv=DV, chunk=128,
+                    decode_pool=[Ns, N_LAYERS, H, DK, DV], parallelism=f"replicas x{world}",
                     l2="inputs larger than L2 (1.2 GB chunk inputs, 36 GB state pool); no flush"),
         roofline=roofline,
         decode=dict(value=dec_gbs, unit="GB/s", ms_per_step=dec_t, states=n_states,
@@ -1105,9 +1109,10 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
-    if args.part != "all" or args.batch != B or args.n_seq != N_SEQ:
+    if args.part != "all":
         args.no_e2e = True
-        args.no_cpu_baseline = True
+    if args.part != "all" or args.batch != B or args.n_seq != N_SEQ:
+        args.no_cpu_baseline = True  # the oracle's samples are of the default workload
     if args.gpus > 1 and world == 1:
         print("bench.py: for --gpus N > 1 launch with torch.distributed.run (one rank per GPU)",
               file=sys.stderr)
