@@ -32,7 +32,7 @@ def _inputs(seed, B, T, D, bf16, with_init, with_bias):
 
 
 @pytest.mark.parametrize("B,T,D,bf16,with_init,with_bias,seed", [
-    (2, 67, 96, True, True, True, 81),       # forward: a full 64-token tile and a ragged one
+    (2, 67, 96, True, True, True, 81),       # forward: two full 32-token tiles and a ragged one
     (2, 259, 96, True, True, True, 88),      # backward: two full 128-token tiles, 3 tokens left
     (1, 2, 8, False, True, True, 82),        # shorter than the state
     (3, 200, 3072, True, False, False, 83),  # the model width, no state, no bias
